@@ -1,0 +1,528 @@
+"""Benchmark of the ZeRO sharded optimizer step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
+
+One "step" is one pass of the whole hot path over one batch of synthetic
+grads already resident in HBM: for the default workload (GPT-2 XL shape,
+1,557,611,200 params, 16 data-parallel ranks on this GPU, fp16 grads and
+params, loss scale 2^16) that is the reduce-scatter sum, average, unscale and
+overflow check (reduce kernel), then Adam + cast + placement (apply kernel),
+then the read of the overflow verdict and the loss-scale update.
+
+Prints ONE JSON line (rank 0).  `value` is params updated per second over
+all GPUs (device-timed with CUDA events, inputs resident); `e2e` repeats the
+measurement with the grads copied from pinned host memory every step and
+the verdict read back; `roofline` reports the dominant kernel's algorithmic
+bytes per launch over its CUDA-event duration against the measured HBM copy
+bandwidth; `cpu_baseline` times the CPU oracle on a bounded sample.
+
+With --gpus N > 1 (torchrun), every GPU runs its own full replica of the
+workload (the N simulated ranks live on each GPU; no data-path collective):
+weak scaling.  `--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+# dram bytes per launch from ncu captures (see profiles/), valid only for the
+# kernel source they were taken on
+TRAFFIC = {}
+KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
+                          "zero_step_kernels.cu")
+GATHER_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc", "zero_gather.cu")
+
+
+def src_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="gpt2_xl",
+                    choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+METRIC = "ZeRO step params-updated/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
+                                          "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    s, m = float(parts[1]), float(parts[2])
+                except ValueError:
+                    continue
+                sm.append(s)
+                mx.append(m)
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------- the device timing
+
+class Launch:
+    """One kernel launch of the step, bracketed by CUDA events."""
+
+    def __init__(self, name, alg_bytes, fn):
+        self.name, self.alg_bytes, self.fn = name, alg_bytes, fn
+
+
+def step_plan(run):
+    """The kernel launches of one step, each with its algorithmic bytes."""
+    import zero_sharded_optimizer_step_gb300 as z
+    w, st = run.w, run.stream
+    bg = 4 if w.grad_dtype == 0 else 2
+    bp = 4 if w.param_dtype == 0 else 2
+    plan = []
+    if w.stage < 3:
+        n_state = w.shard * (w.world if w.rank < 0 else 1)
+        n_valid = w.numel if w.rank < 0 else min(w.shard, max(0, w.numel - w.rank * w.shard))
+        if run.scale > 0:
+            def red():
+                z.zero_step_reduce(run.ctx, run.grads[0], run.scale, st)
+
+            def app():
+                z.zero_step_apply(run.ctx, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st)
+            plan.append(Launch("reduce_kernel", w.world * bg * n_valid + 4 * n_state, red))
+            plan.append(Launch("apply_kernel", (4 + 24 + bp) * n_state, app))
+        else:
+            def fused():
+                z.zero_step(run.ctx, run.grads[0], w.lr, w.beta1, w.beta2, w.eps, run.t + 1,
+                            0.0, st)
+            plan.append(Launch("fused_step_kernel", w.world * bg * n_valid + (24 + bp) * n_state,
+                               fused))
+        if run.shards is not None:
+            n_sh = sum(1 for s in run.shards if s is not None)
+
+            def gat():
+                z.zero_allgather(run.ctx, run.shards, run.params, w.param_dtype, st)
+            plan.append(Launch("gather_kernel", 2 * bp * w.shard * n_sh, gat))
+    else:
+        nunits = len(w.units)
+
+        def first():
+            z.zero3_begin_step(run.ctx)
+        for u in range(nunits):
+            Su = w.unit_shard(u)
+            plan.append(Launch("gather_kernel", 2 * bp * Su * w.world,
+                               (lambda u=u: z.zero3_gather_unit(run.ctx, u, run.shards[u],
+                                                                run.unit_full, st))))
+        for u in reversed(range(nunits)):
+            Su = w.unit_shard(u)
+            nv = min(Su, max(0, w.units[u] - w.rank * Su))
+            plan.append(Launch("gather_kernel", 2 * bp * Su * w.world,
+                               (lambda u=u: z.zero3_gather_unit(run.ctx, u, run.shards[u],
+                                                                run.unit_full, st))))
+            plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * Su,
+                               (lambda u=u: z.zero3_step_unit(run.ctx, u, run.grads[u], w.lr,
+                                                              w.beta1, w.beta2, w.eps,
+                                                              run.t + 1, st))))
+        plan[0] = Launch(plan[0].name, plan[0].alg_bytes,
+                         (lambda f=plan[0].fn: (first(), f())))
+    return plan
+
+
+def run_step(run, plan, events=None):
+    if events is None:
+        for L in plan:
+            L.fn()
+    else:
+        for L, (a, b) in zip(plan, events):
+            a.record(run.stream)
+            L.fn()
+            b.record(run.stream)
+    if run.scale > 0:
+        run.finish_step()          # the verdict decides t and the scale
+    else:
+        run.t += 1
+
+
+def bench_ours(args, rank, world_size, device_index):
+    import torch
+
+    import workloads as W
+    from workloads.runner import Runner
+
+    w = W.ALL[args.workload]()
+    if w.inject:
+        w = w.replace(inject=None)    # timed steps are the ones that apply
+    torch.cuda.set_device(device_index)
+    run = Runner(w, device="cuda:%d" % device_index)
+    run.fill_grads(1)
+    plan = step_plan(run)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        run_step(run, plan)
+    torch.cuda.synchronize()
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in plan] for _ in range(args.steps)]
+    clocks = Clocks(device_index)
+    barrier(world_size)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(run.stream)
+    for k in range(args.steps):
+        run_step(run, plan, ev[k])
+    t_end.record(run.stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier(world_size)
+    ms = t_start.elapsed_time(t_end)
+    ms_max = allreduce_max(ms, world_size)
+    assert all(not s for s in run.skips), "a timed step was skipped"
+
+    # per-kernel durations
+    per = {}
+    for k in range(args.steps):
+        for L, (a, b) in zip(plan, ev[k]):
+            d = per.setdefault(L.name, [0.0, 0, L.alg_bytes])
+            d[0] += a.elapsed_time(b)
+            d[1] += 1
+    dom = max(per, key=lambda n: per[n][0])
+    tot_ms, n_launch, _ = per[dom]
+    alg_per_launch = sum(L.alg_bytes for L in plan if L.name == dom) / \
+        sum(1 for L in plan if L.name == dom)
+    avg_ms = tot_ms / n_launch
+    peak, peak_kind = peaks()
+    achieved = alg_per_launch / (avg_ms * 1e-3) / 1e9
+    kh = src_hash(GATHER_SRC if dom == "gather_kernel" else KERNEL_SRC)
+    tr = TRAFFIC.get((args.workload, dom))
+    traffic = tr[1] if tr and tr[0] == kh else None
+
+    updated = w.updated_per_step()
+    step_ms = ms_max / args.steps
+    value = updated * world_size / (step_ms * 1e-3)
+    step_bytes = sum(L.alg_bytes for L in plan)
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "params/s",
+        "n_gpus": world_size,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {0: "f32", 1: "bf16", 2: "f16"}[w.grad_dtype] + " grads, f32 state",
+        "data": "synthetic (seeded counter-based normal draws; no dataset)",
+        "config": {
+            "workload": describe(w),
+            "params_updated_per_step": updated,
+            "alg_bytes_per_step": step_bytes,
+            "step_hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
+            "step_frac_of_peak": step_bytes / (step_ms * 1e-3) / 1e9 / peak,
+            "method_min_bytes_per_param": method_min_bytes(w),
+            "l2": "inputs larger than L2 (working set %.1f GB)" % (working_set(run) / 1e9),
+            "per_kernel_ms": {n: per[n][0] / per[n][1] for n in per},
+            "parallelism": "%d simulated data-parallel ranks per GPU; %d GPU replica(s)"
+                           % (w.world, world_size),
+        },
+        "roofline": {
+            "kernel": dom,
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "alg_bytes_per_launch": alg_per_launch,
+            "traffic": traffic,
+        },
+        "gpu_launches": len(plan) * args.steps,
+        "clocks": clock_info,
+    }
+    if not args.no_e2e:
+        result["e2e"] = bench_e2e(run, plan, args, world_size)
+    if not args.no_cpu_baseline and rank == 0:
+        result["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
+    run.close()
+    return result
+
+
+def working_set(run):
+    tot = 0
+    for t in [run.master, run.m, run.v, run.params, run.g, run.unit_full]:
+        if t is not None:
+            tot += t.numel() * t.element_size()
+    for row in run.grads:
+        for t in row:
+            tot += t.numel() * t.element_size()
+    return tot
+
+
+def method_min_bytes(w):
+    bg = 4 if w.grad_dtype == 0 else 2
+    bp = 4 if w.param_dtype == 0 else 2
+    return w.world * bg + 24 + bp
+
+
+def describe(w):
+    return ("%s: numel=%d world=%d stage=%d grad=%s param=%s rank=%s%s%s"
+            % (w.name, w.numel, w.world, w.stage, "f32 bf16 f16".split()[w.grad_dtype],
+               "f32 bf16 f16".split()[w.param_dtype], "all" if w.rank < 0 else w.rank,
+               " loss_scale=%g" % w.loss_scale if w.loss_scale else "",
+               " units=%dx%d" % (len(w.units), w.units[0]) if w.units else ""))
+
+
+def bench_e2e(run, plan, args, world_size):
+    """Same step, with every rank's grads copied from pinned host memory each
+    step and the verdict word read back to the host."""
+    import torch
+    import zero_sharded_optimizer_step_gb300 as z
+
+    dev_bufs = [t for row in run.grads for t in row]
+    h2d = sum(t.numel() * t.element_size() for t in dev_bufs)
+    try:
+        avail = int(open("/proc/meminfo").read().split("MemAvailable:")[1].split()[0]) * 1024
+    except Exception:
+        avail = 32 << 30
+    cap = min(h2d, int(0.3 * avail), 48 << 30)
+    # pinned host copies of the grads (cycled through when RAM is short)
+    host = []
+    used = 0
+    for t in dev_bufs:
+        nb = t.numel() * t.element_size()
+        if used + nb > cap and host:
+            break
+        h = torch.empty(t.numel(), dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        host.append(h)
+        used += nb
+    st = run.stream
+    steps = max(2, args.e2e_steps)
+
+    def one():
+        with torch.cuda.stream(st):
+            for i, t in enumerate(dev_bufs):
+                t.copy_(host[i % len(host)], non_blocking=True)
+        for L in plan:
+            L.fn()
+        z.zero_step_status(run.ctx)       # 8-byte read of the verdict
+        if run.scale > 0:
+            run.scale, run.good = z.zero_scale_update(run.scale, False, run.good,
+                                                      run.w.growth_interval)
+        run.t += 1
+
+    one()
+    torch.cuda.synchronize()
+    barrier(world_size)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = allreduce_max(time.perf_counter() - t0, world_size)
+    return {"value": run.w.updated_per_step() * world_size * steps / dt, "unit": "params/s",
+            "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": 8, "host_buffers_distinct": len(host),
+            "device_buffers": len(dev_bufs)}
+
+
+# ---------------------------------------------------------------- the oracle
+
+def oracle_sample(w, n_s):
+    """Inputs of a bounded contiguous sample of the workload for the oracle."""
+    import synth
+    import workloads as W
+    grads = [synth.fill_host(n_s, w.grad_dtype, synth.key(w.seed, synth.KIND_GRAD, 1, k),
+                             W.grad_sigma(w, w.loss_scale)) for k in range(w.world)]
+    x = synth.fill_host(n_s, synth.F32, synth.key(w.seed, synth.KIND_MASTER), w.sigma_master)
+    return grads, x
+
+
+def oracle_time(w, n_s, steps):
+    """Seconds per oracle step on n_s elements (single thread)."""
+    import oracle
+    grads, x0 = oracle_sample(w, n_s)
+    times = []
+    if w.rank < 0 and w.stage < 3:
+        P = oracle.shard_size(n_s, w.world) * w.world
+        x = np.zeros(P, np.float32)
+        x[:n_s] = x0
+        m, v = np.zeros(P, np.float32), np.zeros(P, np.float32)
+        full = np.zeros(P, oracle.NP_STORAGE[w.param_dtype])
+        for t in range(1, steps + 1):
+            t0 = time.perf_counter()
+            oracle.zero_step(grads, w.grad_dtype, n_s, x, m, v, full, w.param_dtype, w.lr,
+                             w.beta1, w.beta2, w.eps, t, loss_scale=w.loss_scale)
+            times.append(time.perf_counter() - t0)
+        updated = n_s
+    else:
+        # one rank's view: the sample is a piece of its shard, rank 0 of world
+        x = x0.copy()
+        m, v = np.zeros(n_s, np.float32), np.zeros(n_s, np.float32)
+        lp = np.zeros(n_s, oracle.NP_STORAGE[w.param_dtype])
+        numel = n_s * w.world
+        for t in range(1, steps + 1):
+            t0 = time.perf_counter()
+            oracle.zero_rank_step(grads, w.grad_dtype, numel, 0, x, m, v, lp, w.param_dtype,
+                                  w.lr, w.beta1, w.beta2, w.eps, t, loss_scale=w.loss_scale)
+            times.append(time.perf_counter() - t0)
+        updated = n_s
+    return updated, times
+
+
+def cpu_baseline(w, budget_s=12.0, steps=None):
+    n_s = 1 << 20
+    upd, times = oracle_time(w, n_s, 1)
+    per = times[0]
+    # scale the sample so that the timed steps take about the budget
+    steps = steps or 4
+    n_s = int(min(1 << 26, max(1 << 16, n_s * budget_s / steps / max(per, 1e-6))))
+    upd, times = oracle_time(w, n_s, steps)
+    return {"value": upd / statistics.median(times), "unit": "params/s", "cores": 1,
+            "kind": "oracle",
+            "sample": "contiguous %d-element piece of the workload (%d ranks), %d steps, "
+                      "median step time; C oracle, one thread" % (n_s, w.world, steps)}
+
+
+def bench_reference(args, rank, world_size):
+    import workloads as W
+    if rank != 0:
+        return None
+    w = W.ALL[args.workload]()
+    n_s = 1 << 22
+    _, warm = oracle_time(w, n_s, max(1, min(args.warmup, 2)))
+    per = statistics.median(warm)
+    # keep the whole run within a few minutes
+    n_s = int(max(1 << 16, min(1 << 24, n_s * 3.0 / max(per, 1e-6))))
+    _, times = oracle_time(w, n_s, args.steps)
+    ms = sum(times) * 1e3
+    value = n_s * len(times) / (ms * 1e-3)
+    cb = {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+          "sample": "contiguous %d-element piece of %s per step, %d timed steps; C oracle, one "
+                    "thread" % (n_s, w.name, len(times))}
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
+            "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / len(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 arithmetic (CPU oracle)",
+            "data": "synthetic", "config": {"workload": describe(w)},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# -------------------------------------------------------------- distributed
+
+def barrier(world_size):
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x, world_size):
+    if world_size <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    world_size = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world_size > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        res = bench_reference(args, rank, world_size)
+    else:
+        import __graft_entry__
+        __graft_entry__.build() if rank == 0 else None
+        barrier(world_size)
+        res = bench_ours(args, rank, world_size, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,272 @@
+/*
+ * zero.h -- C ABI of the GB300 ZeRO sharded optimizer step (libzero.so).
+ *
+ * The method (ZeRO data parallelism, stages 1/2/3):
+ *   - "ZeRO 与 FSDP：切分优化器状态、梯度与参数", section 从零实现 ZeRO 的 Adam:
+ *     all parameters form one flat vector, cut into N shards of
+ *     S = ceil(numel / N) elements with a zero-padded tail; rank r owns
+ *     [r*S, r*S + S).  One step = reduce-scatter (sum) of the grads, divide by
+ *     N, Adam with bias correction on the owned shard, all-gather of the
+ *     updated shards back into the full parameter vector.
+ *   - "论文专题讲解：ZeRO：大模型训练的零冗余状态优化", sections 显存账 and
+ *     ZeRO-DP 三阶段: fp32 master weights, momentum and variance beside 16-bit
+ *     params and grads; stage 1 shards the optimizer states, stage 2 also the
+ *     grads, stage 3 also the params.
+ *   - "ZeRO 与 FSDP…", section ZeRO-3 与 FSDP, and guanweilu.cn article 1460,
+ *     section Stage 3: with params sharded, each unit (layer) is all-gathered
+ *     before its forward and again before its backward, then its grads are
+ *     reduce-scattered.
+ *   - "PaddlePaddle ZeRO优化", section 混合精度才是最佳拍档: with a loss
+ *     scale, a step whose grads hold inf/nan is skipped and the scale halved.
+ *
+ * On one GPU the N data-parallel ranks are N device buffers, so every
+ * "collective" here is a kernel reading those buffers; nothing talks to
+ * another GPU.  Two views are supported:
+ *   rank = -1  ("all ranks"): the state of every rank lives here.  master, m,
+ *              v hold the N shards end to end (P = N*S floats, rank r's at
+ *              r*S); grads[k] is rank k's whole local gradient (numel
+ *              elements; no padding needed).  One step performs the
+ *              reduce-scatter, Adam on every shard, the cast and the
+ *              all-gather in one pass over P elements.
+ *   rank = r   ("one rank's view"): master, m, v hold rank r's shard (S
+ *              floats); grads[k] is the S-element slice of rank k's flat
+ *              gradient that belongs to shard r (what reduce-scatter brings to
+ *              rank r).  The updated shard is cast into rank r's place of the
+ *              full parameter buffer; zero_allgather() places the others.
+ *
+ * Numerics (every backend path follows this exactly, element by element):
+ *   acc = g_0 + g_1 + ... + g_{N-1}      (fp32, rank order, starting at g_0)
+ *   g   = acc / N, then g = g / loss_scale when loss_scale > 0
+ *   nonfinite |= !isfinite(g)            (over every element of the step)
+ *   m   = b1*m + (1-b1)*g ;  v = b2*v + (1-b2)*(g*g)
+ *   x   = x - (lr * (m/(1-b1^t))) / (sqrt(v/(1-b2^t)) + eps)
+ *   param = round-to-nearest-even(x) in the param type
+ * each operation a single IEEE binary32 operation (no fused multiply-add, no
+ * flush to zero).  lr, b1, b2 and eps arrive as doubles; the fp32 scalars
+ * b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr and eps are computed in double on the
+ * host and rounded once.  Padding positions (flat index >= numel) take grad 0
+ * and therefore stay exactly +0.
+ *
+ * Conventions:
+ *   - Every call returns an int: >= 0 is success (ZERO_OK, or ZERO_SKIPPED
+ *     from zero_step_status), < 0 an error code; zero_strerror() names it and
+ *     zero_last_error() gives a message for the calling thread.  A call that
+ *     fails launches nothing.
+ *   - The caller owns every device buffer (allocated by PyTorch or
+ *     cudaMalloc).  The library never allocates device memory; the context
+ *     itself is a small host object.
+ *   - Launching calls are asynchronous on the caller's stream (a
+ *     cudaStream_t passed as void*; NULL = legacy default stream).  Only
+ *     zero_step_status() synchronizes.
+ *   - Device pointers must be aligned to their element size.  16-byte
+ *     alignment is not required: unaligned buffers take slower but correct
+ *     paths.
+ *   - A context is not thread-safe; use one per host thread.
+ *   - Element types: ZERO_F32, ZERO_BF16, ZERO_F16.  master/m/v are fp32.
+ */
+#ifndef ZERO_GB300_ZERO_H
+#define ZERO_GB300_ZERO_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct zero_ctx zero_ctx;
+
+enum zero_dtype { ZERO_F32 = 0, ZERO_BF16 = 1, ZERO_F16 = 2 };
+
+enum zero_code {
+    ZERO_OK = 0,
+    ZERO_SKIPPED = 1,      /* status: the step was skipped (loss-scale overflow) */
+    ZERO_EINVAL = -1,      /* bad argument (size, dtype, rank, unit, null pointer) */
+    ZERO_ECUDA = -2,       /* a CUDA runtime call failed */
+    ZERO_EALIGN = -3,      /* a device pointer is not aligned to its element size */
+    ZERO_ESTATE = -4       /* call not valid in this context's state (e.g. unbound) */
+};
+
+#define ZERO_MAX_RANKS 256
+
+/* ------------------------------------------------------------ host only */
+
+/* Shard length S = ceil(numel / world) ("ZeRO 与 FSDP…", 从零实现 ZeRO 的
+ * Adam).  Returns -1 when world < 1 or numel < 0. */
+int64_t zero_shard_size(int64_t numel, int32_t world);
+
+/* Per-device bytes of model states for `numel` parameters over `world`
+ * ranks, mixed-precision Adam (K = 12): stage 0 (plain data parallelism)
+ * 16*numel, stage 1 4*numel + 12*numel/world, stage 2 2*numel +
+ * 14*numel/world, stage 3 16*numel/world ("论文专题讲解：ZeRO", ZeRO-DP 三阶段;
+ * Table 1).  Returns -1.0 on bad arguments. */
+double zero_model_state_bytes(int64_t numel, int32_t world, int32_t stage);
+
+/* Loss-scale update after a step, as GradScaler.update does ("PaddlePaddle
+ * ZeRO优化", 混合精度才是最佳拍档): a skipped step halves the scale and
+ * resets *good_steps; otherwise *good_steps counts up and, on reaching
+ * growth_interval (> 0), the scale doubles and the count restarts.
+ * Returns the new scale; a NULL good_steps returns the scale unchanged. */
+float zero_scale_update(float scale, int32_t skipped, int64_t *good_steps,
+                        int64_t growth_interval);
+
+/* Name of a return code.  Never NULL. */
+const char *zero_strerror(int code);
+
+/* Message describing the last error returned on the calling thread ("" if
+ * none).  Valid until the next failing call on this thread. */
+const char *zero_last_error(void);
+
+/* ------------------------------------------------------------- context */
+
+/* Create a context.
+ *   numel       parameters in the flat vector (stages 1, 2); ignored for
+ *               stage 3, where it must equal the sum of unit_numels.
+ *   world       N, data-parallel ranks, 1..ZERO_MAX_RANKS.
+ *   stage       1, 2 or 3.  Stages 1 and 2 step identically; stage 1 can
+ *               also write the averaged grads (zero_bind_allreduce_out).
+ *   grad_dtype, param_dtype  element types of the grads and of the params.
+ *   rank        -1 for the all-ranks view, or 0..world-1 for one rank's view.
+ *   unit_numels, n_units  stage 3 only: parameter counts of the units
+ *               (layers), each sharded on its own with S_u = ceil(numel_u/N).
+ *               Must be NULL, 0 for stages 1 and 2.
+ * On success *out owns a host allocation released by zero_destroy(). */
+int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage,
+              int32_t grad_dtype, int32_t param_dtype, int32_t rank,
+              const int64_t *unit_numels, int32_t n_units);
+
+int zero_destroy(zero_ctx *ctx);
+
+/* Geometry of a context.  unit = -1 means the whole flat vector (stages 1,
+ * 2); for stage 3 pass a unit id.  Return -1 on bad arguments. */
+int64_t zero_ctx_shard_size(const zero_ctx *ctx, int32_t unit);
+/* floats the caller allocates for each of master, m and v */
+int64_t zero_ctx_state_elems(const zero_ctx *ctx);
+/* param-type elements of the bound parameter buffer: P for stages 1 and 2
+ * (the full vector), and for stage 3 the persistent shards: sum of P_u
+ * (all ranks) or sum of S_u (one rank) */
+int64_t zero_ctx_param_elems(const zero_ctx *ctx);
+/* where unit u starts inside the bound state (and scratch) and param buffers */
+int64_t zero_ctx_unit_state_offset(const zero_ctx *ctx, int32_t unit);
+int64_t zero_ctx_unit_param_offset(const zero_ctx *ctx, int32_t unit);
+
+/* Bytes of fp32 master + m + v the bound state occupies: 12 *
+ * zero_ctx_state_elems (what ZeroAdam.state_bytes() reports per rank in
+ * "ZeRO 与 FSDP…", 从零实现 ZeRO 的 Adam, for the one-rank view). */
+int64_t zero_state_bytes(const zero_ctx *ctx);
+
+/* ---------------------------------------------------- caller's buffers */
+
+/* Bind the caller's device buffers (the caller keeps ownership).
+ *   master, m, v  zero_ctx_state_elems() floats each.  The caller
+ *                 initializes master and zeroes m and v before step 1.
+ *   params        zero_ctx_param_elems() elements of param_dtype: the full
+ *                 parameter buffer every rank holds (stages 1, 2), or the
+ *                 persistent parameter shards (stage 3).
+ *   g_scratch     zero_ctx_state_elems() floats, or NULL.  Needed only by
+ *                 the two-pass loss-scaled path (zero_step with loss_scale >
+ *                 0, zero_step_reduce, zero3_reduce_unit): the reduced and
+ *                 unscaled grads wait there until the global overflow
+ *                 verdict is known.
+ *   flag          one 8-byte device word, zeroed by the caller before the
+ *                 first step.  Holds the id of the latest step that saw a
+ *                 non-finite grad; never needs clearing.
+ * May be called again to rebind. */
+int zero_bind(zero_ctx *ctx, float *master, float *m, float *v, void *params,
+              float *g_scratch, uint64_t *flag);
+
+/* Stage 1 only: also write the all-reduced mean grad (acc / N, before
+ * unscaling, in grad_dtype) to `grad_avg` (guanweilu.cn article 1460, Stage
+ * 1: each rank keeps the full averaged gradient).  All ranks: P elements,
+ * every position.  One rank: rank r writes its S positions at r*S of a
+ * P-element buffer.  NULL turns it off. */
+int zero_bind_allreduce_out(zero_ctx *ctx, void *grad_avg);
+
+/* ------------------------------------------------------------ the step */
+
+/* One ZeRO step (stages 1, 2) on `stream`.
+ *   grads, n_grads  host array of n_grads == world device pointers (see the
+ *                   two views above).
+ *   lr, beta1, beta2, eps  Adam hyperparameters; t >= 1 is the step count,
+ *                   advanced by the caller only for applied steps.
+ *   loss_scale      <= 0: no loss scaling, one fused pass (reduce-scatter +
+ *                   average + Adam + cast + all-gather placement); a
+ *                   non-finite grad is still reported by zero_step_status
+ *                   but never skips the step.  > 0: grads are divided by it
+ *                   after averaging; two passes: zero_step_reduce then
+ *                   zero_step_apply, and if any element of the step is
+ *                   non-finite the apply pass changes nothing (needs
+ *                   g_scratch).
+ * The overflow verdict is read with zero_step_status() after the stream
+ * reaches it. */
+int zero_step(zero_ctx *ctx, const void *const *grads, int32_t n_grads, double lr,
+              double beta1, double beta2, double eps, int64_t t, float loss_scale,
+              void *stream);
+
+/* First pass of the two-pass step: reduce-scatter sum, average, unscale
+ * (loss_scale > 0 divides), write the grads to g_scratch and record a
+ * non-finite value in the flag word.  Starts a new step. */
+int zero_step_reduce(zero_ctx *ctx, const void *const *grads, int32_t n_grads,
+                     float loss_scale, void *stream);
+
+/* Second pass: Adam from g_scratch on every element of the bound state, cast
+ * and placement -- unless the flag word names the current step, in which
+ * case the kernel returns without writing.  In the one-rank view the flag
+ * word may first be combined with the other ranks' words (a MAX
+ * all-reduce in a multi-process deployment); for stage 3 call it once after
+ * every unit's zero3_reduce_unit. */
+int zero_step_apply(zero_ctx *ctx, double lr, double beta1, double beta2, double eps,
+                    int64_t t, void *stream);
+
+/* Synchronizes the stream of the context's last step and reads the flag.
+ * *nonfinite (may be NULL) = 1 if the step saw an inf/nan; *skipped (may be
+ * NULL) = 1 if the step was loss-scaled and therefore skipped.  Returns
+ * ZERO_SKIPPED when skipped, ZERO_OK otherwise, < 0 on error. */
+int zero_step_status(zero_ctx *ctx, int32_t *nonfinite, int32_t *skipped);
+
+/* The id of the current step (what the flag word holds when it overflowed). */
+uint64_t zero_step_id(const zero_ctx *ctx);
+
+/* ------------------------------------------------------------ all-gather */
+
+/* Place the N shards of S = zero_ctx_shard_size(ctx, -1) elements of `dtype`
+ * into `full` (N*S elements): shard k lands at k*S ("ZeRO 与 FSDP…",
+ * all_gather_into_tensor).  shards is a host array of n_shards == world
+ * device pointers; a NULL entry is skipped (e.g. the own shard, already
+ * written by zero_step in the one-rank view).  Shard and destination may
+ * have any element-aligned addresses. */
+int zero_allgather(zero_ctx *ctx, const void *const *shards, int32_t n_shards,
+                   void *full, int32_t dtype, void *stream);
+
+/* ------------------------------------------------------------- stage 3 */
+
+/* Begin a stage-3 step: the units' calls until the next begin share one
+ * step id and one overflow verdict. */
+int zero3_begin_step(zero_ctx *ctx);
+
+/* Gather unit `unit`'s N parameter shards (S_u elements of param_dtype
+ * each) into unit_full (N*S_u elements), before the unit's forward and again
+ * before its backward ("ZeRO 与 FSDP…", ZeRO-3 与 FSDP).  NULL shards are
+ * skipped. */
+int zero3_gather_unit(zero_ctx *ctx, int32_t unit, const void *const *shards,
+                      int32_t n_shards, void *unit_full, void *stream);
+
+/* Reduce-scatter + average + Adam + cast for unit `unit` in one fused pass,
+ * without loss scaling (a skip would need every unit's verdict first).
+ * grads follow the view: all ranks -> numel_u-element local grads of the
+ * unit; one rank -> S_u-element slices.  The cast shard is written to the
+ * unit's place in the bound param buffer. */
+int zero3_step_unit(zero_ctx *ctx, int32_t unit, const void *const *grads,
+                    int32_t n_grads, double lr, double beta1, double beta2, double eps,
+                    int64_t t, void *stream);
+
+/* Loss-scaled stage 3: first pass for one unit (as zero_step_reduce on the
+ * unit's range).  After every unit, one zero_step_apply() applies Adam to all
+ * units, or to none if any unit overflowed. */
+int zero3_reduce_unit(zero_ctx *ctx, int32_t unit, const void *const *grads,
+                      int32_t n_grads, float loss_scale, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_GB300_ZERO_H */

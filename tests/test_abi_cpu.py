@@ -1,0 +1,138 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/zero.h declares, and its host-only logic (geometry, closed
+forms, loss-scale policy, argument checks) behaves."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "zero.h")
+
+
+@pytest.fixture(scope="module")
+def z():
+    from zero_sharded_optimizer_step_gb300 import build
+    build.build()
+    import zero_sharded_optimizer_step_gb300 as z
+    return z
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[a-z_][\w\s\*]*?\b(zero\w*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ["zero_init", "zero_bind", "zero_step", "zero_step_reduce", "zero_step_apply",
+                 "zero_step_status", "zero_allgather", "zero3_gather_unit", "zero3_step_unit",
+                 "zero3_reduce_unit", "zero_state_bytes", "zero_model_state_bytes",
+                 "zero_destroy", "zero_strerror", "zero_shard_size"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(z):
+    lib = ctypes.CDLL(z.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    out = subprocess.run(["nm", "-D", "--defined-only", z.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (zero\w*)$", out, flags=re.M))
+    assert set(declared_functions()) <= exported
+    # the binding wraps exactly the declared entry points
+    assert set(z.EXPORTED) == set(declared_functions())
+
+
+def test_header_compiles_as_c():
+    src = '#include "zero.h"\nint main(void){return ZERO_OK;}\n'
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                    "-x", "c", "-", "-o", os.devnull], input=src, text=True, check=True)
+
+
+def test_host_geometry_and_closed_forms(z):
+    import oracle
+    from oracle import memory as mem
+    for numel in (0, 1, 5, 19210, 7_500_000_000, 1_557_611_200):
+        for n in (1, 3, 4, 16, 64, 256):
+            assert z.zero_shard_size(numel, n) == oracle.shard_size(numel, n)
+    assert z.zero_shard_size(5, 0) == -1
+    for stage in range(4):
+        for psi, n in [(7 * 10**9, 8), (13 * 10**9, 16), (7_500_000_000, 64)]:
+            got = z.zero_model_state_bytes(psi, n, stage)
+            want = float(mem.model_state_bytes(psi, n, stage))
+            assert got == pytest.approx(want, rel=1e-15)
+    assert z.zero_model_state_bytes(1, 1, 4) == -1.0
+
+
+def test_scale_update_matches_oracle(z):
+    import oracle
+    s_z, g_z = 65536.0, 0
+    s_o, g_o = 65536.0, 0
+    pattern = [False] * 5 + [True] + [False] * 12 + [True, True] + [False] * 30
+    for sk in pattern:
+        s_z, g_z = z.zero_scale_update(s_z, sk, g_z, 10)
+        s_o, g_o = oracle.scale_update(s_o, sk, g_o, 10)
+        assert (s_z, g_z) == (s_o, g_o)
+
+
+def test_init_validation(z):
+    bad = [
+        dict(numel=10, world=0, stage=2),
+        dict(numel=10, world=257, stage=2),
+        dict(numel=10, world=4, stage=0),
+        dict(numel=10, world=4, stage=4),
+        dict(numel=-1, world=4, stage=2),
+        dict(numel=10, world=4, stage=2, rank=4),
+        dict(numel=10, world=4, stage=2, rank=-2),
+        dict(numel=10, world=4, stage=2, grad_dtype=7),
+        dict(numel=10, world=4, stage=2, unit_numels=[5, 5]),
+        dict(numel=10, world=4, stage=3),
+        dict(numel=11, world=4, stage=3, unit_numels=[5, 5]),
+        dict(numel=10, world=4, stage=3, unit_numels=[5, -5, 10]),
+    ]
+    for kw in bad:
+        args = dict(grad_dtype=z.ZERO_BF16, param_dtype=z.ZERO_BF16, rank=-1, unit_numels=None)
+        args.update(kw)
+        with pytest.raises(z.ZeroError) as ei:
+            z.zero_init(args["numel"], args["world"], args["stage"], args["grad_dtype"],
+                        args["param_dtype"], args["rank"], args["unit_numels"])
+        assert ei.value.code == z.ZERO_EINVAL
+        assert z.zero_last_error()
+
+
+def test_context_geometry(z):
+    c = z.zero_init(19210, 4, 2, z.ZERO_F32, z.ZERO_F32, -1)
+    assert z.zero_ctx_shard_size(c, -1) == 4803
+    assert z.zero_ctx_state_elems(c) == 19212
+    assert z.zero_ctx_param_elems(c) == 19212
+    c1 = z.zero_init(19210, 4, 2, z.ZERO_F32, z.ZERO_F32, 2)
+    assert z.zero_ctx_state_elems(c1) == 4803
+    assert z.zero_state_bytes(c1) == 57636          # ZeroAdam.state_bytes() per rank
+    units = [10, 7, 33]
+    c3 = z.zero_init(sum(units), 4, 3, z.ZERO_BF16, z.ZERO_BF16, 1, units)
+    S = [3, 2, 9]
+    assert [z.zero_ctx_shard_size(c3, u) for u in range(3)] == S
+    assert [z.zero_ctx_unit_state_offset(c3, u) for u in range(3)] == [0, 3, 5]
+    assert z.zero_ctx_state_elems(c3) == 14 and z.zero_ctx_param_elems(c3) == 14
+    c3a = z.zero_init(sum(units), 4, 3, z.ZERO_BF16, z.ZERO_BF16, -1, units)
+    assert [z.zero_ctx_unit_param_offset(c3a, u) for u in range(3)] == [0, 12, 20]
+    assert z.zero_ctx_state_elems(c3a) == 56
+    assert z.zero_ctx_shard_size(c3a, 3) == -1 and z.zero_ctx_shard_size(c3a, -1) == -1
+    c0 = z.zero_init(0, 8, 2, z.ZERO_BF16, z.ZERO_BF16, -1)
+    assert z.zero_ctx_state_elems(c0) == 0
+
+
+def test_calls_before_bind_fail_cleanly(z):
+    c = z.zero_init(100, 4, 2, z.ZERO_BF16, z.ZERO_BF16, -1)
+    with pytest.raises(z.ZeroError) as ei:
+        z.zero_step(c, [0, 0, 0, 0], 1e-3, 0.9, 0.999, 1e-8, 1, stream=0)
+    assert ei.value.code == z.ZERO_ESTATE
+    with pytest.raises(z.ZeroError) as ei:
+        z.zero_step_status(c)
+    assert ei.value.code == z.ZERO_ESTATE
+    with pytest.raises(z.ZeroError):
+        z.zero3_begin_step(c)   # not stage 3

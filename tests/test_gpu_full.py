@@ -1,0 +1,120 @@
+"""The five workloads at their full sizes, in the launch configuration the
+benchmark times.  The oracle computes sampled elements one by one (the step
+is elementwise): the first and last 4096 positions of every shard plus 2^20
+seeded random positions.  Properties that hold at any size cover the rest:
+the skip pattern, the padding, and the placement (the full buffer is the
+concatenation of the shards)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import workloads as W
+from tests import refs
+from tests.test_gpu_parity import assert_params_close, assert_state_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_positions(n_state, S, seed=0, n_rand=1 << 20):
+    rng = np.random.default_rng(seed)
+    idx = [np.arange(0, min(4096, n_state))]
+    for lo in range(0, n_state, S):
+        idx.append(np.arange(lo, min(lo + 4096, n_state)))
+        idx.append(np.arange(max(lo, min(lo + S, n_state) - 4096), min(lo + S, n_state)))
+    idx.append(rng.integers(0, n_state, n_rand))
+    return np.unique(np.concatenate(idx)).astype(np.int64)
+
+
+def gpu_at(t: torch.Tensor, idx: np.ndarray) -> np.ndarray:
+    return to_np(t[torch.from_numpy(idx).to(t.device)])
+
+
+def check_sampled(run, w, idx, unit=0, state_off=0, param_off=None, skipped=()):
+    iters = list(range(1, w.steps + 1))
+    x, m, v, p = refs.sampled_reference(w, idx, iters, skipped_iters=set(skipped),
+                                        rank=w.rank, unit=unit)
+    assert_state_close(gpu_at(run.master, idx + state_off), x, w.name + " master")
+    assert_state_close(gpu_at(run.m, idx + state_off), m, w.name + " m")
+    assert_state_close(gpu_at(run.v, idx + state_off), v, w.name + " v")
+    poff = state_off if param_off is None else param_off
+    assert_params_close(gpu_at(run.params, idx + poff), p, w.param_dtype, w.name + " params")
+    # bit-identical as well (same operations in the same order)
+    assert gpu_at(run.master, idx + state_off).tobytes() == x.tobytes()
+
+
+def run_all(w):
+    from workloads.runner import Runner
+    run = Runner(w)
+    for it in range(1, w.steps + 1):
+        run.step(it)
+    torch.cuda.synchronize()
+    return run
+
+
+def test_gpt2_small_full():
+    w = W.gpt2_small()
+    run = run_all(w)
+    assert run.skips == [False] * w.steps
+    P = w.shard * w.world
+    check_sampled(run, w, sample_positions(P, w.shard))
+    run.close()
+
+
+def test_gpt2_xl_full_loss_scaled():
+    w = W.gpt2_xl()
+    run = run_all(w)
+    # the one +inf at iteration 3 skips exactly that step; the draws are
+    # bounded (|x| <= 3.47 sigma * scale), so no other overflow is possible
+    assert run.skips == [i == 3 for i in range(1, w.steps + 1)]
+    assert run.scale == 2.0 ** 15 and run.t == w.steps - 1
+    P = w.shard * w.world
+    idx = sample_positions(P, w.shard)
+    e = refs.synth.pick_index(w.seed, w.numel, step=3, rank=5)
+    idx = np.unique(np.concatenate([idx, [e]]))
+    check_sampled(run, w, idx, skipped=(3,))
+    run.close()
+
+
+@pytest.mark.parametrize("rank", [0, 1])
+def test_one_rank_7p5b_full(rank):
+    """Rank 0 (aligned) and rank 1 (its place in the full buffer is 8 bytes
+    off a 16-byte boundary) of 64, then placement into 7.5e9 bf16."""
+    w = W.one_rank_7p5b(rank)
+    run = run_all(w)
+    S = w.shard
+    check_sampled(run, w, sample_positions(S, S), param_off=rank * S)
+    # placement: the full buffer is the concatenation of the shards
+    full = run.params
+    for k in range(w.world):
+        part = full[k * S:(k + 1) * S]
+        if k == rank:
+            assert torch.equal(part, run.master.to(torch.bfloat16))
+        else:
+            assert torch.equal(part, run.shards[k])
+    # and the shards hold the seeded draws (sampled)
+    for k in (0, 1, 33, 63):
+        if k == rank:
+            continue
+        pos = np.array([0, 1, 12345, S - 1], np.int64)
+        want = synth.fill_host(pos.size, w.param_dtype, synth.key(w.seed, W.KIND_SHARD, 0, k),
+                               w.sigma_master, indices=pos + k * S)
+        assert gpu_at(full, pos + k * S).tobytes() == want.tobytes()
+    run.close()
+
+
+def test_zero3_llama7b_full():
+    from zero_sharded_optimizer_step_gb300 import zero_ctx_unit_state_offset
+    w = W.zero3_llama7b()
+    run = run_all(w)
+    assert run.skips == [False] * w.steps
+    Su = w.unit_shard(0)
+    for u in (0, 13, 31):
+        off = zero_ctx_unit_state_offset(run.ctx, u)
+        idx = sample_positions(Su, Su, seed=u, n_rand=1 << 17)
+        check_sampled(run, w, idx, unit=u, state_off=off)
+    # the last gather (unit 0, before its backward) placed all 8 shards
+    full = run.unit_full
+    for k in range(w.world):
+        assert torch.equal(full[k * Su:(k + 1) * Su], run.shards[0][k])
+    run.close()

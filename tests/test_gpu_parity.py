@@ -1,0 +1,360 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, element by
+element, at sizes the oracle finishes in seconds that still span many
+thread blocks and end in a ragged tail.
+
+Bars (the method's stated tolerances):
+  master, m, v:   |gpu - oracle| <= 2e-6 * |oracle| + 1e-9
+  params:         at most 1 ulp apart (16-bit patterns)
+  layout, padding, placement, skip decisions: bit-exact
+The kernels perform the oracle's operations in the oracle's order, so they
+are also expected to be bit-identical; test_bit_identical checks that.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import workloads as W
+from tests import refs
+
+pytestmark = pytest.mark.gpu
+
+STORAGE = oracle.NP_STORAGE
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().contiguous().cpu()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def assert_state_close(got, ref, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    both_nan = np.isnan(got) & np.isnan(ref)
+    d = np.abs(got - ref)
+    ok = (d <= 2e-6 * np.abs(ref) + 1e-9) | both_nan | (got == ref)
+    if not ok.all():
+        i = np.flatnonzero(~ok)[:5]
+        raise AssertionError("%s: %d elements out of tolerance, e.g. %s: gpu %s oracle %s"
+                             % (what, (~ok).sum(), i, got[i], ref[i]))
+
+
+def assert_params_close(got, ref, dtype, what):
+    if dtype == oracle.F32:
+        return assert_state_close(got, ref, what)
+    g = got.astype(np.int32)
+    r = ref.astype(np.int32)
+    gv = oracle.widen(got, dtype)
+    rv = oracle.widen(ref, dtype)
+    nan = np.isnan(gv) & np.isnan(rv)
+    # same sign: 1 ulp = adjacent patterns; +0/-0 count as equal
+    ok = (np.abs(g - r) <= 1) & ((g >> 15) == (r >> 15)) | nan | (gv == rv)
+    if not ok.all():
+        i = np.flatnonzero(~ok)[:5]
+        raise AssertionError("%s: %d params more than 1 ulp off, e.g. %s" % (what, (~ok).sum(), i))
+
+
+def compare_runner(run, ref, exact=True, what=""):
+    w = run.w
+    if w.stage < 3:
+        x, m, v = ref.state[0]
+        full_ref = ref.full
+    else:
+        x = np.concatenate([ref.state[u][0] for u in sorted(ref.state)])
+        m = np.concatenate([ref.state[u][1] for u in sorted(ref.state)])
+        v = np.concatenate([ref.state[u][2] for u in sorted(ref.state)])
+        full_ref = np.concatenate([ref.own[u] for u in sorted(ref.own)])
+    gx, gm, gv, gp = to_np(run.master), to_np(run.m), to_np(run.v), to_np(run.params)
+    assert_state_close(gx, x, what + " master")
+    assert_state_close(gm, m, what + " m")
+    assert_state_close(gv, v, what + " v")
+    assert_params_close(gp, full_ref, w.param_dtype, what + " params")
+    if exact:
+        for name, a, b in [("master", gx, x), ("m", gm, m), ("v", gv, v), ("params", gp, full_ref)]:
+            assert a.tobytes() == b.tobytes(), "%s %s not bit-identical" % (what, name)
+
+
+def run_both(w, iters=None):
+    from workloads.runner import Runner
+    iters = iters or list(range(1, w.steps + 1))
+    run = Runner(w)
+    ref = refs.OracleRun(w)
+    for it in iters:
+        run.step(it)
+        ref.step(it)
+    torch.cuda.synchronize()
+    assert run.skips == ref.skips
+    return run, ref
+
+
+def test_bit_identical_tiny_config():
+    """The tiny MLP config: 4 ranks, fp32, 3 steps."""
+    run, ref = run_both(W.tiny())
+    compare_runner(run, ref, exact=True, what="tiny")
+    # and the same as plain Adam over the whole vector on the mean grad
+    w = W.tiny()
+    x = refs.host_master(w)
+    m, v = np.zeros_like(x), np.zeros_like(x)
+    for t in range(1, 4):
+        g = oracle.all_reduce_mean(refs.host_grads(w, t, 0.0), w.grad_dtype, w.numel)
+        oracle.adam(x, m, v, g, w.lr, w.beta1, w.beta2, w.eps, t)
+    assert to_np(run.master).tobytes() == x.tobytes()
+    run.close()
+
+
+CASES = []
+for gdt, pdt in [(W.BF16, W.BF16), (W.F16, W.F16), (W.F32, W.F32), (W.BF16, W.F32),
+                 (W.F32, W.BF16), (W.F16, W.BF16), (W.BF16, W.F16), (W.F32, W.F16),
+                 (W.F16, W.F32)]:
+    CASES.append((1_000_003, 8, gdt, pdt, -1))
+for numel, world, rank in [(1_000_003, 3, -1), (1_000_003, 3, 0), (1_000_003, 3, 2),
+                           (777_777, 16, 5), (777_777, 16, 15), (500_000, 1, -1),
+                           (500_000, 1, 0), (99_999, 64, -1), (99_999, 64, 63),
+                           (2_000_001, 13, 7)]:
+    CASES.append((numel, world, W.BF16, W.BF16, rank))
+    CASES.append((numel, world, W.F16, W.F32, rank))
+
+
+@pytest.mark.parametrize("numel,world,gdt,pdt,rank", CASES)
+def test_parity_fused(numel, world, gdt, pdt, rank):
+    w = W.Workload("case", numel, world, 2, gdt, pdt, rank=rank, steps=3, lr=1e-3)
+    run, ref = run_both(w)
+    compare_runner(run, ref, what=str((numel, world, gdt, pdt, rank)))
+    run.close()
+
+
+@pytest.mark.parametrize("rank", [-1, 0, 11])
+def test_parity_loss_scaled_skip_sequence(rank):
+    """Sixteen fp16 ranks, loss scale 2^16, a +inf in rank 5 at iteration 3:
+    iterations 1-2 apply, 3 is skipped (nothing written, scale halved), 4-6
+    apply with t = 3, 4, 5 -- bit-identical to the oracle."""
+    w = W.Workload("scaled", 1_234_567, 16, 2, W.F16, W.F16, rank=rank, steps=6,
+                   loss_scale=2.0 ** 16, inject=(3, 5))
+    if rank >= 0:
+        # the injected element must fall in this rank's shard for a local verdict
+        e = synth.pick_index(w.seed, w.numel, step=3, rank=5)
+        w = w.replace(rank=e // w.shard)
+    run, ref = run_both(w)
+    assert ref.skips == [False, False, True, False, False, False]
+    assert run.scale == ref.scale == 2.0 ** 15
+    compare_runner(run, ref, what="scaled")
+    run.close()
+
+
+def test_two_pass_equals_fused():
+    """zero_step_reduce (no scaling) + zero_step_apply == the fused step."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    w = W.Workload("tp", 654_321, 8, 2, W.BF16, W.BF16, steps=3)
+    a = Runner(w)
+    b = Runner(w, scratch=True)
+    for it in range(1, 4):
+        a.fill_grads(it)
+        a.launch_step()
+        a.finish_step()
+        b.fill_grads(it)
+        z.zero_step_reduce(b.ctx, b.grads[0], 0.0, b.stream)
+        z.zero_step_apply(b.ctx, w.lr, w.beta1, w.beta2, w.eps, it, b.stream)
+    torch.cuda.synchronize()
+    for x, y in [(a.master, b.master), (a.m, b.m), (a.v, b.v), (a.params, b.params)]:
+        assert torch.equal(x, y)
+
+
+def test_misaligned_buffers_take_the_exact_path():
+    """Buffers that start off a 16-byte boundary (element-aligned views)."""
+    import zero_sharded_optimizer_step_gb300 as z
+    numel, world = 100_003, 5
+    w = W.Workload("mis", numel, world, 2, W.BF16, W.BF16, steps=2)
+    ref = refs.OracleRun(w)
+    P = w.shard * world
+    dev = torch.device("cuda:0")
+    big = lambda n, dt, off: torch.zeros(n + 16, dtype=dt, device=dev)[off:off + n]  # noqa
+    master = big(P, torch.float32, 1)
+    m, v = big(P, torch.float32, 3), big(P, torch.float32, 2)
+    params = big(P, torch.bfloat16, 5)
+    flag = torch.zeros(1, dtype=torch.int64, device=dev)
+    master[:] = torch.from_numpy(refs.host_master(w)).to(dev)
+    ctx = z.zero_init(numel, world, 2, z.ZERO_BF16, z.ZERO_BF16, -1)
+    z.zero_bind(ctx, master, m, v, params, None, flag)
+    for t in (1, 2):
+        hg = refs.host_grads(w, t, 0.0)
+        gd = [big(numel, torch.bfloat16, 1 + k) for k in range(world)]
+        for k in range(world):
+            gd[k].copy_(torch.from_numpy(hg[k].view(np.int16)).view(torch.bfloat16))
+        z.zero_step(ctx, gd, w.lr, w.beta1, w.beta2, w.eps, t)
+        ref.step(t)
+    torch.cuda.synchronize()
+    x, mm, vv = ref.state[0]
+    assert to_np(master).tobytes() == x.tobytes()
+    assert to_np(m).tobytes() == mm.tobytes() and to_np(v).tobytes() == vv.tobytes()
+    assert to_np(params).tobytes() == ref.full.tobytes()
+
+
+@pytest.mark.parametrize("rank", [-1, 2])
+def test_stage1_allreduce_output(rank):
+    """Stage 1 keeps the full averaged grads: RS + AG == AR, bit-exact."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    w = W.Workload("s1", 300_007, 6, 1, W.BF16, W.BF16, rank=rank, steps=1)
+    run = Runner(w)
+    avg = torch.zeros(w.shard * w.world, dtype=torch.bfloat16, device="cuda:0")
+    z.zero_bind_allreduce_out(run.ctx, avg)
+    run.step(1)
+    torch.cuda.synchronize()
+    want = oracle.cast(oracle.all_reduce_mean(refs.host_grads(w, 1, 0.0), w.grad_dtype,
+                                              w.numel), w.grad_dtype)
+    got = to_np(avg)
+    if rank < 0:
+        assert got.tobytes() == want.tobytes()
+    else:
+        S = w.shard
+        assert got[rank * S:(rank + 1) * S].tobytes() == want[rank * S:(rank + 1) * S].tobytes()
+        assert not got[:rank * S].any() and not got[(rank + 1) * S:].any()
+    run.close()
+
+
+@pytest.mark.parametrize("S,world,dtype,dst_off", [(1, 1, W.BF16, 0), (7, 3, W.BF16, 1),
+                                                    (1001, 8, W.F16, 3), (4096, 4, W.F32, 1),
+                                                    (117_187, 64, W.BF16, 0),
+                                                    (250_001, 5, W.BF16, 7),
+                                                    (3_000_000, 4, W.F32, 2)])
+def test_gather_placement(S, world, dtype, dst_off):
+    """All-gather placement is a bit-exact copy for any alignment."""
+    import zero_sharded_optimizer_step_gb300 as z
+    dev = torch.device("cuda:0")
+    tdt = {W.F32: torch.float32, W.BF16: torch.bfloat16, W.F16: torch.float16}[dtype]
+    numel = S * world
+    ctx = z.zero_init(numel, world, 2, dtype, dtype, 0)
+    shards_h = [synth.fill_host(S, dtype, synth.key(5, W.KIND_SHARD, 0, k), 1.0)
+                for k in range(world)]
+    shards = []
+    for k, h in enumerate(shards_h):
+        buf = torch.zeros(S + 16, dtype=tdt, device=dev)[(k * 3) % 8:][:S]
+        src = torch.from_numpy(h.view(np.int16) if dtype != W.F32 else h)
+        buf.copy_(src.view(tdt) if dtype != W.F32 else src)
+        shards.append(buf)
+    full = torch.full((numel + 16,), 7, dtype=tdt, device=dev)[dst_off:dst_off + numel]
+    master = torch.zeros(S, device=dev)
+    flag = torch.zeros(1, dtype=torch.int64, device=dev)
+    z.zero_bind(ctx, master, master, master, full, None, flag)
+    skip = world // 2
+    z.zero_allgather(ctx, [s if k != skip else None for k, s in enumerate(shards)], full, dtype)
+    torch.cuda.synchronize()
+    got = to_np(full)
+    want = oracle.all_gather(shards_h, dtype)
+    keep = np.ones(numel, bool)
+    keep[skip * S:(skip + 1) * S] = False
+    assert got[keep].tobytes() == want[keep].tobytes()
+    seven = to_np(torch.full((1,), 7, dtype=tdt))
+    assert (got[~keep] == seven[0]).all()      # the skipped shard is untouched
+
+
+@pytest.mark.parametrize("rank,scaled", [(1, False), (-1, False), (0, True)])
+def test_stage3_units(rank, scaled):
+    """ZeRO-3: per unit, gather before forward and before backward, then the
+    unit's reduce + Adam; every gathered buffer and the final state match."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    units = [100_003, 7, 250_000, 33_333]
+    w = W.Workload("z3", sum(units), 4, 3, W.BF16, W.BF16, rank=rank, units=units, steps=3,
+                   loss_scale=2.0 ** 10 if scaled else 0.0)
+    run = Runner(w)
+    ref = refs.OracleRun(w)
+    for it in range(1, 4):
+        run.fill_grads(it)
+        t = run.t + 1
+        z.zero3_begin_step(run.ctx)
+        seen = []
+        for u in range(len(units)):
+            z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full)
+            seen.append(to_np(run.unit_full[:w.unit_shard(u) * w.world]))
+        for u in reversed(range(len(units))):
+            z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full)
+            seen.append(to_np(run.unit_full[:w.unit_shard(u) * w.world]))
+            if scaled:
+                z.zero3_reduce_unit(run.ctx, u, run.grads[u], run.scale)
+            else:
+                z.zero3_step_unit(run.ctx, u, run.grads[u], w.lr, w.beta1, w.beta2, w.eps, t)
+        if scaled:
+            z.zero_step_apply(run.ctx, w.lr, w.beta1, w.beta2, w.eps, t)
+        run.finish_step()
+        ref.step(it)
+        want = [g[2] for g in ref.gathers[-2 * len(units):]]
+        for a, b in zip(seen, want):
+            assert a.tobytes() == b.tobytes()
+    assert run.skips == ref.skips
+    compare_runner(run, ref, what="stage3")
+    run.close()
+
+
+def test_degenerate_sizes():
+    """numel = 0 (nothing to do), numel < world (ranks owning only padding)
+    and world = 1 (the identity reduce)."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    c = z.zero_init(0, 8, 2, z.ZERO_BF16, z.ZERO_BF16, -1)
+    dev = torch.device("cuda:0")
+    e = torch.zeros(0, device=dev)
+    flag = torch.zeros(1, dtype=torch.int64, device=dev)
+    z.zero_bind(c, e, e, e, e, None, flag)
+    z.zero_step(c, [None] * 8, 1e-3, 0.9, 0.999, 1e-8, 1)
+    assert z.zero_step_status(c) == (False, False)
+    for numel, world, rank in [(3, 4, -1), (3, 4, 3), (1, 1, -1), (5, 8, 6), (17, 1, 0)]:
+        w = W.Workload("deg", numel, world, 2, W.BF16, W.F32, rank=rank, steps=2)
+        run, ref = run_both(w)
+        compare_runner(run, ref, what="deg")
+        run.close()
+
+
+def test_nonfinite_without_loss_scaling_is_reported_not_skipped():
+    from workloads.runner import Runner
+    w = W.Workload("nf", 10_000, 4, 2, W.F32, W.F32, steps=1, inject=(1, 2))
+    run, ref = run_both(w)
+    assert run.skips == [False]
+    compare_runner(run, ref, what="nf")
+    import zero_sharded_optimizer_step_gb300 as z
+    assert z.zero_step_status(run.ctx) == (True, False)
+    run.close()
+
+
+def test_error_codes_on_device():
+    import zero_sharded_optimizer_step_gb300 as z
+    dev = torch.device("cuda:0")
+    c = z.zero_init(1000, 4, 2, z.ZERO_BF16, z.ZERO_BF16, -1)
+    P = z.zero_ctx_state_elems(c)
+    f = torch.zeros(P, device=dev)
+    p = torch.zeros(P, dtype=torch.bfloat16, device=dev)
+    flag = torch.zeros(1, dtype=torch.int64, device=dev)
+    z.zero_bind(c, f, f.clone(), f.clone(), p, None, flag)
+    g = [torch.zeros(1000, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    cases = [
+        (lambda: z.zero_step(c, g[:3], 1e-3, 0.9, 0.999, 1e-8, 1), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g, 1e-3, 0.9, 0.999, 1e-8, 0), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g[:3] + [None], 1e-3, 0.9, 0.999, 1e-8, 1), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g[:3] + [g[3].data_ptr() + 1], 1e-3, 0.9, 0.999, 1e-8, 1),
+         z.ZERO_EALIGN),
+        (lambda: z.zero_step(c, g, 1e-3, 0.9, 0.999, 1e-8, 1, loss_scale=1024.0),
+         z.ZERO_ESTATE),
+        (lambda: z.zero3_gather_unit(c, 0, g, p), z.ZERO_EINVAL),
+        (lambda: z.zero_bind(c, f.data_ptr() + 2, f, f, p, None, flag), z.ZERO_EALIGN),
+    ]
+    for fn, code in cases:
+        with pytest.raises(z.ZeroError) as ei:
+            fn()
+        assert ei.value.code == code, z.zero_last_error()
+    torch.cuda.synchronize()
+    assert not f.any()         # nothing was launched
+
+
+@pytest.mark.parametrize("numel,world,rank", [(1_000_001, 6, 1), (999_999, 64, 63)])
+def test_one_rank_step_then_placement(numel, world, rank):
+    """One rank's view: its shard is updated in place in the full buffer,
+    then the other ranks' shards are placed around it."""
+    w = W.Workload("or", numel, world, 2, W.BF16, W.BF16, rank=rank, steps=2,
+                   gather_after=True)
+    run, ref = run_both(w)
+    compare_runner(run, ref, what="one-rank+placement")
+    run.close()

@@ -1,0 +1,118 @@
+"""The synthetic workloads: parameter counts built from the model shapes the
+pages' experiments use, and the input recipe (seeded draws from ``synth``).
+
+No arithmetic of the method lives here.
+
+  tiny            MLP Linear(64,256)+GELU+Linear(256,10): 19,210 fp32 params,
+                  4 ranks, 3 steps, lr 1e-2 ("ZeRO 与 FSDP…", zero_check).
+  gpt2_small      GPT-2 small (d 768, 12 layers, vocab 50257, context 1024):
+                  124,439,808 params, 8 ranks, bf16 grads and params, 10 steps.
+  gpt2_xl         GPT-2 XL (d 1600, 48 layers; the 1.5B model of "论文专题讲解：
+                  ZeRO", Table 5): 1,557,611,200 params, 16 ranks, fp16 grads
+                  drawn at N(0,1e-3) times the current loss scale (2^16 at the
+                  start), one +inf in rank 5 at iteration 3.
+  one_rank_7p5b   rank 0 of 64 for a 7.5B model (the Figure 1 setting of the
+                  same page): shard 117,187,500, 64 incoming bf16 slices, then
+                  the placement of 64 bf16 shards into the 7.5e9 buffer.
+  zero3_llama7b   32 units shaped like a Llama-7B layer (hidden 4096, SwiGLU
+                  FFN 11008, no bias): 202,383,360 params each, rank 0 of 8.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional, Tuple
+
+F32, BF16, F16 = 0, 1, 2
+KIND_SHARD = 3   # synthetic parameter shards held by the other ranks
+
+
+def gpt2_numel(d: int, layers: int, vocab: int = 50257, ctx: int = 1024) -> int:
+    per_layer = (2 * 2 * d                 # ln_1, ln_2 (weight, bias)
+                 + d * 3 * d + 3 * d       # attn c_attn
+                 + d * d + d               # attn c_proj
+                 + d * 4 * d + 4 * d       # mlp c_fc
+                 + 4 * d * d + d)          # mlp c_proj
+    return vocab * d + ctx * d + layers * per_layer + 2 * d
+
+
+def mlp_numel() -> int:
+    return 64 * 256 + 256 + 256 * 10 + 10
+
+
+def llama_layer_numel(hidden: int = 4096, ffn: int = 11008) -> int:
+    return 4 * hidden * hidden + 3 * hidden * ffn + 2 * hidden
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    numel: int
+    world: int
+    stage: int
+    grad_dtype: int
+    param_dtype: int
+    rank: int = -1                       # -1: every rank's state on this GPU
+    units: Optional[List[int]] = None    # stage 3
+    steps: int = 3
+    lr: float = 1e-4
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    sigma_grad: float = 1e-3
+    sigma_master: float = 0.01
+    loss_scale: float = 0.0              # initial scale; 0 = off
+    growth_interval: int = 2000
+    inject: Optional[Tuple[int, int]] = None   # (iteration, rank): one +inf
+    gather_after: bool = False           # place the other ranks' shards too
+    seed: int = 0
+
+    @property
+    def shard(self) -> int:
+        return -(-self.numel // self.world)
+
+    def unit_shard(self, u: int) -> int:
+        return -(-self.units[u] // self.world)
+
+    def updated_per_step(self) -> int:
+        """Owned elements one step updates (the params-updated/s unit)."""
+        if self.stage == 3:
+            s = sum(self.unit_shard(u) for u in range(len(self.units)))
+            return s * (self.world if self.rank < 0 else 1)
+        return self.shard * (self.world if self.rank < 0 else 1)
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+def tiny() -> Workload:
+    return Workload("tiny", mlp_numel(), 4, 2, F32, F32, steps=3, lr=1e-2,
+                    sigma_grad=0.01, sigma_master=0.01)
+
+
+def gpt2_small() -> Workload:
+    return Workload("gpt2_small", gpt2_numel(768, 12), 8, 2, BF16, BF16, steps=10)
+
+
+def gpt2_xl() -> Workload:
+    return Workload("gpt2_xl", gpt2_numel(1600, 48), 16, 2, F16, F16, steps=10,
+                    loss_scale=2.0 ** 16, inject=(3, 5))
+
+
+def one_rank_7p5b(rank: int = 0) -> Workload:
+    return Workload("one_rank_7p5b", 7_500_000_000, 64, 2, BF16, BF16, rank=rank, steps=3,
+                    gather_after=True)
+
+
+def zero3_llama7b(n_units: int = 32) -> Workload:
+    return Workload("zero3_llama7b", 32 * llama_layer_numel() if n_units == 32
+                    else n_units * llama_layer_numel(), 8, 3, BF16, BF16, rank=0,
+                    units=[llama_layer_numel()] * n_units, steps=2)
+
+
+ALL = {"tiny": tiny, "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl,
+       "one_rank_7p5b": one_rank_7p5b, "zero3_llama7b": zero3_llama7b}
+
+
+def grad_sigma(w: Workload, scale: float) -> float:
+    """Grads are drawn at sigma_grad times the loss scale in force."""
+    return w.sigma_grad * (scale if scale > 0 else 1.0)

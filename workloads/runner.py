@@ -1,0 +1,207 @@
+"""Runs a Workload on one GPU through the C ABI binding.
+
+PyTorch allocates the buffers; ``synth`` draws the inputs on the device; every
+step of the method runs in libzero.so.  Shared by the GPU tests and bench.py.
+
+Index space of the draws (the same on the oracle side): rank k's local
+gradient at iteration `it` and flat position i is stream (GRAD, it, k, unit)
+at index i; the initial master weight at i is stream (MASTER, 0, 0, unit) at
+index i.  In one rank's view rank r holds positions r*S ... r*S+S-1.
+"""
+from __future__ import annotations
+
+import torch
+
+import synth
+import zero_sharded_optimizer_step_gb300 as z
+
+from . import KIND_SHARD, Workload, grad_sigma
+
+TORCH_DTYPE = {0: torch.float32, 1: torch.bfloat16, 2: torch.float16}
+
+
+def valid_len(numel: int, S: int, rank: int) -> int:
+    """Positions of rank `rank`'s shard that hold real parameters."""
+    return max(0, min(S, numel - rank * S))
+
+
+def inject_index(w: Workload, it: int, rank: int, unit: int = 0) -> int:
+    n = w.units[unit] if w.units else w.numel
+    return synth.pick_index(w.seed, n, step=it, rank=rank, unit=unit)
+
+
+class Runner:
+    def __init__(self, w: Workload, device: str = "cuda:0", scratch: bool | None = None):
+        self.w = w
+        self.dev = torch.device(device)
+        torch.cuda.set_device(self.dev)
+        self.ctx = z.zero_init(w.numel, w.world, w.stage, w.grad_dtype, w.param_dtype, w.rank,
+                               w.units)
+        ns = z.zero_ctx_state_elems(self.ctx)
+        npar = z.zero_ctx_param_elems(self.ctx)
+        f32 = dict(dtype=torch.float32, device=self.dev)
+        self.master = torch.zeros(ns, **f32)
+        self.m = torch.zeros(ns, **f32)
+        self.v = torch.zeros(ns, **f32)
+        self.params = torch.zeros(npar, dtype=TORCH_DTYPE[w.param_dtype], device=self.dev)
+        need_scratch = w.loss_scale > 0 if scratch is None else scratch
+        self.g = torch.zeros(ns, **f32) if need_scratch else None
+        self.flag = torch.zeros(1, dtype=torch.int64, device=self.dev)
+        z.zero_bind(self.ctx, self.master, self.m, self.v, self.params, self.g, self.flag)
+        self.stream = torch.cuda.current_stream(self.dev)
+        self.scale = w.loss_scale
+        self.good = 0
+        self.t = 0
+        self.skips = []
+        self._init_state()
+        self._alloc_grads()
+        self._alloc_shards()
+
+    # ------------------------------------------------------------ set-up
+
+    def _fill(self, buf: torch.Tensor, n: int, dtype: int, key: int, sigma: float,
+              index0: int = 0):
+        if n > 0:
+            synth.fill_device(buf.data_ptr(), n, dtype, key, sigma, self.stream.cuda_stream,
+                              index0=index0)
+
+    def _units(self):
+        """(unit id, numel, S, state offset) for every shardable range."""
+        w = self.w
+        if w.stage < 3:
+            return [(0, w.numel, w.shard, 0)]
+        return [(u, w.units[u], w.unit_shard(u), z.zero_ctx_unit_state_offset(self.ctx, u))
+                for u in range(len(w.units))]
+
+    def _init_state(self):
+        w = self.w
+        for u, nu, Su, off in self._units():
+            k = synth.key(w.seed, synth.KIND_MASTER, 0, 0, u)
+            if w.rank < 0:
+                self._fill(self.master[off:], nu, synth.F32, k, w.sigma_master)
+            else:
+                self._fill(self.master[off:], valid_len(nu, Su, w.rank), synth.F32, k,
+                           w.sigma_master, index0=w.rank * Su)
+        # the low-precision copy starts as the rounded master
+        if w.stage < 3 and w.rank >= 0:
+            S = w.shard
+            self.params[w.rank * S:(w.rank + 1) * S] = self.master.to(self.params.dtype)
+        else:
+            self.params.copy_(self.master.to(self.params.dtype))
+
+    def _alloc_grads(self):
+        w = self.w
+        dt = TORCH_DTYPE[w.grad_dtype]
+        self.grads = []   # per unit: list of world tensors
+        for u, nu, Su, off in self._units():
+            n = nu if w.rank < 0 else Su
+            self.grads.append([torch.zeros(n, dtype=dt, device=self.dev) for _ in range(w.world)])
+
+    def _alloc_shards(self):
+        """The other ranks' parameter shards (one-rank view with placement,
+        and stage 3) and the stage-3 unit buffer."""
+        w = self.w
+        self.shards = None
+        self.unit_full = None
+        dt = TORCH_DTYPE[w.param_dtype]
+        if w.stage == 3:
+            self.shards = []
+            Pmax = 0
+            for u, nu, Su, off in self._units():
+                row = []
+                for k in range(w.world):
+                    if w.rank < 0:
+                        row.append(self.params[off + k * Su: off + (k + 1) * Su])
+                    elif k == w.rank:
+                        row.append(self.params[off: off + Su])
+                    else:
+                        t = torch.zeros(Su, dtype=dt, device=self.dev)
+                        kk = synth.key(w.seed, KIND_SHARD, 0, k, u)
+                        self._fill(t, valid_len(nu, Su, k), w.param_dtype, kk, w.sigma_master,
+                                   index0=k * Su)
+                        row.append(t)
+                self.shards.append(row)
+                Pmax = max(Pmax, Su * w.world)
+            self.unit_full = torch.zeros(Pmax, dtype=dt, device=self.dev)
+        elif w.rank >= 0 and w.gather_after:
+            S = w.shard
+            self.shards = []
+            for k in range(w.world):
+                if k == w.rank:
+                    self.shards.append(None)   # written by the step itself
+                    continue
+                t = torch.zeros(S, dtype=dt, device=self.dev)
+                kk = synth.key(w.seed, KIND_SHARD, 0, k, 0)
+                self._fill(t, valid_len(w.numel, S, k), w.param_dtype, kk, w.sigma_master,
+                           index0=k * S)
+                self.shards.append(t)
+
+    # ------------------------------------------------------------- inputs
+
+    def fill_grads(self, it: int):
+        """Draw iteration `it`'s grads of every rank (and unit) on the device."""
+        w = self.w
+        sigma = grad_sigma(w, self.scale)
+        for (u, nu, Su, off), row in zip(self._units(), self.grads):
+            for k in range(w.world):
+                key = synth.key(w.seed, synth.KIND_GRAD, it, k, u)
+                if w.rank < 0:
+                    self._fill(row[k], nu, w.grad_dtype, key, sigma)
+                else:
+                    self._fill(row[k], valid_len(nu, Su, w.rank), w.grad_dtype, key, sigma,
+                               index0=w.rank * Su)
+        if w.inject and w.inject[0] == it:
+            k = w.inject[1]
+            e = inject_index(w, it, k)
+            if w.rank < 0:
+                self.grads[0][k][e] = float("inf")
+            elif w.rank * w.shard <= e < (w.rank + 1) * w.shard:
+                self.grads[0][k][e - w.rank * w.shard] = float("inf")
+
+    # --------------------------------------------------------------- step
+
+    def launch_step(self, grads_override=None):
+        """Launch one whole step (no synchronization).  Returns the t used."""
+        w = self.w
+        t = self.t + 1
+        st = self.stream
+        if w.stage < 3:
+            g = grads_override if grads_override is not None else self.grads[0]
+            z.zero_step(self.ctx, g, w.lr, w.beta1, w.beta2, w.eps, t, self.scale, st)
+            if self.shards is not None:
+                z.zero_allgather(self.ctx, self.shards, self.params, w.param_dtype, st)
+        else:
+            z.zero3_begin_step(self.ctx)
+            nunits = len(w.units)
+            for u in range(nunits):                      # forward
+                z.zero3_gather_unit(self.ctx, u, self.shards[u], self.unit_full, st)
+            for u in reversed(range(nunits)):            # backward
+                z.zero3_gather_unit(self.ctx, u, self.shards[u], self.unit_full, st)
+                if self.scale > 0:
+                    z.zero3_reduce_unit(self.ctx, u, self.grads[u], self.scale, st)
+                else:
+                    z.zero3_step_unit(self.ctx, u, self.grads[u], w.lr, w.beta1, w.beta2,
+                                      w.eps, t, st)
+            if self.scale > 0:
+                z.zero_step_apply(self.ctx, w.lr, w.beta1, w.beta2, w.eps, t, st)
+        return t
+
+    def finish_step(self):
+        """Read the verdict (synchronizes), advance t and the loss scale."""
+        nonfinite, skipped = z.zero_step_status(self.ctx)
+        self.skips.append(skipped)
+        if not skipped:
+            self.t += 1
+        if self.scale > 0:
+            self.scale, self.good = z.zero_scale_update(self.scale, skipped, self.good,
+                                                         self.w.growth_interval)
+        return nonfinite, skipped
+
+    def step(self, it: int, draw: bool = True):
+        if draw:
+            self.fill_grads(it)
+        self.launch_step()
+        return self.finish_step()
+
+    def close(self):
+        self.ctx.close()

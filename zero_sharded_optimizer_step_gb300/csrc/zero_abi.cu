@@ -1,0 +1,641 @@
+// C ABI of the ZeRO step library: argument checking, geometry of the flat
+// sharded vector, the per-step fp32 scalars, and the kernel launches.  The
+// declarations and their contracts are in include/zero.h.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/zero.h"
+#include "zero_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(ZERO_ECUDA, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+}
+
+bool valid_dtype(int32_t d) { return d == ZERO_F32 || d == ZERO_BF16 || d == ZERO_F16; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned(const void *p, int64_t a) { return ((uintptr_t)p % (uintptr_t)a) == 0; }
+
+int align_of(const void *p)
+{
+    const uintptr_t u = (uintptr_t)p;
+    return (u & 15) == 0 ? 16 : (u & 7) == 0 ? 8 : (u & 3) == 0 ? 4 : (u & 1) == 0 ? 2 : 1;
+}
+
+// A power of two whose reciprocal is a normal binary32 (so multiplying by
+// the reciprocal rounds exactly like dividing).
+bool pow2_with_normal_inverse(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    const uint32_t exp = (u >> 23) & 0xffu, man = u & 0x7fffffu;
+    return (u >> 31) == 0 && man == 0 && exp >= 1 && exp <= 253;
+}
+
+}  // namespace
+
+struct zero_ctx {
+    int64_t numel = 0;
+    int32_t world = 1, stage = 2, gdt = 0, pdt = 0, rank = -1;
+    int64_t S = 0, P = 0;
+    std::vector<int64_t> unit_numel, unit_S, unit_state_off;
+    int64_t state_elems = 0, param_elems = 0;
+
+    float *master = nullptr, *m = nullptr, *v = nullptr, *g = nullptr;
+    void *params = nullptr, *grad_avg = nullptr;
+    uint64_t *flag = nullptr;
+    bool bound = false;
+    int device = -1, sms = 0;
+
+    uint64_t step_id = 0;
+    bool step_scaled = false;
+    cudaStream_t last_stream = nullptr;
+};
+
+namespace zgb {
+
+int resident_blocks_per_sm(const void *kernel, int threads)
+{
+    struct Entry { const void *k; int dev, threads, blocks; };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &e : cache)
+        if (e.k == kernel && e.dev == dev && e.threads == threads) return e.blocks;
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, 0) != cudaSuccess || b < 1) {
+        cudaGetLastError();
+        b = 1;
+    }
+    cache.push_back({kernel, dev, threads, b});
+    return b;
+}
+
+}  // namespace zgb
+
+namespace {
+
+using zgb::StepArgs;
+
+int check_ready(zero_ctx *c)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (!c->bound) return fail(ZERO_ESTATE, "no buffers bound (call zero_bind first)");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != c->device)
+        return fail(ZERO_ESTATE, "current device %d is not the device %d the buffers were bound on",
+                    dev, c->device);
+    return ZERO_OK;
+}
+
+int check_ptr_array(const void *const *p, int32_t n, int32_t world, int es, bool need,
+                    const char *what)
+{
+    if (n != world) return fail(ZERO_EINVAL, "%s: %d pointers given, world is %d", what, n, world);
+    if (!p) return fail(ZERO_EINVAL, "%s: null pointer array", what);
+    for (int32_t k = 0; k < n; ++k) {
+        if (!p[k]) {
+            if (need) return fail(ZERO_EINVAL, "%s[%d] is null", what, k);
+            continue;
+        }
+        if (!aligned(p[k], es))
+            return fail(ZERO_EALIGN, "%s[%d] is not aligned to its %d-byte elements", what, k, es);
+    }
+    return ZERO_OK;
+}
+
+zgb::AdamScalars adam_scalars(double lr, double b1, double b2, double eps, int64_t t)
+{
+    zgb::AdamScalars s;
+    s.lr = (float)lr;
+    s.b1 = (float)b1;
+    s.b2 = (float)b2;
+    s.c1 = (float)(1.0 - b1);
+    s.c2 = (float)(1.0 - b2);
+    s.bc1 = (float)(1.0 - std::pow(b1, (double)t));
+    s.bc2 = (float)(1.0 - std::pow(b2, (double)t));
+    s.eps = (float)eps;
+    return s;
+}
+
+zgb::AverageScalars average_scalars(int32_t world, float loss_scale)
+{
+    zgb::AverageScalars s{};
+    s.world_f = (float)world;
+    s.world_pow2 = (world & (world - 1)) == 0;
+    s.inv_world = 1.0f / (float)world;
+    s.scaled = loss_scale > 0.0f;
+    s.scale = s.scaled ? loss_scale : 1.0f;
+    s.scale_pow2 = s.scaled && pow2_with_normal_inverse(loss_scale);
+    s.inv_scale = 1.0f / s.scale;
+    return s;
+}
+
+// One contiguous range of the state: [state_off, state_off + n), with the
+// first n_valid elements backed by real grads.
+struct Range {
+    int64_t state_off = 0, n = 0, n_valid = 0;
+    char *params = nullptr;     // low-precision destination of element 0
+    char *grad_avg = nullptr;   // stage-1 output of element 0, or null
+};
+
+// The whole-vector range of stages 1 and 2.
+Range vector_range(const zero_ctx *c)
+{
+    Range r;
+    const int es_p = zgb::elem_size(c->pdt), es_g = zgb::elem_size(c->gdt);
+    if (c->rank < 0) {
+        r.n = c->P;
+        r.n_valid = c->numel;
+        r.params = static_cast<char *>(c->params);
+        r.grad_avg = static_cast<char *>(c->grad_avg);
+    } else {
+        const int64_t lo = (int64_t)c->rank * c->S;
+        r.n = c->S;
+        r.n_valid = std::max<int64_t>(0, std::min<int64_t>(c->S, c->numel - lo));
+        r.params = static_cast<char *>(c->params) + lo * es_p;
+        r.grad_avg = c->grad_avg ? static_cast<char *>(c->grad_avg) + lo * es_g : nullptr;
+    }
+    return r;
+}
+
+// Unit u of stage 3.
+Range unit_range(const zero_ctx *c, int32_t u)
+{
+    Range r;
+    const int es_p = zgb::elem_size(c->pdt);
+    const int64_t Su = c->unit_S[u];
+    r.state_off = c->unit_state_off[u];
+    if (c->rank < 0) {
+        r.n = Su * c->world;
+        r.n_valid = c->unit_numel[u];
+    } else {
+        r.n = Su;
+        r.n_valid = std::max<int64_t>(0, std::min<int64_t>(Su, c->unit_numel[u] - (int64_t)c->rank * Su));
+    }
+    r.params = static_cast<char *>(c->params) + r.state_off * es_p;
+    return r;
+}
+
+StepArgs make_args(const zero_ctx *c, const Range &r, const void *const *grads)
+{
+    StepArgs a;
+    memset(&a, 0, sizeof a);
+    a.world = c->world;
+    a.n = r.n;
+    a.n_valid = r.n_valid;
+    a.master = c->master + r.state_off;
+    a.m = c->m + r.state_off;
+    a.v = c->v + r.state_off;
+    a.g = c->g ? c->g + r.state_off : nullptr;
+    a.params = r.params;
+    a.grad_avg = r.grad_avg;
+    a.param_align = align_of(r.params);
+    a.avg_align = r.grad_avg ? align_of(r.grad_avg) : 16;
+    a.flag = reinterpret_cast<unsigned long long *>(c->flag);
+    bool ok = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16) &&
+              (!a.g || aligned(a.g, 16));
+    if (grads) {
+        for (int32_t k = 0; k < c->world; ++k) {
+            a.grads[k] = grads[k];
+            ok = ok && aligned(grads[k], 16);
+        }
+    }
+    a.vec_ok = ok ? 1 : 0;
+    return a;
+}
+
+int finish_launch(zero_ctx *c, cudaError_t e, const char *what, cudaStream_t s)
+{
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    c->last_stream = s;
+    return ZERO_OK;
+}
+
+int do_reduce(zero_ctx *c, const Range &r, const void *const *grads, float loss_scale,
+              cudaStream_t s)
+{
+    if (r.n == 0) return ZERO_OK;
+    StepArgs a = make_args(c, r, grads);
+    a.av = average_scalars(c->world, loss_scale);
+    a.step_id = c->step_id;
+    return finish_launch(c, zgb::launch_reduce(c->gdt, a, c->sms, s), "reduce kernel", s);
+}
+
+int do_apply(zero_ctx *c, const Range &r, double lr, double b1, double b2, double eps,
+             int64_t t, cudaStream_t s)
+{
+    if (r.n == 0) return ZERO_OK;
+    StepArgs a = make_args(c, r, nullptr);
+    a.ad = adam_scalars(lr, b1, b2, eps, t);
+    // an unscaled step never skips: use an id the flag cannot hold
+    a.step_id = c->step_scaled ? c->step_id : ~0ull;
+    return finish_launch(c, zgb::launch_apply(c->pdt, a, c->sms, s), "apply kernel", s);
+}
+
+int do_fused(zero_ctx *c, const Range &r, const void *const *grads, double lr, double b1,
+             double b2, double eps, int64_t t, cudaStream_t s)
+{
+    if (r.n == 0) return ZERO_OK;
+    StepArgs a = make_args(c, r, grads);
+    a.av = average_scalars(c->world, 0.0f);
+    a.ad = adam_scalars(lr, b1, b2, eps, t);
+    a.step_id = c->step_id;
+    return finish_launch(c, zgb::launch_fused_step(c->gdt, c->pdt, a, c->sms, s), "step kernel", s);
+}
+
+int check_hyper(int64_t t)
+{
+    if (t < 1) return fail(ZERO_EINVAL, "step count t must be >= 1 (got %lld)", (long long)t);
+    return ZERO_OK;
+}
+
+// The apply pass covers every element of the bound state: the whole vector
+// range for stages 1 and 2, all units (laid end to end) for stage 3.
+Range apply_range(const zero_ctx *c)
+{
+    if (c->stage < 3) return vector_range(c);
+    Range r;
+    r.n = c->state_elems;
+    r.params = static_cast<char *>(c->params);
+    return r;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t zero_shard_size(int64_t numel, int32_t world)
+{
+    if (world < 1 || numel < 0) return -1;
+    return ceil_div(numel, world);
+}
+
+double zero_model_state_bytes(int64_t numel, int32_t world, int32_t stage)
+{
+    if (numel < 0 || world < 1) return -1.0;
+    const double p = (double)numel, n = (double)world;
+    switch (stage) {
+    case 0: return 16.0 * p;
+    case 1: return 4.0 * p + 12.0 * p / n;
+    case 2: return 2.0 * p + 14.0 * p / n;
+    case 3: return 16.0 * p / n;
+    }
+    return -1.0;
+}
+
+float zero_scale_update(float scale, int32_t skipped, int64_t *good_steps, int64_t growth_interval)
+{
+    if (!good_steps) return scale;
+    if (skipped) {
+        *good_steps = 0;
+        return scale * 0.5f;
+    }
+    if (++*good_steps >= growth_interval && growth_interval > 0) {
+        *good_steps = 0;
+        return scale * 2.0f;
+    }
+    return scale;
+}
+
+const char *zero_strerror(int code)
+{
+    switch (code) {
+    case ZERO_OK: return "ZERO_OK";
+    case ZERO_SKIPPED: return "ZERO_SKIPPED";
+    case ZERO_EINVAL: return "ZERO_EINVAL: invalid argument";
+    case ZERO_ECUDA: return "ZERO_ECUDA: CUDA runtime error";
+    case ZERO_EALIGN: return "ZERO_EALIGN: misaligned device pointer";
+    case ZERO_ESTATE: return "ZERO_ESTATE: call not valid in this state";
+    }
+    return "unknown zero code";
+}
+
+const char *zero_last_error(void) { return g_last_error.c_str(); }
+
+int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage, int32_t grad_dtype,
+              int32_t param_dtype, int32_t rank, const int64_t *unit_numels, int32_t n_units)
+{
+    if (!out) return fail(ZERO_EINVAL, "out is null");
+    *out = nullptr;
+    if (world < 1 || world > ZERO_MAX_RANKS)
+        return fail(ZERO_EINVAL, "world must be in [1, %d] (got %d)", ZERO_MAX_RANKS, world);
+    if (stage < 1 || stage > 3) return fail(ZERO_EINVAL, "stage must be 1, 2 or 3 (got %d)", stage);
+    if (!valid_dtype(grad_dtype) || !valid_dtype(param_dtype))
+        return fail(ZERO_EINVAL, "unknown dtype code (grad %d, param %d)", grad_dtype, param_dtype);
+    if (rank < -1 || rank >= world)
+        return fail(ZERO_EINVAL, "rank must be -1 or in [0, %d) (got %d)", world, rank);
+    const int64_t kLimit = (int64_t)1 << 56;
+    zero_ctx *c = new zero_ctx;
+    c->world = world;
+    c->stage = stage;
+    c->gdt = grad_dtype;
+    c->pdt = param_dtype;
+    c->rank = rank;
+    if (stage < 3) {
+        if (unit_numels || n_units) {
+            delete c;
+            return fail(ZERO_EINVAL, "units are only for stage 3");
+        }
+        if (numel < 0 || numel > kLimit) {
+            delete c;
+            return fail(ZERO_EINVAL, "numel out of range (%lld)", (long long)numel);
+        }
+        c->numel = numel;
+        c->S = ceil_div(numel, world);
+        c->P = c->S * world;
+        c->state_elems = rank < 0 ? c->P : c->S;
+        c->param_elems = c->P;
+    } else {
+        if (!unit_numels || n_units < 1) {
+            delete c;
+            return fail(ZERO_EINVAL, "stage 3 needs unit_numels and n_units >= 1");
+        }
+        int64_t sum = 0, off = 0;
+        for (int32_t u = 0; u < n_units; ++u) {
+            const int64_t nu = unit_numels[u];
+            if (nu < 0 || nu > kLimit) {
+                delete c;
+                return fail(ZERO_EINVAL, "unit %d numel out of range (%lld)", u, (long long)nu);
+            }
+            const int64_t su = ceil_div(nu, world);
+            c->unit_numel.push_back(nu);
+            c->unit_S.push_back(su);
+            c->unit_state_off.push_back(off);
+            off += rank < 0 ? su * world : su;
+            sum += nu;
+            if (sum > kLimit || off > kLimit) {
+                delete c;
+                return fail(ZERO_EINVAL, "units too large");
+            }
+        }
+        if (numel != sum) {
+            delete c;
+            return fail(ZERO_EINVAL, "numel (%lld) must equal the sum of unit_numels (%lld)",
+                        (long long)numel, (long long)sum);
+        }
+        c->numel = sum;
+        c->S = -1;
+        c->P = -1;
+        c->state_elems = off;
+        c->param_elems = off;
+    }
+    *out = c;
+    return ZERO_OK;
+}
+
+int zero_destroy(zero_ctx *ctx)
+{
+    delete ctx;
+    return ZERO_OK;
+}
+
+int64_t zero_ctx_shard_size(const zero_ctx *c, int32_t unit)
+{
+    if (!c) return -1;
+    if (unit < 0) return c->stage < 3 ? c->S : -1;
+    if (c->stage < 3 || unit >= (int32_t)c->unit_S.size()) return -1;
+    return c->unit_S[unit];
+}
+
+int64_t zero_ctx_state_elems(const zero_ctx *c) { return c ? c->state_elems : -1; }
+
+int64_t zero_ctx_param_elems(const zero_ctx *c) { return c ? c->param_elems : -1; }
+
+int64_t zero_ctx_unit_state_offset(const zero_ctx *c, int32_t unit)
+{
+    if (!c) return -1;
+    if (c->stage < 3) return unit == -1 ? 0 : -1;
+    if (unit < 0 || unit >= (int32_t)c->unit_S.size()) return -1;
+    return c->unit_state_off[unit];
+}
+
+int64_t zero_ctx_unit_param_offset(const zero_ctx *c, int32_t unit)
+{
+    return zero_ctx_unit_state_offset(c, unit);
+}
+
+int64_t zero_state_bytes(const zero_ctx *c) { return c ? 12 * c->state_elems : -1; }
+
+int zero_bind(zero_ctx *c, float *master, float *m, float *v, void *params, float *g_scratch,
+              uint64_t *flag)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (c->state_elems > 0 && (!master || !m || !v || !params))
+        return fail(ZERO_EINVAL, "master, m, v and params must not be null");
+    if (!flag) return fail(ZERO_EINVAL, "flag must not be null");
+    const int es_p = zgb::elem_size(c->pdt);
+    if (!aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) || !aligned(g_scratch, 4))
+        return fail(ZERO_EALIGN, "master/m/v/g_scratch must be 4-byte aligned");
+    if (!aligned(params, es_p)) return fail(ZERO_EALIGN, "params not aligned to %d bytes", es_p);
+    if (!aligned(flag, 8)) return fail(ZERO_EALIGN, "flag must be 8-byte aligned");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    c->master = master;
+    c->m = m;
+    c->v = v;
+    c->params = params;
+    c->g = g_scratch;
+    c->flag = flag;
+    c->device = dev;
+    c->sms = sms > 0 ? sms : 1;
+    c->bound = true;
+    return ZERO_OK;
+}
+
+int zero_bind_allreduce_out(zero_ctx *c, void *grad_avg)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (c->stage != 1) return fail(ZERO_EINVAL, "the all-reduce output is a stage-1 feature");
+    if (!aligned(grad_avg, zgb::elem_size(c->gdt)))
+        return fail(ZERO_EALIGN, "grad_avg not aligned to its elements");
+    c->grad_avg = grad_avg;
+    return ZERO_OK;
+}
+
+int zero_step_reduce(zero_ctx *c, const void *const *grads, int32_t n_grads, float loss_scale,
+                     void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if (c->stage == 3) return fail(ZERO_EINVAL, "stage 3 reduces per unit (zero3_reduce_unit)");
+    if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
+    const Range r = vector_range(c);
+    rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
+    if (rc) return rc;
+    c->step_id += 1;
+    c->step_scaled = loss_scale > 0.0f;
+    return do_reduce(c, r, grads, loss_scale, (cudaStream_t)stream);
+}
+
+int zero_step_apply(zero_ctx *c, double lr, double b1, double b2, double eps, int64_t t,
+                    void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if ((rc = check_hyper(t))) return rc;
+    if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
+    if (c->step_id == 0) return fail(ZERO_ESTATE, "no reduce pass ran before apply");
+    return do_apply(c, apply_range(c), lr, b1, b2, eps, t, (cudaStream_t)stream);
+}
+
+int zero_step(zero_ctx *c, const void *const *grads, int32_t n_grads, double lr, double b1,
+              double b2, double eps, int64_t t, float loss_scale, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if ((rc = check_hyper(t))) return rc;
+    if (c->stage == 3) return fail(ZERO_EINVAL, "stage 3 steps per unit (zero3_step_unit)");
+    const Range r = vector_range(c);
+    rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (loss_scale > 0.0f) {
+        if (!c->g) return fail(ZERO_ESTATE, "a loss-scaled step needs g_scratch (zero_bind)");
+        c->step_id += 1;
+        c->step_scaled = true;
+        rc = do_reduce(c, r, grads, loss_scale, s);
+        if (rc) return rc;
+        return do_apply(c, r, lr, b1, b2, eps, t, s);
+    }
+    c->step_id += 1;
+    c->step_scaled = false;
+    return do_fused(c, r, grads, lr, b1, b2, eps, t, s);
+}
+
+int zero_step_status(zero_ctx *c, int32_t *nonfinite, int32_t *skipped)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (!c->bound) return fail(ZERO_ESTATE, "no buffers bound");
+    unsigned long long h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, c->flag, sizeof h, cudaMemcpyDeviceToHost, c->last_stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->last_stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the flag word");
+    const bool bad = c->step_id > 0 && h == c->step_id;
+    const bool skip = bad && c->step_scaled;
+    if (nonfinite) *nonfinite = bad ? 1 : 0;
+    if (skipped) *skipped = skip ? 1 : 0;
+    return skip ? ZERO_SKIPPED : ZERO_OK;
+}
+
+uint64_t zero_step_id(const zero_ctx *c) { return c ? c->step_id : 0; }
+
+static int gather(zero_ctx *c, const void *const *shards, int32_t n, void *full, int32_t dtype,
+                  int64_t S, cudaStream_t s)
+{
+    if (!valid_dtype(dtype)) return fail(ZERO_EINVAL, "unknown dtype %d", dtype);
+    const int es = zgb::elem_size(dtype);
+    int rc = check_ptr_array(shards, n, c->world, es, false, "shards");
+    if (rc) return rc;
+    if (!full && S > 0) return fail(ZERO_EINVAL, "full is null");
+    if (!aligned(full, es)) return fail(ZERO_EALIGN, "full not aligned to %d bytes", es);
+    if (S == 0) return ZERO_OK;
+    zgb::GatherArgs a;
+    memset(&a, 0, sizeof a);
+    for (int32_t k = 0; k < n; ++k) a.src[k] = shards[k];
+    a.dst = static_cast<char *>(full);
+    a.shard_bytes = S * es;
+    a.n = n;
+    a.es = es;
+    return finish_launch(c, zgb::launch_gather(a, c->sms, s), "gather kernel", s);
+}
+
+int zero_allgather(zero_ctx *c, const void *const *shards, int32_t n_shards, void *full,
+                   int32_t dtype, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if (c->stage == 3) return fail(ZERO_EINVAL, "stage 3 gathers per unit (zero3_gather_unit)");
+    return gather(c, shards, n_shards, full, dtype, c->S, (cudaStream_t)stream);
+}
+
+int zero3_begin_step(zero_ctx *c)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (c->stage != 3) return fail(ZERO_EINVAL, "zero3_begin_step is for stage 3");
+    c->step_id += 1;
+    c->step_scaled = false;
+    return ZERO_OK;
+}
+
+static int check_unit(zero_ctx *c, int32_t unit)
+{
+    if (c->stage != 3) return fail(ZERO_EINVAL, "unit calls are for stage 3");
+    if (unit < 0 || unit >= (int32_t)c->unit_S.size())
+        return fail(ZERO_EINVAL, "unit %d out of range [0, %d)", unit, (int)c->unit_S.size());
+    if (c->step_id == 0) return fail(ZERO_ESTATE, "call zero3_begin_step first");
+    return ZERO_OK;
+}
+
+int zero3_gather_unit(zero_ctx *c, int32_t unit, const void *const *shards, int32_t n_shards,
+                      void *unit_full, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if (c->stage != 3) return fail(ZERO_EINVAL, "unit calls are for stage 3");
+    if (unit < 0 || unit >= (int32_t)c->unit_S.size())
+        return fail(ZERO_EINVAL, "unit %d out of range [0, %d)", unit, (int)c->unit_S.size());
+    return gather(c, shards, n_shards, unit_full, c->pdt, c->unit_S[unit], (cudaStream_t)stream);
+}
+
+int zero3_step_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32_t n_grads,
+                    double lr, double b1, double b2, double eps, int64_t t, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if ((rc = check_unit(c, unit))) return rc;
+    if ((rc = check_hyper(t))) return rc;
+    if (c->step_scaled)
+        return fail(ZERO_ESTATE, "this step is loss-scaled: use zero3_reduce_unit + zero_step_apply");
+    const Range r = unit_range(c, unit);
+    rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
+    if (rc) return rc;
+    return do_fused(c, r, grads, lr, b1, b2, eps, t, (cudaStream_t)stream);
+}
+
+int zero3_reduce_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32_t n_grads,
+                      float loss_scale, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if ((rc = check_unit(c, unit))) return rc;
+    if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
+    const Range r = unit_range(c, unit);
+    rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
+    if (rc) return rc;
+    if (loss_scale > 0.0f) c->step_scaled = true;
+    return do_reduce(c, r, grads, loss_scale, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,113 @@
+// All-gather placement on one GPU: shard k (S elements) is copied to
+// full + k*S ("ZeRO 与 FSDP…", all_gather_into_tensor; for stage 3 the same
+// placement per unit before its forward and backward, section ZeRO-3 与
+// FSDP).  A pure copy, bound by HBM bandwidth: 2 bytes moved per byte placed.
+//
+// One grid row (blockIdx.y) per shard.  Shards start wherever their buffers
+// are; the destination of shard k sits k*S elements into `full`, which for an
+// odd S and 16-bit elements is only 2-byte aligned.  Each row therefore
+// peels the bytes before the source's first 16-byte boundary, copies the
+// body with 16-byte loads, and writes each 16 bytes with the widest store
+// the destination's alignment allows (one 16-byte store, or two of 8, four
+// of 4, eight of 2); the last partial 16 bytes go element by element.
+#include "zero_internal.h"
+
+namespace zgb {
+namespace {
+
+constexpr int kItems = 4;   // 16-byte chunks in flight per thread
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_any(char *p, uint4 v, int align)
+{
+    if (align >= 16) {
+        __stcs(reinterpret_cast<uint4 *>(p), v);
+    } else if (align == 8) {
+        uint2 *q = reinterpret_cast<uint2 *>(p);
+        __stcs(q, make_uint2(v.x, v.y));
+        __stcs(q + 1, make_uint2(v.z, v.w));
+    } else if (align == 4) {
+        unsigned *q = reinterpret_cast<unsigned *>(p);
+        q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+    } else {
+        unsigned short *q = reinterpret_cast<unsigned short *>(p);
+        const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q[2 * i] = (unsigned short)(w[i] & 0xffffu);
+            q[2 * i + 1] = (unsigned short)(w[i] >> 16);
+        }
+    }
+}
+
+__device__ __forceinline__ void copy_elem(char *d, const char *s, int es)
+{
+    if (es == 4) *reinterpret_cast<unsigned *>(d) = *reinterpret_cast<const unsigned *>(s);
+    else *reinterpret_cast<unsigned short *>(d) = *reinterpret_cast<const unsigned short *>(s);
+}
+
+__global__ void __launch_bounds__(kThreads)
+gather_kernel(const __grid_constant__ GatherArgs a)
+{
+    const int k = blockIdx.y;
+    const char *src = static_cast<const char *>(a.src[k]);
+    if (src == nullptr) return;
+    char *dst = a.dst + (int64_t)k * a.shard_bytes;
+    const int64_t nb = a.shard_bytes;
+    int64_t head = (int64_t)((16 - ((uintptr_t)src & 15)) & 15);
+    if (head > nb) head = nb;
+    const int64_t nchunks = (nb - head) >> 4;
+    const int64_t tail = head + (nchunks << 4);
+    const uintptr_t d0 = (uintptr_t)(dst + head);
+    const int align = (d0 & 15) == 0 ? 16 : (d0 & 7) == 0 ? 8 : (d0 & 3) == 0 ? 4 : 2;
+
+    if (blockIdx.x == 0) {
+        for (int64_t b = (int64_t)threadIdx.x * a.es; b < head; b += (int64_t)blockDim.x * a.es)
+            copy_elem(dst + b, src + b, a.es);
+        for (int64_t b = tail + (int64_t)threadIdx.x * a.es; b < nb; b += (int64_t)blockDim.x * a.es)
+            copy_elem(dst + b, src + b, a.es);
+    }
+
+    const char *s = src + head;
+    char *d = dst + head;
+    const int64_t T = (int64_t)gridDim.x * blockDim.x;
+    int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // kItems chunks per thread per round, each T apart so a warp's accesses
+    // stay contiguous
+    for (; c + (kItems - 1) * T < nchunks; c += kItems * T) {
+        uint4 v[kItems];
+#pragma unroll
+        for (int u = 0; u < kItems; ++u) v[u] = ld_stream(s + ((c + u * T) << 4));
+#pragma unroll
+        for (int u = 0; u < kItems; ++u) st_any(d + ((c + u * T) << 4), v[u], align);
+    }
+    for (; c < nchunks; c += T) st_any(d + (c << 4), ld_stream(s + (c << 4)), align);
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s)
+{
+    if (a.n <= 0 || a.shard_bytes <= 0) return cudaSuccess;
+    const int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(gather_kernel), kThreads);
+    const int64_t chunks = (a.shard_bytes + 15) / 16;
+    int64_t want = (chunks + (int64_t)kThreads * kItems - 1) / ((int64_t)kThreads * kItems);
+    // all rows together fill the GPU about once
+    int64_t cap = ((int64_t)sms * per_sm + a.n - 1) / a.n;
+    if (cap < 1) cap = 1;
+    int64_t bx = want < cap ? want : cap;
+    if (bx < 1) bx = 1;
+    dim3 grid((unsigned)bx, (unsigned)a.n);
+    gather_kernel<<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace zgb

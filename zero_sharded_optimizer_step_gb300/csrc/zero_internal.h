@@ -1,0 +1,71 @@
+// Internal interface between the C ABI (zero_abi.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace zgb {
+
+constexpr int kMaxRanks = 256;   // == ZERO_MAX_RANKS
+constexpr int kThreads = 256;    // threads per block of every streaming kernel
+constexpr int kVec = 8;          // elements per thread per iteration
+
+enum DType : int32_t { F32 = 0, BF16 = 1, F16 = 2 };
+
+inline int elem_size(int32_t dt) { return dt == F32 ? 4 : 2; }
+
+// fp32 scalars of one Adam step, each rounded once from a double.
+struct AdamScalars {
+    float lr, b1, b2, c1, c2, bc1, bc2, eps;
+};
+
+// How the rank sum becomes the gradient: g = acc / world, then / loss_scale.
+// Division by a power of two equals multiplication by its reciprocal (both
+// round the same exact value once), so those cases multiply.
+struct AverageScalars {
+    float world_f, inv_world;
+    float scale, inv_scale;
+    int32_t world_pow2, scaled, scale_pow2, pad_;
+};
+
+// Arguments of the per-element step kernels over one contiguous range of
+// `n` elements of the state.  Every pointer is already offset to the
+// range's first element.
+struct StepArgs {
+    const void *grads[kMaxRanks];  // rank k's grads for this range
+    int32_t world;
+    int32_t vec_ok;                // grads, state, scratch 16-byte aligned
+    int32_t param_align;           // byte alignment of `params` (2..16)
+    int32_t avg_align;             // byte alignment of `grad_avg`
+    int64_t n;                     // elements in the range
+    int64_t n_valid;               // leading elements with real grads (rest = pad)
+    float *master, *m, *v;
+    void *params;                  // low-precision output
+    void *grad_avg;                // stage-1 all-reduce output (grad type) or null
+    float *g;                      // two-pass scratch
+    unsigned long long *flag;      // id of the latest step with a non-finite grad
+    unsigned long long step_id;
+    AverageScalars av;
+    AdamScalars ad;
+};
+
+struct GatherArgs {
+    const void *src[kMaxRanks];    // shard k (null = skip)
+    char *dst;                     // shard k lands at dst + k * shard_bytes
+    int64_t shard_bytes;
+    int32_t n;
+    int32_t es;                    // element size in bytes
+};
+
+// Blocks of `threads` threads of `kernel` that fit on one SM of the current
+// device (cached per kernel and device; at least 1).
+int resident_blocks_per_sm(const void *kernel, int threads);
+
+// Launchers: return a cudaError_t.  `sms` is the device's SM count.
+cudaError_t launch_fused_step(int32_t gdt, int32_t pdt, const StepArgs &a, int sms,
+                              cudaStream_t s);
+cudaError_t launch_reduce(int32_t gdt, const StepArgs &a, int sms, cudaStream_t s);
+cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s);
+cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s);
+
+}  // namespace zgb

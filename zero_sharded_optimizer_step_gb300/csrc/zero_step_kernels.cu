@@ -1,0 +1,486 @@
+// Streaming kernels of the ZeRO step on sm_103a.
+//
+//   fused_step  reduce-scatter sum over N rank buffers (rank order) -> average
+//               -> unscale -> Adam on fp32 master/m/v -> cast -> param store,
+//               one read-modify-write pass ("ZeRO 与 FSDP…", 从零实现 ZeRO 的
+//               Adam: reduce_scatter_tensor, g /= world, the Adam update and
+//               all_gather_into_tensor, here fused into a single pass because
+//               every rank's buffers are on this GPU).
+//   reduce      first pass of the loss-scaled step: the same sum, average and
+//               unscale, written to an fp32 scratch, with the overflow flag.
+//   apply       second pass: Adam + cast from the scratch, or nothing at all
+//               when the flag names this step ("PaddlePaddle ZeRO优化",
+//               混合精度才是最佳拍档: the step is skipped on inf/nan).
+//
+// The work is a few flops per byte, so HBM bandwidth bounds every kernel;
+// no tensor cores are involved.  Each thread handles kVec = 8 consecutive
+// elements per iteration with 16-byte loads (one per 16-bit gradient
+// buffer), issues the state loads and a chunk of 8 gradient loads before
+// consuming any, and walks a grid sized to fill every SM (grid-stride
+// loop, 64-bit indices).  Elements past the last full vector, padding
+// positions and buffers that are not 16-byte aligned take a per-element path
+// that performs the same operations in the same order.
+//
+// Numerics follow the header's definition operation by operation; explicit
+// __fadd_rn/__fmul_rn/__fdiv_rn/__fsqrt_rn keep the compiler from fusing or
+// reordering anything, and the library is built without fast-math or FTZ.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "zero_internal.h"
+
+namespace zgb {
+namespace {
+
+// ------------------------------------------------------------ memory ops
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_state(const float *p)
+{
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+
+__device__ __forceinline__ void st_state(float *p, float4 v)
+{
+    __stcs(reinterpret_cast<float4 *>(p), v);
+}
+
+// Store 16 bytes at an address aligned to `align` (16, 8, 4 or 2) bytes.
+__device__ __forceinline__ void st16(void *p, uint4 v, int align)
+{
+    if (align >= 16) {
+        __stcs(reinterpret_cast<uint4 *>(p), v);
+    } else if (align == 8) {
+        uint2 *q = reinterpret_cast<uint2 *>(p);
+        __stcs(q, make_uint2(v.x, v.y));
+        __stcs(q + 1, make_uint2(v.z, v.w));
+    } else if (align == 4) {
+        unsigned *q = reinterpret_cast<unsigned *>(p);
+        q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+    } else {
+        unsigned short *q = reinterpret_cast<unsigned short *>(p);
+        const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q[2 * i] = (unsigned short)(w[i] & 0xffffu);
+            q[2 * i + 1] = (unsigned short)(w[i] >> 16);
+        }
+    }
+}
+
+// ------------------------------------------------------- element types
+
+template <int DT> struct Ty;
+
+template <> struct Ty<F32> {
+    static constexpr int kLoads = 2;   // 16-byte loads per 8 elements
+    __device__ static float load1(const void *p, int64_t i) { return static_cast<const float *>(p)[i]; }
+    __device__ static void store1(void *p, int64_t i, float x) { static_cast<float *>(p)[i] = x; }
+    __device__ static void widen(const uint4 *r, float (&o)[kVec])
+    {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            o[4 * h + 0] = __uint_as_float(r[h].x);
+            o[4 * h + 1] = __uint_as_float(r[h].y);
+            o[4 * h + 2] = __uint_as_float(r[h].z);
+            o[4 * h + 3] = __uint_as_float(r[h].w);
+        }
+    }
+    __device__ static void narrow(const float (&x)[kVec], uint4 *r)
+    {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            r[h] = make_uint4(__float_as_uint(x[4 * h]), __float_as_uint(x[4 * h + 1]),
+                              __float_as_uint(x[4 * h + 2]), __float_as_uint(x[4 * h + 3]));
+    }
+};
+
+template <> struct Ty<BF16> {
+    static constexpr int kLoads = 1;
+    __device__ static float load1(const void *p, int64_t i)
+    {
+        return __uint_as_float((unsigned)static_cast<const unsigned short *>(p)[i] << 16);
+    }
+    __device__ static void store1(void *p, int64_t i, float x)
+    {
+        static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
+    }
+    // bf16 -> fp32 is exact: the 16 bits become the top half of the word.
+    __device__ static void widen(const uint4 *r, float (&o)[kVec])
+    {
+        const unsigned w[4] = {r[0].x, r[0].y, r[0].z, r[0].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o[2 * i] = __uint_as_float(w[i] << 16);
+            o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ static void narrow(const float (&x)[kVec], uint4 *r)
+    {
+        unsigned w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+            w[i] = *reinterpret_cast<unsigned *>(&h);
+        }
+        r[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+template <> struct Ty<F16> {
+    static constexpr int kLoads = 1;
+    __device__ static float load1(const void *p, int64_t i)
+    {
+        return __half2float(static_cast<const __half *>(p)[i]);
+    }
+    __device__ static void store1(void *p, int64_t i, float x)
+    {
+        static_cast<__half *>(p)[i] = __float2half_rn(x);
+    }
+    __device__ static void widen(const uint4 *r, float (&o)[kVec])
+    {
+        const unsigned w[4] = {r[0].x, r[0].y, r[0].z, r[0].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            float2 f = __half22float2(h);
+            o[2 * i] = f.x;
+            o[2 * i + 1] = f.y;
+        }
+    }
+    __device__ static void narrow(const float (&x)[kVec], uint4 *r)
+    {
+        unsigned w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+            w[i] = *reinterpret_cast<unsigned *>(&h);
+        }
+        r[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+// ------------------------------------------------------------ arithmetic
+
+__device__ __forceinline__ bool nonfinite(float x)
+{
+    return (__float_as_uint(x) & 0x7f800000u) == 0x7f800000u;
+}
+
+// acc -> g: divide by N, then by the loss scale.
+__device__ __forceinline__ float average(float acc, const AverageScalars &s)
+{
+    float g = s.world_pow2 ? __fmul_rn(acc, s.inv_world) : __fdiv_rn(acc, s.world_f);
+    if (s.scaled) g = s.scale_pow2 ? __fmul_rn(g, s.inv_scale) : __fdiv_rn(g, s.scale);
+    return g;
+}
+
+// One element of Adam with bias correction, eps outside the root.
+__device__ __forceinline__ void adam1(float g, float &x, float &m, float &v, const AdamScalars &s)
+{
+    const float mj = __fadd_rn(__fmul_rn(m, s.b1), __fmul_rn(s.c1, g));
+    const float vj = __fadd_rn(__fmul_rn(v, s.b2), __fmul_rn(s.c2, __fmul_rn(g, g)));
+    const float mh = __fdiv_rn(mj, s.bc1);
+    const float vh = __fdiv_rn(vj, s.bc2);
+    const float den = __fadd_rn(__fsqrt_rn(vh), s.eps);
+    const float upd = __fdiv_rn(__fmul_rn(s.lr, mh), den);
+    m = mj;
+    v = vj;
+    x = __fsub_rn(x, upd);
+}
+
+// Rank-order sum of 8 consecutive elements at vector index k of every rank
+// buffer, chunk by chunk: a chunk's 16-byte loads are all issued before any
+// of them is added, and within the chunk the adds go in rank order.
+template <int GT>
+__device__ __forceinline__ void rank_sum8(const StepArgs &a, int64_t i, float (&acc)[kVec])
+{
+    constexpr int L = Ty<GT>::kLoads;
+    constexpr int kChunk = 8;
+    const int64_t byte_off = i * (GT == F32 ? 4 : 2);
+    for (int c = 0; c < a.world; c += kChunk) {
+        uint4 raw[kChunk][L];
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+            if (c + u < a.world) {
+                const char *p = static_cast<const char *>(a.grads[c + u]) + byte_off;
+#pragma unroll
+                for (int l = 0; l < L; ++l) raw[u][l] = ld_stream(p + 16 * l);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+            if (c + u < a.world) {
+                float f[kVec];
+                Ty<GT>::widen(raw[u], f);
+                if (c + u == 0) {
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) acc[e] = f[e];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
+                }
+            }
+        }
+    }
+}
+
+template <int GT>
+__device__ __forceinline__ float rank_sum1(const StepArgs &a, int64_t i)
+{
+    if (i >= a.n_valid) return 0.0f;
+    float acc = Ty<GT>::load1(a.grads[0], i);
+    for (int r = 1; r < a.world; ++r) acc = __fadd_rn(acc, Ty<GT>::load1(a.grads[r], i));
+    return acc;
+}
+
+template <int PT>
+__device__ __forceinline__ void store_params8(void *base, int64_t i, const float (&x)[kVec],
+                                              int align)
+{
+    constexpr int L = Ty<PT>::kLoads;
+    uint4 r[L];
+    Ty<PT>::narrow(x, r);
+    char *p = static_cast<char *>(base) + i * (PT == F32 ? 4 : 2);
+#pragma unroll
+    for (int l = 0; l < L; ++l) st16(p + 16 * l, r[l], align);
+}
+
+__device__ __forceinline__ void load_state8(const float *p, int64_t i, float (&o)[kVec])
+{
+    const float4 a = ld_state(p + i), b = ld_state(p + i + 4);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
+__device__ __forceinline__ void store_state8(float *p, int64_t i, const float (&o)[kVec])
+{
+    st_state(p + i, make_float4(o[0], o[1], o[2], o[3]));
+    st_state(p + i + 4, make_float4(o[4], o[5], o[6], o[7]));
+}
+
+// One block-wide OR of the per-thread overflow bits, then at most one atomic
+// per block.  Every thread of the block reaches this point.
+__device__ __forceinline__ void publish_flag(const StepArgs &a, bool bad)
+{
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicMax(a.flag, a.step_id);
+}
+
+// ---------------------------------------------------------------- kernels
+
+template <int GT, int PT, bool AVG>
+__global__ void __launch_bounds__(kThreads)
+fused_step_kernel(const __grid_constant__ StepArgs a)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
+    bool bad = false;
+    for (int64_t k = tid; k < nvec; k += stride) {
+        const int64_t i = k * kVec;
+        float x[kVec], m[kVec], v[kVec], acc[kVec];
+        load_state8(a.master, i, x);
+        load_state8(a.m, i, m);
+        load_state8(a.v, i, v);
+        rank_sum8<GT>(a, i, acc);
+        float g[kVec];
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            if (AVG) {
+                // the all-reduce mean itself, before unscaling
+                acc[e] = a.av.world_pow2 ? __fmul_rn(acc[e], a.av.inv_world)
+                                         : __fdiv_rn(acc[e], a.av.world_f);
+                g[e] = !a.av.scaled ? acc[e]
+                       : (a.av.scale_pow2 ? __fmul_rn(acc[e], a.av.inv_scale)
+                                          : __fdiv_rn(acc[e], a.av.scale));
+            } else {
+                g[e] = average(acc[e], a.av);
+            }
+            bad |= nonfinite(g[e]);
+            adam1(g[e], x[e], m[e], v[e], a.ad);
+        }
+        store_state8(a.master, i, x);
+        store_state8(a.m, i, m);
+        store_state8(a.v, i, v);
+        store_params8<PT>(a.params, i, x, a.param_align);
+        if (AVG) store_params8<GT>(a.grad_avg, i, acc, a.avg_align);
+    }
+    // per-element path: ragged tail, padding, unaligned buffers
+    for (int64_t i = nvec * kVec + tid; i < a.n; i += stride) {
+        float acc = rank_sum1<GT>(a, i);
+        float mean = a.av.world_pow2 ? __fmul_rn(acc, a.av.inv_world) : __fdiv_rn(acc, a.av.world_f);
+        float g = !a.av.scaled ? mean
+                  : (a.av.scale_pow2 ? __fmul_rn(mean, a.av.inv_scale) : __fdiv_rn(mean, a.av.scale));
+        bad |= nonfinite(g);
+        float x = a.master[i], m = a.m[i], v = a.v[i];
+        adam1(g, x, m, v, a.ad);
+        a.master[i] = x;
+        a.m[i] = m;
+        a.v[i] = v;
+        Ty<PT>::store1(a.params, i, x);
+        if (AVG) Ty<GT>::store1(a.grad_avg, i, mean);
+    }
+    publish_flag(a, bad);
+}
+
+template <int GT, bool AVG>
+__global__ void __launch_bounds__(kThreads)
+reduce_kernel(const __grid_constant__ StepArgs a)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
+    bool bad = false;
+    for (int64_t k = tid; k < nvec; k += stride) {
+        const int64_t i = k * kVec;
+        float acc[kVec], g[kVec];
+        rank_sum8<GT>(a, i, acc);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+            acc[e] = a.av.world_pow2 ? __fmul_rn(acc[e], a.av.inv_world)
+                                     : __fdiv_rn(acc[e], a.av.world_f);
+            g[e] = !a.av.scaled ? acc[e]
+                   : (a.av.scale_pow2 ? __fmul_rn(acc[e], a.av.inv_scale)
+                                      : __fdiv_rn(acc[e], a.av.scale));
+            bad |= nonfinite(g[e]);
+        }
+        store_state8(a.g, i, g);
+        if (AVG) store_params8<GT>(a.grad_avg, i, acc, a.avg_align);
+    }
+    for (int64_t i = nvec * kVec + tid; i < a.n; i += stride) {
+        float acc = rank_sum1<GT>(a, i);
+        float mean = a.av.world_pow2 ? __fmul_rn(acc, a.av.inv_world) : __fdiv_rn(acc, a.av.world_f);
+        float g = !a.av.scaled ? mean
+                  : (a.av.scale_pow2 ? __fmul_rn(mean, a.av.inv_scale) : __fdiv_rn(mean, a.av.scale));
+        bad |= nonfinite(g);
+        a.g[i] = g;
+        if (AVG) Ty<GT>::store1(a.grad_avg, i, mean);
+    }
+    publish_flag(a, bad);
+}
+
+template <int PT>
+__global__ void __launch_bounds__(kThreads)
+apply_kernel(const __grid_constant__ StepArgs a)
+{
+    // The verdict of the whole step is known: a skipped step writes nothing.
+    if (*reinterpret_cast<volatile unsigned long long *>(a.flag) == a.step_id) return;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nvec = a.vec_ok ? a.n / kVec : 0;
+    for (int64_t k = tid; k < nvec; k += stride) {
+        const int64_t i = k * kVec;
+        float x[kVec], m[kVec], v[kVec], g[kVec];
+        load_state8(a.g, i, g);
+        load_state8(a.master, i, x);
+        load_state8(a.m, i, m);
+        load_state8(a.v, i, v);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) adam1(g[e], x[e], m[e], v[e], a.ad);
+        store_state8(a.master, i, x);
+        store_state8(a.m, i, m);
+        store_state8(a.v, i, v);
+        store_params8<PT>(a.params, i, x, a.param_align);
+    }
+    for (int64_t i = nvec * kVec + tid; i < a.n; i += stride) {
+        float x = a.master[i], m = a.m[i], v = a.v[i];
+        adam1(a.g[i], x, m, v, a.ad);
+        a.master[i] = x;
+        a.m[i] = m;
+        a.v[i] = v;
+        Ty<PT>::store1(a.params, i, x);
+    }
+}
+
+// ------------------------------------------------------------- launching
+
+template <typename K>
+cudaError_t launch(K kernel, const StepArgs &a, int64_t work_items, int sms, cudaStream_t s)
+{
+    const int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(kernel), kThreads);
+    int64_t want = (work_items + kThreads - 1) / kThreads;
+    int64_t cap = (int64_t)sms * per_sm;
+    int64_t blocks = want < cap ? want : cap;
+    if (blocks < 1) blocks = 1;
+    kernel<<<(unsigned)blocks, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+int64_t items(const StepArgs &a, int64_t nvec_src)
+{
+    // threads needed: one per vector of the aligned part, plus the tail
+    const int64_t nvec = a.vec_ok ? nvec_src / kVec : 0;
+    const int64_t tail = a.n - nvec * kVec;
+    return nvec > tail ? nvec : tail;
+}
+
+template <int GT, int PT>
+cudaError_t fused_pt(const StepArgs &a, int sms, cudaStream_t s)
+{
+    const int64_t w = items(a, a.n_valid);
+    return a.grad_avg ? launch(fused_step_kernel<GT, PT, true>, a, w, sms, s)
+                      : launch(fused_step_kernel<GT, PT, false>, a, w, sms, s);
+}
+
+template <int GT>
+cudaError_t fused_gt(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s)
+{
+    switch (pdt) {
+    case F32: return fused_pt<GT, F32>(a, sms, s);
+    case BF16: return fused_pt<GT, BF16>(a, sms, s);
+    case F16: return fused_pt<GT, F16>(a, sms, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int GT>
+cudaError_t reduce_gt(const StepArgs &a, int sms, cudaStream_t s)
+{
+    const int64_t w = items(a, a.n_valid);
+    return a.grad_avg ? launch(reduce_kernel<GT, true>, a, w, sms, s)
+                      : launch(reduce_kernel<GT, false>, a, w, sms, s);
+}
+
+}  // namespace
+
+cudaError_t launch_fused_step(int32_t gdt, int32_t pdt, const StepArgs &a, int sms,
+                              cudaStream_t s)
+{
+    switch (gdt) {
+    case F32: return fused_gt<F32>(pdt, a, sms, s);
+    case BF16: return fused_gt<BF16>(pdt, a, sms, s);
+    case F16: return fused_gt<F16>(pdt, a, sms, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_reduce(int32_t gdt, const StepArgs &a, int sms, cudaStream_t s)
+{
+    switch (gdt) {
+    case F32: return reduce_gt<F32>(a, sms, s);
+    case BF16: return reduce_gt<BF16>(a, sms, s);
+    case F16: return reduce_gt<F16>(a, sms, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s)
+{
+    const int64_t w = items(a, a.n);
+    switch (pdt) {
+    case F32: return launch(apply_kernel<F32>, a, w, sms, s);
+    case BF16: return launch(apply_kernel<BF16>, a, w, sms, s);
+    case F16: return launch(apply_kernel<F16>, a, w, sms, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace zgb
