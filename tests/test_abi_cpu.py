@@ -14,8 +14,8 @@ HEADER = os.path.join(ROOT, "include", "zero.h")
 
 @pytest.fixture(scope="module")
 def z():
-    from zero_sharded_optimizer_step_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._library_builder().build()
     import zero_sharded_optimizer_step_gb300 as z
     return z
 
