@@ -53,7 +53,7 @@ def src_hash(path):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="gpt2_xl",
                     choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny"])
@@ -95,7 +95,7 @@ class Clocks:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
                                           "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=self.f,
+                                          "-lms", "100"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
