@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--numel", type=int, default=0,
+                    help="override the workload's parameter count (small profiling cases)")
     return ap.parse_args()
 
 
@@ -219,6 +221,8 @@ def bench_ours(args, rank, world_size, device_index):
     from workloads.runner import Runner
 
     w = W.ALL[args.workload]()
+    if args.numel:
+        w = w.replace(numel=args.numel, name=w.name + "_numel%d" % args.numel)
     if w.inject:
         w = w.replace(inject=None)    # timed steps are the ones that apply
     torch.cuda.set_device(device_index)
