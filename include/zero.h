@@ -265,6 +265,37 @@ int zero3_step_unit(zero_ctx *ctx, int32_t unit, const void *const *grads,
 int zero3_reduce_unit(zero_ctx *ctx, int32_t unit, const void *const *grads,
                       int32_t n_grads, float loss_scale, void *stream);
 
+/* ------------------------------------------------ step without allocation */
+
+/* The pages have no counterpart of this call; it serves callers that can
+ * hand the library only their inputs and outputs and cannot call cudaMalloc
+ * for a scratch buffer -- for example a plugin whose host framework owns all
+ * device memory, or a code path that must not trigger cudaMalloc's implicit
+ * device synchronization.
+ *
+ * Same step as zero_step (stages 1 and 2, either view; loss_scale <= 0 means
+ * no unscaling and no skip), always run as the two passes, with the fp32
+ * scratch taken from a fixed 16 MiB array inside the library (4,194,304
+ * floats) instead of the bound g_scratch, which may be NULL.  Every GPU that
+ * loads the library holds that array until the process exits.  The call
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *   - The rank's range (zero_ctx_state_elems) must be at most 4,194,304
+ *     elements; larger ranges return ZERO_EINVAL with a message and launch
+ *     nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls in the process share the one array per device, and it keeps
+ *     the last call's contents.  Nothing in it needs to start at zero: the
+ *     first pass writes every element the second pass reads.  Calls that
+ *     overlap on the GPU (different streams, or contexts used concurrently)
+ *     race on the array and corrupt each other's results; calls on one
+ *     stream are ordered and safe.
+ * The verdict is read with zero_step_status() as for zero_step. */
+int zero_step_noalloc(zero_ctx *ctx, const void *const *grads, int32_t n_grads, double lr,
+                      double beta1, double beta2, double eps, int64_t t, float loss_scale,
+                      void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -64,6 +64,8 @@ _SIGS = {
     "zero3_step_unit": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f64, _f64, _f64, _f64, _i64,
                                        _vp]),
     "zero3_reduce_unit": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f32, _vp]),
+    "zero_step_noalloc": (ctypes.c_int, [_ctxp, _vpp, _i32, _f64, _f64, _f64, _f64, _i64, _f32,
+                                         _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_L, _name)
@@ -265,3 +267,13 @@ def zero3_step_unit(ctx, unit: int, grads, lr: float, beta1: float, beta2: float
 def zero3_reduce_unit(ctx, unit: int, grads, loss_scale: float = 0.0, stream=None) -> None:
     _check(_L.zero3_reduce_unit(_h(ctx), unit, _ptrs(grads), len(grads), loss_scale,
                                 _stream(stream)))
+
+
+# ------------------------------------------------- step without allocation
+
+def zero_step_noalloc(ctx, grads, lr: float, beta1: float, beta2: float, eps: float, t: int,
+                      loss_scale: float = 0.0, stream=None) -> None:
+    """zero_step with the scratch taken from the library's built-in array
+    (for callers that cannot allocate device memory; see include/zero.h)."""
+    _check(_L.zero_step_noalloc(_h(ctx), _ptrs(grads), len(grads), lr, beta1, beta2, eps, t,
+                                loss_scale, _stream(stream)))

@@ -639,3 +639,77 @@ int zero3_reduce_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- step without allocation
+//
+// zero_step_noalloc: the two-pass step with its fp32 scratch in a fixed
+// array compiled into this library instead of a caller buffer.  The array is
+// a device-side object; host code cannot use its name as an address, so the
+// address is looked up once per device (cudaGetSymbolAddress, with that
+// device current) and handed to the kernels.
+namespace {
+
+constexpr int64_t kNoAllocScratchFloats = (int64_t)1 << 22;   // 16 MiB per device
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+std::mutex g_noalloc_mu;
+std::vector<std::pair<int, float *>> g_noalloc_addr;   // (device, scratch address)
+
+int noalloc_scratch_address(float **out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    for (const auto &p : g_noalloc_addr)
+        if (p.first == dev) {
+            *out = p.second;
+            return ZERO_OK;
+        }
+    void *addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
+    g_noalloc_addr.push_back({dev, static_cast<float *>(addr)});
+    *out = static_cast<float *>(addr);
+    return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" int zero_step_noalloc(zero_ctx *c, const void *const *grads, int32_t n_grads,
+                                 double lr, double b1, double b2, double eps, int64_t t,
+                                 float loss_scale, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if ((rc = check_hyper(t))) return rc;
+    if (c->stage == 3) return fail(ZERO_EINVAL, "zero_step_noalloc covers stages 1 and 2");
+    const Range r = vector_range(c);
+    if (r.n > kNoAllocScratchFloats)
+        return fail(ZERO_EINVAL,
+                    "zero_step_noalloc: this rank's range has %lld elements but the built-in "
+                    "scratch holds %lld floats (16 MiB); bind a g_scratch and use zero_step",
+                    (long long)r.n, (long long)kNoAllocScratchFloats);
+    rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
+    if (rc) return rc;
+    float *scratch = nullptr;
+    if ((rc = noalloc_scratch_address(&scratch))) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    c->step_id += 1;
+    c->step_scaled = loss_scale > 0.0f;
+    if (r.n == 0) return ZERO_OK;
+
+    StepArgs a = make_args(c, r, grads);
+    a.g = scratch;    // every element of the range is written by the reduce pass first
+    bool ok = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16);
+    for (int32_t k = 0; k < c->world; ++k) ok = ok && aligned(grads[k], 16);
+    a.vec_ok = ok ? 1 : 0;
+    a.av = average_scalars(c->world, loss_scale);
+    a.step_id = c->step_id;
+    rc = finish_launch(c, zgb::launch_reduce(c->gdt, a, c->sms, s), "reduce kernel", s);
+    if (rc) return rc;
+    a.ad = adam_scalars(lr, b1, b2, eps, t);
+    a.step_id = c->step_scaled ? c->step_id : ~0ull;
+    return finish_launch(c, zgb::launch_apply(c->pdt, a, c->sms, s), "apply kernel", s);
+}
