@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--two-pass", action="store_true",
+                    help="loss-scaled workloads: the scratch-based two-pass step instead of the "
+                         "single pass over two state sets")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     return ap.parse_args()
@@ -140,8 +143,9 @@ class Clocks:
 class Launch:
     """One kernel launch of the step, bracketed by CUDA events."""
 
-    def __init__(self, name, alg_bytes, fn):
+    def __init__(self, name, alg_bytes, fn, kernels=1):
         self.name, self.alg_bytes, self.fn = name, alg_bytes, fn
+        self.kernels = kernels      # kernel launches the call makes
 
 
 def step_plan(run):
@@ -154,7 +158,15 @@ def step_plan(run):
     if w.stage < 3:
         n_state = w.shard * (w.world if w.rank < 0 else 1)
         n_valid = w.numel if w.rank < 0 else min(w.shard, max(0, w.numel - w.rank * w.shard))
-        if run.scale > 0:
+        if run.shadow is not None:
+            # one pass over two state sets; the call also launches the small
+            # finalize kernel (flip the current set, or recast on overflow)
+            def single():
+                z.zero_step(run.ctx, run.grads[0], w.lr, w.beta1, w.beta2, w.eps, run.t + 1,
+                            run.scale, st)
+            plan.append(Launch("fused_step_kernel", w.world * bg * n_valid + (24 + bp) * n_state,
+                               single, kernels=2))
+        elif run.scale > 0:
             def red():
                 z.zero_step_reduce(run.ctx, run.grads[0], run.scale, st)
 
@@ -226,7 +238,8 @@ def bench_ours(args, rank, world_size, device_index):
     if w.inject:
         w = w.replace(inject=None)    # timed steps are the ones that apply
     torch.cuda.set_device(device_index)
-    run = Runner(w, device="cuda:%d" % device_index)
+    shadow = w.loss_scale > 0 and w.stage < 3 and not args.two_pass
+    run = Runner(w, device="cuda:%d" % device_index, shadow=shadow)
     run.fill_grads(1)
     plan = step_plan(run)
     torch.cuda.synchronize()
@@ -299,6 +312,8 @@ def bench_ours(args, rank, world_size, device_index):
             "per_kernel_ms": {n: per[n][0] / per[n][1] for n in per},
             "parallelism": "%d simulated data-parallel ranks per GPU; %d GPU replica(s)"
                            % (w.world, world_size),
+            "path": ("single pass over two state sets" if shadow else
+                     "two passes with an fp32 scratch" if w.loss_scale > 0 else "single pass"),
         },
         "roofline": {
             "kernel": dom,
@@ -311,7 +326,7 @@ def bench_ours(args, rank, world_size, device_index):
             "alg_bytes_per_launch": alg_per_launch,
             "traffic": traffic,
         },
-        "gpu_launches": len(plan) * args.steps,
+        "gpu_launches": sum(L.kernels for L in plan) * args.steps,
         "clocks": clock_info,
     }
     if not args.no_e2e:
@@ -324,7 +339,8 @@ def bench_ours(args, rank, world_size, device_index):
 
 def working_set(run):
     tot = 0
-    for t in [run.master, run.m, run.v, run.params, run.g, run.unit_full]:
+    for t in [run.master, run.m, run.v, run.params, run.g, run.unit_full,
+              *(run.shadow or ())]:
         if t is not None:
             tot += t.numel() * t.element_size()
     for row in run.grads:

@@ -181,6 +181,28 @@ int zero_bind(zero_ctx *ctx, float *master, float *m, float *v, void *params,
  * P-element buffer.  NULL turns it off. */
 int zero_bind_allreduce_out(zero_ctx *ctx, void *grad_avg);
 
+/* Bind a second fp32 state set (stages 1 and 2) so that every step is one
+ * pass, loss-scaled or not: the step reads the current set, writes the
+ * other, and a small finalize kernel then makes the written set current --
+ * unless the step is loss-scaled and overflowed, in which case the old set
+ * stays current and the params are cast again from it ("PaddlePaddle
+ * ZeRO优化", 混合精度才是最佳拍档: the skipped step changes nothing).  This
+ * trades zero_ctx_state_elems() * 12 more bytes of memory for the two-pass
+ * path's extra scratch write and read (8 bytes per element).
+ *   master_b, m_b, v_b  zero_ctx_state_elems() floats each (contents unused
+ *               until written).
+ *   cur         one 8-byte device word, zeroed by the caller before the first
+ *               step: bit 0 clear = the zero_bind set is current, set = this
+ *               one.  Read it with zero_current_state().
+ * All four NULL unbinds.  With a second set bound, zero_step_apply and
+ * zero_step_noalloc update whichever set is current, in place. */
+int zero_bind_shadow(zero_ctx *ctx, float *master_b, float *m_b, float *v_b, uint64_t *cur);
+
+/* Synchronizes the stream of the last step and reports which state set holds
+ * the current master/m/v: 0 = the zero_bind buffers, 1 = the second set.
+ * Always 0 without a second set. */
+int zero_current_state(zero_ctx *ctx, int32_t *which);
+
 /* ------------------------------------------------------------ the step */
 
 /* One ZeRO step (stages 1, 2) on `stream`.
@@ -192,10 +214,11 @@ int zero_bind_allreduce_out(zero_ctx *ctx, void *grad_avg);
  *                   average + Adam + cast + all-gather placement); a
  *                   non-finite grad is still reported by zero_step_status
  *                   but never skips the step.  > 0: grads are divided by it
- *                   after averaging; two passes: zero_step_reduce then
- *                   zero_step_apply, and if any element of the step is
- *                   non-finite the apply pass changes nothing (needs
- *                   g_scratch).
+ *                   after averaging, and if any element of the step is
+ *                   non-finite the step changes nothing.  With a second
+ *                   state set bound (zero_bind_shadow) that is still one
+ *                   pass; otherwise two passes, zero_step_reduce then
+ *                   zero_step_apply (needs g_scratch).
  * The overflow verdict is read with zero_step_status() after the stream
  * reaches it. */
 int zero_step(zero_ctx *ctx, const void *const *grads, int32_t n_grads, double lr,

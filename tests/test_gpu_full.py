@@ -35,18 +35,19 @@ def check_sampled(run, w, idx, unit=0, state_off=0, param_off=None, skipped=()):
     iters = list(range(1, w.steps + 1))
     x, m, v, p = refs.sampled_reference(w, idx, iters, skipped_iters=set(skipped),
                                         rank=w.rank, unit=unit)
-    assert_state_close(gpu_at(run.master, idx + state_off), x, w.name + " master")
-    assert_state_close(gpu_at(run.m, idx + state_off), m, w.name + " m")
-    assert_state_close(gpu_at(run.v, idx + state_off), v, w.name + " v")
+    cx, cm, cv = run.state()
+    assert_state_close(gpu_at(cx, idx + state_off), x, w.name + " master")
+    assert_state_close(gpu_at(cm, idx + state_off), m, w.name + " m")
+    assert_state_close(gpu_at(cv, idx + state_off), v, w.name + " v")
     poff = state_off if param_off is None else param_off
     assert_params_close(gpu_at(run.params, idx + poff), p, w.param_dtype, w.name + " params")
     # bit-identical as well (same operations in the same order)
-    assert_bit_identical(gpu_at(run.master, idx + state_off), x, 0, w.name + " master")
+    assert_bit_identical(gpu_at(cx, idx + state_off), x, 0, w.name + " master")
 
 
-def run_all(w):
+def run_all(w, shadow=False):
     from workloads.runner import Runner
-    run = Runner(w)
+    run = Runner(w, shadow=shadow)
     for it in range(1, w.steps + 1):
         run.step(it)
     torch.cuda.synchronize()
@@ -62,9 +63,12 @@ def test_gpt2_small_full():
     run.close()
 
 
-def test_gpt2_xl_full_loss_scaled():
+@pytest.mark.parametrize("shadow", [False, True])
+def test_gpt2_xl_full_loss_scaled(shadow):
+    """Two passes (scratch), and one pass over two state sets (the bench's
+    configuration)."""
     w = W.gpt2_xl()
-    run = run_all(w)
+    run = run_all(w, shadow=shadow)
     # the one +inf at iteration 3 skips exactly that step; the draws are
     # bounded (|x| <= 3.47 sigma * scale), so no other overflow is possible
     assert run.skips == [i == 3 for i in range(1, w.steps + 1)]

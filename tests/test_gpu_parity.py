@@ -81,7 +81,8 @@ def compare_runner(run, ref, exact=True, what=""):
         m = np.concatenate([ref.state[u][1] for u in sorted(ref.state)])
         v = np.concatenate([ref.state[u][2] for u in sorted(ref.state)])
         full_ref = np.concatenate([ref.own[u] for u in sorted(ref.own)])
-    gx, gm, gv, gp = to_np(run.master), to_np(run.m), to_np(run.v), to_np(run.params)
+    cx, cm, cv = run.state()
+    gx, gm, gv, gp = to_np(cx), to_np(cm), to_np(cv), to_np(run.params)
     assert_state_close(gx, x, what + " master")
     assert_state_close(gm, m, what + " m")
     assert_state_close(gv, v, what + " v")
@@ -92,10 +93,10 @@ def compare_runner(run, ref, exact=True, what=""):
                                  "%s %s" % (what, name))
 
 
-def run_both(w, iters=None):
+def run_both(w, iters=None, shadow=False):
     from workloads.runner import Runner
     iters = iters or list(range(1, w.steps + 1))
-    run = Runner(w)
+    run = Runner(w, shadow=shadow)
     ref = refs.OracleRun(w)
     for it in iters:
         run.step(it)
@@ -372,4 +373,56 @@ def test_one_rank_step_then_placement(numel, world, rank):
                    gather_after=True)
     run, ref = run_both(w)
     compare_runner(run, ref, what="one-rank+placement")
+    run.close()
+
+
+# ------------------------------------------- one pass with two state sets
+
+@pytest.mark.parametrize("rank", [-1, 0])
+def test_shadow_single_pass_skip_sequence(rank):
+    """The loss-scaled step as one pass over two state sets: the skipped
+    iteration leaves the old set current and recasts the params from it;
+    bit-identical to the oracle over the whole sequence."""
+    w = W.Workload("shadow", 1_234_567, 16, 2, W.F16, W.F16, rank=rank, steps=6,
+                   loss_scale=2.0 ** 16, inject=(3, 5))
+    if rank >= 0:
+        e = synth.pick_index(w.seed, w.numel, step=3, rank=5)
+        w = w.replace(rank=e // w.shard)
+    run, ref = run_both(w, shadow=True)
+    assert ref.skips == [False, False, True, False, False, False]
+    import zero_sharded_optimizer_step_gb300 as z
+    # five applied steps flip the current set five times
+    assert z.zero_current_state(run.ctx) == 1
+    compare_runner(run, ref, what="shadow")
+    run.close()
+
+
+@pytest.mark.parametrize("numel,world,gdt,pdt,rank", [(1_000_003, 8, W.BF16, W.BF16, -1),
+                                                     (1_000_003, 3, W.F16, W.F32, 2),
+                                                     (99_999, 64, W.F32, W.BF16, 63)])
+def test_shadow_unscaled_steps(numel, world, gdt, pdt, rank):
+    w = W.Workload("shadow-u", numel, world, 2, gdt, pdt, rank=rank, steps=3, lr=1e-3)
+    run, ref = run_both(w, shadow=True)
+    compare_runner(run, ref, what="shadow-u")
+    run.close()
+
+
+def test_shadow_mixed_with_two_pass_steps():
+    """With two sets bound, the two-pass calls update the current set in
+    place; alternating them with one-pass steps still matches the oracle."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    w = W.Workload("mix", 500_001, 8, 2, W.BF16, W.BF16, steps=4, loss_scale=2.0 ** 8)
+    run = Runner(w, scratch=True, shadow=True)
+    ref = refs.OracleRun(w)
+    for it in range(1, 5):
+        run.fill_grads(it)
+        if it % 2:
+            run.launch_step()
+        else:
+            z.zero_step_reduce(run.ctx, run.grads[0], run.scale, run.stream)
+            z.zero_step_apply(run.ctx, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, run.stream)
+        run.finish_step()
+        ref.step(it)
+    compare_runner(run, ref, what="mix")
     run.close()

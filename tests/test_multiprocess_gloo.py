@@ -1,0 +1,130 @@
+"""The multi-rank protocol on CPU with real collectives (gloo, 2 and 4
+processes): each process is one data-parallel rank in the one-rank view --
+reduce-scatter in rank order, the overflow verdict combined across ranks with
+a MAX all-reduce between the reduce and the apply (as the one-rank ABI
+documents), Adam on the own shard, all-gather of the cast shards -- and the
+result must be bit-identical to the all-ranks step.  Also covers the
+benchmark's cross-rank timing helpers (barrier, max over ranks)."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, numel, inject_at, out_dir):
+    import sys
+    sys.path.insert(0, ROOT)
+    import oracle
+    import synth
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    S = oracle.shard_size(numel, world)
+    P = S * world
+    lo = rank * S
+    nv = max(0, min(S, numel - lo))
+    x = np.zeros(S, np.float32)
+    x[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER), 0.01, index0=lo)
+    m, v = np.zeros(S, np.float32), np.zeros(S, np.float32)
+    scale, good, t = 2.0 ** 12, 0, 0
+    full = np.zeros(P, np.uint16)
+    skips = []
+    for it in (1, 2, 3):
+        g = synth.fill_host(numel, synth.F16, synth.key(0, synth.KIND_GRAD, it, rank),
+                            1e-3 * scale)
+        if inject_at and it == inject_at[0] and rank == inject_at[1]:
+            g[inject_at[2]] = 0x7C00                          # +inf in fp16
+        padded = np.zeros(P, np.uint16)
+        padded[:numel] = g
+        # reduce-scatter in rank order: gather every rank's piece of my shard
+        # (16-bit patterns travel as int32: gloo has no 16-bit integer type)
+        pieces = [torch.zeros(S, dtype=torch.int32) for _ in range(world)]
+        for r in range(world):
+            send = torch.from_numpy(padded[r * S:(r + 1) * S].astype(np.int32))
+            dist.gather(send, pieces if r == rank else None, dst=r)
+        slices = [p.numpy().astype(np.uint16) for p in pieces]
+        # local verdict, then the MAX combine across ranks
+        acc = oracle.rank_sum(slices, oracle.F16, S, nv)
+        _, bad = oracle.average(acc, world, scale)
+        flag = torch.tensor([bad], dtype=torch.int64)
+        dist.all_reduce(flag, op=dist.ReduceOp.MAX)
+        others = int(flag.item())        # any rank's finding skips every rank
+        lp = full[lo:lo + S].copy()
+        skipped, _ = oracle.zero_rank_step(slices, oracle.F16, numel, rank, x, m, v, lp,
+                                           oracle.F16, 1e-3, 0.9, 0.999, 1e-8, t + 1,
+                                           loss_scale=scale, others_nonfinite=others)
+        skips.append(skipped)
+        if not skipped:
+            t += 1
+        # all-gather of the cast shards
+        shards = [torch.zeros(S, dtype=torch.int32) for _ in range(world)]
+        dist.all_gather(shards, torch.from_numpy(lp.astype(np.int32)))
+        full = np.concatenate([s.numpy().astype(np.uint16) for s in shards])
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    np.savez(os.path.join(out_dir, "rank%d.npz" % rank), x=x, m=m, v=v, full=full,
+             skips=np.array(skips))
+    # the benchmark's helpers under gloo
+    sys.argv = ["bench.py"]
+    import bench
+    bench.barrier(world)
+    assert bench.allreduce_max(float(rank) * 1.5, world) == 1.5 * (world - 1)
+    dist.destroy_process_group()
+
+
+def _all_ranks_reference(numel, world, inject_at):
+    import oracle
+    import synth
+    S = oracle.shard_size(numel, world)
+    P = S * world
+    x = np.zeros(P, np.float32)
+    x[:numel] = synth.fill_host(numel, synth.F32, synth.key(0, synth.KIND_MASTER), 0.01)
+    m, v = np.zeros(P, np.float32), np.zeros(P, np.float32)
+    full = np.zeros(P, np.uint16)
+    scale, good, t, skips = 2.0 ** 12, 0, 0, []
+    for it in (1, 2, 3):
+        grads = [synth.fill_host(numel, synth.F16, synth.key(0, synth.KIND_GRAD, it, k),
+                                 1e-3 * scale) for k in range(world)]
+        if inject_at and it == inject_at[0]:
+            grads[inject_at[1]][inject_at[2]] = 0x7C00
+        skipped, _ = oracle.zero_step(grads, oracle.F16, numel, x, m, v, full, oracle.F16,
+                                      1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale)
+        skips.append(skipped)
+        if not skipped:
+            t += 1
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    return x, m, v, full, skips
+
+
+@pytest.mark.parametrize("world,numel,inject_at", [
+    (2, 10_001, None),
+    (2, 10_001, (2, 1, 9_999)),      # rank 1's element in rank 1's shard
+    (4, 20_003, (2, 3, 17)),         # rank 3's element in rank 0's shard
+])
+def test_one_rank_views_with_real_collectives(tmp_path, world, numel, inject_at):
+    port = _free_port()
+    mp.start_processes(_rank_main, args=(world, port, numel, inject_at, str(tmp_path)),
+                       nprocs=world, join=True, start_method="spawn")
+    import oracle
+    x, m, v, full, skips = _all_ranks_reference(numel, world, inject_at)
+    S = oracle.shard_size(numel, world)
+    want_skips = [bool(inject_at) and it == inject_at[0] for it in (1, 2, 3)]
+    assert skips == want_skips
+    for r in range(world):
+        d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
+        assert list(d["skips"]) == skips, r
+        sl = slice(r * S, (r + 1) * S)
+        assert d["x"].tobytes() == x[sl].tobytes()
+        assert d["m"].tobytes() == m[sl].tobytes()
+        assert d["v"].tobytes() == v[sl].tobytes()
+        assert d["full"].tobytes() == full.tobytes()

@@ -31,7 +31,8 @@ def inject_index(w: Workload, it: int, rank: int, unit: int = 0) -> int:
 
 
 class Runner:
-    def __init__(self, w: Workload, device: str = "cuda:0", scratch: bool | None = None):
+    def __init__(self, w: Workload, device: str = "cuda:0", scratch: bool | None = None,
+                 shadow: bool = False):
         self.w = w
         self.dev = torch.device(device)
         torch.cuda.set_device(self.dev)
@@ -44,10 +45,17 @@ class Runner:
         self.m = torch.zeros(ns, **f32)
         self.v = torch.zeros(ns, **f32)
         self.params = torch.zeros(npar, dtype=TORCH_DTYPE[w.param_dtype], device=self.dev)
-        need_scratch = w.loss_scale > 0 if scratch is None else scratch
+        need_scratch = (w.loss_scale > 0 and not shadow) if scratch is None else scratch
         self.g = torch.zeros(ns, **f32) if need_scratch else None
         self.flag = torch.zeros(1, dtype=torch.int64, device=self.dev)
         z.zero_bind(self.ctx, self.master, self.m, self.v, self.params, self.g, self.flag)
+        self.shadow = None
+        if shadow:
+            # a second state set: every step is one pass, loss-scaled or not
+            self.shadow = (torch.zeros(ns, **f32), torch.zeros(ns, **f32),
+                           torch.zeros(ns, **f32))
+            self.cur = torch.zeros(1, dtype=torch.int64, device=self.dev)
+            z.zero_bind_shadow(self.ctx, *self.shadow, self.cur)
         self.stream = torch.cuda.current_stream(self.dev)
         self.scale = w.loss_scale
         self.good = 0
@@ -202,6 +210,12 @@ class Runner:
             self.fill_grads(it)
         self.launch_step()
         return self.finish_step()
+
+    def state(self):
+        """(master, m, v) of the current state set (synchronizes)."""
+        if self.shadow is None or z.zero_current_state(self.ctx) == 0:
+            return self.master, self.m, self.v
+        return self.shadow
 
     def close(self):
         self.ctx.close()

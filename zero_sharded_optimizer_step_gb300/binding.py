@@ -53,6 +53,8 @@ _SIGS = {
     "zero_state_bytes": (_i64, [_ctxp]),
     "zero_bind": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_bind_allreduce_out": (ctypes.c_int, [_ctxp, _vp]),
+    "zero_bind_shadow": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp]),
+    "zero_current_state": (ctypes.c_int, [_ctxp, ctypes.POINTER(_i32)]),
     "zero_step": (ctypes.c_int, [_ctxp, _vpp, _i32, _f64, _f64, _f64, _f64, _i64, _f32, _vp]),
     "zero_step_reduce": (ctypes.c_int, [_ctxp, _vpp, _i32, _f32, _vp]),
     "zero_step_apply": (ctypes.c_int, [_ctxp, _f64, _f64, _f64, _f64, _i64, _vp]),
@@ -208,6 +210,17 @@ def zero_state_bytes(ctx) -> int:
 def zero_bind(ctx, master, m, v, params, g_scratch=None, flag=None) -> None:
     _check(_L.zero_bind(_h(ctx), _ptr(master), _ptr(m), _ptr(v), _ptr(params),
                         _ptr(g_scratch), _ptr(flag)))
+
+
+def zero_bind_shadow(ctx, master_b, m_b, v_b, cur) -> None:
+    _check(_L.zero_bind_shadow(_h(ctx), _ptr(master_b), _ptr(m_b), _ptr(v_b), _ptr(cur)))
+
+
+def zero_current_state(ctx) -> int:
+    """Synchronizes; 0 = the zero_bind state set is current, 1 = the second."""
+    w = _i32(0)
+    _check(_L.zero_current_state(_h(ctx), ctypes.byref(w)))
+    return int(w.value)
 
 
 def zero_bind_allreduce_out(ctx, grad_avg) -> None:

@@ -65,6 +65,8 @@ struct zero_ctx {
     int64_t state_elems = 0, param_elems = 0;
 
     float *master = nullptr, *m = nullptr, *v = nullptr, *g = nullptr;
+    float *xb = nullptr, *mb = nullptr, *vb = nullptr;   // second state set
+    uint64_t *cur = nullptr;                              // which set is current
     void *params = nullptr, *grad_avg = nullptr;
     uint64_t *flag = nullptr;
     bool bound = false;
@@ -215,13 +217,20 @@ StepArgs make_args(const zero_ctx *c, const Range &r, const void *const *grads)
     a.m = c->m + r.state_off;
     a.v = c->v + r.state_off;
     a.g = c->g ? c->g + r.state_off : nullptr;
+    if (c->cur) {
+        a.xb = c->xb + r.state_off;
+        a.mb = c->mb + r.state_off;
+        a.vb = c->vb + r.state_off;
+        a.cur = reinterpret_cast<unsigned long long *>(c->cur);
+    }
     a.params = r.params;
     a.grad_avg = r.grad_avg;
     a.param_align = align_of(r.params);
     a.avg_align = r.grad_avg ? align_of(r.grad_avg) : 16;
     a.flag = reinterpret_cast<unsigned long long *>(c->flag);
     bool ok = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16) &&
-              (!a.g || aligned(a.g, 16));
+              (!a.g || aligned(a.g, 16)) &&
+              (!a.cur || (aligned(a.xb, 16) && aligned(a.mb, 16) && aligned(a.vb, 16)));
     if (grads) {
         for (int32_t k = 0; k < c->world; ++k) {
             a.grads[k] = grads[k];
@@ -261,14 +270,19 @@ int do_apply(zero_ctx *c, const Range &r, double lr, double b1, double b2, doubl
 }
 
 int do_fused(zero_ctx *c, const Range &r, const void *const *grads, double lr, double b1,
-             double b2, double eps, int64_t t, cudaStream_t s)
+             double b2, double eps, int64_t t, cudaStream_t s, float loss_scale = 0.0f)
 {
     if (r.n == 0) return ZERO_OK;
     StepArgs a = make_args(c, r, grads);
-    a.av = average_scalars(c->world, 0.0f);
+    a.av = average_scalars(c->world, loss_scale);
     a.ad = adam_scalars(lr, b1, b2, eps, t);
     a.step_id = c->step_id;
-    return finish_launch(c, zgb::launch_fused_step(c->gdt, c->pdt, a, c->sms, s), "step kernel", s);
+    int rc = finish_launch(c, zgb::launch_fused_step(c->gdt, c->pdt, a, c->sms, s), "step kernel", s);
+    if (rc || !c->cur) return rc;
+    // two state sets: the written set becomes current unless the step is
+    // loss-scaled and overflowed
+    a.step_id = c->step_scaled ? c->step_id : ~0ull;
+    return finish_launch(c, zgb::launch_finalize(c->pdt, a, c->sms, s), "finalize kernel", s);
 }
 
 int check_hyper(int64_t t)
@@ -474,6 +488,42 @@ int zero_bind(zero_ctx *c, float *master, float *m, float *v, void *params, floa
     return ZERO_OK;
 }
 
+int zero_bind_shadow(zero_ctx *c, float *master_b, float *m_b, float *v_b, uint64_t *cur)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (!master_b && !m_b && !v_b && !cur) {
+        c->xb = c->mb = c->vb = nullptr;
+        c->cur = nullptr;
+        return ZERO_OK;
+    }
+    if (c->stage == 3) return fail(ZERO_EINVAL, "a second state set is for stages 1 and 2");
+    if (!cur || (c->state_elems > 0 && (!master_b || !m_b || !v_b)))
+        return fail(ZERO_EINVAL, "master_b, m_b, v_b and cur must all be given (or all NULL)");
+    if (!aligned(master_b, 4) || !aligned(m_b, 4) || !aligned(v_b, 4))
+        return fail(ZERO_EALIGN, "the second state set must be 4-byte aligned");
+    if (!aligned(cur, 8)) return fail(ZERO_EALIGN, "cur must be 8-byte aligned");
+    c->xb = master_b;
+    c->mb = m_b;
+    c->vb = v_b;
+    c->cur = cur;
+    return ZERO_OK;
+}
+
+int zero_current_state(zero_ctx *c, int32_t *which)
+{
+    if (!c || !which) return fail(ZERO_EINVAL, "null argument");
+    if (!c->cur) {
+        *which = 0;
+        return ZERO_OK;
+    }
+    unsigned long long h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, c->cur, sizeof h, cudaMemcpyDeviceToHost, c->last_stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->last_stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the current-set word");
+    *which = (int32_t)(h & 1ull);
+    return ZERO_OK;
+}
+
 int zero_bind_allreduce_out(zero_ctx *c, void *grad_avg)
 {
     if (!c) return fail(ZERO_EINVAL, "null context");
@@ -521,6 +571,12 @@ int zero_step(zero_ctx *c, const void *const *grads, int32_t n_grads, double lr,
     rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
     if (rc) return rc;
     cudaStream_t s = (cudaStream_t)stream;
+    if (c->cur) {
+        // two state sets: one pass whatever the loss scale
+        c->step_id += 1;
+        c->step_scaled = loss_scale > 0.0f;
+        return do_fused(c, r, grads, lr, b1, b2, eps, t, s, loss_scale);
+    }
     if (loss_scale > 0.0f) {
         if (!c->g) return fail(ZERO_ESTATE, "a loss-scaled step needs g_scratch (zero_bind)");
         c->step_id += 1;

@@ -43,6 +43,10 @@ struct StepArgs {
     void *params;                  // low-precision output
     void *grad_avg;                // stage-1 all-reduce output (grad type) or null
     float *g;                      // two-pass scratch
+    // second state set (null when not bound) and the word naming the
+    // current set: bit 0 clear = master/m/v, set = xb/mb/vb
+    float *xb, *mb, *vb;
+    unsigned long long *cur;
     unsigned long long *flag;      // id of the latest step with a non-finite grad
     unsigned long long step_id;
     AverageScalars av;
@@ -66,6 +70,10 @@ cudaError_t launch_fused_step(int32_t gdt, int32_t pdt, const StepArgs &a, int s
                               cudaStream_t s);
 cudaError_t launch_reduce(int32_t gdt, const StepArgs &a, int sms, cudaStream_t s);
 cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s);
+// After a single-pass step on two state sets: make the written set current,
+// or, when the step overflowed, keep the old set and rewrite the params
+// from it.
+cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s);
 
 }  // namespace zgb

@@ -11,6 +11,11 @@
 //   apply       second pass: Adam + cast from the scratch, or nothing at all
 //               when the flag names this step ("PaddlePaddle ZeRO优化",
 //               混合精度才是最佳拍档: the step is skipped on inf/nan).
+//   finalize    with two state sets bound, the loss-scaled step is a single
+//               pass: fused_step reads the current set and writes the other
+//               one; finalize then makes the written set current, or, if the
+//               step overflowed, leaves the old set current and rewrites the
+//               params from it -- the skip without a second pass.
 //
 // The work is a few flops per byte, so HBM bandwidth bounds every kernel;
 // no tensor cores are involved.  Each thread handles kVec = 8 consecutive
@@ -274,6 +279,27 @@ __device__ __forceinline__ void publish_flag(const StepArgs &a, bool bad)
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicMax(a.flag, a.step_id);
 }
 
+// Where a pass reads and writes the state.  One set: in place.  Two sets:
+// read the current one; `fresh` passes (fused_step) write the other one,
+// in-place passes (apply) write the current one.
+struct StatePtrs {
+    const float *sx, *sm, *sv;
+    float *dx, *dm, *dv;
+};
+
+__device__ __forceinline__ StatePtrs select_state(const StepArgs &a, bool fresh)
+{
+    StatePtrs p{a.master, a.m, a.v, a.master, a.m, a.v};
+    if (a.cur) {
+        const bool b = (*reinterpret_cast<volatile unsigned long long *>(a.cur) & 1ull) != 0;
+        float *cx = b ? a.xb : a.master, *cm = b ? a.mb : a.m, *cv = b ? a.vb : a.v;
+        float *ox = b ? a.master : a.xb, *om = b ? a.m : a.mb, *ov = b ? a.v : a.vb;
+        p.sx = cx; p.sm = cm; p.sv = cv;
+        p.dx = fresh ? ox : cx; p.dm = fresh ? om : cm; p.dv = fresh ? ov : cv;
+    }
+    return p;
+}
+
 // ---------------------------------------------------------------- kernels
 
 template <int GT, int PT, bool AVG>
@@ -283,13 +309,14 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
+    const StatePtrs st = select_state(a, true);
     bool bad = false;
     for (int64_t k = tid; k < nvec; k += stride) {
         const int64_t i = k * kVec;
         float x[kVec], m[kVec], v[kVec], acc[kVec];
-        load_state8(a.master, i, x);
-        load_state8(a.m, i, m);
-        load_state8(a.v, i, v);
+        load_state8(st.sx, i, x);
+        load_state8(st.sm, i, m);
+        load_state8(st.sv, i, v);
         rank_sum8<GT>(a, i, acc);
         float g[kVec];
 #pragma unroll
@@ -307,9 +334,9 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
             bad |= nonfinite(g[e]);
             adam1(g[e], x[e], m[e], v[e], a.ad);
         }
-        store_state8(a.master, i, x);
-        store_state8(a.m, i, m);
-        store_state8(a.v, i, v);
+        store_state8(st.dx, i, x);
+        store_state8(st.dm, i, m);
+        store_state8(st.dv, i, v);
         store_params8<PT>(a.params, i, x, a.param_align);
         if (AVG) store_params8<GT>(a.grad_avg, i, acc, a.avg_align);
     }
@@ -320,11 +347,11 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
         float g = !a.av.scaled ? mean
                   : (a.av.scale_pow2 ? __fmul_rn(mean, a.av.inv_scale) : __fdiv_rn(mean, a.av.scale));
         bad |= nonfinite(g);
-        float x = a.master[i], m = a.m[i], v = a.v[i];
+        float x = st.sx[i], m = st.sm[i], v = st.sv[i];
         adam1(g, x, m, v, a.ad);
-        a.master[i] = x;
-        a.m[i] = m;
-        a.v[i] = v;
+        st.dx[i] = x;
+        st.dm[i] = m;
+        st.dv[i] = v;
         Ty<PT>::store1(a.params, i, x);
         if (AVG) Ty<GT>::store1(a.grad_avg, i, mean);
     }
@@ -376,28 +403,55 @@ apply_kernel(const __grid_constant__ StepArgs a)
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n / kVec : 0;
+    const StatePtrs st = select_state(a, false);
     for (int64_t k = tid; k < nvec; k += stride) {
         const int64_t i = k * kVec;
         float x[kVec], m[kVec], v[kVec], g[kVec];
         load_state8(a.g, i, g);
-        load_state8(a.master, i, x);
-        load_state8(a.m, i, m);
-        load_state8(a.v, i, v);
+        load_state8(st.sx, i, x);
+        load_state8(st.sm, i, m);
+        load_state8(st.sv, i, v);
 #pragma unroll
         for (int e = 0; e < kVec; ++e) adam1(g[e], x[e], m[e], v[e], a.ad);
-        store_state8(a.master, i, x);
-        store_state8(a.m, i, m);
-        store_state8(a.v, i, v);
+        store_state8(st.dx, i, x);
+        store_state8(st.dm, i, m);
+        store_state8(st.dv, i, v);
         store_params8<PT>(a.params, i, x, a.param_align);
     }
     for (int64_t i = nvec * kVec + tid; i < a.n; i += stride) {
-        float x = a.master[i], m = a.m[i], v = a.v[i];
+        float x = st.sx[i], m = st.sm[i], v = st.sv[i];
         adam1(a.g[i], x, m, v, a.ad);
-        a.master[i] = x;
-        a.m[i] = m;
-        a.v[i] = v;
+        st.dx[i] = x;
+        st.dm[i] = m;
+        st.dv[i] = v;
         Ty<PT>::store1(a.params, i, x);
     }
+}
+
+template <int PT>
+__global__ void __launch_bounds__(kThreads)
+finalize_kernel(const __grid_constant__ StepArgs a)
+{
+    const bool overflowed =
+        *reinterpret_cast<volatile unsigned long long *>(a.flag) == a.step_id;
+    if (!overflowed) {
+        // the set the step wrote becomes current; no block reads the word here
+        if (blockIdx.x == 0 && threadIdx.x == 0) *a.cur ^= 1ull;
+        return;
+    }
+    // skipped step: the old set stays current; the params were written from
+    // the discarded update, so cast them again from the kept master
+    const bool b = (*reinterpret_cast<volatile unsigned long long *>(a.cur) & 1ull) != 0;
+    const float *x = b ? a.xb : a.master;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nvec = a.vec_ok ? a.n / kVec : 0;
+    for (int64_t k = tid; k < nvec; k += stride) {
+        float v[kVec];
+        load_state8(x, k * kVec, v);
+        store_params8<PT>(a.params, k * kVec, v, a.param_align);
+    }
+    for (int64_t i = nvec * kVec + tid; i < a.n; i += stride) Ty<PT>::store1(a.params, i, x[i]);
 }
 
 // ------------------------------------------------------------- launching
@@ -468,6 +522,17 @@ cudaError_t launch_reduce(int32_t gdt, const StepArgs &a, int sms, cudaStream_t 
     case F32: return reduce_gt<F32>(a, sms, s);
     case BF16: return reduce_gt<BF16>(a, sms, s);
     case F16: return reduce_gt<F16>(a, sms, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s)
+{
+    const int64_t w = items(a, a.n);
+    switch (pdt) {
+    case F32: return launch(finalize_kernel<F32>, a, w, sms, s);
+    case BF16: return launch(finalize_kernel<BF16>, a, w, sms, s);
+    case F16: return launch(finalize_kernel<F16>, a, w, sms, s);
     }
     return cudaErrorInvalidValue;
 }
