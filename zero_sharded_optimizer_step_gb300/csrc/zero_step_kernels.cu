@@ -20,7 +20,7 @@
 // The work is a few flops per byte, so HBM bandwidth bounds every kernel;
 // no tensor cores are involved.  Each thread handles kVec = 8 consecutive
 // elements per iteration with 16-byte loads (one per 16-bit gradient
-// buffer), issues the state loads and a chunk of 8 gradient loads before
+// buffer), issues the state loads and a chunk of 4 gradient loads before
 // consuming any, and walks a grid sized to fill every SM (grid-stride
 // loop, 64-bit indices).  Elements past the last full vector, padding
 // positions and buffers that are not 16-byte aligned take a per-element path
@@ -203,13 +203,15 @@ __device__ __forceinline__ void adam1(float g, float &x, float &m, float &v, con
 }
 
 // Rank-order sum of 8 consecutive elements at vector index k of every rank
-// buffer, chunk by chunk: a chunk's 16-byte loads are all issued before any
-// of them is added, and within the chunk the adds go in rank order.
+// buffer, chunk by chunk: a chunk's 16-byte loads (4 ranks) are all issued
+// before any of them is added, and within the chunk the adds go in rank
+// order.  Four ranks per chunk keeps the registers low enough for four
+// resident blocks per SM; the bytes in flight come from occupancy.
 template <int GT>
 __device__ __forceinline__ void rank_sum8(const StepArgs &a, int64_t i, float (&acc)[kVec])
 {
     constexpr int L = Ty<GT>::kLoads;
-    constexpr int kChunk = 8;
+    constexpr int kChunk = 4;
     const int64_t byte_off = i * (GT == F32 ? 4 : 2);
     for (int c = 0; c < a.world; c += kChunk) {
         uint4 raw[kChunk][L];
@@ -300,10 +302,16 @@ __device__ __forceinline__ StatePtrs select_state(const StepArgs &a, bool fresh)
     return p;
 }
 
+// Resident blocks per SM the step kernels are compiled for: four with 16-bit
+// grads (measured fastest on GB300: more warps in flight beat a deeper
+// per-thread chunk); two with fp32 grads, whose eight-element vectors need
+// twice the load registers.
+template <int GT> struct MinBlocks { static constexpr int value = GT == F32 ? 2 : 4; };
+
 // ---------------------------------------------------------------- kernels
 
 template <int GT, int PT, bool AVG>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
 fused_step_kernel(const __grid_constant__ StepArgs a)
 {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -359,7 +367,7 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
 }
 
 template <int GT, bool AVG>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
 reduce_kernel(const __grid_constant__ StepArgs a)
 {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
