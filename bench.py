@@ -37,9 +37,17 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-# dram bytes per launch from ncu captures (see profiles/), valid only for the
-# kernel source they were taken on
-TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the dominant kernel, from ncu
+# captures summarised under profiles/: small cases of the same kernel scaled
+# to the full launch by the elements processed (the kernels stream, so
+# traffic grows in proportion).  Each entry is valid only for the kernel
+# source it was taken on (sha256 prefix); otherwise the bench reports null.
+TRAFFIC = {
+    ("gpt2_xl", "fused_step_kernel"): ("94ca1758ce0b4378", (4.400171e9 + 1.403571e9) * 15.576112),
+    ("one_rank_7p5b", "gather_kernel"): ("d09e0618a79e1973", (1.260070e9 + 1.208794e9) * 11.71875),
+    ("one_rank_7p5b", "fused_step_kernel"): ("94ca1758ce0b4378",
+                                             (1.400088576e9 + 0.13635968e9) * 11.71875),
+}
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
                           "zero_step_kernels.cu")
 GATHER_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc", "zero_gather.cu")
