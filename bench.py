@@ -289,7 +289,7 @@ def bench_ours(args, rank, world_size, device_index):
     peak, peak_kind = peaks()
     achieved = alg_per_launch / (avg_ms * 1e-3) / 1e9
     kh = src_hash(GATHER_SRC if dom == "gather_kernel" else KERNEL_SRC)
-    tr = TRAFFIC.get((args.workload, dom))
+    tr = None if args.numel else TRAFFIC.get((args.workload, dom))
     traffic = tr[1] if tr and tr[0] == kh else None
 
     updated = w.updated_per_step()
