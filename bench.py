@@ -383,7 +383,9 @@ def bench_e2e(run, plan, args, world_size):
         avail = int(open("/proc/meminfo").read().split("MemAvailable:")[1].split()[0]) * 1024
     except Exception:
         avail = 32 << 30
-    cap = min(h2d, int(0.3 * avail), 48 << 30)
+    # the ranks on this node share its RAM
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", str(world_size)))
+    cap = min(h2d, int(0.3 * avail / max(1, local_ranks)), 48 << 30)
     # pinned host copies of the grads (cycled through when RAM is short)
     host = []
     used = 0
