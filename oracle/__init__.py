@@ -67,12 +67,12 @@ def lib() -> ctypes.CDLL:
                 "orc_all_gather": (None, [vpp, i32, i64, i32, vp, i64p]),
                 "orc_all_reduce_mean": (None, [vpp, i32, i64, i32, fp]),
                 "orc_adam_scalars": (None, [f64, f64, i64, fp]),
-                "orc_adam": (None, [fp, fp, fp, fp, i64, f64, f64, f64, f64, i64]),
+                "orc_adam": (None, [fp, fp, fp, fp, i64, f64, f64, f64, f64, i64, f64]),
                 "orc_zero_step": (ctypes.c_int, [vpp, i32, i64, i32, fp, fp, fp, vp, i32,
-                                                 f64, f64, f64, f64, i64, f32, fp, i64p]),
+                                                 f64, f64, f64, f64, i64, f32, fp, i64p, f64]),
                 "orc_zero_rank_step": (ctypes.c_int, [vpp, i32, i64, i32, i32, fp, fp, fp,
                                                       vp, i32, f64, f64, f64, f64, i64, f32,
-                                                      i64, fp, i64p]),
+                                                      i64, fp, i64p, f64]),
                 "orc_scale_update": (f32, [f32, i32, i64p, i64]),
             }
             for name, (res, args) in sig.items():
@@ -188,16 +188,17 @@ def adam_scalars(beta1: float, beta2: float, t: int):
     return out
 
 
-def adam(x, m, v, g, lr, beta1, beta2, eps, t):
-    """In-place Adam on float32 arrays x, m, v with gradient g."""
+def adam(x, m, v, g, lr, beta1, beta2, eps, t, weight_decay=0.0):
+    """In-place Adam (AdamW when weight_decay != 0) on float32 arrays x, m, v
+    with gradient g."""
     for a in (x, m, v, g):
         assert a.dtype == np.float32 and a.size == x.size
     lib().orc_adam(_fp(x), _fp(m), _fp(v), _fp(np.ascontiguousarray(g)), x.size,
-                   lr, beta1, beta2, eps, t)
+                   lr, beta1, beta2, eps, t, weight_decay)
 
 
 def zero_step(grads, grad_dtype, numel, master, m, v, full, param_dtype,
-              lr, beta1, beta2, eps, t, loss_scale=0.0):
+              lr, beta1, beta2, eps, t, loss_scale=0.0, weight_decay=0.0):
     """All-ranks ZeRO-2 step, in place.  Returns (skipped, n_nonfinite)."""
     world = len(grads)
     for g in grads:
@@ -212,14 +213,15 @@ def zero_step(grads, grad_dtype, numel, master, m, v, full, param_dtype,
     bad = ctypes.c_int64(0)
     rc = lib().orc_zero_step(_ptrs(grads), grad_dtype, numel, world, _fp(master), _fp(m),
                              _fp(v), _vp(full), param_dtype, lr, beta1, beta2, eps, t,
-                             loss_scale, _fp(work), ctypes.byref(bad))
+                             loss_scale, _fp(work), ctypes.byref(bad), weight_decay)
     if rc < 0:
         raise ValueError("orc_zero_step: bad arguments")
     return bool(rc == 1), int(bad.value)
 
 
 def zero_rank_step(slices, grad_dtype, numel, rank, master, m, v, lp_out, param_dtype,
-                   lr, beta1, beta2, eps, t, loss_scale=0.0, others_nonfinite=0):
+                   lr, beta1, beta2, eps, t, loss_scale=0.0, others_nonfinite=0,
+                   weight_decay=0.0):
     """One rank's view, in place.  Returns (skipped, n_nonfinite_local)."""
     world = len(slices)
     S = shard_size(numel, world)
@@ -235,7 +237,7 @@ def zero_rank_step(slices, grad_dtype, numel, rank, master, m, v, lp_out, param_
     rc = lib().orc_zero_rank_step(_ptrs(slices), grad_dtype, numel, world, rank, _fp(master),
                                   _fp(m), _fp(v), _vp(lp_out), param_dtype, lr, beta1, beta2,
                                   eps, t, loss_scale, others_nonfinite, _fp(work),
-                                  ctypes.byref(bad))
+                                  ctypes.byref(bad), weight_decay)
     if rc < 0:
         raise ValueError("orc_zero_rank_step: bad arguments")
     return bool(rc == 1), int(bad.value)

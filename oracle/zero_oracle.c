@@ -222,10 +222,17 @@ void orc_adam_scalars(double beta1, double beta2, int64_t t, float *out)
  *   v     = beta2*v + (1-beta2)*g*g
  *   m_hat = m / (1 - beta1^t)
  *   v_hat = v / (1 - beta2^t)
- *   x     = x - lr*m_hat / (sqrt(v_hat) + eps)       (eps outside the root) */
+ *   x     = x - lr*m_hat / (sqrt(v_hat) + eps)       (eps outside the root)
+ * With weight_decay != 0 the decay is decoupled from the gradient (AdamW,
+ * Loshchilov & Hutter, "Decoupled Weight Decay Regularization", ICLR 2019;
+ * the Paddle page names AdamW as the optimizer): the weight is first scaled
+ * by 1 - lr*weight_decay (one fp32 scalar, computed in double), then the
+ * Adam step is subtracted:  x = x*(1 - lr*wd) - lr*m_hat/(sqrt(v_hat)+eps). */
 void orc_adam(float *x, float *m, float *v, const float *g, int64_t n,
-              double lr, double beta1, double beta2, double eps, int64_t t)
+              double lr, double beta1, double beta2, double eps, int64_t t,
+              double weight_decay)
 {
+    const float decay = (float)(1.0 - lr * weight_decay);
     float s[4];
     orc_adam_scalars(beta1, beta2, t, s);
     const float c1 = s[0], c2 = s[1], bc1 = s[2], bc2 = s[3];
@@ -238,9 +245,11 @@ void orc_adam(float *x, float *m, float *v, const float *g, int64_t n,
         float vh = vj / bc2;
         float den = sqrtf(vh) + epsf;
         float upd = (lrf * mh) / den;
+        float xj = x[j];
+        if (weight_decay != 0.0) xj = xj * decay;
         m[j] = mj;
         v[j] = vj;
-        x[j] = x[j] - upd;
+        x[j] = xj - upd;
     }
 }
 
@@ -264,7 +273,7 @@ void orc_adam(float *x, float *m, float *v, const float *g, int64_t n,
 int orc_zero_step(const void *const *grads, int32_t grad_dtype, int64_t numel, int32_t world,
                   float *master, float *m, float *v, void *full, int32_t param_dtype,
                   double lr, double beta1, double beta2, double eps, int64_t t, float loss_scale,
-                  float *work, int64_t *n_nonfinite)
+                  float *work, int64_t *n_nonfinite, double weight_decay)
 {
     int64_t S = orc_shard_size(numel, world);
     if (S < 0 || t < 1 || world > 4096) return -1;
@@ -279,7 +288,7 @@ int orc_zero_step(const void *const *grads, int32_t grad_dtype, int64_t numel, i
     if (loss_scale > 0.0f && bad > 0) return 1;
     for (int32_t r = 0; r < world; ++r) {
         int64_t o = (int64_t)r * S;
-        orc_adam(master + o, m + o, v + o, work + o, S, lr, beta1, beta2, eps, t);
+        orc_adam(master + o, m + o, v + o, work + o, S, lr, beta1, beta2, eps, t, weight_decay);
     }
     int32_t es = orc_elem_size(param_dtype);
     char *lp = (char *)(work + P);            /* rank r's cast shard at lp + r*S*es */
@@ -308,7 +317,7 @@ int orc_zero_rank_step(const void *const *slices, int32_t grad_dtype, int64_t nu
                        int32_t world, int32_t rank, float *master, float *m, float *v,
                        void *lp_out, int32_t param_dtype, double lr, double beta1, double beta2,
                        double eps, int64_t t, float loss_scale, int64_t others_nonfinite,
-                       float *work, int64_t *n_nonfinite)
+                       float *work, int64_t *n_nonfinite, double weight_decay)
 {
     int64_t S = orc_shard_size(numel, world);
     if (S < 0 || t < 1 || rank < 0 || rank >= world) return -1;
@@ -319,7 +328,7 @@ int orc_zero_rank_step(const void *const *slices, int32_t grad_dtype, int64_t nu
     int64_t bad = orc_average(work, S, world, loss_scale, work);
     if (n_nonfinite) *n_nonfinite = bad;
     if (loss_scale > 0.0f && bad + others_nonfinite > 0) return 1;
-    orc_adam(master, m, v, work, S, lr, beta1, beta2, eps, t);
+    orc_adam(master, m, v, work, S, lr, beta1, beta2, eps, t, weight_decay);
     orc_cast(master, S, param_dtype, lp_out);
     return 0;
 }

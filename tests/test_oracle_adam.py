@@ -230,3 +230,58 @@ def test_pages_four_rank_mlp_check():
     diff = max((a - b).abs().max().item() for a, b in zip(ref.parameters(), model.parameters()))
     assert diff < float(golden["max_abs_diff_below"])
     assert oracle.memory.zero_adam_state_bytes(numel, world) == int(golden["state_bytes_rank"])
+
+
+# ------------------------------------------------------------------ AdamW
+
+def test_adamw_zero_gradient_is_pure_decay():
+    """AdamW with g = 0: m = v = 0, the Adam step is exactly 0, and each step
+    multiplies x by d = fp32(1 - lr*wd): x_t is t exact fp32 products."""
+    rng = np.random.default_rng(30)
+    x, m, v = _fresh(1000, rng)
+    x0 = x.copy()
+    lr, wd = 1e-2, 0.1
+    d = np.float32(1.0 - lr * wd)
+    want = x0.copy()
+    for t in range(1, 8):
+        oracle.adam(x, m, v, np.zeros(1000, np.float32), lr, 0.9, 0.999, 1e-8, t,
+                    weight_decay=wd)
+        want = (want * d).astype(np.float32)
+    assert x.tobytes() == want.tobytes()
+    assert np.allclose(x, x0.astype(np.float64) * (1 - lr * wd) ** 7, rtol=8 * U, atol=0)
+
+
+def test_adamw_without_decay_is_adam_bit_for_bit():
+    rng = np.random.default_rng(31)
+    xa, ma, va = _fresh(3000, rng)
+    xb, mb, vb = xa.copy(), ma.copy(), va.copy()
+    for t in range(1, 5):
+        g = rng.normal(0, 1e-2, 3000).astype(np.float32)
+        oracle.adam(xa, ma, va, g, 1e-3, 0.9, 0.999, 1e-8, t)
+        oracle.adam(xb, mb, vb, g, 1e-3, 0.9, 0.999, 1e-8, t, weight_decay=0.0)
+    assert xa.tobytes() == xb.tobytes()
+
+
+def test_adamw_against_torch():
+    """torch.optim.AdamW (library): decay first, then the Adam step."""
+    rng = np.random.default_rng(32)
+    n, T, lr, wd = 5000, 10, 1e-2, 0.05
+    x, m, v = _fresh(n, rng, sigma=0.5)
+    p = torch.nn.Parameter(torch.from_numpy(x.copy()))
+    opt = torch.optim.AdamW([p], lr=lr, betas=(0.9, 0.999), eps=1e-8, weight_decay=wd,
+                            foreach=False)
+    for t in range(1, T + 1):
+        g = rng.normal(0, 1e-2, n).astype(np.float32)
+        oracle.adam(x, m, v, g, lr, 0.9, 0.999, 1e-8, t, weight_decay=wd)
+        p.grad = torch.from_numpy(g.copy())
+        opt.step()
+    got, want = x.astype(np.float64), p.detach().numpy().astype(np.float64)
+    assert np.abs(got - want).max() <= 64 * U * T * (lr + np.abs(want).max() * lr * wd)
+    # and the decay is really applied: far from plain Adam's result
+    y, my, vy = _fresh(n, np.random.default_rng(32), sigma=0.5)
+    rng2 = np.random.default_rng(32)
+    _fresh(n, rng2, sigma=0.5)
+    for t in range(1, T + 1):
+        oracle.adam(y, my, vy, rng2.normal(0, 1e-2, n).astype(np.float32), lr, 0.9, 0.999,
+                    1e-8, t)
+    assert np.abs(y - x).max() > 100 * np.abs(got - want).max()
