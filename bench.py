@@ -64,7 +64,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="gpt2_xl",
-                    choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny"])
+                    choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny",
+                             "gpt2_xl_bucketed"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -163,7 +164,26 @@ def step_plan(run):
     bg = 4 if w.grad_dtype == 0 else 2
     bp = 4 if w.param_dtype == 0 else 2
     plan = []
-    if w.stage < 3:
+    if w.stage < 3 and w.bucket:
+        # constant-size bucket buffers, reused for every bucket of the step
+        bufs = run.bucket_buffers
+        ranges = run.bucket_ranges()
+        n_valid_all = w.numel if w.rank < 0 else min(w.shard, max(0, w.numel - w.rank * w.shard))
+
+        def begin_and(fn):
+            return lambda: (z.zero_bucket_begin(run.ctx, run.scale), fn())
+        for i, (off, cnt) in enumerate(ranges):
+            nv = max(0, min(cnt, n_valid_all - off))
+            fn = (lambda off=off, cnt=cnt: z.zero_bucket_step(
+                run.ctx, off, cnt, bufs, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st))
+            plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * cnt,
+                               begin_and(fn) if i == 0 else fn))
+        kernels_end = 1 if (run.shadow is not None or run.scale > 0) else 0
+        plan.append(Launch("finalize_kernel" if run.shadow is not None else "apply_kernel",
+                           0 if run.shadow is not None else (28 + bp) * w.shard * w.world,
+                           lambda: z.zero_bucket_end(run.ctx, w.lr, w.beta1, w.beta2, w.eps,
+                                                     run.t + 1, st), kernels=kernels_end))
+    elif w.stage < 3:
         n_state = w.shard * (w.world if w.rank < 0 else 1)
         n_valid = w.numel if w.rank < 0 else min(w.shard, max(0, w.numel - w.rank * w.shard))
         if run.shadow is not None:
@@ -247,8 +267,19 @@ def bench_ours(args, rank, world_size, device_index):
         w = w.replace(inject=None)    # timed steps are the ones that apply
     torch.cuda.set_device(device_index)
     shadow = w.loss_scale > 0 and w.stage < 3 and not args.two_pass
-    run = Runner(w, device="cuda:%d" % device_index, shadow=shadow)
-    run.fill_grads(1)
+    run = Runner(w, device="cuda:%d" % device_index, shadow=shadow, alloc_grads=not w.bucket)
+    if w.bucket:
+        import synth
+        import torch as _t
+        dt = {0: _t.float32, 1: _t.bfloat16, 2: _t.float16}[w.grad_dtype]
+        run.bucket_buffers = [_t.empty(w.bucket, dtype=dt, device=run.dev)
+                              for _ in range(w.world)]
+        for k, b in enumerate(run.bucket_buffers):
+            synth.fill_device(b.data_ptr(), w.bucket, w.grad_dtype,
+                              synth.key(w.seed, synth.KIND_GRAD, 1, k),
+                              W.grad_sigma(w, run.scale), run.stream.cuda_stream)
+    else:
+        run.fill_grads(1)
     plan = step_plan(run)
     torch.cuda.synchronize()
     for _ in range(args.warmup):
@@ -320,6 +351,7 @@ def bench_ours(args, rank, world_size, device_index):
             "per_kernel_ms": {n: per[n][0] / per[n][1] for n in per},
             "parallelism": "%d simulated data-parallel ranks per GPU; %d GPU replica(s)"
                            % (w.world, world_size),
+            "bucket_elems": w.bucket or None,
             "path": ("single pass over two state sets" if shadow else
                      "two passes with an fp32 scratch" if w.loss_scale > 0 else "single pass"),
         },
@@ -337,7 +369,7 @@ def bench_ours(args, rank, world_size, device_index):
         "gpu_launches": sum(L.kernels for L in plan) * args.steps,
         "clocks": clock_info,
     }
-    if not args.no_e2e:
+    if not args.no_e2e and not w.bucket:
         result["e2e"] = bench_e2e(run, plan, args, world_size)
     if not args.no_cpu_baseline and rank == 0:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
@@ -354,6 +386,8 @@ def working_set(run):
     for row in run.grads:
         for t in row:
             tot += t.numel() * t.element_size()
+    for t in getattr(run, "bucket_buffers", []):
+        tot += t.numel() * t.element_size()
     return tot
 
 
@@ -377,7 +411,7 @@ def bench_e2e(run, plan, args, world_size):
     import torch
     import zero_sharded_optimizer_step_gb300 as z
 
-    dev_bufs = [t for row in run.grads for t in row]
+    dev_bufs = [t for row in run.grads for t in row] or list(getattr(run, "bucket_buffers", []))
     h2d = sum(t.numel() * t.element_size() for t in dev_bufs)
     try:
         avail = int(open("/proc/meminfo").read().split("MemAvailable:")[1].split()[0]) * 1024

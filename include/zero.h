@@ -203,6 +203,15 @@ int zero_bind_shadow(zero_ctx *ctx, float *master_b, float *m_b, float *v_b, uin
  * Always 0 without a second set. */
 int zero_current_state(zero_ctx *ctx, int32_t *which);
 
+/* Decoupled weight decay (AdamW; Loshchilov & Hutter, "Decoupled Weight
+ * Decay Regularization", ICLR 2019 -- "PaddlePaddle ZeRO优化" names AdamW as
+ * the optimizer whose states are sharded).  From the next step on, every
+ * update scales the master weight by fp32(1 - lr*weight_decay) before
+ * subtracting the Adam step:  x = x*(1 - lr*wd) - lr*m_hat/(sqrt(v_hat)+eps).
+ * 0 (the default) is plain Adam.  Returns ZERO_EINVAL for a negative or
+ * non-finite value. */
+int zero_set_weight_decay(zero_ctx *ctx, double weight_decay);
+
 /* ------------------------------------------------------------ the step */
 
 /* One ZeRO step (stages 1, 2) on `stream`.
@@ -238,6 +247,32 @@ int zero_step_reduce(zero_ctx *ctx, const void *const *grads, int32_t n_grads,
  * all-reduce in a multi-process deployment); for stage 3 call it once after
  * every unit's zero3_reduce_unit. */
 int zero_step_apply(zero_ctx *ctx, double lr, double beta1, double beta2, double eps,
+                    int64_t t, void *stream);
+
+/* ------------------------------------------------------- bucketed step */
+
+/* The step one bucket at a time, as ZeRO-2 reduce-scatters gradient buckets
+ * during backward and frees each full bucket at once ("ZeRO 与 FSDP…", 从零
+ * 实现 ZeRO 的 Adam, closing note: real ZeRO-2 reduce-scatters by bucket so
+ * resident grads fall to 1/N).  Here a bucket is a range [offset,
+ * offset+count) of this context's elements (stages 1 and 2; all ranks: the
+ * P-element vector; one rank: its S-element shard), and grads[k] hold only
+ * that range of rank k's grads -- constant-size buffers reused bucket after
+ * bucket.  A step is zero_bucket_begin, bucket calls covering every element
+ * once (any order, any sizes), then zero_bucket_end; the result equals
+ * zero_step's bit for bit.
+ *   - No loss scaling: each bucket is updated in place at once.
+ *   - Loss-scaled with a second state set: each bucket writes the other
+ *     set; zero_bucket_end makes it current or, on overflow, keeps the old.
+ *   - Loss-scaled with g_scratch only: each bucket is reduced into the
+ *     scratch; zero_bucket_end applies Adam to every element, or to none.
+ * Bucket offsets that are multiples of 8 elements keep every access on the
+ * 16-byte vector path. */
+int zero_bucket_begin(zero_ctx *ctx, float loss_scale);
+int zero_bucket_step(zero_ctx *ctx, int64_t offset, int64_t count, const void *const *grads,
+                     int32_t n_grads, double lr, double beta1, double beta2, double eps,
+                     int64_t t, void *stream);
+int zero_bucket_end(zero_ctx *ctx, double lr, double beta1, double beta2, double eps,
                     int64_t t, void *stream);
 
 /* Synchronizes the stream of the context's last step and reads the flag.

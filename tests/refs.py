@@ -120,14 +120,16 @@ class OracleRun:
             if w.rank < 0:
                 grads = host_grads(w, it, self.scale)
                 skipped, _ = oracle.zero_step(grads, w.grad_dtype, w.numel, x, m, v, self.full,
-                                              w.param_dtype, *hp, loss_scale=self.scale)
+                                              w.param_dtype, *hp, loss_scale=self.scale,
+                                              weight_decay=w.weight_decay)
             else:
                 S = w.shard
                 sl = host_slices(w, it, self.scale, w.rank)
                 lp = self.full[w.rank * S:(w.rank + 1) * S].copy()
                 skipped, _ = oracle.zero_rank_step(sl, w.grad_dtype, w.numel, w.rank, x, m, v,
                                                    lp, w.param_dtype, *hp,
-                                                   loss_scale=self.scale)
+                                                   loss_scale=self.scale,
+                                                   weight_decay=w.weight_decay)
                 self.full[w.rank * S:(w.rank + 1) * S] = lp
                 if w.gather_after:
                     shards = [lp if k == w.rank else host_other_shard(w, k)
@@ -147,14 +149,16 @@ class OracleRun:
                     grads = host_grads(w, it, self.scale, u)
                     full = np.zeros(x.size, STORAGE[w.param_dtype])
                     sk, _ = oracle.zero_step(grads, w.grad_dtype, w.units[u], x, m, v, full,
-                                             w.param_dtype, *hp, loss_scale=self.scale)
+                                             w.param_dtype, *hp, loss_scale=self.scale,
+                                             weight_decay=w.weight_decay)
                     lp = full
                 else:
                     sl = host_slices(w, it, self.scale, w.rank, u)
                     lp = self.own[u].copy()
                     sk, _ = oracle.zero_rank_step(sl, w.grad_dtype, w.units[u], w.rank, x, m,
                                                   v, lp, w.param_dtype, *hp,
-                                                  loss_scale=self.scale)
+                                                  loss_scale=self.scale,
+                                                  weight_decay=w.weight_decay)
                 skipped |= sk
                 new_state[u] = [x, m, v]
                 new_own[u] = lp
@@ -202,7 +206,8 @@ def sampled_reference(w: Workload, idx: np.ndarray, iterations, skipped_iters=()
                 bufs.append(b)
             acc = oracle.rank_sum(bufs, w.grad_dtype, idx.size, idx.size)
             g, _ = oracle.average(acc, w.world, scale)
-            oracle.adam(x, m, v, g, w.lr, w.beta1, w.beta2, w.eps, t)
+            oracle.adam(x, m, v, g, w.lr, w.beta1, w.beta2, w.eps, t,
+            weight_decay=w.weight_decay)
         if scale > 0:
             scale, good = oracle.scale_update(scale, skipped, good, w.growth_interval)
     return x, m, v, oracle.cast(x, w.param_dtype)

@@ -426,3 +426,79 @@ def test_shadow_mixed_with_two_pass_steps():
         ref.step(it)
     compare_runner(run, ref, what="mix")
     run.close()
+
+
+# -------------------------------------------------------------------- AdamW
+
+@pytest.mark.parametrize("shadow,scaled,rank", [(False, False, -1), (False, True, -1),
+                                               (True, True, -1), (False, False, 2)])
+def test_adamw_parity(shadow, scaled, rank):
+    """Decoupled weight decay on every path: fused, two-pass, one pass over
+    two state sets, one rank's view -- bit-identical to the oracle."""
+    w = W.Workload("adamw", 777_777, 8, 2, W.BF16, W.BF16, rank=rank, steps=3, lr=1e-3,
+                   weight_decay=0.1, loss_scale=2.0 ** 10 if scaled else 0.0)
+    run, ref = run_both(w, shadow=shadow)
+    compare_runner(run, ref, what="adamw")
+    run.close()
+
+
+def test_adamw_stage3_units():
+    units = [300_001, 77, 123_456]
+    w = W.Workload("adamw3", sum(units), 4, 3, W.F16, W.F16, rank=1, units=units, steps=2,
+                   weight_decay=0.01)
+    run, ref = run_both(w)
+    compare_runner(run, ref, what="adamw3")
+    run.close()
+
+
+def test_weight_decay_argument_checked():
+    import zero_sharded_optimizer_step_gb300 as z
+    c = z.zero_init(10, 2, 2, z.ZERO_F32, z.ZERO_F32, -1)
+    for bad in (-0.1, float("nan"), float("inf")):
+        with pytest.raises(z.ZeroError):
+            z.zero_set_weight_decay(c, bad)
+    z.zero_set_weight_decay(c, 0.0)
+
+
+# ------------------------------------------------------------ bucketed step
+
+@pytest.mark.parametrize("bucket,shadow,scaled,rank", [
+    (100_000, False, False, -1),       # multiples of 8: vector path
+    (99_999, False, False, -1),        # ragged buckets: per-element path
+    (65_536, True, True, -1),          # one pass over two state sets, with a skip
+    (65_536, False, True, -1),         # two passes, with a skip
+    (50_000, False, False, 3),         # one rank's view
+    (10_000_000, True, True, 0),       # a single bucket larger than the shard
+])
+def test_bucketed_step_equals_the_whole_step(bucket, shadow, scaled, rank):
+    w = W.Workload("bk", 654_321, 8, 2, W.F16, W.F16, rank=rank, steps=4, bucket=bucket,
+                   loss_scale=2.0 ** 12 if scaled else 0.0, inject=(2, 5) if scaled else None)
+    if scaled and rank >= 0:
+        e = synth.pick_index(w.seed, w.numel, step=2, rank=5)
+        w = w.replace(rank=e // w.shard)
+    run, ref = run_both(w, shadow=shadow)
+    if scaled:
+        assert ref.skips == [False, True, False, False]
+    compare_runner(run, ref, what="bucketed")
+    run.close()
+
+
+def test_bucket_protocol_errors():
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    w = W.Workload("bkerr", 1000, 4, 2, W.BF16, W.BF16, steps=1)
+    run = Runner(w)
+    g = run.grads[0]
+    with pytest.raises(z.ZeroError):                       # not begun
+        z.zero_bucket_step(run.ctx, 0, 8, g, 1e-3, 0.9, 0.999, 1e-8, 1)
+    z.zero_bucket_begin(run.ctx)
+    with pytest.raises(z.ZeroError):                       # outside the range
+        z.zero_bucket_step(run.ctx, 999, 8, g, 1e-3, 0.9, 0.999, 1e-8, 1)
+    with pytest.raises(z.ZeroError):                       # whole step while open
+        z.zero_step(run.ctx, g, 1e-3, 0.9, 0.999, 1e-8, 1)
+    with pytest.raises(z.ZeroError):                       # twice begun
+        z.zero_bucket_begin(run.ctx)
+    z.zero_bucket_end(run.ctx, 1e-3, 0.9, 0.999, 1e-8, 1)
+    with pytest.raises(z.ZeroError):                       # loss-scaled, no scratch or set
+        z.zero_bucket_begin(run.ctx, 1024.0)
+    run.close()

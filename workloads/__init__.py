@@ -58,12 +58,14 @@ class Workload:
     beta1: float = 0.9
     beta2: float = 0.999
     eps: float = 1e-8
+    weight_decay: float = 0.0            # AdamW's decoupled decay; 0 = Adam
     sigma_grad: float = 1e-3
     sigma_master: float = 0.01
     loss_scale: float = 0.0              # initial scale; 0 = off
     growth_interval: int = 2000
     inject: Optional[Tuple[int, int]] = None   # (iteration, rank): one +inf
     gather_after: bool = False           # place the other ranks' shards too
+    bucket: int = 0                      # > 0: step bucket by bucket (elements per bucket)
     seed: int = 0
 
     @property
@@ -109,7 +111,13 @@ def zero3_llama7b(n_units: int = 32) -> Workload:
                     units=[llama_layer_numel()] * n_units, steps=2)
 
 
-ALL = {"tiny": tiny, "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl,
+def gpt2_xl_bucketed() -> Workload:
+    """GPT-2 XL stepped in 32 Mi-element buckets from constant-size gradient
+    buffers (16 ranks x 64 MiB), the way ZeRO-2 reduce-scatters during backward."""
+    return gpt2_xl().replace(name="gpt2_xl_bucketed", bucket=1 << 25)
+
+
+ALL = {"tiny": tiny, "gpt2_xl_bucketed": gpt2_xl_bucketed, "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl,
        "one_rank_7p5b": one_rank_7p5b, "zero3_llama7b": zero3_llama7b}
 
 

@@ -32,7 +32,7 @@ def inject_index(w: Workload, it: int, rank: int, unit: int = 0) -> int:
 
 class Runner:
     def __init__(self, w: Workload, device: str = "cuda:0", scratch: bool | None = None,
-                 shadow: bool = False):
+                 shadow: bool = False, alloc_grads: bool = True):
         self.w = w
         self.dev = torch.device(device)
         torch.cuda.set_device(self.dev)
@@ -56,13 +56,18 @@ class Runner:
                            torch.zeros(ns, **f32))
             self.cur = torch.zeros(1, dtype=torch.int64, device=self.dev)
             z.zero_bind_shadow(self.ctx, *self.shadow, self.cur)
+        if w.weight_decay:
+            z.zero_set_weight_decay(self.ctx, w.weight_decay)
         self.stream = torch.cuda.current_stream(self.dev)
         self.scale = w.loss_scale
         self.good = 0
         self.t = 0
         self.skips = []
         self._init_state()
-        self._alloc_grads()
+        if alloc_grads:
+            self._alloc_grads()
+        else:
+            self.grads = [[]]     # the caller supplies constant-size bucket buffers
         self._alloc_shards()
 
     # ------------------------------------------------------------ set-up
@@ -173,7 +178,11 @@ class Runner:
         w = self.w
         t = self.t + 1
         st = self.stream
-        if w.stage < 3:
+        if w.stage < 3 and w.bucket:
+            self.launch_buckets(t, grads_override)
+            if self.shards is not None:
+                z.zero_allgather(self.ctx, self.shards, self.params, w.param_dtype, st)
+        elif w.stage < 3:
             g = grads_override if grads_override is not None else self.grads[0]
             z.zero_step(self.ctx, g, w.lr, w.beta1, w.beta2, w.eps, t, self.scale, st)
             if self.shards is not None:
@@ -193,6 +202,26 @@ class Runner:
             if self.scale > 0:
                 z.zero_step_apply(self.ctx, w.lr, w.beta1, w.beta2, w.eps, t, st)
         return t
+
+    def bucket_ranges(self):
+        w = self.w
+        n = w.shard * (w.world if w.rank < 0 else 1)
+        return [(off, min(w.bucket, n - off)) for off in range(0, n, w.bucket)]
+
+    def bucket_grads(self, off, cnt, grads=None):
+        """Rank k's grads for elements [off, off+cnt) of this view: views into
+        the full local grads (or the given constant-size bucket buffers)."""
+        if grads is not None:
+            return grads
+        return [g[min(off, g.numel()):min(off + cnt, g.numel())] for g in self.grads[0]]
+
+    def launch_buckets(self, t, bucket_buffers=None):
+        w, st = self.w, self.stream
+        z.zero_bucket_begin(self.ctx, self.scale)
+        for off, cnt in self.bucket_ranges():
+            z.zero_bucket_step(self.ctx, off, cnt, self.bucket_grads(off, cnt, bucket_buffers),
+                               w.lr, w.beta1, w.beta2, w.eps, t, st)
+        z.zero_bucket_end(self.ctx, w.lr, w.beta1, w.beta2, w.eps, t, st)
 
     def finish_step(self):
         """Read the verdict (synchronizes), advance t and the loss scale."""

@@ -53,11 +53,16 @@ _SIGS = {
     "zero_state_bytes": (_i64, [_ctxp]),
     "zero_bind": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_bind_allreduce_out": (ctypes.c_int, [_ctxp, _vp]),
+    "zero_set_weight_decay": (ctypes.c_int, [_ctxp, _f64]),
     "zero_bind_shadow": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp]),
     "zero_current_state": (ctypes.c_int, [_ctxp, ctypes.POINTER(_i32)]),
     "zero_step": (ctypes.c_int, [_ctxp, _vpp, _i32, _f64, _f64, _f64, _f64, _i64, _f32, _vp]),
     "zero_step_reduce": (ctypes.c_int, [_ctxp, _vpp, _i32, _f32, _vp]),
     "zero_step_apply": (ctypes.c_int, [_ctxp, _f64, _f64, _f64, _f64, _i64, _vp]),
+    "zero_bucket_begin": (ctypes.c_int, [_ctxp, _f32]),
+    "zero_bucket_step": (ctypes.c_int, [_ctxp, _i64, _i64, _vpp, _i32, _f64, _f64, _f64, _f64,
+                                        _i64, _vp]),
+    "zero_bucket_end": (ctypes.c_int, [_ctxp, _f64, _f64, _f64, _f64, _i64, _vp]),
     "zero_step_status": (ctypes.c_int, [_ctxp, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]),
     "zero_step_id": (_u64, [_ctxp]),
     "zero_allgather": (ctypes.c_int, [_ctxp, _vpp, _i32, _vp, _i32, _vp]),
@@ -223,6 +228,10 @@ def zero_current_state(ctx) -> int:
     return int(w.value)
 
 
+def zero_set_weight_decay(ctx, weight_decay: float) -> None:
+    _check(_L.zero_set_weight_decay(_h(ctx), weight_decay))
+
+
 def zero_bind_allreduce_out(ctx, grad_avg) -> None:
     _check(_L.zero_bind_allreduce_out(_h(ctx), _ptr(grad_avg)))
 
@@ -242,6 +251,21 @@ def zero_step_reduce(ctx, grads, loss_scale: float = 0.0, stream=None) -> None:
 def zero_step_apply(ctx, lr: float, beta1: float, beta2: float, eps: float, t: int,
                     stream=None) -> None:
     _check(_L.zero_step_apply(_h(ctx), lr, beta1, beta2, eps, t, _stream(stream)))
+
+
+def zero_bucket_begin(ctx, loss_scale: float = 0.0) -> None:
+    _check(_L.zero_bucket_begin(_h(ctx), loss_scale))
+
+
+def zero_bucket_step(ctx, offset: int, count: int, grads, lr: float, beta1: float, beta2: float,
+                     eps: float, t: int, stream=None) -> None:
+    _check(_L.zero_bucket_step(_h(ctx), offset, count, _ptrs(grads), len(grads), lr, beta1,
+                               beta2, eps, t, _stream(stream)))
+
+
+def zero_bucket_end(ctx, lr: float, beta1: float, beta2: float, eps: float, t: int,
+                    stream=None) -> None:
+    _check(_L.zero_bucket_end(_h(ctx), lr, beta1, beta2, eps, t, _stream(stream)))
 
 
 def zero_step_status(ctx):

@@ -72,8 +72,12 @@ struct zero_ctx {
     bool bound = false;
     int device = -1, sms = 0;
 
+    double weight_decay = 0.0;   // AdamW's decoupled decay; 0 = Adam
+
     uint64_t step_id = 0;
     bool step_scaled = false;
+    bool bucket_open = false;    // between zero_bucket_begin and zero_bucket_end
+    float bucket_scale = 0.0f;
     cudaStream_t last_stream = nullptr;
 };
 
@@ -133,9 +137,12 @@ int check_ptr_array(const void *const *p, int32_t n, int32_t world, int es, bool
     return ZERO_OK;
 }
 
-zgb::AdamScalars adam_scalars(double lr, double b1, double b2, double eps, int64_t t)
+zgb::AdamScalars adam_scalars(double lr, double b1, double b2, double eps, int64_t t,
+                              double weight_decay)
 {
     zgb::AdamScalars s;
+    s.decoupled = weight_decay != 0.0;
+    s.decay = (float)(1.0 - lr * weight_decay);
     s.lr = (float)lr;
     s.b1 = (float)b1;
     s.b2 = (float)b2;
@@ -263,22 +270,31 @@ int do_apply(zero_ctx *c, const Range &r, double lr, double b1, double b2, doubl
 {
     if (r.n == 0) return ZERO_OK;
     StepArgs a = make_args(c, r, nullptr);
-    a.ad = adam_scalars(lr, b1, b2, eps, t);
+    a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
     // an unscaled step never skips: use an id the flag cannot hold
     a.step_id = c->step_scaled ? c->step_id : ~0ull;
     return finish_launch(c, zgb::launch_apply(c->pdt, a, c->sms, s), "apply kernel", s);
 }
 
+int do_finalize(zero_ctx *c, const Range &r, cudaStream_t s)
+{
+    if (r.n == 0 || !c->cur) return ZERO_OK;
+    StepArgs a = make_args(c, r, nullptr);
+    a.step_id = c->step_scaled ? c->step_id : ~0ull;
+    return finish_launch(c, zgb::launch_finalize(c->pdt, a, c->sms, s), "finalize kernel", s);
+}
+
 int do_fused(zero_ctx *c, const Range &r, const void *const *grads, double lr, double b1,
-             double b2, double eps, int64_t t, cudaStream_t s, float loss_scale = 0.0f)
+             double b2, double eps, int64_t t, cudaStream_t s, float loss_scale = 0.0f,
+             bool finalize = true)
 {
     if (r.n == 0) return ZERO_OK;
     StepArgs a = make_args(c, r, grads);
     a.av = average_scalars(c->world, loss_scale);
-    a.ad = adam_scalars(lr, b1, b2, eps, t);
+    a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
     a.step_id = c->step_id;
     int rc = finish_launch(c, zgb::launch_fused_step(c->gdt, c->pdt, a, c->sms, s), "step kernel", s);
-    if (rc || !c->cur) return rc;
+    if (rc || !c->cur || !finalize) return rc;
     // two state sets: the written set becomes current unless the step is
     // loss-scaled and overflowed
     a.step_id = c->step_scaled ? c->step_id : ~0ull;
@@ -524,6 +540,15 @@ int zero_current_state(zero_ctx *c, int32_t *which)
     return ZERO_OK;
 }
 
+int zero_set_weight_decay(zero_ctx *c, double weight_decay)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (!(weight_decay >= 0.0) || weight_decay > 1e6)
+        return fail(ZERO_EINVAL, "weight_decay must be a finite value >= 0");
+    c->weight_decay = weight_decay;
+    return ZERO_OK;
+}
+
 int zero_bind_allreduce_out(zero_ctx *c, void *grad_avg)
 {
     if (!c) return fail(ZERO_EINVAL, "null context");
@@ -540,6 +565,7 @@ int zero_step_reduce(zero_ctx *c, const void *const *grads, int32_t n_grads, flo
     int rc = check_ready(c);
     if (rc) return rc;
     if (c->stage == 3) return fail(ZERO_EINVAL, "stage 3 reduces per unit (zero3_reduce_unit)");
+    if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
     if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
     const Range r = vector_range(c);
     rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
@@ -567,6 +593,7 @@ int zero_step(zero_ctx *c, const void *const *grads, int32_t n_grads, double lr,
     if (rc) return rc;
     if ((rc = check_hyper(t))) return rc;
     if (c->stage == 3) return fail(ZERO_EINVAL, "stage 3 steps per unit (zero3_step_unit)");
+    if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
     const Range r = vector_range(c);
     rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
     if (rc) return rc;
@@ -588,6 +615,63 @@ int zero_step(zero_ctx *c, const void *const *grads, int32_t n_grads, double lr,
     c->step_id += 1;
     c->step_scaled = false;
     return do_fused(c, r, grads, lr, b1, b2, eps, t, s);
+}
+
+int zero_bucket_begin(zero_ctx *c, float loss_scale)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (c->stage == 3) return fail(ZERO_EINVAL, "buckets cover the flat vector of stages 1 and 2");
+    if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is already open");
+    if (loss_scale > 0.0f && !c->cur && !c->g)
+        return fail(ZERO_ESTATE, "a loss-scaled bucketed step needs g_scratch or a second state set");
+    c->step_id += 1;
+    c->step_scaled = loss_scale > 0.0f;
+    c->bucket_scale = loss_scale;
+    c->bucket_open = true;
+    return ZERO_OK;
+}
+
+int zero_bucket_step(zero_ctx *c, int64_t offset, int64_t count, const void *const *grads,
+                     int32_t n_grads, double lr, double b1, double b2, double eps, int64_t t,
+                     void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if (!c->bucket_open) return fail(ZERO_ESTATE, "call zero_bucket_begin first");
+    if ((rc = check_hyper(t))) return rc;
+    const Range whole = vector_range(c);
+    if (offset < 0 || count < 0 || offset > whole.n || count > whole.n - offset)
+        return fail(ZERO_EINVAL, "bucket [%lld, %lld) outside the range of %lld elements",
+                    (long long)offset, (long long)(offset + count), (long long)whole.n);
+    Range r;
+    r.state_off = whole.state_off + offset;
+    r.n = count;
+    r.n_valid = std::max<int64_t>(0, std::min<int64_t>(count, whole.n_valid - offset));
+    r.params = whole.params + offset * zgb::elem_size(c->pdt);
+    r.grad_avg = whole.grad_avg ? whole.grad_avg + offset * zgb::elem_size(c->gdt) : nullptr;
+    rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (c->cur)              // one pass into the other set; finalized by zero_bucket_end
+        return do_fused(c, r, grads, lr, b1, b2, eps, t, s, c->bucket_scale, false);
+    if (c->step_scaled)      // first pass only; zero_bucket_end applies
+        return do_reduce(c, r, grads, c->bucket_scale, s);
+    return do_fused(c, r, grads, lr, b1, b2, eps, t, s);
+}
+
+int zero_bucket_end(zero_ctx *c, double lr, double b1, double b2, double eps, int64_t t,
+                    void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if (!c->bucket_open) return fail(ZERO_ESTATE, "no bucketed step is open");
+    if ((rc = check_hyper(t))) return rc;
+    c->bucket_open = false;
+    cudaStream_t s = (cudaStream_t)stream;
+    const Range whole = vector_range(c);
+    if (c->cur) return do_finalize(c, whole, s);
+    if (c->step_scaled) return do_apply(c, whole, lr, b1, b2, eps, t, s);
+    return ZERO_OK;
 }
 
 int zero_step_status(zero_ctx *c, int32_t *nonfinite, int32_t *skipped)
@@ -765,7 +849,7 @@ extern "C" int zero_step_noalloc(zero_ctx *c, const void *const *grads, int32_t 
     a.step_id = c->step_id;
     rc = finish_launch(c, zgb::launch_reduce(c->gdt, a, c->sms, s), "reduce kernel", s);
     if (rc) return rc;
-    a.ad = adam_scalars(lr, b1, b2, eps, t);
+    a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
     a.step_id = c->step_scaled ? c->step_id : ~0ull;
     return finish_launch(c, zgb::launch_apply(c->pdt, a, c->sms, s), "apply kernel", s);
 }

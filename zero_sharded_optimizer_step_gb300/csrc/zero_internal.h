@@ -17,6 +17,8 @@ inline int elem_size(int32_t dt) { return dt == F32 ? 4 : 2; }
 // fp32 scalars of one Adam step, each rounded once from a double.
 struct AdamScalars {
     float lr, b1, b2, c1, c2, bc1, bc2, eps;
+    float decay;        // 1 - lr * weight_decay (AdamW), used when decoupled != 0
+    int32_t decoupled;
 };
 
 // How the rank sum becomes the gradient: g = acc / world, then / loss_scale.

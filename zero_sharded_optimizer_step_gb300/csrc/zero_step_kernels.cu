@@ -188,7 +188,9 @@ __device__ __forceinline__ float average(float acc, const AverageScalars &s)
     return g;
 }
 
-// One element of Adam with bias correction, eps outside the root.
+// One element of Adam with bias correction, eps outside the root; with
+// decoupled weight decay (AdamW) the weight is scaled before the step is
+// subtracted.
 __device__ __forceinline__ void adam1(float g, float &x, float &m, float &v, const AdamScalars &s)
 {
     const float mj = __fadd_rn(__fmul_rn(m, s.b1), __fmul_rn(s.c1, g));
@@ -199,7 +201,8 @@ __device__ __forceinline__ void adam1(float g, float &x, float &m, float &v, con
     const float upd = __fdiv_rn(__fmul_rn(s.lr, mh), den);
     m = mj;
     v = vj;
-    x = __fsub_rn(x, upd);
+    const float xd = s.decoupled ? __fmul_rn(x, s.decay) : x;
+    x = __fsub_rn(xd, upd);
 }
 
 // Rank-order sum of 8 consecutive elements at vector index k of every rank
