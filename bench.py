@@ -65,7 +65,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="gpt2_xl",
                     choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny",
-                             "gpt2_xl_bucketed"])
+                             "gpt2_xl_bucketed", "zero3_prefetch"])
+    ap.add_argument("--unit-fwd-ms", type=float, default=0.25,
+                    help="zero3_prefetch: stand-in forward compute per unit (backward = 2x)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -377,6 +379,75 @@ def bench_ours(args, rank, world_size, device_index):
     return result
 
 
+def bench_prefetch(args, rank, world_size, device_index):
+    """ZeRO-3 with the next unit's gather prefetched on a second stream while
+    a stand-in kernel plays the unit's compute: how much gather time stays
+    exposed.  Three schedules over the same workload: compute only (no
+    gathers), serial (gather, then compute, one stream), overlapped."""
+    import torch
+
+    import workloads as W
+    from workloads import standin
+    from workloads.runner import Runner
+    from workloads.zero3_schedule import Zero3Schedule
+
+    w = W.zero3_llama7b().replace(name="zero3_prefetch")
+    torch.cuda.set_device(device_index)
+    run = Runner(w, device="cuda:%d" % device_index)
+    run.fill_grads(1)
+    sms = torch.cuda.get_device_properties(device_index).multi_processor_count
+    blocks = 2 * sms
+    sink = torch.empty(blocks * 128, device=run.dev)
+    # calibrate the stand-in's iterations to the requested duration
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    probe = 200_000
+    for _ in range(2):
+        e0.record(run.stream)
+        standin.busy(sink.data_ptr(), blocks, probe, run.stream.cuda_stream)
+        e1.record(run.stream)
+        torch.cuda.synchronize()
+    per_iter = e0.elapsed_time(e1) / probe
+    it_f = max(1, int(args.unit_fwd_ms / per_iter))
+    times = {}
+    for mode in ("compute_only", "serial", "overlap"):
+        sch = Zero3Schedule(run, it_f, 2 * it_f, blocks, mode)
+        for _ in range(args.warmup):
+            sch.launch_step()
+        torch.cuda.synchronize()
+        barrier(world_size)
+        e0.record(run.stream)
+        for _ in range(args.steps):
+            sch.launch_step()
+        e1.record(run.stream)
+        torch.cuda.synchronize()
+        times[mode] = allreduce_max(e0.elapsed_time(e1) / args.steps, world_size)
+    exposed = times["overlap"] - times["compute_only"]
+    gathers = times["serial"] - times["compute_only"]
+    updated = w.updated_per_step()
+    run.close()
+    peak, peak_kind = peaks()
+    U = len(w.units)
+    return {
+        "metric": METRIC, "value": updated * world_size / (times["overlap"] * 1e-3),
+        "unit": "params/s", "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": times["overlap"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 grads, f32 state",
+        "data": "synthetic (seeded draws; a stand-in kernel plays each unit's compute)",
+        "config": {
+            "workload": describe(w) + " + stand-in compute %.3f ms fwd / %.3f ms bwd per unit"
+                        % (args.unit_fwd_ms, 2 * args.unit_fwd_ms),
+            "compute_only_ms": times["compute_only"], "serial_ms": times["serial"],
+            "overlap_ms": times["overlap"], "gather_time_serial_ms": gathers,
+            "exposed_gather_ms": exposed,
+            "hidden_fraction": (1 - exposed / gathers) if gathers > 0 else None,
+            "gathers_per_step": 2 * U, "standin_blocks": blocks,
+        },
+        "roofline": None,
+        "gpu_launches": (2 * U + 2 * U + U) * args.steps,
+        "clocks": None,
+    }
+
+
 def working_set(run):
     tot = 0
     for t in [run.master, run.m, run.v, run.params, run.g, run.unit_full,
@@ -580,7 +651,10 @@ def main():
         import __graft_entry__
         __graft_entry__.build() if rank == 0 else None
         barrier(world_size)
-        res = bench_ours(args, rank, world_size, local)
+        if args.workload == "zero3_prefetch":
+            res = bench_prefetch(args, rank, world_size, local)
+        else:
+            res = bench_ours(args, rank, world_size, local)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world_size > 1:

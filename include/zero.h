@@ -88,6 +88,11 @@ enum zero_code {
 
 #define ZERO_MAX_RANKS 256
 
+enum zero_gather_mode {
+    ZERO_GATHER_FAST = 0,  /* all SMs, many blocks: the fastest placement on an idle GPU */
+    ZERO_GATHER_LEAN = 1   /* bulk-copy (TMA) engine, one warp per SM: placement beside compute */
+};
+
 /* ------------------------------------------------------------ host only */
 
 /* Shard length S = ceil(numel / world) ("ZeRO 与 FSDP…", 从零实现 ZeRO 的
@@ -275,7 +280,8 @@ int zero_bucket_step(zero_ctx *ctx, int64_t offset, int64_t count, const void *c
 int zero_bucket_end(zero_ctx *ctx, double lr, double beta1, double beta2, double eps,
                     int64_t t, void *stream);
 
-/* Synchronizes the stream of the context's last step and reads the flag.
+/* Synchronizes the stream of the context's last step launch (gathers do not
+ * count: they never touch the flag) and reads the flag.
  * *nonfinite (may be NULL) = 1 if the step saw an inf/nan; *skipped (may be
  * NULL) = 1 if the step was loss-scaled and therefore skipped.  Returns
  * ZERO_SKIPPED when skipped, ZERO_OK otherwise, < 0 on error. */
@@ -294,6 +300,25 @@ uint64_t zero_step_id(const zero_ctx *ctx);
  * have any element-aligned addresses. */
 int zero_allgather(zero_ctx *ctx, const void *const *shards, int32_t n_shards,
                    void *full, int32_t dtype, void *stream);
+
+/* How this context's gathers (zero_allgather, zero3_gather_unit) run.
+ * ZERO_GATHER_FAST (default) fills every SM with copy blocks -- the fastest
+ * placement when nothing else runs, but blocks queued first hold the SMs, so
+ * a compute kernel launched after it waits.  ZERO_GATHER_LEAN drives the
+ * SMs' bulk-copy (TMA) units from one warp per SM through a 128 KB shared
+ * ring: nearly as fast alone, and it leaves the SMs' threads and registers to
+ * kernels running at the same time -- the ZeRO-3 prefetch of the next unit
+ * while this one computes ("ZeRO 与 FSDP…", ZeRO-3 与 FSDP: prefetch hides the
+ * all-gather behind the computation).  LEAN needs 16-byte aligned shards and
+ * destinations and a shard length that is a multiple of 16 bytes; other
+ * gathers fall back to FAST.  Its waits are bounded: see
+ * zero_gather_timeouts. */
+int zero_set_gather_mode(zero_ctx *ctx, int32_t mode);
+
+/* Number of lean-gather waits that ran out in this process (each one drains
+ * its copies in flight and abandons the rest of that gather; the result is
+ * then incomplete).  0 in normal operation. */
+int zero_gather_timeouts(uint32_t *count);
 
 /* ------------------------------------------------------------- stage 3 */
 

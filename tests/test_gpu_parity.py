@@ -502,3 +502,66 @@ def test_bucket_protocol_errors():
     with pytest.raises(z.ZeroError):                       # loss-scaled, no scratch or set
         z.zero_bucket_begin(run.ctx, 1024.0)
     run.close()
+
+
+# --------------------------------------------------- ZeRO-3 with prefetch
+
+def test_zero3_prefetch_schedule_matches_serial_and_oracle():
+    """Gathers prefetched on a second stream into alternating unit buffers
+    leave every result as the serial schedule and the oracle have it."""
+    from workloads.runner import Runner
+    from workloads.zero3_schedule import Zero3Schedule
+    units = [200_003, 150_000, 99_999, 250_000]
+    w = W.Workload("z3p", sum(units), 4, 3, W.BF16, W.BF16, rank=2, units=units, steps=3)
+    runs = {}
+    for mode in ("serial", "overlap"):
+        run = Runner(w)
+        sch = Zero3Schedule(run, 2000, 4000, 64, mode)
+        for it in range(1, 4):
+            run.fill_grads(it)
+            sch.launch_step()
+        torch.cuda.synchronize()
+        runs[mode] = run
+    ref = refs.OracleRun(w)
+    for it in range(1, 4):
+        ref.step(it)
+    for a, b in [(runs["serial"].master, runs["overlap"].master),
+                 (runs["serial"].params, runs["overlap"].params)]:
+        assert torch.equal(a, b)
+    runs["overlap"].skips = ref.skips
+    compare_runner(runs["overlap"], ref, what="prefetch")
+
+
+@pytest.mark.parametrize("S,world,dtype,src_off,dst_off", [
+    (25_297_920, 8, W.BF16, 0, 0),      # one Llama-7B unit: the TMA path
+    (16384 + 8, 5, W.F16, 0, 0),        # ragged last tile (shard of 32,784 bytes)
+    (4096, 3, W.F32, 0, 0),
+    (1001, 8, W.BF16, 0, 0),            # 2,002-byte shards: not 16-byte multiples -> fallback
+    (250_000, 4, W.BF16, 1, 0),         # unaligned sources -> fallback
+])
+def test_lean_gather_placement(S, world, dtype, src_off, dst_off):
+    """The bulk-copy (lean) gather places bit-exactly; gathers it cannot take
+    fall back to the SM kernel; no wait runs out."""
+    import zero_sharded_optimizer_step_gb300 as z
+    dev = torch.device("cuda:0")
+    tdt = {W.F32: torch.float32, W.BF16: torch.bfloat16, W.F16: torch.float16}[dtype]
+    before = z.zero_gather_timeouts()
+    ctx = z.zero_init(S * world, world, 3, dtype, dtype, 0, [S * world])
+    z.zero_set_gather_mode(ctx, z.ZERO_GATHER_LEAN)
+    hs = [synth.fill_host(S, dtype, synth.key(9, W.KIND_SHARD, 0, k), 1.0) for k in range(world)]
+    shards = []
+    for h in hs:
+        buf = torch.zeros(S + 16, dtype=tdt, device=dev)[src_off:src_off + S]
+        src = torch.from_numpy(h.view(np.int16) if dtype != W.F32 else h)
+        buf.copy_(src.view(tdt) if dtype != W.F32 else src)
+        shards.append(buf)
+    full = torch.zeros(S * world + 16, dtype=tdt, device=dev)[dst_off:dst_off + S * world]
+    st = torch.zeros(S, device=dev)
+    flag = torch.zeros(1, dtype=torch.int64, device=dev)
+    z.zero_bind(ctx, st, st, st, torch.zeros(S, dtype=tdt, device=dev), None, flag)
+    z.zero3_begin_step(ctx)
+    for _ in range(2):
+        z.zero3_gather_unit(ctx, 0, shards, full)
+    torch.cuda.synchronize()
+    assert to_np(full).tobytes() == oracle.all_gather(hs, dtype).tobytes()
+    assert z.zero_gather_timeouts() == before

@@ -1,0 +1,83 @@
+"""The ZeRO-3 step with the next unit's gather prefetched on a second stream
+("ZeRO 与 FSDP：切分优化器状态、梯度与参数", section ZeRO-3 与 FSDP: while
+unit i computes, all-gather unit i+1, so the communication hides behind the
+computation).  The model's own compute is played by a stand-in kernel
+(workloads/standin.cu) of a set duration per unit visit.
+
+Visits: forward over units 0..U-1, then backward over U-1..0, each backward
+visit followed by that unit's reduce + Adam.  Two unit buffers alternate:
+the gather for visit v+1 writes the buffer visit v-1 used, so it waits for
+visit v-1's compute to finish.
+"""
+from __future__ import annotations
+
+import torch
+
+import zero_sharded_optimizer_step_gb300 as z
+
+from . import standin
+
+
+class Zero3Schedule:
+    def __init__(self, run, iters_fwd: int, iters_bwd: int, busy_blocks: int,
+                 mode: str = "overlap"):
+        assert run.w.stage == 3 and mode in ("overlap", "serial", "compute_only")
+        self.run, self.mode = run, mode
+        self.iters = {"f": iters_fwd, "b": iters_bwd}
+        self.blocks = busy_blocks
+        self.sink = torch.empty(busy_blocks * 128, device=run.dev)
+        self.bufs = [run.unit_full, torch.empty_like(run.unit_full)]
+        # prefetches run in the background: the lean (bulk-copy) gather leaves
+        # the SMs to the compute, which gets the higher stream priority
+        self.gs = torch.cuda.Stream(run.dev, priority=0)
+        self.cs = torch.cuda.Stream(run.dev, priority=-1)
+        z.zero_set_gather_mode(run.ctx, z.ZERO_GATHER_LEAN if mode == "overlap"
+                               else z.ZERO_GATHER_FAST)
+        U = len(run.w.units)
+        self.visits = [(u, "f") for u in range(U)] + [(u, "b") for u in reversed(range(U))]
+        n = len(self.visits)
+        self.ready = [torch.cuda.Event() for _ in range(n)]
+        self.used = [torch.cuda.Event() for _ in range(n)]
+
+    def _gather(self, v, stream):
+        u, _ = self.visits[v]
+        z.zero3_gather_unit(self.run.ctx, u, self.run.shards[u], self.bufs[v % 2], stream)
+
+    def _compute(self, v, stream):
+        u, phase = self.visits[v]
+        standin.busy(self.sink.data_ptr(), self.blocks, self.iters[phase], stream.cuda_stream)
+        if phase == "b":
+            w = self.run.w
+            z.zero3_step_unit(self.run.ctx, u, self.run.grads[u], w.lr, w.beta1, w.beta2,
+                              w.eps, self.run.t + 1, stream)
+
+    def launch_step(self):
+        """Launch one whole step (no synchronization)."""
+        run = self.run
+        cs = self.cs if self.mode == "overlap" else run.stream
+        if cs is not run.stream:
+            cs.wait_stream(run.stream)
+        z.zero3_begin_step(run.ctx)
+        n = len(self.visits)
+        if self.mode != "overlap":
+            for v in range(n):
+                if self.mode == "serial":
+                    self._gather(v, cs)
+                self._compute(v, cs)
+        else:
+            gs = self.gs
+            gs.wait_stream(cs)            # the shards the last step wrote
+            self._gather(0, gs)
+            self.ready[0].record(gs)
+            for v in range(n):
+                cs.wait_event(self.ready[v])
+                self._compute(v, cs)
+                self.used[v].record(cs)
+                if v + 1 < n:
+                    if v >= 1:
+                        gs.wait_event(self.used[v - 1])   # its buffer is free again
+                    self._gather(v + 1, gs)
+                    self.ready[v + 1].record(gs)
+            cs.wait_stream(gs)
+            run.stream.wait_stream(cs)
+        run.t += 1

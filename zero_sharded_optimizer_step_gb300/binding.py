@@ -17,6 +17,7 @@ ZERO_F32, ZERO_BF16, ZERO_F16 = 0, 1, 2
 ZERO_OK, ZERO_SKIPPED = 0, 1
 ZERO_EINVAL, ZERO_ECUDA, ZERO_EALIGN, ZERO_ESTATE = -1, -2, -3, -4
 ZERO_MAX_RANKS = 256
+ZERO_GATHER_FAST, ZERO_GATHER_LEAN = 0, 1
 
 
 class ZeroError(RuntimeError):
@@ -54,6 +55,8 @@ _SIGS = {
     "zero_bind": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_bind_allreduce_out": (ctypes.c_int, [_ctxp, _vp]),
     "zero_set_weight_decay": (ctypes.c_int, [_ctxp, _f64]),
+    "zero_set_gather_mode": (ctypes.c_int, [_ctxp, _i32]),
+    "zero_gather_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "zero_bind_shadow": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp]),
     "zero_current_state": (ctypes.c_int, [_ctxp, ctypes.POINTER(_i32)]),
     "zero_step": (ctypes.c_int, [_ctxp, _vpp, _i32, _f64, _f64, _f64, _f64, _i64, _f32, _vp]),
@@ -226,6 +229,16 @@ def zero_current_state(ctx) -> int:
     w = _i32(0)
     _check(_L.zero_current_state(_h(ctx), ctypes.byref(w)))
     return int(w.value)
+
+
+def zero_set_gather_mode(ctx, mode: int) -> None:
+    _check(_L.zero_set_gather_mode(_h(ctx), mode))
+
+
+def zero_gather_timeouts() -> int:
+    c = ctypes.c_uint32(0)
+    _check(_L.zero_gather_timeouts(ctypes.byref(c)))
+    return int(c.value)
 
 
 def zero_set_weight_decay(ctx, weight_decay: float) -> None:

@@ -73,6 +73,7 @@ struct zero_ctx {
     int device = -1, sms = 0;
 
     double weight_decay = 0.0;   // AdamW's decoupled decay; 0 = Adam
+    int32_t gather_mode = 0;     // ZERO_GATHER_FAST or ZERO_GATHER_LEAN
 
     uint64_t step_id = 0;
     bool step_scaled = false;
@@ -540,6 +541,25 @@ int zero_current_state(zero_ctx *c, int32_t *which)
     return ZERO_OK;
 }
 
+int zero_set_gather_mode(zero_ctx *c, int32_t mode)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (mode != ZERO_GATHER_FAST && mode != ZERO_GATHER_LEAN)
+        return fail(ZERO_EINVAL, "unknown gather mode %d", mode);
+    c->gather_mode = mode;
+    return ZERO_OK;
+}
+
+int zero_gather_timeouts(uint32_t *count)
+{
+    if (!count) return fail(ZERO_EINVAL, "null argument");
+    unsigned int h = 0;
+    cudaError_t e = zgb::lean_gather_timeouts(&h);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the gather timeout counter");
+    *count = h;
+    return ZERO_OK;
+}
+
 int zero_set_weight_decay(zero_ctx *c, double weight_decay)
 {
     if (!c) return fail(ZERO_EINVAL, "null context");
@@ -708,7 +728,12 @@ static int gather(zero_ctx *c, const void *const *shards, int32_t n, void *full,
     a.shard_bytes = S * es;
     a.n = n;
     a.es = es;
-    return finish_launch(c, zgb::launch_gather(a, c->sms, s), "gather kernel", s);
+    // a gather neither reads nor writes the flag: it does not become the
+    // stream zero_step_status waits on
+    const cudaError_t e = (c->gather_mode == ZERO_GATHER_LEAN && zgb::lean_gather_eligible(a))
+                              ? zgb::launch_gather_lean(a, c->sms, s)
+                              : zgb::launch_gather(a, c->sms, s);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "gather kernel");
 }
 
 int zero_allgather(zero_ctx *c, const void *const *shards, int32_t n_shards, void *full,

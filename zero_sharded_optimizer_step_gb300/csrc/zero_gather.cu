@@ -11,6 +11,8 @@
 // body with 16-byte loads, and writes each 16 bytes with the widest store
 // the destination's alignment allows (one 16-byte store, or two of 8, four
 // of 4, eight of 2); the last partial 16 bytes go element by element.
+#include <cstring>
+
 #include "zero_internal.h"
 
 namespace zgb {
@@ -93,6 +95,134 @@ gather_kernel(const __grid_constant__ GatherArgs a)
     for (; c < nchunks; c += T) st_any(d + (c << 4), ld_stream(s + (c << 4)), align);
 }
 
+
+// ------------------------------------------------------------ lean gather
+//
+// The same placement driven by the SM's bulk-copy (TMA) unit: one warp per
+// CTA, one CTA per SM, 1-D cp.async.bulk copies of up to 32 KB global ->
+// shared -> global through a 4-stage ring (128 KB of shared memory), with
+// completion of each load signalled on an mbarrier.  Lane 0 issues
+// everything; the CTA holds 32 threads and few registers, so kernels running
+// concurrently (the next unit's compute during a ZeRO-3 prefetch) keep
+// almost all of every SM.  Tiles are numbered row-major over all placed
+// shards and dealt round-robin to the CTAs, so the GPU sweeps one compact
+// window of one shard at a time.  Needs 16-byte aligned sources and
+// destinations and a shard length that is a multiple of 16 bytes.
+//
+// Every wait is bounded: a load that has not completed after kWaitPolls
+// polls counts a timeout in g_gather_timeouts, stops issuing, drains what is
+// in flight (again with bounded waits) and returns.
+
+constexpr int kTmaTile = 32768;
+constexpr int kTmaStages = 4;
+constexpr long long kWaitPolls = 1ll << 22;
+
+__device__ unsigned int g_gather_timeouts;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    for (long long i = 0; i < kWaitPolls; ++i) {
+        uint32_t done;
+        asm volatile("{\n .reg .pred p;\n"
+                     " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                     " selp.u32 %0, 1, 0, p;\n}"
+                     : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tma_load(uint32_t dst_smem, const char *src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1], %2, [%3];"
+                 :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tma_store(char *dst, uint32_t src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst), "r"(src_smem), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+struct LeanArgs {
+    const char *src[kMaxRanks];   // active rows only
+    char *dst[kMaxRanks];
+    int32_t rows;
+    int64_t row_bytes;            // multiple of 16
+    int64_t tiles_per_row;
+};
+
+__global__ void __launch_bounds__(32)
+lean_gather_kernel(const __grid_constant__ LeanArgs a)
+{
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t bars[kTmaStages];
+    if (threadIdx.x != 0) return;
+    const uint32_t ring0 = smem_addr(ring);
+    for (int s = 0; s < kTmaStages; ++s)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_addr(&bars[s])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+    const int64_t total = (int64_t)a.rows * a.tiles_per_row;
+    const int64_t G = gridDim.x;
+    auto tile_of = [&](int64_t m, const char *&src, char *&dst, uint32_t &bytes) -> bool {
+        const int64_t t = blockIdx.x + m * G;
+        if (t >= total) return false;
+        const int64_t r = t / a.tiles_per_row, j = t - r * a.tiles_per_row;
+        const int64_t off = j * kTmaTile;
+        const int64_t left = a.row_bytes - off;
+        bytes = (uint32_t)(left < kTmaTile ? left : kTmaTile);
+        src = a.src[r] + off;
+        dst = a.dst[r] + off;
+        return true;
+    };
+
+    int64_t issued = 0;   // loads issued (tiles m = 0 .. issued-1)
+    for (; issued < kTmaStages; ++issued) {
+        const char *src; char *dst; uint32_t bytes;
+        if (!tile_of(issued, src, dst, bytes)) break;
+        tma_load(ring0 + (uint32_t)(issued * kTmaTile), src, bytes,
+                 smem_addr(&bars[issued % kTmaStages]));
+    }
+    bool ok = true;
+    int64_t m = 0;
+    for (; m < issued; ++m) {
+        const int s = (int)(m % kTmaStages);
+        const uint32_t parity = (uint32_t)((m / kTmaStages) & 1);
+        if (!mbar_wait(smem_addr(&bars[s]), parity)) { ok = false; break; }
+        const char *src; char *dst; uint32_t bytes;
+        tile_of(m, src, dst, bytes);
+        tma_store(dst, ring0 + (uint32_t)(s * kTmaTile), bytes);
+        // the buffer may take the next load once this store has read it
+        const char *nsrc; char *ndst; uint32_t nbytes;
+        if (tile_of(issued, nsrc, ndst, nbytes)) {
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            tma_load(ring0 + (uint32_t)(s * kTmaTile), nsrc, nbytes, smem_addr(&bars[s]));
+            ++issued;
+        }
+    }
+    if (!ok) {
+        atomicAdd(&g_gather_timeouts, 1u);
+        // drain: every load still in flight must land before the ring goes away
+        for (int64_t k = m; k < issued; ++k) {     // tile m's own load included
+            const int s = (int)(k % kTmaStages);
+            if (!mbar_wait(smem_addr(&bars[s]), (uint32_t)((k / kTmaStages) & 1)))
+                atomicAdd(&g_gather_timeouts, 1u);
+        }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 }  // namespace
 
 cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s)
@@ -113,6 +243,53 @@ cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s)
     dim3 grid((unsigned)bx, (unsigned)a.n);
     gather_kernel<<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+bool lean_gather_eligible(const GatherArgs &a)
+{
+    if (a.shard_bytes % 16) return false;
+    for (int32_t k = 0; k < a.n; ++k) {
+        if (!a.src[k]) continue;
+        if (((uintptr_t)a.src[k] & 15) || ((uintptr_t)(a.dst + (int64_t)k * a.shard_bytes) & 15))
+            return false;
+    }
+    return true;
+}
+
+cudaError_t launch_gather_lean(const GatherArgs &a, int sms, cudaStream_t s)
+{
+    if (a.n <= 0 || a.shard_bytes <= 0) return cudaSuccess;
+    if (!lean_gather_eligible(a)) return cudaErrorInvalidValue;
+    LeanArgs l;
+    memset(&l, 0, sizeof l);
+    for (int32_t k = 0; k < a.n; ++k) {
+        if (!a.src[k]) continue;
+        l.src[l.rows] = static_cast<const char *>(a.src[k]);
+        l.dst[l.rows] = a.dst + (int64_t)k * a.shard_bytes;
+        ++l.rows;
+    }
+    if (l.rows == 0) return cudaSuccess;
+    l.row_bytes = a.shard_bytes;
+    l.tiles_per_row = (a.shard_bytes + kTmaTile - 1) / kTmaTile;
+    const int smem = kTmaStages * kTmaTile;
+    static int attr_device = -1;   // the attribute is per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(lean_gather_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_device = dev;
+    }
+    const int64_t total = (int64_t)l.rows * l.tiles_per_row;
+    const int blocks = (int)(total < sms ? total : sms);
+    lean_gather_kernel<<<blocks, 32, smem, s>>>(l);
+    return cudaGetLastError();
+}
+
+cudaError_t lean_gather_timeouts(unsigned int *count)
+{
+    return cudaMemcpyFromSymbol(count, g_gather_timeouts, sizeof(unsigned int));
 }
 
 }  // namespace zgb

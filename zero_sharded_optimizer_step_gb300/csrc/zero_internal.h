@@ -77,5 +77,12 @@ cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s
 // from it.
 cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s);
+// The bulk-copy (TMA) placement for 16-byte aligned shards: one warp per SM,
+// for gathers that run beside other kernels.  cudaErrorInvalidValue when the
+// shards are not eligible (lean_gather_eligible).
+bool lean_gather_eligible(const GatherArgs &a);
+cudaError_t launch_gather_lean(const GatherArgs &a, int sms, cudaStream_t s);
+// Waits of the lean gather that ran out (cumulative, this process).
+cudaError_t lean_gather_timeouts(unsigned int *count);
 
 }  // namespace zgb
