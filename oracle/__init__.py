@@ -74,6 +74,12 @@ def lib() -> ctypes.CDLL:
                                                       vp, i32, f64, f64, f64, f64, i64, f32,
                                                       i64, fp, i64p, f64]),
                 "orc_scale_update": (f32, [f32, i32, i64p, i64]),
+                "orc_row_shard_size": (i64, [i64, i64, i32]),
+                "orc_zero_step_s": (ctypes.c_int, [vpp, i32, i64, i32, i64, fp, fp, fp, vp, i32,
+                                                   f64, f64, f64, f64, i64, f32, fp, i64p, f64]),
+                "orc_zero_rank_step_s": (ctypes.c_int, [vpp, i32, i64, i32, i64, i32, fp, fp, fp,
+                                                        vp, i32, f64, f64, f64, f64, i64, f32,
+                                                        i64, fp, i64p, f64]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -197,23 +203,30 @@ def adam(x, m, v, g, lr, beta1, beta2, eps, t, weight_decay=0.0):
                    lr, beta1, beta2, eps, t, weight_decay)
 
 
+def row_shard_size(rows: int, row_elems: int, world: int) -> int:
+    """Shard length of FSDP2's dim-0 layout: ceil(rows/world) whole rows."""
+    return int(lib().orc_row_shard_size(rows, row_elems, world))
+
+
 def zero_step(grads, grad_dtype, numel, master, m, v, full, param_dtype,
-              lr, beta1, beta2, eps, t, loss_scale=0.0, weight_decay=0.0):
-    """All-ranks ZeRO-2 step, in place.  Returns (skipped, n_nonfinite)."""
+              lr, beta1, beta2, eps, t, loss_scale=0.0, weight_decay=0.0, shard=None):
+    """All-ranks ZeRO-2 step, in place.  Returns (skipped, n_nonfinite).
+    `shard` overrides the shard length ceil(numel/N) (the dim-0 layout)."""
     world = len(grads)
     for g in grads:
         _check(g, grad_dtype)
         assert g.size >= numel
-    P = shard_size(numel, world) * world
+    S = shard_size(numel, world) if shard is None else shard
+    P = S * world
     for a in (master, m, v):
         assert a.dtype == np.float32 and a.size == P
     _check(full, param_dtype)
     assert full.size == P
     work = np.empty(2 * P + 16, np.float32)
     bad = ctypes.c_int64(0)
-    rc = lib().orc_zero_step(_ptrs(grads), grad_dtype, numel, world, _fp(master), _fp(m),
-                             _fp(v), _vp(full), param_dtype, lr, beta1, beta2, eps, t,
-                             loss_scale, _fp(work), ctypes.byref(bad), weight_decay)
+    rc = lib().orc_zero_step_s(_ptrs(grads), grad_dtype, numel, world, S, _fp(master), _fp(m),
+                               _fp(v), _vp(full), param_dtype, lr, beta1, beta2, eps, t,
+                               loss_scale, _fp(work), ctypes.byref(bad), weight_decay)
     if rc < 0:
         raise ValueError("orc_zero_step: bad arguments")
     return bool(rc == 1), int(bad.value)
@@ -221,10 +234,11 @@ def zero_step(grads, grad_dtype, numel, master, m, v, full, param_dtype,
 
 def zero_rank_step(slices, grad_dtype, numel, rank, master, m, v, lp_out, param_dtype,
                    lr, beta1, beta2, eps, t, loss_scale=0.0, others_nonfinite=0,
-                   weight_decay=0.0):
-    """One rank's view, in place.  Returns (skipped, n_nonfinite_local)."""
+                   weight_decay=0.0, shard=None):
+    """One rank's view, in place.  Returns (skipped, n_nonfinite_local).
+    `shard` overrides the shard length ceil(numel/N) (the dim-0 layout)."""
     world = len(slices)
-    S = shard_size(numel, world)
+    S = shard_size(numel, world) if shard is None else shard
     for s in slices:
         _check(s, grad_dtype)
         assert s.size == S
@@ -234,10 +248,10 @@ def zero_rank_step(slices, grad_dtype, numel, rank, master, m, v, lp_out, param_
     assert lp_out.size == S and lp_out.flags.c_contiguous
     work = np.empty(max(S, 1), np.float32)
     bad = ctypes.c_int64(0)
-    rc = lib().orc_zero_rank_step(_ptrs(slices), grad_dtype, numel, world, rank, _fp(master),
-                                  _fp(m), _fp(v), _vp(lp_out), param_dtype, lr, beta1, beta2,
-                                  eps, t, loss_scale, others_nonfinite, _fp(work),
-                                  ctypes.byref(bad), weight_decay)
+    rc = lib().orc_zero_rank_step_s(_ptrs(slices), grad_dtype, numel, world, S, rank,
+                                    _fp(master), _fp(m), _fp(v), _vp(lp_out), param_dtype, lr,
+                                    beta1, beta2, eps, t, loss_scale, others_nonfinite, _fp(work),
+                                    ctypes.byref(bad), weight_decay)
     if rc < 0:
         raise ValueError("orc_zero_rank_step: bad arguments")
     return bool(rc == 1), int(bad.value)

@@ -253,6 +253,32 @@ void orc_adam(float *x, float *m, float *v, const float *g, int64_t n,
     }
 }
 
+/* Reduce-scatter as above for an explicit shard length S (S*world >= numel):
+ * the row-granular layout below rounds shards up to whole rows. */
+static void reduce_scatter_s(const void *const *grads, int32_t dtype, int64_t numel,
+                             int32_t world, int64_t S, int32_t rank, float *out)
+{
+    for (int64_t j = 0; j < S; ++j) {
+        int64_t i = (int64_t)rank * S + j;
+        if (i >= numel) { out[j] = 0.0f; continue; }
+        float a = widen(grads[0], dtype, i);
+        for (int32_t k = 1; k < world; ++k) a = a + widen(grads[k], dtype, i);
+        out[j] = a;
+    }
+}
+
+/* FSDP2's per-parameter layout ("ZeRO 与 FSDP…", section ZeRO-3 与 FSDP: each
+ * parameter is a DTensor sharded along dim 0): a parameter of `rows` rows of
+ * `row_elems` elements is cut into chunks of ceil(rows/world) whole rows;
+ * rank r holds rows [r*c, r*c + c), padded with zero rows past the end
+ * (ranks past the last row hold padding only).  As a flat shard length:
+ * S = ceil(rows / world) * row_elems. */
+int64_t orc_row_shard_size(int64_t rows, int64_t row_elems, int32_t world)
+{
+    if (world <= 0 || rows < 0 || row_elems < 0) return -1;
+    return (rows + world - 1) / world * row_elems;
+}
+
 /* -------------------------------------------------------- the whole step */
 
 /* One ZeRO-2 step with every rank's state held here ("all ranks" layout):
@@ -270,18 +296,17 @@ void orc_adam(float *x, float *m, float *v, const float *g, int64_t n,
  * Returns 1 when skipped, 0 when applied, -1 on bad arguments.
  * *n_nonfinite (optional) gets the count from step 3.
  * `work` must hold P floats plus P param elements (8*P bytes suffice). */
-int orc_zero_step(const void *const *grads, int32_t grad_dtype, int64_t numel, int32_t world,
-                  float *master, float *m, float *v, void *full, int32_t param_dtype,
-                  double lr, double beta1, double beta2, double eps, int64_t t, float loss_scale,
-                  float *work, int64_t *n_nonfinite, double weight_decay)
+int orc_zero_step_s(const void *const *grads, int32_t grad_dtype, int64_t numel, int32_t world,
+                    int64_t S, float *master, float *m, float *v, void *full, int32_t param_dtype,
+                    double lr, double beta1, double beta2, double eps, int64_t t,
+                    float loss_scale, float *work, int64_t *n_nonfinite, double weight_decay)
 {
-    int64_t S = orc_shard_size(numel, world);
-    if (S < 0 || t < 1 || world > 4096) return -1;
+    if (S < 0 || S * world < numel || t < 1 || world > 4096) return -1;
     int64_t P = S * world;
     int64_t bad = 0;
     for (int32_t r = 0; r < world; ++r) {
         float *gr = work + (int64_t)r * S;
-        orc_reduce_scatter_sum(grads, grad_dtype, numel, world, r, gr, 0);
+        reduce_scatter_s(grads, grad_dtype, numel, world, S, r, gr);
         bad += orc_average(gr, S, world, loss_scale, gr);
     }
     if (n_nonfinite) *n_nonfinite = bad;
@@ -302,6 +327,16 @@ int orc_zero_step(const void *const *grads, int32_t grad_dtype, int64_t numel, i
     return 0;
 }
 
+int orc_zero_step(const void *const *grads, int32_t grad_dtype, int64_t numel, int32_t world,
+                  float *master, float *m, float *v, void *full, int32_t param_dtype,
+                  double lr, double beta1, double beta2, double eps, int64_t t, float loss_scale,
+                  float *work, int64_t *n_nonfinite, double weight_decay)
+{
+    return orc_zero_step_s(grads, grad_dtype, numel, world, orc_shard_size(numel, world), master,
+                           m, v, full, param_dtype, lr, beta1, beta2, eps, t, loss_scale, work,
+                           n_nonfinite, weight_decay);
+}
+
 /* One rank's view of the same step ([ZH] ZeroAdam.step as run by rank
  * `rank`): slices[k] is the S-element piece of rank k's flat grads that
  * belongs to this rank's shard (what reduce-scatter brings in), master/m/v
@@ -313,14 +348,14 @@ int orc_zero_step(const void *const *grads, int32_t grad_dtype, int64_t numel, i
  * ranks' findings, combined by the caller) has a non-finite value.
  * Returns 1 when skipped, 0 when applied, -1 on bad arguments.  `work` holds
  * S floats. */
-int orc_zero_rank_step(const void *const *slices, int32_t grad_dtype, int64_t numel,
-                       int32_t world, int32_t rank, float *master, float *m, float *v,
-                       void *lp_out, int32_t param_dtype, double lr, double beta1, double beta2,
-                       double eps, int64_t t, float loss_scale, int64_t others_nonfinite,
-                       float *work, int64_t *n_nonfinite, double weight_decay)
+int orc_zero_rank_step_s(const void *const *slices, int32_t grad_dtype, int64_t numel,
+                         int32_t world, int64_t S, int32_t rank, float *master, float *m,
+                         float *v, void *lp_out, int32_t param_dtype, double lr, double beta1,
+                         double beta2, double eps, int64_t t, float loss_scale,
+                         int64_t others_nonfinite, float *work, int64_t *n_nonfinite,
+                         double weight_decay)
 {
-    int64_t S = orc_shard_size(numel, world);
-    if (S < 0 || t < 1 || rank < 0 || rank >= world) return -1;
+    if (S < 0 || S * world < numel || t < 1 || rank < 0 || rank >= world) return -1;
     int64_t n_valid = numel - (int64_t)rank * S;
     if (n_valid < 0) n_valid = 0;
     if (n_valid > S) n_valid = S;
@@ -331,6 +366,18 @@ int orc_zero_rank_step(const void *const *slices, int32_t grad_dtype, int64_t nu
     orc_adam(master, m, v, work, S, lr, beta1, beta2, eps, t, weight_decay);
     orc_cast(master, S, param_dtype, lp_out);
     return 0;
+}
+
+int orc_zero_rank_step(const void *const *slices, int32_t grad_dtype, int64_t numel,
+                       int32_t world, int32_t rank, float *master, float *m, float *v,
+                       void *lp_out, int32_t param_dtype, double lr, double beta1, double beta2,
+                       double eps, int64_t t, float loss_scale, int64_t others_nonfinite,
+                       float *work, int64_t *n_nonfinite, double weight_decay)
+{
+    return orc_zero_rank_step_s(slices, grad_dtype, numel, world, orc_shard_size(numel, world),
+                                rank, master, m, v, lp_out, param_dtype, lr, beta1, beta2, eps,
+                                t, loss_scale, others_nonfinite, work, n_nonfinite,
+                                weight_decay);
 }
 
 /* GradScaler-style update of the loss scale after a step ([PP]): halve on a
