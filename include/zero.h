@@ -139,6 +139,19 @@ int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage,
               int32_t grad_dtype, int32_t param_dtype, int32_t rank,
               const int64_t *unit_numels, int32_t n_units);
 
+/* A stage-3 context in FSDP2's per-parameter layout ("ZeRO 与 FSDP…", section
+ * ZeRO-3 与 FSDP: each parameter is a DTensor sharded along dim 0, a
+ * (256,64) weight over 2 ranks being (128,64) on each).  Unit u is one
+ * parameter of rows[u] rows of row_elems[u] elements (the product of its
+ * other dimensions); it is cut into chunks of ceil(rows/N) whole rows, rank r
+ * holding rows [r*c, r*c + c) and zero rows past the end (ranks past the last
+ * row hold padding only).  Its shard length is ceil(rows/N) * row_elems; all
+ * stage-3 calls then work as for zero_init's units, and a gather places the
+ * N chunks one after another, i.e. the parameter's rows in order followed by
+ * the padding rows. */
+int zero_init_dim0(zero_ctx **out, int32_t world, int32_t grad_dtype, int32_t param_dtype,
+                   int32_t rank, const int64_t *rows, const int64_t *row_elems, int32_t n_units);
+
 int zero_destroy(zero_ctx *ctx);
 
 /* Geometry of a context.  unit = -1 means the whole flat vector (stages 1,

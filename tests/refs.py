@@ -32,10 +32,14 @@ def host_grads(w: Workload, it: int, scale: float, unit: int = 0):
     return out
 
 
+def shard_of(w: Workload, unit: int = 0) -> int:
+    return w.unit_shard(unit) if w.units else w.shard
+
+
 def host_slices(w: Workload, it: int, scale: float, rank: int, unit: int = 0):
     """The S-element slices rank `rank` receives (one-rank view)."""
     n = w.units[unit] if w.units else w.numel
-    S = -(-n // w.world)
+    S = shard_of(w, unit)
     nv = valid_len(n, S, rank)
     sigma = grad_sigma(w, scale)
     out = []
@@ -55,7 +59,7 @@ def host_slices(w: Workload, it: int, scale: float, rank: int, unit: int = 0):
 
 def host_master(w: Workload, unit: int = 0, rank: int = -1):
     n = w.units[unit] if w.units else w.numel
-    S = -(-n // w.world)
+    S = shard_of(w, unit)
     k = synth.key(w.seed, synth.KIND_MASTER, 0, 0, unit)
     if rank < 0:
         x = np.zeros(S * w.world, np.float32)
@@ -69,7 +73,7 @@ def host_master(w: Workload, unit: int = 0, rank: int = -1):
 
 def host_other_shard(w: Workload, k: int, unit: int = 0):
     n = w.units[unit] if w.units else w.numel
-    S = -(-n // w.world)
+    S = shard_of(w, unit)
     s = np.zeros(S, STORAGE[w.param_dtype])
     nv = valid_len(n, S, k)
     s[:nv] = synth.fill_host(nv, w.param_dtype, synth.key(w.seed, KIND_SHARD, 0, k, unit),
@@ -150,7 +154,8 @@ class OracleRun:
                     full = np.zeros(x.size, STORAGE[w.param_dtype])
                     sk, _ = oracle.zero_step(grads, w.grad_dtype, w.units[u], x, m, v, full,
                                              w.param_dtype, *hp, loss_scale=self.scale,
-                                             weight_decay=w.weight_decay)
+                                             weight_decay=w.weight_decay,
+                                             shard=w.unit_shard(u))
                     lp = full
                 else:
                     sl = host_slices(w, it, self.scale, w.rank, u)
@@ -158,7 +163,8 @@ class OracleRun:
                     sk, _ = oracle.zero_rank_step(sl, w.grad_dtype, w.units[u], w.rank, x, m,
                                                   v, lp, w.param_dtype, *hp,
                                                   loss_scale=self.scale,
-                                                  weight_decay=w.weight_decay)
+                                                  weight_decay=w.weight_decay,
+                                                  shard=w.unit_shard(u))
                 skipped |= sk
                 new_state[u] = [x, m, v]
                 new_own[u] = lp
@@ -182,7 +188,7 @@ def sampled_reference(w: Workload, idx: np.ndarray, iterations, skipped_iters=()
     shard.  The global skip verdicts are given (`skipped_iters`).  Returns
     (master, m, v, param) at idx."""
     n = w.units[unit] if w.units else w.numel
-    S = -(-n // w.world)
+    S = shard_of(w, unit)
     gidx = idx if rank < 0 else idx + rank * S      # global flat position
     valid = gidx < n
     kmaster = synth.key(w.seed, synth.KIND_MASTER, 0, 0, unit)

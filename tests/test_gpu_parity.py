@@ -565,3 +565,45 @@ def test_lean_gather_placement(S, world, dtype, src_off, dst_off):
     torch.cuda.synchronize()
     assert to_np(full).tobytes() == oracle.all_gather(hs, dtype).tobytes()
     assert z.zero_gather_timeouts() == before
+
+
+# -------------------------------------------------- FSDP2's dim-0 layout
+
+@pytest.mark.parametrize("rank,scaled", [(1, False), (-1, False), (3, True), (0, False)])
+def test_dim0_layout_units(rank, scaled):
+    """Per-parameter units sharded by whole rows (the MLP's four tensors and
+    uneven Llama-like shapes): gathers before forward and backward, per-unit
+    reduce + Adam, bit-identical to the oracle; ranks past the last row hold
+    only padding."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    shapes = [(256, 64), (256, 1), (10, 256), (10, 1), (4097, 33), (3, 11)]
+    w = W.dim0(shapes, 4, rank=rank, steps=3, loss_scale=2.0 ** 8 if scaled else 0.0)
+    run = Runner(w)
+    ref = refs.OracleRun(w)
+    for u, (rows, row) in enumerate(shapes):
+        assert z.zero_ctx_shard_size(run.ctx, u) == -(-rows // 4) * row
+    for it in range(1, 4):
+        run.fill_grads(it)
+        t = run.t + 1
+        z.zero3_begin_step(run.ctx)
+        seen = []
+        order = list(range(len(shapes))) + list(reversed(range(len(shapes))))
+        for i, u in enumerate(order):
+            z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full)
+            seen.append(to_np(run.unit_full[:w.unit_shard(u) * w.world]))
+            if i >= len(shapes):
+                if scaled:
+                    z.zero3_reduce_unit(run.ctx, u, run.grads[u], run.scale)
+                else:
+                    z.zero3_step_unit(run.ctx, u, run.grads[u], w.lr, w.beta1, w.beta2, w.eps, t)
+        if scaled:
+            z.zero_step_apply(run.ctx, w.lr, w.beta1, w.beta2, w.eps, t)
+        run.finish_step()
+        ref.step(it)
+        want = [g[2] for g in ref.gathers[-2 * len(shapes):]]
+        for a, b in zip(seen, want):
+            assert a.tobytes() == b.tobytes()
+    assert run.skips == ref.skips
+    compare_runner(run, ref, what="dim0")
+    run.close()

@@ -53,6 +53,7 @@ class Workload:
     param_dtype: int
     rank: int = -1                       # -1: every rank's state on this GPU
     units: Optional[List[int]] = None    # stage 3
+    unit_rows: Optional[List[Tuple[int, int]]] = None   # stage 3, dim-0 layout: (rows, row_elems)
     steps: int = 3
     lr: float = 1e-4
     beta1: float = 0.9
@@ -73,6 +74,9 @@ class Workload:
         return -(-self.numel // self.world)
 
     def unit_shard(self, u: int) -> int:
+        if self.unit_rows:
+            rows, row = self.unit_rows[u]
+            return -(-rows // self.world) * row
         return -(-self.units[u] // self.world)
 
     def updated_per_step(self) -> int:
@@ -115,6 +119,13 @@ def gpt2_xl_bucketed() -> Workload:
     """GPT-2 XL stepped in 32 Mi-element buckets from constant-size gradient
     buffers (16 ranks x 64 MiB), the way ZeRO-2 reduce-scatters during backward."""
     return gpt2_xl().replace(name="gpt2_xl_bucketed", bucket=1 << 25)
+
+
+def dim0(shapes, world: int, rank: int = -1, **kw) -> Workload:
+    """Stage 3 in FSDP2's per-parameter dim-0 layout; shapes = [(rows, row_elems)]."""
+    units = [r * e for r, e in shapes]
+    return Workload("dim0", sum(units), world, 3, BF16, BF16, rank=rank, units=units,
+                    unit_rows=list(shapes), **kw)
 
 
 ALL = {"tiny": tiny, "gpt2_xl_bucketed": gpt2_xl_bucketed, "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl,

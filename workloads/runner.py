@@ -36,8 +36,11 @@ class Runner:
         self.w = w
         self.dev = torch.device(device)
         torch.cuda.set_device(self.dev)
-        self.ctx = z.zero_init(w.numel, w.world, w.stage, w.grad_dtype, w.param_dtype, w.rank,
-                               w.units)
+        if w.unit_rows:
+            self.ctx = z.zero_init_dim0(w.world, w.grad_dtype, w.param_dtype, w.rank, w.unit_rows)
+        else:
+            self.ctx = z.zero_init(w.numel, w.world, w.stage, w.grad_dtype, w.param_dtype,
+                                   w.rank, w.units)
         ns = z.zero_ctx_state_elems(self.ctx)
         npar = z.zero_ctx_param_elems(self.ctx)
         f32 = dict(dtype=torch.float32, device=self.dev)

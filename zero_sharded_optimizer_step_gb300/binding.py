@@ -45,6 +45,8 @@ _SIGS = {
     "zero_last_error": (ctypes.c_char_p, []),
     "zero_init": (ctypes.c_int, [ctypes.POINTER(_ctxp), _i64, _i32, _i32, _i32, _i32, _i32,
                                  ctypes.POINTER(_i64), _i32]),
+    "zero_init_dim0": (ctypes.c_int, [ctypes.POINTER(_ctxp), _i32, _i32, _i32, _i32,
+                                      ctypes.POINTER(_i64), ctypes.POINTER(_i64), _i32]),
     "zero_destroy": (ctypes.c_int, [_ctxp]),
     "zero_ctx_shard_size": (_i64, [_ctxp, _i32]),
     "zero_ctx_state_elems": (_i64, [_ctxp]),
@@ -184,6 +186,17 @@ def zero_init(numel: int, world: int, stage: int, grad_dtype: int, param_dtype: 
         units = (_i64 * n_units)(*unit_numels)
     _check(_L.zero_init(ctypes.byref(h), numel, world, stage, grad_dtype, param_dtype, rank,
                         units, n_units))
+    return Ctx(h.value)
+
+
+def zero_init_dim0(world: int, grad_dtype: int, param_dtype: int, rank: int, shapes) -> Ctx:
+    """Stage 3 in FSDP2's dim-0 layout; shapes = [(rows, row_elems), ...]."""
+    h = _ctxp()
+    n = len(shapes)
+    rows = (_i64 * n)(*[r for r, _ in shapes])
+    elems = (_i64 * n)(*[e for _, e in shapes])
+    _check(_L.zero_init_dim0(ctypes.byref(h), world, grad_dtype, param_dtype, rank, rows,
+                             elems, n))
     return Ctx(h.value)
 
 

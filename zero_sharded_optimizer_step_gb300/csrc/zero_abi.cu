@@ -319,6 +319,36 @@ Range apply_range(const zero_ctx *c)
     return r;
 }
 
+// Units of stage 3: unit u has numel[u] elements sharded into shard[u] per
+// rank (shard[u] * world >= numel[u]); state, scratch and param shards lie
+// unit after unit.
+int init_units(zero_ctx *c, const int64_t *numel, const int64_t *shard, int32_t n, int64_t total)
+{
+    const int64_t kLimit = (int64_t)1 << 56;
+    int64_t sum = 0, off = 0;
+    for (int32_t u = 0; u < n; ++u) {
+        const int64_t nu = numel[u], su = shard[u];
+        if (nu < 0 || nu > kLimit || su < 0 || su > kLimit || su * c->world < nu)
+            return fail(ZERO_EINVAL, "unit %d: bad size (%lld elements, shard %lld)", u,
+                        (long long)nu, (long long)su);
+        c->unit_numel.push_back(nu);
+        c->unit_S.push_back(su);
+        c->unit_state_off.push_back(off);
+        off += c->rank < 0 ? su * c->world : su;
+        sum += nu;
+        if (sum > kLimit || off > kLimit) return fail(ZERO_EINVAL, "units too large");
+    }
+    if (total != sum)
+        return fail(ZERO_EINVAL, "numel (%lld) must equal the sum of the units (%lld)",
+                    (long long)total, (long long)sum);
+    c->numel = sum;
+    c->S = -1;
+    c->P = -1;
+    c->state_elems = off;
+    c->param_elems = off;
+    return ZERO_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -409,34 +439,48 @@ int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage, int32
             delete c;
             return fail(ZERO_EINVAL, "stage 3 needs unit_numels and n_units >= 1");
         }
-        int64_t sum = 0, off = 0;
-        for (int32_t u = 0; u < n_units; ++u) {
-            const int64_t nu = unit_numels[u];
-            if (nu < 0 || nu > kLimit) {
-                delete c;
-                return fail(ZERO_EINVAL, "unit %d numel out of range (%lld)", u, (long long)nu);
-            }
-            const int64_t su = ceil_div(nu, world);
-            c->unit_numel.push_back(nu);
-            c->unit_S.push_back(su);
-            c->unit_state_off.push_back(off);
-            off += rank < 0 ? su * world : su;
-            sum += nu;
-            if (sum > kLimit || off > kLimit) {
-                delete c;
-                return fail(ZERO_EINVAL, "units too large");
-            }
-        }
-        if (numel != sum) {
+        std::vector<int64_t> shards;
+        for (int32_t u = 0; u < n_units; ++u)
+            shards.push_back(unit_numels[u] < 0 ? -1 : ceil_div(unit_numels[u], world));
+        int rc = init_units(c, unit_numels, shards.data(), n_units, numel);
+        if (rc) {
             delete c;
-            return fail(ZERO_EINVAL, "numel (%lld) must equal the sum of unit_numels (%lld)",
-                        (long long)numel, (long long)sum);
+            return rc;
         }
-        c->numel = sum;
-        c->S = -1;
-        c->P = -1;
-        c->state_elems = off;
-        c->param_elems = off;
+    }
+    *out = c;
+    return ZERO_OK;
+}
+
+int zero_init_dim0(zero_ctx **out, int32_t world, int32_t grad_dtype, int32_t param_dtype,
+                   int32_t rank, const int64_t *rows, const int64_t *row_elems, int32_t n_units)
+{
+    if (!out) return fail(ZERO_EINVAL, "out is null");
+    *out = nullptr;
+    if (!rows || !row_elems || n_units < 1)
+        return fail(ZERO_EINVAL, "rows and row_elems of n_units >= 1 parameters are needed");
+    std::vector<int64_t> numel, shard;
+    int64_t total = 0;
+    for (int32_t u = 0; u < n_units; ++u) {
+        if (rows[u] < 0 || row_elems[u] < 0 || (row_elems[u] && rows[u] > ((int64_t)1 << 56) / row_elems[u]))
+            return fail(ZERO_EINVAL, "parameter %d: bad shape (%lld x %lld)", u,
+                        (long long)rows[u], (long long)row_elems[u]);
+        numel.push_back(rows[u] * row_elems[u]);
+        total += numel.back();
+    }
+    // the shared checks of world, dtypes and rank
+    zero_ctx *c = nullptr;
+    int rc = zero_init(&c, total, world, 3, grad_dtype, param_dtype, rank, numel.data(), n_units);
+    if (rc) return rc;
+    c->unit_numel.clear();
+    c->unit_S.clear();
+    c->unit_state_off.clear();
+    for (int32_t u = 0; u < n_units; ++u)
+        shard.push_back(ceil_div(rows[u], world) * row_elems[u]);
+    rc = init_units(c, numel.data(), shard.data(), n_units, total);
+    if (rc) {
+        delete c;
+        return rc;
     }
     *out = c;
     return ZERO_OK;
