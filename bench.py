@@ -38,15 +38,15 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from ncu
-# captures summarised under profiles/: small cases of the same kernel scaled
-# to the full launch by the elements processed (the kernels stream, so
-# traffic grows in proportion).  Each entry is valid only for the kernel
-# source it was taken on (sha256 prefix); otherwise the bench reports null.
+# captures of the full workloads (dram__bytes_read.sum + dram__bytes_write.sum,
+# one pass; summarised under profiles/).  Each entry is valid only for the
+# kernel source it was taken on (sha256 prefix); otherwise bench reports null.
 TRAFFIC = {
-    ("gpt2_xl", "fused_step_kernel"): ("94ca1758ce0b4378", (4.400171e9 + 1.403571e9) * 15.576112),
-    ("one_rank_7p5b", "gather_kernel"): ("d09e0618a79e1973", (1.260070e9 + 1.208794e9) * 11.71875),
-    ("one_rank_7p5b", "fused_step_kernel"): ("94ca1758ce0b4378",
-                                             (1.400088576e9 + 0.13635968e9) * 11.71875),
+    ("gpt2_xl", "fused_step_kernel"): ("191a346d13c7fd77", 68.54e9 + 22.32e9),
+    ("one_rank_7p5b", "gather_kernel"): ("d48998624012af79", 14.79e9 + 14.72e9),
+    ("one_rank_7p5b", "fused_step_kernel"): ("191a346d13c7fd77", 16.41e9 + 1.94e9),
+    # the 2-unit capture has the full workload's launch sizes
+    ("zero3_llama7b", "gather_kernel"): ("d48998624012af79", 404.80128e6 + 353.814272e6),
 }
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
                           "zero_step_kernels.cu")
@@ -75,6 +75,8 @@ def parse():
     ap.add_argument("--two-pass", action="store_true",
                     help="loss-scaled workloads: the scratch-based two-pass step instead of the "
                          "single pass over two state sets")
+    ap.add_argument("--units", type=int, default=0,
+                    help="ZeRO-3 workloads: use this many Llama-7B-shaped units (small cases)")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     return ap.parse_args()
@@ -262,7 +264,8 @@ def bench_ours(args, rank, world_size, device_index):
     import workloads as W
     from workloads.runner import Runner
 
-    w = W.ALL[args.workload]()
+    w = W.ALL[args.workload](**({"n_units": args.units} if args.units and
+                                args.workload.startswith("zero3") else {}))
     if args.numel:
         w = w.replace(numel=args.numel, name=w.name + "_numel%d" % args.numel)
     if w.inject:
@@ -322,7 +325,7 @@ def bench_ours(args, rank, world_size, device_index):
     peak, peak_kind = peaks()
     achieved = alg_per_launch / (avg_ms * 1e-3) / 1e9
     kh = src_hash(GATHER_SRC if dom == "gather_kernel" else KERNEL_SRC)
-    tr = None if args.numel else TRAFFIC.get((args.workload, dom))
+    tr = None if (args.numel or args.units) else TRAFFIC.get((args.workload, dom))
     traffic = tr[1] if tr and tr[0] == kh else None
 
     updated = w.updated_per_step()
@@ -391,7 +394,7 @@ def bench_prefetch(args, rank, world_size, device_index):
     from workloads.runner import Runner
     from workloads.zero3_schedule import Zero3Schedule
 
-    w = W.zero3_llama7b().replace(name="zero3_prefetch")
+    w = W.zero3_llama7b(args.units or 32).replace(name="zero3_prefetch")
     torch.cuda.set_device(device_index)
     run = Runner(w, device="cuda:%d" % device_index)
     run.fill_grads(1)
