@@ -129,7 +129,7 @@ for gdt, pdt in [(W.BF16, W.BF16), (W.F16, W.F16), (W.F32, W.F32), (W.BF16, W.F3
 for numel, world, rank in [(1_000_003, 3, -1), (1_000_003, 3, 0), (1_000_003, 3, 2),
                            (777_777, 16, 5), (777_777, 16, 15), (500_000, 1, -1),
                            (500_000, 1, 0), (99_999, 64, -1), (99_999, 64, 63),
-                           (2_000_001, 13, 7)]:
+                           (2_000_001, 13, 7), (100_007, 256, -1), (100_007, 256, 255)]:
     CASES.append((numel, world, W.BF16, W.BF16, rank))
     CASES.append((numel, world, W.F16, W.F32, rank))
 
