@@ -343,7 +343,9 @@ def bench_ours(args, rank, world_size, device_index):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {0: "f32", 1: "bf16", 2: "f16"}[w.grad_dtype] + " grads, f32 state",
+        "dtype": "f32",
+        "storage": {"grads": "f32 bf16 f16".split()[w.grad_dtype],
+                    "params": "f32 bf16 f16".split()[w.param_dtype], "state": "f32"},
         "data": "synthetic (seeded counter-based normal draws; no dataset)",
         "config": {
             "workload": describe(w),
@@ -435,7 +437,7 @@ def bench_prefetch(args, rank, world_size, device_index):
         "metric": METRIC, "value": updated * world_size / (times["overlap"] * 1e-3),
         "unit": "params/s", "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": times["overlap"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 grads, f32 state",
+        "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded draws; a stand-in kernel plays each unit's compute)",
         "config": {
             "workload": describe(w) + " + stand-in compute %.3f ms fwd / %.3f ms bwd per unit"
@@ -689,7 +691,7 @@ def bench_reference(args, rank, world_size):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
             "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / len(times), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32 arithmetic (CPU oracle)",
+            "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": {"workload": describe(w)},
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
