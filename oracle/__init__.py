@@ -45,48 +45,69 @@ def build(force: bool = False) -> str:
     return LIB
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Open an oracle library at `path` with its function signatures."""
+    L = ctypes.CDLL(path)
+    i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_double
+    vp, fp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)
+    vpp = ctypes.POINTER(ctypes.c_void_p)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    sig = {
+        "orc_shard_size": (i64, [i64, i32]),
+        "orc_owner": (i32, [i64, i64, i32]),
+        "orc_elem_size": (i32, [i32]),
+        "orc_widen_array": (None, [vp, i32, i64, fp]),
+        "orc_cast": (None, [fp, i64, i32, vp]),
+        "orc_rank_sum": (None, [vpp, i32, i32, i64, i64, fp]),
+        "orc_reduce_scatter_sum": (ctypes.c_int, [vpp, i32, i64, i32, i32, fp, i64p]),
+        "orc_average": (i64, [fp, i64, i32, f32, fp]),
+        "orc_all_gather": (None, [vpp, i32, i64, i32, vp, i64p]),
+        "orc_all_reduce_mean": (None, [vpp, i32, i64, i32, fp]),
+        "orc_adam_scalars": (None, [f64, f64, i64, fp]),
+        "orc_adam": (None, [fp, fp, fp, fp, i64, f64, f64, f64, f64, i64, f64]),
+        "orc_zero_step": (ctypes.c_int, [vpp, i32, i64, i32, fp, fp, fp, vp, i32,
+                                         f64, f64, f64, f64, i64, f32, fp, i64p, f64]),
+        "orc_zero_rank_step": (ctypes.c_int, [vpp, i32, i64, i32, i32, fp, fp, fp,
+                                              vp, i32, f64, f64, f64, f64, i64, f32,
+                                              i64, fp, i64p, f64]),
+        "orc_scale_update": (f32, [f32, i32, i64p, i64]),
+        "orc_row_shard_size": (i64, [i64, i64, i32]),
+        "orc_zero_step_s": (ctypes.c_int, [vpp, i32, i64, i32, i64, fp, fp, fp, vp, i32,
+                                           f64, f64, f64, f64, i64, f32, fp, i64p, f64]),
+        "orc_zero_rank_step_s": (ctypes.c_int, [vpp, i32, i64, i32, i64, i32, fp, fp, fp,
+                                                vp, i32, f64, f64, f64, f64, i64, f32,
+                                                i64, fp, i64p, f64]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = ctypes.CDLL(LIB)
-            i64, i32, f32, f64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_double
-            vp, fp = ctypes.c_void_p, ctypes.POINTER(ctypes.c_float)
-            vpp = ctypes.POINTER(ctypes.c_void_p)
-            i64p = ctypes.POINTER(ctypes.c_int64)
-            sig = {
-                "orc_shard_size": (i64, [i64, i32]),
-                "orc_owner": (i32, [i64, i64, i32]),
-                "orc_elem_size": (i32, [i32]),
-                "orc_widen_array": (None, [vp, i32, i64, fp]),
-                "orc_cast": (None, [fp, i64, i32, vp]),
-                "orc_rank_sum": (None, [vpp, i32, i32, i64, i64, fp]),
-                "orc_reduce_scatter_sum": (ctypes.c_int, [vpp, i32, i64, i32, i32, fp, i64p]),
-                "orc_average": (i64, [fp, i64, i32, f32, fp]),
-                "orc_all_gather": (None, [vpp, i32, i64, i32, vp, i64p]),
-                "orc_all_reduce_mean": (None, [vpp, i32, i64, i32, fp]),
-                "orc_adam_scalars": (None, [f64, f64, i64, fp]),
-                "orc_adam": (None, [fp, fp, fp, fp, i64, f64, f64, f64, f64, i64, f64]),
-                "orc_zero_step": (ctypes.c_int, [vpp, i32, i64, i32, fp, fp, fp, vp, i32,
-                                                 f64, f64, f64, f64, i64, f32, fp, i64p, f64]),
-                "orc_zero_rank_step": (ctypes.c_int, [vpp, i32, i64, i32, i32, fp, fp, fp,
-                                                      vp, i32, f64, f64, f64, f64, i64, f32,
-                                                      i64, fp, i64p, f64]),
-                "orc_scale_update": (f32, [f32, i32, i64p, i64]),
-                "orc_row_shard_size": (i64, [i64, i64, i32]),
-                "orc_zero_step_s": (ctypes.c_int, [vpp, i32, i64, i32, i64, fp, fp, fp, vp, i32,
-                                                   f64, f64, f64, f64, i64, f32, fp, i64p, f64]),
-                "orc_zero_rank_step_s": (ctypes.c_int, [vpp, i32, i64, i32, i64, i32, fp, fp, fp,
-                                                        vp, i32, f64, f64, f64, f64, i64, f32,
-                                                        i64, fp, i64p, f64]),
-            }
-            for name, (res, args) in sig.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            # a copy of the oracle with a planted mistake, for the tests that
+            # check the pins catch it
+            override = os.environ.get("ZERO_ORACLE_LIB")
+            if override:
+                _lib = load(override)
+            else:
+                build()
+                _lib = load(LIB)
     return _lib
+
+
+def use_library(L) -> ctypes.CDLL:
+    """Swap the library every oracle function calls (None: back to the
+    built one); returns the previous one.  For the tests that plant
+    mistakes in copies of the oracle."""
+    global _lib
+    with _lock:
+        prev, _lib = _lib, L
+    return prev
 
 
 # ----------------------------------------------------------------- helpers
