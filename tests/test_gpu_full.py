@@ -126,3 +126,45 @@ def test_zero3_llama7b_full():
         if k != w.rank:
             assert torch.equal(full[k * Su:(k + 1) * Su], run.shards[0][k])
     run.close()
+
+
+@pytest.mark.parametrize("shadow", [True, False])
+def test_gpt2_xl_bucketed_full(shadow):
+    """The bucketed step (32 Mi-element buckets) at the full GPT-2 XL size,
+    loss-scaled with the +inf at iteration 3: same skips and, on the sample,
+    the same state as the oracle."""
+    w = W.gpt2_xl_bucketed()
+    run = run_all(w, shadow=shadow)
+    assert run.skips == [i == 3 for i in range(1, w.steps + 1)]
+    P = w.shard * w.world
+    idx = sample_positions(P, 1 << 25, n_rand=1 << 19)      # bucket edges included
+    check_sampled(run, w, idx, skipped=(3,))
+    run.close()
+
+
+def test_zero3_prefetch_full():
+    """The prefetched ZeRO-3 schedule (lean gathers on a background stream,
+    stand-in compute) at the full 32-unit size: sampled state matches the
+    oracle; the last gather holds the foreign shards; no wait ran out."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    from workloads.zero3_schedule import Zero3Schedule
+    w = W.zero3_llama7b()
+    before = z.zero_gather_timeouts()
+    run = Runner(w)
+    sch = Zero3Schedule(run, 20000, 40000, 304, "overlap")
+    for it in range(1, w.steps + 1):
+        run.fill_grads(it)
+        sch.launch_step()
+    torch.cuda.synchronize()
+    Su = w.unit_shard(0)
+    for u in (0, 31):
+        off = z.zero_ctx_unit_state_offset(run.ctx, u)
+        check_sampled(run, w, sample_positions(Su, Su, seed=u, n_rand=1 << 16), unit=u,
+                      state_off=off)
+    last = sch.bufs[(len(sch.visits) - 1) % 2]
+    for k in range(w.world):
+        if k != w.rank:
+            assert torch.equal(last[k * Su:(k + 1) * Su], run.shards[0][k])
+    assert z.zero_gather_timeouts() == before
+    run.close()
