@@ -65,7 +65,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="gpt2_xl",
                     choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny",
-                             "gpt2_xl_bucketed", "zero3_prefetch"])
+                             "gpt2_xl_bucketed", "zero3_prefetch", "zero3_gpt2_small"])
+    ap.add_argument("--graph", action="store_true",
+                    help="also capture one step in a CUDA graph and time its replays")
     ap.add_argument("--unit-fwd-ms", type=float, default=0.25,
                     help="zero3_prefetch: stand-in forward compute per unit (backward = 2x)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -285,6 +287,10 @@ def bench_ours(args, rank, world_size, device_index):
                               W.grad_sigma(w, run.scale), run.stream.cuda_stream)
     else:
         run.fill_grads(1)
+    if args.graph:
+        # graphs are captured on a stream of their own
+        torch.cuda.synchronize()
+        run.stream = torch.cuda.Stream(run.dev)
     plan = step_plan(run)
     torch.cuda.synchronize()
     for _ in range(args.warmup):
@@ -376,6 +382,11 @@ def bench_ours(args, rank, world_size, device_index):
         "gpu_launches": sum(L.kernels for L in plan) * args.steps,
         "clocks": clock_info,
     }
+    if args.graph and run.scale <= 0:
+        gms = bench_graph(run, plan, args, world_size)
+        result["config"]["graph_ms_per_step"] = gms
+        result["config"]["graph_params_per_s"] = updated * world_size / (gms * 1e-3)
+        result["config"]["eager_ms_per_step"] = step_ms
     if not args.no_e2e and not w.bucket:
         e2e = (bench_e2e_pipelined(run, args, world_size) if w.stage < 3 else
                bench_e2e_units(run, args, world_size) if w.rank >= 0 else None)
@@ -453,6 +464,68 @@ def bench_prefetch(args, rank, world_size, device_index):
         "gpu_launches": (2 * U + 2 * U + U) * args.steps,
         "clocks": None,
     }
+
+
+def bench_graph(run, plan, args, world_size):
+    """Replays of one step captured in a CUDA graph.  The per-step scalars
+    live in a device block (zero_bind_hyper) refreshed by a memcpy node from
+    pinned host memory that zero_prepare_step fills before each replay.  Two
+    graphs read two host blocks in turn, and a host block is refilled only
+    after the replay that read it has run (an event), so one step is always
+    queued ahead of the GPU."""
+    import torch
+    import zero_sharded_optimizer_step_gb300 as z
+
+    w, st = run.w, run.stream
+    d = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, device=run.dev)
+    hs = [torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    z.zero_bind_hyper(run.ctx, d)
+
+    def body(i):
+        with torch.cuda.stream(st):
+            d.copy_(hs[i], non_blocking=True)
+        for L in plan:
+            L.fn()
+
+    def prepare(i):
+        z.zero_prepare_step(run.ctx, hs[i], w.lr, w.beta1, w.beta2, w.eps, run.t + 1, run.scale)
+
+    torch.cuda.synchronize()
+    prepare(0)
+    body(0)                                 # one eager step in this mode first
+    torch.cuda.synchronize()
+    run.t += 1
+    graphs = [torch.cuda.CUDAGraph() for _ in range(2)]
+    for i in range(2):
+        with torch.cuda.graph(graphs[i], stream=st):
+            body(i)
+    read = [torch.cuda.Event(), torch.cuda.Event()]
+    started = [False, False]
+
+    def step(k):
+        i = k % 2
+        if started[i]:
+            read[i].synchronize()           # the replay that read hs[i] has run
+        prepare(i)
+        with torch.cuda.stream(st):
+            graphs[i].replay()
+        read[i].record(st)
+        started[i] = True
+        run.t += 1
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    barrier(world_size)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for k in range(args.steps):
+        step(k)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = allreduce_max(e0.elapsed_time(e1) / args.steps, world_size)
+    z.zero_bind_hyper(run.ctx, None)
+    return ms
 
 
 def working_set(run):

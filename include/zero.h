@@ -87,6 +87,7 @@ enum zero_code {
 };
 
 #define ZERO_MAX_RANKS 256
+#define ZERO_HYPER_BYTES 128     /* size of a device block of per-step scalars */
 
 enum zero_gather_mode {
     ZERO_GATHER_FAST = 0,  /* all SMs, many blocks: the fastest placement on an idle GPU */
@@ -229,6 +230,32 @@ int zero_current_state(zero_ctx *ctx, int32_t *which);
  * 0 (the default) is plain Adam.  Returns ZERO_EINVAL for a negative or
  * non-finite value. */
 int zero_set_weight_decay(zero_ctx *ctx, double weight_decay);
+
+/* ------------------------------------------- steps captured in a graph */
+
+/* Bind a device block of ZERO_HYPER_BYTES (16-byte aligned; NULL unbinds)
+ * from which every kernel of this context then reads the step's scalars (the
+ * Adam scalars, the averaging and loss-scale divisors, the step id) instead of
+ * taking them as launch arguments -- so a whole step, however many launches
+ * it makes, can be captured once in a CUDA graph and replayed step after
+ * step.  With a block bound, a step is:
+ *   1. zero_prepare_step(ctx, host_block, ...): starts the step (new step id,
+ *      loss scaling on or off) and writes its scalars into host_block
+ *      (ZERO_HYPER_BYTES of host memory; pinned, when the copy is captured);
+ *   2. a copy of host_block into the device block on the stream (inside the
+ *      graph: a memcpy node), before the step's kernels;
+ *   3. the step's calls (zero_step, the bucket calls, zero3_begin_step and
+ *      the unit calls, ...), or the replay of a graph that captured them.
+ *      They no longer start steps; their lr, betas, eps and t arguments are
+ *      not used (the block's are), and loss scaling must be on exactly when
+ *      the prepared step has it.
+ * zero_step_status reads the verdict of the prepared step as usual.
+ * A host block must not be refilled before the copy that reads it has run:
+ * with steps queued ahead of the GPU, alternate two host blocks (two
+ * captured graphs) and wait on an event recorded after the older one. */
+int zero_bind_hyper(zero_ctx *ctx, void *d_hyper);
+int zero_prepare_step(zero_ctx *ctx, void *host_hyper, double lr, double beta1, double beta2,
+                      double eps, int64_t t, float loss_scale);
 
 /* ------------------------------------------------------------ the step */
 

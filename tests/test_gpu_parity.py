@@ -607,3 +607,118 @@ def test_dim0_layout_units(rank, scaled):
     assert run.skips == ref.skips
     compare_runner(run, ref, what="dim0")
     run.close()
+
+
+# ------------------------------------------- steps captured in a CUDA graph
+
+def _hyper(run):
+    import zero_sharded_optimizer_step_gb300 as z
+    d = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, device=run.dev)
+    h = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, pin_memory=True)
+    z.zero_bind_hyper(run.ctx, d)
+    return d, h
+
+
+def test_zero3_step_replayed_from_a_cuda_graph():
+    """A whole ZeRO-3 step (forward gathers, backward gathers + unit steps)
+    captured once and replayed: per-step scalars come from the device block
+    refreshed by a memcpy node, so three replays equal three real steps."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    units = [100_003, 7, 250_000, 33_333]
+    w = W.Workload("z3g", sum(units), 4, 3, W.BF16, W.BF16, rank=1, units=units, steps=3)
+    run = Runner(w)
+    d, h = _hyper(run)
+    ref = refs.OracleRun(w)
+    U = len(units)
+
+    def body():
+        d.copy_(h, non_blocking=True)
+        z.zero3_begin_step(run.ctx)
+        for u in range(U):
+            z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full, None)
+        for u in reversed(range(U)):
+            z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full, None)
+            z.zero3_step_unit(run.ctx, u, run.grads[u], 0.0, 0.0, 0.0, 0.0, 1, None)
+
+    graph = torch.cuda.CUDAGraph()
+    for it in range(1, 4):
+        run.fill_grads(it)
+        torch.cuda.synchronize()
+        z.zero_prepare_step(run.ctx, h, w.lr, w.beta1, w.beta2, w.eps, it)
+        if it == 1:                   # the first step runs eagerly, then is captured
+            body()
+            torch.cuda.synchronize()
+            ref.step(it)
+            # capture (the capture itself does not run the kernels)
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(graph, stream=s):
+                    body()
+            continue
+        graph.replay()
+        torch.cuda.synchronize()
+        ref.step(it)
+    run.t = 3
+    run.skips = ref.skips
+    compare_runner(run, ref, what="graph z3")
+    run.close()
+
+
+def test_loss_scaled_single_pass_replayed_with_a_skip():
+    """The loss-scaled single pass over two state sets in a graph: the +inf
+    at iteration 2 is seen by the replayed kernels (they take the step id
+    from the block), the step is skipped, the scale halves, later replays
+    apply -- bit-identical to the oracle."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    w = W.Workload("g2", 1_000_003, 8, 2, W.F16, W.F16, steps=4, loss_scale=2.0 ** 12,
+                   inject=(2, 3))
+    run = Runner(w, shadow=True)
+    d, h = _hyper(run)
+    ref = refs.OracleRun(w)
+
+    def body():
+        d.copy_(h, non_blocking=True)
+        z.zero_step(run.ctx, run.grads[0], 0.0, 0.0, 0.0, 0.0, 1, loss_scale=1.0, stream=None)
+
+    graph = torch.cuda.CUDAGraph()
+    t = 0
+    for it in range(1, 5):
+        run.fill_grads(it)
+        torch.cuda.synchronize()
+        z.zero_prepare_step(run.ctx, h, w.lr, w.beta1, w.beta2, w.eps, t + 1, run.scale)
+        if it == 1:
+            body()
+            torch.cuda.synchronize()
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(graph, stream=s):
+                    body()
+        else:
+            graph.replay()
+        torch.cuda.synchronize()
+        nonfinite, skipped = z.zero_step_status(run.ctx)
+        run.skips.append(skipped)
+        if not skipped:
+            t += 1
+        run.scale, run.good = z.zero_scale_update(run.scale, skipped, run.good, 2000)
+        ref.step(it)
+    assert run.skips == ref.skips == [False, True, False, False]
+    compare_runner(run, ref, what="graph shadow")
+    run.close()
+
+
+def test_prepared_step_protocol():
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    w = W.Workload("gp", 1000, 4, 2, W.BF16, W.BF16, steps=1)
+    run = Runner(w)
+    d, h = _hyper(run)
+    with pytest.raises(z.ZeroError):          # not prepared yet
+        z.zero_step(run.ctx, run.grads[0], 1e-3, 0.9, 0.999, 1e-8, 1)
+    z.zero_prepare_step(run.ctx, h, 1e-3, 0.9, 0.999, 1e-8, 1)
+    with pytest.raises(z.ZeroError):          # loss scaling differs from the prepared step
+        z.zero_step(run.ctx, run.grads[0], 1e-3, 0.9, 0.999, 1e-8, 1, loss_scale=8.0)
+    z.zero_bind_hyper(run.ctx, None)
+    run.close()

@@ -128,7 +128,18 @@ def dim0(shapes, world: int, rank: int = -1, **kw) -> Workload:
                     unit_rows=list(shapes), **kw)
 
 
-ALL = {"tiny": tiny, "gpt2_xl_bucketed": gpt2_xl_bucketed, "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl,
+def zero3_gpt2_small() -> Workload:
+    """ZeRO-3 over GPT-2 small with one unit per transformer block, plus the
+    embeddings and the final norm (rank 0 of 8): 14 small units, where the
+    launch overhead of a 42-launch step matters."""
+    d, layers, vocab, ctx = 768, 12, 50257, 1024
+    block = gpt2_numel(d, 1, vocab=0, ctx=0) - 2 * d
+    units = [vocab * d + ctx * d] + [block] * layers + [2 * d]
+    return Workload("zero3_gpt2_small", sum(units), 8, 3, BF16, BF16, rank=0, units=units,
+                    steps=2)
+
+
+ALL = {"tiny": tiny, "zero3_gpt2_small": zero3_gpt2_small, "gpt2_xl_bucketed": gpt2_xl_bucketed, "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl,
        "one_rank_7p5b": one_rank_7p5b, "zero3_llama7b": zero3_llama7b}
 
 

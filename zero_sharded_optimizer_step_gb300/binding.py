@@ -17,6 +17,7 @@ ZERO_F32, ZERO_BF16, ZERO_F16 = 0, 1, 2
 ZERO_OK, ZERO_SKIPPED = 0, 1
 ZERO_EINVAL, ZERO_ECUDA, ZERO_EALIGN, ZERO_ESTATE = -1, -2, -3, -4
 ZERO_MAX_RANKS = 256
+ZERO_HYPER_BYTES = 128
 ZERO_GATHER_FAST, ZERO_GATHER_LEAN = 0, 1
 
 
@@ -57,6 +58,8 @@ _SIGS = {
     "zero_bind": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_bind_allreduce_out": (ctypes.c_int, [_ctxp, _vp]),
     "zero_set_weight_decay": (ctypes.c_int, [_ctxp, _f64]),
+    "zero_bind_hyper": (ctypes.c_int, [_ctxp, _vp]),
+    "zero_prepare_step": (ctypes.c_int, [_ctxp, _vp, _f64, _f64, _f64, _f64, _i64, _f32]),
     "zero_set_gather_mode": (ctypes.c_int, [_ctxp, _i32]),
     "zero_gather_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "zero_bind_shadow": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp]),
@@ -252,6 +255,18 @@ def zero_gather_timeouts() -> int:
     c = ctypes.c_uint32(0)
     _check(_L.zero_gather_timeouts(ctypes.byref(c)))
     return int(c.value)
+
+
+def zero_bind_hyper(ctx, d_hyper) -> None:
+    _check(_L.zero_bind_hyper(_h(ctx), _ptr(d_hyper)))
+
+
+def zero_prepare_step(ctx, host_hyper, lr: float, beta1: float, beta2: float, eps: float,
+                      t: int, loss_scale: float = 0.0) -> None:
+    """host_hyper: a host buffer of ZERO_HYPER_BYTES (a pinned uint8 tensor or an
+    int address)."""
+    _check(_L.zero_prepare_step(_h(ctx), _ptr(host_hyper), lr, beta1, beta2, eps, t,
+                                loss_scale))
 
 
 def zero_set_weight_decay(ctx, weight_decay: float) -> None:

@@ -75,6 +75,8 @@ struct zero_ctx {
     double weight_decay = 0.0;   // AdamW's decoupled decay; 0 = Adam
     int32_t gather_mode = 0;     // ZERO_GATHER_FAST or ZERO_GATHER_LEAN
 
+    void *hyper = nullptr;       // device block of per-step scalars (graph capture)
+
     uint64_t step_id = 0;
     bool step_scaled = false;
     bool bucket_open = false;    // between zero_bucket_begin and zero_bucket_end
@@ -236,6 +238,7 @@ StepArgs make_args(const zero_ctx *c, const Range &r, const void *const *grads)
     a.param_align = align_of(r.params);
     a.avg_align = r.grad_avg ? align_of(r.grad_avg) : 16;
     a.flag = reinterpret_cast<unsigned long long *>(c->flag);
+    a.hyper = static_cast<const zgb::DeviceHyper *>(c->hyper);
     bool ok = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16) &&
               (!a.g || aligned(a.g, 16)) &&
               (!a.cur || (aligned(a.xb, 16) && aligned(a.mb, 16) && aligned(a.vb, 16)));
@@ -247,6 +250,23 @@ StepArgs make_args(const zero_ctx *c, const Range &r, const void *const *grads)
     }
     a.vec_ok = ok ? 1 : 0;
     return a;
+}
+
+// Start a step: a new step id and whether it is loss-scaled.  With a device
+// block of scalars bound, zero_prepare_step has started it already (the
+// kernels of a captured graph take the id from the block); the call must then
+// take the prepared path.
+int begin_step(zero_ctx *c, bool scaled)
+{
+    if (c->hyper) {
+        if (c->step_id == 0) return fail(ZERO_ESTATE, "call zero_prepare_step first");
+        if (scaled != c->step_scaled)
+            return fail(ZERO_EINVAL, "loss scaling differs from the prepared step");
+        return ZERO_OK;
+    }
+    c->step_id += 1;
+    c->step_scaled = scaled;
+    return ZERO_OK;
 }
 
 int finish_launch(zero_ctx *c, cudaError_t e, const char *what, cudaStream_t s)
@@ -613,6 +633,36 @@ int zero_set_weight_decay(zero_ctx *c, double weight_decay)
     return ZERO_OK;
 }
 
+int zero_bind_hyper(zero_ctx *c, void *d_hyper)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    static_assert(sizeof(zgb::DeviceHyper) <= ZERO_HYPER_BYTES, "hyper block too large");
+    if (!aligned(d_hyper, 16)) return fail(ZERO_EALIGN, "the hyper block must be 16-byte aligned");
+    c->hyper = d_hyper;
+    return ZERO_OK;
+}
+
+int zero_prepare_step(zero_ctx *c, void *host_hyper, double lr, double b1, double b2,
+                      double eps, int64_t t, float loss_scale)
+{
+    if (!c || !host_hyper) return fail(ZERO_EINVAL, "null argument");
+    if (!c->hyper) return fail(ZERO_ESTATE, "no device hyper block bound (zero_bind_hyper)");
+    if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open");
+    int rc = check_hyper(t);
+    if (rc) return rc;
+    c->step_id += 1;
+    c->step_scaled = loss_scale > 0.0f;
+    zgb::DeviceHyper h;
+    memset(&h, 0, sizeof h);
+    h.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
+    h.av = average_scalars(c->world, loss_scale);
+    h.flag_id = c->step_id;
+    h.skip_id = c->step_scaled ? c->step_id : ~0ull;
+    memset(host_hyper, 0, ZERO_HYPER_BYTES);
+    memcpy(host_hyper, &h, sizeof h);
+    return ZERO_OK;
+}
+
 int zero_bind_allreduce_out(zero_ctx *c, void *grad_avg)
 {
     if (!c) return fail(ZERO_EINVAL, "null context");
@@ -634,8 +684,7 @@ int zero_step_reduce(zero_ctx *c, const void *const *grads, int32_t n_grads, flo
     const Range r = vector_range(c);
     rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
     if (rc) return rc;
-    c->step_id += 1;
-    c->step_scaled = loss_scale > 0.0f;
+    if ((rc = begin_step(c, loss_scale > 0.0f))) return rc;
     return do_reduce(c, r, grads, loss_scale, (cudaStream_t)stream);
 }
 
@@ -664,20 +713,17 @@ int zero_step(zero_ctx *c, const void *const *grads, int32_t n_grads, double lr,
     cudaStream_t s = (cudaStream_t)stream;
     if (c->cur) {
         // two state sets: one pass whatever the loss scale
-        c->step_id += 1;
-        c->step_scaled = loss_scale > 0.0f;
+        if ((rc = begin_step(c, loss_scale > 0.0f))) return rc;
         return do_fused(c, r, grads, lr, b1, b2, eps, t, s, loss_scale);
     }
     if (loss_scale > 0.0f) {
         if (!c->g) return fail(ZERO_ESTATE, "a loss-scaled step needs g_scratch (zero_bind)");
-        c->step_id += 1;
-        c->step_scaled = true;
+        if ((rc = begin_step(c, true))) return rc;
         rc = do_reduce(c, r, grads, loss_scale, s);
         if (rc) return rc;
         return do_apply(c, r, lr, b1, b2, eps, t, s);
     }
-    c->step_id += 1;
-    c->step_scaled = false;
+    if ((rc = begin_step(c, false))) return rc;
     return do_fused(c, r, grads, lr, b1, b2, eps, t, s);
 }
 
@@ -688,8 +734,8 @@ int zero_bucket_begin(zero_ctx *c, float loss_scale)
     if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is already open");
     if (loss_scale > 0.0f && !c->cur && !c->g)
         return fail(ZERO_ESTATE, "a loss-scaled bucketed step needs g_scratch or a second state set");
-    c->step_id += 1;
-    c->step_scaled = loss_scale > 0.0f;
+    int rc = begin_step(c, loss_scale > 0.0f);
+    if (rc) return rc;
     c->bucket_scale = loss_scale;
     c->bucket_open = true;
     return ZERO_OK;
@@ -793,6 +839,10 @@ int zero3_begin_step(zero_ctx *c)
 {
     if (!c) return fail(ZERO_EINVAL, "null context");
     if (c->stage != 3) return fail(ZERO_EINVAL, "zero3_begin_step is for stage 3");
+    if (c->hyper) {
+        if (c->step_id == 0) return fail(ZERO_ESTATE, "call zero_prepare_step first");
+        return ZERO_OK;      // the prepared step (loss scaling chosen there)
+    }
     c->step_id += 1;
     c->step_scaled = false;
     return ZERO_OK;
@@ -843,7 +893,12 @@ int zero3_reduce_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32
     const Range r = unit_range(c, unit);
     rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
     if (rc) return rc;
-    if (loss_scale > 0.0f) c->step_scaled = true;
+    if (c->hyper) {
+        if ((loss_scale > 0.0f) != c->step_scaled)
+            return fail(ZERO_EINVAL, "loss scaling differs from the prepared step");
+    } else if (loss_scale > 0.0f) {
+        c->step_scaled = true;
+    }
     return do_reduce(c, r, grads, loss_scale, (cudaStream_t)stream);
 }
 
@@ -905,8 +960,7 @@ extern "C" int zero_step_noalloc(zero_ctx *c, const void *const *grads, int32_t 
     float *scratch = nullptr;
     if ((rc = noalloc_scratch_address(&scratch))) return rc;
     cudaStream_t s = (cudaStream_t)stream;
-    c->step_id += 1;
-    c->step_scaled = loss_scale > 0.0f;
+    if ((rc = begin_step(c, loss_scale > 0.0f))) return rc;
     if (r.n == 0) return ZERO_OK;
 
     StepArgs a = make_args(c, r, grads);

@@ -30,6 +30,15 @@ struct AverageScalars {
     int32_t world_pow2, scaled, scale_pow2, pad_;
 };
 
+// Per-step scalars in device memory, for steps captured in a CUDA graph: the
+// kernels read them at run time instead of taking them as launch arguments.
+struct DeviceHyper {
+    AdamScalars ad;
+    AverageScalars av;
+    unsigned long long flag_id;   // id a pass records a non-finite grad under
+    unsigned long long skip_id;   // id apply/finalize treat as "skip" (~0 = never)
+};
+
 // Arguments of the per-element step kernels over one contiguous range of
 // `n` elements of the state.  Every pointer is already offset to the
 // range's first element.
@@ -51,6 +60,7 @@ struct StepArgs {
     unsigned long long *cur;
     unsigned long long *flag;      // id of the latest step with a non-finite grad
     unsigned long long step_id;
+    const DeviceHyper *hyper;      // when set, ad/av/step_id come from here
     AverageScalars av;
     AdamScalars ad;
 };

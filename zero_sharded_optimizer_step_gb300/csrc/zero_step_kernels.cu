@@ -279,9 +279,32 @@ __device__ __forceinline__ void store_state8(float *p, int64_t i, const float (&
 
 // One block-wide OR of the per-thread overflow bits, then at most one atomic
 // per block.  Every thread of the block reaches this point.
-__device__ __forceinline__ void publish_flag(const StepArgs &a, bool bad)
+__device__ __forceinline__ void publish_flag(const StepArgs &a, bool bad, unsigned long long id)
 {
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicMax(a.flag, a.step_id);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicMax(a.flag, id);
+}
+
+// The step's scalars: from the launch arguments, or, for a step captured in
+// a CUDA graph, from the device block written before the kernels run.
+struct Scalars {
+    AdamScalars ad;
+    AverageScalars av;
+    unsigned long long id;
+};
+
+__device__ __forceinline__ Scalars step_scalars(const StepArgs &a, bool publishing)
+{
+    Scalars s;
+    if (a.hyper) {
+        s.ad = a.hyper->ad;
+        s.av = a.hyper->av;
+        s.id = publishing ? a.hyper->flag_id : a.hyper->skip_id;
+    } else {
+        s.ad = a.ad;
+        s.av = a.av;
+        s.id = a.step_id;
+    }
+    return s;
 }
 
 // Where a pass reads and writes the state.  One set: in place.  Two sets:
@@ -321,6 +344,7 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
     const StatePtrs st = select_state(a, true);
+    const Scalars sc = step_scalars(a, true);
     bool bad = false;
     for (int64_t k = tid; k < nvec; k += stride) {
         const int64_t i = k * kVec;
@@ -334,16 +358,16 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
         for (int e = 0; e < kVec; ++e) {
             if (AVG) {
                 // the all-reduce mean itself, before unscaling
-                acc[e] = a.av.world_pow2 ? __fmul_rn(acc[e], a.av.inv_world)
-                                         : __fdiv_rn(acc[e], a.av.world_f);
-                g[e] = !a.av.scaled ? acc[e]
-                       : (a.av.scale_pow2 ? __fmul_rn(acc[e], a.av.inv_scale)
-                                          : __fdiv_rn(acc[e], a.av.scale));
+                acc[e] = sc.av.world_pow2 ? __fmul_rn(acc[e], sc.av.inv_world)
+                                         : __fdiv_rn(acc[e], sc.av.world_f);
+                g[e] = !sc.av.scaled ? acc[e]
+                       : (sc.av.scale_pow2 ? __fmul_rn(acc[e], sc.av.inv_scale)
+                                          : __fdiv_rn(acc[e], sc.av.scale));
             } else {
-                g[e] = average(acc[e], a.av);
+                g[e] = average(acc[e], sc.av);
             }
             bad |= nonfinite(g[e]);
-            adam1(g[e], x[e], m[e], v[e], a.ad);
+            adam1(g[e], x[e], m[e], v[e], sc.ad);
         }
         store_state8(st.dx, i, x);
         store_state8(st.dm, i, m);
@@ -354,19 +378,19 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
     // per-element path: ragged tail, padding, unaligned buffers
     for (int64_t i = nvec * kVec + tid; i < a.n; i += stride) {
         float acc = rank_sum1<GT>(a, i);
-        float mean = a.av.world_pow2 ? __fmul_rn(acc, a.av.inv_world) : __fdiv_rn(acc, a.av.world_f);
-        float g = !a.av.scaled ? mean
-                  : (a.av.scale_pow2 ? __fmul_rn(mean, a.av.inv_scale) : __fdiv_rn(mean, a.av.scale));
+        float mean = sc.av.world_pow2 ? __fmul_rn(acc, sc.av.inv_world) : __fdiv_rn(acc, sc.av.world_f);
+        float g = !sc.av.scaled ? mean
+                  : (sc.av.scale_pow2 ? __fmul_rn(mean, sc.av.inv_scale) : __fdiv_rn(mean, sc.av.scale));
         bad |= nonfinite(g);
         float x = st.sx[i], m = st.sm[i], v = st.sv[i];
-        adam1(g, x, m, v, a.ad);
+        adam1(g, x, m, v, sc.ad);
         st.dx[i] = x;
         st.dm[i] = m;
         st.dv[i] = v;
         Ty<PT>::store1(a.params, i, x);
         if (AVG) Ty<GT>::store1(a.grad_avg, i, mean);
     }
-    publish_flag(a, bad);
+    publish_flag(a, bad, sc.id);
 }
 
 template <int GT, bool AVG>
@@ -376,6 +400,7 @@ reduce_kernel(const __grid_constant__ StepArgs a)
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
+    const Scalars sc = step_scalars(a, true);
     bool bad = false;
     for (int64_t k = tid; k < nvec; k += stride) {
         const int64_t i = k * kVec;
@@ -383,11 +408,11 @@ reduce_kernel(const __grid_constant__ StepArgs a)
         rank_sum8<GT>(a, i, acc);
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
-            acc[e] = a.av.world_pow2 ? __fmul_rn(acc[e], a.av.inv_world)
-                                     : __fdiv_rn(acc[e], a.av.world_f);
-            g[e] = !a.av.scaled ? acc[e]
-                   : (a.av.scale_pow2 ? __fmul_rn(acc[e], a.av.inv_scale)
-                                      : __fdiv_rn(acc[e], a.av.scale));
+            acc[e] = sc.av.world_pow2 ? __fmul_rn(acc[e], sc.av.inv_world)
+                                     : __fdiv_rn(acc[e], sc.av.world_f);
+            g[e] = !sc.av.scaled ? acc[e]
+                   : (sc.av.scale_pow2 ? __fmul_rn(acc[e], sc.av.inv_scale)
+                                      : __fdiv_rn(acc[e], sc.av.scale));
             bad |= nonfinite(g[e]);
         }
         store_state8(a.g, i, g);
@@ -395,14 +420,14 @@ reduce_kernel(const __grid_constant__ StepArgs a)
     }
     for (int64_t i = nvec * kVec + tid; i < a.n; i += stride) {
         float acc = rank_sum1<GT>(a, i);
-        float mean = a.av.world_pow2 ? __fmul_rn(acc, a.av.inv_world) : __fdiv_rn(acc, a.av.world_f);
-        float g = !a.av.scaled ? mean
-                  : (a.av.scale_pow2 ? __fmul_rn(mean, a.av.inv_scale) : __fdiv_rn(mean, a.av.scale));
+        float mean = sc.av.world_pow2 ? __fmul_rn(acc, sc.av.inv_world) : __fdiv_rn(acc, sc.av.world_f);
+        float g = !sc.av.scaled ? mean
+                  : (sc.av.scale_pow2 ? __fmul_rn(mean, sc.av.inv_scale) : __fdiv_rn(mean, sc.av.scale));
         bad |= nonfinite(g);
         a.g[i] = g;
         if (AVG) Ty<GT>::store1(a.grad_avg, i, mean);
     }
-    publish_flag(a, bad);
+    publish_flag(a, bad, sc.id);
 }
 
 template <int PT>
@@ -410,7 +435,8 @@ __global__ void __launch_bounds__(kThreads)
 apply_kernel(const __grid_constant__ StepArgs a)
 {
     // The verdict of the whole step is known: a skipped step writes nothing.
-    if (*reinterpret_cast<volatile unsigned long long *>(a.flag) == a.step_id) return;
+    const Scalars sc = step_scalars(a, false);
+    if (*reinterpret_cast<volatile unsigned long long *>(a.flag) == sc.id) return;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n / kVec : 0;
@@ -423,7 +449,7 @@ apply_kernel(const __grid_constant__ StepArgs a)
         load_state8(st.sm, i, m);
         load_state8(st.sv, i, v);
 #pragma unroll
-        for (int e = 0; e < kVec; ++e) adam1(g[e], x[e], m[e], v[e], a.ad);
+        for (int e = 0; e < kVec; ++e) adam1(g[e], x[e], m[e], v[e], sc.ad);
         store_state8(st.dx, i, x);
         store_state8(st.dm, i, m);
         store_state8(st.dv, i, v);
@@ -431,7 +457,7 @@ apply_kernel(const __grid_constant__ StepArgs a)
     }
     for (int64_t i = nvec * kVec + tid; i < a.n; i += stride) {
         float x = st.sx[i], m = st.sm[i], v = st.sv[i];
-        adam1(a.g[i], x, m, v, a.ad);
+        adam1(a.g[i], x, m, v, sc.ad);
         st.dx[i] = x;
         st.dm[i] = m;
         st.dv[i] = v;
@@ -443,8 +469,9 @@ template <int PT>
 __global__ void __launch_bounds__(kThreads)
 finalize_kernel(const __grid_constant__ StepArgs a)
 {
+    const unsigned long long skip_id = a.hyper ? a.hyper->skip_id : a.step_id;
     const bool overflowed =
-        *reinterpret_cast<volatile unsigned long long *>(a.flag) == a.step_id;
+        *reinterpret_cast<volatile unsigned long long *>(a.flag) == skip_id;
     if (!overflowed) {
         // the set the step wrote becomes current; no block reads the word here
         if (blockIdx.x == 0 && threadIdx.x == 0) *a.cur ^= 1ull;
