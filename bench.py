@@ -42,9 +42,9 @@ import numpy as np  # noqa: E402
 # one pass; summarised under profiles/).  Each entry is valid only for the
 # kernel source it was taken on (sha256 prefix); otherwise bench reports null.
 TRAFFIC = {
-    ("gpt2_xl", "fused_step_kernel"): ("191a346d13c7fd77", 68.54e9 + 22.32e9),
-    ("one_rank_7p5b", "gather_kernel"): ("d48998624012af79", 14.79e9 + 14.72e9),
-    ("one_rank_7p5b", "fused_step_kernel"): ("191a346d13c7fd77", 16.41e9 + 1.94e9),
+    ("gpt2_xl", "fused_step_kernel"): ("a50021f501aff811", 68.538e9 + 21.778e9),
+    ("one_rank_7p5b", "gather_kernel"): ("d48998624012af79", 14.787e9 + 14.721e9),
+    ("one_rank_7p5b", "fused_step_kernel"): ("a50021f501aff811", 16.406e9 + 1.621e9),
     # the 2-unit capture has the full workload's launch sizes
     ("zero3_llama7b", "gather_kernel"): ("d48998624012af79", 404.80128e6 + 353.814272e6),
 }

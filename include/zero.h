@@ -290,7 +290,8 @@ int zero_step_reduce(zero_ctx *ctx, const void *const *grads, int32_t n_grads,
  * case the kernel returns without writing.  In the one-rank view the flag
  * word may first be combined with the other ranks' words (a MAX
  * all-reduce in a multi-process deployment); for stage 3 call it once after
- * every unit's zero3_reduce_unit. */
+ * every unit's zero3_reduce_unit.  ZERO_ESTATE while a bucketed step is
+ * open. */
 int zero_step_apply(zero_ctx *ctx, double lr, double beta1, double beta2, double eps,
                     int64_t t, void *stream);
 
@@ -414,7 +415,8 @@ int zero3_reduce_unit(zero_ctx *ctx, int32_t unit, const void *const *grads,
  *     overlap on the GPU (different streams, or contexts used concurrently)
  *     race on the array and corrupt each other's results; calls on one
  *     stream are ordered and safe.
- * The verdict is read with zero_step_status() as for zero_step. */
+ * ZERO_ESTATE while a bucketed step is open.  The verdict is read with
+ * zero_step_status() as for zero_step. */
 int zero_step_noalloc(zero_ctx *ctx, const void *const *grads, int32_t n_grads, double lr,
                       double beta1, double beta2, double eps, int64_t t, float loss_scale,
                       void *stream);

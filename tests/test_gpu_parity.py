@@ -498,7 +498,13 @@ def test_bucket_protocol_errors():
         z.zero_step(run.ctx, g, 1e-3, 0.9, 0.999, 1e-8, 1)
     with pytest.raises(z.ZeroError):                       # twice begun
         z.zero_bucket_begin(run.ctx)
+    with pytest.raises(z.ZeroError):                       # apply pass while open
+        z.zero_step_apply(run.ctx, 1e-3, 0.9, 0.999, 1e-8, 1)
+    with pytest.raises(z.ZeroError):                       # built-in scratch step while open
+        z.zero_step_noalloc(run.ctx, g, 1e-3, 0.9, 0.999, 1e-8, 1)
+    id_open = z.zero_step_id(run.ctx)
     z.zero_bucket_end(run.ctx, 1e-3, 0.9, 0.999, 1e-8, 1)
+    assert z.zero_step_id(run.ctx) == id_open              # the refused calls began no step
     with pytest.raises(z.ZeroError):                       # loss-scaled, no scratch or set
         z.zero_bucket_begin(run.ctx, 1024.0)
     run.close()
@@ -506,29 +512,40 @@ def test_bucket_protocol_errors():
 
 # --------------------------------------------------- ZeRO-3 with prefetch
 
-def test_zero3_prefetch_schedule_matches_serial_and_oracle():
+@pytest.mark.parametrize("rank,scaled", [(2, False), (-1, True), (1, True)])
+def test_zero3_prefetch_schedule_matches_serial_and_oracle(rank, scaled):
     """Gathers prefetched on a second stream into alternating unit buffers
-    leave every result as the serial schedule and the oracle have it."""
+    leave every result as the serial schedule and the oracle have it; with
+    loss scaling (Adam deferred to one apply after the last unit) the step
+    with a planted +inf is skipped by every unit."""
     from workloads.runner import Runner
     from workloads.zero3_schedule import Zero3Schedule
     units = [200_003, 150_000, 99_999, 250_000]
-    w = W.Workload("z3p", sum(units), 4, 3, W.BF16, W.BF16, rank=2, units=units, steps=3)
+    w = W.Workload("z3p", sum(units), 4, 3, W.BF16, W.BF16, rank=rank, units=units, steps=4,
+                   loss_scale=2.0 ** 10 if scaled else 0.0, inject=(2, 1) if scaled else None)
     runs = {}
     for mode in ("serial", "overlap"):
         run = Runner(w)
         sch = Zero3Schedule(run, 2000, 4000, 64, mode)
-        for it in range(1, 4):
+        for it in range(1, 5):
             run.fill_grads(it)
             sch.launch_step()
+            if scaled:
+                run.finish_step()
         torch.cuda.synchronize()
         runs[mode] = run
     ref = refs.OracleRun(w)
-    for it in range(1, 4):
+    for it in range(1, 5):
         ref.step(it)
     for a, b in [(runs["serial"].master, runs["overlap"].master),
                  (runs["serial"].params, runs["overlap"].params)]:
         assert torch.equal(a, b)
-    runs["overlap"].skips = ref.skips
+    if scaled:
+        for run in runs.values():
+            assert run.skips == ref.skips
+        assert ref.skips == [0, 1, 0, 0]      # the +inf lands in rank 1's part of unit 0
+    else:
+        runs["overlap"].skips = ref.skips
     compare_runner(runs["overlap"], ref, what="prefetch")
 
 

@@ -169,10 +169,11 @@ class Runner:
         if w.inject and w.inject[0] == it:
             k = w.inject[1]
             e = inject_index(w, it, k)
+            S0 = w.unit_shard(0) if w.units else w.shard     # the planted value is in unit 0
             if w.rank < 0:
                 self.grads[0][k][e] = float("inf")
-            elif w.rank * w.shard <= e < (w.rank + 1) * w.shard:
-                self.grads[0][k][e - w.rank * w.shard] = float("inf")
+            elif w.rank * S0 <= e < (w.rank + 1) * S0:
+                self.grads[0][k][e - w.rank * S0] = float("inf")
 
     # --------------------------------------------------------------- step
 

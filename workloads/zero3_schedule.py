@@ -8,6 +8,11 @@ Visits: forward over units 0..U-1, then backward over U-1..0, each backward
 visit followed by that unit's reduce + Adam.  Two unit buffers alternate:
 the gather for visit v+1 writes the buffer visit v-1 used, so it waits for
 visit v-1's compute to finish.
+
+With loss scaling the backward visit only reduces (and unscales) its unit's
+grads; Adam waits until every unit's overflow flag is in, and one apply pass
+after the last visit updates all units or, on overflow, none ("PaddlePaddle
+ZeRO优化", section 混合精度才是最佳拍档: the scaler skips the whole step).
 """
 from __future__ import annotations
 
@@ -47,12 +52,22 @@ class Zero3Schedule:
         u, phase = self.visits[v]
         standin.busy(self.sink.data_ptr(), self.blocks, self.iters[phase], stream.cuda_stream)
         if phase == "b":
-            w = self.run.w
-            z.zero3_step_unit(self.run.ctx, u, self.run.grads[u], w.lr, w.beta1, w.beta2,
-                              w.eps, self.run.t + 1, stream)
+            run, w = self.run, self.run.w
+            if run.scale > 0:
+                z.zero3_reduce_unit(run.ctx, u, run.grads[u], run.scale, stream)
+            else:
+                z.zero3_step_unit(run.ctx, u, run.grads[u], w.lr, w.beta1, w.beta2,
+                                  w.eps, run.t + 1, stream)
+
+    def _apply(self, stream):
+        run, w = self.run, self.run.w
+        if run.scale > 0:
+            z.zero_step_apply(run.ctx, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, stream)
 
     def launch_step(self):
-        """Launch one whole step (no synchronization)."""
+        """Launch one whole step (no synchronization).  A step without loss
+        scaling always applies and advances t here; a loss-scaled one leaves t
+        and the scale to run.finish_step(), which reads the verdict."""
         run = self.run
         cs = self.cs if self.mode == "overlap" else run.stream
         if cs is not run.stream:
@@ -64,6 +79,7 @@ class Zero3Schedule:
                 if self.mode == "serial":
                     self._gather(v, cs)
                 self._compute(v, cs)
+            self._apply(cs)
         else:
             gs = self.gs
             gs.wait_stream(cs)            # the shards the last step wrote
@@ -78,6 +94,8 @@ class Zero3Schedule:
                         gs.wait_event(self.used[v - 1])   # its buffer is free again
                     self._gather(v + 1, gs)
                     self.ready[v + 1].record(gs)
+            self._apply(cs)
             cs.wait_stream(gs)
             run.stream.wait_stream(cs)
-        run.t += 1
+        if run.scale <= 0:
+            run.t += 1

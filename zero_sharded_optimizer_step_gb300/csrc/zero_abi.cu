@@ -694,6 +694,7 @@ int zero_step_apply(zero_ctx *c, double lr, double b1, double b2, double eps, in
     int rc = check_ready(c);
     if (rc) return rc;
     if ((rc = check_hyper(t))) return rc;
+    if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
     if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
     if (c->step_id == 0) return fail(ZERO_ESTATE, "no reduce pass ran before apply");
     return do_apply(c, apply_range(c), lr, b1, b2, eps, t, (cudaStream_t)stream);
@@ -949,6 +950,7 @@ extern "C" int zero_step_noalloc(zero_ctx *c, const void *const *grads, int32_t 
     if (rc) return rc;
     if ((rc = check_hyper(t))) return rc;
     if (c->stage == 3) return fail(ZERO_EINVAL, "zero_step_noalloc covers stages 1 and 2");
+    if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
     const Range r = vector_range(c);
     if (r.n > kNoAllocScratchFloats)
         return fail(ZERO_EINVAL,

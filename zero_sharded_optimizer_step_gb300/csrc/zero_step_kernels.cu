@@ -284,27 +284,26 @@ __device__ __forceinline__ void publish_flag(const StepArgs &a, bool bad, unsign
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicMax(a.flag, id);
 }
 
-// The step's scalars: from the launch arguments, or, for a step captured in
-// a CUDA graph, from the device block written before the kernels run.
-struct Scalars {
-    AdamScalars ad;
-    AverageScalars av;
+// The step's scalars.  An eager launch reads them straight from the kernel's
+// parameters (constant-bank operands: no registers held across the loop).  A
+// step captured in a CUDA graph (HYPER) reads them from the device block
+// written before its kernels run.  The choice is a template argument, so
+// the eager kernels carry neither a branch nor a copy of the scalars.
+template <bool HYPER>
+struct ScalarRefs {
+    const AdamScalars &ad;
+    const AverageScalars &av;
     unsigned long long id;
 };
 
-__device__ __forceinline__ Scalars step_scalars(const StepArgs &a, bool publishing)
+template <bool HYPER>
+__device__ __forceinline__ ScalarRefs<HYPER> step_scalars(const StepArgs &a, bool publishing)
 {
-    Scalars s;
-    if (a.hyper) {
-        s.ad = a.hyper->ad;
-        s.av = a.hyper->av;
-        s.id = publishing ? a.hyper->flag_id : a.hyper->skip_id;
-    } else {
-        s.ad = a.ad;
-        s.av = a.av;
-        s.id = a.step_id;
-    }
-    return s;
+    if constexpr (HYPER)
+        return ScalarRefs<HYPER>{a.hyper->ad, a.hyper->av,
+                                 publishing ? a.hyper->flag_id : a.hyper->skip_id};
+    else
+        return ScalarRefs<HYPER>{a.ad, a.av, a.step_id};
 }
 
 // Where a pass reads and writes the state.  One set: in place.  Two sets:
@@ -333,41 +332,52 @@ __device__ __forceinline__ StatePtrs select_state(const StepArgs &a, bool fresh)
 // per-thread chunk); two with fp32 grads, whose eight-element vectors need
 // twice the load registers.
 template <int GT> struct MinBlocks { static constexpr int value = GT == F32 ? 2 : 4; };
+// The fused kernel of a graph-captured step holds its scalars in registers
+// (they come from memory, not the constant bank): three blocks per SM leave
+// it room enough not to spill, which measured faster than four that spill.
+template <int GT, bool HYPER> struct MinBlocksFused {
+    static constexpr int value = HYPER && GT != F32 ? 3 : MinBlocks<GT>::value;
+};
 
 // ---------------------------------------------------------------- kernels
 
-template <int GT, int PT, bool AVG>
-__global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
+template <int GT, int PT, bool AVG, bool HYPER>
+__global__ void __launch_bounds__(kThreads, MinBlocksFused<GT, HYPER>::value)
 fused_step_kernel(const __grid_constant__ StepArgs a)
 {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
     const StatePtrs st = select_state(a, true);
-    const Scalars sc = step_scalars(a, true);
+    const ScalarRefs<HYPER> sc = step_scalars<HYPER>(a, true);
+    const AverageScalars &av = sc.av;
+    const AdamScalars &ad = sc.ad;
     bool bad = false;
     for (int64_t k = tid; k < nvec; k += stride) {
         const int64_t i = k * kVec;
         float x[kVec], m[kVec], v[kVec], acc[kVec];
+        // the ranks' grads first, then the state: the state's 24 registers
+        // are not held through the rank sum, so the kernel fits 64 registers
+        // (four blocks per SM) without spilling
+        rank_sum8<GT>(a, i, acc);
         load_state8(st.sx, i, x);
         load_state8(st.sm, i, m);
         load_state8(st.sv, i, v);
-        rank_sum8<GT>(a, i, acc);
         float g[kVec];
 #pragma unroll
         for (int e = 0; e < kVec; ++e) {
             if (AVG) {
                 // the all-reduce mean itself, before unscaling
-                acc[e] = sc.av.world_pow2 ? __fmul_rn(acc[e], sc.av.inv_world)
-                                         : __fdiv_rn(acc[e], sc.av.world_f);
-                g[e] = !sc.av.scaled ? acc[e]
-                       : (sc.av.scale_pow2 ? __fmul_rn(acc[e], sc.av.inv_scale)
-                                          : __fdiv_rn(acc[e], sc.av.scale));
+                acc[e] = av.world_pow2 ? __fmul_rn(acc[e], av.inv_world)
+                                       : __fdiv_rn(acc[e], av.world_f);
+                g[e] = !av.scaled ? acc[e]
+                       : (av.scale_pow2 ? __fmul_rn(acc[e], av.inv_scale)
+                                        : __fdiv_rn(acc[e], av.scale));
             } else {
-                g[e] = average(acc[e], sc.av);
+                g[e] = average(acc[e], av);
             }
             bad |= nonfinite(g[e]);
-            adam1(g[e], x[e], m[e], v[e], sc.ad);
+            adam1(g[e], x[e], m[e], v[e], ad);
         }
         store_state8(st.dx, i, x);
         store_state8(st.dm, i, m);
@@ -378,12 +388,12 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
     // per-element path: ragged tail, padding, unaligned buffers
     for (int64_t i = nvec * kVec + tid; i < a.n; i += stride) {
         float acc = rank_sum1<GT>(a, i);
-        float mean = sc.av.world_pow2 ? __fmul_rn(acc, sc.av.inv_world) : __fdiv_rn(acc, sc.av.world_f);
-        float g = !sc.av.scaled ? mean
-                  : (sc.av.scale_pow2 ? __fmul_rn(mean, sc.av.inv_scale) : __fdiv_rn(mean, sc.av.scale));
+        float mean = av.world_pow2 ? __fmul_rn(acc, av.inv_world) : __fdiv_rn(acc, av.world_f);
+        float g = !av.scaled ? mean
+                  : (av.scale_pow2 ? __fmul_rn(mean, av.inv_scale) : __fdiv_rn(mean, av.scale));
         bad |= nonfinite(g);
         float x = st.sx[i], m = st.sm[i], v = st.sv[i];
-        adam1(g, x, m, v, sc.ad);
+        adam1(g, x, m, v, ad);
         st.dx[i] = x;
         st.dm[i] = m;
         st.dv[i] = v;
@@ -393,14 +403,14 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
     publish_flag(a, bad, sc.id);
 }
 
-template <int GT, bool AVG>
+template <int GT, bool AVG, bool HYPER>
 __global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
 reduce_kernel(const __grid_constant__ StepArgs a)
 {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
-    const Scalars sc = step_scalars(a, true);
+    const ScalarRefs<HYPER> sc = step_scalars<HYPER>(a, true);
     bool bad = false;
     for (int64_t k = tid; k < nvec; k += stride) {
         const int64_t i = k * kVec;
@@ -430,12 +440,12 @@ reduce_kernel(const __grid_constant__ StepArgs a)
     publish_flag(a, bad, sc.id);
 }
 
-template <int PT>
+template <int PT, bool HYPER>
 __global__ void __launch_bounds__(kThreads)
 apply_kernel(const __grid_constant__ StepArgs a)
 {
     // The verdict of the whole step is known: a skipped step writes nothing.
-    const Scalars sc = step_scalars(a, false);
+    const ScalarRefs<HYPER> sc = step_scalars<HYPER>(a, false);
     if (*reinterpret_cast<volatile unsigned long long *>(a.flag) == sc.id) return;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -514,12 +524,18 @@ int64_t items(const StepArgs &a, int64_t nvec_src)
     return nvec > tail ? nvec : tail;
 }
 
+template <int GT, int PT, bool HYPER>
+cudaError_t fused_h(const StepArgs &a, int sms, cudaStream_t s)
+{
+    const int64_t w = items(a, a.n_valid);
+    return a.grad_avg ? launch(fused_step_kernel<GT, PT, true, HYPER>, a, w, sms, s)
+                      : launch(fused_step_kernel<GT, PT, false, HYPER>, a, w, sms, s);
+}
+
 template <int GT, int PT>
 cudaError_t fused_pt(const StepArgs &a, int sms, cudaStream_t s)
 {
-    const int64_t w = items(a, a.n_valid);
-    return a.grad_avg ? launch(fused_step_kernel<GT, PT, true>, a, w, sms, s)
-                      : launch(fused_step_kernel<GT, PT, false>, a, w, sms, s);
+    return a.hyper ? fused_h<GT, PT, true>(a, sms, s) : fused_h<GT, PT, false>(a, sms, s);
 }
 
 template <int GT>
@@ -533,12 +549,26 @@ cudaError_t fused_gt(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s)
     return cudaErrorInvalidValue;
 }
 
+template <int GT, bool HYPER>
+cudaError_t reduce_h(const StepArgs &a, int sms, cudaStream_t s)
+{
+    const int64_t w = items(a, a.n_valid);
+    return a.grad_avg ? launch(reduce_kernel<GT, true, HYPER>, a, w, sms, s)
+                      : launch(reduce_kernel<GT, false, HYPER>, a, w, sms, s);
+}
+
 template <int GT>
 cudaError_t reduce_gt(const StepArgs &a, int sms, cudaStream_t s)
 {
-    const int64_t w = items(a, a.n_valid);
-    return a.grad_avg ? launch(reduce_kernel<GT, true>, a, w, sms, s)
-                      : launch(reduce_kernel<GT, false>, a, w, sms, s);
+    return a.hyper ? reduce_h<GT, true>(a, sms, s) : reduce_h<GT, false>(a, sms, s);
+}
+
+template <int PT>
+cudaError_t apply_pt(const StepArgs &a, int sms, cudaStream_t s)
+{
+    const int64_t w = items(a, a.n);
+    return a.hyper ? launch(apply_kernel<PT, true>, a, w, sms, s)
+                   : launch(apply_kernel<PT, false>, a, w, sms, s);
 }
 
 }  // namespace
@@ -577,11 +607,10 @@ cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, cudaStream_
 
 cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s)
 {
-    const int64_t w = items(a, a.n);
     switch (pdt) {
-    case F32: return launch(apply_kernel<F32>, a, w, sms, s);
-    case BF16: return launch(apply_kernel<BF16>, a, w, sms, s);
-    case F16: return launch(apply_kernel<F16>, a, w, sms, s);
+    case F32: return apply_pt<F32>(a, sms, s);
+    case BF16: return apply_pt<BF16>(a, sms, s);
+    case F16: return apply_pt<F16>(a, sms, s);
     }
     return cudaErrorInvalidValue;
 }
