@@ -93,10 +93,10 @@ def compare_runner(run, ref, exact=True, what=""):
                                  "%s %s" % (what, name))
 
 
-def run_both(w, iters=None, shadow=False):
+def run_both(w, iters=None, shadow=False, hyper=False):
     from workloads.runner import Runner
     iters = iters or list(range(1, w.steps + 1))
-    run = Runner(w, shadow=shadow)
+    run = Runner(w, shadow=shadow, hyper=hyper)
     ref = refs.OracleRun(w)
     for it in iters:
         run.step(it)
@@ -723,6 +723,66 @@ def test_loss_scaled_single_pass_replayed_with_a_skip():
         ref.step(it)
     assert run.skips == ref.skips == [False, True, False, False]
     compare_runner(run, ref, what="graph shadow")
+    run.close()
+
+
+HYPER_CASES = [(dict(gdt=g, pdt=p), {}) for g, p in
+               [(W.BF16, W.BF16), (W.F16, W.F16), (W.F32, W.F32), (W.BF16, W.F32),
+                (W.F32, W.BF16), (W.F16, W.BF16), (W.BF16, W.F16), (W.F32, W.F16),
+                (W.F16, W.F32)]]
+HYPER_CASES += [
+    (dict(gdt=W.F16, pdt=W.F16, loss_scale=2.0 ** 10, inject=(2, 3)), {}),            # two passes
+    (dict(gdt=W.F16, pdt=W.F16, loss_scale=2.0 ** 10, inject=(2, 3)), {"shadow": True}),
+    (dict(gdt=W.BF16, pdt=W.BF16, weight_decay=0.1), {"shadow": True}),               # AdamW
+    (dict(gdt=W.F16, pdt=W.F32, rank=5, world=16), {}),
+    (dict(gdt=W.BF16, pdt=W.BF16, bucket=100_000, loss_scale=2.0 ** 8, inject=(2, 1)),
+     {"shadow": True}),
+    (dict(gdt=W.BF16, pdt=W.BF16, bucket=100_000, loss_scale=2.0 ** 8, inject=(2, 1)), {}),
+    (dict(gdt=W.BF16, pdt=W.BF16, units=[300_001, 77, 123_456], rank=1), {}),
+    (dict(gdt=W.BF16, pdt=W.BF16, units=[300_001, 77, 123_456], loss_scale=2.0 ** 8,
+          inject=(2, 2)), {}),
+]
+
+
+@pytest.mark.parametrize("spec,kw", HYPER_CASES)
+def test_device_scalar_block_parity(spec, kw):
+    """The kernels compiled to read the step's scalars from a device block
+    (the form a CUDA graph replays) over the dtype matrix and every path --
+    fused, two passes, two state sets, AdamW, one rank's view, buckets,
+    ZeRO-3 units, with and without a skipped step -- run eagerly with the
+    block refreshed before each step and junk hyperparameters in the calls:
+    bit-identical to the oracle."""
+    spec = dict(spec)
+    numel = sum(spec["units"]) if "units" in spec else 1_000_003
+    w = W.Workload("hyper", numel, spec.pop("world", 8), 3 if "units" in spec else 2,
+                   spec.pop("gdt"), spec.pop("pdt"), steps=3, lr=1e-3, **spec)
+    run, ref = run_both(w, hyper=True, **kw)
+    if w.inject:
+        assert True in ref.skips
+    compare_runner(run, ref, what="hyper " + str((spec, kw)))
+    run.close()
+
+
+def test_device_scalar_block_unaligned_grads():
+    """Grads 2 bytes off a 16-byte boundary take the per-element path of the
+    device-block kernels; same result as the oracle."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    w = W.Workload("hyper-mis", 200_003, 4, 2, W.BF16, W.BF16, steps=2, lr=1e-3)
+    run = Runner(w, hyper=True)
+    ref = refs.OracleRun(w)
+    n = run.grads[0][0].numel()
+    for it in (1, 2):
+        run.fill_grads(it)
+        off = [torch.empty(n + 8, dtype=torch.bfloat16, device=run.dev)[1:1 + n]
+               for _ in run.grads[0]]
+        for a, b in zip(off, run.grads[0]):
+            a.copy_(b)
+        run.launch_step(grads_override=off)
+        run.finish_step()
+        ref.step(it)
+    compare_runner(run, ref, what="hyper unaligned")
+    z.zero_bind_hyper(run.ctx, None)
     run.close()
 
 

@@ -32,7 +32,7 @@ def inject_index(w: Workload, it: int, rank: int, unit: int = 0) -> int:
 
 class Runner:
     def __init__(self, w: Workload, device: str = "cuda:0", scratch: bool | None = None,
-                 shadow: bool = False, alloc_grads: bool = True):
+                 shadow: bool = False, alloc_grads: bool = True, hyper: bool = False):
         self.w = w
         self.dev = torch.device(device)
         torch.cuda.set_device(self.dev)
@@ -61,6 +61,13 @@ class Runner:
             z.zero_bind_shadow(self.ctx, *self.shadow, self.cur)
         if w.weight_decay:
             z.zero_set_weight_decay(self.ctx, w.weight_decay)
+        self.hyper = None
+        if hyper:
+            # the per-step scalars from a device block (the form a CUDA graph
+            # replays), refreshed before every step
+            self.hyper = (torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, device=self.dev),
+                          torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, pin_memory=True))
+            z.zero_bind_hyper(self.ctx, self.hyper[0])
         self.stream = torch.cuda.current_stream(self.dev)
         self.scale = w.loss_scale
         self.good = 0
@@ -177,18 +184,33 @@ class Runner:
 
     # --------------------------------------------------------------- step
 
+    def _hp(self, t: int):
+        """The hyperparameters the step calls get.  With a device scalar
+        block bound, the real ones go into the block (zero_prepare_step, then
+        a copy on the step's stream) and the calls get values that the
+        kernels must ignore."""
+        w = self.w
+        if self.hyper is None:
+            return w.lr, w.beta1, w.beta2, w.eps, t
+        d, h = self.hyper
+        z.zero_prepare_step(self.ctx, h, w.lr, w.beta1, w.beta2, w.eps, t, self.scale)
+        with torch.cuda.stream(self.stream):
+            d.copy_(h, non_blocking=True)
+        return 0.5, 0.25, 0.125, 1.0, 1
+
     def launch_step(self, grads_override=None):
         """Launch one whole step (no synchronization).  Returns the t used."""
         w = self.w
         t = self.t + 1
         st = self.stream
+        hp = self._hp(t)
         if w.stage < 3 and w.bucket:
-            self.launch_buckets(t, grads_override)
+            self.launch_buckets(hp, grads_override)
             if self.shards is not None:
                 z.zero_allgather(self.ctx, self.shards, self.params, w.param_dtype, st)
         elif w.stage < 3:
             g = grads_override if grads_override is not None else self.grads[0]
-            z.zero_step(self.ctx, g, w.lr, w.beta1, w.beta2, w.eps, t, self.scale, st)
+            z.zero_step(self.ctx, g, *hp, self.scale, st)
             if self.shards is not None:
                 z.zero_allgather(self.ctx, self.shards, self.params, w.param_dtype, st)
         else:
@@ -201,10 +223,9 @@ class Runner:
                 if self.scale > 0:
                     z.zero3_reduce_unit(self.ctx, u, self.grads[u], self.scale, st)
                 else:
-                    z.zero3_step_unit(self.ctx, u, self.grads[u], w.lr, w.beta1, w.beta2,
-                                      w.eps, t, st)
+                    z.zero3_step_unit(self.ctx, u, self.grads[u], *hp, st)
             if self.scale > 0:
-                z.zero_step_apply(self.ctx, w.lr, w.beta1, w.beta2, w.eps, t, st)
+                z.zero_step_apply(self.ctx, *hp, st)
         return t
 
     def bucket_ranges(self):
@@ -219,13 +240,14 @@ class Runner:
             return grads
         return [g[min(off, g.numel()):min(off + cnt, g.numel())] for g in self.grads[0]]
 
-    def launch_buckets(self, t, bucket_buffers=None):
-        w, st = self.w, self.stream
+    def launch_buckets(self, hp, bucket_buffers=None):
+        """One bucketed step; hp = (lr, beta1, beta2, eps, t) as the calls get them."""
+        st = self.stream
         z.zero_bucket_begin(self.ctx, self.scale)
         for off, cnt in self.bucket_ranges():
             z.zero_bucket_step(self.ctx, off, cnt, self.bucket_grads(off, cnt, bucket_buffers),
-                               w.lr, w.beta1, w.beta2, w.eps, t, st)
-        z.zero_bucket_end(self.ctx, w.lr, w.beta1, w.beta2, w.eps, t, st)
+                               *hp, st)
+        z.zero_bucket_end(self.ctx, *hp, st)
 
     def finish_step(self):
         """Read the verdict (synchronizes), advance t and the loss scale."""
