@@ -60,6 +60,8 @@ __device__ __forceinline__ void copy_elem(char *d, const char *s, int es)
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const __grid_constant__ GatherArgs a)
 {
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
     const int k = blockIdx.y;
     const char *src = static_cast<const char *>(a.src[k]);
     if (src == nullptr) return;
@@ -241,8 +243,7 @@ cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s)
     int64_t bx = 2 * resident < want ? 2 * resident : want;
     if (bx < 1) bx = 1;
     dim3 grid((unsigned)bx, (unsigned)a.n);
-    gather_kernel<<<grid, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(gather_kernel, grid, dim3(kThreads), 0, s, a);
 }
 
 bool lean_gather_eligible(const GatherArgs &a)

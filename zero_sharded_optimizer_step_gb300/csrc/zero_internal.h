@@ -77,6 +77,41 @@ struct GatherArgs {
 // device (cached per kernel and device; at least 1).
 int resident_blocks_per_sm(const void *kernel, int threads);
 
+// Programmatic dependent launch.  A kernel launched by launch_dependent may
+// be scheduled while the kernel before it in the stream is still finishing:
+// its blocks become resident as that kernel's blocks retire, so the launch
+// latency and the ramp-up overlap the previous kernel's tail.  Every such
+// kernel calls pdl_wait() before its first access to global memory, which
+// returns once the previous kernel has completed and its writes are visible,
+// so the stream's ordering is unchanged.  pdl_launch_dependents() lets the
+// next kernel be scheduled the same way (without it, that happens when every
+// block has exited).  Other work in the stream (copies, event waits) keeps
+// its full ordering.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+#endif
+
 // Launchers: return a cudaError_t.  `sms` is the device's SM count.
 cudaError_t launch_fused_step(int32_t gdt, int32_t pdt, const StepArgs &a, int sms,
                               cudaStream_t s);

@@ -345,6 +345,8 @@ template <int GT, int PT, bool AVG, bool HYPER>
 __global__ void __launch_bounds__(kThreads, MinBlocksFused<GT, HYPER>::value)
 fused_step_kernel(const __grid_constant__ StepArgs a)
 {
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
@@ -407,6 +409,8 @@ template <int GT, bool AVG, bool HYPER>
 __global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
 reduce_kernel(const __grid_constant__ StepArgs a)
 {
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
@@ -444,6 +448,8 @@ template <int PT, bool HYPER>
 __global__ void __launch_bounds__(kThreads)
 apply_kernel(const __grid_constant__ StepArgs a)
 {
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
     // The verdict of the whole step is known: a skipped step writes nothing.
     const ScalarRefs<HYPER> sc = step_scalars<HYPER>(a, false);
     if (*reinterpret_cast<volatile unsigned long long *>(a.flag) == sc.id) return;
@@ -479,6 +485,8 @@ template <int PT>
 __global__ void __launch_bounds__(kThreads)
 finalize_kernel(const __grid_constant__ StepArgs a)
 {
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
     const unsigned long long skip_id = a.hyper ? a.hyper->skip_id : a.step_id;
     const bool overflowed =
         *reinterpret_cast<volatile unsigned long long *>(a.flag) == skip_id;
@@ -512,8 +520,7 @@ cudaError_t launch(K kernel, const StepArgs &a, int64_t work_items, int sms, cud
     int64_t cap = (int64_t)sms * per_sm;
     int64_t blocks = want < cap ? want : cap;
     if (blocks < 1) blocks = 1;
-    kernel<<<(unsigned)blocks, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kernel, dim3((unsigned)blocks), dim3(kThreads), 0, s, a);
 }
 
 int64_t items(const StepArgs &a, int64_t nvec_src)
