@@ -42,11 +42,12 @@ import numpy as np  # noqa: E402
 # one pass; summarised under profiles/).  Each entry is valid only for the
 # kernel source it was taken on (sha256 prefix); otherwise bench reports null.
 TRAFFIC = {
-    ("gpt2_xl", "fused_step_kernel"): ("a50021f501aff811", 68.538e9 + 21.778e9),
-    ("one_rank_7p5b", "gather_kernel"): ("d48998624012af79", 14.787e9 + 14.721e9),
-    ("one_rank_7p5b", "fused_step_kernel"): ("a50021f501aff811", 16.406e9 + 1.621e9),
-    # the 2-unit capture has the full workload's launch sizes
-    ("zero3_llama7b", "gather_kernel"): ("d48998624012af79", 404.80128e6 + 353.814272e6),
+    ("gpt2_xl", "fused_step_kernel"): ("2cb1a8d55f497d73", 68.538e9 + 21.777e9),
+    ("one_rank_7p5b", "gather_kernel"): ("c24f81b787f5ee20", 14.786e9 + 14.721e9),
+    ("one_rank_7p5b", "fused_step_kernel"): ("2cb1a8d55f497d73", 16.406e9 + 1.621e9),
+    # mean of two full-size launches; part of each launch's writes is still in
+    # L2 when it ends
+    ("zero3_llama7b", "gather_kernel"): ("c24f81b787f5ee20", 404.81e6 + 352.97e6),
 }
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
                           "zero_step_kernels.cu")
