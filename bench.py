@@ -769,50 +769,107 @@ def oracle_sample(w, n_s):
     return grads, x
 
 
-def oracle_time(w, n_s, steps):
-    """Seconds per oracle step on n_s elements (single thread)."""
+def host_threads():
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_time(w, n_s, steps, threads=1):
+    """Wall seconds of each oracle step over a contiguous n_s-element sample,
+    split into `threads` contiguous pieces, one thread per piece.  The update
+    is elementwise, so the pieces are independent, and the C oracle runs
+    without the interpreter lock.  Returns (elements per step, times)."""
+    import threading
     import oracle
     grads, x0 = oracle_sample(w, n_s)
+    threads = max(1, min(threads, n_s))
+    bounds = [(j * n_s // threads, (j + 1) * n_s // threads) for j in range(threads)]
+    pieces = []
+    for lo, hi in bounds:
+        n = hi - lo
+        g = [a[lo:hi] for a in grads]
+        if w.rank < 0 and w.stage < 3:
+            P = oracle.shard_size(n, w.world) * w.world
+            x = np.zeros(P, np.float32)
+            x[:n] = x0[lo:hi]
+            m, v = np.zeros(P, np.float32), np.zeros(P, np.float32)
+            out = np.zeros(P, oracle.NP_STORAGE[w.param_dtype])
+        else:
+            # one rank's view: the piece is part of its shard, rank 0 of world
+            x = x0[lo:hi].copy()
+            m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+            out = np.zeros(n, oracle.NP_STORAGE[w.param_dtype])
+        pieces.append((n, g, x, m, v, out))
+
+    def step(piece, t):
+        n, g, x, m, v, out = piece
+        if w.rank < 0 and w.stage < 3:
+            oracle.zero_step(g, w.grad_dtype, n, x, m, v, out, w.param_dtype, w.lr, w.beta1,
+                             w.beta2, w.eps, t, loss_scale=w.loss_scale)
+        else:
+            oracle.zero_rank_step(g, w.grad_dtype, n * w.world, 0, x, m, v, out,
+                                  w.param_dtype, w.lr, w.beta1, w.beta2, w.eps, t,
+                                  loss_scale=w.loss_scale)
+
     times = []
-    if w.rank < 0 and w.stage < 3:
-        P = oracle.shard_size(n_s, w.world) * w.world
-        x = np.zeros(P, np.float32)
-        x[:n_s] = x0
-        m, v = np.zeros(P, np.float32), np.zeros(P, np.float32)
-        full = np.zeros(P, oracle.NP_STORAGE[w.param_dtype])
+    if threads == 1:
         for t in range(1, steps + 1):
             t0 = time.perf_counter()
-            oracle.zero_step(grads, w.grad_dtype, n_s, x, m, v, full, w.param_dtype, w.lr,
-                             w.beta1, w.beta2, w.eps, t, loss_scale=w.loss_scale)
+            step(pieces[0], t)
             times.append(time.perf_counter() - t0)
-        updated = n_s
-    else:
-        # one rank's view: the sample is a piece of its shard, rank 0 of world
-        x = x0.copy()
-        m, v = np.zeros(n_s, np.float32), np.zeros(n_s, np.float32)
-        lp = np.zeros(n_s, oracle.NP_STORAGE[w.param_dtype])
-        numel = n_s * w.world
+        return n_s, times
+    bar = threading.Barrier(threads + 1)
+    errors = []
+
+    def worker(piece):
+        try:
+            for t in range(1, steps + 1):
+                bar.wait()
+                step(piece, t)
+                bar.wait()
+        except Exception as e:        # reported by the main thread
+            errors.append(e)
+            bar.abort()
+
+    pool = [threading.Thread(target=worker, args=(p,), daemon=True) for p in pieces]
+    for th in pool:
+        th.start()
+    try:
         for t in range(1, steps + 1):
+            bar.wait()                    # every thread starts step t
             t0 = time.perf_counter()
-            oracle.zero_rank_step(grads, w.grad_dtype, numel, 0, x, m, v, lp, w.param_dtype,
-                                  w.lr, w.beta1, w.beta2, w.eps, t, loss_scale=w.loss_scale)
+            bar.wait()                    # every thread has finished it
             times.append(time.perf_counter() - t0)
-        updated = n_s
-    return updated, times
+    except threading.BrokenBarrierError:
+        pass
+    for th in pool:
+        th.join()
+    if errors:
+        raise errors[0]
+    return n_s, times
 
 
-def cpu_baseline(w, budget_s=12.0, steps=None):
+def cpu_baseline(w, budget_s=10.0, steps=4):
+    """The oracle on the host: one thread, then one thread per core."""
     n_s = 1 << 20
-    upd, times = oracle_time(w, n_s, 1)
-    per = times[0]
-    # scale the sample so that the timed steps take about the budget
-    steps = steps or 4
-    n_s = int(min(1 << 26, max(1 << 16, n_s * budget_s / steps / max(per, 1e-6))))
+    _, times = oracle_time(w, n_s, 1)
+    # scale the sample so that the single-thread steps take about the budget
+    n_s = int(min(1 << 26, max(1 << 16, n_s * budget_s / steps / max(times[0], 1e-6))))
     upd, times = oracle_time(w, n_s, steps)
-    return {"value": upd / statistics.median(times), "unit": "params/s", "cores": 1,
+    single = upd / statistics.median(times)
+    T = host_threads()
+    steps_t = min(32, steps * T)          # the same sample goes T times faster
+    upd, times = oracle_time(w, n_s, steps_t, T)
+    return {"value": upd / statistics.median(times), "unit": "params/s", "cores": T,
             "kind": "oracle",
-            "sample": "contiguous %d-element piece of the workload (%d ranks), %d steps, "
-                      "median step time; C oracle, one thread" % (n_s, w.world, steps)}
+            "sample": "contiguous %d-element piece of the workload (%d ranks) split into %d "
+                      "contiguous parts, one thread each; %d steps, median step time; C oracle"
+                      % (n_s, w.world, T, steps_t),
+            "single_thread": {"value": single, "cores": 1,
+                              "sample": "the same piece, one thread, %d steps" % steps}}
 
 
 def bench_reference(args, rank, world_size):
@@ -820,17 +877,18 @@ def bench_reference(args, rank, world_size):
     if rank != 0:
         return None
     w = W.ALL[args.workload]()
+    T = host_threads()
     n_s = 1 << 22
-    _, warm = oracle_time(w, n_s, max(1, min(args.warmup, 2)))
+    _, warm = oracle_time(w, n_s, max(1, min(args.warmup, 2)), T)
     per = statistics.median(warm)
     # keep the whole run within a few minutes
-    n_s = int(max(1 << 16, min(1 << 24, n_s * 3.0 / max(per, 1e-6))))
-    _, times = oracle_time(w, n_s, args.steps)
+    n_s = int(max(1 << 16, min(1 << 26, n_s * 3.0 / max(per, 1e-6))))
+    _, times = oracle_time(w, n_s, args.steps, T)
     ms = sum(times) * 1e3
     value = n_s * len(times) / (ms * 1e-3)
-    cb = {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-          "sample": "contiguous %d-element piece of %s per step, %d timed steps; C oracle, one "
-                    "thread" % (n_s, w.name, len(times))}
+    cb = {"value": value, "unit": "params/s", "cores": T, "kind": "oracle",
+          "sample": "contiguous %d-element piece of %s per step split into %d contiguous parts, "
+                    "one thread each; %d timed steps; C oracle" % (n_s, w.name, T, len(times))}
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
             "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / len(times), "higher_is_better": True, "scaling": "weak",

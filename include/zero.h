@@ -189,7 +189,18 @@ int64_t zero_state_bytes(const zero_ctx *ctx);
  *   flag          one 8-byte device word, zeroed by the caller before the
  *                 first step.  Holds the id of the latest step that saw a
  *                 non-finite grad; never needs clearing.
- * May be called again to rebind. */
+ * May be called again to rebind.
+ *
+ * Saving and resuming: the whole optimizer state is in the caller's
+ * buffers.  To save, copy master, m and v (with two state sets, the current
+ * one: zero_current_state) and params, and keep the step count t and the
+ * loss-scale state (scale, good steps).  To resume, create a context of the
+ * same shape, bind buffers holding those copies (the saved set as the
+ * zero_bind set; a second set's cur word zeroed), zero the flag word, and
+ * continue with t + 1.  Step ids restart at 1 in a new context, so a flag
+ * word kept from another context could name one of them: it must be zeroed
+ * ("PaddlePaddle ZeRO优化", sharded checkpoints: each rank saves and restores
+ * its own shard of the optimizer state). */
 int zero_bind(zero_ctx *ctx, float *master, float *m, float *v, void *params,
               float *g_scratch, uint64_t *flag);
 

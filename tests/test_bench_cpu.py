@@ -1,6 +1,6 @@
-"""bench.py's reference arm on CPU: one process and two torchrun ranks over
-gloo (rank 0 alone prints one JSON line; the other rank exits 0 without
-work)."""
+"""bench.py on CPU: the reference arm in one process and under two torchrun
+ranks over gloo (rank 0 alone prints one JSON line; the other rank exits 0
+without work), and the oracle timing split over host threads."""
 import json
 import os
 import subprocess
@@ -20,7 +20,8 @@ def _run(cmd):
 def _check(line):
     d = json.loads(line)
     assert d["impl"] == "reference" and d["unit"] == "params/s" and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["higher_is_better"] is True
     return d
 
@@ -30,6 +31,45 @@ def test_reference_arm_single_process():
                   "--steps", "1", "--warmup", "1"])
     assert len(lines) == 1
     _check(lines[0])
+
+
+def test_threaded_oracle_timing_steps_independent_pieces():
+    """The all-cores timing steps contiguous pieces of the sample on separate
+    threads.  That measures the same work as one thread only because the
+    update is elementwise: stepping the pieces gives, element for element,
+    what one call on the whole sample gives."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import oracle
+    import workloads as W
+    w = W.gpt2_xl()                       # 16 fp16 ranks, loss-scaled
+    n = 50_001
+    grads, x0 = bench.oracle_sample(w, n)
+
+    def run(lo, hi):
+        k = hi - lo
+        P = oracle.shard_size(k, w.world) * w.world
+        x = np.zeros(P, np.float32)
+        x[:k] = x0[lo:hi]
+        m, v = np.zeros(P, np.float32), np.zeros(P, np.float32)
+        out = np.zeros(P, oracle.NP_STORAGE[w.param_dtype])
+        for t in (1, 2):
+            oracle.zero_step([g[lo:hi] for g in grads], w.grad_dtype, k, x, m, v, out,
+                             w.param_dtype, w.lr, w.beta1, w.beta2, w.eps, t,
+                             loss_scale=w.loss_scale)
+        return x[:k], m[:k], v[:k], out[:k]
+
+    whole = run(0, n)
+    cuts = [0, 7, 20_000, 33_333, n]
+    for a, b in zip(cuts, cuts[1:]):
+        for got, want in zip(run(a, b), whole):
+            assert got.tobytes() == want[a:b].tobytes()
+    # and the threaded timing runs on both views
+    n_s, times = bench.oracle_time(W.gpt2_small(), 1 << 16, 2, threads=4)
+    assert n_s == 1 << 16 and len(times) == 2 and all(t > 0 for t in times)
+    n_s, times = bench.oracle_time(W.one_rank_7p5b(0), 1 << 15, 1, threads=3)
+    assert n_s == 1 << 15 and len(times) == 1
 
 
 def test_reference_arm_under_torchrun_two_ranks():

@@ -626,6 +626,49 @@ def test_dim0_layout_units(rank, scaled):
     run.close()
 
 
+# ------------------------------------------------------- save and resume
+
+@pytest.mark.parametrize("kind", ["shadow", "two_pass_rank", "stage3"])
+def test_resume_from_saved_state(kind):
+    """Save after two steps (the second skipped), resume in a new context
+    from the copies, run two more steps: bit-identical to the run that
+    never stopped (the protocol the header states for zero_bind)."""
+    from workloads.runner import Runner
+    if kind == "stage3":
+        units = [200_003, 99, 150_000]
+        w = W.Workload("res3", sum(units), 8, 3, W.BF16, W.BF16, units=units, steps=4,
+                       loss_scale=2.0 ** 10, inject=(2, 3))
+    else:
+        w = W.Workload("res", 500_003, 8, 2, W.F16, W.F16, rank=3 if kind == "two_pass_rank" else -1,
+                       steps=4, loss_scale=2.0 ** 12, inject=(2, 3))
+    shadow = kind == "shadow"
+    whole = Runner(w, shadow=shadow)
+    for it in range(1, 5):
+        whole.step(it)
+    first = Runner(w, shadow=shadow)
+    for it in (1, 2):
+        first.step(it)
+    torch.cuda.synchronize()
+    saved = [t.clone() for t in first.state()] + [first.params.clone()]
+    t, scale, good, skips = first.t, first.scale, first.good, list(first.skips)
+    assert skips == [False, True] or kind == "two_pass_rank"
+    first.close()
+    resumed = Runner(w, shadow=shadow)      # fresh buffers: flag and cur words zero
+    for dst, src in zip([resumed.master, resumed.m, resumed.v, resumed.params], saved):
+        dst.copy_(src)
+    resumed.t, resumed.scale, resumed.good = t, scale, good
+    for it in (3, 4):
+        resumed.step(it)
+    torch.cuda.synchronize()
+    for a, b in zip(resumed.state() + (resumed.params,), whole.state() + (whole.params,)):
+        assert torch.equal(a.view(torch.uint8) if a.dtype != torch.float32 else a.view(torch.int32),
+                           b.view(torch.uint8) if b.dtype != torch.float32 else b.view(torch.int32))
+    assert skips + resumed.skips == whole.skips
+    assert resumed.t == whole.t and resumed.scale == whole.scale
+    for r in (whole, resumed):
+        r.close()
+
+
 # ------------------------------------------- steps captured in a CUDA graph
 
 def _hyper(run):
