@@ -66,7 +66,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="gpt2_xl",
                     choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny",
-                             "gpt2_xl_bucketed", "zero3_prefetch", "zero3_gpt2_small"])
+                             "gpt2_xl_bucketed", "zero3_prefetch", "zero3_gpt2_small",
+                             "gpt2_xl_adamw", "fsdp2_llama7b"])
     ap.add_argument("--graph", action="store_true",
                     help="also capture one step in a CUDA graph and time its replays")
     ap.add_argument("--unit-fwd-ms", type=float, default=0.25,
@@ -79,7 +80,8 @@ def parse():
                     help="loss-scaled workloads: the scratch-based two-pass step instead of the "
                          "single pass over two state sets")
     ap.add_argument("--units", type=int, default=0,
-                    help="ZeRO-3 workloads: use this many Llama-7B-shaped units (small cases)")
+                    help="zero3_llama7b / fsdp2_llama7b: use this many Llama-7B layers (small "
+                         "cases)")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     return ap.parse_args()
@@ -268,7 +270,7 @@ def bench_ours(args, rank, world_size, device_index):
     from workloads.runner import Runner
 
     w = W.ALL[args.workload](**({"n_units": args.units} if args.units and
-                                args.workload.startswith("zero3") else {}))
+                                args.workload in ("zero3_llama7b", "fsdp2_llama7b") else {}))
     if args.numel:
         w = w.replace(numel=args.numel, name=w.name + "_numel%d" % args.numel)
     if w.inject:
@@ -715,7 +717,11 @@ def bench_e2e_units(run, args, world_size):
             h.copy_(t)
             hr.append(h)
         host.append(hr)
-    dev = [[torch.empty_like(t) for t in run.grads[0]] for _ in range(2)]
+    # two sets of device buffers, each the size of the largest unit's slices
+    longest = max(t.numel() for row in run.grads for t in row)
+    gdt = run.grads[0][0].dtype
+    dev = [[torch.empty(longest, dtype=gdt, device=run.dev) for _ in run.grads[0]]
+           for _ in range(2)]
     cp = torch.cuda.Stream(run.dev)
     st = run.stream
     ready = [torch.cuda.Event() for _ in range(2)]
@@ -727,15 +733,16 @@ def bench_e2e_units(run, args, world_size):
             z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full, st)
         for i, u in enumerate(reversed(range(U))):           # backward
             k2 = i % 2
+            views = [d[:h.numel()] for d, h in zip(dev[k2], host[u])]
             with torch.cuda.stream(cp):
                 if i >= 2:
                     cp.wait_event(done[k2])
-                for d, h in zip(dev[k2], host[u]):
+                for d, h in zip(views, host[u]):
                     d.copy_(h, non_blocking=True)
                 ready[k2].record(cp)
             z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full, st)
             st.wait_event(ready[k2])
-            z.zero3_step_unit(run.ctx, u, dev[k2], w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st)
+            z.zero3_step_unit(run.ctx, u, views, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st)
             done[k2].record(st)
         z.zero_step_status(run.ctx)                          # 8-byte read of the verdict
         run.t += 1

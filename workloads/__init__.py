@@ -128,6 +128,26 @@ def dim0(shapes, world: int, rank: int = -1, **kw) -> Workload:
                     unit_rows=list(shapes), **kw)
 
 
+def llama_layer_shapes(hidden: int = 4096, ffn: int = 11008):
+    """The parameter tensors of one Llama decoder layer as (rows, row_elems):
+    the q, k, v, o projections, gate, up, down, and the two RMSNorm weights."""
+    return ([(hidden, hidden)] * 4 + [(ffn, hidden), (ffn, hidden), (hidden, ffn)]
+            + [(hidden, 1)] * 2)
+
+
+def fsdp2_llama7b(n_units: int = 32) -> Workload:
+    """ZeRO-3 over Llama-7B decoder layers in FSDP2's per-parameter dim-0
+    layout: one unit per parameter tensor, each sharded by whole rows (rank 0
+    of 8).  32 layers hold the elements and bytes of zero3_llama7b, in 288
+    units instead of 32.  n_units counts layers."""
+    return dim0(llama_layer_shapes() * n_units, 8, 0, steps=2).replace(name="fsdp2_llama7b")
+
+
+def gpt2_xl_adamw() -> Workload:
+    """The GPT-2 XL workload with decoupled weight decay 0.1 (AdamW)."""
+    return gpt2_xl().replace(name="gpt2_xl_adamw", weight_decay=0.1)
+
+
 def zero3_gpt2_small() -> Workload:
     """ZeRO-3 over GPT-2 small with one unit per transformer block, plus the
     embeddings and the final norm (rank 0 of 8): 14 small units, where the
@@ -139,8 +159,10 @@ def zero3_gpt2_small() -> Workload:
                     steps=2)
 
 
-ALL = {"tiny": tiny, "zero3_gpt2_small": zero3_gpt2_small, "gpt2_xl_bucketed": gpt2_xl_bucketed, "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl,
-       "one_rank_7p5b": one_rank_7p5b, "zero3_llama7b": zero3_llama7b}
+ALL = {"tiny": tiny, "zero3_gpt2_small": zero3_gpt2_small, "gpt2_xl_bucketed": gpt2_xl_bucketed,
+       "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl, "gpt2_xl_adamw": gpt2_xl_adamw,
+       "one_rank_7p5b": one_rank_7p5b, "zero3_llama7b": zero3_llama7b,
+       "fsdp2_llama7b": fsdp2_llama7b}
 
 
 def grad_sigma(w: Workload, scale: float) -> float:
