@@ -83,7 +83,8 @@ enum zero_code {
     ZERO_EINVAL = -1,      /* bad argument (size, dtype, rank, unit, null pointer) */
     ZERO_ECUDA = -2,       /* a CUDA runtime call failed */
     ZERO_EALIGN = -3,      /* a device pointer is not aligned to its element size */
-    ZERO_ESTATE = -4       /* call not valid in this context's state (e.g. unbound) */
+    ZERO_ESTATE = -4,      /* call not valid in this context's state (e.g. unbound) */
+    ZERO_ETIMEOUT = -5     /* a bounded device wait ran out (zero_gather_timeouts) */
 };
 
 #define ZERO_MAX_RANKS 256
@@ -369,7 +370,10 @@ int zero_set_gather_mode(zero_ctx *ctx, int32_t mode);
 
 /* Number of lean-gather waits that ran out in this process (each one drains
  * its copies in flight and abandons the rest of that gather; the result is
- * then incomplete).  0 in normal operation. */
+ * then incomplete).  0 in normal operation.  Returns ZERO_OK when the count
+ * is 0, ZERO_ETIMEOUT (the count still written) when a wait ran out, and
+ * ZERO_ECUDA when the counter cannot be read.  Read it after the gathers'
+ * streams are synchronized. */
 int zero_gather_timeouts(uint32_t *count);
 
 /* ------------------------------------------------------------- stage 3 */

@@ -53,6 +53,24 @@ def test_header_compiles_as_c():
                     "-x", "c", "-", "-o", os.devnull], input=src, text=True, check=True)
 
 
+def test_error_codes_match_the_header(z):
+    """The binding's codes equal the header's enum, and every code has its
+    own message (no GPU needed)."""
+    text = open(HEADER).read()
+    import re
+    enum = dict((k, int(v)) for k, v in re.findall(r"(ZERO_[A-Z]+) = (-?\d+)", text)
+                if k in ("ZERO_OK", "ZERO_SKIPPED", "ZERO_EINVAL", "ZERO_ECUDA", "ZERO_EALIGN",
+                         "ZERO_ESTATE", "ZERO_ETIMEOUT"))
+    assert len(enum) == 7
+    msgs = set()
+    for name, code in enum.items():
+        assert getattr(z, name) == code
+        msg = z.zero_strerror(code)
+        assert msg.startswith(name)
+        msgs.add(msg)
+    assert len(msgs) == 7 and z.zero_strerror(-99) == "unknown zero code"
+
+
 def test_host_geometry_and_closed_forms(z):
     import oracle
     from oracle import memory as mem

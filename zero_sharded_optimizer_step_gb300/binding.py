@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(HERE, "libzero.so")
 
 ZERO_F32, ZERO_BF16, ZERO_F16 = 0, 1, 2
 ZERO_OK, ZERO_SKIPPED = 0, 1
-ZERO_EINVAL, ZERO_ECUDA, ZERO_EALIGN, ZERO_ESTATE = -1, -2, -3, -4
+ZERO_EINVAL, ZERO_ECUDA, ZERO_EALIGN, ZERO_ESTATE, ZERO_ETIMEOUT = -1, -2, -3, -4, -5
 ZERO_MAX_RANKS = 256
 ZERO_HYPER_BYTES = 128
 ZERO_GATHER_FAST, ZERO_GATHER_LEAN = 0, 1
@@ -252,8 +252,12 @@ def zero_set_gather_mode(ctx, mode: int) -> None:
 
 
 def zero_gather_timeouts() -> int:
+    """The count of lean-gather waits that ran out (ZERO_ETIMEOUT from the C
+    call when it is not 0; the count is returned either way)."""
     c = ctypes.c_uint32(0)
-    _check(_L.zero_gather_timeouts(ctypes.byref(c)))
+    rc = _L.zero_gather_timeouts(ctypes.byref(c))
+    if rc != ZERO_ETIMEOUT:
+        _check(rc)
     return int(c.value)
 
 

@@ -415,6 +415,7 @@ const char *zero_strerror(int code)
     case ZERO_ECUDA: return "ZERO_ECUDA: CUDA runtime error";
     case ZERO_EALIGN: return "ZERO_EALIGN: misaligned device pointer";
     case ZERO_ESTATE: return "ZERO_ESTATE: call not valid in this state";
+    case ZERO_ETIMEOUT: return "ZERO_ETIMEOUT: a bounded device wait ran out";
     }
     return "unknown zero code";
 }
@@ -621,7 +622,7 @@ int zero_gather_timeouts(uint32_t *count)
     cudaError_t e = zgb::lean_gather_timeouts(&h);
     if (e != cudaSuccess) return cuda_fail(e, "reading the gather timeout counter");
     *count = h;
-    return ZERO_OK;
+    return h ? ZERO_ETIMEOUT : ZERO_OK;
 }
 
 int zero_set_weight_decay(zero_ctx *c, double weight_decay)
