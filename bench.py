@@ -1,21 +1,27 @@
 """Benchmark of the ZeRO sharded optimizer step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
+                    [--impl ours|reference] [--no-e2e] [--no-cpu-baseline] [--graph]
 
 One "step" is one pass of the whole hot path over one batch of synthetic
-grads already resident in HBM: for the default workload (GPT-2 XL shape,
+grads already resident in HBM.  For the default workload (GPT-2 XL shape,
 1,557,611,200 params, 16 data-parallel ranks on this GPU, fp16 grads and
-params, loss scale 2^16) that is the reduce-scatter sum, average, unscale and
-overflow check (reduce kernel), then Adam + cast + placement (apply kernel),
-then the read of the overflow verdict and the loss-scale update.
+params, loss scale 2^16) that is one kernel that reduce-scatters (sums the
+ranks' grads in rank order), averages, unscales, checks for overflow, runs
+Adam on the fp32 state and casts into the full fp16 parameter buffer, reading
+the current state set and writing the other; a finalize kernel that makes
+the written set current unless the step overflowed; and the read of the
+overflow verdict with the loss-scale update.
 
 Prints ONE JSON line (rank 0).  `value` is params updated per second over
-all GPUs (device-timed with CUDA events, inputs resident); `e2e` repeats the
-measurement with the grads copied from pinned host memory every step and
-the verdict read back; `roofline` reports the dominant kernel's algorithmic
-bytes per launch over its CUDA-event duration against the measured HBM copy
-bandwidth; `cpu_baseline` times the CPU oracle on a bounded sample.
+all GPUs: K steps between one pair of CUDA events, inputs resident, nothing
+between the launches.  A second pass of K steps puts an event pair around
+every launch for the per-kernel durations behind `roofline`: the dominant
+kernel's algorithmic bytes per launch over its average duration, against the
+measured HBM copy bandwidth.  `e2e` repeats the measurement with the grads
+copied from pinned host memory every step and the verdict read back;
+`cpu_baseline` times the CPU oracle on a bounded sample (all host cores, and
+one).  `--graph` also times replays of one step captured in a CUDA graph.
 
 With --gpus N > 1 (torchrun), every GPU runs its own full replica of the
 workload (the N simulated ranks live on each GPU; no data-path collective):
@@ -306,17 +312,27 @@ def bench_ours(args, rank, world_size, device_index):
     barrier(world_size)
     torch.cuda.synchronize()
     clocks.start()
+    # the step time: K steps bracketed by one pair of events, nothing between
+    # the launches
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(run.stream)
     for k in range(args.steps):
-        run_step(run, plan, ev[k])
+        run_step(run, plan)
     t_end.record(run.stream)
     torch.cuda.synchronize()
-    clock_info = clocks.stop()
     barrier(world_size)
     ms = t_start.elapsed_time(t_end)
     ms_max = allreduce_max(ms, world_size)
+    # the per-kernel durations (the roofline's): K more steps with a pair of
+    # events around every launch (they serialize the launches, so this pass
+    # is not the step time)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        run_step(run, plan, ev[k])
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier(world_size)
     assert all(not s for s in run.skips), "a timed step was skipped"
 
     # per-kernel durations
@@ -365,6 +381,8 @@ def bench_ours(args, rank, world_size, device_index):
             "method_min_bytes_per_param": method_min_bytes(w),
             "l2": "inputs larger than L2 (working set %.1f GB)" % (working_set(run) / 1e9),
             "per_kernel_ms": {n: per[n][0] / per[n][1] for n in per},
+            "per_kernel_timing": "a second pass of the same number of steps with an event "
+                                 "pair around every launch",
             "parallelism": "%d simulated data-parallel ranks per GPU; %d GPU replica(s)"
                            % (w.world, world_size),
             "bucket_elems": w.bucket or None,
