@@ -73,7 +73,7 @@ def parse():
     ap.add_argument("--workload", default="gpt2_xl",
                     choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny",
                              "gpt2_xl_bucketed", "zero3_prefetch", "zero3_gpt2_small",
-                             "gpt2_xl_adamw", "fsdp2_llama7b"])
+                             "gpt2_xl_adamw", "fsdp2_llama7b", "fsdp2_llama7b_per_param"])
     ap.add_argument("--graph", action="store_true",
                     help="also capture one step in a CUDA graph and time its replays")
     ap.add_argument("--unit-fwd-ms", type=float, default=0.25,
@@ -86,8 +86,8 @@ def parse():
                     help="loss-scaled workloads: the scratch-based two-pass step instead of the "
                          "single pass over two state sets")
     ap.add_argument("--units", type=int, default=0,
-                    help="zero3_llama7b / fsdp2_llama7b: use this many Llama-7B layers (small "
-                         "cases)")
+                    help="zero3_llama7b / fsdp2_llama7b(_per_param): use this many Llama-7B "
+                         "layers (small cases)")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
     return ap.parse_args()
@@ -229,6 +229,32 @@ def step_plan(run):
             def gat():
                 z.zero_allgather(run.ctx, run.shards, run.params, w.param_dtype, st)
             plan.append(Launch("gather_kernel", 2 * bp * w.shard * n_sh, gat))
+    elif w.groups:
+        # one launch per group of units (a layer's parameters) for each
+        # gather and for the step
+        groups = run.group_ranges()
+
+        def first():
+            z.zero3_begin_step(run.ctx)
+
+        def gather(g, f, n):
+            sh = run.shards[f:f + n]
+            return lambda: z.zero3_gather_group(run.ctx, f, sh, run.group_fulls[g], st)
+        for g, (f, n) in enumerate(groups):
+            S = sum(w.unit_shard(u) for u in range(f, f + n))
+            plan.append(Launch("gather_rows_kernel", 2 * bp * S * w.world, gather(g, f, n)))
+        for g in reversed(range(len(groups))):
+            f, n = groups[g]
+            S = sum(w.unit_shard(u) for u in range(f, f + n))
+            nv = sum(min(w.unit_shard(u), max(0, w.units[u] - w.rank * w.unit_shard(u)))
+                     for u in range(f, f + n))
+            plan.append(Launch("gather_rows_kernel", 2 * bp * S * w.world, gather(g, f, n)))
+            plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * S,
+                               (lambda g=g, f=f, n=n: z.zero3_step_group(
+                                   run.ctx, f, n, run.group_grads[g], w.lr, w.beta1, w.beta2,
+                                   w.eps, run.t + 1, st))))
+        plan[0] = Launch(plan[0].name, plan[0].alg_bytes,
+                         (lambda f=plan[0].fn: (first(), f())))
     else:
         nunits = len(w.units)
 
@@ -276,7 +302,8 @@ def bench_ours(args, rank, world_size, device_index):
     from workloads.runner import Runner
 
     w = W.ALL[args.workload](**({"n_units": args.units} if args.units and
-                                args.workload in ("zero3_llama7b", "fsdp2_llama7b") else {}))
+                                args.workload in ("zero3_llama7b", "fsdp2_llama7b",
+                                                  "fsdp2_llama7b_per_param") else {}))
     if args.numel:
         w = w.replace(numel=args.numel, name=w.name + "_numel%d" % args.numel)
     if w.inject:
@@ -710,16 +737,21 @@ def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
 
 
 def bench_e2e_units(run, args, world_size):
-    """ZeRO-3 end to end: each unit's grads (all ranks' slices) are copied
-    from pinned host memory on a copy stream into one of two device buffer
-    sets while the previous unit is gathered and stepped; then the verdict is
-    read back."""
+    """ZeRO-3 end to end: each unit's grads (all ranks' slices; for a grouped
+    workload each group's per-rank buffers) are copied from pinned host memory
+    on a copy stream into one of two device buffer sets while the previous
+    unit is gathered and stepped; then the verdict is read back."""
     import torch
     import zero_sharded_optimizer_step_gb300 as z
 
     w = run.w
-    U = len(w.units)
-    h2d = sum(t.numel() * t.element_size() for row in run.grads for t in row)
+    if w.groups:
+        pieces = run.group_ranges()
+        src = run.group_grads
+    else:
+        pieces = [(u, 1) for u in range(len(w.units))]
+        src = run.grads
+    h2d = sum(t.numel() * t.element_size() for row in src for t in row)
     try:
         avail = int(open("/proc/meminfo").read().split("MemAvailable:")[1].split()[0]) * 1024
     except Exception:
@@ -728,39 +760,54 @@ def bench_e2e_units(run, args, world_size):
     if h2d > int(0.3 * avail / max(1, local_ranks)):
         return None
     host = []
-    for row in run.grads:
+    for row in src:
         hr = []
         for t in row:
             h = torch.empty(t.numel(), dtype=t.dtype, pin_memory=True)
             h.copy_(t)
             hr.append(h)
         host.append(hr)
-    # two sets of device buffers, each the size of the largest unit's slices
-    longest = max(t.numel() for row in run.grads for t in row)
-    gdt = run.grads[0][0].dtype
-    dev = [[torch.empty(longest, dtype=gdt, device=run.dev) for _ in run.grads[0]]
+    # two sets of device buffers, each the size of the largest piece
+    longest = max(t.numel() for row in src for t in row)
+    gdt = src[0][0].dtype
+    dev = [[torch.empty(longest, dtype=gdt, device=run.dev) for _ in src[0]]
            for _ in range(2)]
     cp = torch.cuda.Stream(run.dev)
     st = run.stream
     ready = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
 
+    def gather(i):
+        f, n = pieces[i]
+        if w.groups:
+            z.zero3_gather_group(run.ctx, f, run.shards[f:f + n], run.group_fulls[i], st)
+        else:
+            z.zero3_gather_unit(run.ctx, f, run.shards[f], run.unit_full, st)
+
+    def step(i, views):
+        f, n = pieces[i]
+        if w.groups:
+            z.zero3_step_group(run.ctx, f, n, views, w.lr, w.beta1, w.beta2, w.eps, run.t + 1,
+                               st)
+        else:
+            z.zero3_step_unit(run.ctx, f, views, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st)
+
     def one():
         z.zero3_begin_step(run.ctx)
-        for u in range(U):                                   # forward gathers
-            z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full, st)
-        for i, u in enumerate(reversed(range(U))):           # backward
-            k2 = i % 2
-            views = [d[:h.numel()] for d, h in zip(dev[k2], host[u])]
+        for i in range(len(pieces)):                         # forward gathers
+            gather(i)
+        for j, i in enumerate(reversed(range(len(pieces)))):  # backward
+            k2 = j % 2
+            views = [d[:h.numel()] for d, h in zip(dev[k2], host[i])]
             with torch.cuda.stream(cp):
-                if i >= 2:
+                if j >= 2:
                     cp.wait_event(done[k2])
-                for d, h in zip(views, host[u]):
+                for d, h in zip(views, host[i]):
                     d.copy_(h, non_blocking=True)
                 ready[k2].record(cp)
-            z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full, st)
+            gather(i)
             st.wait_event(ready[k2])
-            z.zero3_step_unit(run.ctx, u, views, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st)
+            step(i, views)
             done[k2].record(st)
         z.zero_step_status(run.ctx)                          # 8-byte read of the verdict
         run.t += 1
@@ -778,8 +825,8 @@ def bench_e2e_units(run, args, world_size):
             "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": 8, "host_buffers_distinct": sum(len(r) for r in host),
             "device_buffers": 2 * len(dev[0]),
-            "path": "per-unit host-to-device copies overlapped with the previous unit's "
-                    "gather and step"}
+            "path": "per-%s host-to-device copies overlapped with the previous %s's gather "
+                    "and step" % (("group", "group") if w.groups else ("unit", "unit"))}
 
 
 # ---------------------------------------------------------------- the oracle

@@ -404,6 +404,39 @@ int zero3_step_unit(zero_ctx *ctx, int32_t unit, const void *const *grads,
 int zero3_reduce_unit(zero_ctx *ctx, int32_t unit, const void *const *grads,
                       int32_t n_grads, float loss_scale, void *stream);
 
+/* Groups of units: FSDP2 shards every parameter tensor on dim 0 and
+ * gathers and reduces the parameters of one module together ("ZeRO 与
+ * FSDP…", ZeRO-3 与 FSDP: per-parameter dim-0 sharding; a module's
+ * parameters form one gather unit).  With one unit per parameter tensor
+ * (zero_init_dim0), a group is a run of consecutive units -- a module's
+ * parameters -- handled in one launch.
+ *
+ * zero3_gather_group: units [first_unit, first_unit + n_units) at once.
+ *   shards      n_units * N pointers, unit-major: shards[ul*N + k] is shard k
+ *               (S_u elements) of unit first_unit + ul; NULL skips it.
+ *   unit_fulls  n_units destinations of N*S_u elements each (as
+ *               zero3_gather_unit's unit_full).
+ * At most 512 shards per call (n_units * N); any element alignment.  Always
+ * the SM placement (the lean mode applies to zero3_gather_unit). */
+int zero3_gather_group(zero_ctx *ctx, int32_t first_unit, int32_t n_units,
+                       const void *const *shards, int32_t n_shards, void *const *unit_fulls,
+                       void *stream);
+
+/* zero3_step_group / zero3_reduce_group: zero3_step_unit / zero3_reduce_unit
+ * over units [first_unit, first_unit + n_units) in one launch.  grads[k]
+ * holds rank k's grads of every unit of the group end to end, in unit order
+ * -- one rank: S_u-element slices; all ranks: numel_u-element local grads --
+ * the layout of one flat reduce-scatter buffer per module.  Every unit of the
+ * group must be free of padding in this view (one rank: numel_u >= (r+1)*S_u;
+ * all ranks: numel_u == N*S_u); otherwise ZERO_EINVAL, and that unit is
+ * stepped on its own.  Results are bit-identical to the per-unit calls. */
+int zero3_step_group(zero_ctx *ctx, int32_t first_unit, int32_t n_units,
+                     const void *const *grads, int32_t n_grads, double lr, double beta1,
+                     double beta2, double eps, int64_t t, void *stream);
+int zero3_reduce_group(zero_ctx *ctx, int32_t first_unit, int32_t n_units,
+                       const void *const *grads, int32_t n_grads, float loss_scale,
+                       void *stream);
+
 /* ------------------------------------------------ step without allocation */
 
 /* The pages have no counterpart of this call; it serves callers that can

@@ -626,6 +626,79 @@ def test_dim0_layout_units(rank, scaled):
     run.close()
 
 
+# ------------------------------------------- groups of units (per module)
+
+@pytest.mark.parametrize("rank", [-1, 0, 3])
+def test_group_gather_equals_unit_gathers(rank):
+    """One launch placing every shard of a run of units equals the per-unit
+    gathers byte for byte, padded units and odd row lengths included."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    shapes = [(256, 64), (10, 1), (4097, 33), (3, 11), (64, 7)]
+    w = W.dim0(shapes, 4, rank=rank, steps=1)
+    run = Runner(w)
+    z.zero3_begin_step(run.ctx)
+    want = []
+    for u in range(1, 5):
+        z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full)
+        want.append(to_np(run.unit_full[:w.unit_shard(u) * w.world]).copy())
+    from workloads.runner import TORCH_DTYPE
+    dt = TORCH_DTYPE[w.param_dtype]
+    fulls = [torch.full((w.unit_shard(u) * w.world + 3,), 7.0, dtype=dt,
+                        device="cuda:0")[1:1 + w.unit_shard(u) * w.world] for u in range(1, 5)]
+    z.zero3_gather_group(run.ctx, 1, run.shards[1:5], fulls)
+    torch.cuda.synchronize()
+    for got, ref in zip(fulls, want):
+        assert to_np(got).tobytes() == ref.tobytes()
+    run.close()
+
+
+@pytest.mark.parametrize("rank,scaled", [(-1, False), (1, False), (-1, True), (2, True)])
+def test_group_step_parity(rank, scaled):
+    """Runs of units gathered and stepped (or reduced, then one apply) in one
+    launch per group, each rank's grads of a group end to end: bit-identical
+    to the oracle, with a skipped step when loss-scaled."""
+    shapes = [(256, 64), (512, 33), (128, 7), (64, 1), (1024, 3), (8, 5)]
+    w = W.dim0(shapes, 4, rank=rank, steps=3, loss_scale=2.0 ** 8 if scaled else 0.0,
+               inject=(2, 1) if scaled else None).replace(groups=[2, 3, 1])
+    run, ref = run_both(w)
+    if scaled and rank < 0:
+        assert ref.skips == [False, True, False]
+    compare_runner(run, ref, what="groups")
+    run.close()
+
+
+def test_group_call_errors():
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    shapes = [(256, 64), (10, 1), (64, 7)]          # (10, 1) leaves padding on rank 3
+    w = W.dim0(shapes, 4, rank=3, steps=1)
+    run = Runner(w)
+    z.zero3_begin_step(run.ctx)
+    g = [torch.zeros(w.unit_shard(0) + w.unit_shard(1), dtype=torch.bfloat16, device="cuda:0")
+         for _ in range(4)]
+    with pytest.raises(z.ZeroError) as ei:          # a padded unit in the group
+        z.zero3_step_group(run.ctx, 0, 2, g, 1e-3, 0.9, 0.999, 1e-8, 1)
+    assert ei.value.code == z.ZERO_EINVAL and "padding" in str(ei.value)
+    with pytest.raises(z.ZeroError):                # past the last unit
+        z.zero3_step_group(run.ctx, 2, 2, g, 1e-3, 0.9, 0.999, 1e-8, 1)
+    with pytest.raises(z.ZeroError):                # wrong number of grad buffers
+        z.zero3_step_group(run.ctx, 0, 1, g[:3], 1e-3, 0.9, 0.999, 1e-8, 1)
+    with pytest.raises(z.ZeroError):                # shards for the wrong number of units
+        z.zero3_gather_group(run.ctx, 0, run.shards[0:2], [run.unit_full])
+    z.zero3_step_group(run.ctx, 2, 1, [b[:w.unit_shard(2)] for b in g], 1e-3, 0.9, 0.999,
+                       1e-8, 1)                     # a group without padding is fine
+    run.close()
+    big = W.dim0([(64, 1)] * 130, 4, rank=0, steps=1)   # 130 units x 4 ranks > 512 shards
+    run = Runner(big)
+    z.zero3_begin_step(run.ctx)
+    fulls = [run.unit_full[:64] for _ in range(130)]
+    with pytest.raises(z.ZeroError) as ei:
+        z.zero3_gather_group(run.ctx, 0, run.shards, fulls)
+    assert "512" in str(ei.value)
+    run.close()
+
+
 # ------------------------------------------------------- save and resume
 
 @pytest.mark.parametrize("kind", ["shadow", "two_pass_rank", "stage3"])

@@ -54,6 +54,7 @@ class Workload:
     rank: int = -1                       # -1: every rank's state on this GPU
     units: Optional[List[int]] = None    # stage 3
     unit_rows: Optional[List[Tuple[int, int]]] = None   # stage 3, dim-0 layout: (rows, row_elems)
+    groups: Optional[List[int]] = None   # stage 3: sizes of runs of units stepped as one
     steps: int = 3
     lr: float = 1e-4
     beta1: float = 0.9
@@ -135,12 +136,22 @@ def llama_layer_shapes(hidden: int = 4096, ffn: int = 11008):
             + [(hidden, 1)] * 2)
 
 
-def fsdp2_llama7b(n_units: int = 32) -> Workload:
+def fsdp2_llama7b_per_param(n_units: int = 32) -> Workload:
     """ZeRO-3 over Llama-7B decoder layers in FSDP2's per-parameter dim-0
     layout: one unit per parameter tensor, each sharded by whole rows (rank 0
-    of 8).  32 layers hold the elements and bytes of zero3_llama7b, in 288
-    units instead of 32.  n_units counts layers."""
-    return dim0(llama_layer_shapes() * n_units, 8, 0, steps=2).replace(name="fsdp2_llama7b")
+    of 8), every parameter gathered and stepped on its own.  32 layers hold
+    the elements and bytes of zero3_llama7b, in 288 units instead of 32.
+    n_units counts layers."""
+    return dim0(llama_layer_shapes() * n_units, 8, 0, steps=2).replace(
+        name="fsdp2_llama7b_per_param")
+
+
+def fsdp2_llama7b(n_units: int = 32) -> Workload:
+    """The same per-parameter layout with each layer's nine parameters
+    gathered and stepped together (one group per layer), as FSDP2 gathers and
+    reduces a module's parameters at once."""
+    w = fsdp2_llama7b_per_param(n_units)
+    return w.replace(name="fsdp2_llama7b", groups=[len(llama_layer_shapes())] * n_units)
 
 
 def gpt2_xl_adamw() -> Workload:
@@ -162,7 +173,7 @@ def zero3_gpt2_small() -> Workload:
 ALL = {"tiny": tiny, "zero3_gpt2_small": zero3_gpt2_small, "gpt2_xl_bucketed": gpt2_xl_bucketed,
        "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl, "gpt2_xl_adamw": gpt2_xl_adamw,
        "one_rank_7p5b": one_rank_7p5b, "zero3_llama7b": zero3_llama7b,
-       "fsdp2_llama7b": fsdp2_llama7b}
+       "fsdp2_llama7b": fsdp2_llama7b, "fsdp2_llama7b_per_param": fsdp2_llama7b_per_param}
 
 
 def grad_sigma(w: Workload, scale: float) -> float:

@@ -112,12 +112,35 @@ class Runner:
         else:
             self.params.copy_(self.master.to(self.params.dtype))
 
+    def group_ranges(self):
+        """(first unit, unit count) of each group of a grouped stage-3 workload."""
+        out, first = [], 0
+        for n in self.w.groups or []:
+            out.append((first, n))
+            first += n
+        return out
+
     def _alloc_grads(self):
         w = self.w
         dt = TORCH_DTYPE[w.grad_dtype]
+        units = self._units()
+        lens = [nu if w.rank < 0 else Su for u, nu, Su, off in units]
         self.grads = []   # per unit: list of world tensors
-        for u, nu, Su, off in self._units():
-            n = nu if w.rank < 0 else Su
+        self.group_grads = None
+        if w.groups:
+            # per group and rank one buffer with the group's units end to end
+            # (the layout the group calls take); the units' grads are views
+            self.group_grads = []
+            for first, n in self.group_ranges():
+                tot = sum(lens[first:first + n])
+                bufs = [torch.zeros(tot, dtype=dt, device=self.dev) for _ in range(w.world)]
+                self.group_grads.append(bufs)
+                off = 0
+                for u in range(first, first + n):
+                    self.grads.append([b[off:off + lens[u]] for b in bufs])
+                    off += lens[u]
+            return
+        for n in lens:
             self.grads.append([torch.zeros(n, dtype=dt, device=self.dev) for _ in range(w.world)])
 
     def _alloc_shards(self):
@@ -146,6 +169,19 @@ class Runner:
                 self.shards.append(row)
                 Pmax = max(Pmax, Su * w.world)
             self.unit_full = torch.zeros(Pmax, dtype=dt, device=self.dev)
+            self.group_fulls = None
+            if w.groups:
+                # one destination per unit of a group, side by side in one buffer
+                sizes = [Su * w.world for u, nu, Su, off in self._units()]
+                longest = max(sum(sizes[f:f + n]) for f, n in self.group_ranges())
+                self.group_full = torch.zeros(longest, dtype=dt, device=self.dev)
+                self.group_fulls = []
+                for f, n in self.group_ranges():
+                    views, off = [], 0
+                    for u in range(f, f + n):
+                        views.append(self.group_full[off:off + sizes[u]])
+                        off += sizes[u]
+                    self.group_fulls.append(views)
         elif w.rank >= 0 and w.gather_after:
             S = w.shard
             self.shards = []
@@ -213,6 +249,20 @@ class Runner:
             z.zero_step(self.ctx, g, *hp, self.scale, st)
             if self.shards is not None:
                 z.zero_allgather(self.ctx, self.shards, self.params, w.param_dtype, st)
+        elif w.groups:
+            z.zero3_begin_step(self.ctx)
+            groups = self.group_ranges()
+            for g, (f, n) in enumerate(groups):          # forward
+                z.zero3_gather_group(self.ctx, f, self.shards[f:f + n], self.group_fulls[g], st)
+            for g in reversed(range(len(groups))):       # backward
+                f, n = groups[g]
+                z.zero3_gather_group(self.ctx, f, self.shards[f:f + n], self.group_fulls[g], st)
+                if self.scale > 0:
+                    z.zero3_reduce_group(self.ctx, f, n, self.group_grads[g], self.scale, st)
+                else:
+                    z.zero3_step_group(self.ctx, f, n, self.group_grads[g], *hp, st)
+            if self.scale > 0:
+                z.zero_step_apply(self.ctx, *hp, st)
         else:
             z.zero3_begin_step(self.ctx)
             nunits = len(w.units)

@@ -79,6 +79,10 @@ _SIGS = {
     "zero3_step_unit": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f64, _f64, _f64, _f64, _i64,
                                        _vp]),
     "zero3_reduce_unit": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f32, _vp]),
+    "zero3_gather_group": (ctypes.c_int, [_ctxp, _i32, _i32, _vpp, _i32, _vpp, _vp]),
+    "zero3_step_group": (ctypes.c_int, [_ctxp, _i32, _i32, _vpp, _i32, _f64, _f64, _f64, _f64,
+                                        _i64, _vp]),
+    "zero3_reduce_group": (ctypes.c_int, [_ctxp, _i32, _i32, _vpp, _i32, _f32, _vp]),
     "zero_step_noalloc": (ctypes.c_int, [_ctxp, _vpp, _i32, _f64, _f64, _f64, _f64, _i64, _f32,
                                          _vp]),
 }
@@ -349,6 +353,28 @@ def zero3_step_unit(ctx, unit: int, grads, lr: float, beta1: float, beta2: float
 def zero3_reduce_unit(ctx, unit: int, grads, loss_scale: float = 0.0, stream=None) -> None:
     _check(_L.zero3_reduce_unit(_h(ctx), unit, _ptrs(grads), len(grads), loss_scale,
                                 _stream(stream)))
+
+
+def zero3_gather_group(ctx, first_unit: int, shards, unit_fulls, stream=None) -> None:
+    """shards: one list of N shards per unit of the group (or the flat
+    unit-major list); unit_fulls: one destination per unit."""
+    flat = [p for row in shards for p in row] if shards and isinstance(shards[0], (list, tuple)) \
+        else list(shards)
+    _check(_L.zero3_gather_group(_h(ctx), first_unit, len(unit_fulls), _ptrs(flat), len(flat),
+                                 _ptrs(unit_fulls), _stream(stream)))
+
+
+def zero3_step_group(ctx, first_unit: int, n_units: int, grads, lr: float, beta1: float,
+                     beta2: float, eps: float, t: int, stream=None) -> None:
+    """grads: N buffers, rank k's grads of the group's units end to end."""
+    _check(_L.zero3_step_group(_h(ctx), first_unit, n_units, _ptrs(grads), len(grads), lr,
+                               beta1, beta2, eps, t, _stream(stream)))
+
+
+def zero3_reduce_group(ctx, first_unit: int, n_units: int, grads, loss_scale: float = 0.0,
+                       stream=None) -> None:
+    _check(_L.zero3_reduce_group(_h(ctx), first_unit, n_units, _ptrs(grads), len(grads),
+                                 loss_scale, _stream(stream)))
 
 
 # ------------------------------------------------- step without allocation

@@ -904,6 +904,107 @@ int zero3_reduce_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32
     return do_reduce(c, r, grads, loss_scale, (cudaStream_t)stream);
 }
 
+// A run of consecutive units of stage 3 as one range (their state, scratch
+// and param shards lie end to end).  A unit with padding in this view cannot
+// join a group: the kernels treat only the tail of a range as padding.
+static int group_range(zero_ctx *c, int32_t first, int32_t count, Range *out)
+{
+    const int32_t U = (int32_t)c->unit_S.size();
+    if (count < 1 || first < 0 || first > U - count)
+        return fail(ZERO_EINVAL, "units [%d, %d) outside [0, %d)", first, first + count, U);
+    for (int32_t u = first; u < first + count; ++u) {
+        const Range ru = unit_range(c, u);
+        if (ru.n_valid != ru.n)
+            return fail(ZERO_EINVAL, "unit %d has padding in this view: step it on its own", u);
+    }
+    Range r = unit_range(c, first);
+    const Range last = unit_range(c, first + count - 1);
+    r.n = last.state_off + last.n - r.state_off;
+    r.n_valid = r.n;
+    *out = r;
+    return ZERO_OK;
+}
+
+int zero3_gather_group(zero_ctx *c, int32_t first_unit, int32_t n_units,
+                       const void *const *shards, int32_t n_shards, void *const *unit_fulls,
+                       void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if (c->stage != 3) return fail(ZERO_EINVAL, "unit calls are for stage 3");
+    const int32_t U = (int32_t)c->unit_S.size();
+    if (n_units < 1 || first_unit < 0 || first_unit > U - n_units)
+        return fail(ZERO_EINVAL, "units [%d, %d) outside [0, %d)", first_unit,
+                    first_unit + n_units, U);
+    if ((int64_t)n_units * c->world > zgb::kMaxRows)
+        return fail(ZERO_EINVAL, "a group gather places at most %d shards (%d units x %d ranks)",
+                    zgb::kMaxRows, n_units, c->world);
+    if (n_shards != n_units * c->world)
+        return fail(ZERO_EINVAL, "shards: %d pointers given, the group needs %d", n_shards,
+                    n_units * c->world);
+    if (!shards || !unit_fulls) return fail(ZERO_EINVAL, "null pointer array");
+    const int es = zgb::elem_size(c->pdt);
+    zgb::GatherRowsArgs a;
+    memset(&a, 0, sizeof a);
+    a.es = es;
+    for (int32_t ul = 0; ul < n_units; ++ul) {
+        const int64_t Su = c->unit_S[first_unit + ul];
+        char *full = static_cast<char *>(unit_fulls[ul]);
+        if (!full && Su > 0) return fail(ZERO_EINVAL, "unit_fulls[%d] is null", ul);
+        if (!aligned(full, es)) return fail(ZERO_EALIGN, "unit_fulls[%d] not aligned to %d bytes", ul, es);
+        for (int32_t k = 0; k < c->world; ++k) {
+            const int32_t y = ul * c->world + k;
+            if (shards[y] && !aligned(shards[y], es))
+                return fail(ZERO_EALIGN, "shards[%d] is not aligned to its %d-byte elements", y, es);
+            a.src[y] = Su > 0 ? shards[y] : nullptr;
+            a.dst[y] = full + (int64_t)k * Su * es;
+            a.bytes[y] = Su * es;
+        }
+    }
+    a.n = n_units * c->world;
+    // like every gather, this one leaves the flag word alone and does not
+    // become the stream zero_step_status waits on
+    const cudaError_t e = zgb::launch_gather_rows(a, c->sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "group gather kernel");
+}
+
+int zero3_step_group(zero_ctx *c, int32_t first_unit, int32_t n_units, const void *const *grads,
+                     int32_t n_grads, double lr, double b1, double b2, double eps, int64_t t,
+                     void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if ((rc = check_unit(c, first_unit))) return rc;
+    if ((rc = check_hyper(t))) return rc;
+    if (c->step_scaled)
+        return fail(ZERO_ESTATE, "this step is loss-scaled: use zero3_reduce_group + zero_step_apply");
+    Range r;
+    if ((rc = group_range(c, first_unit, n_units, &r))) return rc;
+    rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n > 0, "grads");
+    if (rc) return rc;
+    return do_fused(c, r, grads, lr, b1, b2, eps, t, (cudaStream_t)stream);
+}
+
+int zero3_reduce_group(zero_ctx *c, int32_t first_unit, int32_t n_units,
+                       const void *const *grads, int32_t n_grads, float loss_scale, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if ((rc = check_unit(c, first_unit))) return rc;
+    if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
+    Range r;
+    if ((rc = group_range(c, first_unit, n_units, &r))) return rc;
+    rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n > 0, "grads");
+    if (rc) return rc;
+    if (c->hyper) {
+        if ((loss_scale > 0.0f) != c->step_scaled)
+            return fail(ZERO_EINVAL, "loss scaling differs from the prepared step");
+    } else if (loss_scale > 0.0f) {
+        c->step_scaled = true;
+    }
+    return do_reduce(c, r, grads, loss_scale, (cudaStream_t)stream);
+}
+
 }  // extern "C"
 
 // ------------------------------------------------- step without allocation

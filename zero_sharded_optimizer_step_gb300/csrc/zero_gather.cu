@@ -57,16 +57,13 @@ __device__ __forceinline__ void copy_elem(char *d, const char *s, int es)
     else *reinterpret_cast<unsigned short *>(d) = *reinterpret_cast<const unsigned short *>(s);
 }
 
-__global__ void __launch_bounds__(kThreads)
-gather_kernel(const __grid_constant__ GatherArgs a)
+// One row of a placement: nb bytes from src to dst, spread over the row's
+// nblk blocks (this one is number blk).  Block 0 of the row also copies the
+// ragged head (up to the source's next 16-byte boundary) and tail element
+// by element.
+__device__ __forceinline__ void gather_row(const char *src, char *dst, int64_t nb, int es,
+                                           int64_t blk, int64_t nblk)
 {
-    pdl_wait();                 // the previous kernel in the stream is done
-    pdl_launch_dependents();
-    const int k = blockIdx.y;
-    const char *src = static_cast<const char *>(a.src[k]);
-    if (src == nullptr) return;
-    char *dst = a.dst + (int64_t)k * a.shard_bytes;
-    const int64_t nb = a.shard_bytes;
     int64_t head = (int64_t)((16 - ((uintptr_t)src & 15)) & 15);
     if (head > nb) head = nb;
     const int64_t nchunks = (nb - head) >> 4;
@@ -74,17 +71,17 @@ gather_kernel(const __grid_constant__ GatherArgs a)
     const uintptr_t d0 = (uintptr_t)(dst + head);
     const int align = (d0 & 15) == 0 ? 16 : (d0 & 7) == 0 ? 8 : (d0 & 3) == 0 ? 4 : 2;
 
-    if (blockIdx.x == 0) {
-        for (int64_t b = (int64_t)threadIdx.x * a.es; b < head; b += (int64_t)blockDim.x * a.es)
-            copy_elem(dst + b, src + b, a.es);
-        for (int64_t b = tail + (int64_t)threadIdx.x * a.es; b < nb; b += (int64_t)blockDim.x * a.es)
-            copy_elem(dst + b, src + b, a.es);
+    if (blk == 0) {
+        for (int64_t b = (int64_t)threadIdx.x * es; b < head; b += (int64_t)blockDim.x * es)
+            copy_elem(dst + b, src + b, es);
+        for (int64_t b = tail + (int64_t)threadIdx.x * es; b < nb; b += (int64_t)blockDim.x * es)
+            copy_elem(dst + b, src + b, es);
     }
 
     const char *s = src + head;
     char *d = dst + head;
-    const int64_t T = (int64_t)gridDim.x * blockDim.x;
-    int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t T = nblk * blockDim.x;
+    int64_t c = blk * blockDim.x + threadIdx.x;
     // kItems chunks per thread per round, each T apart so a warp's accesses
     // stay contiguous
     for (; c + (kItems - 1) * T < nchunks; c += kItems * T) {
@@ -95,6 +92,37 @@ gather_kernel(const __grid_constant__ GatherArgs a)
         for (int u = 0; u < kItems; ++u) st_any(d + ((c + u * T) << 4), v[u], align);
     }
     for (; c < nchunks; c += T) st_any(d + (c << 4), ld_stream(s + (c << 4)), align);
+}
+
+__global__ void __launch_bounds__(kThreads)
+gather_kernel(const __grid_constant__ GatherArgs a)
+{
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
+    const int k = blockIdx.y;
+    const char *src = static_cast<const char *>(a.src[k]);
+    if (src == nullptr) return;
+    gather_row(src, a.dst + (int64_t)k * a.shard_bytes, a.shard_bytes, a.es, blockIdx.x,
+               gridDim.x);
+}
+
+__global__ void __launch_bounds__(kThreads)
+gather_rows_kernel(const __grid_constant__ GatherRowsArgs a)
+{
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
+    // the row this block belongs to: the last y with first_block[y] <= b
+    const int32_t b = (int32_t)blockIdx.x;
+    int lo = 0, hi = a.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.first_block[mid] <= b) lo = mid; else hi = mid - 1;
+    }
+    const int y = lo;
+    const char *src = static_cast<const char *>(a.src[y]);
+    if (src == nullptr || a.bytes[y] <= 0) return;
+    gather_row(src, a.dst[y], a.bytes[y], a.es, b - a.first_block[y],
+               a.first_block[y + 1] - a.first_block[y]);
 }
 
 
@@ -244,6 +272,35 @@ cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s)
     if (bx < 1) bx = 1;
     dim3 grid((unsigned)bx, (unsigned)a.n);
     return launch_dependent(gather_kernel, grid, dim3(kThreads), 0, s, a);
+}
+
+cudaError_t launch_gather_rows(const GatherRowsArgs &a, int sms, cudaStream_t s)
+{
+    if (a.n <= 0) return cudaSuccess;
+    if (a.n > kMaxRows) return cudaErrorInvalidValue;
+    const int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(gather_rows_kernel),
+                                              kThreads);
+    // each row gets the blocks its length needs, at most twice the resident
+    // blocks (as launch_gather); rows are laid out one after another in the
+    // grid, so they are dispatched in order and one or two are in flight
+    const int64_t cap = 2 * (int64_t)sms * per_sm;
+    GatherRowsArgs r = a;
+    int64_t total = 0;
+    for (int32_t y = 0; y < a.n; ++y) {
+        r.first_block[y] = (int32_t)total;
+        int64_t want = 0;
+        if (a.src[y] && a.bytes[y] > 0) {
+            const int64_t chunks = (a.bytes[y] + 15) / 16;
+            want = (chunks + (int64_t)kThreads * kItems - 1) / ((int64_t)kThreads * kItems);
+            if (want < 1) want = 1;
+            if (want > cap) want = cap;
+        }
+        total += want;
+        if (total > 0x7fffffff) return cudaErrorInvalidValue;
+    }
+    r.first_block[a.n] = (int32_t)total;
+    if (total == 0) return cudaSuccess;
+    return launch_dependent(gather_rows_kernel, dim3((unsigned)total), dim3(kThreads), 0, s, r);
 }
 
 bool lean_gather_eligible(const GatherArgs &a)

@@ -73,6 +73,21 @@ struct GatherArgs {
     int32_t es;                    // element size in bytes
 };
 
+// A placement of independent rows in one launch: row y copies bytes[y]
+// bytes from src[y] to dst[y] (a group of units, one row per unit and shard).
+// The launcher fills first_block: row y owns blocks [first_block[y],
+// first_block[y + 1]) of the one-dimensional grid, as many as its length
+// needs.
+constexpr int kMaxRows = 512;
+struct GatherRowsArgs {
+    const void *src[kMaxRows];     // null = skip the row
+    char *dst[kMaxRows];
+    int64_t bytes[kMaxRows];       // multiple of es
+    int32_t first_block[kMaxRows + 1];
+    int32_t n;                     // rows
+    int32_t es;
+};
+
 // Blocks of `threads` threads of `kernel` that fit on one SM of the current
 // device (cached per kernel and device; at least 1).
 int resident_blocks_per_sm(const void *kernel, int threads);
@@ -122,6 +137,8 @@ cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s
 // from it.
 cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s);
+// Fills a copy's first_block table and launches; `a` itself is not changed.
+cudaError_t launch_gather_rows(const GatherRowsArgs &a, int sms, cudaStream_t s);
 // The bulk-copy (TMA) placement for 16-byte aligned shards: one warp per SM,
 // for gathers that run beside other kernels.  cudaErrorInvalidValue when the
 // shards are not eligible (lean_gather_eligible).
