@@ -49,11 +49,12 @@ import numpy as np  # noqa: E402
 # kernel source it was taken on (sha256 prefix); otherwise bench reports null.
 TRAFFIC = {
     ("gpt2_xl", "fused_step_kernel"): ("2cb1a8d55f497d73", 68.538e9 + 21.777e9),
-    ("one_rank_7p5b", "gather_kernel"): ("c24f81b787f5ee20", 14.786e9 + 14.721e9),
-    ("one_rank_7p5b", "fused_step_kernel"): ("2cb1a8d55f497d73", 16.406e9 + 1.621e9),
-    # mean of two full-size launches; part of each launch's writes is still in
-    # L2 when it ends
-    ("zero3_llama7b", "gather_kernel"): ("c24f81b787f5ee20", 404.81e6 + 352.97e6),
+    ("one_rank_7p5b", "gather_kernel"): ("91d51734053b3f9b", 14.786e9 + 14.721e9),
+    ("one_rank_7p5b", "fused_step_kernel"): ("2cb1a8d55f497d73", 16.407e9 + 1.621e9),
+    # means of two full-size launches; part of each launch's writes is still
+    # in L2 when it ends
+    ("zero3_llama7b", "gather_kernel"): ("91d51734053b3f9b", 404.81e6 + 352.84e6),
+    ("fsdp2_llama7b", "gather_rows_kernel"): ("91d51734053b3f9b", 404.79e6 + 348.01e6),
 }
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
                           "zero_step_kernels.cu")
@@ -376,7 +377,7 @@ def bench_ours(args, rank, world_size, device_index):
     avg_ms = tot_ms / n_launch
     peak, peak_kind = peaks()
     achieved = alg_per_launch / (avg_ms * 1e-3) / 1e9
-    kh = src_hash(GATHER_SRC if dom == "gather_kernel" else KERNEL_SRC)
+    kh = src_hash(GATHER_SRC if dom in ("gather_kernel", "gather_rows_kernel") else KERNEL_SRC)
     tr = None if (args.numel or args.units) else TRAFFIC.get((args.workload, dom))
     traffic = tr[1] if tr and tr[0] == kh else None
 
