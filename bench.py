@@ -598,11 +598,21 @@ def method_min_bytes(w):
 
 
 def describe(w):
-    return ("%s: numel=%d world=%d stage=%d grad=%s param=%s rank=%s%s%s"
+    if not w.units:
+        units = ""
+    elif len(set(w.units)) == 1:
+        units = " units=%dx%d" % (len(w.units), w.units[0])
+    else:
+        units = " units=%d (%d to %d elements)" % (len(w.units), min(w.units), max(w.units))
+    if w.unit_rows:
+        units += " dim-0 row shards"
+    if w.groups:
+        units += " in %d groups" % len(w.groups)
+    return ("%s: numel=%d world=%d stage=%d grad=%s param=%s rank=%s%s%s%s"
             % (w.name, w.numel, w.world, w.stage, "f32 bf16 f16".split()[w.grad_dtype],
                "f32 bf16 f16".split()[w.param_dtype], "all" if w.rank < 0 else w.rank,
                " loss_scale=%g" % w.loss_scale if w.loss_scale else "",
-               " units=%dx%d" % (len(w.units), w.units[0]) if w.units else ""))
+               " weight_decay=%g" % w.weight_decay if w.weight_decay else "", units))
 
 
 def bench_e2e(run, plan, args, world_size):
