@@ -40,6 +40,7 @@
  *   nonfinite |= !isfinite(g)            (over every element of the step)
  *   m   = b1*m + (1-b1)*g ;  v = b2*v + (1-b2)*(g*g)
  *   x   = x - (lr * (m/(1-b1^t))) / (sqrt(v/(1-b2^t)) + eps)
+ *         (AdamW, zero_set_weight_decay: x*(1 - lr*wd) in place of the first x)
  *   param = round-to-nearest-even(x) in the param type
  * each operation a single IEEE binary32 operation (no fused multiply-add, no
  * flush to zero).  lr, b1, b2 and eps arrive as doubles; the fp32 scalars
@@ -56,8 +57,13 @@
  *     cudaMalloc).  The library never allocates device memory; the context
  *     itself is a small host object.
  *   - Launching calls are asynchronous on the caller's stream (a
- *     cudaStream_t passed as void*; NULL = legacy default stream).  Only
- *     zero_step_status() synchronizes.
+ *     cudaStream_t passed as void*; NULL = legacy default stream).  Only the
+ *     calls that read a device word back synchronize: zero_step_status(),
+ *     zero_current_state() and zero_gather_timeouts().
+ *   - The step kernels and the SM gathers are launched with programmatic
+ *     dependent launch: one may be scheduled while the kernel before it in the
+ *     stream is finishing, but it touches memory only after that kernel has
+ *     completed, so stream order holds as for any launch.
  *   - Device pointers must be aligned to their element size.  16-byte
  *     alignment is not required: unaligned buffers take slower but correct
  *     paths.
