@@ -20,9 +20,9 @@
 // The work is a few flops per byte, so HBM bandwidth bounds every kernel;
 // no tensor cores are involved.  Each thread handles kVec = 8 consecutive
 // elements per iteration with 16-byte loads (one per 16-bit gradient
-// buffer), issues the state loads and a chunk of 4 gradient loads before
-// consuming any, and walks a grid sized to fill every SM (grid-stride
-// loop, 64-bit indices).  Elements past the last full vector, padding
+// buffer): the ranks' loads in chunks of 4, each chunk issued before its
+// adds, then the state loads, and walks a grid sized to fill every SM
+// (grid-stride loop, 64-bit indices).  Elements past the last full vector, padding
 // positions and buffers that are not 16-byte aligned take a per-element path
 // that performs the same operations in the same order.
 //
