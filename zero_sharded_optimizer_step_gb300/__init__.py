@@ -15,3 +15,11 @@ def dtype_code(torch_dtype) -> int:
     if torch_dtype not in codes:
         raise ValueError("unsupported dtype %s" % torch_dtype)
     return codes[torch_dtype]
+
+
+def __getattr__(name):
+    # the ZeroAdam facade imports torch; load it on first use
+    if name == "ZeroAdam":
+        from .optim import ZeroAdam
+        return ZeroAdam
+    raise AttributeError(name)

@@ -1,0 +1,130 @@
+"""ZeroAdam: the optimizer interface of "ZeRO 与 FSDP：切分优化器状态、梯度与参数"
+(section 从零实现 ZeRO 的 Adam: ZeroAdam(params, lr, betas, eps) with step(),
+zero_grad() and state_bytes()) over the C ABI, for N data-parallel ranks
+simulated on one GPU.
+
+Buffer management only.  The model's parameters become views of one flat,
+zero-padded parameter buffer (the page's flat vector in parameters() order);
+each simulated rank gets a flat gradient buffer with per-parameter views for
+its backward to write into; master weights, m and v are fp32 buffers of the
+padded length.  step() is one zero_step call: the reduce-scatter, average,
+optional unscale and overflow skip, Adam, cast and placement all run in the
+library's kernels.
+"""
+from __future__ import annotations
+
+from typing import Iterable, List
+
+import torch
+
+from . import binding as z
+
+_DT = {torch.float32: z.ZERO_F32, torch.bfloat16: z.ZERO_BF16, torch.float16: z.ZERO_F16}
+
+
+class ZeroAdam:
+    """Sharded mixed-precision Adam (ZeRO stage 2) for `world` ranks on this GPU.
+
+    params        tensors of one dtype (fp32, bf16 or fp16) on one CUDA device;
+                  afterwards each is a view of self.flat (same values).
+    world         N, the data-parallel ranks simulated here.
+    grad_dtype    element type of the ranks' grads (default: the params').
+    loss_scale    > 0 turns on loss scaling: grads are divided by it, a step
+                  whose grads hold inf/nan is skipped and the scale halved,
+                  and it doubles after growth_interval clean steps.  The step
+                  runs as one pass over two fp32 state sets.
+    weight_decay  decoupled (AdamW) decay; 0 = Adam.
+    """
+
+    def __init__(self, params: Iterable[torch.Tensor], world: int, lr: float = 1e-3,
+                 betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0,
+                 grad_dtype: torch.dtype | None = None, loss_scale: float = 0.0,
+                 growth_interval: int = 2000, stream=None):
+        self.params: List[torch.Tensor] = list(params)
+        if not self.params:
+            raise ValueError("ZeroAdam needs at least one parameter")
+        dev, pdt = self.params[0].device, self.params[0].dtype
+        if dev.type != "cuda" or pdt not in _DT:
+            raise ValueError("parameters must be fp32, bf16 or fp16 CUDA tensors")
+        for p in self.params:
+            if p.device != dev or p.dtype != pdt:
+                raise ValueError("all parameters must share one device and dtype")
+        gdt = grad_dtype or pdt
+        if gdt not in _DT:
+            raise ValueError("grad_dtype must be fp32, bf16 or fp16")
+        self.lr, (self.beta1, self.beta2), self.eps = lr, betas, eps
+        self.world, self.t, self.scale = world, 0, float(loss_scale)
+        self.growth_interval, self.good_steps = growth_interval, 0
+        self.stream = stream
+        self.numel = sum(p.numel() for p in self.params)
+        self.ctx = z.zero_init(self.numel, world, 2, _DT[gdt], _DT[pdt], -1)
+        P = z.zero_ctx_state_elems(self.ctx)
+
+        # the flat padded parameter vector; parameters become views of it
+        self.flat = torch.zeros(P, dtype=pdt, device=dev)
+        self._offsets = []
+        off = 0
+        with torch.no_grad():
+            for p in self.params:
+                n = p.numel()
+                self.flat[off:off + n].copy_(p.reshape(-1))
+                p.data = self.flat[off:off + n].view_as(p)
+                self._offsets.append((off, n))
+                off += n
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.master = self.flat.float()
+        self.m = torch.zeros(P, **f32)
+        self.v = torch.zeros(P, **f32)
+        self.flag = torch.zeros(1, dtype=torch.int64, device=dev)
+        z.zero_bind(self.ctx, self.master, self.m, self.v, self.flat, None, self.flag)
+        self._shadow = None
+        if self.scale > 0:
+            self._shadow = (torch.zeros(P, **f32), torch.zeros(P, **f32), torch.zeros(P, **f32),
+                            torch.zeros(1, dtype=torch.int64, device=dev))
+            self._shadow[0].copy_(self.master)
+            z.zero_bind_shadow(self.ctx, *self._shadow)
+        if weight_decay:
+            z.zero_set_weight_decay(self.ctx, weight_decay)
+        # rank k's flat local gradient (numel elements; the pad needs none)
+        self.grads = [torch.zeros(self.numel, dtype=gdt, device=dev) for _ in range(world)]
+
+    def rank_grads(self, rank: int) -> List[torch.Tensor]:
+        """Per-parameter views of rank `rank`'s gradient buffer, shaped like
+        the parameters (write the rank's backward here)."""
+        g = self.grads[rank]
+        return [g[off:off + n].view_as(p) for p, (off, n) in zip(self.params, self._offsets)]
+
+    def zero_grad(self) -> None:
+        for g in self.grads:
+            g.zero_()
+
+    def step(self) -> bool:
+        """One optimizer step over the ranks' grads.  Returns True when the
+        step was skipped (loss scaling on and a non-finite grad); then t does
+        not advance.  With loss scaling the call reads the verdict back (a
+        synchronization)."""
+        z.zero_step(self.ctx, self.grads, self.lr, self.beta1, self.beta2, self.eps, self.t + 1,
+                    self.scale, self.stream)
+        if self.scale <= 0:
+            self.t += 1
+            return False
+        _, skipped = z.zero_step_status(self.ctx)
+        if not skipped:
+            self.t += 1
+        self.scale, self.good_steps = z.zero_scale_update(self.scale, skipped, self.good_steps,
+                                                          self.growth_interval)
+        return skipped
+
+    def state(self):
+        """(master, m, v) of the current fp32 state set, padded length."""
+        if self._shadow is not None and z.zero_current_state(self.ctx) == 1:
+            return self._shadow[:3]
+        return self.master, self.m, self.v
+
+    def state_bytes(self) -> int:
+        """Bytes of fp32 optimizer state (master, m, v) per rank: 12 * S, as
+        the page's ZeroAdam.state_bytes() reports for its shard."""
+        return 12 * z.zero_ctx_shard_size(self.ctx, -1)
+
+    def close(self) -> None:
+        self.ctx.close()
