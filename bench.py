@@ -48,9 +48,9 @@ import numpy as np  # noqa: E402
 # one pass; summarised under profiles/).  Each entry is valid only for the
 # kernel source it was taken on (sha256 prefix); otherwise bench reports null.
 TRAFFIC = {
-    ("gpt2_xl", "fused_step_kernel"): ("2cb1a8d55f497d73", 68.538e9 + 21.777e9),
+    ("gpt2_xl", "fused_step_kernel"): ("a5b9a674470ff3d3", 68.537e9 + 21.777e9),
     ("one_rank_7p5b", "gather_kernel"): ("91d51734053b3f9b", 14.786e9 + 14.721e9),
-    ("one_rank_7p5b", "fused_step_kernel"): ("2cb1a8d55f497d73", 16.407e9 + 1.621e9),
+    ("one_rank_7p5b", "fused_step_kernel"): ("a5b9a674470ff3d3", 16.407e9 + 1.621e9),
     # means of two full-size launches; part of each launch's writes is still
     # in L2 when it ends
     ("zero3_llama7b", "gather_kernel"): ("91d51734053b3f9b", 404.81e6 + 352.84e6),
@@ -439,7 +439,12 @@ def bench_ours(args, rank, world_size, device_index):
     if not args.no_e2e and not w.bucket:
         e2e = (bench_e2e_pipelined(run, args, world_size) if w.stage < 3 else
                bench_e2e_units(run, args, world_size) if w.rank >= 0 else None)
-        result["e2e"] = e2e or bench_e2e(run, plan, args, world_size)
+        e2e = e2e or bench_e2e(run, plan, args, world_size)
+        # the host link on this machine, for reading e2e against it
+        link = h2d_link_gbs(run.dev)
+        e2e["h2d_link_gbs"] = link
+        e2e["link_bound_ms_per_step"] = e2e["h2d_bytes_per_step"] / (link * 1e9) * 1e3
+        result["e2e"] = e2e
     if not args.no_cpu_baseline and rank == 0:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
     run.close()
@@ -668,6 +673,26 @@ def bench_e2e(run, plan, args, world_size):
             "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": 8, "host_buffers_distinct": len(host),
             "device_buffers": len(dev_bufs)}
+
+
+def h2d_link_gbs(dev, nbytes=2 << 30, reps=3):
+    """Host-to-device bandwidth of one large copy from pinned memory (GB/s),
+    timed with CUDA events on a stream of its own."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        d.copy_(h, non_blocking=True)
+        e0.record(s)
+        for _ in range(reps):
+            d.copy_(h, non_blocking=True)
+        e1.record(s)
+    s.synchronize()
+    gbs = reps * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del h, d
+    return gbs
 
 
 def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
