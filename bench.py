@@ -409,6 +409,10 @@ def bench_ours(args, rank, world_size, device_index):
             "method_min_bytes_per_param": method_min_bytes(w),
             "l2": "inputs larger than L2 (working set %.1f GB)" % (working_set(run) / 1e9),
             "per_kernel_ms": {n: per[n][0] / per[n][1] for n in per},
+            "per_kernel_alg_gbs": {n: sum(L.alg_bytes for L in plan if L.name == n)
+                                   / sum(1 for L in plan if L.name == n)
+                                   / (per[n][0] / per[n][1] * 1e-3) / 1e9
+                                   for n in per if per[n][0] > 0},
             "per_kernel_timing": "a second pass of the same number of steps with an event "
                                  "pair around every launch",
             "parallelism": "%d simulated data-parallel ranks per GPU; %d GPU replica(s)"
