@@ -1,7 +1,7 @@
 """The five workloads at their full sizes, in the launch configuration the
 benchmark times.  The oracle computes sampled elements one by one (the step
-is elementwise): the first and last 4096 positions of every shard plus 2^20
-seeded random positions.  Properties that hold at any size cover the rest:
+is elementwise): the first and last 65,536 positions of every shard plus
+2^20 seeded random positions.  Properties that hold at any size cover the rest:
 the skip pattern, the padding, and the placement (the full buffer is the
 concatenation of the shards)."""
 import numpy as np
@@ -17,12 +17,15 @@ from tests.test_gpu_parity import (assert_bit_identical, assert_params_close,
 pytestmark = pytest.mark.gpu
 
 
-def sample_positions(n_state, S, seed=0, n_rand=1 << 20):
+EDGE = 1 << 16      # positions sampled at each end of every shard
+
+
+def sample_positions(n_state, S, seed=0, n_rand=1 << 20, edge=EDGE):
     rng = np.random.default_rng(seed)
-    idx = [np.arange(0, min(4096, n_state))]
+    idx = [np.arange(0, min(edge, n_state))]
     for lo in range(0, n_state, S):
-        idx.append(np.arange(lo, min(lo + 4096, n_state)))
-        idx.append(np.arange(max(lo, min(lo + S, n_state) - 4096), min(lo + S, n_state)))
+        idx.append(np.arange(lo, min(lo + edge, n_state)))
+        idx.append(np.arange(max(lo, min(lo + S, n_state) - edge), min(lo + S, n_state)))
     idx.append(rng.integers(0, n_state, n_rand))
     return np.unique(np.concatenate(idx)).astype(np.int64)
 
@@ -128,6 +131,29 @@ def test_zero3_llama7b_full():
     run.close()
 
 
+def test_fsdp2_llama7b_grouped_full():
+    """32 Llama-7B layers as 288 per-parameter dim-0 units, each layer's nine
+    gathered and stepped as one group (the grads of a group end to end per
+    rank): sampled state of every kind of parameter matches the oracle, and
+    the last group gather placed the other ranks' shards of every unit."""
+    from zero_sharded_optimizer_step_gb300 import zero_ctx_unit_state_offset
+    w = W.fsdp2_llama7b()
+    run = run_all(w)
+    assert run.skips == [False] * w.steps
+    for u in (0, 4, 6, 7, 8, 148, 287):            # q, gate, down, both norms, mid, last
+        Su = w.unit_shard(u)
+        off = zero_ctx_unit_state_offset(run.ctx, u)
+        idx = sample_positions(Su, Su, seed=u, n_rand=1 << 15)
+        check_sampled(run, w, idx, unit=u, state_off=off)
+    # the last group gather was layer 0's (before its backward)
+    for ul, full in enumerate(run.group_fulls[0]):
+        Su = w.unit_shard(ul)
+        for k in range(w.world):
+            if k != w.rank:
+                assert torch.equal(full[k * Su:(k + 1) * Su], run.shards[ul][k])
+    run.close()
+
+
 @pytest.mark.parametrize("shadow", [True, False])
 def test_gpt2_xl_bucketed_full(shadow):
     """The bucketed step (32 Mi-element buckets) at the full GPT-2 XL size,
@@ -137,7 +163,7 @@ def test_gpt2_xl_bucketed_full(shadow):
     run = run_all(w, shadow=shadow)
     assert run.skips == [i == 3 for i in range(1, w.steps + 1)]
     P = w.shard * w.world
-    idx = sample_positions(P, 1 << 25, n_rand=1 << 19)      # bucket edges included
+    idx = sample_positions(P, 1 << 25, n_rand=1 << 19, edge=4096)   # every bucket edge
     check_sampled(run, w, idx, skipped=(3,))
     run.close()
 
