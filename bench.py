@@ -74,7 +74,8 @@ def parse():
     ap.add_argument("--workload", default="gpt2_xl",
                     choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny",
                              "gpt2_xl_bucketed", "zero3_prefetch", "zero3_gpt2_small",
-                             "gpt2_xl_adamw", "fsdp2_llama7b", "fsdp2_llama7b_per_param"])
+                             "gpt2_xl_adamw", "fsdp2_llama7b", "fsdp2_llama7b_per_param",
+                             "gpt2_small_stage1"])
     ap.add_argument("--graph", action="store_true",
                     help="also capture one step in a CUDA graph and time its replays")
     ap.add_argument("--unit-fwd-ms", type=float, default=0.25,
@@ -222,8 +223,10 @@ def step_plan(run):
             def fused():
                 z.zero_step(run.ctx, run.grads[0], w.lr, w.beta1, w.beta2, w.eps, run.t + 1,
                             0.0, st)
-            plan.append(Launch("fused_step_kernel", w.world * bg * n_valid + (24 + bp) * n_state,
-                               fused))
+            # stage 1 with the all-reduce output also writes the mean grads
+            avg = bg * n_state if run.grad_avg is not None else 0
+            plan.append(Launch("fused_step_kernel",
+                               w.world * bg * n_valid + (24 + bp) * n_state + avg, fused))
         if run.shards is not None:
             n_sh = sum(1 for s in run.shards if s is not None)
 
@@ -603,7 +606,7 @@ def working_set(run):
 def method_min_bytes(w):
     bg = 4 if w.grad_dtype == 0 else 2
     bp = 4 if w.param_dtype == 0 else 2
-    return w.world * bg + 24 + bp
+    return w.world * bg + 24 + bp + (bg if w.allreduce_out else 0)
 
 
 def describe(w):
@@ -617,6 +620,8 @@ def describe(w):
         units += " dim-0 row shards"
     if w.groups:
         units += " in %d groups" % len(w.groups)
+    if w.allreduce_out:
+        units += " all-reduce output"
     return ("%s: numel=%d world=%d stage=%d grad=%s param=%s rank=%s%s%s%s"
             % (w.name, w.numel, w.world, w.stage, "f32 bf16 f16".split()[w.grad_dtype],
                "f32 bf16 f16".split()[w.param_dtype], "all" if w.rank < 0 else w.rank,

@@ -68,6 +68,7 @@ class Workload:
     inject: Optional[Tuple[int, int]] = None   # (iteration, rank): one +inf
     gather_after: bool = False           # place the other ranks' shards too
     bucket: int = 0                      # > 0: step bucket by bucket (elements per bucket)
+    allreduce_out: bool = False          # stage 1: also write the averaged grads (all-reduce)
     seed: int = 0
 
     @property
@@ -98,6 +99,13 @@ def tiny() -> Workload:
 
 def gpt2_small() -> Workload:
     return Workload("gpt2_small", gpt2_numel(768, 12), 8, 2, BF16, BF16, steps=10)
+
+
+def gpt2_small_stage1() -> Workload:
+    """Stage 1 over the GPT-2 small workload, keeping the all-reduced mean
+    grads in a full buffer beside the sharded step (ZeRO-1: grads stay whole,
+    only the optimizer states are sharded)."""
+    return gpt2_small().replace(name="gpt2_small_stage1", stage=1, allreduce_out=True)
 
 
 def gpt2_xl() -> Workload:
@@ -171,7 +179,8 @@ def zero3_gpt2_small() -> Workload:
 
 
 ALL = {"tiny": tiny, "zero3_gpt2_small": zero3_gpt2_small, "gpt2_xl_bucketed": gpt2_xl_bucketed,
-       "gpt2_small": gpt2_small, "gpt2_xl": gpt2_xl, "gpt2_xl_adamw": gpt2_xl_adamw,
+       "gpt2_small": gpt2_small, "gpt2_small_stage1": gpt2_small_stage1,
+       "gpt2_xl": gpt2_xl, "gpt2_xl_adamw": gpt2_xl_adamw,
        "one_rank_7p5b": one_rank_7p5b, "zero3_llama7b": zero3_llama7b,
        "fsdp2_llama7b": fsdp2_llama7b, "fsdp2_llama7b_per_param": fsdp2_llama7b_per_param}
 

@@ -61,6 +61,12 @@ class Runner:
             z.zero_bind_shadow(self.ctx, *self.shadow, self.cur)
         if w.weight_decay:
             z.zero_set_weight_decay(self.ctx, w.weight_decay)
+        self.grad_avg = None
+        if w.allreduce_out:
+            # stage 1: the all-reduced mean grads, P elements of the grad type
+            self.grad_avg = torch.zeros(w.shard * w.world, dtype=TORCH_DTYPE[w.grad_dtype],
+                                        device=self.dev)
+            z.zero_bind_allreduce_out(self.ctx, self.grad_avg)
         self.hyper = None
         if hyper:
             # the per-step scalars from a device block (the form a CUDA graph
