@@ -79,3 +79,60 @@ def test_reference_arm_under_torchrun_two_ranks():
                   "--steps", "1", "--warmup", "1"])
     assert len(lines) == 1
     assert _check(lines[0])["n_gpus"] == 2
+
+
+def _plan_bytes(w, shadow=False):
+    """The bench's per-step algorithmic bytes for a workload, from its launch
+    plan built on a stand-in for the GPU runner (no launch is made)."""
+    from types import SimpleNamespace
+    sys.path.insert(0, ROOT)
+    import bench
+
+    def bucket_ranges():
+        n = w.shard * (w.world if w.rank < 0 else 1)
+        return [(off, min(w.bucket, n - off)) for off in range(0, n, w.bucket)]
+
+    def group_ranges():
+        out, first = [], 0
+        for n in w.groups or []:
+            out.append((first, n))
+            first += n
+        return out
+    shards = None
+    if w.stage == 3:
+        shards = [[None] * w.world for _ in w.units]
+    elif w.rank >= 0 and w.gather_after:
+        shards = [None if k == w.rank else object() for k in range(w.world)]
+    run = SimpleNamespace(w=w, stream=None, shadow=(None,) if shadow else None,
+                          scale=w.loss_scale, grads=[[None]], shards=shards,
+                          grad_avg=object() if w.allreduce_out else None, bucket_buffers=None,
+                          bucket_ranges=bucket_ranges, group_ranges=group_ranges,
+                          group_fulls=[None] * len(w.groups or []), group_grads=None,
+                          params=None, unit_full=None, ctx=None, t=0)
+    return sum(L.alg_bytes for L in bench.step_plan(run))
+
+
+def test_algorithmic_bytes_match_the_closed_forms():
+    """The bytes behind every roofline figure: per parameter N*b_g + 24 + b_p
+    for the fused step (+ b_g with the all-reduce output), 36 + 30 for the
+    two passes, 2*b_p per placed element, two unit gathers per ZeRO-3 step."""
+    sys.path.insert(0, ROOT)
+    import workloads as W
+    xl = W.gpt2_xl()
+    psi = xl.numel
+    assert _plan_bytes(xl, shadow=True) == 58 * psi == 90_341_449_600
+    assert _plan_bytes(xl) == (16 * 2 + 4) * psi + (4 + 24 + 2) * psi        # two passes
+    assert _plan_bytes(W.gpt2_xl_adamw(), shadow=True) == 58 * psi
+    assert _plan_bytes(W.gpt2_xl_bucketed(), shadow=True) == 58 * psi
+    sm = W.gpt2_small()
+    assert _plan_bytes(sm) == 42 * sm.numel
+    assert _plan_bytes(W.gpt2_small_stage1()) == 44 * sm.numel
+    one = W.one_rank_7p5b(0)
+    S = one.shard
+    assert _plan_bytes(one) == (64 * 2 + 26) * S + 63 * 2 * 2 * S == 47_578_125_000
+    z3 = W.zero3_llama7b()
+    Su = z3.unit_shard(0)
+    assert _plan_bytes(z3) == 32 * (2 * 2 * 2 * 8 + 8 * 2 + 26) * Su == 85_810_544_640
+    fs = W.fsdp2_llama7b()
+    assert sum(fs.unit_shard(u) for u in range(len(fs.units))) == 32 * Su
+    assert _plan_bytes(fs) == _plan_bytes(W.fsdp2_llama7b_per_param()) == 85_810_544_640
