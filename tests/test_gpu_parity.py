@@ -857,6 +857,10 @@ HYPER_CASES += [
     (dict(gdt=W.BF16, pdt=W.BF16, units=[300_001, 77, 123_456], rank=1), {}),
     (dict(gdt=W.BF16, pdt=W.BF16, units=[300_001, 77, 123_456], loss_scale=2.0 ** 8,
           inject=(2, 2)), {}),
+    # groups of units (sizes divisible by the 8 ranks: no padding)
+    (dict(gdt=W.BF16, pdt=W.BF16, units=[300_000, 80_000, 123_456], groups=[2, 1]), {}),
+    (dict(gdt=W.F16, pdt=W.F16, units=[300_000, 80_000, 123_456], groups=[1, 2],
+          loss_scale=2.0 ** 8, inject=(2, 2)), {}),
 ]
 
 
