@@ -117,7 +117,8 @@ double zero_model_state_bytes(int64_t numel, int32_t world, int32_t stage);
 /* Loss-scale update after a step, as GradScaler.update does ("PaddlePaddle
  * ZeRO优化", 混合精度才是最佳拍档): a skipped step halves the scale and
  * resets *good_steps; otherwise *good_steps counts up and, on reaching
- * growth_interval (> 0), the scale doubles and the count restarts.
+ * growth_interval (> 0), the scale doubles (unless that would overflow to
+ * infinity, when it stays) and the count restarts.
  * Returns the new scale; a NULL good_steps returns the scale unchanged. */
 float zero_scale_update(float scale, int32_t skipped, int64_t *good_steps,
                         int64_t growth_interval);

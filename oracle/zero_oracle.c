@@ -393,7 +393,9 @@ float orc_scale_update(float scale, int32_t skipped, int64_t *good_steps,
     *good_steps += 1;
     if (growth_interval > 0 && *good_steps >= growth_interval) {
         *good_steps = 0;
-        return scale * 2.0f;
+        /* grow only to a finite scale */
+        const float grown = scale * 2.0f;
+        return isfinite(grown) ? grown : scale;
     }
     return scale;
 }

@@ -193,3 +193,27 @@ def test_scale_update_policy():
     assert (s, g) == (32768.0, 1999)
     s, g = oracle.scale_update(32768.0, False, 1999, 2000)
     assert (s, g) == (65536.0, 0)
+
+
+def test_scale_update_equals_torch_grad_scaler():
+    """The loss-scale policy against a library routine: PyTorch's GradScaler
+    update (backoff 0.5 on a non-finite step, growth x2 after growth_interval
+    clean steps, never growing to infinity), over random sequences of
+    skipped and clean steps, from ordinary and extreme scales."""
+    import torch
+    rng = np.random.default_rng(5)
+    fmax = float(np.finfo(np.float32).max)
+    starts = [65536.0, 1.0, 2.0 ** -140, 2.0 ** 126, fmax / 2, 3.0]
+    for trial in range(60):
+        interval = int(rng.integers(1, 6))
+        s0 = starts[trial % len(starts)]
+        s_o, g_o = s0, 0
+        s_t = torch.tensor([s0], dtype=torch.float32)
+        g_t = torch.tensor([0], dtype=torch.int32)
+        for _ in range(40):
+            skipped = bool(rng.random() < 0.3)
+            s_o, g_o = oracle.scale_update(s_o, skipped, g_o, interval)
+            torch._amp_update_scale_(s_t, g_t, torch.tensor([1.0 if skipped else 0.0]),
+                                     2.0, 0.5, interval)
+            assert np.float32(s_o).tobytes() == s_t.numpy().tobytes(), (trial, s_o, s_t)
+            assert g_o == int(g_t.item())

@@ -38,6 +38,11 @@ MUTANTS = [
     ("dim-0 shard not whole rows", "return (rows + world - 1) / world * row_elems;",
      "return (rows * row_elems + world - 1) / world;"),
     ("scale doubled on a skip", "return scale * 0.5f;", "return scale * 2.0f;"),
+    ("scale grows to infinity", "return isfinite(grown) ? grown : scale;", "return grown;"),
+    ("scale grows by 4", "const float grown = scale * 2.0f;", "const float grown = scale * 4.0f;"),
+    ("clean-step count kept after growth",
+     "        *good_steps = 0;\n        /* grow only to a finite scale */",
+     "        /* grow only to a finite scale */"),
 ]
 
 

@@ -401,7 +401,8 @@ float zero_scale_update(float scale, int32_t skipped, int64_t *good_steps, int64
     }
     if (++*good_steps >= growth_interval && growth_interval > 0) {
         *good_steps = 0;
-        return scale * 2.0f;
+        const float grown = scale * 2.0f;      // grow only to a finite scale
+        return isfinite(grown) ? grown : scale;
     }
     return scale;
 }
