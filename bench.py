@@ -925,11 +925,12 @@ def oracle_time(w, n_s, steps, threads=1):
         n, g, x, m, v, out = piece
         if w.rank < 0 and w.stage < 3:
             oracle.zero_step(g, w.grad_dtype, n, x, m, v, out, w.param_dtype, w.lr, w.beta1,
-                             w.beta2, w.eps, t, loss_scale=w.loss_scale)
+                             w.beta2, w.eps, t, loss_scale=w.loss_scale,
+                             weight_decay=w.weight_decay)
         else:
             oracle.zero_rank_step(g, w.grad_dtype, n * w.world, 0, x, m, v, out,
                                   w.param_dtype, w.lr, w.beta1, w.beta2, w.eps, t,
-                                  loss_scale=w.loss_scale)
+                                  loss_scale=w.loss_scale, weight_decay=w.weight_decay)
 
     times = []
     if threads == 1:
