@@ -219,8 +219,9 @@ int zero_bind(zero_ctx *ctx, float *master, float *m, float *v, void *params,
  * P-element buffer.  NULL turns it off. */
 int zero_bind_allreduce_out(zero_ctx *ctx, void *grad_avg);
 
-/* Bind a second fp32 state set (stages 1 and 2) so that every step is one
- * pass, loss-scaled or not: the step reads the current set, writes the
+/* Bind a second fp32 state set so that every step is one pass, loss-scaled
+ * or not (stages 1 and 2; for stage 3 see zero3_begin_step_scaled and
+ * zero3_end_step): the step reads the current set, writes the
  * other, and a small finalize kernel then makes the written set current --
  * unless the step is loss-scaled and overflowed, in which case the old set
  * stays current and the params are cast again from it ("PaddlePaddle
@@ -233,7 +234,8 @@ int zero_bind_allreduce_out(zero_ctx *ctx, void *grad_avg);
  *               step: bit 0 clear = the zero_bind set is current, set = this
  *               one.  Read it with zero_current_state().
  * All four NULL unbinds.  With a second set bound, zero_step_apply and
- * zero_step_noalloc update whichever set is current, in place. */
+ * zero_step_noalloc update whichever set is current, in place (stages 1 and
+ * 2).  ZERO_ESTATE while a stage-3 step is open. */
 int zero_bind_shadow(zero_ctx *ctx, float *master_b, float *m_b, float *v_b, uint64_t *cur);
 
 /* Synchronizes the stream of the last step and reports which state set holds
@@ -386,8 +388,28 @@ int zero_gather_timeouts(uint32_t *count);
 /* ------------------------------------------------------------- stage 3 */
 
 /* Begin a stage-3 step: the units' calls until the next begin share one
- * step id and one overflow verdict. */
+ * step id and one overflow verdict.  Same as zero3_begin_step_scaled(ctx, 0). */
 int zero3_begin_step(zero_ctx *ctx);
+
+/* Begin a stage-3 step with loss scaling (loss_scale > 0: grads divided by
+ * it, and the step skipped when any unit's grads hold inf/nan).  Two ways to
+ * run it:
+ *   - one state set: zero3_reduce_unit (or _group) for every unit, then one
+ *     zero_step_apply (the fp32 scratch holds the grads until the verdict);
+ *   - a second state set bound (zero_bind_shadow): zero3_step_unit (or
+ *     _group) for every unit, each one pass that reads the current set and
+ *     writes the other, then zero3_end_step, which makes the written set
+ *     current or, when some unit overflowed, keeps the old set and casts
+ *     every unit's params again from it -- the skip without a second pass
+ *     ("PaddlePaddle ZeRO优化", 混合精度才是最佳拍档).
+ * With a second set bound every stage-3 step, scaled or not, runs the second
+ * way and must end with zero3_end_step before the next begins (ZERO_ESTATE
+ * otherwise); zero3_reduce_unit/_group and zero_step_apply are refused. */
+int zero3_begin_step_scaled(zero_ctx *ctx, float loss_scale);
+
+/* End a stage-3 step begun with a second state set bound (the finalize
+ * described above, one small launch); without one it does nothing. */
+int zero3_end_step(zero_ctx *ctx, void *stream);
 
 /* Gather unit `unit`'s N parameter shards (S_u elements of param_dtype
  * each) into unit_full (N*S_u elements), before the unit's forward and again
@@ -396,8 +418,10 @@ int zero3_begin_step(zero_ctx *ctx);
 int zero3_gather_unit(zero_ctx *ctx, int32_t unit, const void *const *shards,
                       int32_t n_shards, void *unit_full, void *stream);
 
-/* Reduce-scatter + average + Adam + cast for unit `unit` in one fused pass,
- * without loss scaling (a skip would need every unit's verdict first).
+/* Reduce-scatter + average + Adam + cast for unit `unit` in one fused pass:
+ * without loss scaling, or loss-scaled into the second state set (see
+ * zero3_begin_step_scaled; with one set a skip would need every unit's
+ * verdict first).
  * grads follow the view: all ranks -> numel_u-element local grads of the
  * unit; one rank -> S_u-element slices.  The cast shard is written to the
  * unit's place in the bound param buffer. */

@@ -699,6 +699,95 @@ def test_group_call_errors():
     run.close()
 
 
+# ------------------------------- stage 3 in one pass over two state sets
+
+@pytest.mark.parametrize("rank,scaled,layout", [(-1, True, "units"), (1, True, "units"),
+                                                (-1, False, "units"), (2, True, "dim0"),
+                                                (-1, True, "groups"), (3, True, "hyper")])
+def test_stage3_one_pass_two_state_sets(rank, scaled, layout):
+    """Loss-scaled ZeRO-3 with a second state set: every unit steps in one
+    pass into the other set and zero3_end_step applies the verdict once --
+    bit-identical to the oracle (which defers Adam), the +inf step skipped by
+    every unit, params recast from the kept set."""
+    kw = dict(steps=4, loss_scale=2.0 ** 9 if scaled else 0.0, inject=(2, 1) if scaled else None)
+    if layout == "dim0":
+        w = W.dim0([(256, 64), (10, 1), (4097, 33), (3, 11)], 4, rank=rank, **kw)
+    elif layout == "groups":
+        w = W.Workload("s3g", 300_000 + 80_000 + 123_456, 8, 3, W.F16, W.F16, rank=rank,
+                       units=[300_000, 80_000, 123_456], groups=[2, 1], **kw)
+    else:
+        units = [100_003, 7, 250_000, 33_333]
+        w = W.Workload("s3s", sum(units), 4, 3, W.F16, W.F16, rank=rank, units=units, **kw)
+    run, ref = run_both(w, shadow=True, hyper=layout == "hyper")
+    if scaled and rank < 0:
+        assert ref.skips == [False, True, False, False]
+    compare_runner(run, ref, what="stage3 one pass")
+    run.close()
+
+
+def test_stage3_one_pass_prefetched_schedule():
+    """The prefetch schedule with two state sets: the same results as the
+    serial one and the oracle, with a skipped step."""
+    from workloads.runner import Runner
+    from workloads.zero3_schedule import Zero3Schedule
+    units = [200_003, 150_000, 99_999, 250_000]
+    w = W.Workload("s3p", sum(units), 4, 3, W.BF16, W.BF16, rank=-1, units=units, steps=4,
+                   loss_scale=2.0 ** 10, inject=(2, 1))
+    runs = {}
+    for mode in ("serial", "overlap"):
+        run = Runner(w, shadow=True)
+        sch = Zero3Schedule(run, 2000, 4000, 64, mode)
+        for it in range(1, 5):
+            run.fill_grads(it)
+            sch.launch_step()
+            run.finish_step()
+        torch.cuda.synchronize()
+        runs[mode] = run
+    ref = refs.OracleRun(w)
+    for it in range(1, 5):
+        ref.step(it)
+    for run in runs.values():
+        assert run.skips == ref.skips == [False, True, False, False]
+        compare_runner(run, ref, what="stage3 one pass prefetch")
+        run.close()
+
+
+def test_stage3_two_state_sets_protocol():
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    units = [1000, 2000]
+    w = W.Workload("s3e", 3000, 4, 3, W.BF16, W.BF16, units=units, steps=1,
+                   loss_scale=2.0 ** 8)
+    run = Runner(w, shadow=True, scratch=True)
+    g = run.grads[0]
+    with pytest.raises(z.ZeroError):                 # not begun
+        z.zero3_step_unit(run.ctx, 0, g, 1e-3, 0.9, 0.999, 1e-8, 1)
+    z.zero3_begin_step_scaled(run.ctx, run.scale)
+    with pytest.raises(z.ZeroError):                 # the previous step is still open
+        z.zero3_begin_step(run.ctx)
+    with pytest.raises(z.ZeroError):                 # the two-pass calls are refused
+        z.zero3_reduce_unit(run.ctx, 0, g, run.scale)
+    with pytest.raises(z.ZeroError):
+        z.zero_step_apply(run.ctx, 1e-3, 0.9, 0.999, 1e-8, 1)
+    with pytest.raises(z.ZeroError):                 # no unbinding mid-step
+        z.zero_bind_shadow(run.ctx, None, None, None, None)
+    z.zero3_step_unit(run.ctx, 0, g, 1e-3, 0.9, 0.999, 1e-8, 1)
+    z.zero3_step_unit(run.ctx, 1, run.grads[1], 1e-3, 0.9, 0.999, 1e-8, 1)
+    z.zero3_end_step(run.ctx)
+    with pytest.raises(z.ZeroError):                 # nothing open any more
+        z.zero3_end_step(run.ctx)
+    torch.cuda.synchronize()
+    assert z.zero_current_state(run.ctx) == 1        # the written set is current
+    run.close()
+    # one state set: a loss-scaled stage-3 step cannot run in one pass
+    run = Runner(w)
+    z.zero3_begin_step_scaled(run.ctx, run.scale)
+    with pytest.raises(z.ZeroError):
+        z.zero3_step_unit(run.ctx, 0, run.grads[0], 1e-3, 0.9, 0.999, 1e-8, 1)
+    z.zero3_end_step(run.ctx)                        # a no-op with one set
+    run.close()
+
+
 # ------------------------------------------------------- save and resume
 
 @pytest.mark.parametrize("kind", ["shadow", "two_pass_rank", "stage3"])

@@ -255,32 +255,44 @@ class Runner:
             z.zero_step(self.ctx, g, *hp, self.scale, st)
             if self.shards is not None:
                 z.zero_allgather(self.ctx, self.shards, self.params, w.param_dtype, st)
-        elif w.groups:
-            z.zero3_begin_step(self.ctx)
-            groups = self.group_ranges()
-            for g, (f, n) in enumerate(groups):          # forward
-                z.zero3_gather_group(self.ctx, f, self.shards[f:f + n], self.group_fulls[g], st)
-            for g in reversed(range(len(groups))):       # backward
-                f, n = groups[g]
-                z.zero3_gather_group(self.ctx, f, self.shards[f:f + n], self.group_fulls[g], st)
-                if self.scale > 0:
-                    z.zero3_reduce_group(self.ctx, f, n, self.group_grads[g], self.scale, st)
-                else:
-                    z.zero3_step_group(self.ctx, f, n, self.group_grads[g], *hp, st)
-            if self.scale > 0:
-                z.zero_step_apply(self.ctx, *hp, st)
         else:
-            z.zero3_begin_step(self.ctx)
-            nunits = len(w.units)
-            for u in range(nunits):                      # forward
-                z.zero3_gather_unit(self.ctx, u, self.shards[u], self.unit_full, st)
-            for u in reversed(range(nunits)):            # backward
-                z.zero3_gather_unit(self.ctx, u, self.shards[u], self.unit_full, st)
-                if self.scale > 0:
-                    z.zero3_reduce_unit(self.ctx, u, self.grads[u], self.scale, st)
-                else:
-                    z.zero3_step_unit(self.ctx, u, self.grads[u], *hp, st)
-            if self.scale > 0:
+            # with two state sets every unit steps in one pass (loss-scaled or
+            # not) and zero3_end_step applies the verdict; with one, a
+            # loss-scaled step reduces every unit, then applies once
+            one_pass = self.shadow is not None or self.scale <= 0
+            z.zero3_begin_step_scaled(self.ctx, self.scale)
+            if w.groups:
+                pieces = self.group_ranges()
+
+                def gather(i):
+                    f, n = pieces[i]
+                    z.zero3_gather_group(self.ctx, f, self.shards[f:f + n], self.group_fulls[i], st)
+
+                def update(i):
+                    f, n = pieces[i]
+                    if one_pass:
+                        z.zero3_step_group(self.ctx, f, n, self.group_grads[i], *hp, st)
+                    else:
+                        z.zero3_reduce_group(self.ctx, f, n, self.group_grads[i], self.scale, st)
+            else:
+                pieces = [(u, 1) for u in range(len(w.units))]
+
+                def gather(i):
+                    z.zero3_gather_unit(self.ctx, i, self.shards[i], self.unit_full, st)
+
+                def update(i):
+                    if one_pass:
+                        z.zero3_step_unit(self.ctx, i, self.grads[i], *hp, st)
+                    else:
+                        z.zero3_reduce_unit(self.ctx, i, self.grads[i], self.scale, st)
+            for i in range(len(pieces)):                 # forward
+                gather(i)
+            for i in reversed(range(len(pieces))):       # backward
+                gather(i)
+                update(i)
+            if self.shadow is not None:
+                z.zero3_end_step(self.ctx, st)
+            elif self.scale > 0:
                 z.zero_step_apply(self.ctx, *hp, st)
         return t
 

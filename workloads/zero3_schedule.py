@@ -53,7 +53,7 @@ class Zero3Schedule:
         standin.busy(self.sink.data_ptr(), self.blocks, self.iters[phase], stream.cuda_stream)
         if phase == "b":
             run, w = self.run, self.run.w
-            if run.scale > 0:
+            if run.scale > 0 and run.shadow is None:
                 z.zero3_reduce_unit(run.ctx, u, run.grads[u], run.scale, stream)
             else:
                 z.zero3_step_unit(run.ctx, u, run.grads[u], w.lr, w.beta1, w.beta2,
@@ -61,7 +61,9 @@ class Zero3Schedule:
 
     def _apply(self, stream):
         run, w = self.run, self.run.w
-        if run.scale > 0:
+        if run.shadow is not None:
+            z.zero3_end_step(run.ctx, stream)
+        elif run.scale > 0:
             z.zero_step_apply(run.ctx, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, stream)
 
     def launch_step(self):
@@ -72,7 +74,7 @@ class Zero3Schedule:
         cs = self.cs if self.mode == "overlap" else run.stream
         if cs is not run.stream:
             cs.wait_stream(run.stream)
-        z.zero3_begin_step(run.ctx)
+        z.zero3_begin_step_scaled(run.ctx, run.scale)
         n = len(self.visits)
         if self.mode != "overlap":
             for v in range(n):

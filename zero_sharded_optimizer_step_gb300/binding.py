@@ -75,6 +75,8 @@ _SIGS = {
     "zero_step_id": (_u64, [_ctxp]),
     "zero_allgather": (ctypes.c_int, [_ctxp, _vpp, _i32, _vp, _i32, _vp]),
     "zero3_begin_step": (ctypes.c_int, [_ctxp]),
+    "zero3_begin_step_scaled": (ctypes.c_int, [_ctxp, _f32]),
+    "zero3_end_step": (ctypes.c_int, [_ctxp, _vp]),
     "zero3_gather_unit": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _vp, _vp]),
     "zero3_step_unit": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f64, _f64, _f64, _f64, _i64,
                                        _vp]),
@@ -337,6 +339,14 @@ def zero_allgather(ctx, shards, full, dtype: int, stream=None) -> None:
 
 def zero3_begin_step(ctx) -> None:
     _check(_L.zero3_begin_step(_h(ctx)))
+
+
+def zero3_begin_step_scaled(ctx, loss_scale: float) -> None:
+    _check(_L.zero3_begin_step_scaled(_h(ctx), loss_scale))
+
+
+def zero3_end_step(ctx, stream=None) -> None:
+    _check(_L.zero3_end_step(_h(ctx), _stream(stream)))
 
 
 def zero3_gather_unit(ctx, unit: int, shards, unit_full, stream=None) -> None:

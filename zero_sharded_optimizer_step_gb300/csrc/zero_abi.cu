@@ -81,6 +81,10 @@ struct zero_ctx {
     bool step_scaled = false;
     bool bucket_open = false;    // between zero_bucket_begin and zero_bucket_end
     float bucket_scale = 0.0f;
+    // stage 3 with two state sets: units step into the other set between
+    // zero3_begin_step(_scaled) and zero3_end_step, which finalizes once
+    bool stage3_open = false;
+    float step_scale = 0.0f;     // the loss scale of the open stage-3 step
     cudaStream_t last_stream = nullptr;
 };
 
@@ -574,12 +578,12 @@ int zero_bind(zero_ctx *c, float *master, float *m, float *v, void *params, floa
 int zero_bind_shadow(zero_ctx *c, float *master_b, float *m_b, float *v_b, uint64_t *cur)
 {
     if (!c) return fail(ZERO_EINVAL, "null context");
+    if (c->stage3_open) return fail(ZERO_ESTATE, "a stage-3 step is open (zero3_end_step)");
     if (!master_b && !m_b && !v_b && !cur) {
         c->xb = c->mb = c->vb = nullptr;
         c->cur = nullptr;
         return ZERO_OK;
     }
-    if (c->stage == 3) return fail(ZERO_EINVAL, "a second state set is for stages 1 and 2");
     if (!cur || (c->state_elems > 0 && (!master_b || !m_b || !v_b)))
         return fail(ZERO_EINVAL, "master_b, m_b, v_b and cur must all be given (or all NULL)");
     if (!aligned(master_b, 4) || !aligned(m_b, 4) || !aligned(v_b, 4))
@@ -697,6 +701,8 @@ int zero_step_apply(zero_ctx *c, double lr, double b1, double b2, double eps, in
     if (rc) return rc;
     if ((rc = check_hyper(t))) return rc;
     if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
+    if (c->stage == 3 && c->cur)
+        return fail(ZERO_ESTATE, "with two state sets, stage-3 steps finish with zero3_end_step");
     if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
     if (c->step_id == 0) return fail(ZERO_ESTATE, "no reduce pass ran before apply");
     return do_apply(c, apply_range(c), lr, b1, b2, eps, t, (cudaStream_t)stream);
@@ -838,17 +844,44 @@ int zero_allgather(zero_ctx *c, const void *const *shards, int32_t n_shards, voi
     return gather(c, shards, n_shards, full, dtype, c->S, (cudaStream_t)stream);
 }
 
-int zero3_begin_step(zero_ctx *c)
+int zero3_begin_step_scaled(zero_ctx *c, float loss_scale)
 {
     if (!c) return fail(ZERO_EINVAL, "null context");
     if (c->stage != 3) return fail(ZERO_EINVAL, "zero3_begin_step is for stage 3");
+    if (c->stage3_open) return fail(ZERO_ESTATE, "the last stage-3 step is open (zero3_end_step)");
+    const bool scaled = loss_scale > 0.0f;
     if (c->hyper) {
         if (c->step_id == 0) return fail(ZERO_ESTATE, "call zero_prepare_step first");
-        return ZERO_OK;      // the prepared step (loss scaling chosen there)
+        if (scaled && !c->step_scaled)
+            return fail(ZERO_EINVAL, "loss scaling differs from the prepared step");
+    } else {
+        c->step_id += 1;
+        c->step_scaled = scaled;
     }
-    c->step_id += 1;
-    c->step_scaled = false;
+    c->step_scale = scaled ? loss_scale : 0.0f;
+    c->stage3_open = c->cur != nullptr;
     return ZERO_OK;
+}
+
+int zero3_begin_step(zero_ctx *c)
+{
+    // with a device scalar block the prepared step fixes the loss scaling;
+    // the kernels take the scale from the block
+    return zero3_begin_step_scaled(c, 0.0f);
+}
+
+int zero3_end_step(zero_ctx *c, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if (c->stage != 3) return fail(ZERO_EINVAL, "zero3_end_step is for stage 3");
+    if (!c->cur) return ZERO_OK;     // one state set: every unit call was complete
+    if (!c->stage3_open) return fail(ZERO_ESTATE, "no stage-3 step is open");
+    c->stage3_open = false;
+    // the written set becomes current, or, when some unit overflowed in a
+    // loss-scaled step, the old set stays and every unit's params are cast
+    // again from it
+    return do_finalize(c, apply_range(c), (cudaStream_t)stream);
 }
 
 static int check_unit(zero_ctx *c, int32_t unit)
@@ -858,6 +891,32 @@ static int check_unit(zero_ctx *c, int32_t unit)
         return fail(ZERO_EINVAL, "unit %d out of range [0, %d)", unit, (int)c->unit_S.size());
     if (c->step_id == 0) return fail(ZERO_ESTATE, "call zero3_begin_step first");
     return ZERO_OK;
+}
+
+static const char *kTwoSetsStage3 =
+    "with two state sets, stage-3 steps run one pass per unit (zero3_step_unit / "
+    "zero3_step_group) and finish with zero3_end_step";
+
+// A stage-3 fused pass may run: a loss-scaled step needs the second state
+// set (one pass into it, the verdict applied by zero3_end_step), and with
+// that set bound the step must have been begun with it.
+static int check_stage3_pass(zero_ctx *c)
+{
+    if (c->cur && !c->stage3_open)
+        return fail(ZERO_ESTATE, "no stage-3 step is open (zero3_begin_step)");
+    if (c->step_scaled && !c->cur)
+        return fail(ZERO_ESTATE, "this step is loss-scaled: bind a second state set "
+                                 "(zero_bind_shadow) or use zero3_reduce_unit + zero_step_apply");
+    return ZERO_OK;
+}
+
+// With two state sets the pass reads the current set and writes the other;
+// zero3_end_step finalizes once for every unit of the step.
+static int stage3_fused(zero_ctx *c, const Range &r, const void *const *grads, double lr,
+                        double b1, double b2, double eps, int64_t t, cudaStream_t s)
+{
+    if (c->cur) return do_fused(c, r, grads, lr, b1, b2, eps, t, s, c->step_scale, false);
+    return do_fused(c, r, grads, lr, b1, b2, eps, t, s);
 }
 
 int zero3_gather_unit(zero_ctx *c, int32_t unit, const void *const *shards, int32_t n_shards,
@@ -878,12 +937,11 @@ int zero3_step_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32_t
     if (rc) return rc;
     if ((rc = check_unit(c, unit))) return rc;
     if ((rc = check_hyper(t))) return rc;
-    if (c->step_scaled)
-        return fail(ZERO_ESTATE, "this step is loss-scaled: use zero3_reduce_unit + zero_step_apply");
+    if ((rc = check_stage3_pass(c))) return rc;
     const Range r = unit_range(c, unit);
     rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
     if (rc) return rc;
-    return do_fused(c, r, grads, lr, b1, b2, eps, t, (cudaStream_t)stream);
+    return stage3_fused(c, r, grads, lr, b1, b2, eps, t, (cudaStream_t)stream);
 }
 
 int zero3_reduce_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32_t n_grads,
@@ -892,6 +950,7 @@ int zero3_reduce_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32
     int rc = check_ready(c);
     if (rc) return rc;
     if ((rc = check_unit(c, unit))) return rc;
+    if (c->cur) return fail(ZERO_ESTATE, kTwoSetsStage3);
     if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
     const Range r = unit_range(c, unit);
     rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
@@ -977,13 +1036,12 @@ int zero3_step_group(zero_ctx *c, int32_t first_unit, int32_t n_units, const voi
     if (rc) return rc;
     if ((rc = check_unit(c, first_unit))) return rc;
     if ((rc = check_hyper(t))) return rc;
-    if (c->step_scaled)
-        return fail(ZERO_ESTATE, "this step is loss-scaled: use zero3_reduce_group + zero_step_apply");
+    if ((rc = check_stage3_pass(c))) return rc;
     Range r;
     if ((rc = group_range(c, first_unit, n_units, &r))) return rc;
     rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n > 0, "grads");
     if (rc) return rc;
-    return do_fused(c, r, grads, lr, b1, b2, eps, t, (cudaStream_t)stream);
+    return stage3_fused(c, r, grads, lr, b1, b2, eps, t, (cudaStream_t)stream);
 }
 
 int zero3_reduce_group(zero_ctx *c, int32_t first_unit, int32_t n_units,
@@ -992,6 +1050,7 @@ int zero3_reduce_group(zero_ctx *c, int32_t first_unit, int32_t n_units,
     int rc = check_ready(c);
     if (rc) return rc;
     if ((rc = check_unit(c, first_unit))) return rc;
+    if (c->cur) return fail(ZERO_ESTATE, kTwoSetsStage3);
     if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
     Range r;
     if ((rc = group_range(c, first_unit, n_units, &r))) return rc;
