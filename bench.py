@@ -75,7 +75,7 @@ def parse():
                     choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny",
                              "gpt2_xl_bucketed", "zero3_prefetch", "zero3_gpt2_small",
                              "gpt2_xl_adamw", "fsdp2_llama7b", "fsdp2_llama7b_per_param",
-                             "gpt2_small_stage1"])
+                             "gpt2_small_stage1", "zero3_llama7b_fp16"])
     ap.add_argument("--graph", action="store_true",
                     help="also capture one step in a CUDA graph and time its replays")
     ap.add_argument("--unit-fwd-ms", type=float, default=0.25,
@@ -233,52 +233,69 @@ def step_plan(run):
             def gat():
                 z.zero_allgather(run.ctx, run.shards, run.params, w.param_dtype, st)
             plan.append(Launch("gather_kernel", 2 * bp * w.shard * n_sh, gat))
-    elif w.groups:
-        # one launch per group of units (a layer's parameters) for each
-        # gather and for the step
-        groups = run.group_ranges()
+    else:
+        # ZeRO-3: per unit (or per group of units: a layer's parameters, one
+        # launch each) a gather before forward, a gather before backward and
+        # the unit's update; loss-scaled with two state sets, one pass per
+        # unit and zero3_end_step; loss-scaled with one, a reduce per unit and
+        # one apply over all units
+        shadow = run.shadow is not None
+        one_pass = shadow or run.scale <= 0
+        if w.groups:
+            pieces = run.group_ranges()
+            gname = "gather_rows_kernel"
+        else:
+            pieces = [(u, 1) for u in range(len(w.units))]
+            gname = "gather_kernel"
 
         def first():
-            z.zero3_begin_step(run.ctx)
+            z.zero3_begin_step_scaled(run.ctx, run.scale)
 
-        def gather(g, f, n):
-            sh = run.shards[f:f + n]
-            return lambda: z.zero3_gather_group(run.ctx, f, sh, run.group_fulls[g], st)
-        for g, (f, n) in enumerate(groups):
-            S = sum(w.unit_shard(u) for u in range(f, f + n))
-            plan.append(Launch("gather_rows_kernel", 2 * bp * S * w.world, gather(g, f, n)))
-        for g in reversed(range(len(groups))):
-            f, n = groups[g]
+        def gather(i):
+            f, n = pieces[i]
+            if w.groups:
+                sh = run.shards[f:f + n]
+                return lambda: z.zero3_gather_group(run.ctx, f, sh, run.group_fulls[i], st)
+            return lambda: z.zero3_gather_unit(run.ctx, f, run.shards[f], run.unit_full, st)
+
+        def update(i):
+            f, n = pieces[i]
+            if w.groups:
+                if one_pass:
+                    return lambda: z.zero3_step_group(run.ctx, f, n, run.group_grads[i], w.lr,
+                                                      w.beta1, w.beta2, w.eps, run.t + 1, st)
+                return lambda: z.zero3_reduce_group(run.ctx, f, n, run.group_grads[i],
+                                                    run.scale, st)
+            if one_pass:
+                return lambda: z.zero3_step_unit(run.ctx, f, run.grads[f], w.lr, w.beta1,
+                                                 w.beta2, w.eps, run.t + 1, st)
+            return lambda: z.zero3_reduce_unit(run.ctx, f, run.grads[f], run.scale, st)
+
+        def sizes(i):
+            f, n = pieces[i]
             S = sum(w.unit_shard(u) for u in range(f, f + n))
             nv = sum(min(w.unit_shard(u), max(0, w.units[u] - w.rank * w.unit_shard(u)))
                      for u in range(f, f + n))
-            plan.append(Launch("gather_rows_kernel", 2 * bp * S * w.world, gather(g, f, n)))
-            plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * S,
-                               (lambda g=g, f=f, n=n: z.zero3_step_group(
-                                   run.ctx, f, n, run.group_grads[g], w.lr, w.beta1, w.beta2,
-                                   w.eps, run.t + 1, st))))
-        plan[0] = Launch(plan[0].name, plan[0].alg_bytes,
-                         (lambda f=plan[0].fn: (first(), f())))
-    else:
-        nunits = len(w.units)
-
-        def first():
-            z.zero3_begin_step(run.ctx)
-        for u in range(nunits):
-            Su = w.unit_shard(u)
-            plan.append(Launch("gather_kernel", 2 * bp * Su * w.world,
-                               (lambda u=u: z.zero3_gather_unit(run.ctx, u, run.shards[u],
-                                                                run.unit_full, st))))
-        for u in reversed(range(nunits)):
-            Su = w.unit_shard(u)
-            nv = min(Su, max(0, w.units[u] - w.rank * Su))
-            plan.append(Launch("gather_kernel", 2 * bp * Su * w.world,
-                               (lambda u=u: z.zero3_gather_unit(run.ctx, u, run.shards[u],
-                                                                run.unit_full, st))))
-            plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * Su,
-                               (lambda u=u: z.zero3_step_unit(run.ctx, u, run.grads[u], w.lr,
-                                                              w.beta1, w.beta2, w.eps,
-                                                              run.t + 1, st))))
+            return S, nv
+        for i in range(len(pieces)):
+            S, _ = sizes(i)
+            plan.append(Launch(gname, 2 * bp * S * w.world, gather(i)))
+        total_S = 0
+        for i in reversed(range(len(pieces))):
+            S, nv = sizes(i)
+            total_S += S
+            plan.append(Launch(gname, 2 * bp * S * w.world, gather(i)))
+            if one_pass:
+                plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * S,
+                                   update(i)))
+            else:
+                plan.append(Launch("reduce_kernel", w.world * bg * nv + 4 * S, update(i)))
+        if shadow:
+            plan.append(Launch("finalize_kernel", 0, lambda: z.zero3_end_step(run.ctx, st)))
+        elif run.scale > 0:
+            plan.append(Launch("apply_kernel", (4 + 24 + bp) * total_S,
+                               lambda: z.zero_step_apply(run.ctx, w.lr, w.beta1, w.beta2,
+                                                         w.eps, run.t + 1, st)))
         plan[0] = Launch(plan[0].name, plan[0].alg_bytes,
                          (lambda f=plan[0].fn: (first(), f())))
     return plan
@@ -307,13 +324,14 @@ def bench_ours(args, rank, world_size, device_index):
 
     w = W.ALL[args.workload](**({"n_units": args.units} if args.units and
                                 args.workload in ("zero3_llama7b", "fsdp2_llama7b",
-                                                  "fsdp2_llama7b_per_param") else {}))
+                                                  "fsdp2_llama7b_per_param",
+                                                  "zero3_llama7b_fp16") else {}))
     if args.numel:
         w = w.replace(numel=args.numel, name=w.name + "_numel%d" % args.numel)
     if w.inject:
         w = w.replace(inject=None)    # timed steps are the ones that apply
     torch.cuda.set_device(device_index)
-    shadow = w.loss_scale > 0 and w.stage < 3 and not args.two_pass
+    shadow = w.loss_scale > 0 and not args.two_pass
     run = Runner(w, device="cuda:%d" % device_index, shadow=shadow, alloc_grads=not w.bucket)
     if w.bucket:
         import synth
@@ -829,16 +847,22 @@ def bench_e2e_units(run, args, world_size):
         else:
             z.zero3_gather_unit(run.ctx, f, run.shards[f], run.unit_full, st)
 
+    one_pass = run.shadow is not None or run.scale <= 0
+
     def step(i, views):
         f, n = pieces[i]
-        if w.groups:
+        if w.groups and one_pass:
             z.zero3_step_group(run.ctx, f, n, views, w.lr, w.beta1, w.beta2, w.eps, run.t + 1,
                                st)
-        else:
+        elif w.groups:
+            z.zero3_reduce_group(run.ctx, f, n, views, run.scale, st)
+        elif one_pass:
             z.zero3_step_unit(run.ctx, f, views, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st)
+        else:
+            z.zero3_reduce_unit(run.ctx, f, views, run.scale, st)
 
     def one():
-        z.zero3_begin_step(run.ctx)
+        z.zero3_begin_step_scaled(run.ctx, run.scale)
         for i in range(len(pieces)):                         # forward gathers
             gather(i)
         for j, i in enumerate(reversed(range(len(pieces)))):  # backward
@@ -854,8 +878,16 @@ def bench_e2e_units(run, args, world_size):
             st.wait_event(ready[k2])
             step(i, views)
             done[k2].record(st)
-        z.zero_step_status(run.ctx)                          # 8-byte read of the verdict
-        run.t += 1
+        if run.shadow is not None:
+            z.zero3_end_step(run.ctx, st)
+        elif run.scale > 0:
+            z.zero_step_apply(run.ctx, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st)
+        _, skipped = z.zero_step_status(run.ctx)             # 8-byte read of the verdict
+        if run.scale > 0:
+            run.scale, run.good = z.zero_scale_update(run.scale, skipped, run.good,
+                                                      w.growth_interval)
+        if not skipped:
+            run.t += 1
 
     one()
     torch.cuda.synchronize()

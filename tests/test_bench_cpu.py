@@ -133,6 +133,9 @@ def test_algorithmic_bytes_match_the_closed_forms():
     z3 = W.zero3_llama7b()
     Su = z3.unit_shard(0)
     assert _plan_bytes(z3) == 32 * (2 * 2 * 2 * 8 + 8 * 2 + 26) * Su == 85_810_544_640
+    f16 = W.zero3_llama7b_fp16()
+    assert _plan_bytes(f16, shadow=True) == 32 * (2 * 2 * 2 * 8 + 8 * 2 + 26) * Su
+    assert _plan_bytes(f16) == 32 * (2 * 2 * 2 * 8 + (8 * 2 + 4) + (4 + 24 + 2)) * Su
     fs = W.fsdp2_llama7b()
     assert sum(fs.unit_shard(u) for u in range(len(fs.units))) == 32 * Su
     assert _plan_bytes(fs) == _plan_bytes(W.fsdp2_llama7b_per_param()) == 85_810_544_640

@@ -124,6 +124,13 @@ def zero3_llama7b(n_units: int = 32) -> Workload:
                     units=[llama_layer_numel()] * n_units, steps=2)
 
 
+def zero3_llama7b_fp16(n_units: int = 32) -> Workload:
+    """The ZeRO-3 Llama-7B-shaped workload in fp16 with loss scaling (2^16):
+    every unit's verdict decides the whole step."""
+    return zero3_llama7b(n_units).replace(name="zero3_llama7b_fp16", grad_dtype=F16,
+                                          param_dtype=F16, loss_scale=2.0 ** 16)
+
+
 def gpt2_xl_bucketed() -> Workload:
     """GPT-2 XL stepped in 32 Mi-element buckets from constant-size gradient
     buffers (16 ranks x 64 MiB), the way ZeRO-2 reduce-scatters during backward."""
@@ -182,6 +189,7 @@ ALL = {"tiny": tiny, "zero3_gpt2_small": zero3_gpt2_small, "gpt2_xl_bucketed": g
        "gpt2_small": gpt2_small, "gpt2_small_stage1": gpt2_small_stage1,
        "gpt2_xl": gpt2_xl, "gpt2_xl_adamw": gpt2_xl_adamw,
        "one_rank_7p5b": one_rank_7p5b, "zero3_llama7b": zero3_llama7b,
+       "zero3_llama7b_fp16": zero3_llama7b_fp16,
        "fsdp2_llama7b": fsdp2_llama7b, "fsdp2_llama7b_per_param": fsdp2_llama7b_per_param}
 
 
