@@ -3,8 +3,11 @@ processes): each process is one data-parallel rank in the one-rank view --
 reduce-scatter in rank order, the overflow verdict combined across ranks with
 a MAX all-reduce between the reduce and the apply (as the one-rank ABI
 documents), Adam on the own shard, all-gather of the cast shards -- and the
-result must be bit-identical to the all-ranks step.  Also covers the
-benchmark's cross-rank timing helpers (barrier, max over ranks)."""
+result must be bit-identical to the all-ranks step.  The same for ZeRO-3:
+per unit an all-gather before forward and backward, the unit's
+reduce-scatter, and every unit's verdict combined before any unit's Adam
+counts.  Also covers the benchmark's cross-rank timing helpers (barrier,
+max over ranks)."""
 import os
 import socket
 
@@ -128,3 +131,146 @@ def test_one_rank_views_with_real_collectives(tmp_path, world, numel, inject_at)
         assert d["m"].tobytes() == m[sl].tobytes()
         assert d["v"].tobytes() == v[sl].tobytes()
         assert d["full"].tobytes() == full.tobytes()
+
+
+# ------------------------------------------------------------------ stage 3
+
+def _rank_main3(rank, world, port, units, inject_at, out_dir):
+    """One rank of a ZeRO-3 step over gloo: per unit an all-gather of the
+    cast shards before forward and again before backward, the unit's grads
+    reduce-scattered in rank order after its backward; with loss scaling
+    every unit's verdict is combined (MAX) before any unit's Adam counts."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import oracle
+    import synth
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+
+    def all_gather16(lp):
+        parts = [torch.zeros(lp.size, dtype=torch.int32) for _ in range(world)]
+        dist.all_gather(parts, torch.from_numpy(lp.astype(np.int32)))
+        return np.concatenate([p.numpy().astype(np.uint16) for p in parts])
+
+    state, lps, Ss = [], [], []
+    for u, nu in enumerate(units):
+        S = oracle.shard_size(nu, world)
+        nv = max(0, min(S, nu - rank * S))
+        x = np.zeros(S, np.float32)
+        x[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER, 0, 0, u), 0.01,
+                                 index0=rank * S)
+        state.append([x, np.zeros(S, np.float32), np.zeros(S, np.float32)])
+        lps.append(oracle.cast(x, oracle.F16))
+        Ss.append(S)
+    scale, good, t, skips, gathered = 2.0 ** 12, 0, 0, [], {}
+    for it in (1, 2, 3):
+        for u in range(len(units)):                       # forward
+            gathered[u] = all_gather16(lps[u])
+        slices_of, bad_total = {}, 0
+        for u in reversed(range(len(units))):             # backward
+            gathered[u] = all_gather16(lps[u])
+            nu, S = units[u], Ss[u]
+            g = synth.fill_host(nu, synth.F16, synth.key(0, synth.KIND_GRAD, it, rank, u),
+                                1e-3 * scale)
+            if inject_at and (it, rank, u) == inject_at[:3]:
+                g[inject_at[3]] = 0x7C00                  # +inf in fp16
+            padded = np.zeros(S * world, np.uint16)
+            padded[:nu] = g
+            pieces = [torch.zeros(S, dtype=torch.int32) for _ in range(world)]
+            for r in range(world):
+                send = torch.from_numpy(padded[r * S:(r + 1) * S].astype(np.int32))
+                dist.gather(send, pieces if r == rank else None, dst=r)
+            slices = [p.numpy().astype(np.uint16) for p in pieces]
+            nv = max(0, min(S, nu - rank * S))
+            _, bad = oracle.average(oracle.rank_sum(slices, oracle.F16, S, nv), world, scale)
+            bad_total += bad
+            slices_of[u] = slices
+        flag = torch.tensor([bad_total], dtype=torch.int64)
+        dist.all_reduce(flag, op=dist.ReduceOp.MAX)
+        others = int(flag.item())
+        skipped = False
+        for u in range(len(units)):                       # Adam, now that the verdict is in
+            x, m, v = state[u]
+            lp = lps[u].copy()
+            sk, _ = oracle.zero_rank_step(slices_of[u], oracle.F16, units[u], rank, x, m, v, lp,
+                                          oracle.F16, 1e-3, 0.9, 0.999, 1e-8, t + 1,
+                                          loss_scale=scale, others_nonfinite=others)
+            skipped = skipped or sk
+            lps[u] = lp
+        skips.append(skipped)
+        if not skipped:
+            t += 1
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    out = {"skips": np.array(skips)}
+    for u in range(len(units)):
+        out["x%d" % u], out["m%d" % u], out["v%d" % u] = state[u]
+        out["lp%d" % u] = lps[u]
+        out["full%d" % u] = gathered[u]
+    np.savez(os.path.join(out_dir, "rank%d.npz" % rank), **out)
+    dist.destroy_process_group()
+
+
+def _stage3_reference(units, world, inject_at):
+    """All ranks in one process: per unit the oracle's all-ranks step on the
+    unit's own flat vector; a step counts only if no unit overflowed."""
+    import oracle
+    import synth
+    st, fulls = [], []
+    for u, nu in enumerate(units):
+        P = oracle.shard_size(nu, world) * world
+        x = np.zeros(P, np.float32)
+        x[:nu] = synth.fill_host(nu, synth.F32, synth.key(0, synth.KIND_MASTER, 0, 0, u), 0.01)
+        st.append([x, np.zeros(P, np.float32), np.zeros(P, np.float32)])
+        fulls.append(oracle.cast(x, oracle.F16))
+    scale, good, t, skips = 2.0 ** 12, 0, 0, []
+    for it in (1, 2, 3):
+        new, skipped = [], False
+        for u, nu in enumerate(units):
+            grads = [synth.fill_host(nu, synth.F16, synth.key(0, synth.KIND_GRAD, it, k, u),
+                                     1e-3 * scale) for k in range(world)]
+            if inject_at and (it, u) == (inject_at[0], inject_at[2]):
+                grads[inject_at[1]][inject_at[3]] = 0x7C00
+            x, m, v = (a.copy() for a in st[u])
+            full = fulls[u].copy()
+            sk, _ = oracle.zero_step(grads, oracle.F16, nu, x, m, v, full, oracle.F16, 1e-3, 0.9,
+                                     0.999, 1e-8, t + 1, loss_scale=scale)
+            skipped = skipped or sk
+            new.append(([x, m, v], full))
+        if not skipped:
+            st = [n[0] for n in new]
+            fulls = [n[1] for n in new]
+            t += 1
+        skips.append(skipped)
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    return st, fulls, skips
+
+
+@pytest.mark.parametrize("world,units,inject_at", [
+    (2, [3001, 17, 5000], None),
+    (2, [3001, 17, 5000], (2, 1, 0, 1400)),      # (iteration, rank, unit, element)
+    (4, [3001, 17, 5000], (2, 3, 2, 11)),       # rank 3's element in rank 0's shard of unit 2
+])
+def test_stage3_ranks_with_real_collectives(tmp_path, world, units, inject_at):
+    port = _free_port()
+    mp.start_processes(_rank_main3, args=(world, port, units, inject_at, str(tmp_path)),
+                       nprocs=world, join=True, start_method="spawn")
+    import oracle
+    st, fulls, skips = _stage3_reference(units, world, inject_at)
+    assert skips == [bool(inject_at) and it == 2 for it in (1, 2, 3)]
+    for r in range(world):
+        d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
+        assert list(d["skips"]) == skips, r
+        for u, nu in enumerate(units):
+            S = oracle.shard_size(nu, world)
+            sl = slice(r * S, (r + 1) * S)
+            for name, a in zip("xmv", st[u]):
+                assert d["%s%d" % (name, u)].tobytes() == a[sl].tobytes(), (r, u, name)
+            assert d["lp%d" % u].tobytes() == fulls[u][sl].tobytes()
+            # the last gather (before unit u's backward) placed the shards
+            # every rank held then, which the third step has since updated
+        # every rank saw the same gathered units
+        if r == 0:
+            first = {u: d["full%d" % u].copy() for u in range(len(units))}
+        else:
+            for u in range(len(units)):
+                assert d["full%d" % u].tobytes() == first[u].tobytes()
