@@ -447,8 +447,10 @@ int zero3_reduce_unit(zero_ctx *ctx, int32_t unit, const void *const *grads,
  *               (S_u elements) of unit first_unit + ul; NULL skips it.
  *   unit_fulls  n_units destinations of N*S_u elements each (as
  *               zero3_gather_unit's unit_full).
- * At most 512 shards per call (n_units * N); any element alignment.  Always
- * the SM placement (the lean mode applies to zero3_gather_unit). */
+ * At most 512 shards per call (n_units * N); any element alignment.  In the
+ * lean mode (zero_set_gather_mode) a group whose shards and destinations are
+ * all 16-byte aligned with lengths that are multiples of 16 bytes runs on the
+ * bulk-copy engine; any other group takes the SM placement. */
 int zero3_gather_group(zero_ctx *ctx, int32_t first_unit, int32_t n_units,
                        const void *const *shards, int32_t n_shards, void *const *unit_fulls,
                        void *stream);

@@ -653,6 +653,39 @@ def test_group_gather_equals_unit_gathers(rank):
     run.close()
 
 
+@pytest.mark.parametrize("shapes", [[(256, 64), (64, 8), (512, 16), (1024, 1)],   # bulk-copy form
+                                    [(256, 64), (10, 1), (4097, 33)]])           # falls back
+def test_group_gather_lean_mode(shapes):
+    """With the lean (bulk-copy) gather mode a group gather whose rows are all
+    16-byte aligned multiples of 16 bytes runs on the bulk-copy engine, any
+    other on the SM kernel; either way the same bytes, and no wait runs out."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner, TORCH_DTYPE
+    w = W.dim0(shapes, 4, rank=0, steps=1)
+    run = Runner(w)
+    before = z.zero_gather_timeouts()
+    z.zero3_begin_step(run.ctx)
+    dt = TORCH_DTYPE[w.param_dtype]
+    n = len(shapes)
+    outs = {}
+    for mode in (z.ZERO_GATHER_FAST, z.ZERO_GATHER_LEAN):
+        z.zero_set_gather_mode(run.ctx, mode)
+        fulls = [torch.zeros(w.unit_shard(u) * w.world, dtype=dt, device="cuda:0")
+                 for u in range(n)]
+        z.zero3_gather_group(run.ctx, 0, run.shards[:n], fulls)
+        torch.cuda.synchronize()
+        outs[mode] = [to_np(f) for f in fulls]
+    for a, b in zip(outs[z.ZERO_GATHER_FAST], outs[z.ZERO_GATHER_LEAN]):
+        assert a.tobytes() == b.tobytes()
+    for u in range(n):                       # the shards themselves, in rank order
+        S = w.unit_shard(u)
+        for k in range(w.world):
+            assert outs[z.ZERO_GATHER_LEAN][u][k * S:(k + 1) * S].tobytes() == \
+                to_np(run.shards[u][k]).tobytes()
+    assert z.zero_gather_timeouts() == before
+    run.close()
+
+
 @pytest.mark.parametrize("rank,scaled", [(-1, False), (1, False), (-1, True), (2, True)])
 def test_group_step_parity(rank, scaled):
     """Runs of units gathered and stepped (or reduced, then one apply) in one

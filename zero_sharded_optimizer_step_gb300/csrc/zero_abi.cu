@@ -1024,7 +1024,9 @@ int zero3_gather_group(zero_ctx *c, int32_t first_unit, int32_t n_units,
     a.n = n_units * c->world;
     // like every gather, this one leaves the flag word alone and does not
     // become the stream zero_step_status waits on
-    const cudaError_t e = zgb::launch_gather_rows(a, c->sms, (cudaStream_t)stream);
+    const cudaError_t e = (c->gather_mode == ZERO_GATHER_LEAN && zgb::lean_gather_rows_eligible(a))
+                              ? zgb::launch_gather_rows_lean(a, c->sms, (cudaStream_t)stream)
+                              : zgb::launch_gather_rows(a, c->sms, (cudaStream_t)stream);
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "group gather kernel");
 }
 

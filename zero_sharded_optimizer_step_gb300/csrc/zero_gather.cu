@@ -185,11 +185,11 @@ __device__ __forceinline__ void tma_store(char *dst, uint32_t src_smem, uint32_t
 }
 
 struct LeanArgs {
-    const char *src[kMaxRanks];   // active rows only
-    char *dst[kMaxRanks];
+    const char *src[kMaxRows];    // active rows only
+    char *dst[kMaxRows];
+    int64_t bytes[kMaxRows];      // multiple of 16
+    int64_t first_tile[kMaxRows + 1];   // row r owns tiles [first_tile[r], first_tile[r+1])
     int32_t rows;
-    int64_t row_bytes;            // multiple of 16
-    int64_t tiles_per_row;
 };
 
 __global__ void __launch_bounds__(32)
@@ -204,17 +204,22 @@ lean_gather_kernel(const __grid_constant__ LeanArgs a)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 
-    const int64_t total = (int64_t)a.rows * a.tiles_per_row;
+    const int64_t total = a.first_tile[a.rows];
     const int64_t G = gridDim.x;
     auto tile_of = [&](int64_t m, const char *&src, char *&dst, uint32_t &bytes) -> bool {
         const int64_t t = blockIdx.x + m * G;
         if (t >= total) return false;
-        const int64_t r = t / a.tiles_per_row, j = t - r * a.tiles_per_row;
-        const int64_t off = j * kTmaTile;
-        const int64_t left = a.row_bytes - off;
+        // the row holding tile t: the last r with first_tile[r] <= t
+        int lo = 0, hi = a.rows - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.first_tile[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        const int64_t off = (t - a.first_tile[lo]) * kTmaTile;
+        const int64_t left = a.bytes[lo] - off;
         bytes = (uint32_t)(left < kTmaTile ? left : kTmaTile);
-        src = a.src[r] + off;
-        dst = a.dst[r] + off;
+        src = a.src[lo] + off;
+        dst = a.dst[lo] + off;
         return true;
     };
 
@@ -314,21 +319,33 @@ bool lean_gather_eligible(const GatherArgs &a)
     return true;
 }
 
-cudaError_t launch_gather_lean(const GatherArgs &a, int sms, cudaStream_t s)
+namespace {
+
+// Rows in the lean form: every active row 16-byte aligned at both ends with a
+// length that is a multiple of 16 bytes.  Returns false when some row is not.
+bool lean_rows(const void *const *src, char *const *dst, const int64_t *bytes, int32_t n,
+               LeanArgs &l)
 {
-    if (a.n <= 0 || a.shard_bytes <= 0) return cudaSuccess;
-    if (!lean_gather_eligible(a)) return cudaErrorInvalidValue;
-    LeanArgs l;
     memset(&l, 0, sizeof l);
-    for (int32_t k = 0; k < a.n; ++k) {
-        if (!a.src[k]) continue;
-        l.src[l.rows] = static_cast<const char *>(a.src[k]);
-        l.dst[l.rows] = a.dst + (int64_t)k * a.shard_bytes;
+    int64_t tiles = 0;
+    for (int32_t y = 0; y < n; ++y) {
+        if (!src[y] || bytes[y] <= 0) continue;
+        if (bytes[y] % 16 || ((uintptr_t)src[y] & 15) || ((uintptr_t)dst[y] & 15)) return false;
+        l.src[l.rows] = static_cast<const char *>(src[y]);
+        l.dst[l.rows] = dst[y];
+        l.bytes[l.rows] = bytes[y];
+        l.first_tile[l.rows] = tiles;
+        tiles += (bytes[y] + kTmaTile - 1) / kTmaTile;
         ++l.rows;
     }
-    if (l.rows == 0) return cudaSuccess;
-    l.row_bytes = a.shard_bytes;
-    l.tiles_per_row = (a.shard_bytes + kTmaTile - 1) / kTmaTile;
+    l.first_tile[l.rows] = tiles;
+    return true;
+}
+
+cudaError_t launch_lean(const LeanArgs &l, int sms, cudaStream_t s)
+{
+    const int64_t total = l.first_tile[l.rows];
+    if (l.rows == 0 || total == 0) return cudaSuccess;
     const int smem = kTmaStages * kTmaTile;
     static int attr_device = -1;   // the attribute is per device
     int dev = 0;
@@ -339,10 +356,42 @@ cudaError_t launch_gather_lean(const GatherArgs &a, int sms, cudaStream_t s)
         if (e != cudaSuccess) return e;
         attr_device = dev;
     }
-    const int64_t total = (int64_t)l.rows * l.tiles_per_row;
     const int blocks = (int)(total < sms ? total : sms);
     lean_gather_kernel<<<blocks, 32, smem, s>>>(l);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gather_lean(const GatherArgs &a, int sms, cudaStream_t s)
+{
+    if (a.n <= 0 || a.shard_bytes <= 0) return cudaSuccess;
+    const void *src[kMaxRanks];
+    char *dst[kMaxRanks];
+    int64_t bytes[kMaxRanks];
+    for (int32_t k = 0; k < a.n; ++k) {
+        src[k] = a.src[k];
+        dst[k] = a.dst + (int64_t)k * a.shard_bytes;
+        bytes[k] = a.shard_bytes;
+    }
+    LeanArgs l;
+    if (!lean_rows(src, dst, bytes, a.n, l)) return cudaErrorInvalidValue;
+    return launch_lean(l, sms, s);
+}
+
+bool lean_gather_rows_eligible(const GatherRowsArgs &a)
+{
+    LeanArgs l;
+    return a.n <= kMaxRows && lean_rows(a.src, a.dst, a.bytes, a.n, l);
+}
+
+cudaError_t launch_gather_rows_lean(const GatherRowsArgs &a, int sms, cudaStream_t s)
+{
+    if (a.n <= 0) return cudaSuccess;
+    if (a.n > kMaxRows) return cudaErrorInvalidValue;
+    LeanArgs l;
+    if (!lean_rows(a.src, a.dst, a.bytes, a.n, l)) return cudaErrorInvalidValue;
+    return launch_lean(l, sms, s);
 }
 
 cudaError_t lean_gather_timeouts(unsigned int *count)

@@ -144,6 +144,10 @@ cudaError_t launch_gather_rows(const GatherRowsArgs &a, int sms, cudaStream_t s)
 // shards are not eligible (lean_gather_eligible).
 bool lean_gather_eligible(const GatherArgs &a);
 cudaError_t launch_gather_lean(const GatherArgs &a, int sms, cudaStream_t s);
+// The same for rows of any lengths (a group gather): every row 16-byte
+// aligned at both ends, lengths multiples of 16 bytes.
+bool lean_gather_rows_eligible(const GatherRowsArgs &a);
+cudaError_t launch_gather_rows_lean(const GatherRowsArgs &a, int sms, cudaStream_t s);
 // Waits of the lean gather that ran out (cumulative, this process).
 cudaError_t lean_gather_timeouts(unsigned int *count);
 
