@@ -49,12 +49,12 @@ import numpy as np  # noqa: E402
 # kernel source it was taken on (sha256 prefix); otherwise bench reports null.
 TRAFFIC = {
     ("gpt2_xl", "fused_step_kernel"): ("a5b9a674470ff3d3", 68.537e9 + 21.777e9),
-    ("one_rank_7p5b", "gather_kernel"): ("91d51734053b3f9b", 14.786e9 + 14.721e9),
+    ("one_rank_7p5b", "gather_kernel"): ("8285f3d7f2dee1cb", 14.787e9 + 14.724e9),
     ("one_rank_7p5b", "fused_step_kernel"): ("a5b9a674470ff3d3", 16.407e9 + 1.621e9),
     # means of two full-size launches; part of each launch's writes is still
     # in L2 when it ends
-    ("zero3_llama7b", "gather_kernel"): ("91d51734053b3f9b", 404.81e6 + 352.84e6),
-    ("fsdp2_llama7b", "gather_rows_kernel"): ("91d51734053b3f9b", 404.79e6 + 348.01e6),
+    ("zero3_llama7b", "gather_kernel"): ("8285f3d7f2dee1cb", 404.79e6 + 351.73e6),
+    ("fsdp2_llama7b", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.79e6 + 347.49e6),
 }
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
                           "zero_step_kernels.cu")
