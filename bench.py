@@ -53,7 +53,9 @@ TRAFFIC = {
     ("one_rank_7p5b", "fused_step_kernel"): ("a5b9a674470ff3d3", 16.407e9 + 1.621e9),
     # means of two full-size launches; part of each launch's writes is still
     # in L2 when it ends
-    ("zero3_llama7b", "gather_kernel"): ("8285f3d7f2dee1cb", 404.79e6 + 351.73e6),
+    ("zero3_llama7b", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.83e6 + 350.27e6),
+    # the same gathers (2-byte params, the same shard sizes)
+    ("zero3_llama7b_fp16", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.83e6 + 350.27e6),
     ("fsdp2_llama7b", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.79e6 + 347.49e6),
 }
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
@@ -243,10 +245,16 @@ def step_plan(run):
         one_pass = shadow or run.scale <= 0
         if w.groups:
             pieces = run.group_ranges()
-            gname = "gather_rows_kernel"
         else:
             pieces = [(u, 1) for u in range(len(w.units))]
-            gname = "gather_kernel"
+
+        def gname(i):
+            # the library places a group, or a unit with shards of 32 MiB or
+            # more, with gather_rows_kernel; smaller units with gather_kernel
+            f, n = pieces[i]
+            if w.groups or w.unit_shard(f) * bp >= (32 << 20):
+                return "gather_rows_kernel"
+            return "gather_kernel"
 
         def first():
             z.zero3_begin_step_scaled(run.ctx, run.scale)
@@ -279,12 +287,12 @@ def step_plan(run):
             return S, nv
         for i in range(len(pieces)):
             S, _ = sizes(i)
-            plan.append(Launch(gname, 2 * bp * S * w.world, gather(i)))
+            plan.append(Launch(gname(i), 2 * bp * S * w.world, gather(i)))
         total_S = 0
         for i in reversed(range(len(pieces))):
             S, nv = sizes(i)
             total_S += S
-            plan.append(Launch(gname, 2 * bp * S * w.world, gather(i)))
+            plan.append(Launch(gname(i), 2 * bp * S * w.world, gather(i)))
             if one_pass:
                 plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * S,
                                    update(i)))
@@ -464,12 +472,7 @@ def bench_ours(args, rank, world_size, device_index):
     if not args.no_e2e and not w.bucket:
         e2e = (bench_e2e_pipelined(run, args, world_size) if w.stage < 3 else
                bench_e2e_units(run, args, world_size) if w.rank >= 0 else None)
-        e2e = e2e or bench_e2e(run, plan, args, world_size)
-        # the host link on this machine, for reading e2e against it
-        link = h2d_link_gbs(run.dev)
-        e2e["h2d_link_gbs"] = link
-        e2e["link_bound_ms_per_step"] = e2e["h2d_bytes_per_step"] / (link * 1e9) * 1e3
-        result["e2e"] = e2e
+        result["e2e"] = e2e or bench_e2e(run, plan, args, world_size)
     if not args.no_cpu_baseline and rank == 0:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
     run.close()
@@ -702,26 +705,6 @@ def bench_e2e(run, plan, args, world_size):
             "device_buffers": len(dev_bufs)}
 
 
-def h2d_link_gbs(dev, nbytes=2 << 30, reps=3):
-    """Host-to-device bandwidth of one large copy from pinned memory (GB/s),
-    timed with CUDA events on a stream of its own."""
-    import torch
-    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    s = torch.cuda.Stream(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        d.copy_(h, non_blocking=True)
-        e0.record(s)
-        for _ in range(reps):
-            d.copy_(h, non_blocking=True)
-        e1.record(s)
-    s.synchronize()
-    gbs = reps * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
-    del h, d
-    return gbs
-
-
 def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
     """The end-to-end step through the bucketed API: while bucket b is
     stepped on the compute stream, bucket b+1's grads of every rank are
@@ -756,7 +739,9 @@ def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
     n_valid = srcs[0].numel()
     ranges = [(off, min(bucket, n_range - off)) for off in range(0, n_range, bucket)]
 
-    def one():
+    pairs = []        # event pairs around each bucket's copies (timed steps)
+
+    def one(record=False):
         z.zero_bucket_begin(run.ctx, run.scale)
         for b, (off, cnt) in enumerate(ranges):
             k2 = b % 2
@@ -764,9 +749,15 @@ def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
             with torch.cuda.stream(cp):
                 if b >= 2:
                     cp.wait_event(done[k2])    # the step of bucket b-2 is done with this set
+                if record:
+                    pairs.append((torch.cuda.Event(enable_timing=True),
+                                  torch.cuda.Event(enable_timing=True)))
+                    pairs[-1][0].record(cp)
                 for d, h in zip(dev[k2], host):
                     if nv:
                         d[:nv].copy_(h[off:off + nv], non_blocking=True)
+                if record:
+                    pairs[-1][1].record(cp)
                 ready[k2].record(cp)
             st.wait_event(ready[k2])
             z.zero_bucket_step(run.ctx, off, cnt, [d[:max(nv, 1)] for d in dev[k2]], w.lr,
@@ -788,11 +779,15 @@ def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
     steps = max(2, args.e2e_steps)
     t0 = time.perf_counter()
     for _ in range(steps):
-        one()
+        one(record=True)
     torch.cuda.synchronize()
     dt = allreduce_max(time.perf_counter() - t0, world_size)
+    copy_ms = sum(a.elapsed_time(b) for a, b in pairs) / steps
     return {"value": w.updated_per_step() * world_size * steps / dt, "unit": "params/s",
             "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
+            # the time the copy stream spent copying, and the link rate it saw
+            "h2d_copy_ms_per_step": copy_ms,
+            "h2d_gbs_while_stepping": h2d / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None,
             "d2h_bytes_per_step": 8, "host_buffers_distinct": len(host),
             "device_buffers": len(srcs),
             "path": "bucketed step (%d-element buckets) overlapped with the host-to-device "
@@ -861,7 +856,9 @@ def bench_e2e_units(run, args, world_size):
         else:
             z.zero3_reduce_unit(run.ctx, f, views, run.scale, st)
 
-    def one():
+    pairs = []        # event pairs around each piece's copies (timed steps)
+
+    def one(record=False):
         z.zero3_begin_step_scaled(run.ctx, run.scale)
         for i in range(len(pieces)):                         # forward gathers
             gather(i)
@@ -871,8 +868,14 @@ def bench_e2e_units(run, args, world_size):
             with torch.cuda.stream(cp):
                 if j >= 2:
                     cp.wait_event(done[k2])
+                if record:
+                    pairs.append((torch.cuda.Event(enable_timing=True),
+                                  torch.cuda.Event(enable_timing=True)))
+                    pairs[-1][0].record(cp)
                 for d, h in zip(views, host[i]):
                     d.copy_(h, non_blocking=True)
+                if record:
+                    pairs[-1][1].record(cp)
                 ready[k2].record(cp)
             gather(i)
             st.wait_event(ready[k2])
@@ -895,11 +898,15 @@ def bench_e2e_units(run, args, world_size):
     steps = max(2, args.e2e_steps)
     t0 = time.perf_counter()
     for _ in range(steps):
-        one()
+        one(record=True)
     torch.cuda.synchronize()
     dt = allreduce_max(time.perf_counter() - t0, world_size)
+    copy_ms = sum(a.elapsed_time(b) for a, b in pairs) / steps
     return {"value": w.updated_per_step() * world_size * steps / dt, "unit": "params/s",
             "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
+            # the time the copy stream spent copying, and the link rate it saw
+            "h2d_copy_ms_per_step": copy_ms,
+            "h2d_gbs_while_stepping": h2d / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None,
             "d2h_bytes_per_step": 8, "host_buffers_distinct": sum(len(r) for r in host),
             "device_buffers": 2 * len(dev[0]),
             "path": "per-%s host-to-device copies overlapped with the previous %s's gather "

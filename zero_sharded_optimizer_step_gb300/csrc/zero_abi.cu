@@ -810,8 +810,15 @@ int zero_step_status(zero_ctx *c, int32_t *nonfinite, int32_t *skipped)
 
 uint64_t zero_step_id(const zero_ctx *c) { return c ? c->step_id : 0; }
 
+// Shards at least this long take the row placement (gather_rows_kernel) in
+// a ZeRO-3 unit gather: measured on GB300, a Llama-7B-layer unit's 8 shards
+// of 50.6 MB in 0.1214 ms against 0.1248 ms with gather_kernel, while 4-11 MB
+// shards were faster with gather_kernel (0.0178 against 0.0185 ms) and the
+// one-rank placement of 234 MB shards too (4.24 against 4.35 ms).
+constexpr int64_t kRowsGatherMinShardBytes = (int64_t)32 << 20;
+
 static int gather(zero_ctx *c, const void *const *shards, int32_t n, void *full, int32_t dtype,
-                  int64_t S, cudaStream_t s)
+                  int64_t S, cudaStream_t s, bool unit = false)
 {
     if (!valid_dtype(dtype)) return fail(ZERO_EINVAL, "unknown dtype %d", dtype);
     const int es = zgb::elem_size(dtype);
@@ -829,9 +836,23 @@ static int gather(zero_ctx *c, const void *const *shards, int32_t n, void *full,
     a.es = es;
     // a gather neither reads nor writes the flag: it does not become the
     // stream zero_step_status waits on
-    const cudaError_t e = (c->gather_mode == ZERO_GATHER_LEAN && zgb::lean_gather_eligible(a))
-                              ? zgb::launch_gather_lean(a, c->sms, s)
-                              : zgb::launch_gather(a, c->sms, s);
+    cudaError_t e;
+    if (c->gather_mode == ZERO_GATHER_LEAN && zgb::lean_gather_eligible(a)) {
+        e = zgb::launch_gather_lean(a, c->sms, s);
+    } else if (unit && a.shard_bytes >= kRowsGatherMinShardBytes) {
+        zgb::GatherRowsArgs r;
+        memset(&r, 0, sizeof r);
+        for (int32_t k = 0; k < n; ++k) {
+            r.src[k] = a.src[k];
+            r.dst[k] = a.dst + (int64_t)k * a.shard_bytes;
+            r.bytes[k] = a.shard_bytes;
+        }
+        r.n = n;
+        r.es = es;
+        e = zgb::launch_gather_rows(r, c->sms, s);
+    } else {
+        e = zgb::launch_gather(a, c->sms, s);
+    }
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "gather kernel");
 }
 
@@ -927,7 +948,8 @@ int zero3_gather_unit(zero_ctx *c, int32_t unit, const void *const *shards, int3
     if (c->stage != 3) return fail(ZERO_EINVAL, "unit calls are for stage 3");
     if (unit < 0 || unit >= (int32_t)c->unit_S.size())
         return fail(ZERO_EINVAL, "unit %d out of range [0, %d)", unit, (int)c->unit_S.size());
-    return gather(c, shards, n_shards, unit_full, c->pdt, c->unit_S[unit], (cudaStream_t)stream);
+    return gather(c, shards, n_shards, unit_full, c->pdt, c->unit_S[unit], (cudaStream_t)stream,
+                  true);
 }
 
 int zero3_step_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32_t n_grads,
