@@ -77,7 +77,7 @@ def parse():
                     choices=["gpt2_xl", "gpt2_small", "one_rank_7p5b", "zero3_llama7b", "tiny",
                              "gpt2_xl_bucketed", "zero3_prefetch", "zero3_gpt2_small",
                              "gpt2_xl_adamw", "fsdp2_llama7b", "fsdp2_llama7b_per_param",
-                             "gpt2_small_stage1", "zero3_llama7b_fp16"])
+                             "gpt2_small_stage1", "zero3_llama7b_fp16", "fsdp2_prefetch"])
     ap.add_argument("--graph", action="store_true",
                     help="also capture one step in a CUDA graph and time its replays")
     ap.add_argument("--unit-fwd-ms", type=float, default=0.25,
@@ -491,7 +491,10 @@ def bench_prefetch(args, rank, world_size, device_index):
     from workloads.runner import Runner
     from workloads.zero3_schedule import Zero3Schedule
 
-    w = W.zero3_llama7b(args.units or 32).replace(name="zero3_prefetch")
+    if args.workload == "fsdp2_prefetch":
+        w = W.fsdp2_llama7b(args.units or 32).replace(name="fsdp2_prefetch")
+    else:
+        w = W.zero3_llama7b(args.units or 32).replace(name="zero3_prefetch")
     torch.cuda.set_device(device_index)
     run = Runner(w, device="cuda:%d" % device_index)
     run.fill_grads(1)
@@ -526,7 +529,7 @@ def bench_prefetch(args, rank, world_size, device_index):
     updated = w.updated_per_step()
     run.close()
     peak, peak_kind = peaks()
-    U = len(w.units)
+    U = len(w.groups) if w.groups else len(w.units)     # visits per direction
     return {
         "metric": METRIC, "value": updated * world_size / (times["overlap"] * 1e-3),
         "unit": "params/s", "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
@@ -534,8 +537,9 @@ def bench_prefetch(args, rank, world_size, device_index):
         "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded draws; a stand-in kernel plays each unit's compute)",
         "config": {
-            "workload": describe(w) + " + stand-in compute %.3f ms fwd / %.3f ms bwd per unit"
-                        % (args.unit_fwd_ms, 2 * args.unit_fwd_ms),
+            "workload": describe(w) + " + stand-in compute %.3f ms fwd / %.3f ms bwd per %s"
+                        % (args.unit_fwd_ms, 2 * args.unit_fwd_ms,
+                           "group" if w.groups else "unit"),
             "compute_only_ms": times["compute_only"], "serial_ms": times["serial"],
             "overlap_ms": times["overlap"], "gather_time_serial_ms": gathers,
             "exposed_gather_ms": exposed,
@@ -1092,7 +1096,7 @@ def main():
         import __graft_entry__
         __graft_entry__.build() if rank == 0 else None
         barrier(world_size)
-        if args.workload == "zero3_prefetch":
+        if args.workload in ("zero3_prefetch", "fsdp2_prefetch"):
             res = bench_prefetch(args, rank, world_size, local)
         else:
             res = bench_ours(args, rank, world_size, local)

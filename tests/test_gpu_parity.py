@@ -758,6 +758,35 @@ def test_stage3_one_pass_two_state_sets(rank, scaled, layout):
     run.close()
 
 
+def test_grouped_prefetch_schedule_matches_serial_and_oracle():
+    """FSDP2's per-parameter units in layer groups, each group's gather
+    prefetched on the background stream (the lean bulk-copy form: every
+    shard 16-byte aligned) while the previous group computes: the same
+    results as the serial schedule and the oracle."""
+    from workloads.runner import Runner
+    from workloads.zero3_schedule import Zero3Schedule
+    shapes = [(256, 64), (512, 16), (64, 8), (1024, 8), (128, 32)]
+    w = W.dim0(shapes, 4, rank=1, steps=3).replace(groups=[2, 2, 1])
+    runs = {}
+    for mode in ("serial", "overlap"):
+        run = Runner(w)
+        sch = Zero3Schedule(run, 2000, 4000, 64, mode)
+        for it in range(1, 4):
+            run.fill_grads(it)
+            sch.launch_step()
+        torch.cuda.synchronize()
+        runs[mode] = run
+    ref = refs.OracleRun(w)
+    for it in range(1, 4):
+        ref.step(it)
+    assert torch.equal(runs["serial"].master, runs["overlap"].master)
+    assert torch.equal(runs["serial"].params, runs["overlap"].params)
+    runs["overlap"].skips = ref.skips
+    compare_runner(runs["overlap"], ref, what="grouped prefetch")
+    for run in runs.values():
+        run.close()
+
+
 def test_stage3_one_pass_prefetched_schedule():
     """The prefetch schedule with two state sets: the same results as the
     serial one and the oracle, with a skipped step."""

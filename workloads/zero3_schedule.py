@@ -13,6 +13,12 @@ With loss scaling the backward visit only reduces (and unscales) its unit's
 grads; Adam waits until every unit's overflow flag is in, and one apply pass
 after the last visit updates all units or, on overflow, none ("PaddlePaddle
 ZeRO优化", section 混合精度才是最佳拍档: the scaler skips the whole step).
+With a second state set bound, the backward visit steps its unit in one
+pass into that set and zero3_end_step applies the verdict after the last.
+
+A workload with groups of units (FSDP2's per-parameter layout, a layer's
+parameters per group) visits groups instead: one group gather and one group
+step per visit.
 """
 from __future__ import annotations
 
@@ -31,32 +37,62 @@ class Zero3Schedule:
         self.iters = {"f": iters_fwd, "b": iters_bwd}
         self.blocks = busy_blocks
         self.sink = torch.empty(busy_blocks * 128, device=run.dev)
-        self.bufs = [run.unit_full, torch.empty_like(run.unit_full)]
+        w = run.w
+        # the pieces a visit gathers and steps: single units, or groups of
+        # units (a layer's parameters) gathered and stepped in one launch each
+        self.pieces = run.group_ranges() if w.groups else [(u, 1) for u in range(len(w.units))]
+        if w.groups:
+            # two buffers of a group's destinations, alternating between visits
+            sizes = [w.unit_shard(u) * w.world for u in range(len(w.units))]
+            self.bufs = []
+            for big in (run.group_full, torch.empty_like(run.group_full)):
+                per_piece = []
+                for f, n in self.pieces:
+                    views, off = [], 0
+                    for u in range(f, f + n):
+                        views.append(big[off:off + sizes[u]])
+                        off += sizes[u]
+                    per_piece.append(views)
+                self.bufs.append(per_piece)
+        else:
+            self.bufs = [run.unit_full, torch.empty_like(run.unit_full)]
         # prefetches run in the background: the lean (bulk-copy) gather leaves
         # the SMs to the compute, which gets the higher stream priority
         self.gs = torch.cuda.Stream(run.dev, priority=0)
         self.cs = torch.cuda.Stream(run.dev, priority=-1)
         z.zero_set_gather_mode(run.ctx, z.ZERO_GATHER_LEAN if mode == "overlap"
                                else z.ZERO_GATHER_FAST)
-        U = len(run.w.units)
+        U = len(self.pieces)
         self.visits = [(u, "f") for u in range(U)] + [(u, "b") for u in reversed(range(U))]
         n = len(self.visits)
         self.ready = [torch.cuda.Event() for _ in range(n)]
         self.used = [torch.cuda.Event() for _ in range(n)]
 
     def _gather(self, v, stream):
-        u, _ = self.visits[v]
-        z.zero3_gather_unit(self.run.ctx, u, self.run.shards[u], self.bufs[v % 2], stream)
+        i, _ = self.visits[v]
+        f, n = self.pieces[i]
+        run = self.run
+        if run.w.groups:
+            z.zero3_gather_group(run.ctx, f, run.shards[f:f + n], self.bufs[v % 2][i], stream)
+        else:
+            z.zero3_gather_unit(run.ctx, f, run.shards[f], self.bufs[v % 2], stream)
 
     def _compute(self, v, stream):
-        u, phase = self.visits[v]
+        i, phase = self.visits[v]
         standin.busy(self.sink.data_ptr(), self.blocks, self.iters[phase], stream.cuda_stream)
         if phase == "b":
             run, w = self.run, self.run.w
-            if run.scale > 0 and run.shadow is None:
-                z.zero3_reduce_unit(run.ctx, u, run.grads[u], run.scale, stream)
+            f, n = self.pieces[i]
+            two_pass = run.scale > 0 and run.shadow is None
+            if w.groups and two_pass:
+                z.zero3_reduce_group(run.ctx, f, n, run.group_grads[i], run.scale, stream)
+            elif w.groups:
+                z.zero3_step_group(run.ctx, f, n, run.group_grads[i], w.lr, w.beta1, w.beta2,
+                                   w.eps, run.t + 1, stream)
+            elif two_pass:
+                z.zero3_reduce_unit(run.ctx, f, run.grads[f], run.scale, stream)
             else:
-                z.zero3_step_unit(run.ctx, u, run.grads[u], w.lr, w.beta1, w.beta2,
+                z.zero3_step_unit(run.ctx, f, run.grads[f], w.lr, w.beta1, w.beta2,
                                   w.eps, run.t + 1, stream)
 
     def _apply(self, stream):
