@@ -701,6 +701,19 @@ def test_group_step_parity(rank, scaled):
     run.close()
 
 
+@pytest.mark.parametrize("rank", [-1, 2])
+def test_group_with_an_empty_unit(rank):
+    """A group holding a unit of zero parameters (and units whose shards are
+    not multiples of 16 bytes): gathers, steps and the skip as the oracle
+    has them."""
+    units = [1000, 0, 2000, 44]
+    w = W.Workload("gempty", sum(units), 4, 3, W.F16, W.F16, rank=rank, units=units, steps=3,
+                   loss_scale=2.0 ** 8, inject=(2, 1)).replace(groups=[3, 1])
+    run, ref = run_both(w, shadow=True)
+    compare_runner(run, ref, what="group with an empty unit")
+    run.close()
+
+
 def test_group_call_errors():
     import zero_sharded_optimizer_step_gb300 as z
     from workloads.runner import Runner
