@@ -464,7 +464,7 @@ def bench_ours(args, rank, world_size, device_index):
         "gpu_launches": sum(L.kernels for L in plan) * args.steps,
         "clocks": clock_info,
     }
-    if args.graph and run.scale <= 0:
+    if args.graph:
         gms = bench_graph(run, plan, args, world_size)
         result["config"]["graph_ms_per_step"] = gms
         result["config"]["graph_params_per_s"] = updated * world_size / (gms * 1e-3)
@@ -563,6 +563,8 @@ def bench_graph(run, plan, args, world_size):
     import zero_sharded_optimizer_step_gb300 as z
 
     w, st = run.w, run.stream
+    if run.scale > 0:
+        return bench_graph_advance(run, plan, args, world_size)
     d = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, device=run.dev)
     hs = [torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
     z.zero_bind_hyper(run.ctx, d)
@@ -610,6 +612,61 @@ def bench_graph(run, plan, args, world_size):
     e1.record(st)
     torch.cuda.synchronize()
     ms = allreduce_max(e0.elapsed_time(e1) / args.steps, world_size)
+    z.zero_bind_hyper(run.ctx, None)
+    return ms
+
+
+def bench_graph_advance(run, plan, args, world_size):
+    """Loss-scaled steps replayed from one CUDA graph of [step, advance]: the
+    advance kernel reads each step's verdict and rewrites the device block of
+    scalars (t, loss scale, bias corrections) for the next, so the host
+    neither prepares a step nor reads a verdict between replays."""
+    import torch
+    import zero_sharded_optimizer_step_gb300 as z
+
+    w, st = run.w, run.stream
+    d = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, device=run.dev)
+    h = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, pin_memory=True)
+    z.zero_bind_hyper(run.ctx, d)
+    T = run.t + args.warmup + args.steps + 4
+    tab = np.zeros(2 * T, np.float32)
+    z.zero_fill_advance_table(tab.ctypes.data, T, w.beta1, w.beta2)
+    dtab = torch.from_numpy(tab).to(run.dev)
+    hs = np.zeros(4, np.int64)
+    z.zero_advance_state(hs.ctypes.data, run.t + 1, run.scale, w.growth_interval)
+    ds = torch.from_numpy(hs).to(run.dev)
+    z.zero_bind_advance(run.ctx, dtab, T, ds)
+    z.zero_prepare_step(run.ctx, h, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, run.scale)
+    d.copy_(h)
+    torch.cuda.synchronize()
+
+    def body():
+        for L in plan:
+            L.fn()
+        z.zero_advance_step(run.ctx, st)
+
+    with torch.cuda.stream(st):
+        body()                              # one eager step in this mode first
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        body()
+    with torch.cuda.stream(st):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    barrier(world_size)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(st)
+    torch.cuda.synchronize()
+    ms = allreduce_max(e0.elapsed_time(e1) / args.steps, world_size)
+    status = int(np.frombuffer(ds.cpu().numpy()[1].tobytes()[4:], np.int32)[0])
+    assert status == 0, "the bias table ran out during the graph replays"
+    z.zero_bind_advance(run.ctx, None, 0, None)
     z.zero_bind_hyper(run.ctx, None)
     return ms
 

@@ -278,6 +278,42 @@ int zero_bind_hyper(zero_ctx *ctx, void *d_hyper);
 int zero_prepare_step(zero_ctx *ctx, void *host_hyper, double lr, double beta1, double beta2,
                       double eps, int64_t t, float loss_scale);
 
+/* Scalars that advance on the device: asynchronous loss scaling.  With a
+ * device scalar block bound, zero_advance_step() launched after a step's
+ * kernels does on the GPU what the host otherwise does between steps: it
+ * reads the step's overflow verdict, applies the loss-scale policy of
+ * zero_scale_update (halve on a skipped step; t advances only on applied
+ * steps; double after growth_interval clean steps, never to infinity) and
+ * rewrites the block for the next step -- bias corrections 1 - beta^t from
+ * a table the host computed (the same values zero_prepare_step derives), the
+ * unscale factor from the new scale, the next step id.  No host round trip
+ * per step: a loss-scaled training loop, or one CUDA graph of [step,
+ * advance] replayed, runs without reading the verdict back.  lr, betas, eps
+ * and the weight decay stay as the block has them.
+ *
+ * zero_advance_table_bytes(t_max): bytes of the table for steps 1..t_max
+ *   (8 per step), or -1.
+ * zero_fill_advance_table(host_table, t_max, beta1, beta2): fill a host
+ *   buffer of that size (two floats per step); the caller copies it to the
+ *   device.
+ * zero_advance_state(host_state, t, loss_scale, growth_interval): fill the
+ *   32-byte state block -- {int64 t; float scale; int32 status; int64
+ *   good_steps; int64 growth_interval} -- for the step the block describes
+ *   (the one zero_prepare_step prepared); the caller copies it to the device
+ *   and may read it back at any time (status 1: the table ran out and the
+ *   block stopped advancing).
+ * zero_bind_advance(ctx, d_table, t_max, d_state): bind both (NULL, NULL
+ *   unbinds); the table 4-byte, the state 8-byte aligned.
+ * zero_advance_step(ctx, stream): the advance itself (one small launch).  The
+ *   context's host-side step id advances with it, so zero_step_status()
+ *   describes the step before the last advance only until that advance is
+ *   issued; read the verdict before advancing, or read the state block. */
+int64_t zero_advance_table_bytes(int64_t t_max);
+int zero_fill_advance_table(void *host_table, int64_t t_max, double beta1, double beta2);
+int zero_advance_state(void *host_state, int64_t t, float loss_scale, int64_t growth_interval);
+int zero_bind_advance(zero_ctx *ctx, const void *d_table, int64_t t_max, void *d_state);
+int zero_advance_step(zero_ctx *ctx, void *stream);
+
 /* ------------------------------------------------------------ the step */
 
 /* One ZeRO step (stages 1, 2) on `stream`.

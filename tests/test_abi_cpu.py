@@ -6,6 +6,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -154,3 +155,26 @@ def test_calls_before_bind_fail_cleanly(z):
     assert ei.value.code == z.ZERO_ESTATE
     with pytest.raises(z.ZeroError):
         z.zero3_begin_step(c)   # not stage 3
+
+
+def test_advance_table_and_state_on_the_host(z):
+    """The device-advance table holds, per step, the bias corrections the
+    oracle derives for that step (bit for bit), and the state block packs t,
+    scale, status, good steps and the growth interval in 32 bytes."""
+    import oracle
+    T = 3000
+    buf = np.zeros(z.zero_advance_table_bytes(T) // 4, np.float32)
+    assert buf.size == 2 * T
+    z.zero_fill_advance_table(buf.ctypes.data, T, 0.9, 0.999)
+    for t in (1, 2, 3, 17, 100, 999, 3000):
+        sc = oracle.adam_scalars(0.9, 0.999, t)       # c1, c2, bc1, bc2
+        assert buf[2 * (t - 1)].tobytes() == sc[2].tobytes()
+        assert buf[2 * (t - 1) + 1].tobytes() == sc[3].tobytes()
+    assert z.zero_advance_table_bytes(0) == -1
+    st = np.zeros(4, np.int64)
+    z.zero_advance_state(st.ctypes.data, 7, 65536.0, 2000)
+    assert st[0] == 7 and st[2] == 0 and st[3] == 2000
+    assert np.frombuffer(st[1].tobytes()[:4], np.float32)[0] == 65536.0
+    assert np.frombuffer(st[1].tobytes()[4:], np.int32)[0] == 0
+    with pytest.raises(z.ZeroError):
+        z.zero_fill_advance_table(None, 5, 0.9, 0.999)

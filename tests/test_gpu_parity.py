@@ -1083,3 +1083,100 @@ def test_prepared_step_protocol():
         z.zero_step(run.ctx, run.grads[0], 1e-3, 0.9, 0.999, 1e-8, 1, loss_scale=8.0)
     z.zero_bind_hyper(run.ctx, None)
     run.close()
+
+
+# ----------------------------------------- scalars advanced on the device
+
+def _advance_setup(run, w, T, growth_interval):
+    import zero_sharded_optimizer_step_gb300 as z
+    d = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, device=run.dev)
+    h = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, pin_memory=True)
+    z.zero_bind_hyper(run.ctx, d)
+    tab = np.zeros(2 * T, np.float32)
+    z.zero_fill_advance_table(tab.ctypes.data, T, w.beta1, w.beta2)
+    dtab = torch.from_numpy(tab).to(run.dev)
+    hs = np.zeros(4, np.int64)
+    z.zero_advance_state(hs.ctypes.data, 1, run.scale, growth_interval)
+    ds = torch.from_numpy(hs).to(run.dev)
+    z.zero_bind_advance(run.ctx, dtab, T, ds)
+    z.zero_prepare_step(run.ctx, h, w.lr, w.beta1, w.beta2, w.eps, 1, run.scale)
+    d.copy_(h)
+    torch.cuda.synchronize()
+    return d, h, dtab, ds
+
+
+def _state(ds):
+    raw = ds.cpu().numpy()
+    return (int(raw[0]), float(np.frombuffer(raw[1].tobytes()[:4], np.float32)[0]),
+            int(np.frombuffer(raw[1].tobytes()[4:], np.int32)[0]), int(raw[2]))
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_device_advance_matches_the_host_policy(graph):
+    """Loss-scaled steps whose t, loss scale and bias corrections advance on
+    the device (no verdict read back): a skipped step, two growths
+    (growth_interval 2), bit-identical to the oracle stepping with the host
+    policy; as eager launches and as one CUDA graph of [step, advance]
+    replayed step after step."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    w = W.Workload("adv", 1_000_003, 8, 2, W.F16, W.F16, steps=7, loss_scale=2.0 ** 12,
+                   inject=(3, 2), growth_interval=2)
+    run = Runner(w, shadow=True)
+    d, h, dtab, ds = _advance_setup(run, w, 32, 2)
+    ref = refs.OracleRun(w)
+    s = torch.cuda.Stream()
+
+    def body():
+        z.zero_step(run.ctx, run.grads[0], 0.0, 0.0, 0.0, 0.0, 1, loss_scale=1.0, stream=s)
+        z.zero_advance_step(run.ctx, s)
+
+    g = torch.cuda.CUDAGraph() if graph else None
+    for it in range(1, 8):
+        run.scale = ref.scale                 # the grads are drawn at the scale in force
+        run.fill_grads(it)
+        torch.cuda.synchronize()
+        if graph and it == 1:
+            with torch.cuda.stream(s):
+                body()
+            torch.cuda.synchronize()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    body()
+        elif graph:
+            with torch.cuda.stream(s):
+                g.replay()
+        else:
+            with torch.cuda.stream(s):
+                body()
+        torch.cuda.synchronize()
+        ref.step(it)
+        t, scale, status, good = _state(ds)
+        assert (t, scale, status) == (ref.t + 1, ref.scale, 0), (it, t, scale, ref.t, ref.scale)
+        assert good == ref.good
+    assert ref.skips == [False, False, True, False, False, False, False]
+    compare_runner(run, ref, what="device advance" + (" graph" if graph else ""))
+    run.close()
+
+
+def test_device_advance_stops_when_the_table_runs_out():
+    """With bias corrections for 3 steps only, the advance after step 3 sets
+    the status and leaves the block as it was; nothing faults."""
+    import zero_sharded_optimizer_step_gb300 as z
+    from workloads.runner import Runner
+    w = W.Workload("advT", 10_001, 4, 2, W.BF16, W.BF16, steps=4)
+    run = Runner(w)
+    d, h, dtab, ds = _advance_setup(run, w, 3, 0)
+    for it in (1, 2, 3):
+        run.fill_grads(it)
+        z.zero_step(run.ctx, run.grads[0], 0.0, 0.0, 0.0, 0.0, 1)
+        before = d.cpu().clone()
+        z.zero_advance_step(run.ctx)
+        torch.cuda.synchronize()
+        t, scale, status, good = _state(ds)
+        if it < 3:
+            assert (t, status) == (it + 1, 0)
+        else:
+            assert status == 1 and t == 3
+            assert torch.equal(d.cpu(), before)
+    run.close()

@@ -61,6 +61,11 @@ _SIGS = {
     "zero_bind_hyper": (ctypes.c_int, [_ctxp, _vp]),
     "zero_prepare_step": (ctypes.c_int, [_ctxp, _vp, _f64, _f64, _f64, _f64, _i64, _f32]),
     "zero_set_gather_mode": (ctypes.c_int, [_ctxp, _i32]),
+    "zero_advance_table_bytes": (_i64, [_i64]),
+    "zero_fill_advance_table": (ctypes.c_int, [_vp, _i64, _f64, _f64]),
+    "zero_advance_state": (ctypes.c_int, [_vp, _i64, _f32, _i64]),
+    "zero_bind_advance": (ctypes.c_int, [_ctxp, _vp, _i64, _vp]),
+    "zero_advance_step": (ctypes.c_int, [_ctxp, _vp]),
     "zero_gather_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "zero_bind_shadow": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp]),
     "zero_current_state": (ctypes.c_int, [_ctxp, ctypes.POINTER(_i32)]),
@@ -277,6 +282,31 @@ def zero_prepare_step(ctx, host_hyper, lr: float, beta1: float, beta2: float, ep
     int address)."""
     _check(_L.zero_prepare_step(_h(ctx), _ptr(host_hyper), lr, beta1, beta2, eps, t,
                                 loss_scale))
+
+
+ZERO_ADVANCE_STATE_BYTES = 32
+
+
+def zero_advance_table_bytes(t_max: int) -> int:
+    return int(_L.zero_advance_table_bytes(t_max))
+
+
+def zero_fill_advance_table(host_table, t_max: int, beta1: float, beta2: float) -> None:
+    """host_table: a host buffer of zero_advance_table_bytes(t_max) bytes."""
+    _check(_L.zero_fill_advance_table(_ptr(host_table), t_max, beta1, beta2))
+
+
+def zero_advance_state(host_state, t: int, loss_scale: float, growth_interval: int) -> None:
+    """host_state: a host buffer of ZERO_ADVANCE_STATE_BYTES bytes."""
+    _check(_L.zero_advance_state(_ptr(host_state), t, loss_scale, growth_interval))
+
+
+def zero_bind_advance(ctx, d_table, t_max: int, d_state) -> None:
+    _check(_L.zero_bind_advance(_h(ctx), _ptr(d_table), t_max, _ptr(d_state)))
+
+
+def zero_advance_step(ctx, stream=None) -> None:
+    _check(_L.zero_advance_step(_h(ctx), _stream(stream)))
 
 
 def zero_set_weight_decay(ctx, weight_decay: float) -> None:

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzero.so")
-SOURCES = ["zero_abi.cu", "zero_step_kernels.cu", "zero_gather.cu"]
+SOURCES = ["zero_abi.cu", "zero_step_kernels.cu", "zero_gather.cu", "zero_advance.cu"]
 HEADERS = ["zero_internal.h", os.path.join("..", "..", "include", "zero.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

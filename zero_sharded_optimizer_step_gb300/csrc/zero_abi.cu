@@ -76,6 +76,9 @@ struct zero_ctx {
     int32_t gather_mode = 0;     // ZERO_GATHER_FAST or ZERO_GATHER_LEAN
 
     void *hyper = nullptr;       // device block of per-step scalars (graph capture)
+    const float *adv_table = nullptr;   // zero_bind_advance: bias corrections per t
+    int64_t adv_tmax = 0;
+    void *adv_state = nullptr;          // 32-byte device step state
 
     uint64_t step_id = 0;
     bool step_scaled = false;
@@ -666,6 +669,74 @@ int zero_prepare_step(zero_ctx *c, void *host_hyper, double lr, double b1, doubl
     h.skip_id = c->step_scaled ? c->step_id : ~0ull;
     memset(host_hyper, 0, ZERO_HYPER_BYTES);
     memcpy(host_hyper, &h, sizeof h);
+    return ZERO_OK;
+}
+
+int64_t zero_advance_table_bytes(int64_t t_max)
+{
+    return t_max >= 1 && t_max <= ((int64_t)1 << 40) ? 8 * t_max : -1;
+}
+
+int zero_fill_advance_table(void *host_table, int64_t t_max, double b1, double b2)
+{
+    if (!host_table || t_max < 1 || t_max > ((int64_t)1 << 40))
+        return fail(ZERO_EINVAL, "host_table and 1 <= t_max required");
+    float *p = static_cast<float *>(host_table);
+    for (int64_t t = 1; t <= t_max; ++t) {
+        // exactly the host's derivation of a step's bias corrections
+        p[2 * (t - 1)] = (float)(1.0 - std::pow(b1, (double)t));
+        p[2 * (t - 1) + 1] = (float)(1.0 - std::pow(b2, (double)t));
+    }
+    return ZERO_OK;
+}
+
+int zero_advance_state(void *host_state, int64_t t, float loss_scale, int64_t growth_interval)
+{
+    if (!host_state || t < 1) return fail(ZERO_EINVAL, "host_state and t >= 1 required");
+    zgb::AdvanceState st{};
+    st.t = t;
+    st.scale = loss_scale > 0.0f ? loss_scale : 0.0f;
+    st.status = 0;
+    st.good_steps = 0;
+    st.growth_interval = growth_interval;
+    memcpy(host_state, &st, sizeof st);
+    return ZERO_OK;
+}
+
+int zero_bind_advance(zero_ctx *c, const void *d_table, int64_t t_max, void *d_state)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (!d_table && !d_state) {
+        c->adv_table = nullptr;
+        c->adv_tmax = 0;
+        c->adv_state = nullptr;
+        return ZERO_OK;
+    }
+    if (!d_table || !d_state || t_max < 1)
+        return fail(ZERO_EINVAL, "d_table, d_state and t_max >= 1 required (or both NULL)");
+    if (!aligned(d_table, 4) || !aligned(d_state, 8))
+        return fail(ZERO_EALIGN, "the table must be 4-byte and the state 8-byte aligned");
+    c->adv_table = static_cast<const float *>(d_table);
+    c->adv_tmax = t_max;
+    c->adv_state = d_state;
+    return ZERO_OK;
+}
+
+int zero_advance_step(zero_ctx *c, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if (!c->hyper) return fail(ZERO_ESTATE, "no device scalar block bound (zero_bind_hyper)");
+    if (!c->adv_state) return fail(ZERO_ESTATE, "no device step state bound (zero_bind_advance)");
+    if (c->step_id == 0) return fail(ZERO_ESTATE, "prepare the first step (zero_prepare_step)");
+    if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
+    if (c->stage3_open) return fail(ZERO_ESTATE, "a stage-3 step is open (zero3_end_step)");
+    const cudaError_t e = zgb::launch_advance(
+        static_cast<zgb::DeviceHyper *>(c->hyper), reinterpret_cast<const unsigned long long *>(c->flag),
+        static_cast<zgb::AdvanceState *>(c->adv_state), c->adv_table, c->adv_tmax,
+        (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "advance kernel");
+    c->step_id += 1;             // the device block now describes the next step
     return ZERO_OK;
 }
 

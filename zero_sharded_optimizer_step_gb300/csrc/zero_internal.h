@@ -39,6 +39,18 @@ struct DeviceHyper {
     unsigned long long skip_id;   // id apply/finalize treat as "skip" (~0 = never)
 };
 
+// The device-resident step state of steps whose scalars advance on the
+// device (zero_bind_advance): what the host's loss-scale policy keeps, for
+// the step the device block currently describes.
+struct AdvanceState {
+    int64_t t;                 // the step count of the described step
+    float scale;               // its loss scale (as prepared; 0 = unscaled)
+    int32_t status;            // 0, or 1 once the bias table ran out
+    int64_t good_steps;        // clean steps since the scale last changed
+    int64_t growth_interval;   // doubling period (<= 0: never)
+};
+static_assert(sizeof(AdvanceState) == 32, "AdvanceState is 32 bytes");
+
 // Arguments of the per-element step kernels over one contiguous range of
 // `n` elements of the state.  Every pointer is already offset to the
 // range's first element.
@@ -148,6 +160,11 @@ cudaError_t launch_gather_lean(const GatherArgs &a, int sms, cudaStream_t s);
 // aligned at both ends, lengths multiples of 16 bytes.
 bool lean_gather_rows_eligible(const GatherRowsArgs &a);
 cudaError_t launch_gather_rows_lean(const GatherRowsArgs &a, int sms, cudaStream_t s);
+// After a step: read its verdict, advance *st by the loss-scale policy and
+// rewrite *hyper for the next step (bias corrections from table: 2 floats per
+// t = 1..t_max).  One thread.
+cudaError_t launch_advance(DeviceHyper *hyper, const unsigned long long *flag, AdvanceState *st,
+                           const float *table, int64_t t_max, cudaStream_t s);
 // Waits of the lean gather that ran out (cumulative, this process).
 cudaError_t lean_gather_timeouts(unsigned int *count);
 
