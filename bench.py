@@ -565,13 +565,12 @@ def bench_graph(run, plan, args, world_size):
     w, st = run.w, run.stream
     if run.scale > 0:
         return bench_graph_advance(run, plan, args, world_size)
-    d = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, device=run.dev)
     hs = [torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
-    z.zero_bind_hyper(run.ctx, d)
+    # the scalars go straight into the context's constant slot (one copy per step)
+    z.zero_bind_hyper(run.ctx, z.zero_hyper_slot(run.ctx))
 
     def body(i):
-        with torch.cuda.stream(st):
-            d.copy_(hs[i], non_blocking=True)
+        z.zero_load_hyper(run.ctx, hs[i], st)
         for L in plan:
             L.fn()
 

@@ -273,8 +273,25 @@ int zero_set_weight_decay(zero_ctx *ctx, double weight_decay);
  * zero_step_status reads the verdict of the prepared step as usual.
  * A host block must not be refilled before the copy that reads it has run:
  * with steps queued ahead of the GPU, alternate two host blocks (two
- * captured graphs) and wait on an event recorded after the older one. */
+ * captured graphs) and wait on an event recorded after the older one.
+ * The kernels read the scalars as constant-bank operands: each bound context
+ * holds one of 8 constant-memory slots per device (ZERO_ESTATE when all are
+ * taken; unbinding or zero_destroy frees it), and the step's first launch
+ * copies the device block into the slot on its stream (one small copy per
+ * step, captured with the step).  Binding the slot's own address
+ * (zero_hyper_slot) as the block removes that copy: step 2 then writes the
+ * slot directly.  The device advance (zero_advance_step) needs a block in
+ * ordinary device memory, which it rewrites. */
 int zero_bind_hyper(zero_ctx *ctx, void *d_hyper);
+
+/* The device address of this context's constant slot (claimed if it holds
+ * none yet): a ZERO_HYPER_BYTES block that a host-to-device copy may fill
+ * directly, to be bound with zero_bind_hyper. */
+int zero_hyper_slot(zero_ctx *ctx, void **d_slot);
+
+/* Step 2 for a context bound to its own constant slot: copy host_block
+ * (ZERO_HYPER_BYTES, pinned when captured) into the slot on `stream`. */
+int zero_load_hyper(zero_ctx *ctx, const void *host_block, void *stream);
 int zero_prepare_step(zero_ctx *ctx, void *host_hyper, double lr, double beta1, double beta2,
                       double eps, int64_t t, float loss_scale);
 

@@ -916,21 +916,28 @@ def _hyper(run):
     return d, h
 
 
-def test_zero3_step_replayed_from_a_cuda_graph():
+@pytest.mark.parametrize("direct", [False, True])
+def test_zero3_step_replayed_from_a_cuda_graph(direct):
     """A whole ZeRO-3 step (forward gathers, backward gathers + unit steps)
     captured once and replayed: per-step scalars come from the device block
-    refreshed by a memcpy node, so three replays equal three real steps."""
+    refreshed by a memcpy node (or copied straight into the context's
+    constant slot), so three replays equal three real steps."""
     import zero_sharded_optimizer_step_gb300 as z
     from workloads.runner import Runner
     units = [100_003, 7, 250_000, 33_333]
     w = W.Workload("z3g", sum(units), 4, 3, W.BF16, W.BF16, rank=1, units=units, steps=3)
     run = Runner(w)
     d, h = _hyper(run)
+    if direct:
+        z.zero_bind_hyper(run.ctx, z.zero_hyper_slot(run.ctx))
     ref = refs.OracleRun(w)
     U = len(units)
 
     def body():
-        d.copy_(h, non_blocking=True)
+        if direct:
+            z.zero_load_hyper(run.ctx, h)
+        else:
+            d.copy_(h, non_blocking=True)
         z.zero3_begin_step(run.ctx)
         for u in range(U):
             z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full, None)
@@ -1068,6 +1075,43 @@ def test_device_scalar_block_unaligned_grads():
     compare_runner(run, ref, what="hyper unaligned")
     z.zero_bind_hyper(run.ctx, None)
     run.close()
+
+
+def test_constant_slots_are_limited_and_freed():
+    """Eight contexts per device may hold a scalar block at once; a ninth is
+    refused until one is unbound or destroyed; the device advance refuses a
+    block that is the constant slot itself."""
+    import zero_sharded_optimizer_step_gb300 as z
+    dev = torch.device("cuda:0")
+    ctxs, blocks = [], []
+    for k in range(9):
+        c = z.zero_init(64, 2, 2, z.ZERO_F32, z.ZERO_F32, -1)
+        P = z.zero_ctx_state_elems(c)
+        bufs = [torch.zeros(P, device=dev) for _ in range(4)]
+        flag = torch.zeros(1, dtype=torch.int64, device=dev)
+        z.zero_bind(c, *bufs[:3], bufs[3], None, flag)
+        ctxs.append((c, bufs, flag))
+        blocks.append(torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, device=dev))
+    for k in range(8):
+        z.zero_bind_hyper(ctxs[k][0], blocks[k])
+    with pytest.raises(z.ZeroError) as ei:
+        z.zero_bind_hyper(ctxs[8][0], blocks[8])
+    assert ei.value.code == z.ZERO_ESTATE
+    z.zero_bind_hyper(ctxs[3][0], None)              # unbinding frees a slot
+    z.zero_bind_hyper(ctxs[8][0], blocks[8])
+    with pytest.raises(z.ZeroError):
+        z.zero_bind_hyper(ctxs[3][0], blocks[3])
+    ctxs[0][0].close()                               # so does destroying a context
+    z.zero_bind_hyper(ctxs[3][0], z.zero_hyper_slot(ctxs[3][0]))
+    with pytest.raises(z.ZeroError):                 # the advance rewrites its block
+        st = torch.zeros(4, dtype=torch.int64, device=dev)
+        tab = torch.zeros(8, device=dev)
+        z.zero_bind_advance(ctxs[3][0], tab, 4, st)
+        h = torch.zeros(z.ZERO_HYPER_BYTES, dtype=torch.uint8, pin_memory=True)
+        z.zero_prepare_step(ctxs[3][0], h, 1e-3, 0.9, 0.999, 1e-8, 1)
+        z.zero_advance_step(ctxs[3][0])
+    for c, _, _ in ctxs[1:]:
+        c.close()
 
 
 def test_prepared_step_protocol():

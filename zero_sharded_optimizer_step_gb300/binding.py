@@ -59,6 +59,8 @@ _SIGS = {
     "zero_bind_allreduce_out": (ctypes.c_int, [_ctxp, _vp]),
     "zero_set_weight_decay": (ctypes.c_int, [_ctxp, _f64]),
     "zero_bind_hyper": (ctypes.c_int, [_ctxp, _vp]),
+    "zero_hyper_slot": (ctypes.c_int, [_ctxp, ctypes.POINTER(_vp)]),
+    "zero_load_hyper": (ctypes.c_int, [_ctxp, _vp, _vp]),
     "zero_prepare_step": (ctypes.c_int, [_ctxp, _vp, _f64, _f64, _f64, _f64, _i64, _f32]),
     "zero_set_gather_mode": (ctypes.c_int, [_ctxp, _i32]),
     "zero_advance_table_bytes": (_i64, [_i64]),
@@ -274,6 +276,17 @@ def zero_gather_timeouts() -> int:
 
 def zero_bind_hyper(ctx, d_hyper) -> None:
     _check(_L.zero_bind_hyper(_h(ctx), _ptr(d_hyper)))
+
+
+def zero_load_hyper(ctx, host_block, stream=None) -> None:
+    _check(_L.zero_load_hyper(_h(ctx), _ptr(host_block), _stream(stream)))
+
+
+def zero_hyper_slot(ctx) -> int:
+    """Device address (int) of the context's constant slot for its scalar block."""
+    p = _vp()
+    _check(_L.zero_hyper_slot(_h(ctx), ctypes.byref(p)))
+    return int(p.value)
 
 
 def zero_prepare_step(ctx, host_hyper, lr: float, beta1: float, beta2: float, eps: float,

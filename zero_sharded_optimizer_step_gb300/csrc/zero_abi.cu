@@ -76,6 +76,10 @@ struct zero_ctx {
     int32_t gather_mode = 0;     // ZERO_GATHER_FAST or ZERO_GATHER_LEAN
 
     void *hyper = nullptr;       // device block of per-step scalars (graph capture)
+    int hyper_slot = -1;         // its constant-memory slot on hyper_device
+    int hyper_device = -1;
+    bool slot_stale = false;     // the step's first launch copies the block into the slot
+    bool hyper_direct = false;   // the bound block is the slot itself (no copy)
     const float *adv_table = nullptr;   // zero_bind_advance: bias corrections per t
     int64_t adv_tmax = 0;
     void *adv_state = nullptr;          // 32-byte device step state
@@ -223,6 +227,51 @@ Range unit_range(const zero_ctx *c, int32_t u)
     return r;
 }
 
+// Constant slots in use, per device.
+std::mutex g_slot_mu;
+std::vector<std::pair<int, unsigned>> g_slots_used;   // (device, bit mask of slots)
+
+int claim_slot(int dev)
+{
+    std::lock_guard<std::mutex> lock(g_slot_mu);
+    for (auto &e : g_slots_used)
+        if (e.first == dev) {
+            for (int k = 0; k < zgb::kHyperSlots; ++k)
+                if (!(e.second & (1u << k))) {
+                    e.second |= 1u << k;
+                    return k;
+                }
+            return -1;
+        }
+    g_slots_used.push_back({dev, 1u});
+    return 0;
+}
+
+void release_slot(int dev, int slot)
+{
+    if (slot < 0) return;
+    std::lock_guard<std::mutex> lock(g_slot_mu);
+    for (auto &e : g_slots_used)
+        if (e.first == dev) e.second &= ~(1u << slot);
+}
+
+// The first launch of a step in the graph form copies the context's device
+// block into its constant slot, on that launch's stream (so a captured step
+// holds the copy too).
+int load_slot_if_stale(zero_ctx *c, cudaStream_t s)
+{
+    if (!c->hyper || !c->slot_stale) return ZERO_OK;
+    if (c->hyper_direct) {            // the caller writes the slot itself
+        c->slot_stale = false;
+        return ZERO_OK;
+    }
+    const cudaError_t e =
+        zgb::load_hyper_slot(c->hyper_slot, static_cast<const zgb::DeviceHyper *>(c->hyper), s);
+    if (e != cudaSuccess) return cuda_fail(e, "copying the scalar block to its constant slot");
+    c->slot_stale = false;
+    return ZERO_OK;
+}
+
 StepArgs make_args(const zero_ctx *c, const Range &r, const void *const *grads)
 {
     StepArgs a;
@@ -246,6 +295,7 @@ StepArgs make_args(const zero_ctx *c, const Range &r, const void *const *grads)
     a.avg_align = r.grad_avg ? align_of(r.grad_avg) : 16;
     a.flag = reinterpret_cast<unsigned long long *>(c->flag);
     a.hyper = static_cast<const zgb::DeviceHyper *>(c->hyper);
+    a.slot = c->hyper_slot;
     bool ok = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16) &&
               (!a.g || aligned(a.g, 16)) &&
               (!a.cur || (aligned(a.xb, 16) && aligned(a.mb, 16) && aligned(a.vb, 16)));
@@ -269,6 +319,7 @@ int begin_step(zero_ctx *c, bool scaled)
         if (c->step_id == 0) return fail(ZERO_ESTATE, "call zero_prepare_step first");
         if (scaled != c->step_scaled)
             return fail(ZERO_EINVAL, "loss scaling differs from the prepared step");
+        c->slot_stale = true;
         return ZERO_OK;
     }
     c->step_id += 1;
@@ -287,6 +338,7 @@ int do_reduce(zero_ctx *c, const Range &r, const void *const *grads, float loss_
               cudaStream_t s)
 {
     if (r.n == 0) return ZERO_OK;
+    if (int rc = load_slot_if_stale(c, s)) return rc;
     StepArgs a = make_args(c, r, grads);
     a.av = average_scalars(c->world, loss_scale);
     a.step_id = c->step_id;
@@ -297,6 +349,7 @@ int do_apply(zero_ctx *c, const Range &r, double lr, double b1, double b2, doubl
              int64_t t, cudaStream_t s)
 {
     if (r.n == 0) return ZERO_OK;
+    if (int rc = load_slot_if_stale(c, s)) return rc;
     StepArgs a = make_args(c, r, nullptr);
     a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
     // an unscaled step never skips: use an id the flag cannot hold
@@ -307,6 +360,7 @@ int do_apply(zero_ctx *c, const Range &r, double lr, double b1, double b2, doubl
 int do_finalize(zero_ctx *c, const Range &r, cudaStream_t s)
 {
     if (r.n == 0 || !c->cur) return ZERO_OK;
+    if (int rc = load_slot_if_stale(c, s)) return rc;
     StepArgs a = make_args(c, r, nullptr);
     a.step_id = c->step_scaled ? c->step_id : ~0ull;
     return finish_launch(c, zgb::launch_finalize(c->pdt, a, c->sms, s), "finalize kernel", s);
@@ -317,6 +371,7 @@ int do_fused(zero_ctx *c, const Range &r, const void *const *grads, double lr, d
              bool finalize = true)
 {
     if (r.n == 0) return ZERO_OK;
+    if (int rc = load_slot_if_stale(c, s)) return rc;
     StepArgs a = make_args(c, r, grads);
     a.av = average_scalars(c->world, loss_scale);
     a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
@@ -517,6 +572,7 @@ int zero_init_dim0(zero_ctx **out, int32_t world, int32_t grad_dtype, int32_t pa
 
 int zero_destroy(zero_ctx *ctx)
 {
+    if (ctx) release_slot(ctx->hyper_device, ctx->hyper_slot);
     delete ctx;
     return ZERO_OK;
 }
@@ -647,8 +703,62 @@ int zero_bind_hyper(zero_ctx *c, void *d_hyper)
     if (!c) return fail(ZERO_EINVAL, "null context");
     static_assert(sizeof(zgb::DeviceHyper) <= ZERO_HYPER_BYTES, "hyper block too large");
     if (!aligned(d_hyper, 16)) return fail(ZERO_EALIGN, "the hyper block must be 16-byte aligned");
+    if (c->bucket_open || c->stage3_open) return fail(ZERO_ESTATE, "a step is open");
+    if (!d_hyper) {
+        release_slot(c->hyper_device, c->hyper_slot);
+        c->hyper_slot = -1;
+        c->hyper = nullptr;
+        c->hyper_direct = false;
+        return ZERO_OK;
+    }
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (c->hyper_slot < 0 || c->hyper_device != dev) {
+        release_slot(c->hyper_device, c->hyper_slot);
+        const int slot = claim_slot(dev);
+        if (slot < 0)
+            return fail(ZERO_ESTATE, "all %d constant slots of this device are bound to other "
+                                     "contexts' scalar blocks", zgb::kHyperSlots);
+        c->hyper_slot = slot;
+        c->hyper_device = dev;
+    }
+    void *slot_addr = nullptr;
+    e = zgb::hyper_slot_address(c->hyper_slot, &slot_addr);
+    if (e != cudaSuccess) return cuda_fail(e, "the address of the constant slot");
     c->hyper = d_hyper;
+    c->hyper_direct = d_hyper == slot_addr;
+    c->slot_stale = true;
     return ZERO_OK;
+}
+
+int zero_load_hyper(zero_ctx *c, const void *host_block, void *stream)
+{
+    if (!c || !host_block) return fail(ZERO_EINVAL, "null argument");
+    if (!c->hyper || !c->hyper_direct)
+        return fail(ZERO_ESTATE, "bind the constant slot (zero_hyper_slot) as the block first");
+    const cudaError_t e = cudaMemcpyAsync(c->hyper, host_block, sizeof(zgb::DeviceHyper),
+                                          cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "copying the scalar block to its slot");
+}
+
+int zero_hyper_slot(zero_ctx *c, void **d_slot)
+{
+    if (!c || !d_slot) return fail(ZERO_EINVAL, "null argument");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (c->hyper_slot < 0 || c->hyper_device != dev) {
+        if (c->hyper) return fail(ZERO_ESTATE, "a block is bound on another device");
+        const int slot = claim_slot(dev);
+        if (slot < 0)
+            return fail(ZERO_ESTATE, "all %d constant slots of this device are in use",
+                        zgb::kHyperSlots);
+        c->hyper_slot = slot;
+        c->hyper_device = dev;
+    }
+    e = zgb::hyper_slot_address(c->hyper_slot, d_slot);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "the address of the constant slot");
 }
 
 int zero_prepare_step(zero_ctx *c, void *host_hyper, double lr, double b1, double b2,
@@ -728,6 +838,9 @@ int zero_advance_step(zero_ctx *c, void *stream)
     if (rc) return rc;
     if (!c->hyper) return fail(ZERO_ESTATE, "no device scalar block bound (zero_bind_hyper)");
     if (!c->adv_state) return fail(ZERO_ESTATE, "no device step state bound (zero_bind_advance)");
+    if (c->hyper_direct)
+        return fail(ZERO_ESTATE, "the device advance rewrites the bound block: bind a block in "
+                                 "device memory, not the constant slot");
     if (c->step_id == 0) return fail(ZERO_ESTATE, "prepare the first step (zero_prepare_step)");
     if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
     if (c->stage3_open) return fail(ZERO_ESTATE, "a stage-3 step is open (zero3_end_step)");
@@ -946,6 +1059,7 @@ int zero3_begin_step_scaled(zero_ctx *c, float loss_scale)
         if (c->step_id == 0) return fail(ZERO_ESTATE, "call zero_prepare_step first");
         if (scaled && !c->step_scaled)
             return fail(ZERO_EINVAL, "loss scaling differs from the prepared step");
+        c->slot_stale = true;
     } else {
         c->step_id += 1;
         c->step_scaled = scaled;
@@ -1221,6 +1335,7 @@ extern "C" int zero_step_noalloc(zero_ctx *c, const void *const *grads, int32_t 
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = begin_step(c, loss_scale > 0.0f))) return rc;
     if (r.n == 0) return ZERO_OK;
+    if ((rc = load_slot_if_stale(c, s))) return rc;
 
     StepArgs a = make_args(c, r, grads);
     a.g = scratch;    // every element of the range is written by the reduce pass first

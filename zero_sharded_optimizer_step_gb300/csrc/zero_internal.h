@@ -72,7 +72,8 @@ struct StepArgs {
     unsigned long long *cur;
     unsigned long long *flag;      // id of the latest step with a non-finite grad
     unsigned long long step_id;
-    const DeviceHyper *hyper;      // when set, ad/av/step_id come from here
+    const DeviceHyper *hyper;      // when set, ad/av/step_id come from constant slot `slot`,
+    int32_t slot;                  // a copy of this block made at the step's first launch
     AverageScalars av;
     AdamScalars ad;
 };
@@ -99,6 +100,15 @@ struct GatherRowsArgs {
     int32_t n;                     // rows
     int32_t es;
 };
+
+// Constant-memory slots holding the device scalar blocks of the contexts in
+// the graph form (one slot per bound block and device): the step kernels read
+// their scalars there as constant-bank operands, as eager launches read their
+// parameters.  load_hyper_slot copies a block into its slot on `s`.
+constexpr int kHyperSlots = 8;
+cudaError_t load_hyper_slot(int slot, const DeviceHyper *block, cudaStream_t s);
+// Device address of a slot (a caller may copy its block straight there).
+cudaError_t hyper_slot_address(int slot, void **addr);
 
 // Blocks of `threads` threads of `kernel` that fit on one SM of the current
 // device (cached per kernel and device; at least 1).

@@ -286,9 +286,11 @@ __device__ __forceinline__ void publish_flag(const StepArgs &a, bool bad, unsign
 
 // The step's scalars.  An eager launch reads them straight from the kernel's
 // parameters (constant-bank operands: no registers held across the loop).  A
-// step captured in a CUDA graph (HYPER) reads them from the device block
-// written before its kernels run.  The choice is a template argument, so
-// the eager kernels carry neither a branch nor a copy of the scalars.
+// step in the graph form (HYPER) reads them from the context's constant
+// slot, into which the step's first launch copied the device block.  The
+// choice is a template argument, so the eager kernels carry neither a branch
+// nor a copy of the scalars.
+__constant__ DeviceHyper c_hyper_slots[kHyperSlots];
 template <bool HYPER>
 struct ScalarRefs {
     const AdamScalars &ad;
@@ -299,10 +301,10 @@ struct ScalarRefs {
 template <bool HYPER>
 __device__ __forceinline__ ScalarRefs<HYPER> step_scalars(const StepArgs &a, bool publishing)
 {
-    if constexpr (HYPER)
-        return ScalarRefs<HYPER>{a.hyper->ad, a.hyper->av,
-                                 publishing ? a.hyper->flag_id : a.hyper->skip_id};
-    else
+    if constexpr (HYPER) {
+        const DeviceHyper &h = c_hyper_slots[a.slot];
+        return ScalarRefs<HYPER>{h.ad, h.av, publishing ? h.flag_id : h.skip_id};
+    } else
         return ScalarRefs<HYPER>{a.ad, a.av, a.step_id};
 }
 
@@ -332,17 +334,12 @@ __device__ __forceinline__ StatePtrs select_state(const StepArgs &a, bool fresh)
 // per-thread chunk); two with fp32 grads, whose eight-element vectors need
 // twice the load registers.
 template <int GT> struct MinBlocks { static constexpr int value = GT == F32 ? 2 : 4; };
-// The fused kernel of a graph-captured step holds its scalars in registers
-// (they come from memory, not the constant bank): three blocks per SM leave
-// it room enough not to spill, which measured faster than four that spill.
-template <int GT, bool HYPER> struct MinBlocksFused {
-    static constexpr int value = HYPER && GT != F32 ? 3 : MinBlocks<GT>::value;
-};
+
 
 // ---------------------------------------------------------------- kernels
 
 template <int GT, int PT, bool AVG, bool HYPER>
-__global__ void __launch_bounds__(kThreads, MinBlocksFused<GT, HYPER>::value)
+__global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
 fused_step_kernel(const __grid_constant__ StepArgs a)
 {
     pdl_wait();                 // the previous kernel in the stream is done
@@ -487,7 +484,7 @@ finalize_kernel(const __grid_constant__ StepArgs a)
 {
     pdl_wait();                 // the previous kernel in the stream is done
     pdl_launch_dependents();
-    const unsigned long long skip_id = a.hyper ? a.hyper->skip_id : a.step_id;
+    const unsigned long long skip_id = a.hyper ? c_hyper_slots[a.slot].skip_id : a.step_id;
     const bool overflowed =
         *reinterpret_cast<volatile unsigned long long *>(a.flag) == skip_id;
     if (!overflowed) {
@@ -511,6 +508,28 @@ finalize_kernel(const __grid_constant__ StepArgs a)
 }
 
 // ------------------------------------------------------------- launching
+
+}  // namespace
+
+cudaError_t hyper_slot_address(int slot, void **addr)
+{
+    if (slot < 0 || slot >= kHyperSlots) return cudaErrorInvalidValue;
+    void *base = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&base, c_hyper_slots);
+    if (e != cudaSuccess) return e;
+    *addr = static_cast<char *>(base) + (size_t)slot * sizeof(DeviceHyper);
+    return cudaSuccess;
+}
+
+cudaError_t load_hyper_slot(int slot, const DeviceHyper *block, cudaStream_t s)
+{
+    if (slot < 0 || slot >= kHyperSlots) return cudaErrorInvalidValue;
+    return cudaMemcpyToSymbolAsync(c_hyper_slots, block, sizeof(DeviceHyper),
+                                   (size_t)slot * sizeof(DeviceHyper), cudaMemcpyDeviceToDevice,
+                                   s);
+}
+
+namespace {
 
 template <typename K>
 cudaError_t launch(K kernel, const StepArgs &a, int64_t work_items, int sms, cudaStream_t s)
