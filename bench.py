@@ -48,9 +48,9 @@ import numpy as np  # noqa: E402
 # one pass; summarised under profiles/).  Each entry is valid only for the
 # kernel source it was taken on (sha256 prefix); otherwise bench reports null.
 TRAFFIC = {
-    ("gpt2_xl", "fused_step_kernel"): ("a5b9a674470ff3d3", 68.537e9 + 21.777e9),
+    ("gpt2_xl", "fused_step_kernel"): ("02f54cd48e586eae", 68.538e9 + 21.776e9),
     ("one_rank_7p5b", "gather_kernel"): ("8285f3d7f2dee1cb", 14.787e9 + 14.724e9),
-    ("one_rank_7p5b", "fused_step_kernel"): ("a5b9a674470ff3d3", 16.407e9 + 1.621e9),
+    ("one_rank_7p5b", "fused_step_kernel"): ("02f54cd48e586eae", 16.407e9 + 1.621e9),
     # means of two full-size launches; part of each launch's writes is still
     # in L2 when it ends
     ("zero3_llama7b", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.83e6 + 350.27e6),
