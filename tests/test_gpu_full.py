@@ -194,3 +194,37 @@ def test_zero3_prefetch_full():
             assert torch.equal(last[k * Su:(k + 1) * Su], run.shards[0][k])
     assert z.zero_gather_timeouts() == before
     run.close()
+
+
+@pytest.mark.parametrize("shadow", [False, True])
+def test_past_2p31_elements(shadow):
+    """A flat vector longer than 2^31 elements, 3 ranks (S = 715,831,998,
+    one pad element), bf16 grads, fp16 params, loss
+    scale 2^10.  Iteration 2 carries one +inf in rank 1 at position
+    2^31 + 7, past every 32-bit index: the flag must see it and skip that
+    step.  The oracle is sampled around 2^31 and at every shard edge."""
+    w = W.Workload("past_2p31", (1 << 31) + 12_345, 3, 2, W.BF16, W.F16, steps=3,
+                   loss_scale=2.0 ** 10)
+    from workloads.runner import Runner
+    run = Runner(w, shadow=shadow)
+    e = (1 << 31) + 7
+    for it in range(1, w.steps + 1):
+        run.fill_grads(it)
+        if it == 2:
+            run.grads[0][1][e] = float("inf")
+        run.launch_step()
+        run.finish_step()
+    torch.cuda.synchronize()
+    assert run.skips == [False, True, False]
+    assert run.scale == 2.0 ** 9 and run.t == 2
+    S = w.shard
+    P = S * w.world
+    assert S == 715_831_998 and P - w.numel == 1
+    near = np.arange((1 << 31) - 4096, (1 << 31) + 4096, dtype=np.int64)
+    idx = np.unique(np.concatenate([sample_positions(P, S, n_rand=1 << 18), near]))
+    check_sampled(run, w, idx, skipped=(2,))
+    # the pad element stays exactly +0 in every buffer
+    cx, cm, cv = run.state()
+    for t in (cx, cm, cv, run.params):
+        assert gpu_at(t, np.array([P - 1])).tobytes() == bytes(t.element_size())
+    run.close()
