@@ -57,6 +57,13 @@ TRAFFIC = {
     # the same gathers (2-byte params, the same shard sizes)
     ("zero3_llama7b_fp16", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.83e6 + 350.27e6),
     ("fsdp2_llama7b", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.79e6 + 347.49e6),
+    ("gpt2_small", "fused_step_kernel"): ("02f54cd48e586eae", 3.4844e9 + 1.6928e9),
+    ("gpt2_small_stage1", "fused_step_kernel"): ("02f54cd48e586eae", 3.4844e9 + 1.9533e9),
+    # the two-pass loss-scaled step (--two-pass): its first, larger kernel
+    ("gpt2_xl", "reduce_kernel"): ("02f54cd48e586eae", 49.845e9 + 6.2157e9),
+    # mean over the 28 gathers of one step; the units' full buffers (14 to
+    # 79 MB) mostly stay in L2, so most of the writes never reach DRAM
+    ("zero3_gpt2_small", "gather_kernel"): ("8285f3d7f2dee1cb", 17.793e6 + 1.9387e6),
 }
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
                           "zero_step_kernels.cu")
