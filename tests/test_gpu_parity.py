@@ -1224,3 +1224,86 @@ def test_device_advance_stops_when_the_table_runs_out():
             assert status == 1 and t == 3
             assert torch.equal(d.cpu(), before)
     run.close()
+
+
+def _direct_step_case(grads_h, gdt, pdt, scale, x0, steps, shadow):
+    """Steps the same host grads through zero_step (all ranks) and through
+    the oracle; returns the GPU verdicts and asserts bit-identity."""
+    import zero_sharded_optimizer_step_gb300 as z
+    dev = torch.device("cuda:0")
+    world, numel = len(grads_h), grads_h[0].size
+    c = z.zero_init(numel, world, 2, gdt, pdt, -1)
+    P = z.zero_ctx_state_elems(c)
+    xh = np.zeros(P, np.float32)
+    xh[:numel] = x0
+    mh, vh = np.zeros(P, np.float32), np.zeros(P, np.float32)
+    ph = np.zeros(P, STORAGE[pdt])
+    ph[:] = oracle.cast(xh, pdt)
+    tdt = {W.F32: torch.float32, W.BF16: torch.bfloat16, W.F16: torch.float16}
+    master = torch.from_numpy(xh.copy()).to(dev)
+    m, v = torch.zeros(P, device=dev), torch.zeros(P, device=dev)
+    params = torch.from_numpy(ph.copy().view(np.int16) if pdt != W.F32 else ph.copy()).to(dev)
+    if pdt != W.F32:
+        params = params.view(tdt[pdt])
+    flag = torch.zeros(1, dtype=torch.int64, device=dev)
+    scratch = None if shadow else torch.zeros(P, device=dev)
+    z.zero_bind(c, master, m, v, params, scratch, flag)
+    if shadow:
+        sh = (master.clone(), torch.zeros(P, device=dev), torch.zeros(P, device=dev),
+              torch.zeros(1, dtype=torch.int64, device=dev))
+        z.zero_bind_shadow(c, *sh)
+    gd = []
+    for g in grads_h:
+        t = torch.from_numpy(g.view(np.int16) if gdt != W.F32 else g).to(dev)
+        gd.append(t.view(tdt[gdt]) if gdt != W.F32 else t)
+    verdicts, t = [], 0
+    for _ in range(steps):
+        z.zero_step(c, gd, 1e-3, 0.9, 0.999, 1e-8, t + 1, scale)
+        _, skipped = z.zero_step_status(c)
+        o_skip, _ = oracle.zero_step(grads_h, gdt, numel, xh, mh, vh, ph, pdt, 1e-3, 0.9, 0.999,
+                                     1e-8, t + 1, loss_scale=scale)
+        assert skipped == o_skip
+        verdicts.append(skipped)
+        t += 0 if skipped else 1
+    cur = z.zero_current_state(c) if shadow else 0
+    cx, cm, cv = (sh[:3] if cur == 1 else (master, m, v))
+    for name, a, b in [("master", to_np(cx), xh), ("m", to_np(cm), mh), ("v", to_np(cv), vh)]:
+        assert_bit_identical(a, b, oracle.F32, name)
+    assert_bit_identical(to_np(params), ph, pdt, "params")
+    c.close()
+    return verdicts
+
+
+@pytest.mark.parametrize("shadow", [False, True])
+def test_loss_scale_edge_values(shadow):
+    """(1) A loss scale that is not a power of two (3000): the unscale is a
+    true division on both sides.  (2) A scale of 2^-8 (allowed: its inverse
+    is normal) with finite sums near 2^120: the sum is finite but the
+    unscaled grad overflows, and the step is skipped.  (3) bf16 grads of
+    2^127 in every rank: each is finite, their fp32 sum is not, and the step
+    is skipped.  Each against the oracle, bit for bit."""
+    rng = np.random.default_rng(7)
+    n, world = 70_001, 4
+    x0 = synth.fill_host(n, synth.F32, synth.key(3, synth.KIND_MASTER), 0.01)
+
+    def draws(scale, dtype):
+        return [synth.fill_host(n, dtype, synth.key(3, synth.KIND_GRAD, 1, k), 1e-3 * scale)
+                for k in range(world)]
+
+    # (1) non-power-of-two scale, fp16 grads: applied, division path
+    g = draws(3000.0, W.F16)
+    assert _direct_step_case(g, W.F16, W.F16, 3000.0, x0, 2, shadow) == [False, False]
+    # (2) scale 2^-8: one element's sum ~2^121 is finite, /N then *2^8 overflows
+    g = [a.copy() for a in draws(1.0, W.F32)]
+    e = int(rng.integers(0, n))
+    for k in range(world):
+        g[k][e] = np.float32(2.0 ** 120)
+    assert _direct_step_case(g, W.F32, W.BF16, 2.0 ** -8, x0, 1, shadow) == [True]
+    # the same grads at scale 1 are applied (2^122 / 4 is finite)
+    assert _direct_step_case(g, W.F32, W.BF16, 1.0, x0, 1, shadow) == [False]
+    # (3) bf16 grads 2^127 in every rank at one position: the fp32 sum overflows
+    g = [a.copy() for a in draws(2.0 ** 10, W.BF16)]
+    big = oracle.cast(np.array([2.0 ** 127], np.float32), W.BF16)[0]
+    for k in range(world):
+        g[k][e] = big
+    assert _direct_step_case(g, W.BF16, W.BF16, 2.0 ** 10, x0, 1, shadow) == [True]

@@ -170,6 +170,53 @@ def test_unscaled_step_is_the_scaled_step_divided():
     assert xa.tobytes() == xb.tobytes() and fa.tobytes() == fb.tobytes()
 
 
+def test_overflow_verdict_is_taken_on_the_unscaled_mean():
+    """The verdict tests the grad the update would use (sum, /N, /scale),
+    so it follows from IEEE binary32 range alone: a finite sum whose
+    unscale leaves the range skips (scale 2^-8), the same sum at scale 1
+    does not, finite bf16 grads whose fp32 sum leaves the range skip, and
+    a non-power-of-two scale divides (the step at scale 3000 on grads
+    3000 g equals the plain step on g wherever the unscaled mean comes back
+    exactly)."""
+    psi, n = 64, 4
+    S = oracle.shard_size(psi, n)
+    P = n * S
+
+    def step(grads, gdt, scale):
+        x = np.zeros(P, np.float32)
+        x[:psi] = 0.5
+        m, v = np.zeros(P, np.float32), np.zeros(P, np.float32)
+        full = np.zeros(P, np.uint16)
+        skipped, bad = oracle.zero_step(grads, gdt, psi, x, m, v, full, BF16, 1e-3, 0.9,
+                                        0.999, 1e-8, 1, loss_scale=scale)
+        return skipped, bad, x
+
+    g = [np.full(psi, 1e-3, np.float32) for _ in range(n)]
+    for a in g:
+        a[9] = 2.0 ** 120                      # sum 2^122: finite
+    assert step(g, F32, 2.0 ** -8)[:2] == (True, 1)      # 2^120 * 2^8 = 2^128: inf
+    assert step(g, F32, 1.0)[:2] == (False, 0)
+    assert step(g, F32, 2.0 ** -2)[:2] == (False, 0)      # 2^122: still finite
+    big = [oracle.cast(np.full(psi, 1e-3, np.float32), BF16) for _ in range(n)]
+    for a in big:
+        a[17] = oracle.cast(np.array([2.0 ** 127], np.float32), BF16)[0]
+    assert step(big, BF16, 2.0 ** 10)[:2] == (True, 1)   # 2^127 + 2^127 = inf in fp32
+    base = [np.float32(1e-3) * np.arange(1, psi + 1, dtype=np.float32) for _ in range(n)]
+    scaled = [a * np.float32(3000.0) for a in base]
+    s1, _, x1 = step(base, F32, 0.0)
+    s2, _, x2 = step(scaled, F32, 3000.0)
+    assert not s1 and not s2
+    # wherever the scaled mean divides back to the plain mean exactly, the
+    # two steps agree element for element
+    acc1, acc2 = base[0].copy(), scaled[0].copy()
+    for a, b in zip(base[1:], scaled[1:]):
+        acc1 = acc1 + a
+        acc2 = acc2 + b
+    sums_ok = ((acc2 / np.float32(n)) / np.float32(3000.0)) == (acc1 / np.float32(n))
+    assert sums_ok.sum() > psi // 2
+    assert (x1[:psi][sums_ok] == x2[:psi][sums_ok]).all()
+
+
 def test_without_loss_scaling_nan_propagates():
     """Loss scaling off: no skip; a non-finite grad is reported and reaches
     the state of its element only."""

@@ -28,6 +28,11 @@ MUTANTS = [
     ("shards placed one slot late", "memcpy((char *)full + ((int64_t)r * S + j) * es,",
      "memcpy((char *)full + ((int64_t)((r + 1) % world) * S + j) * es,"),
     ("overflow never skips", "if (loss_scale > 0.0f && bad > 0) return 1;", "if (0) return 1;"),
+    ("overflow tested before the unscale",
+     "        if (loss_scale > 0.0f) x = x / loss_scale;\n        g[j] = x;\n"
+     "        if (!isfinite(x)) ++bad;",
+     "        if (!isfinite(x)) ++bad;\n        if (loss_scale > 0.0f) x = x / loss_scale;\n"
+     "        g[j] = x;"),
     ("last rank left out of the sum",
      "for (int32_t k = 1; k < world; ++k) a = a + widen(grads[k], dtype, i);",
      "for (int32_t k = 1; k < world - 1; ++k) a = a + widen(grads[k], dtype, i);"),
