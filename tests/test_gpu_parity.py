@@ -1307,3 +1307,21 @@ def test_loss_scale_edge_values(shadow):
     for k in range(world):
         g[k][e] = big
     assert _direct_step_case(g, W.BF16, W.BF16, 2.0 ** 10, x0, 1, shadow) == [True]
+
+
+@pytest.mark.parametrize("pdt", [W.F32, W.BF16, W.F16])
+def test_subnormals_are_kept(pdt):
+    """No flush to zero anywhere: fp32 grads around 1e-20 make g*g and v
+    subnormal (about 1e-43), and masters around 1e-39 are subnormal fp32
+    (and bf16) values that the cast must round, not flush.  Bit-identical
+    to the oracle, which runs on the host FPU with subnormals."""
+    n, world = 50_001, 3
+    x0 = synth.fill_host(n, synth.F32, synth.key(5, synth.KIND_MASTER), 0.01)
+    tiny = synth.fill_host(n, synth.F32, synth.key(5, synth.KIND_MASTER, 1), 1e-39)
+    x0[::3] = tiny[::3]
+    g = [synth.fill_host(n, W.F32, synth.key(5, synth.KIND_GRAD, 1, k), 1e-20)
+         for k in range(world)]
+    assert (np.abs(x0[::3]) < np.finfo(np.float32).tiny).mean() > 0.9
+    sq = g[0].astype(np.float32) * g[0].astype(np.float32)
+    assert ((sq != 0) & (np.abs(sq) < np.finfo(np.float32).tiny)).mean() > 0.5
+    assert _direct_step_case(g, W.F32, pdt, 0.0, x0, 3, False) == [False] * 3
