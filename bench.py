@@ -36,6 +36,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -92,6 +93,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the nvidia-smi samples taken during the timed region here")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--two-pass", action="store_true",
                     help="loss-scaled workloads: the scratch-based two-pass step instead of the "
@@ -124,14 +127,20 @@ class Clocks:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, keep=None):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+        self.keep = keep        # a path to keep the raw samples at, or None
+        self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            if self.keep:
+                self.path = self.keep
+                os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
+            else:
+                fd, self.path = tempfile.mkstemp(prefix="bench_clocks_", suffix=".csv")
+                os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
                                           "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
@@ -139,6 +148,10 @@ class Clocks:
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            if getattr(self, "f", None):
+                self.f.close()
+            if self.path and not self.keep and os.path.exists(self.path):
+                os.unlink(self.path)
 
     def stop(self):
         if not self.proc:
@@ -153,19 +166,22 @@ class Clocks:
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for ln in f:
-                parts = [p.strip() for p in ln.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    s, m = float(parts[1]), float(parts[2])
-                except ValueError:
-                    continue
-                sm.append(s)
-                mx.append(m)
-                for nm, val in zip(names, parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(nm)
+            lines = f.readlines()
+        if not self.keep:
+            os.unlink(self.path)
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                s, m = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            sm.append(s)
+            mx.append(m)
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
         if not sm:
             return None
         loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
@@ -372,7 +388,7 @@ def bench_ours(args, rank, world_size, device_index):
 
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in plan] for _ in range(args.steps)]
-    clocks = Clocks(device_index)
+    clocks = Clocks(device_index, args.clocks_csv)
     barrier(world_size)
     torch.cuda.synchronize()
     clocks.start()
