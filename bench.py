@@ -59,6 +59,9 @@ TRAFFIC = {
     ("zero3_llama7b_fp16", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.83e6 + 350.27e6),
     ("fsdp2_llama7b", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.79e6 + 347.49e6),
     ("gpt2_small", "fused_step_kernel"): ("02f54cd48e586eae", 3.4844e9 + 1.6928e9),
+    ("gpt2_xl_adamw", "fused_step_kernel"): ("02f54cd48e586eae", 68.537e9 + 21.780e9),
+    # mean over the 47 bucket launches of one step
+    ("gpt2_xl_bucketed", "fused_step_kernel"): ("02f54cd48e586eae", 1.45832e9 + 0.43176e9),
     ("gpt2_small_stage1", "fused_step_kernel"): ("02f54cd48e586eae", 3.4844e9 + 1.9533e9),
     # the two-pass loss-scaled step (--two-pass): its first, larger kernel
     ("gpt2_xl", "reduce_kernel"): ("02f54cd48e586eae", 49.845e9 + 6.2157e9),
