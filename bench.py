@@ -50,14 +50,14 @@ import numpy as np  # noqa: E402
 # kernel source it was taken on (sha256 prefix); otherwise bench reports null.
 TRAFFIC = {
     ("gpt2_xl", "fused_step_kernel"): ("02f54cd48e586eae", 68.538e9 + 21.776e9),
-    ("one_rank_7p5b", "gather_kernel"): ("8285f3d7f2dee1cb", 14.787e9 + 14.724e9),
+    ("one_rank_7p5b", "gather_kernel"): ("5ad5f8b67603e427", 14.788e9 + 14.724e9),
     ("one_rank_7p5b", "fused_step_kernel"): ("02f54cd48e586eae", 16.407e9 + 1.621e9),
     # means of two full-size launches; part of each launch's writes is still
     # in L2 when it ends
-    ("zero3_llama7b", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.83e6 + 350.27e6),
+    ("zero3_llama7b", "gather_rows_kernel"): ("5ad5f8b67603e427", 404.79e6 + 349.72e6),
     # the same gathers (2-byte params, the same shard sizes)
-    ("zero3_llama7b_fp16", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.83e6 + 350.27e6),
-    ("fsdp2_llama7b", "gather_rows_kernel"): ("8285f3d7f2dee1cb", 404.79e6 + 347.49e6),
+    ("zero3_llama7b_fp16", "gather_rows_kernel"): ("5ad5f8b67603e427", 404.79e6 + 350.47e6),
+    ("fsdp2_llama7b", "gather_rows_kernel"): ("5ad5f8b67603e427", 404.79e6 + 347.54e6),
     ("gpt2_small", "fused_step_kernel"): ("02f54cd48e586eae", 3.4844e9 + 1.6928e9),
     ("gpt2_xl_adamw", "fused_step_kernel"): ("02f54cd48e586eae", 68.537e9 + 21.780e9),
     # mean over the 47 bucket launches of one step
@@ -67,7 +67,7 @@ TRAFFIC = {
     ("gpt2_xl", "reduce_kernel"): ("02f54cd48e586eae", 49.845e9 + 6.2157e9),
     # mean over the 28 gathers of one step; the units' full buffers (14 to
     # 79 MB) mostly stay in L2, so most of the writes never reach DRAM
-    ("zero3_gpt2_small", "gather_kernel"): ("8285f3d7f2dee1cb", 17.793e6 + 1.9387e6),
+    ("zero3_gpt2_small", "gather_kernel"): ("5ad5f8b67603e427", 17.794e6 + 1.9392e6),
 }
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
                           "zero_step_kernels.cu")

@@ -438,6 +438,15 @@ int zero_set_gather_mode(zero_ctx *ctx, int32_t mode);
  * streams are synchronized. */
 int zero_gather_timeouts(uint32_t *count);
 
+/* How many times the lean gather polls for each tile's load before it gives
+ * up on that gather (the drain of the loads in flight after a give-up always
+ * polls for the full default).  polls >= 0 sets the limit -- 0 makes every
+ * such wait run out at once, which exercises the timeout path without a
+ * fault; polls < 0 restores the default (2^22 polls, seconds at the least).
+ * Process-wide; synchronous; call it only while no lean gather is in flight.
+ * Returns ZERO_OK, or ZERO_ECUDA when the device variable cannot be set. */
+int zero_set_gather_wait_polls(int64_t polls);
+
 /* ------------------------------------------------------------- stage 3 */
 
 /* Begin a stage-3 step: the units' calls until the next begin share one

@@ -584,6 +584,46 @@ def test_lean_gather_placement(S, world, dtype, src_off, dst_off):
     assert z.zero_gather_timeouts() == before
 
 
+def test_lean_gather_wait_that_runs_out_is_reported():
+    """The lean gather's bounded waits, made to run out on purpose (a poll
+    limit of 0: no fault, no hang): every CTA with work gives up at its
+    first tile, drains the loads it issued and places nothing; the counter
+    reports it (ZERO_ETIMEOUT); with the default limit restored the same
+    context places bit-exactly again."""
+    import zero_sharded_optimizer_step_gb300 as z
+    dev = torch.device("cuda:0")
+    S, world, dtype = 250_000, 4, W.BF16
+    hs = [synth.fill_host(S, dtype, synth.key(10, W.KIND_SHARD, 0, k), 1.0) for k in range(world)]
+    shards = [torch.from_numpy(h.view(np.int16)).to(dev).view(torch.bfloat16) for h in hs]
+    ctx = z.zero_init(S * world, world, 3, dtype, dtype, 0, [S * world])
+    z.zero_set_gather_mode(ctx, z.ZERO_GATHER_LEAN)
+    st = torch.zeros(S, device=dev)
+    z.zero_bind(ctx, st, st, st, torch.zeros(S, dtype=torch.bfloat16, device=dev), None,
+                torch.zeros(1, dtype=torch.int64, device=dev))
+    z.zero3_begin_step(ctx)
+    full = torch.full((S * world,), 7.0, dtype=torch.bfloat16, device=dev)
+    sentinel = to_np(full).tobytes()
+    before = z.zero_gather_timeouts()
+    try:
+        z.zero_set_gather_wait_polls(0)
+        z.zero3_gather_unit(ctx, 0, shards, full)
+        torch.cuda.synchronize()
+        ran_out = z.zero_gather_timeouts() - before
+    finally:
+        z.zero_set_gather_wait_polls(-1)
+    assert ran_out >= 1
+    assert to_np(full).tobytes() == sentinel           # nothing was placed
+    import ctypes
+    from zero_sharded_optimizer_step_gb300 import binding as zb
+    c = ctypes.c_uint32(0)
+    assert zb._L.zero_gather_timeouts(ctypes.byref(c)) == z.ZERO_ETIMEOUT
+    after = z.zero_gather_timeouts()
+    z.zero3_gather_unit(ctx, 0, shards, full)
+    torch.cuda.synchronize()
+    assert to_np(full).tobytes() == oracle.all_gather(hs, dtype).tobytes()
+    assert z.zero_gather_timeouts() == after
+
+
 # -------------------------------------------------- FSDP2's dim-0 layout
 
 @pytest.mark.parametrize("rank,scaled", [(1, False), (-1, False), (3, True), (0, False)])

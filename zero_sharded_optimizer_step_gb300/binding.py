@@ -69,6 +69,7 @@ _SIGS = {
     "zero_bind_advance": (ctypes.c_int, [_ctxp, _vp, _i64, _vp]),
     "zero_advance_step": (ctypes.c_int, [_ctxp, _vp]),
     "zero_gather_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "zero_set_gather_wait_polls": (ctypes.c_int, [ctypes.c_int64]),
     "zero_bind_shadow": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp]),
     "zero_current_state": (ctypes.c_int, [_ctxp, ctypes.POINTER(_i32)]),
     "zero_step": (ctypes.c_int, [_ctxp, _vpp, _i32, _f64, _f64, _f64, _f64, _i64, _f32, _vp]),
@@ -272,6 +273,12 @@ def zero_gather_timeouts() -> int:
     if rc != ZERO_ETIMEOUT:
         _check(rc)
     return int(c.value)
+
+
+def zero_set_gather_wait_polls(polls: int) -> None:
+    """Polls of the lean gather's first wait on each tile; 0 makes the waits
+    run out (a test of the timeout path), < 0 restores the default."""
+    _check(_L.zero_set_gather_wait_polls(polls))
 
 
 def zero_bind_hyper(ctx, d_hyper) -> None:

@@ -689,6 +689,13 @@ int zero_gather_timeouts(uint32_t *count)
     return h ? ZERO_ETIMEOUT : ZERO_OK;
 }
 
+int zero_set_gather_wait_polls(int64_t polls)
+{
+    cudaError_t e = zgb::set_lean_first_wait_polls((long long)polls);
+    if (e != cudaSuccess) return cuda_fail(e, "setting the lean gather's wait limit");
+    return ZERO_OK;
+}
+
 int zero_set_weight_decay(zero_ctx *c, double weight_decay)
 {
     if (!c) return fail(ZERO_EINVAL, "null context");

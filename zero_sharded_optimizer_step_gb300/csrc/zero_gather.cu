@@ -148,15 +148,18 @@ constexpr int kTmaStages = 4;
 constexpr long long kWaitPolls = 1ll << 22;
 
 __device__ unsigned int g_gather_timeouts;
+// Polls of the first wait on each tile's load (the drain after a timeout
+// always takes kWaitPolls).  Lowered only to exercise the timeout path.
+__device__ long long g_first_wait_polls = kWaitPolls;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long polls)
 {
-    for (long long i = 0; i < kWaitPolls; ++i) {
+    for (long long i = 0; i < polls; ++i) {
         uint32_t done;
         asm volatile("{\n .reg .pred p;\n"
                      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -206,6 +209,7 @@ lean_gather_kernel(const __grid_constant__ LeanArgs a)
 
     const int64_t total = a.first_tile[a.rows];
     const int64_t G = gridDim.x;
+    const long long first_polls = g_first_wait_polls;
     auto tile_of = [&](int64_t m, const char *&src, char *&dst, uint32_t &bytes) -> bool {
         const int64_t t = blockIdx.x + m * G;
         if (t >= total) return false;
@@ -235,7 +239,7 @@ lean_gather_kernel(const __grid_constant__ LeanArgs a)
     for (; m < issued; ++m) {
         const int s = (int)(m % kTmaStages);
         const uint32_t parity = (uint32_t)((m / kTmaStages) & 1);
-        if (!mbar_wait(smem_addr(&bars[s]), parity)) { ok = false; break; }
+        if (!mbar_wait(smem_addr(&bars[s]), parity, first_polls)) { ok = false; break; }
         const char *src; char *dst; uint32_t bytes;
         tile_of(m, src, dst, bytes);
         tma_store(dst, ring0 + (uint32_t)(s * kTmaTile), bytes);
@@ -252,7 +256,7 @@ lean_gather_kernel(const __grid_constant__ LeanArgs a)
         // drain: every load still in flight must land before the ring goes away
         for (int64_t k = m; k < issued; ++k) {     // tile m's own load included
             const int s = (int)(k % kTmaStages);
-            if (!mbar_wait(smem_addr(&bars[s]), (uint32_t)((k / kTmaStages) & 1)))
+            if (!mbar_wait(smem_addr(&bars[s]), (uint32_t)((k / kTmaStages) & 1), kWaitPolls))
                 atomicAdd(&g_gather_timeouts, 1u);
         }
     }
@@ -397,6 +401,12 @@ cudaError_t launch_gather_rows_lean(const GatherRowsArgs &a, int sms, cudaStream
 cudaError_t lean_gather_timeouts(unsigned int *count)
 {
     return cudaMemcpyFromSymbol(count, g_gather_timeouts, sizeof(unsigned int));
+}
+
+cudaError_t set_lean_first_wait_polls(long long polls)
+{
+    const long long v = polls < 0 ? kWaitPolls : polls;
+    return cudaMemcpyToSymbol(g_first_wait_polls, &v, sizeof v);
 }
 
 }  // namespace zgb

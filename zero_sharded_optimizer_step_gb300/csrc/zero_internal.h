@@ -177,5 +177,6 @@ cudaError_t launch_advance(DeviceHyper *hyper, const unsigned long long *flag, A
                            const float *table, int64_t t_max, cudaStream_t s);
 // Waits of the lean gather that ran out (cumulative, this process).
 cudaError_t lean_gather_timeouts(unsigned int *count);
+cudaError_t set_lean_first_wait_polls(long long polls);
 
 }  // namespace zgb
