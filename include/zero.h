@@ -67,6 +67,10 @@
  *   - Device pointers must be aligned to their element size.  16-byte
  *     alignment is not required: unaligned buffers take slower but correct
  *     paths.
+ *   - Hyperparameters are checked as torch.optim.Adam checks them: lr >= 0,
+ *     0 <= beta1 < 1, 0 <= beta2 < 1, eps >= 0, all finite, t >= 1; a loss
+ *     scale must be finite (<= 0 turns scaling off).  Anything else returns
+ *     ZERO_EINVAL and launches nothing.
  *   - A context is not thread-safe; use one per host thread.
  *   - Element types: ZERO_F32, ZERO_BF16, ZERO_F16.  master/m/v are fp32.
  */

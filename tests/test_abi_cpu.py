@@ -157,6 +157,14 @@ def test_calls_before_bind_fail_cleanly(z):
         z.zero3_begin_step(c)   # not stage 3
 
 
+def test_advance_state_rejects_a_non_finite_scale(z):
+    buf = np.zeros(z.ZERO_ADVANCE_STATE_BYTES, np.uint8)
+    for bad in (float("inf"), float("nan")):
+        with pytest.raises(z.ZeroError) as ei:
+            z.zero_advance_state(buf.ctypes.data, 1, bad, 2000)
+        assert ei.value.code == z.ZERO_EINVAL
+
+
 def test_advance_table_and_state_on_the_host(z):
     """The device-advance table holds, per step, the bias corrections the
     oracle derives for that step (bit for bit), and the state block packs t,

@@ -356,6 +356,19 @@ def test_error_codes_on_device():
          z.ZERO_ESTATE),
         (lambda: z.zero3_gather_unit(c, 0, g, p), z.ZERO_EINVAL),
         (lambda: z.zero_bind(c, f.data_ptr() + 2, f, f, p, None, flag), z.ZERO_EALIGN),
+        # outside the ranges Adam is defined on (as torch.optim.Adam checks)
+        (lambda: z.zero_step(c, g, -1e-3, 0.9, 0.999, 1e-8, 1), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g, float("nan"), 0.9, 0.999, 1e-8, 1), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g, 1e-3, 1.0, 0.999, 1e-8, 1), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g, 1e-3, 0.9, 1.0, 1e-8, 1), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g, 1e-3, -0.1, 0.999, 1e-8, 1), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g, 1e-3, 0.9, 0.999, -1e-8, 1), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g, 1e-3, 0.9, 0.999, float("inf"), 1), z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g, 1e-3, 0.9, 0.999, 1e-8, 1, loss_scale=float("inf")),
+         z.ZERO_EINVAL),
+        (lambda: z.zero_step(c, g, 1e-3, 0.9, 0.999, 1e-8, 1, loss_scale=float("nan")),
+         z.ZERO_EINVAL),
+        (lambda: z.zero_bucket_begin(c, float("inf")), z.ZERO_EINVAL),
     ]
     for fn, code in cases:
         with pytest.raises(z.ZeroError) as ei:

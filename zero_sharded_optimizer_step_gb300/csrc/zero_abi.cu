@@ -384,9 +384,26 @@ int do_fused(zero_ctx *c, const Range &r, const void *const *grads, double lr, d
     return finish_launch(c, zgb::launch_finalize(c->pdt, a, c->sms, s), "finalize kernel", s);
 }
 
-int check_hyper(int64_t t)
+// The ranges Adam is defined on (those torch.optim.Adam also enforces):
+// lr >= 0, 0 <= beta < 1 (beta2 = 1 would divide by 1 - beta2^t = 0),
+// eps >= 0, all finite; t counts from 1.
+int check_hyper(double lr, double b1, double b2, double eps, int64_t t)
 {
     if (t < 1) return fail(ZERO_EINVAL, "step count t must be >= 1 (got %lld)", (long long)t);
+    if (!(lr >= 0.0) || !std::isfinite(lr))
+        return fail(ZERO_EINVAL, "lr must be a finite value >= 0 (got %g)", lr);
+    if (!(b1 >= 0.0 && b1 < 1.0)) return fail(ZERO_EINVAL, "beta1 must be in [0, 1) (got %g)", b1);
+    if (!(b2 >= 0.0 && b2 < 1.0)) return fail(ZERO_EINVAL, "beta2 must be in [0, 1) (got %g)", b2);
+    if (!(eps >= 0.0) || !std::isfinite(eps))
+        return fail(ZERO_EINVAL, "eps must be a finite value >= 0 (got %g)", eps);
+    return ZERO_OK;
+}
+
+// A loss scale is finite; <= 0 turns scaling off.
+int check_scale(float loss_scale)
+{
+    if (!std::isfinite(loss_scale))
+        return fail(ZERO_EINVAL, "loss_scale must be finite (<= 0 turns loss scaling off)");
     return ZERO_OK;
 }
 
@@ -774,8 +791,8 @@ int zero_prepare_step(zero_ctx *c, void *host_hyper, double lr, double b1, doubl
     if (!c || !host_hyper) return fail(ZERO_EINVAL, "null argument");
     if (!c->hyper) return fail(ZERO_ESTATE, "no device hyper block bound (zero_bind_hyper)");
     if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open");
-    int rc = check_hyper(t);
-    if (rc) return rc;
+    int rc = check_hyper(lr, b1, b2, eps, t);
+    if (rc || (rc = check_scale(loss_scale))) return rc;
     c->step_id += 1;
     c->step_scaled = loss_scale > 0.0f;
     zgb::DeviceHyper h;
@@ -810,6 +827,7 @@ int zero_fill_advance_table(void *host_table, int64_t t_max, double b1, double b
 int zero_advance_state(void *host_state, int64_t t, float loss_scale, int64_t growth_interval)
 {
     if (!host_state || t < 1) return fail(ZERO_EINVAL, "host_state and t >= 1 required");
+    if (int rc = check_scale(loss_scale)) return rc;
     zgb::AdvanceState st{};
     st.t = t;
     st.scale = loss_scale > 0.0f ? loss_scale : 0.0f;
@@ -874,7 +892,7 @@ int zero_step_reduce(zero_ctx *c, const void *const *grads, int32_t n_grads, flo
                      void *stream)
 {
     int rc = check_ready(c);
-    if (rc) return rc;
+    if (rc || (rc = check_scale(loss_scale))) return rc;
     if (c->stage == 3) return fail(ZERO_EINVAL, "stage 3 reduces per unit (zero3_reduce_unit)");
     if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
     if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
@@ -890,7 +908,7 @@ int zero_step_apply(zero_ctx *c, double lr, double b1, double b2, double eps, in
 {
     int rc = check_ready(c);
     if (rc) return rc;
-    if ((rc = check_hyper(t))) return rc;
+    if ((rc = check_hyper(lr, b1, b2, eps, t))) return rc;
     if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
     if (c->stage == 3 && c->cur)
         return fail(ZERO_ESTATE, "with two state sets, stage-3 steps finish with zero3_end_step");
@@ -904,7 +922,7 @@ int zero_step(zero_ctx *c, const void *const *grads, int32_t n_grads, double lr,
 {
     int rc = check_ready(c);
     if (rc) return rc;
-    if ((rc = check_hyper(t))) return rc;
+    if ((rc = check_hyper(lr, b1, b2, eps, t)) || (rc = check_scale(loss_scale))) return rc;
     if (c->stage == 3) return fail(ZERO_EINVAL, "stage 3 steps per unit (zero3_step_unit)");
     if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
     const Range r = vector_range(c);
@@ -932,6 +950,7 @@ int zero_bucket_begin(zero_ctx *c, float loss_scale)
     if (!c) return fail(ZERO_EINVAL, "null context");
     if (c->stage == 3) return fail(ZERO_EINVAL, "buckets cover the flat vector of stages 1 and 2");
     if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is already open");
+    if (int rc = check_scale(loss_scale)) return rc;
     if (loss_scale > 0.0f && !c->cur && !c->g)
         return fail(ZERO_ESTATE, "a loss-scaled bucketed step needs g_scratch or a second state set");
     int rc = begin_step(c, loss_scale > 0.0f);
@@ -948,7 +967,7 @@ int zero_bucket_step(zero_ctx *c, int64_t offset, int64_t count, const void *con
     int rc = check_ready(c);
     if (rc) return rc;
     if (!c->bucket_open) return fail(ZERO_ESTATE, "call zero_bucket_begin first");
-    if ((rc = check_hyper(t))) return rc;
+    if ((rc = check_hyper(lr, b1, b2, eps, t))) return rc;
     const Range whole = vector_range(c);
     if (offset < 0 || count < 0 || offset > whole.n || count > whole.n - offset)
         return fail(ZERO_EINVAL, "bucket [%lld, %lld) outside the range of %lld elements",
@@ -975,7 +994,7 @@ int zero_bucket_end(zero_ctx *c, double lr, double b1, double b2, double eps, in
     int rc = check_ready(c);
     if (rc) return rc;
     if (!c->bucket_open) return fail(ZERO_ESTATE, "no bucketed step is open");
-    if ((rc = check_hyper(t))) return rc;
+    if ((rc = check_hyper(lr, b1, b2, eps, t))) return rc;
     c->bucket_open = false;
     cudaStream_t s = (cudaStream_t)stream;
     const Range whole = vector_range(c);
@@ -1061,6 +1080,7 @@ int zero3_begin_step_scaled(zero_ctx *c, float loss_scale)
     if (!c) return fail(ZERO_EINVAL, "null context");
     if (c->stage != 3) return fail(ZERO_EINVAL, "zero3_begin_step is for stage 3");
     if (c->stage3_open) return fail(ZERO_ESTATE, "the last stage-3 step is open (zero3_end_step)");
+    if (int rc = check_scale(loss_scale)) return rc;
     const bool scaled = loss_scale > 0.0f;
     if (c->hyper) {
         if (c->step_id == 0) return fail(ZERO_ESTATE, "call zero_prepare_step first");
@@ -1150,7 +1170,7 @@ int zero3_step_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32_t
     int rc = check_ready(c);
     if (rc) return rc;
     if ((rc = check_unit(c, unit))) return rc;
-    if ((rc = check_hyper(t))) return rc;
+    if ((rc = check_hyper(lr, b1, b2, eps, t))) return rc;
     if ((rc = check_stage3_pass(c))) return rc;
     const Range r = unit_range(c, unit);
     rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
@@ -1162,7 +1182,7 @@ int zero3_reduce_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32
                       float loss_scale, void *stream)
 {
     int rc = check_ready(c);
-    if (rc) return rc;
+    if (rc || (rc = check_scale(loss_scale))) return rc;
     if ((rc = check_unit(c, unit))) return rc;
     if (c->cur) return fail(ZERO_ESTATE, kTwoSetsStage3);
     if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
@@ -1251,7 +1271,7 @@ int zero3_step_group(zero_ctx *c, int32_t first_unit, int32_t n_units, const voi
     int rc = check_ready(c);
     if (rc) return rc;
     if ((rc = check_unit(c, first_unit))) return rc;
-    if ((rc = check_hyper(t))) return rc;
+    if ((rc = check_hyper(lr, b1, b2, eps, t))) return rc;
     if ((rc = check_stage3_pass(c))) return rc;
     Range r;
     if ((rc = group_range(c, first_unit, n_units, &r))) return rc;
@@ -1264,7 +1284,7 @@ int zero3_reduce_group(zero_ctx *c, int32_t first_unit, int32_t n_units,
                        const void *const *grads, int32_t n_grads, float loss_scale, void *stream)
 {
     int rc = check_ready(c);
-    if (rc) return rc;
+    if (rc || (rc = check_scale(loss_scale))) return rc;
     if ((rc = check_unit(c, first_unit))) return rc;
     if (c->cur) return fail(ZERO_ESTATE, kTwoSetsStage3);
     if (!c->g) return fail(ZERO_ESTATE, "the two-pass step needs g_scratch (zero_bind)");
@@ -1326,7 +1346,7 @@ extern "C" int zero_step_noalloc(zero_ctx *c, const void *const *grads, int32_t 
 {
     int rc = check_ready(c);
     if (rc) return rc;
-    if ((rc = check_hyper(t))) return rc;
+    if ((rc = check_hyper(lr, b1, b2, eps, t)) || (rc = check_scale(loss_scale))) return rc;
     if (c->stage == 3) return fail(ZERO_EINVAL, "zero_step_noalloc covers stages 1 and 2");
     if (c->bucket_open) return fail(ZERO_ESTATE, "a bucketed step is open (zero_bucket_end)");
     const Range r = vector_range(c);
