@@ -1279,7 +1279,8 @@ def test_device_advance_stops_when_the_table_runs_out():
     run.close()
 
 
-def _direct_step_case(grads_h, gdt, pdt, scale, x0, steps, shadow):
+def _direct_step_case(grads_h, gdt, pdt, scale, x0, steps, shadow, hp=(1e-3, 0.9, 0.999, 1e-8),
+                      t0=0):
     """Steps the same host grads through zero_step (all ranks) and through
     the oracle; returns the GPU verdicts and asserts bit-identity."""
     import zero_sharded_optimizer_step_gb300 as z
@@ -1309,12 +1310,12 @@ def _direct_step_case(grads_h, gdt, pdt, scale, x0, steps, shadow):
     for g in grads_h:
         t = torch.from_numpy(g.view(np.int16) if gdt != W.F32 else g).to(dev)
         gd.append(t.view(tdt[gdt]) if gdt != W.F32 else t)
-    verdicts, t = [], 0
+    verdicts, t = [], t0
     for _ in range(steps):
-        z.zero_step(c, gd, 1e-3, 0.9, 0.999, 1e-8, t + 1, scale)
+        z.zero_step(c, gd, *hp, t + 1, scale)
         _, skipped = z.zero_step_status(c)
-        o_skip, _ = oracle.zero_step(grads_h, gdt, numel, xh, mh, vh, ph, pdt, 1e-3, 0.9, 0.999,
-                                     1e-8, t + 1, loss_scale=scale)
+        o_skip, _ = oracle.zero_step(grads_h, gdt, numel, xh, mh, vh, ph, pdt, *hp, t + 1,
+                                     loss_scale=scale)
         assert skipped == o_skip
         verdicts.append(skipped)
         t += 0 if skipped else 1
@@ -1378,3 +1379,19 @@ def test_subnormals_are_kept(pdt):
     sq = g[0].astype(np.float32) * g[0].astype(np.float32)
     assert ((sq != 0) & (np.abs(sq) < np.finfo(np.float32).tiny)).mean() > 0.5
     assert _direct_step_case(g, W.F32, pdt, 0.0, x0, 3, False) == [False] * 3
+
+
+@pytest.mark.parametrize("hp,t0", [
+    ((0.0, 0.9, 0.999, 1e-8), 0),          # lr 0: masters and params unchanged, m and v move
+    ((1e-3, 0.0, 0.0, 1e-8), 0),           # no momentum: m = g, v = g*g
+    ((1e-3, 0.9, 0.999, 0.0), 0),          # eps 0: the step is lr * mh / sqrt(vh)
+    ((1e-2, 0.9, 0.999, 1e-8), 999_997),   # t near 10^6: bias corrections round to 1
+    ((1e-3, 0.5, 0.5, 1e-3), 1_100),       # 0.5^t underflows double: corrections exactly 1
+])
+def test_extreme_valid_hyperparameters(hp, t0):
+    """Values at the edges of the ranges Adam is defined on, bit-identical to
+    the oracle over three steps (fp32 grads, bf16 params)."""
+    n, world = 40_003, 3
+    x0 = synth.fill_host(n, synth.F32, synth.key(6, synth.KIND_MASTER), 0.01)
+    g = [synth.fill_host(n, W.F32, synth.key(6, synth.KIND_GRAD, 1, k), 1e-3) for k in range(world)]
+    assert _direct_step_case(g, W.F32, W.BF16, 0.0, x0, 3, False, hp=hp, t0=t0) == [False] * 3
