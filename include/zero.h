@@ -247,6 +247,16 @@ int zero_bind_shadow(zero_ctx *ctx, float *master_b, float *m_b, float *v_b, uin
  * Always 0 without a second set. */
 int zero_current_state(zero_ctx *ctx, int32_t *which);
 
+/* At most blocks_per_sm resident blocks per SM for this context's step
+ * kernels (the fused step, the two passes, the finalize); 0, the default,
+ * takes as many as fit (four of 256 threads at 64 registers for 16-bit
+ * grads, which is every register of an SM).  A lower number leaves room on
+ * every SM for a kernel that runs at the same time -- the step of a bucket
+ * during the backward of the next ("论文专题讲解：ZeRO", ZeRO-DP 三阶段: the
+ * gradients are reduce-scattered while backward goes on) -- at some cost to
+ * the step alone.  Results do not depend on it.  ZERO_EINVAL outside [0, 32]. */
+int zero_set_step_occupancy(zero_ctx *ctx, int32_t blocks_per_sm);
+
 /* Decoupled weight decay (AdamW; Loshchilov & Hutter, "Decoupled Weight
  * Decay Regularization", ICLR 2019 -- "PaddlePaddle ZeRO优化" names AdamW as
  * the optimizer whose states are sharded).  From the next step on, every

@@ -157,6 +157,16 @@ def test_calls_before_bind_fail_cleanly(z):
         z.zero3_begin_step(c)   # not stage 3
 
 
+def test_step_occupancy_argument_checked(z):
+    c = z.zero_init(1000, 4, 2, z.ZERO_BF16, z.ZERO_BF16, -1)
+    for ok in (0, 1, 4, 32):
+        z.zero_set_step_occupancy(c, ok)
+    for bad in (-1, 33):
+        with pytest.raises(z.ZeroError) as ei:
+            z.zero_set_step_occupancy(c, bad)
+        assert ei.value.code == z.ZERO_EINVAL
+
+
 def test_advance_state_rejects_a_non_finite_scale(z):
     buf = np.zeros(z.ZERO_ADVANCE_STATE_BYTES, np.uint8)
     for bad in (float("inf"), float("nan")):

@@ -637,6 +637,35 @@ def test_lean_gather_wait_that_runs_out_is_reported():
     assert z.zero_gather_timeouts() == after
 
 
+@pytest.mark.parametrize("shadow,scaled", [(True, True), (False, False), (False, True)])
+def test_zero2_buckets_stepped_during_backward(shadow, scaled):
+    """The bucketed ZeRO-2 step run during backward (each bucket on a second
+    stream while a stand-in kernel plays the next bucket's backward) equals
+    the oracle bit for bit, with a planted +inf skipping iteration 2 when
+    loss-scaled -- in both loss-scaled forms (two state sets; one set with
+    the scratch, where zero_bucket_end applies Adam after the last bucket)."""
+    from workloads.runner import Runner
+    from workloads.zero2_schedule import Zero2Schedule
+    w = W.Workload("z2o", 1_000_003, 8, 2, W.BF16, W.BF16, steps=3, bucket=100_000,
+                   loss_scale=2.0 ** 10 if scaled else 0.0, inject=(2, 5) if scaled else None)
+    run = Runner(w, shadow=shadow)
+    ref = refs.OracleRun(w)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sch = Zero2Schedule(run, 2000, 4000, 2 * sms, "overlap")
+    for it in range(1, w.steps + 1):
+        run.fill_grads(it)
+        sch.launch_step()
+        if scaled:
+            run.finish_step()
+        else:
+            run.skips.append(False)
+        ref.step(it)
+    torch.cuda.synchronize()
+    assert run.skips == ref.skips == ([False, True, False] if scaled else [False] * 3)
+    compare_runner(run, ref, what="zero2 overlap")
+    run.close()
+
+
 # -------------------------------------------------- FSDP2's dim-0 layout
 
 @pytest.mark.parametrize("rank,scaled", [(1, False), (-1, False), (3, True), (0, False)])

@@ -70,6 +70,7 @@ _SIGS = {
     "zero_advance_step": (ctypes.c_int, [_ctxp, _vp]),
     "zero_gather_timeouts": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "zero_set_gather_wait_polls": (ctypes.c_int, [ctypes.c_int64]),
+    "zero_set_step_occupancy": (ctypes.c_int, [_ctxp, _i32]),
     "zero_bind_shadow": (ctypes.c_int, [_ctxp, _vp, _vp, _vp, _vp]),
     "zero_current_state": (ctypes.c_int, [_ctxp, ctypes.POINTER(_i32)]),
     "zero_step": (ctypes.c_int, [_ctxp, _vpp, _i32, _f64, _f64, _f64, _f64, _i64, _f32, _vp]),
@@ -273,6 +274,11 @@ def zero_gather_timeouts() -> int:
     if rc != ZERO_ETIMEOUT:
         _check(rc)
     return int(c.value)
+
+
+def zero_set_step_occupancy(ctx, blocks_per_sm: int) -> None:
+    """At most blocks_per_sm step-kernel blocks per SM (0: as many as fit)."""
+    _check(_L.zero_set_step_occupancy(_h(ctx), blocks_per_sm))
 
 
 def zero_set_gather_wait_polls(polls: int) -> None:

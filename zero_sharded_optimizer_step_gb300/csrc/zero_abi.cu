@@ -74,6 +74,7 @@ struct zero_ctx {
 
     double weight_decay = 0.0;   // AdamW's decoupled decay; 0 = Adam
     int32_t gather_mode = 0;     // ZERO_GATHER_FAST or ZERO_GATHER_LEAN
+    int32_t step_per_sm = 0;     // > 0: step kernels use at most this many blocks per SM
 
     void *hyper = nullptr;       // device block of per-step scalars (graph capture)
     int hyper_slot = -1;         // its constant-memory slot on hyper_device
@@ -342,7 +343,8 @@ int do_reduce(zero_ctx *c, const Range &r, const void *const *grads, float loss_
     StepArgs a = make_args(c, r, grads);
     a.av = average_scalars(c->world, loss_scale);
     a.step_id = c->step_id;
-    return finish_launch(c, zgb::launch_reduce(c->gdt, a, c->sms, s), "reduce kernel", s);
+    return finish_launch(c, zgb::launch_reduce(c->gdt, a, c->sms, c->step_per_sm, s),
+                         "reduce kernel", s);
 }
 
 int do_apply(zero_ctx *c, const Range &r, double lr, double b1, double b2, double eps,
@@ -354,7 +356,8 @@ int do_apply(zero_ctx *c, const Range &r, double lr, double b1, double b2, doubl
     a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
     // an unscaled step never skips: use an id the flag cannot hold
     a.step_id = c->step_scaled ? c->step_id : ~0ull;
-    return finish_launch(c, zgb::launch_apply(c->pdt, a, c->sms, s), "apply kernel", s);
+    return finish_launch(c, zgb::launch_apply(c->pdt, a, c->sms, c->step_per_sm, s),
+                         "apply kernel", s);
 }
 
 int do_finalize(zero_ctx *c, const Range &r, cudaStream_t s)
@@ -363,7 +366,8 @@ int do_finalize(zero_ctx *c, const Range &r, cudaStream_t s)
     if (int rc = load_slot_if_stale(c, s)) return rc;
     StepArgs a = make_args(c, r, nullptr);
     a.step_id = c->step_scaled ? c->step_id : ~0ull;
-    return finish_launch(c, zgb::launch_finalize(c->pdt, a, c->sms, s), "finalize kernel", s);
+    return finish_launch(c, zgb::launch_finalize(c->pdt, a, c->sms, c->step_per_sm, s),
+                         "finalize kernel", s);
 }
 
 int do_fused(zero_ctx *c, const Range &r, const void *const *grads, double lr, double b1,
@@ -376,12 +380,14 @@ int do_fused(zero_ctx *c, const Range &r, const void *const *grads, double lr, d
     a.av = average_scalars(c->world, loss_scale);
     a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
     a.step_id = c->step_id;
-    int rc = finish_launch(c, zgb::launch_fused_step(c->gdt, c->pdt, a, c->sms, s), "step kernel", s);
+    int rc = finish_launch(
+        c, zgb::launch_fused_step(c->gdt, c->pdt, a, c->sms, c->step_per_sm, s), "step kernel", s);
     if (rc || !c->cur || !finalize) return rc;
     // two state sets: the written set becomes current unless the step is
     // loss-scaled and overflowed
     a.step_id = c->step_scaled ? c->step_id : ~0ull;
-    return finish_launch(c, zgb::launch_finalize(c->pdt, a, c->sms, s), "finalize kernel", s);
+    return finish_launch(c, zgb::launch_finalize(c->pdt, a, c->sms, c->step_per_sm, s),
+                         "finalize kernel", s);
 }
 
 // The ranges Adam is defined on (those torch.optim.Adam also enforces):
@@ -710,6 +716,15 @@ int zero_set_gather_wait_polls(int64_t polls)
 {
     cudaError_t e = zgb::set_lean_first_wait_polls((long long)polls);
     if (e != cudaSuccess) return cuda_fail(e, "setting the lean gather's wait limit");
+    return ZERO_OK;
+}
+
+int zero_set_step_occupancy(zero_ctx *c, int32_t blocks_per_sm)
+{
+    if (!c) return fail(ZERO_EINVAL, "null context");
+    if (blocks_per_sm < 0 || blocks_per_sm > 32)
+        return fail(ZERO_EINVAL, "blocks_per_sm must be in [0, 32] (0: as many as fit)");
+    c->step_per_sm = blocks_per_sm;
     return ZERO_OK;
 }
 
@@ -1371,9 +1386,11 @@ extern "C" int zero_step_noalloc(zero_ctx *c, const void *const *grads, int32_t 
     a.vec_ok = ok ? 1 : 0;
     a.av = average_scalars(c->world, loss_scale);
     a.step_id = c->step_id;
-    rc = finish_launch(c, zgb::launch_reduce(c->gdt, a, c->sms, s), "reduce kernel", s);
+    rc = finish_launch(c, zgb::launch_reduce(c->gdt, a, c->sms, c->step_per_sm, s),
+                       "reduce kernel", s);
     if (rc) return rc;
     a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
     a.step_id = c->step_scaled ? c->step_id : ~0ull;
-    return finish_launch(c, zgb::launch_apply(c->pdt, a, c->sms, s), "apply kernel", s);
+    return finish_launch(c, zgb::launch_apply(c->pdt, a, c->sms, c->step_per_sm, s),
+                         "apply kernel", s);
 }

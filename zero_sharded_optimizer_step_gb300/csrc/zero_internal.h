@@ -149,15 +149,20 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, s
 }
 #endif
 
-// Launchers: return a cudaError_t.  `sms` is the device's SM count.
+// Launchers: return a cudaError_t.  `sms` is the device's SM count;
+// cap_per_sm > 0 sizes the grid for at most that many blocks per SM (fewer
+// than fit), leaving the rest of every SM to kernels that run beside it.
 cudaError_t launch_fused_step(int32_t gdt, int32_t pdt, const StepArgs &a, int sms,
-                              cudaStream_t s);
-cudaError_t launch_reduce(int32_t gdt, const StepArgs &a, int sms, cudaStream_t s);
-cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s);
+                              int cap_per_sm, cudaStream_t s);
+cudaError_t launch_reduce(int32_t gdt, const StepArgs &a, int sms, int cap_per_sm,
+                          cudaStream_t s);
+cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, int cap_per_sm,
+                         cudaStream_t s);
 // After a single-pass step on two state sets: make the written set current,
 // or, when the step overflowed, keep the old set and rewrite the params
 // from it.
-cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s);
+cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, int cap_per_sm,
+                            cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s);
 // Fills a copy's first_block table and launches; `a` itself is not changed.
 cudaError_t launch_gather_rows(const GatherRowsArgs &a, int sms, cudaStream_t s);

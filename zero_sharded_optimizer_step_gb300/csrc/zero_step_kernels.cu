@@ -532,9 +532,10 @@ cudaError_t load_hyper_slot(int slot, const DeviceHyper *block, cudaStream_t s)
 namespace {
 
 template <typename K>
-cudaError_t launch(K kernel, const StepArgs &a, int64_t work_items, int sms, cudaStream_t s)
+cudaError_t launch(K kernel, const StepArgs &a, int64_t work_items, int sms, int cap_per_sm, cudaStream_t s)
 {
-    const int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(kernel), kThreads);
+    int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(kernel), kThreads);
+    if (cap_per_sm > 0 && per_sm > cap_per_sm) per_sm = cap_per_sm;   // room for other kernels
     int64_t want = (work_items + kThreads - 1) / kThreads;
     int64_t cap = (int64_t)sms * per_sm;
     int64_t blocks = want < cap ? want : cap;
@@ -551,92 +552,92 @@ int64_t items(const StepArgs &a, int64_t nvec_src)
 }
 
 template <int GT, int PT, bool HYPER>
-cudaError_t fused_h(const StepArgs &a, int sms, cudaStream_t s)
+cudaError_t fused_h(const StepArgs &a, int sms, int cap_per_sm, cudaStream_t s)
 {
     const int64_t w = items(a, a.n_valid);
-    return a.grad_avg ? launch(fused_step_kernel<GT, PT, true, HYPER>, a, w, sms, s)
-                      : launch(fused_step_kernel<GT, PT, false, HYPER>, a, w, sms, s);
+    return a.grad_avg ? launch(fused_step_kernel<GT, PT, true, HYPER>, a, w, sms, cap_per_sm, s)
+                      : launch(fused_step_kernel<GT, PT, false, HYPER>, a, w, sms, cap_per_sm, s);
 }
 
 template <int GT, int PT>
-cudaError_t fused_pt(const StepArgs &a, int sms, cudaStream_t s)
+cudaError_t fused_pt(const StepArgs &a, int sms, int cap_per_sm, cudaStream_t s)
 {
-    return a.hyper ? fused_h<GT, PT, true>(a, sms, s) : fused_h<GT, PT, false>(a, sms, s);
+    return a.hyper ? fused_h<GT, PT, true>(a, sms, cap_per_sm, s) : fused_h<GT, PT, false>(a, sms, cap_per_sm, s);
 }
 
 template <int GT>
-cudaError_t fused_gt(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s)
+cudaError_t fused_gt(int32_t pdt, const StepArgs &a, int sms, int cap_per_sm, cudaStream_t s)
 {
     switch (pdt) {
-    case F32: return fused_pt<GT, F32>(a, sms, s);
-    case BF16: return fused_pt<GT, BF16>(a, sms, s);
-    case F16: return fused_pt<GT, F16>(a, sms, s);
+    case F32: return fused_pt<GT, F32>(a, sms, cap_per_sm, s);
+    case BF16: return fused_pt<GT, BF16>(a, sms, cap_per_sm, s);
+    case F16: return fused_pt<GT, F16>(a, sms, cap_per_sm, s);
     }
     return cudaErrorInvalidValue;
 }
 
 template <int GT, bool HYPER>
-cudaError_t reduce_h(const StepArgs &a, int sms, cudaStream_t s)
+cudaError_t reduce_h(const StepArgs &a, int sms, int cap_per_sm, cudaStream_t s)
 {
     const int64_t w = items(a, a.n_valid);
-    return a.grad_avg ? launch(reduce_kernel<GT, true, HYPER>, a, w, sms, s)
-                      : launch(reduce_kernel<GT, false, HYPER>, a, w, sms, s);
+    return a.grad_avg ? launch(reduce_kernel<GT, true, HYPER>, a, w, sms, cap_per_sm, s)
+                      : launch(reduce_kernel<GT, false, HYPER>, a, w, sms, cap_per_sm, s);
 }
 
 template <int GT>
-cudaError_t reduce_gt(const StepArgs &a, int sms, cudaStream_t s)
+cudaError_t reduce_gt(const StepArgs &a, int sms, int cap_per_sm, cudaStream_t s)
 {
-    return a.hyper ? reduce_h<GT, true>(a, sms, s) : reduce_h<GT, false>(a, sms, s);
+    return a.hyper ? reduce_h<GT, true>(a, sms, cap_per_sm, s) : reduce_h<GT, false>(a, sms, cap_per_sm, s);
 }
 
 template <int PT>
-cudaError_t apply_pt(const StepArgs &a, int sms, cudaStream_t s)
+cudaError_t apply_pt(const StepArgs &a, int sms, int cap_per_sm, cudaStream_t s)
 {
     const int64_t w = items(a, a.n);
-    return a.hyper ? launch(apply_kernel<PT, true>, a, w, sms, s)
-                   : launch(apply_kernel<PT, false>, a, w, sms, s);
+    return a.hyper ? launch(apply_kernel<PT, true>, a, w, sms, cap_per_sm, s)
+                   : launch(apply_kernel<PT, false>, a, w, sms, cap_per_sm, s);
 }
 
 }  // namespace
 
 cudaError_t launch_fused_step(int32_t gdt, int32_t pdt, const StepArgs &a, int sms,
-                              cudaStream_t s)
+                              int cap_per_sm, cudaStream_t s)
 {
     switch (gdt) {
-    case F32: return fused_gt<F32>(pdt, a, sms, s);
-    case BF16: return fused_gt<BF16>(pdt, a, sms, s);
-    case F16: return fused_gt<F16>(pdt, a, sms, s);
+    case F32: return fused_gt<F32>(pdt, a, sms, cap_per_sm, s);
+    case BF16: return fused_gt<BF16>(pdt, a, sms, cap_per_sm, s);
+    case F16: return fused_gt<F16>(pdt, a, sms, cap_per_sm, s);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_reduce(int32_t gdt, const StepArgs &a, int sms, cudaStream_t s)
+cudaError_t launch_reduce(int32_t gdt, const StepArgs &a, int sms, int cap_per_sm, cudaStream_t s)
 {
     switch (gdt) {
-    case F32: return reduce_gt<F32>(a, sms, s);
-    case BF16: return reduce_gt<BF16>(a, sms, s);
-    case F16: return reduce_gt<F16>(a, sms, s);
+    case F32: return reduce_gt<F32>(a, sms, cap_per_sm, s);
+    case BF16: return reduce_gt<BF16>(a, sms, cap_per_sm, s);
+    case F16: return reduce_gt<F16>(a, sms, cap_per_sm, s);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s)
+cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, int cap_per_sm, cudaStream_t s)
 {
     const int64_t w = items(a, a.n);
     switch (pdt) {
-    case F32: return launch(finalize_kernel<F32>, a, w, sms, s);
-    case BF16: return launch(finalize_kernel<BF16>, a, w, sms, s);
-    case F16: return launch(finalize_kernel<F16>, a, w, sms, s);
+    case F32: return launch(finalize_kernel<F32>, a, w, sms, cap_per_sm, s);
+    case BF16: return launch(finalize_kernel<BF16>, a, w, sms, cap_per_sm, s);
+    case F16: return launch(finalize_kernel<F16>, a, w, sms, cap_per_sm, s);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, cudaStream_t s)
+cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, int cap_per_sm, cudaStream_t s)
 {
     switch (pdt) {
-    case F32: return apply_pt<F32>(a, sms, s);
-    case BF16: return apply_pt<BF16>(a, sms, s);
-    case F16: return apply_pt<F16>(a, sms, s);
+    case F32: return apply_pt<F32>(a, sms, cap_per_sm, s);
+    case BF16: return apply_pt<BF16>(a, sms, cap_per_sm, s);
+    case F16: return apply_pt<F16>(a, sms, cap_per_sm, s);
     }
     return cudaErrorInvalidValue;
 }
