@@ -51,22 +51,22 @@ import numpy as np  # noqa: E402
 # for the kernel source it was taken on (sha256 prefix); otherwise bench
 # reports null.
 TRAFFIC = {
-    ("gpt2_xl", "fused_step_kernel"): ("02f54cd48e586eae", 68.538e9 + 21.776e9, 13112.7),
+    ("gpt2_xl", "fused_step_kernel"): ("ef00f5525d2d15b7", 68.537e9 + 21.778e9, 12939.9),
     ("one_rank_7p5b", "gather_kernel"): ("5ad5f8b67603e427", 14.788e9 + 14.724e9, 4254.7),
-    ("one_rank_7p5b", "fused_step_kernel"): ("02f54cd48e586eae", 16.407e9 + 1.621e9, 2605.1),
+    ("one_rank_7p5b", "fused_step_kernel"): ("ef00f5525d2d15b7", 16.408e9 + 1.621e9, 2568.0),
     # means of two full-size launches; part of each launch's writes is still
     # in L2 when it ends
     ("zero3_llama7b", "gather_rows_kernel"): ("5ad5f8b67603e427", 404.79e6 + 349.72e6, 113.7),
     # the same gathers (2-byte params, the same shard sizes)
     ("zero3_llama7b_fp16", "gather_rows_kernel"): ("5ad5f8b67603e427", 404.79e6 + 350.47e6, 113.3),
     ("fsdp2_llama7b", "gather_rows_kernel"): ("5ad5f8b67603e427", 404.79e6 + 347.54e6, 112.4),
-    ("gpt2_small", "fused_step_kernel"): ("02f54cd48e586eae", 3.4844e9 + 1.6928e9, 752.4),
-    ("gpt2_xl_adamw", "fused_step_kernel"): ("02f54cd48e586eae", 68.537e9 + 21.780e9, 12864.0),
+    ("gpt2_small", "fused_step_kernel"): ("ef00f5525d2d15b7", 3.4844e9 + 1.6934e9, 750.0),
+    ("gpt2_xl_adamw", "fused_step_kernel"): ("ef00f5525d2d15b7", 68.536e9 + 21.778e9, 12920.9),
     # mean over the 47 bucket launches of one step
-    ("gpt2_xl_bucketed", "fused_step_kernel"): ("02f54cd48e586eae", 1.45832e9 + 0.43176e9, 275.9),
-    ("gpt2_small_stage1", "fused_step_kernel"): ("02f54cd48e586eae", 3.4844e9 + 1.9533e9, 804.9),
+    ("gpt2_xl_bucketed", "fused_step_kernel"): ("ef00f5525d2d15b7", 1.45833e9 + 0.43173e9, 275.5),
+    ("gpt2_small_stage1", "fused_step_kernel"): ("ef00f5525d2d15b7", 3.4845e9 + 1.9535e9, 800.0),
     # the two-pass loss-scaled step (--two-pass): its first, larger kernel
-    ("gpt2_xl", "reduce_kernel"): ("02f54cd48e586eae", 49.845e9 + 6.2157e9, 8039.7),
+    ("gpt2_xl", "reduce_kernel"): ("ef00f5525d2d15b7", 49.846e9 + 6.2133e9, 7941.7),
     # mean over the 28 gathers of one step; the units' full buffers (14 to
     # 79 MB) mostly stay in L2, so most of the writes never reach DRAM
     ("zero3_gpt2_small", "gather_kernel"): ("5ad5f8b67603e427", 17.794e6 + 1.9392e6, 9.1),
