@@ -100,7 +100,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--step-blocks-per-sm", type=int, default=2,
-                    help="zero2_overlap: step-kernel blocks per SM while backward runs")
+                    help="zero2_overlap, --overlap-steps: step-kernel blocks per SM while "
+                         "backward runs")
+    ap.add_argument("--overlap-steps", action="store_true",
+                    help="zero3_prefetch / fsdp2_prefetch: each unit's reduce + Adam also in "
+                         "the background, beside the next unit's backward")
     ap.add_argument("--clocks-csv", default=None,
                     help="keep the nvidia-smi samples taken during the timed region here")
     ap.add_argument("--e2e-steps", type=int, default=3)
@@ -546,8 +550,10 @@ def bench_prefetch(args, rank, world_size, device_index):
     per_iter = e0.elapsed_time(e1) / probe
     it_f = max(1, int(args.unit_fwd_ms / per_iter))
     times = {}
-    for mode in ("compute_only", "serial", "overlap"):
-        sch = Zero3Schedule(run, it_f, 2 * it_f, blocks, mode)
+    bg = args.overlap_steps
+    for mode in ("standin_only" if bg else "compute_only", "serial", "overlap"):
+        sch = Zero3Schedule(run, it_f, 2 * it_f, blocks, mode, overlap_steps=bg,
+                            step_blocks_per_sm=args.step_blocks_per_sm)
         for _ in range(args.warmup):
             sch.launch_step()
         torch.cuda.synchronize()
@@ -558,8 +564,9 @@ def bench_prefetch(args, rank, world_size, device_index):
         e1.record(run.stream)
         torch.cuda.synchronize()
         times[mode] = allreduce_max(e0.elapsed_time(e1) / args.steps, world_size)
-    exposed = times["overlap"] - times["compute_only"]
-    gathers = times["serial"] - times["compute_only"]
+    base = times["standin_only" if bg else "compute_only"]
+    exposed = times["overlap"] - base
+    gathers = times["serial"] - base     # with bg: the gathers and the unit steps
     updated = w.updated_per_step()
     run.close()
     peak, peak_kind = peaks()
@@ -574,11 +581,14 @@ def bench_prefetch(args, rank, world_size, device_index):
             "workload": describe(w) + " + stand-in compute %.3f ms fwd / %.3f ms bwd per %s"
                         % (args.unit_fwd_ms, 2 * args.unit_fwd_ms,
                            "group" if w.groups else "unit"),
-            "compute_only_ms": times["compute_only"], "serial_ms": times["serial"],
-            "overlap_ms": times["overlap"], "gather_time_serial_ms": gathers,
-            "exposed_gather_ms": exposed,
+            ("standin_only_ms" if bg else "compute_only_ms"): base,
+            "serial_ms": times["serial"], "overlap_ms": times["overlap"],
+            ("gathers_and_steps_serial_ms" if bg else "gather_time_serial_ms"): gathers,
+            ("exposed_gathers_and_steps_ms" if bg else "exposed_gather_ms"): exposed,
             "hidden_fraction": (1 - exposed / gathers) if gathers > 0 else None,
             "gathers_per_step": 2 * U, "standin_blocks": blocks,
+            "unit_steps_in_background": bg,
+            "step_blocks_per_sm_in_background": args.step_blocks_per_sm if bg else None,
         },
         "roofline": None,
         "gpu_launches": (2 * U + 2 * U + U) * args.steps,

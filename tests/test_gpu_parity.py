@@ -537,29 +537,32 @@ def test_zero3_prefetch_schedule_matches_serial_and_oracle(rank, scaled):
     w = W.Workload("z3p", sum(units), 4, 3, W.BF16, W.BF16, rank=rank, units=units, steps=4,
                    loss_scale=2.0 ** 10 if scaled else 0.0, inject=(2, 1) if scaled else None)
     runs = {}
-    for mode in ("serial", "overlap"):
+    for mode, steps_bg in (("serial", False), ("overlap", False), ("overlap", True)):
         run = Runner(w)
-        sch = Zero3Schedule(run, 2000, 4000, 64, mode)
+        sch = Zero3Schedule(run, 2000, 4000, 64, mode, overlap_steps=steps_bg)
         for it in range(1, 5):
             run.fill_grads(it)
             sch.launch_step()
             if scaled:
                 run.finish_step()
         torch.cuda.synchronize()
-        runs[mode] = run
+        runs[(mode, steps_bg)] = run
     ref = refs.OracleRun(w)
     for it in range(1, 5):
         ref.step(it)
-    for a, b in [(runs["serial"].master, runs["overlap"].master),
-                 (runs["serial"].params, runs["overlap"].params)]:
-        assert torch.equal(a, b)
+    serial = runs[("serial", False)]
+    for key in [("overlap", False), ("overlap", True)]:
+        for a, b in [(serial.master, runs[key].master), (serial.params, runs[key].params)]:
+            assert torch.equal(a, b)
     if scaled:
         for run in runs.values():
             assert run.skips == ref.skips
         assert ref.skips == [0, 1, 0, 0]      # the +inf lands in rank 1's part of unit 0
     else:
-        runs["overlap"].skips = ref.skips
-    compare_runner(runs["overlap"], ref, what="prefetch")
+        for run in runs.values():
+            run.skips = ref.skips
+    compare_runner(runs[("overlap", False)], ref, what="prefetch")
+    compare_runner(runs[("overlap", True)], ref, what="prefetch, steps in the background")
 
 
 @pytest.mark.parametrize("S,world,dtype,src_off,dst_off", [

@@ -30,10 +30,20 @@ from . import standin
 
 
 class Zero3Schedule:
+    """mode: "overlap" (gathers prefetched in the background), "serial" (all
+    on one stream), "compute_only" (no gathers), "standin_only" (neither
+    gathers nor steps: the stand-in compute alone).  overlap_steps: in the
+    overlap mode, each backward visit's reduce + Adam also runs in the
+    background, once the visit's compute is done, beside the next visit's
+    compute (the step kernels then take at most step_blocks_per_sm blocks per
+    SM, leaving room for the compute's blocks)."""
+
     def __init__(self, run, iters_fwd: int, iters_bwd: int, busy_blocks: int,
-                 mode: str = "overlap"):
-        assert run.w.stage == 3 and mode in ("overlap", "serial", "compute_only")
+                 mode: str = "overlap", overlap_steps: bool = False, step_blocks_per_sm: int = 2):
+        assert run.w.stage == 3 and mode in ("overlap", "serial", "compute_only",
+                                             "standin_only")
         self.run, self.mode = run, mode
+        self.overlap_steps = overlap_steps and mode == "overlap"
         self.iters = {"f": iters_fwd, "b": iters_bwd}
         self.blocks = busy_blocks
         self.sink = torch.empty(busy_blocks * 128, device=run.dev)
@@ -60,6 +70,8 @@ class Zero3Schedule:
         # the SMs to the compute, which gets the higher stream priority
         self.gs = torch.cuda.Stream(run.dev, priority=0)
         self.cs = torch.cuda.Stream(run.dev, priority=-1)
+        self.ss = torch.cuda.Stream(run.dev, priority=0) if self.overlap_steps else None
+        z.zero_set_step_occupancy(run.ctx, step_blocks_per_sm if self.overlap_steps else 0)
         z.zero_set_gather_mode(run.ctx, z.ZERO_GATHER_LEAN if mode == "overlap"
                                else z.ZERO_GATHER_FAST)
         U = len(self.pieces)
@@ -67,6 +79,7 @@ class Zero3Schedule:
         n = len(self.visits)
         self.ready = [torch.cuda.Event() for _ in range(n)]
         self.used = [torch.cuda.Event() for _ in range(n)]
+        self.grads_done = [torch.cuda.Event() for _ in range(n)]
 
     def _gather(self, v, stream):
         i, _ = self.visits[v]
@@ -80,7 +93,11 @@ class Zero3Schedule:
     def _compute(self, v, stream):
         i, phase = self.visits[v]
         standin.busy(self.sink.data_ptr(), self.blocks, self.iters[phase], stream.cuda_stream)
-        if phase == "b":
+        if phase == "b" and self.mode != "standin_only":
+            if self.overlap_steps:
+                self.grads_done[v].record(stream)   # the unit's backward is done
+                self.ss.wait_event(self.grads_done[v])
+                stream = self.ss
             run, w = self.run, self.run.w
             f, n = self.pieces[i]
             two_pass = run.scale > 0 and run.shadow is None
@@ -97,6 +114,10 @@ class Zero3Schedule:
 
     def _apply(self, stream):
         run, w = self.run, self.run.w
+        if self.mode == "standin_only":
+            return
+        if self.overlap_steps:
+            stream = self.ss
         if run.shadow is not None:
             z.zero3_end_step(run.ctx, stream)
         elif run.scale > 0:
@@ -110,7 +131,10 @@ class Zero3Schedule:
         cs = self.cs if self.mode == "overlap" else run.stream
         if cs is not run.stream:
             cs.wait_stream(run.stream)
-        z.zero3_begin_step_scaled(run.ctx, run.scale)
+        if self.mode != "standin_only":
+            z.zero3_begin_step_scaled(run.ctx, run.scale)
+        if self.overlap_steps:
+            self.ss.wait_stream(cs)                 # nothing of the last step in flight
         n = len(self.visits)
         if self.mode != "overlap":
             for v in range(n):
@@ -134,6 +158,8 @@ class Zero3Schedule:
                     self.ready[v + 1].record(gs)
             self._apply(cs)
             cs.wait_stream(gs)
+            if self.overlap_steps:
+                cs.wait_stream(self.ss)
             run.stream.wait_stream(cs)
         if run.scale <= 0:
             run.t += 1
