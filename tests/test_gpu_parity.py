@@ -866,21 +866,22 @@ def test_grouped_prefetch_schedule_matches_serial_and_oracle():
     shapes = [(256, 64), (512, 16), (64, 8), (1024, 8), (128, 32)]
     w = W.dim0(shapes, 4, rank=1, steps=3).replace(groups=[2, 2, 1])
     runs = {}
-    for mode in ("serial", "overlap"):
+    for mode, bg in (("serial", False), ("overlap", False), ("overlap", True)):
         run = Runner(w)
-        sch = Zero3Schedule(run, 2000, 4000, 64, mode)
+        sch = Zero3Schedule(run, 2000, 4000, 64, mode, overlap_steps=bg)
         for it in range(1, 4):
             run.fill_grads(it)
             sch.launch_step()
         torch.cuda.synchronize()
-        runs[mode] = run
+        runs[(mode, bg)] = run
     ref = refs.OracleRun(w)
     for it in range(1, 4):
         ref.step(it)
-    assert torch.equal(runs["serial"].master, runs["overlap"].master)
-    assert torch.equal(runs["serial"].params, runs["overlap"].params)
-    runs["overlap"].skips = ref.skips
-    compare_runner(runs["overlap"], ref, what="grouped prefetch")
+    for key in [("overlap", False), ("overlap", True)]:
+        assert torch.equal(runs[("serial", False)].master, runs[key].master)
+        assert torch.equal(runs[("serial", False)].params, runs[key].params)
+        runs[key].skips = ref.skips
+        compare_runner(runs[key], ref, what="grouped prefetch %s" % (key,))
     for run in runs.values():
         run.close()
 
@@ -894,15 +895,15 @@ def test_stage3_one_pass_prefetched_schedule():
     w = W.Workload("s3p", sum(units), 4, 3, W.BF16, W.BF16, rank=-1, units=units, steps=4,
                    loss_scale=2.0 ** 10, inject=(2, 1))
     runs = {}
-    for mode in ("serial", "overlap"):
+    for mode, bg in (("serial", False), ("overlap", False), ("overlap", True)):
         run = Runner(w, shadow=True)
-        sch = Zero3Schedule(run, 2000, 4000, 64, mode)
+        sch = Zero3Schedule(run, 2000, 4000, 64, mode, overlap_steps=bg)
         for it in range(1, 5):
             run.fill_grads(it)
             sch.launch_step()
             run.finish_step()
         torch.cuda.synchronize()
-        runs[mode] = run
+        runs[(mode, bg)] = run
     ref = refs.OracleRun(w)
     for it in range(1, 5):
         ref.step(it)
