@@ -39,8 +39,9 @@ class Zero2Schedule:
         self.cs = torch.cuda.Stream(run.dev, priority=-1)
         self.ready = [torch.cuda.Event() for _ in self.ranges]
         # overlapped, the step kernels leave room on every SM for the
-        # backward's blocks (a full-occupancy step holds every register)
-        z.zero_set_step_occupancy(run.ctx, step_blocks_per_sm if mode == "overlap" else 0)
+        # backward's blocks (a full-occupancy step holds every register);
+        # the last bucket's step, after backward, takes every SM again
+        self.cap = step_blocks_per_sm if mode == "overlap" else 0
 
     def _busy(self, phase, stream):
         standin.busy(self.sink.data_ptr(), self.blocks, self.iters[phase], stream.cuda_stream)
@@ -71,6 +72,7 @@ class Zero2Schedule:
             if overlap:
                 self.ready[i].record(cs)            # bucket i's grads exist
                 ss.wait_event(self.ready[i])
+            z.zero_set_step_occupancy(run.ctx, self.cap if i > 0 else 0)
             z.zero_bucket_step(run.ctx, off, cnt, run.bucket_grads(off, cnt), *hp, ss)
         if stepping:
             z.zero_bucket_end(run.ctx, *hp, ss)

@@ -71,7 +71,9 @@ class Zero3Schedule:
         self.gs = torch.cuda.Stream(run.dev, priority=0)
         self.cs = torch.cuda.Stream(run.dev, priority=-1)
         self.ss = torch.cuda.Stream(run.dev, priority=0) if self.overlap_steps else None
-        z.zero_set_step_occupancy(run.ctx, step_blocks_per_sm if self.overlap_steps else 0)
+        # steps beside compute leave room on every SM for its blocks; the
+        # last visit's step, after all compute, takes every SM again
+        self.cap = step_blocks_per_sm if self.overlap_steps else 0
         z.zero_set_gather_mode(run.ctx, z.ZERO_GATHER_LEAN if mode == "overlap"
                                else z.ZERO_GATHER_FAST)
         U = len(self.pieces)
@@ -98,6 +100,7 @@ class Zero3Schedule:
                 self.grads_done[v].record(stream)   # the unit's backward is done
                 self.ss.wait_event(self.grads_done[v])
                 stream = self.ss
+            z.zero_set_step_occupancy(self.run.ctx, self.cap if v + 1 < len(self.visits) else 0)
             run, w = self.run, self.run.w
             f, n = self.pieces[i]
             two_pass = run.scale > 0 and run.shadow is None
