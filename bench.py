@@ -551,6 +551,8 @@ def bench_prefetch(args, rank, world_size, device_index):
     it_f = max(1, int(args.unit_fwd_ms / per_iter))
     times = {}
     bg = args.overlap_steps
+    clocks = Clocks(device_index, args.clocks_csv)
+    clocks.start()
     for mode in ("standin_only" if bg else "compute_only", "serial", "overlap"):
         sch = Zero3Schedule(run, it_f, 2 * it_f, blocks, mode, overlap_steps=bg,
                             step_blocks_per_sm=args.step_blocks_per_sm)
@@ -564,6 +566,7 @@ def bench_prefetch(args, rank, world_size, device_index):
         e1.record(run.stream)
         torch.cuda.synchronize()
         times[mode] = allreduce_max(e0.elapsed_time(e1) / args.steps, world_size)
+    clock_info = clocks.stop()
     base = times["standin_only" if bg else "compute_only"]
     exposed = times["overlap"] - base
     gathers = times["serial"] - base     # with bg: the gathers and the unit steps
@@ -592,7 +595,7 @@ def bench_prefetch(args, rank, world_size, device_index):
         },
         "roofline": None,
         "gpu_launches": (2 * U + 2 * U + U) * args.steps,
-        "clocks": None,
+        "clocks": clock_info,
     }
 
 
@@ -635,6 +638,8 @@ def bench_zero2_overlap(args, rank, world_size, device_index):
     it_f = calibrate_standin(run, blocks, args.unit_fwd_ms)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     times = {}
+    clocks = Clocks(device_index, args.clocks_csv)
+    clocks.start()
     for mode in ("compute_only", "serial", "overlap"):
         sch = Zero2Schedule(run, it_f, 2 * it_f, blocks, mode, args.step_blocks_per_sm)
         for _ in range(args.warmup):
@@ -649,6 +654,7 @@ def bench_zero2_overlap(args, rank, world_size, device_index):
         e1.record(run.stream)
         torch.cuda.synchronize()
         times[mode] = allreduce_max(e0.elapsed_time(e1) / args.steps, world_size)
+    clock_info = clocks.stop()
     exposed = times["overlap"] - times["compute_only"]
     steps_serial = times["serial"] - times["compute_only"]
     updated = w.updated_per_step()
@@ -674,7 +680,7 @@ def bench_zero2_overlap(args, rank, world_size, device_index):
         },
         "roofline": None,
         "gpu_launches": (2 * B + B + 1) * args.steps,
-        "clocks": None,
+        "clocks": clock_info,
     }
 
 
