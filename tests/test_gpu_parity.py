@@ -786,6 +786,19 @@ def test_group_step_parity(rank, scaled):
     run.close()
 
 
+@pytest.mark.parametrize("rank,shadow", [(-1, False), (1, True)])
+def test_group_step_adamw_fp16(rank, shadow):
+    """Groups with AdamW, fp16 grads and params, loss-scaled (two passes, or
+    one pass over two state sets) with a skipped step: the oracle's result
+    bit for bit."""
+    shapes = [(256, 64), (512, 33), (128, 7), (64, 1)]
+    w = W.dim0(shapes, 4, rank=rank, steps=3, loss_scale=2.0 ** 8, inject=(2, 1),
+               weight_decay=0.05).replace(groups=[2, 2], grad_dtype=W.F16, param_dtype=W.F16)
+    run, ref = run_both(w, shadow=shadow)
+    compare_runner(run, ref, what="groups adamw fp16")
+    run.close()
+
+
 @pytest.mark.parametrize("rank", [-1, 2])
 def test_group_with_an_empty_unit(rank):
     """A group holding a unit of zero parameters (and units whose shards are
