@@ -91,15 +91,17 @@ def test_one_rank_7p5b_full(rank):
     w = W.one_rank_7p5b(rank)
     run = run_all(w)
     S = w.shard
-    check_sampled(run, w, sample_positions(S, S), param_off=rank * S)
-    # placement: the full buffer is the concatenation of the shards
+    idx = sample_positions(S, S)
+    check_sampled(run, w, idx, param_off=rank * S)
+    # the own shard's place in the full buffer holds the oracle's params
+    # (sampled, computed element by element on the host)
     full = run.params
+    _, _, _, p = refs.sampled_reference(w, idx, list(range(1, w.steps + 1)), rank=rank)
+    assert gpu_at(full, idx + rank * S).tobytes() == p.tobytes()
+    # placement: every other rank's part of the full buffer is that rank's shard
     for k in range(w.world):
-        part = full[k * S:(k + 1) * S]
-        if k == rank:
-            assert torch.equal(part, run.master.to(torch.bfloat16))
-        else:
-            assert torch.equal(part, run.shards[k])
+        if k != rank:
+            assert torch.equal(full[k * S:(k + 1) * S], run.shards[k])
     # and the shards hold the seeded draws (sampled)
     for k in (0, 1, 33, 63):
         if k == rank:

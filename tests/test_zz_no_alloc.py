@@ -1,18 +1,26 @@
 """zero_step_noalloc: the step for callers that cannot allocate device
 memory (the library supplies the scratch from a built-in 16 MiB array).
 
-Checked against the allocating entry point (zero_step with a bound
-g_scratch) on the same inputs, two calls in a row, with the tolerances of
-the other parity tests: master, m, v within 2e-6*|x| + 1e-9, params within
-1 ulp.  Self-contained, so it passes alone in a fresh process as well as
-after the rest of the suite.
+Checked two ways on the same inputs, two or more calls in a row:
+  - against the allocating entry point (zero_step with a bound g_scratch),
+    with the tolerances of the other parity tests: master, m, v within
+    2e-6*|x| + 1e-9, params within 1 ulp;
+  - against the oracle (tests/refs.OracleRun), bit for bit, skip decisions
+    included, in the forms the header promises: one state set, a second
+    state set bound (the call then updates the current set in place; 16-byte
+    and 4-byte aligned sets), and a bound device scalar block.
+Self-contained, so it passes alone in a fresh process as well as after the
+rest of the suite.
 """
 import numpy as np
 import pytest
 import torch
 
 import synth
+import workloads as W
 import zero_sharded_optimizer_step_gb300 as z
+from tests import refs
+from tests.test_gpu_parity import compare_runner
 
 pytestmark = pytest.mark.gpu
 
@@ -100,6 +108,116 @@ def test_noalloc_skips_like_the_allocating_step():
     torch.cuda.synchronize()
     _close_state(b.master, a.master, "master")
     _close_params(b.params, a.params, "params")
+
+
+# ------------------------------------------------- against the oracle
+
+
+def _noalloc_step(run, it):
+    """Iteration `it` of a Runner's workload through zero_step_noalloc."""
+    w = run.w
+    run.fill_grads(it)
+    hp = run._hp(run.t + 1)           # with a bound scalar block: prepared and copied
+    z.zero_step_noalloc(run.ctx, run.grads[0], *hp, run.scale, run.stream)
+    return run.finish_step()
+
+
+def _scaled(rank=-1):
+    # fp16 grads and params, loss scale 2^12, a +inf in rank 2 at iteration 3
+    w = W.Workload("noalloc", 1_000_003, 8, 2, W.F16, W.F16, rank=rank, steps=5,
+                   loss_scale=2.0 ** 12, inject=(3, 2))
+    if rank >= 0:
+        e = synth.pick_index(w.seed, w.numel, step=3, rank=2)
+        w = w.replace(rank=e // w.shard)      # the planted value falls in this shard
+    return w
+
+
+@pytest.mark.parametrize("rank", [-1, 0])
+def test_noalloc_equals_the_oracle(rank):
+    """One state set, no scratch bound: five calls, the third skipped."""
+    from workloads.runner import Runner
+    w = _scaled(rank)
+    run = Runner(w, scratch=False)
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        _noalloc_step(run, it)
+        ref.step(it)
+    torch.cuda.synchronize()
+    assert run.skips == ref.skips == [False, False, True, False, False]
+    assert run.scale == ref.scale
+    compare_runner(run, ref, exact=True, what="noalloc rank %d" % rank)
+    run.close()
+
+
+def test_noalloc_unscaled_equals_the_oracle():
+    """No loss scaling (loss_scale <= 0): never skips, bf16, ragged world."""
+    from workloads.runner import Runner
+    w = W.Workload("noalloc_u", 777_777, 5, 2, W.BF16, W.BF16, steps=3)
+    run = Runner(w, scratch=False)
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        _noalloc_step(run, it)
+        ref.step(it)
+    torch.cuda.synchronize()
+    compare_runner(run, ref, exact=True, what="noalloc unscaled")
+    run.close()
+
+
+def _bind_offset_shadow(run, float_offset):
+    """A second state set whose buffers start `float_offset` floats into their
+    allocations (0: 16-byte aligned; 1: only 4-byte aligned)."""
+    n = z.zero_ctx_state_elems(run.ctx)
+    bufs = [torch.zeros(n + 8, device=run.dev)[float_offset:float_offset + n] for _ in range(3)]
+    run.shadow = tuple(bufs)
+    run.cur = torch.zeros(1, dtype=torch.int64, device=run.dev)
+    z.zero_bind_shadow(run.ctx, *run.shadow, run.cur)
+
+
+@pytest.mark.parametrize("float_offset", [0, 1])
+def test_noalloc_with_a_second_state_set(float_offset):
+    """With a second state set bound, zero_step (one pass) and
+    zero_step_noalloc alternate: step 1 by zero_step leaves the second set
+    current, step 2 by noalloc updates it in place, step 3 (skipped) by
+    noalloc, step 4 by zero_step writes the first set, step 5 by noalloc.
+    With the set 4-byte aligned only, every launch takes the per-element
+    path; either way the result is the oracle's bit for bit."""
+    from workloads.runner import Runner
+    w = _scaled()
+    run = Runner(w, scratch=False)
+    _bind_offset_shadow(run, float_offset)
+    ref = refs.OracleRun(w)
+    current = []
+    for it in range(1, w.steps + 1):
+        if it in (1, 4):
+            run.step(it)
+        else:
+            _noalloc_step(run, it)
+        ref.step(it)
+        current.append(z.zero_current_state(run.ctx))
+    torch.cuda.synchronize()
+    assert run.skips == ref.skips == [False, False, True, False, False]
+    # noalloc updates the current set in place; zero_step flips it
+    assert current == [1, 1, 1, 0, 0]
+    compare_runner(run, ref, exact=True, what="noalloc shadow offset %d" % float_offset)
+    run.close()
+
+
+def test_noalloc_with_a_device_scalar_block():
+    """A bound device scalar block (zero_bind_hyper + zero_prepare_step before
+    each call): the kernels read the step's scalars from it; the arguments
+    the call gets are ignored.  Bit for bit the oracle's."""
+    from workloads.runner import Runner
+    w = _scaled()
+    run = Runner(w, scratch=False, hyper=True)
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        _noalloc_step(run, it)
+        ref.step(it)
+    torch.cuda.synchronize()
+    assert run.skips == ref.skips
+    compare_runner(run, ref, exact=True, what="noalloc hyper")
+    z.zero_bind_hyper(run.ctx, None)
+    run.close()
 
 
 def test_noalloc_rejects_ranges_beyond_the_builtin_scratch():

@@ -297,16 +297,9 @@ StepArgs make_args(const zero_ctx *c, const Range &r, const void *const *grads)
     a.flag = reinterpret_cast<unsigned long long *>(c->flag);
     a.hyper = static_cast<const zgb::DeviceHyper *>(c->hyper);
     a.slot = c->hyper_slot;
-    bool ok = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16) &&
-              (!a.g || aligned(a.g, 16)) &&
-              (!a.cur || (aligned(a.xb, 16) && aligned(a.mb, 16) && aligned(a.vb, 16)));
-    if (grads) {
-        for (int32_t k = 0; k < c->world; ++k) {
-            a.grads[k] = grads[k];
-            ok = ok && aligned(grads[k], 16);
-        }
-    }
-    a.vec_ok = ok ? 1 : 0;
+    if (grads)
+        for (int32_t k = 0; k < c->world; ++k) a.grads[k] = grads[k];
+    a.vec_ok = zgb::step_vector_path_ok(a) ? 1 : 0;
     return a;
 }
 
@@ -1381,9 +1374,9 @@ extern "C" int zero_step_noalloc(zero_ctx *c, const void *const *grads, int32_t 
 
     StepArgs a = make_args(c, r, grads);
     a.g = scratch;    // every element of the range is written by the reduce pass first
-    bool ok = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16);
-    for (int32_t k = 0; k < c->world; ++k) ok = ok && aligned(grads[k], 16);
-    a.vec_ok = ok ? 1 : 0;
+    // the same predicate as every other launch, over the arguments as they
+    // now stand (a second state set, when bound, still counts)
+    a.vec_ok = zgb::step_vector_path_ok(a) ? 1 : 0;
     a.av = average_scalars(c->world, loss_scale);
     a.step_id = c->step_id;
     rc = finish_launch(c, zgb::launch_reduce(c->gdt, a, c->sms, c->step_per_sm, s),

@@ -78,6 +78,22 @@ struct StepArgs {
     AdamScalars ad;
 };
 
+// Whether the step kernels may take their 16-byte vector path over a range:
+// every buffer they read or write with 16-byte accesses -- the rank grads,
+// master/m/v, the fp32 scratch and, with a second state set bound, that set
+// too -- starts on a 16-byte boundary (null pointers are not accessed).  The
+// params and the stage-1 output are stored at their own alignment
+// (param_align, avg_align) and take no part.  Computed from the finished
+// arguments, so that no launch can leave one of the buffers out.
+inline bool step_vector_path_ok(const StepArgs &a)
+{
+    auto al16 = [](const void *p) { return ((uintptr_t)p & 15) == 0; };
+    bool ok = al16(a.master) && al16(a.m) && al16(a.v) && al16(a.g);
+    if (a.cur) ok = ok && al16(a.xb) && al16(a.mb) && al16(a.vb);
+    for (int32_t k = 0; k < a.world && k < kMaxRanks; ++k) ok = ok && al16(a.grads[k]);
+    return ok;
+}
+
 struct GatherArgs {
     const void *src[kMaxRanks];    // shard k (null = skip)
     char *dst;                     // shard k lands at dst + k * shard_bytes
