@@ -1,7 +1,8 @@
 """Benchmark of the ZeRO sharded optimizer step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--no-e2e] [--no-cpu-baseline] [--graph]
+                    [--extra-workloads A,B|none] [--impl ours|reference]
+                    [--no-e2e] [--no-cpu-baseline] [--graph]
 
 One "step" is one pass of the whole hot path over one batch of synthetic
 grads already resident in HBM.  For the default workload (GPT-2 XL shape,
@@ -19,9 +20,16 @@ between the launches.  A second pass of K steps puts an event pair around
 every launch for the per-kernel durations behind `roofline`: the dominant
 kernel's algorithmic bytes per launch over its average duration, against the
 measured HBM copy bandwidth.  `e2e` repeats the measurement with the grads
-copied from pinned host memory every step and the verdict read back;
+copied from pinned host memory every step, the step's result (the updated
+parameters) copied back to pinned host memory and the verdict read back;
 `cpu_baseline` times the CPU oracle on a bounded sample (all host cores, and
 one).  `--graph` also times replays of one step captured in a CUDA graph.
+
+`config` describes what runs and nothing measured (the reference arm prints
+the same dictionary); the measurements are in `measured`, `roofline`, `e2e`
+and, for the default run, `workloads`: the 7.5B one-rank view with its
+placement, GPT-2 small and the two ZeRO-3 unit paths, each timed after the
+headline in a runner of its own (with its own clocks and e2e).
 
 With --gpus N > 1 (torchrun), every GPU runs its own full replica of the
 workload (the N simulated ranks live on each GPU; no data-path collective):
@@ -116,6 +124,10 @@ def parse():
                          "layers (small cases)")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
+    ap.add_argument("--extra-workloads", default=None,
+                    help="comma-separated workloads timed after the headline one ('none': "
+                         "only the headline); default: %s for the default run"
+                         % ",".join(EXTRA_WORKLOADS))
     return ap.parse_args()
 
 
@@ -211,9 +223,18 @@ class Launch:
         self.kernels = kernels      # kernel launches the call makes
 
 
+class _Library:
+    """The binding, imported at the first call through it: a launch plan can
+    be built (for its algorithmic bytes) where the library is not loaded."""
+
+    def __getattr__(self, name):
+        import zero_sharded_optimizer_step_gb300 as z
+        return getattr(z, name)
+
+
 def step_plan(run):
     """The kernel launches of one step, each with its algorithmic bytes."""
-    import zero_sharded_optimizer_step_gb300 as z
+    z = _Library()
     w, st = run.w, run.stream
     bg = 4 if w.grad_dtype == 0 else 2
     bp = 4 if w.param_dtype == 0 else 2
@@ -226,15 +247,23 @@ def step_plan(run):
 
         def begin_and(fn):
             return lambda: (z.zero_bucket_begin(run.ctx, run.scale), fn())
+        # loss-scaled with one state set: each bucket only reduces into the
+        # scratch, and the end applies Adam to every element
+        two_pass = run.shadow is None and run.scale > 0
         for i, (off, cnt) in enumerate(ranges):
             nv = max(0, min(cnt, n_valid_all - off))
             fn = (lambda off=off, cnt=cnt: z.zero_bucket_step(
                 run.ctx, off, cnt, bufs, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st))
-            plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * cnt,
-                               begin_and(fn) if i == 0 else fn))
+            if two_pass:
+                plan.append(Launch("reduce_kernel", w.world * bg * nv + 4 * cnt,
+                                   begin_and(fn) if i == 0 else fn))
+            else:
+                plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * cnt,
+                                   begin_and(fn) if i == 0 else fn))
+        n_state = w.shard * (w.world if w.rank < 0 else 1)
         kernels_end = 1 if (run.shadow is not None or run.scale > 0) else 0
         plan.append(Launch("finalize_kernel" if run.shadow is not None else "apply_kernel",
-                           0 if run.shadow is not None else (28 + bp) * w.shard * w.world,
+                           (4 + 24 + bp) * n_state if two_pass else 0,
                            lambda: z.zero_bucket_end(run.ctx, w.lr, w.beta1, w.beta2, w.eps,
                                                      run.t + 1, st), kernels=kernels_end))
     elif w.stage < 3:
@@ -359,28 +388,117 @@ def run_step(run, plan, events=None):
         run.t += 1
 
 
-def bench_ours(args, rank, world_size, device_index):
+# Workloads timed after the headline one in the default run, each in its own
+# runner (closed before the next): the 7.5B one-rank view with placement, the
+# GPT-2 small step and the two ZeRO-3 unit paths.
+EXTRA_WORKLOADS = ("one_rank_7p5b", "gpt2_small", "zero3_llama7b", "zero3_gpt2_small")
+
+
+def make_workload(args, name):
+    """The workload `name` with the command line's size overrides; a planted
+    overflow is dropped (the timed steps are the ones that apply)."""
+    import workloads as W
+    sized = ("zero3_llama7b", "fsdp2_llama7b", "fsdp2_llama7b_per_param", "zero3_llama7b_fp16")
+    w = W.ALL[name](**({"n_units": args.units} if args.units and name in sized else {}))
+    if args.numel and name == args.workload:
+        w = w.replace(numel=args.numel, name=w.name + "_numel%d" % args.numel)
+    if w.inject:
+        w = w.replace(inject=None)
+    return w
+
+
+def uses_shadow(args, w):
+    """Loss-scaled workloads step in one pass over two state sets unless
+    --two-pass asks for the scratch-based two passes."""
+    return w.loss_scale > 0 and not args.two_pass
+
+
+def path_of(w, shadow):
+    return ("single pass over two state sets" if shadow else
+            "two passes with an fp32 scratch" if w.loss_scale > 0 else "single pass")
+
+
+def static_plan_bytes(w, shadow):
+    """Algorithmic bytes of one step: the launch plan built on a stand-in for
+    the GPU runner (nothing is allocated or launched)."""
+    from types import SimpleNamespace
+
+    def bucket_ranges():
+        n = w.shard * (w.world if w.rank < 0 else 1)
+        return [(off, min(w.bucket, n - off)) for off in range(0, n, w.bucket)]
+
+    def group_ranges():
+        out, first = [], 0
+        for n in w.groups or []:
+            out.append((first, n))
+            first += n
+        return out
+    shards = None
+    if w.stage == 3:
+        shards = [[None] * w.world for _ in w.units]
+    elif w.rank >= 0 and w.gather_after:
+        shards = [None if k == w.rank else object() for k in range(w.world)]
+    run = SimpleNamespace(w=w, stream=None, shadow=(None,) if shadow else None,
+                          scale=w.loss_scale, grads=[[None]], shards=shards,
+                          grad_avg=object() if w.allreduce_out else None, bucket_buffers=None,
+                          bucket_ranges=bucket_ranges, group_ranges=group_ranges,
+                          group_fulls=[None] * len(w.groups or []), group_grads=None,
+                          params=None, unit_full=None, ctx=None, t=0)
+    return sum(L.alg_bytes for L in step_plan(run))
+
+
+def workload_config(w, shadow):
+    """What a workload is: the same on both arms of the benchmark."""
+    return {"workload": describe(w),
+            "params_updated_per_step": w.updated_per_step(),
+            "alg_bytes_per_step": static_plan_bytes(w, shadow),
+            "method_min_bytes_per_param": method_min_bytes(w),
+            "bucket_elems": w.bucket or None,
+            "path": path_of(w, shadow)}
+
+
+def extra_names(args):
+    if args.extra_workloads is not None:
+        return [n for n in args.extra_workloads.split(",") if n and n != "none"]
+    default_run = (args.workload == "gpt2_xl" and not args.numel and not args.units
+                   and not args.two_pass and not args.graph)
+    return list(EXTRA_WORKLOADS) if default_run else []
+
+
+def static_config(args, world_size):
+    """The line's `config`: the headline workload and the others the run
+    times, described without any measurement (the reference arm prints the
+    same dictionary)."""
+    w = make_workload(args, args.workload)
+    cfg = workload_config(w, uses_shadow(args, w))
+    cfg["l2"] = "inputs larger than L2 (129 MB); no flush between timed steps"
+    cfg["parallelism"] = ("%d simulated data-parallel ranks per GPU; %d GPU replica(s)"
+                          % (w.world, world_size))
+    names = extra_names(args)
+    if names:
+        cfg["workloads"] = {}
+        for n in names:
+            x = make_workload(args, n)
+            cfg["workloads"][n] = workload_config(x, uses_shadow(args, x))
+    return cfg
+
+
+def measure(args, w, shadow, world_size, device_index, steps, kernel_steps, clocks_csv=None):
+    """Time `steps` steps of workload `w` (one pair of CUDA events, nothing
+    between the launches), then `kernel_steps` more with an event pair around
+    every launch for the per-kernel durations.  Returns (figures, runner,
+    plan); the caller closes the runner."""
     import torch
 
     import workloads as W
     from workloads.runner import Runner
 
-    w = W.ALL[args.workload](**({"n_units": args.units} if args.units and
-                                args.workload in ("zero3_llama7b", "fsdp2_llama7b",
-                                                  "fsdp2_llama7b_per_param",
-                                                  "zero3_llama7b_fp16") else {}))
-    if args.numel:
-        w = w.replace(numel=args.numel, name=w.name + "_numel%d" % args.numel)
-    if w.inject:
-        w = w.replace(inject=None)    # timed steps are the ones that apply
     torch.cuda.set_device(device_index)
-    shadow = w.loss_scale > 0 and not args.two_pass
     run = Runner(w, device="cuda:%d" % device_index, shadow=shadow, alloc_grads=not w.bucket)
     if w.bucket:
         import synth
-        import torch as _t
-        dt = {0: _t.float32, 1: _t.bfloat16, 2: _t.float16}[w.grad_dtype]
-        run.bucket_buffers = [_t.empty(w.bucket, dtype=dt, device=run.dev)
+        dt = {0: torch.float32, 1: torch.bfloat16, 2: torch.float16}[w.grad_dtype]
+        run.bucket_buffers = [torch.empty(w.bucket, dtype=dt, device=run.dev)
                               for _ in range(w.world)]
         for k, b in enumerate(run.bucket_buffers):
             synth.fill_device(b.data_ptr(), w.bucket, w.grad_dtype,
@@ -393,70 +511,115 @@ def bench_ours(args, rank, world_size, device_index):
         torch.cuda.synchronize()
         run.stream = torch.cuda.Stream(run.dev)
     plan = step_plan(run)
+    assert sum(L.alg_bytes for L in plan) == static_plan_bytes(w, shadow)
     torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(run.stream)
     for _ in range(args.warmup):
         run_step(run, plan)
+    e1.record(run.stream)
     torch.cuda.synchronize()
+    warm_ms = e0.elapsed_time(e1) / max(1, args.warmup)
+    if steps is None:
+        # a timed region of at least half a second, for the clock samples
+        steps = max(args.steps, min(2000, int(500.0 / max(warm_ms, 1e-3)) + 1))
+    if kernel_steps is None:
+        kernel_steps = min(steps, max(args.steps, 50))
 
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in plan] for _ in range(args.steps)]
-    clocks = Clocks(device_index, args.clocks_csv)
+           for _ in plan] for _ in range(kernel_steps)]
+    clocks = Clocks(device_index, clocks_csv)
     barrier(world_size)
     torch.cuda.synchronize()
     clocks.start()
-    # the step time: K steps bracketed by one pair of events, nothing between
-    # the launches
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(run.stream)
-    for k in range(args.steps):
+    for _ in range(steps):
         run_step(run, plan)
     t_end.record(run.stream)
     torch.cuda.synchronize()
     barrier(world_size)
-    ms = t_start.elapsed_time(t_end)
-    ms_max = allreduce_max(ms, world_size)
-    # the per-kernel durations (the roofline's): K more steps with a pair of
-    # events around every launch (they serialize the launches, so this pass
-    # is not the step time)
+    ms = allreduce_max(t_start.elapsed_time(t_end), world_size)
+    # the per-kernel durations (the roofline's): events between the launches
+    # serialize them, so this pass is not the step time
     torch.cuda.synchronize()
-    for k in range(args.steps):
+    for k in range(kernel_steps):
         run_step(run, plan, ev[k])
     torch.cuda.synchronize()
     clock_info = clocks.stop()
     barrier(world_size)
     assert all(not s for s in run.skips), "a timed step was skipped"
 
-    # per-kernel durations
     per = {}
-    for k in range(args.steps):
+    for k in range(kernel_steps):
         for L, (a, b) in zip(plan, ev[k]):
-            d = per.setdefault(L.name, [0.0, 0, L.alg_bytes])
+            d = per.setdefault(L.name, [0.0, 0])
             d[0] += a.elapsed_time(b)
             d[1] += 1
     dom = max(per, key=lambda n: per[n][0])
-    tot_ms, n_launch, _ = per[dom]
-    alg_per_launch = sum(L.alg_bytes for L in plan if L.name == dom) / \
-        sum(1 for L in plan if L.name == dom)
-    avg_ms = tot_ms / n_launch
-    peak, peak_kind = peaks()
-    achieved = alg_per_launch / (avg_ms * 1e-3) / 1e9
-    kh = src_hash(GATHER_SRC if dom in ("gather_kernel", "gather_rows_kernel") else KERNEL_SRC)
-    tr = None if (args.numel or args.units) else TRAFFIC.get((args.workload, dom))
-    traffic = tr[1] if tr and tr[0] == kh else None
 
-    updated = w.updated_per_step()
-    step_ms = ms_max / args.steps
-    value = updated * world_size / (step_ms * 1e-3)
+    def alg_per_launch(name):
+        sel = [L.alg_bytes for L in plan if L.name == name]
+        return sum(sel) / len(sel)
+    peak, peak_kind = peaks()
+    step_ms = ms / steps
     step_bytes = sum(L.alg_bytes for L in plan)
+    dom_ms = per[dom][0] / per[dom][1]
+    achieved = alg_per_launch(dom) / (dom_ms * 1e-3) / 1e9
+    fig = {
+        "ms_per_step": step_ms,
+        "steps": steps,
+        "params_per_s": w.updated_per_step() * world_size / (step_ms * 1e-3),
+        "alg_bytes_per_step": step_bytes,
+        "step_hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
+        "step_frac_of_peak": step_bytes / (step_ms * 1e-3) / 1e9 / peak,
+        "peak_gbs": peak,
+        "peak_kind": peak_kind,
+        "dominant_kernel": {"name": dom, "ms_per_launch": dom_ms,
+                            "alg_bytes_per_launch": alg_per_launch(dom),
+                            "alg_gbs": achieved, "frac": achieved / peak},
+        "per_kernel_ms": {n: per[n][0] / per[n][1] for n in per},
+        "per_kernel_alg_gbs": {n: alg_per_launch(n) / (per[n][0] / per[n][1] * 1e-3) / 1e9
+                               for n in per if per[n][0] > 0},
+        "per_kernel_timing": "%d more steps with an event pair around every launch"
+                             % kernel_steps,
+        "gpu_launches": sum(L.kernels for L in plan) * steps,
+        "working_set_gb": working_set(run) / 1e9,
+        "clocks": clock_info,
+    }
+    return fig, run, plan
+
+
+def free_memory():
+    """Return the device and pinned host memory of a closed runner."""
+    import gc
+
+    import torch
+    gc.collect()
+    torch.cuda.empty_cache()
+    if hasattr(torch._C, "_host_emptyCache"):
+        torch._C._host_emptyCache()
+
+
+def bench_ours(args, rank, world_size, device_index):
+    w = make_workload(args, args.workload)
+    shadow = uses_shadow(args, w)
+    fig, run, plan = measure(args, w, shadow, world_size, device_index, args.steps, args.steps,
+                             args.clocks_csv)
+    dom = fig["dominant_kernel"]
+    kh = src_hash(GATHER_SRC if dom["name"] in ("gather_kernel", "gather_rows_kernel")
+                  else KERNEL_SRC)
+    tr = None if (args.numel or args.units) else TRAFFIC.get((args.workload, dom["name"]))
+    traffic = tr[1] if tr and tr[0] == kh else None
     result = {
         "metric": METRIC,
-        "value": value,
+        "value": fig["params_per_s"],
         "unit": "params/s",
         "n_gpus": world_size,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": step_ms,
+        "ms_per_step": fig["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -464,57 +627,61 @@ def bench_ours(args, rank, world_size, device_index):
         "storage": {"grads": "f32 bf16 f16".split()[w.grad_dtype],
                     "params": "f32 bf16 f16".split()[w.param_dtype], "state": "f32"},
         "data": "synthetic (seeded counter-based normal draws; no dataset)",
-        "config": {
-            "workload": describe(w),
-            "params_updated_per_step": updated,
-            "alg_bytes_per_step": step_bytes,
-            "step_hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
-            "step_frac_of_peak": step_bytes / (step_ms * 1e-3) / 1e9 / peak,
-            "method_min_bytes_per_param": method_min_bytes(w),
-            "l2": "inputs larger than L2 (working set %.1f GB)" % (working_set(run) / 1e9),
-            "per_kernel_ms": {n: per[n][0] / per[n][1] for n in per},
-            "per_kernel_alg_gbs": {n: sum(L.alg_bytes for L in plan if L.name == n)
-                                   / sum(1 for L in plan if L.name == n)
-                                   / (per[n][0] / per[n][1] * 1e-3) / 1e9
-                                   for n in per if per[n][0] > 0},
-            "per_kernel_timing": "a second pass of the same number of steps with an event "
-                                 "pair around every launch",
-            "parallelism": "%d simulated data-parallel ranks per GPU; %d GPU replica(s)"
-                           % (w.world, world_size),
-            "bucket_elems": w.bucket or None,
-            "path": ("single pass over two state sets" if shadow else
-                     "two passes with an fp32 scratch" if w.loss_scale > 0 else "single pass"),
-        },
+        "config": static_config(args, world_size),
         "roofline": {
-            "kernel": dom,
+            "kernel": dom["name"],
             "bound": "hbm",
-            "achieved": achieved,
-            "peak": peak,
-            "peak_kind": peak_kind,
+            "achieved": dom["alg_gbs"],
+            "peak": fig["peak_gbs"],
+            "peak_kind": fig["peak_kind"],
             "unit": "GB/s",
-            "frac": achieved / peak,
-            "alg_bytes_per_launch": alg_per_launch,
+            "frac": dom["frac"],
+            "alg_bytes_per_launch": dom["alg_bytes_per_launch"],
             "traffic": traffic,
             # the same ncu capture's duration (cold, serialized) and its DRAM rate
             "traffic_ncu_us": tr[2] if traffic is not None else None,
             "traffic_ncu_gbs": traffic / (tr[2] * 1e3) if traffic is not None else None,
         },
-        "gpu_launches": sum(L.kernels for L in plan) * args.steps,
-        "clocks": clock_info,
+        "measured": {k: fig[k] for k in ("alg_bytes_per_step", "step_hbm_gbs",
+                                         "step_frac_of_peak", "per_kernel_ms",
+                                         "per_kernel_alg_gbs", "per_kernel_timing",
+                                         "working_set_gb")},
+        "gpu_launches": fig["gpu_launches"],
+        "clocks": fig["clocks"],
     }
+    updated = w.updated_per_step()
     if args.graph:
         gms = bench_graph(run, plan, args, world_size)
-        result["config"]["graph_ms_per_step"] = gms
-        result["config"]["graph_params_per_s"] = updated * world_size / (gms * 1e-3)
-        result["config"]["eager_ms_per_step"] = step_ms
+        result["measured"]["graph_ms_per_step"] = gms
+        result["measured"]["graph_params_per_s"] = updated * world_size / (gms * 1e-3)
+        result["measured"]["eager_ms_per_step"] = fig["ms_per_step"]
     if not args.no_e2e and not w.bucket:
-        e2e = (bench_e2e_pipelined(run, args, world_size) if w.stage < 3 else
-               bench_e2e_units(run, args, world_size) if w.rank >= 0 else None)
-        result["e2e"] = e2e or bench_e2e(run, plan, args, world_size)
-    if not args.no_cpu_baseline and rank == 0:
+        result["e2e"] = run_e2e(run, plan, args, world_size)
+    if not args.no_cpu_baseline and rank == 0 and world_size == 1:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
     run.close()
+    del run, plan
+    free_memory()
+    names = extra_names(args)
+    if names:
+        result["workloads"] = {}
+    for n in names:
+        x = make_workload(args, n)
+        fx, rx, px = measure(args, x, uses_shadow(args, x), world_size, device_index, None, None)
+        if not args.no_e2e and not x.bucket:
+            fx["e2e"] = run_e2e(rx, px, args, world_size)
+        rx.close()
+        del rx, px
+        free_memory()
+        result["workloads"][n] = fx
     return result
+
+
+def run_e2e(run, plan, args, world_size):
+    w = run.w
+    e2e = (bench_e2e_pipelined(run, args, world_size) if w.stage < 3 else
+           bench_e2e_units(run, args, world_size) if w.rank >= 0 else None)
+    return e2e or bench_e2e(run, plan, args, world_size)
 
 
 def bench_prefetch(args, rank, world_size, device_index):
@@ -842,18 +1009,33 @@ def describe(w):
                " weight_decay=%g" % w.weight_decay if w.weight_decay else "", units))
 
 
+def host_ram_available():
+    try:
+        return int(open("/proc/meminfo").read().split("MemAvailable:")[1].split()[0]) * 1024
+    except Exception:
+        return 32 << 30
+
+
+def result_view(run):
+    """The step's result in device memory, which e2e copies back to the host:
+    the full parameter buffer (all ranks), the rank's own shard of it (one
+    rank's view), or the rank's persistent parameter shards (stage 3)."""
+    w = run.w
+    if w.stage < 3 and w.rank >= 0:
+        return run.params[w.rank * w.shard:(w.rank + 1) * w.shard]
+    return run.params
+
+
 def bench_e2e(run, plan, args, world_size):
     """Same step, with every rank's grads copied from pinned host memory each
-    step and the verdict word read back to the host."""
+    step, the step's result (result_view) copied back to pinned host memory
+    after it, and the verdict word read back to the host."""
     import torch
     import zero_sharded_optimizer_step_gb300 as z
 
     dev_bufs = [t for row in run.grads for t in row] or list(getattr(run, "bucket_buffers", []))
     h2d = sum(t.numel() * t.element_size() for t in dev_bufs)
-    try:
-        avail = int(open("/proc/meminfo").read().split("MemAvailable:")[1].split()[0]) * 1024
-    except Exception:
-        avail = 32 << 30
+    avail = host_ram_available()
     # the ranks on this node share its RAM
     local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", str(world_size)))
     cap = min(h2d, int(0.3 * avail / max(1, local_ranks)), 64 << 30)
@@ -868,6 +1050,8 @@ def bench_e2e(run, plan, args, world_size):
         h.copy_(t)
         host.append(h)
         used += nb
+    out_dev = result_view(run)
+    out_host = torch.empty(out_dev.numel(), dtype=out_dev.dtype, pin_memory=True)
     st = run.stream
     steps = max(2, args.e2e_steps)
 
@@ -877,6 +1061,8 @@ def bench_e2e(run, plan, args, world_size):
                 t.copy_(host[i % len(host)], non_blocking=True)
         for L in plan:
             L.fn()
+        with torch.cuda.stream(st):
+            out_host.copy_(out_dev, non_blocking=True)
         z.zero_step_status(run.ctx)       # 8-byte read of the verdict
         if run.scale > 0:
             run.scale, run.good = z.zero_scale_update(run.scale, False, run.good,
@@ -891,17 +1077,69 @@ def bench_e2e(run, plan, args, world_size):
         one()
     torch.cuda.synchronize()
     dt = allreduce_max(time.perf_counter() - t0, world_size)
+    d2h = out_dev.numel() * out_dev.element_size()
     return {"value": run.w.updated_per_step() * world_size * steps / dt, "unit": "params/s",
             "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": 8, "host_buffers_distinct": len(host),
-            "device_buffers": len(dev_bufs)}
+            "d2h_bytes_per_step": d2h + 8, "d2h_result_bytes": d2h, "d2h_verdict_bytes": 8,
+            "host_buffers_distinct": len(host), "device_buffers": len(dev_bufs),
+            "path": "whole-step copies on the step's stream"}
+
+
+class ResultCopy:
+    """The device-to-host copy of a step's result on a stream of its own,
+    started once the step's last kernel is done, so that it runs while the
+    next step's host-to-device copies go the other way over the link.  The
+    result is copied in pieces; the next step's first write into piece i
+    waits for piece i's copy (wait_before_write)."""
+
+    def __init__(self, run, pieces):
+        import torch
+        self.torch = torch
+        self.dev = result_view(run)
+        self.host = torch.empty(self.dev.numel(), dtype=self.dev.dtype, pin_memory=True)
+        self.stream = torch.cuda.Stream(run.dev)
+        self.pieces = pieces                     # (offset, count) into the result
+        self.done = [torch.cuda.Event() for _ in pieces]
+        self.issued = False
+        self.pairs = []
+        self.bytes = self.dev.numel() * self.dev.element_size()
+
+    def wait_before_write(self, stream, i):
+        if self.issued:
+            stream.wait_event(self.done[i])
+
+    def start(self, after_stream, record=False):
+        torch = self.torch
+        ready = torch.cuda.Event()
+        ready.record(after_stream)
+        with torch.cuda.stream(self.stream):
+            self.stream.wait_event(ready)
+            if record:
+                self.pairs.append((torch.cuda.Event(enable_timing=True),
+                                   torch.cuda.Event(enable_timing=True)))
+                self.pairs[-1][0].record(self.stream)
+            for (off, cnt), ev in zip(self.pieces, self.done):
+                if cnt > 0:
+                    self.host[off:off + cnt].copy_(self.dev[off:off + cnt], non_blocking=True)
+                ev.record(self.stream)
+            if record:
+                self.pairs[-1][1].record(self.stream)
+        self.issued = True
+
+    def report(self, steps):
+        ms = sum(a.elapsed_time(b) for a, b in self.pairs) / max(1, steps)
+        return {"d2h_copy_ms_per_step": ms,
+                "d2h_gbs_while_stepping": self.bytes / (ms * 1e-3) / 1e9 if ms > 0 else None}
 
 
 def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
     """The end-to-end step through the bucketed API: while bucket b is
     stepped on the compute stream, bucket b+1's grads of every rank are
     copied from pinned host memory on a copy stream into the other of two
-    device buffer sets; then the verdict word is read back.  Same result as
+    device buffer sets; once the step's verdict is applied (zero_bucket_end)
+    its result -- the full parameter buffer, or the rank's own shard of it --
+    goes back to pinned host memory on a third stream, beside the next step's
+    host-to-device copies; the verdict word is read back.  Same result as
     zero_step; the host link bounds it."""
     import torch
     import zero_sharded_optimizer_step_gb300 as z
@@ -909,12 +1147,10 @@ def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
     w = run.w
     srcs = run.grads[0]                       # rank k's local grads (or slices)
     h2d = sum(t.numel() * t.element_size() for t in srcs)
-    try:
-        avail = int(open("/proc/meminfo").read().split("MemAvailable:")[1].split()[0]) * 1024
-    except Exception:
-        avail = 32 << 30
+    out = result_view(run)
+    avail = host_ram_available()
     local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", str(world_size)))
-    if h2d > int(0.3 * avail / max(1, local_ranks)):
+    if h2d + out.numel() * out.element_size() > int(0.3 * avail / max(1, local_ranks)):
         return None                           # not enough pinned RAM for distinct inputs
     host = []
     for t in srcs:
@@ -930,6 +1166,9 @@ def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
     n_range = w.shard * (w.world if w.rank < 0 else 1)
     n_valid = srcs[0].numel()
     ranges = [(off, min(bucket, n_range - off)) for off in range(0, n_range, bucket)]
+    # the result in the same pieces as the buckets: bucket b's step writes
+    # only piece b, so it waits only for piece b of the previous result
+    back = ResultCopy(run, ranges)
 
     pairs = []        # event pairs around each bucket's copies (timed steps)
 
@@ -952,10 +1191,12 @@ def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
                     pairs[-1][1].record(cp)
                 ready[k2].record(cp)
             st.wait_event(ready[k2])
+            back.wait_before_write(st, b)
             z.zero_bucket_step(run.ctx, off, cnt, [d[:max(nv, 1)] for d in dev[k2]], w.lr,
                                w.beta1, w.beta2, w.eps, run.t + 1, st)
             done[k2].record(st)
         z.zero_bucket_end(run.ctx, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st)
+        back.start(st, record)                 # the result, final now, back to the host
         if run.shards is not None:
             z.zero_allgather(run.ctx, run.shards, run.params, w.param_dtype, st)
         nonfinite, skipped = z.zero_step_status(run.ctx)   # 8-byte read of the verdict
@@ -972,25 +1213,33 @@ def bench_e2e_pipelined(run, args, world_size, bucket=1 << 25):
     t0 = time.perf_counter()
     for _ in range(steps):
         one(record=True)
-    torch.cuda.synchronize()
+    torch.cuda.synchronize()                  # the last result copy included
     dt = allreduce_max(time.perf_counter() - t0, world_size)
     copy_ms = sum(a.elapsed_time(b) for a, b in pairs) / steps
-    return {"value": w.updated_per_step() * world_size * steps / dt, "unit": "params/s",
-            "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
-            # the time the copy stream spent copying, and the link rate it saw
-            "h2d_copy_ms_per_step": copy_ms,
-            "h2d_gbs_while_stepping": h2d / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None,
-            "d2h_bytes_per_step": 8, "host_buffers_distinct": len(host),
-            "device_buffers": len(srcs),
-            "path": "bucketed step (%d-element buckets) overlapped with the host-to-device "
-                    "copies of the next bucket" % bucket}
+    res = {"value": w.updated_per_step() * world_size * steps / dt, "unit": "params/s",
+           "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
+           # the time the copy stream spent copying, and the link rate it saw
+           "h2d_copy_ms_per_step": copy_ms,
+           "h2d_gbs_while_stepping": h2d / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None,
+           "d2h_bytes_per_step": back.bytes + 8, "d2h_result_bytes": back.bytes,
+           "d2h_verdict_bytes": 8,
+           "d2h_result": ("the full parameter buffer" if w.rank < 0 else
+                          "rank %d's own shard of the parameter buffer" % w.rank),
+           "host_buffers_distinct": len(host) + 1, "device_buffers": len(srcs)}
+    res.update(back.report(steps))
+    res["path"] = ("bucketed step (%d-element buckets) overlapped with the host-to-device "
+                   "copies of the next bucket; the result's copy back overlaps the next "
+                   "step's" % bucket)
+    return res
 
 
 def bench_e2e_units(run, args, world_size):
     """ZeRO-3 end to end: each unit's grads (all ranks' slices; for a grouped
     workload each group's per-rank buffers) are copied from pinned host memory
     on a copy stream into one of two device buffer sets while the previous
-    unit is gathered and stepped; then the verdict is read back."""
+    unit is gathered and stepped; after the step the rank's updated parameter
+    shards go back to pinned host memory beside the next step's copies; the
+    verdict is read back."""
     import torch
     import zero_sharded_optimizer_step_gb300 as z
 
@@ -1002,12 +1251,10 @@ def bench_e2e_units(run, args, world_size):
         pieces = [(u, 1) for u in range(len(w.units))]
         src = run.grads
     h2d = sum(t.numel() * t.element_size() for row in src for t in row)
-    try:
-        avail = int(open("/proc/meminfo").read().split("MemAvailable:")[1].split()[0]) * 1024
-    except Exception:
-        avail = 32 << 30
+    out = result_view(run)
+    avail = host_ram_available()
     local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", str(world_size)))
-    if h2d > int(0.3 * avail / max(1, local_ranks)):
+    if h2d + out.numel() * out.element_size() > int(0.3 * avail / max(1, local_ranks)):
         return None
     host = []
     for row in src:
@@ -1026,6 +1273,15 @@ def bench_e2e_units(run, args, world_size):
     st = run.stream
     ready = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
+    # the result in one piece per unit (or group): a piece's next write is its
+    # own update in the next step's backward
+    offs = []
+    for f, n in pieces:
+        lo = z.zero_ctx_unit_param_offset(run.ctx, f)
+        hi = (z.zero_ctx_unit_param_offset(run.ctx, f + n) if f + n < len(w.units)
+              else out.numel())
+        offs.append((lo, hi - lo))
+    back = ResultCopy(run, offs)
 
     def gather(i):
         f, n = pieces[i]
@@ -1071,12 +1327,17 @@ def bench_e2e_units(run, args, world_size):
                 ready[k2].record(cp)
             gather(i)
             st.wait_event(ready[k2])
+            back.wait_before_write(st, i)
             step(i, views)
             done[k2].record(st)
+        # the finalize (which recasts every unit on a skipped step) and the
+        # apply come after every unit's update, each of which waited for its
+        # piece of the previous result
         if run.shadow is not None:
             z.zero3_end_step(run.ctx, st)
         elif run.scale > 0:
             z.zero_step_apply(run.ctx, w.lr, w.beta1, w.beta2, w.eps, run.t + 1, st)
+        back.start(st, record)
         _, skipped = z.zero_step_status(run.ctx)             # 8-byte read of the verdict
         if run.scale > 0:
             run.scale, run.good = z.zero_scale_update(run.scale, skipped, run.good,
@@ -1094,15 +1355,21 @@ def bench_e2e_units(run, args, world_size):
     torch.cuda.synchronize()
     dt = allreduce_max(time.perf_counter() - t0, world_size)
     copy_ms = sum(a.elapsed_time(b) for a, b in pairs) / steps
-    return {"value": w.updated_per_step() * world_size * steps / dt, "unit": "params/s",
-            "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
-            # the time the copy stream spent copying, and the link rate it saw
-            "h2d_copy_ms_per_step": copy_ms,
-            "h2d_gbs_while_stepping": h2d / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None,
-            "d2h_bytes_per_step": 8, "host_buffers_distinct": sum(len(r) for r in host),
-            "device_buffers": 2 * len(dev[0]),
-            "path": "per-%s host-to-device copies overlapped with the previous %s's gather "
-                    "and step" % (("group", "group") if w.groups else ("unit", "unit"))}
+    res = {"value": w.updated_per_step() * world_size * steps / dt, "unit": "params/s",
+           "ms_per_step": dt / steps * 1e3, "h2d_bytes_per_step": h2d,
+           # the time the copy stream spent copying, and the link rate it saw
+           "h2d_copy_ms_per_step": copy_ms,
+           "h2d_gbs_while_stepping": h2d / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None,
+           "d2h_bytes_per_step": back.bytes + 8, "d2h_result_bytes": back.bytes,
+           "d2h_verdict_bytes": 8,
+           "d2h_result": "rank %d's persistent parameter shards of every unit" % w.rank,
+           "host_buffers_distinct": sum(len(r) for r in host) + 1,
+           "device_buffers": 2 * len(dev[0])}
+    res.update(back.report(steps))
+    res["path"] = ("per-%s host-to-device copies overlapped with the previous %s's gather "
+                   "and step; the result's copy back overlaps the next step's"
+                   % (("group", "group") if w.groups else ("unit", "unit")))
+    return res
 
 
 # ---------------------------------------------------------------- the oracle
@@ -1222,10 +1489,9 @@ def cpu_baseline(w, budget_s=10.0, steps=4):
 
 
 def bench_reference(args, rank, world_size):
-    import workloads as W
     if rank != 0:
         return None
-    w = W.ALL[args.workload]()
+    w = make_workload(args, args.workload)
     T = host_threads()
     n_s = 1 << 22
     _, warm = oracle_time(w, n_s, max(1, min(args.warmup, 2)), T)
@@ -1242,7 +1508,11 @@ def bench_reference(args, rank, world_size):
             "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / len(times), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": describe(w)},
+            "storage": {"grads": "f32 bf16 f16".split()[w.grad_dtype],
+                        "params": "f32 bf16 f16".split()[w.param_dtype], "state": "f32"},
+            "data": "synthetic (seeded counter-based normal draws; no dataset)",
+            # the very dictionary the GPU arm prints for the same command line
+            "config": static_config(args, world_size),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

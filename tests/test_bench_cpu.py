@@ -84,32 +84,30 @@ def test_reference_arm_under_torchrun_two_ranks():
 def _plan_bytes(w, shadow=False):
     """The bench's per-step algorithmic bytes for a workload, from its launch
     plan built on a stand-in for the GPU runner (no launch is made)."""
-    from types import SimpleNamespace
     sys.path.insert(0, ROOT)
     import bench
+    return bench.static_plan_bytes(w, shadow)
 
-    def bucket_ranges():
-        n = w.shard * (w.world if w.rank < 0 else 1)
-        return [(off, min(w.bucket, n - off)) for off in range(0, n, w.bucket)]
 
-    def group_ranges():
-        out, first = [], 0
-        for n in w.groups or []:
-            out.append((first, n))
-            first += n
-        return out
-    shards = None
-    if w.stage == 3:
-        shards = [[None] * w.world for _ in w.units]
-    elif w.rank >= 0 and w.gather_after:
-        shards = [None if k == w.rank else object() for k in range(w.world)]
-    run = SimpleNamespace(w=w, stream=None, shadow=(None,) if shadow else None,
-                          scale=w.loss_scale, grads=[[None]], shards=shards,
-                          grad_avg=object() if w.allreduce_out else None, bucket_buffers=None,
-                          bucket_ranges=bucket_ranges, group_ranges=group_ranges,
-                          group_fulls=[None] * len(w.groups or []), group_grads=None,
-                          params=None, unit_full=None, ctx=None, t=0)
-    return sum(L.alg_bytes for L in bench.step_plan(run))
+def test_reference_arm_prints_the_gpu_arms_config():
+    """Both arms describe the run with the same `config` dictionary: the
+    default command line (GPT-2 XL headline plus the four other workloads)
+    and a single-workload one."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for extra in ([], ["--workload", "gpt2_small"]):
+        lines = _run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                      "--warmup", "1", *extra])
+        d = _check(lines[0])
+        old = sys.argv
+        sys.argv = ["bench.py", *extra]
+        try:
+            want = bench.static_config(bench.parse(), 1)
+        finally:
+            sys.argv = old
+        assert d["config"] == want
+        assert ("workloads" in want) == (not extra)
+    assert set(want) >= {"workload", "params_updated_per_step", "alg_bytes_per_step"}
 
 
 def test_algorithmic_bytes_match_the_closed_forms():
@@ -124,6 +122,10 @@ def test_algorithmic_bytes_match_the_closed_forms():
     assert _plan_bytes(xl) == (16 * 2 + 4) * psi + (4 + 24 + 2) * psi        # two passes
     assert _plan_bytes(W.gpt2_xl_adamw(), shadow=True) == 58 * psi
     assert _plan_bytes(W.gpt2_xl_bucketed(), shadow=True) == 58 * psi
+    # bucketed, loss-scaled with one state set: a reduce per bucket, one apply
+    assert _plan_bytes(W.gpt2_xl_bucketed()) == (16 * 2 + 4) * psi + (4 + 24 + 2) * psi
+    # bucketed without loss scaling: the buckets' fused passes only
+    assert _plan_bytes(W.gpt2_xl_bucketed().replace(loss_scale=0.0)) == 58 * psi
     sm = W.gpt2_small()
     assert _plan_bytes(sm) == 42 * sm.numel
     assert _plan_bytes(W.gpt2_small_stage1()) == 44 * sm.numel
