@@ -349,17 +349,41 @@ def step_plan(run):
             nv = sum(min(w.unit_shard(u), max(0, w.units[u] - w.rank * w.unit_shard(u)))
                      for u in range(f, f + n))
             return S, nv
+        def visit(i):
+            # unit i's update and unit i-1's gather in one call
+            return lambda: z.zero3_step_unit_gather(run.ctx, i, run.grads[i], w.lr, w.beta1,
+                                                    w.beta2, w.eps, run.t + 1, i - 1,
+                                                    run.shards[i - 1], run.unit_full, st)
+        # the Runner's backward: a unit's update and the next unit's gather as
+        # one call, which the library makes one launch when the gathered
+        # shards are under 32 MiB (and two, the separate calls', otherwise)
+        fused_visits = one_pass and not w.groups and getattr(run, "visits", "fused") == "fused"
         for i in range(len(pieces)):
             S, _ = sizes(i)
             plan.append(Launch(gname(i), 2 * bp * S * w.world, gather(i)))
         total_S = 0
-        for i in reversed(range(len(pieces))):
+        U = len(pieces)
+        for i in reversed(range(U)):
             S, nv = sizes(i)
             total_S += S
+            step_bytes = w.world * bg * nv + (24 + bp) * S
+            if fused_visits:
+                if i == U - 1:
+                    plan.append(Launch(gname(i), 2 * bp * S * w.world, gather(i)))
+                if i == 0:
+                    plan.append(Launch("fused_step_kernel", step_bytes, update(i)))
+                elif gname(i - 1) == "gather_kernel":
+                    Sg, _ = sizes(i - 1)
+                    plan.append(Launch("step_gather_kernel", step_bytes + 2 * bp * Sg * w.world,
+                                       visit(i)))
+                else:
+                    Sg, _ = sizes(i - 1)
+                    plan.append(Launch("fused_step_kernel", step_bytes, update(i)))
+                    plan.append(Launch(gname(i - 1), 2 * bp * Sg * w.world, gather(i - 1)))
+                continue
             plan.append(Launch(gname(i), 2 * bp * S * w.world, gather(i)))
             if one_pass:
-                plan.append(Launch("fused_step_kernel", w.world * bg * nv + (24 + bp) * S,
-                                   update(i)))
+                plan.append(Launch("fused_step_kernel", step_bytes, update(i)))
             else:
                 plan.append(Launch("reduce_kernel", w.world * bg * nv + 4 * S, update(i)))
         if shadow:

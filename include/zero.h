@@ -505,6 +505,29 @@ int zero3_step_unit(zero_ctx *ctx, int32_t unit, const void *const *grads,
                     int32_t n_grads, double lr, double beta1, double beta2, double eps,
                     int64_t t, void *stream);
 
+/* One visit of the stage-3 backward in one call: unit `unit`'s step (as
+ * zero3_step_unit, same arguments and conditions) and the gather of unit
+ * `gather_unit`'s shards into unit_full (as zero3_gather_unit).  In the
+ * backward each unit is gathered before its backward and reduce-scattered
+ * and updated after it ("ZeRO 与 FSDP…", section ZeRO-3 与 FSDP), so once unit
+ * u's backward is done, u's update and the gather of the unit visited next
+ * (u - 1) are both due; issuing them together saves one launch per unit,
+ * which is most of the cost of small units.  The result equals the two
+ * calls in either order, bit for bit.
+ *   - gather_unit must differ from unit, and the two halves must touch
+ *     disjoint memory: unit_full and the shards may not overlap the stepped
+ *     unit's params, state, flag or current-set word, and unit_full may not
+ *     overlap its grads (ZERO_EINVAL, nothing launched).
+ *   - One launch (a kernel whose first blocks run the unit's fused pass and
+ *     whose other blocks place the shards) for the default gather mode;
+ *     in the lean mode, with a bound scalar block, with a capped step
+ *     occupancy, or for shards of 32 MiB or more it makes the two launches
+ *     of the two calls instead. */
+int zero3_step_unit_gather(zero_ctx *ctx, int32_t unit, const void *const *grads,
+                           int32_t n_grads, double lr, double beta1, double beta2, double eps,
+                           int64_t t, int32_t gather_unit, const void *const *shards,
+                           int32_t n_shards, void *unit_full, void *stream);
+
 /* Loss-scaled stage 3: first pass for one unit (as zero_step_reduce on the
  * unit's range).  After every unit, one zero_step_apply() applies Adam to all
  * units, or to none if any unit overflowed. */

@@ -133,6 +133,29 @@ def test_zero3_llama7b_full():
     run.close()
 
 
+def test_zero3_gpt2_small_full():
+    """ZeRO-3 over GPT-2 small's 14 units (embeddings, 12 blocks, final norm;
+    rank 0 of 8) in the launch configuration the benchmark times: each
+    backward visit one launch (a unit's update with the next unit's gather).
+    Sampled state of the embeddings, a block and the norm match the oracle;
+    the last gather (unit 0, before its backward) placed the other ranks'
+    shards."""
+    from zero_sharded_optimizer_step_gb300 import zero_ctx_unit_state_offset
+    w = W.zero3_gpt2_small()
+    run = run_all(w)
+    assert run.visits == "fused" and run.skips == [False] * w.steps
+    for u in (0, 6, 13):
+        Su = w.unit_shard(u)
+        off = zero_ctx_unit_state_offset(run.ctx, u)
+        idx = sample_positions(Su, Su, seed=u, n_rand=1 << 16)
+        check_sampled(run, w, idx, unit=u, state_off=off)
+    S0 = w.unit_shard(0)
+    for k in range(w.world):
+        if k != w.rank:
+            assert torch.equal(run.unit_full[k * S0:(k + 1) * S0], run.shards[0][k])
+    run.close()
+
+
 def test_fsdp2_llama7b_grouped_full():
     """32 Llama-7B layers as 288 per-parameter dim-0 units, each layer's nine
     gathered and stepped as one group (the grads of a group end to end per

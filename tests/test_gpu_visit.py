@@ -1,0 +1,182 @@
+"""zero3_step_unit_gather: a ZeRO-3 backward visit (unit u's update and the
+gather of unit u-1) in one call, against the oracle.
+
+Every gathered buffer (forward and backward) and the final state and params
+match the oracle bit for bit; the one-call visit equals the two separate
+calls; the library refuses a visit whose halves would touch the same memory
+(nothing launched); large shards, the lean gather mode, a bound scalar block
+and a capped step occupancy take the two-launch form with the same results.
+"""
+import pytest
+import torch
+
+import workloads as W
+import zero_sharded_optimizer_step_gb300 as z
+from tests import refs
+from tests.test_gpu_parity import compare_runner, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _visit_step(run, it, seen=None):
+    """One ZeRO-3 step with fused backward visits, recording what every
+    gather left in the unit buffer (the buffer is read after each call)."""
+    w = run.w
+    run.fill_grads(it)
+    hp = run._hp(run.t + 1)
+    U = len(w.units)
+    z.zero3_begin_step_scaled(run.ctx, run.scale)
+
+    def look(u):
+        if seen is not None:
+            torch.cuda.synchronize()
+            seen.append(to_np(run.unit_full[:w.unit_shard(u) * w.world]).copy())
+    for u in range(U):
+        z.zero3_gather_unit(run.ctx, u, run.shards[u], run.unit_full, run.stream)
+        look(u)
+    z.zero3_gather_unit(run.ctx, U - 1, run.shards[U - 1], run.unit_full, run.stream)
+    look(U - 1)
+    for u in reversed(range(1, U)):
+        z.zero3_step_unit_gather(run.ctx, u, run.grads[u], *hp, u - 1, run.shards[u - 1],
+                                 run.unit_full, run.stream)
+        look(u - 1)
+    z.zero3_step_unit(run.ctx, 0, run.grads[0], *hp, run.stream)
+    if run.shadow is not None:
+        z.zero3_end_step(run.ctx, run.stream)
+    return run.finish_step()
+
+
+CASES = [
+    # (rank, grad dtype, param dtype, loss-scaled with two state sets)
+    (1, W.BF16, W.BF16, False),
+    (-1, W.BF16, W.BF16, False),
+    (0, W.F16, W.F16, True),
+    (-1, W.F16, W.F16, True),
+    (2, W.F32, W.BF16, False),
+    (3, W.BF16, W.F32, True),
+]
+
+
+@pytest.mark.parametrize("rank,gdt,pdt,scaled", CASES)
+def test_visits_equal_the_oracle(rank, gdt, pdt, scaled):
+    """Units of uneven sizes (an empty one and a 7-element one among them),
+    4 ranks; loss-scaled cases plant a +inf at iteration 2 (every unit's
+    update is discarded and the params recast)."""
+    from workloads.runner import Runner
+    units = [100_003, 7, 0, 250_000, 33_333, 4096]
+    w = W.Workload("visit", sum(units), 4, 3, gdt, pdt, rank=rank, units=units, steps=3,
+                   loss_scale=2.0 ** 10 if scaled else 0.0, inject=(2, 1) if scaled else None)
+    run = Runner(w, shadow=scaled)
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        seen = []
+        _visit_step(run, it, seen)
+        ref.step(it)
+        want = [g[2] for g in ref.gathers[-2 * len(units):]]
+        assert len(seen) == len(want)
+        for a, b in zip(seen, want):
+            assert a.tobytes() == b.tobytes()
+    assert run.skips == ref.skips
+    if scaled and rank < 0:
+        assert ref.skips == [False, True, False]
+    compare_runner(run, ref, what="visits %s" % ((rank, gdt, pdt, scaled),))
+    run.close()
+
+
+@pytest.mark.parametrize("mode", ["lean", "hyper", "capped", "large"])
+def test_two_launch_forms_equal_the_oracle(mode):
+    """The forms in which the call makes the two separate launches."""
+    from workloads.runner import Runner
+    if mode == "large":
+        # shards of 32 MiB and more take the row placement: 16,777,216 bf16
+        # elements per shard, then a small unit
+        units = [4 * (1 << 24) + 12, 60_000]
+        rank = 1
+    else:
+        units = [200_000, 33_333, 120_000]
+        rank = 0
+    w = W.Workload("visit2", sum(units), 4, 3, W.BF16, W.BF16, rank=rank, units=units,
+                   steps=2)
+    run = Runner(w, hyper=mode == "hyper")
+    if mode == "lean":
+        z.zero_set_gather_mode(run.ctx, z.ZERO_GATHER_LEAN)
+    if mode == "capped":
+        z.zero_set_step_occupancy(run.ctx, 2)
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        seen = []
+        _visit_step(run, it, seen if mode != "large" else None)
+        ref.step(it)
+        if mode != "large":
+            want = [g[2] for g in ref.gathers[-2 * len(units):]]
+            for a, b in zip(seen, want):
+                assert a.tobytes() == b.tobytes()
+    torch.cuda.synchronize()
+    compare_runner(run, ref, what="visit two launches %s" % mode)
+    if mode == "large":
+        # the last gather placed unit 0's shards
+        S0 = w.unit_shard(0)
+        full = to_np(run.unit_full[:S0 * w.world])
+        want = ref.gathers[-1][2]
+        assert full.tobytes() == want.tobytes()
+    if mode == "hyper":
+        z.zero_bind_hyper(run.ctx, None)
+    run.close()
+
+
+def test_fused_visits_equal_separate_calls():
+    """The Runner's two backward forms on one workload: identical bits."""
+    from workloads.runner import Runner
+    units = [300_001, 150_000, 77_777, 500_000]
+    w = W.Workload("visit3", sum(units), 8, 3, W.F16, W.F16, rank=5, units=units, steps=3,
+                   loss_scale=2.0 ** 12, inject=(2, 3))
+    a = Runner(w, shadow=True, visits="fused")
+    b = Runner(w, shadow=True, visits="separate")
+    for it in range(1, w.steps + 1):
+        a.step(it)
+        b.step(it)
+    torch.cuda.synchronize()
+    assert a.skips == b.skips
+    for x, y in zip(a.state(), b.state()):
+        assert torch.equal(x, y)
+    assert torch.equal(a.params, b.params)
+    assert torch.equal(a.unit_full, b.unit_full)
+    a.close()
+    b.close()
+
+
+def test_visits_that_would_overlap_are_refused():
+    """A unit buffer that overlaps the stepped unit's params, state or grads,
+    shards that overlap its params, or the same unit on both halves: the call
+    returns ZERO_EINVAL and launches nothing."""
+    from workloads.runner import Runner
+    units = [50_000, 40_000, 30_000]
+    w = W.Workload("visit4", sum(units), 4, 3, W.BF16, W.BF16, rank=0, units=units, steps=1)
+    run = Runner(w)
+    run.fill_grads(1)
+    z.zero3_begin_step(run.ctx)
+    torch.cuda.synchronize()
+    before = [t.clone() for t in (run.master, run.m, run.v, run.params, run.unit_full)]
+    hp = (w.lr, w.beta1, w.beta2, w.eps, 1)
+    off2 = z.zero_ctx_unit_param_offset(run.ctx, 2)
+    soff2 = z.zero_ctx_unit_state_offset(run.ctx, 2)
+    bad = [
+        # unit_full starting inside unit 2's params
+        (2, 1, run.shards[1], run.params[off2:]),
+        # unit_full ending inside unit 2's master (viewed as bf16)
+        (2, 1, run.shards[1], run.master[soff2 - 100:].view(torch.bfloat16)),
+        # unit_full over one of unit 2's grad slices
+        (2, 1, run.shards[1], run.grads[2][3]),
+        # a shard that is unit 2's own params
+        (2, 1, [run.params[off2:]] + list(run.shards[1][1:]), run.unit_full),
+        # the same unit on both halves
+        (1, 1, run.shards[1], run.unit_full),
+    ]
+    for unit, gu, shards, full in bad:
+        with pytest.raises(z.ZeroError) as ei:
+            z.zero3_step_unit_gather(run.ctx, unit, run.grads[unit], *hp, gu, shards, full)
+        assert ei.value.code == z.ZERO_EINVAL
+    torch.cuda.synchronize()
+    for x, y in zip(before, (run.master, run.m, run.v, run.params, run.unit_full)):
+        assert torch.equal(x, y)
+    run.close()

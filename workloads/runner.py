@@ -32,8 +32,13 @@ def inject_index(w: Workload, it: int, rank: int, unit: int = 0) -> int:
 
 class Runner:
     def __init__(self, w: Workload, device: str = "cuda:0", scratch: bool | None = None,
-                 shadow: bool = False, alloc_grads: bool = True, hyper: bool = False):
+                 shadow: bool = False, alloc_grads: bool = True, hyper: bool = False,
+                 visits: str = "fused"):
         self.w = w
+        # stage 3 backward: "fused" issues unit u's update and the gather of
+        # unit u-1 as one call (zero3_step_unit_gather), "separate" as two
+        assert visits in ("fused", "separate")
+        self.visits = visits
         self.dev = torch.device(device)
         torch.cuda.set_device(self.dev)
         if w.unit_rows:
@@ -287,9 +292,19 @@ class Runner:
                         z.zero3_reduce_unit(self.ctx, i, self.grads[i], self.scale, st)
             for i in range(len(pieces)):                 # forward
                 gather(i)
-            for i in reversed(range(len(pieces))):       # backward
-                gather(i)
-                update(i)
+            if one_pass and not w.groups and self.visits == "fused" and pieces:
+                # backward: after unit i's backward, its update and the
+                # gather of unit i-1 in one call
+                U = len(pieces)
+                gather(U - 1)
+                for i in reversed(range(1, U)):
+                    z.zero3_step_unit_gather(self.ctx, i, self.grads[i], *hp, i - 1,
+                                             self.shards[i - 1], self.unit_full, st)
+                update(0)
+            else:
+                for i in reversed(range(len(pieces))):   # backward
+                    gather(i)
+                    update(i)
             if self.shadow is not None:
                 z.zero3_end_step(self.ctx, st)
             elif self.scale > 0:

@@ -90,6 +90,8 @@ _SIGS = {
     "zero3_step_unit": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f64, _f64, _f64, _f64, _i64,
                                        _vp]),
     "zero3_reduce_unit": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f32, _vp]),
+    "zero3_step_unit_gather": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f64, _f64, _f64, _f64,
+                                              _i64, _i32, _vpp, _i32, _vp, _vp]),
     "zero3_gather_group": (ctypes.c_int, [_ctxp, _i32, _i32, _vpp, _i32, _vpp, _vp]),
     "zero3_step_group": (ctypes.c_int, [_ctxp, _i32, _i32, _vpp, _i32, _f64, _f64, _f64, _f64,
                                         _i64, _vp]),
@@ -414,6 +416,15 @@ def zero3_step_unit(ctx, unit: int, grads, lr: float, beta1: float, beta2: float
                     t: int, stream=None) -> None:
     _check(_L.zero3_step_unit(_h(ctx), unit, _ptrs(grads), len(grads), lr, beta1, beta2, eps,
                               t, _stream(stream)))
+
+
+def zero3_step_unit_gather(ctx, unit: int, grads, lr: float, beta1: float, beta2: float,
+                           eps: float, t: int, gather_unit: int, shards, unit_full,
+                           stream=None) -> None:
+    """One backward visit: unit `unit`'s step and unit `gather_unit`'s gather."""
+    _check(_L.zero3_step_unit_gather(_h(ctx), unit, _ptrs(grads), len(grads), lr, beta1, beta2,
+                                     eps, t, gather_unit, _ptrs(shards), len(shards),
+                                     _ptr(unit_full), _stream(stream)))
 
 
 def zero3_reduce_unit(ctx, unit: int, grads, loss_scale: float = 0.0, stream=None) -> None:

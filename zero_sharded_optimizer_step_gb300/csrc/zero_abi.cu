@@ -1186,6 +1186,94 @@ int zero3_step_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32_t
     return stage3_fused(c, r, grads, lr, b1, b2, eps, t, (cudaStream_t)stream);
 }
 
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
+static bool overlap(const void *a, int64_t na, const void *b, int64_t nb)
+{
+    if (!a || !b || na <= 0 || nb <= 0) return false;
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
+// The buffers a unit's step writes (its params and state, the flag and
+// current-set words) or reads (its grads), against a gather's destination
+// and sources: the two halves of a visit may run at the same time only if
+// the gather writes none of the step's buffers and reads none it writes.
+static int check_visit_disjoint(const zero_ctx *c, const Range &r, const void *const *grads,
+                                const void *const *shards, int64_t shard_bytes,
+                                const void *full, int64_t full_bytes)
+{
+    const int es_p = zgb::elem_size(c->pdt), es_g = zgb::elem_size(c->gdt);
+    const int64_t sb = r.n * 4;
+    const void *written[] = {r.params, c->master + r.state_off, c->m + r.state_off,
+                             c->v + r.state_off, c->cur ? c->xb + r.state_off : nullptr,
+                             c->cur ? c->mb + r.state_off : nullptr,
+                             c->cur ? c->vb + r.state_off : nullptr, c->flag, c->cur};
+    const int64_t wbytes[] = {r.n * es_p, sb, sb, sb, sb, sb, sb, 8, 8};
+    for (int i = 0; i < 9; ++i) {
+        if (overlap(full, full_bytes, written[i], wbytes[i]))
+            return fail(ZERO_EINVAL, "unit_full overlaps a buffer the stepped unit writes");
+        for (int32_t k = 0; k < c->world; ++k)
+            if (overlap(shards[k], shard_bytes, written[i], wbytes[i]))
+                return fail(ZERO_EINVAL, "shards[%d] overlaps a buffer the stepped unit writes", k);
+    }
+    for (int32_t k = 0; k < c->world; ++k)
+        if (overlap(full, full_bytes, grads[k], r.n_valid * es_g))
+            return fail(ZERO_EINVAL, "unit_full overlaps grads[%d] of the stepped unit", k);
+    return ZERO_OK;
+}
+
+int zero3_step_unit_gather(zero_ctx *c, int32_t unit, const void *const *grads, int32_t n_grads,
+                           double lr, double b1, double b2, double eps, int64_t t,
+                           int32_t gather_unit, const void *const *shards, int32_t n_shards,
+                           void *unit_full, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if ((rc = check_unit(c, unit))) return rc;
+    const int32_t U = (int32_t)c->unit_S.size();
+    if (gather_unit < 0 || gather_unit >= U)
+        return fail(ZERO_EINVAL, "gather_unit %d out of range [0, %d)", gather_unit, U);
+    if (gather_unit == unit)
+        return fail(ZERO_EINVAL, "a visit steps one unit and gathers another (both are %d)", unit);
+    if ((rc = check_hyper(lr, b1, b2, eps, t))) return rc;
+    if ((rc = check_stage3_pass(c))) return rc;
+    const Range r = unit_range(c, unit);
+    rc = check_ptr_array(grads, n_grads, c->world, zgb::elem_size(c->gdt), r.n_valid > 0, "grads");
+    if (rc) return rc;
+    const int es = zgb::elem_size(c->pdt);
+    const int64_t Sg = c->unit_S[gather_unit];
+    if ((rc = check_ptr_array(shards, n_shards, c->world, es, false, "shards"))) return rc;
+    if (!unit_full && Sg > 0) return fail(ZERO_EINVAL, "unit_full is null");
+    if (!aligned(unit_full, es)) return fail(ZERO_EALIGN, "unit_full not aligned to %d bytes", es);
+    rc = check_visit_disjoint(c, r, grads, shards, Sg * es, unit_full, Sg * es * c->world);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    // Two launches where one would not pay: a lean gather (it runs beside
+    // compute), a bound scalar block (the graph form), a capped step
+    // occupancy, or shards of the size the row placement serves better.
+    if (c->gather_mode == ZERO_GATHER_LEAN || c->hyper || c->step_per_sm > 0 ||
+        Sg * es >= kRowsGatherMinShardBytes) {
+        if ((rc = stage3_fused(c, r, grads, lr, b1, b2, eps, t, s))) return rc;
+        return gather(c, shards, n_shards, unit_full, c->pdt, Sg, s, true);
+    }
+    StepArgs a = make_args(c, r, grads);
+    // with two state sets the pass writes the other set under the step's
+    // loss scale (zero3_end_step decides); with one, the step is unscaled
+    a.av = average_scalars(c->world, c->cur ? c->step_scale : 0.0f);
+    a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
+    a.step_id = c->step_id;
+    zgb::GatherArgs g;
+    memset(&g, 0, sizeof g);
+    for (int32_t k = 0; k < c->world; ++k) g.src[k] = Sg > 0 ? shards[k] : nullptr;
+    g.dst = static_cast<char *>(unit_full);
+    g.shard_bytes = Sg * es;
+    g.n = c->world;
+    g.es = es;
+    const cudaError_t e = zgb::launch_step_gather(c->gdt, c->pdt, a, g, c->sms, 0, s);
+    if (r.n > 0) return finish_launch(c, e, "visit kernel", s);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "visit kernel");
+}
+
 int zero3_reduce_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32_t n_grads,
                       float loss_scale, void *stream)
 {

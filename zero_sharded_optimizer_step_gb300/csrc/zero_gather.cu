@@ -4,95 +4,17 @@
 // FSDP).  A pure copy, bound by HBM bandwidth: 2 bytes moved per byte placed.
 //
 // One grid row (blockIdx.y) per shard, each with more blocks than the GPU
-// holds at once (see launch_gather).  Shards start wherever their buffers
-// are; the destination of shard k sits k*S elements into `full`, which for an
-// odd S and 16-bit elements is only 2-byte aligned.  Each row therefore
-// peels the bytes before the source's first 16-byte boundary, copies the
-// body with 16-byte loads, and writes each 16 bytes with the widest store
-// the destination's alignment allows (one 16-byte store, or two of 8, four
-// of 4, eight of 2); the last partial 16 bytes go element by element.
+// holds at once (see launch_gather); the row copy itself (peeled head,
+// 16-byte body, widest store the destination allows) is in zero_row_copy.cuh.
 #include <cstring>
 
 #include "zero_internal.h"
+#include "zero_row_copy.cuh"
 
 namespace zgb {
 namespace {
 
-constexpr int kItems = 4;   // 16-byte chunks in flight per thread
-
-__device__ __forceinline__ uint4 ld_stream(const void *p)
-{
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ void st_any(char *p, uint4 v, int align)
-{
-    if (align >= 16) {
-        __stcs(reinterpret_cast<uint4 *>(p), v);
-    } else if (align == 8) {
-        uint2 *q = reinterpret_cast<uint2 *>(p);
-        __stcs(q, make_uint2(v.x, v.y));
-        __stcs(q + 1, make_uint2(v.z, v.w));
-    } else if (align == 4) {
-        unsigned *q = reinterpret_cast<unsigned *>(p);
-        q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
-    } else {
-        unsigned short *q = reinterpret_cast<unsigned short *>(p);
-        const unsigned w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            q[2 * i] = (unsigned short)(w[i] & 0xffffu);
-            q[2 * i + 1] = (unsigned short)(w[i] >> 16);
-        }
-    }
-}
-
-__device__ __forceinline__ void copy_elem(char *d, const char *s, int es)
-{
-    if (es == 4) *reinterpret_cast<unsigned *>(d) = *reinterpret_cast<const unsigned *>(s);
-    else *reinterpret_cast<unsigned short *>(d) = *reinterpret_cast<const unsigned short *>(s);
-}
-
-// One row of a placement: nb bytes from src to dst, spread over the row's
-// nblk blocks (this one is number blk).  Block 0 of the row also copies the
-// ragged head (up to the source's next 16-byte boundary) and tail element
-// by element.
-__device__ __forceinline__ void gather_row(const char *src, char *dst, int64_t nb, int es,
-                                           int64_t blk, int64_t nblk)
-{
-    int64_t head = (int64_t)((16 - ((uintptr_t)src & 15)) & 15);
-    if (head > nb) head = nb;
-    const int64_t nchunks = (nb - head) >> 4;
-    const int64_t tail = head + (nchunks << 4);
-    const uintptr_t d0 = (uintptr_t)(dst + head);
-    const int align = (d0 & 15) == 0 ? 16 : (d0 & 7) == 0 ? 8 : (d0 & 3) == 0 ? 4 : 2;
-
-    if (blk == 0) {
-        for (int64_t b = (int64_t)threadIdx.x * es; b < head; b += (int64_t)blockDim.x * es)
-            copy_elem(dst + b, src + b, es);
-        for (int64_t b = tail + (int64_t)threadIdx.x * es; b < nb; b += (int64_t)blockDim.x * es)
-            copy_elem(dst + b, src + b, es);
-    }
-
-    const char *s = src + head;
-    char *d = dst + head;
-    const int64_t T = nblk * blockDim.x;
-    int64_t c = blk * blockDim.x + threadIdx.x;
-    // kItems chunks per thread per round, each T apart so a warp's accesses
-    // stay contiguous
-    for (; c + (kItems - 1) * T < nchunks; c += kItems * T) {
-        uint4 v[kItems];
-#pragma unroll
-        for (int u = 0; u < kItems; ++u) v[u] = ld_stream(s + ((c + u * T) << 4));
-#pragma unroll
-        for (int u = 0; u < kItems; ++u) st_any(d + ((c + u * T) << 4), v[u], align);
-    }
-    for (; c < nchunks; c += T) st_any(d + (c << 4), ld_stream(s + (c << 4)), align);
-}
+using rowcopy::gather_row;
 
 __global__ void __launch_bounds__(kThreads)
 gather_kernel(const __grid_constant__ GatherArgs a)
@@ -268,17 +190,9 @@ cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s)
 {
     if (a.n <= 0 || a.shard_bytes <= 0) return cudaSuccess;
     const int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(gather_kernel), kThreads);
-    const int64_t chunks = (a.shard_bytes + 15) / 16;
-    int64_t want = (chunks + (int64_t)kThreads * kItems - 1) / ((int64_t)kThreads * kItems);
-    // Give each row (shard) twice as many blocks as fit on the GPU at once.
-    // Blocks are dispatched row after row, so only one or two shards are in
-    // flight at any time and all resident blocks sweep one compact window of
-    // each: measured on GB300 for 63 shards of 234 MB, 6.9 TB/s, against
-    // 5.4 TB/s when ~32 shards were in flight with 19 blocks each (and 4.1
-    // TB/s when every block streamed its own contiguous slice).
-    const int64_t resident = (int64_t)sms * per_sm;
-    int64_t bx = 2 * resident < want ? 2 * resident : want;
-    if (bx < 1) bx = 1;
+    // each row (shard) gets up to twice as many blocks as fit on the GPU at
+    // once, so one or two shards are in flight at any time
+    const int64_t bx = rowcopy::row_blocks(a.shard_bytes, kThreads, (int64_t)sms * per_sm);
     dim3 grid((unsigned)bx, (unsigned)a.n);
     return launch_dependent(gather_kernel, grid, dim3(kThreads), 0, s, a);
 }
@@ -298,12 +212,7 @@ cudaError_t launch_gather_rows(const GatherRowsArgs &a, int sms, cudaStream_t s)
     for (int32_t y = 0; y < a.n; ++y) {
         r.first_block[y] = (int32_t)total;
         int64_t want = 0;
-        if (a.src[y] && a.bytes[y] > 0) {
-            const int64_t chunks = (a.bytes[y] + 15) / 16;
-            want = (chunks + (int64_t)kThreads * kItems - 1) / ((int64_t)kThreads * kItems);
-            if (want < 1) want = 1;
-            if (want > cap) want = cap;
-        }
+        if (a.src[y] && a.bytes[y] > 0) want = rowcopy::row_blocks(a.bytes[y], kThreads, cap / 2);
         total += want;
         if (total > 0x7fffffff) return cudaErrorInvalidValue;
     }

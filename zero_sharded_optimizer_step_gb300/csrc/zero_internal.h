@@ -102,6 +102,16 @@ struct GatherArgs {
     int32_t es;                    // element size in bytes
 };
 
+// A ZeRO-3 backward visit in one launch: the fused pass over one unit's
+// range (`step`, blocks [0, step_blocks)) and the placement of another
+// unit's shards (`gather`, row_blocks blocks per shard after them).
+struct StepGatherArgs {
+    StepArgs step;
+    GatherArgs gather;
+    int32_t step_blocks;
+    int32_t row_blocks;
+};
+
 // A placement of independent rows in one launch: row y copies bytes[y]
 // bytes from src[y] to dst[y] (a group of units, one row per unit and shard).
 // The launcher fills first_block: row y owns blocks [first_block[y],
@@ -180,6 +190,12 @@ cudaError_t launch_apply(int32_t pdt, const StepArgs &a, int sms, int cap_per_sm
 cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, int cap_per_sm,
                             cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s);
+// The visit kernel: the fused pass of launch_fused_step over `step` (eager
+// scalars, no stage-1 output) and the placement of launch_gather over
+// `gather`, in one launch; the launcher sizes both parts of the grid.
+cudaError_t launch_step_gather(int32_t gdt, int32_t pdt, const StepArgs &step,
+                               const GatherArgs &gather, int sms, int cap_per_sm,
+                               cudaStream_t s);
 // Fills a copy's first_block table and launches; `a` itself is not changed.
 cudaError_t launch_gather_rows(const GatherRowsArgs &a, int sms, cudaStream_t s);
 // The bulk-copy (TMA) placement for 16-byte aligned shards: one warp per SM,

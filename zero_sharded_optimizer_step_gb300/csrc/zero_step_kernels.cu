@@ -33,6 +33,7 @@
 #include <cuda_fp16.h>
 
 #include "zero_internal.h"
+#include "zero_row_copy.cuh"
 
 namespace zgb {
 namespace {
@@ -338,14 +339,13 @@ template <int GT> struct MinBlocks { static constexpr int value = GT == F32 ? 2 
 
 // ---------------------------------------------------------------- kernels
 
+// The fused pass over the range, as block `block` of the `nblocks` blocks
+// that share it (grid-stride over the aligned vectors, then the tail).
 template <int GT, int PT, bool AVG, bool HYPER>
-__global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
-fused_step_kernel(const __grid_constant__ StepArgs a)
+__device__ __forceinline__ void fused_step_body(const StepArgs &a, int64_t block, int64_t nblocks)
 {
-    pdl_wait();                 // the previous kernel in the stream is done
-    pdl_launch_dependents();
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = nblocks * blockDim.x;
+    const int64_t tid = block * blockDim.x + threadIdx.x;
     const int64_t nvec = a.vec_ok ? a.n_valid / kVec : 0;
     const StatePtrs st = select_state(a, true);
     const ScalarRefs<HYPER> sc = step_scalars<HYPER>(a, true);
@@ -400,6 +400,39 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
         if (AVG) Ty<GT>::store1(a.grad_avg, i, mean);
     }
     publish_flag(a, bad, sc.id);
+}
+
+template <int GT, int PT, bool AVG, bool HYPER>
+__global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
+fused_step_kernel(const __grid_constant__ StepArgs a)
+{
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
+    fused_step_body<GT, PT, AVG, HYPER>(a, blockIdx.x, gridDim.x);
+}
+
+// A ZeRO-3 backward visit in one launch: blocks [0, step_blocks) run the
+// fused pass over one unit (as fused_step_kernel), the rest place the next
+// unit's shards (as gather_kernel, row_blocks blocks per shard).  The two
+// touch disjoint memory (the host checks it), so neither waits for the
+// other; one launch pays one ramp-up and one drain instead of two.
+template <int GT, int PT>
+__global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
+step_gather_kernel(const __grid_constant__ StepGatherArgs a)
+{
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
+    const int b = (int)blockIdx.x;
+    if (b < a.step_blocks) {
+        fused_step_body<GT, PT, false, false>(a.step, b, a.step_blocks);
+        return;
+    }
+    const int gb = b - a.step_blocks;
+    const int k = gb / a.row_blocks;
+    const char *src = static_cast<const char *>(a.gather.src[k]);
+    if (src == nullptr) return;
+    rowcopy::gather_row(src, a.gather.dst + (int64_t)k * a.gather.shard_bytes,
+                        a.gather.shard_bytes, a.gather.es, gb % a.row_blocks, a.row_blocks);
 }
 
 template <int GT, bool AVG, bool HYPER>
@@ -628,6 +661,61 @@ cudaError_t launch_finalize(int32_t pdt, const StepArgs &a, int sms, int cap_per
     case F32: return launch(finalize_kernel<F32>, a, w, sms, cap_per_sm, s);
     case BF16: return launch(finalize_kernel<BF16>, a, w, sms, cap_per_sm, s);
     case F16: return launch(finalize_kernel<F16>, a, w, sms, cap_per_sm, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+namespace {
+
+template <int GT, int PT>
+cudaError_t step_gather_pt(const StepArgs &st, const GatherArgs &g, int sms, int cap_per_sm,
+                           cudaStream_t s)
+{
+    auto kernel = step_gather_kernel<GT, PT>;
+    int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(kernel), kThreads);
+    const int resident = sms * per_sm;
+    if (cap_per_sm > 0 && per_sm > cap_per_sm) per_sm = cap_per_sm;
+    // the step part: the grid fused_step_kernel would get
+    const int64_t want = (items(st, st.n_valid) + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)sms * per_sm;
+    int64_t step_blocks = st.n > 0 ? (want < cap ? want : cap) : 0;
+    if (st.n > 0 && step_blocks < 1) step_blocks = 1;
+    // the gather part: the rows gather_kernel would get
+    StepGatherArgs a;
+    a.step = st;
+    a.gather = g;
+    const int64_t row_blocks =
+        g.shard_bytes > 0 ? rowcopy::row_blocks(g.shard_bytes, kThreads, resident) : 0;
+    a.step_blocks = (int32_t)step_blocks;
+    a.row_blocks = (int32_t)row_blocks;
+    const int64_t blocks = step_blocks + row_blocks * (g.shard_bytes > 0 ? g.n : 0);
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    return launch_dependent(kernel, dim3((unsigned)blocks), dim3(kThreads), 0, s, a);
+}
+
+template <int GT>
+cudaError_t step_gather_gt(int32_t pdt, const StepArgs &st, const GatherArgs &g, int sms,
+                           int cap_per_sm, cudaStream_t s)
+{
+    switch (pdt) {
+    case F32: return step_gather_pt<GT, F32>(st, g, sms, cap_per_sm, s);
+    case BF16: return step_gather_pt<GT, BF16>(st, g, sms, cap_per_sm, s);
+    case F16: return step_gather_pt<GT, F16>(st, g, sms, cap_per_sm, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_step_gather(int32_t gdt, int32_t pdt, const StepArgs &st,
+                               const GatherArgs &g, int sms, int cap_per_sm, cudaStream_t s)
+{
+    if (st.hyper || st.grad_avg) return cudaErrorInvalidValue;   // eager unit steps only
+    switch (gdt) {
+    case F32: return step_gather_gt<F32>(pdt, st, g, sms, cap_per_sm, s);
+    case BF16: return step_gather_gt<BF16>(pdt, st, g, sms, cap_per_sm, s);
+    case F16: return step_gather_gt<F16>(pdt, st, g, sms, cap_per_sm, s);
     }
     return cudaErrorInvalidValue;
 }
