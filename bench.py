@@ -31,9 +31,14 @@ and, for the default run, `workloads`: the 7.5B one-rank view with its
 placement, GPT-2 small and the two ZeRO-3 unit paths, each timed after the
 headline in a runner of its own (with its own clocks and e2e).
 
-With --gpus N > 1 (torchrun), every GPU runs its own full replica of the
-workload (the N simulated ranks live on each GPU; no data-path collective):
-weak scaling.  `--impl reference` times the CPU oracle instead (rank 0 only).
+With --gpus N > 1 (torchrun), process r is data-parallel rank r of N in the
+one-rank view of the headline workload's flat vector, stepped through the
+library's sharded step (an all-to-all of the grad slices, the local fused
+pass, a MAX all-reduce of the flag word, the finalize and an all-gather of
+the cast shards; NCCL, or gloo through host memory with --dist-backend
+gloo): strong scaling.  --replicas instead runs one full replica of the
+workload per GPU with no data-path collective (weak scaling).
+`--impl reference` times the CPU oracle instead (rank 0 only).
 """
 from __future__ import annotations
 
@@ -124,6 +129,12 @@ def parse():
                          "layers (small cases)")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the workload's parameter count (small profiling cases)")
+    ap.add_argument("--replicas", action="store_true",
+                    help="with --gpus N > 1: N independent replicas of the workload (the "
+                         "simulated ranks on every GPU) instead of one rank per process")
+    ap.add_argument("--dist-backend", default="auto", choices=["auto", "nccl", "gloo"],
+                    help="process group backend with --gpus N > 1 (auto: nccl on GPUs); a "
+                         "gloo group moves the exchanged data through host memory")
     ap.add_argument("--extra-workloads", default=None,
                     help="comma-separated workloads timed after the headline one ('none': "
                          "only the headline); default: %s for the default run"
@@ -706,6 +717,123 @@ def run_e2e(run, plan, args, world_size):
     e2e = (bench_e2e_pipelined(run, args, world_size) if w.stage < 3 else
            bench_e2e_units(run, args, world_size) if w.rank >= 0 else None)
     return e2e or bench_e2e(run, plan, args, world_size)
+
+
+def bench_sharded(args, rank, world_size, device_index):
+    """One process per data-parallel rank (the default for --gpus N > 1):
+    process r is rank r of N in the one-rank view of the headline workload's
+    flat vector (N = the number of processes), stepped through the library's
+    sharded step: an all-to-all of the grad slices, the local fused pass into
+    the other state set, a MAX all-reduce of the flag word, the finalize, an
+    all-gather of the cast shards (zero_sharded_optimizer_step_gb300.sharded).
+    The total work is the whole vector whatever N is: strong scaling.
+    `value` is the elements of all shards updated per second."""
+    import torch
+
+    import synth
+    import workloads as W
+    import zero_sharded_optimizer_step_gb300 as z
+    from zero_sharded_optimizer_step_gb300.sharded import LibraryRank, ShardedStep
+
+    base = make_workload(args, args.workload)
+    if base.stage == 3 or base.rank >= 0 or base.bucket:
+        raise SystemExit("the sharded mode steps a stage-1/2 flat vector; --workload %s is not "
+                         "one (use --replicas)" % args.workload)
+    w = base.replace(world=world_size, name=base.name + "_sharded")
+    torch.cuda.set_device(device_index)
+    dev = torch.device("cuda:%d" % device_index)
+    scale = w.loss_scale
+    local = LibraryRank(w.numel, w.world, rank, w.grad_dtype, w.param_dtype, dev,
+                        shadow=scale > 0, weight_decay=w.weight_decay)
+    S = local.shard
+    lo = rank * S
+    nv = max(0, min(S, w.numel - lo))
+    st = torch.cuda.current_stream(dev).cuda_stream
+    if nv:
+        synth.fill_device(local.master.data_ptr(), nv, synth.F32,
+                          synth.key(w.seed, synth.KIND_MASTER), w.sigma_master, st, index0=lo)
+    local.set_master(local.master.clone())
+    grads = local.grad_buffer(S * w.world)
+    synth.fill_device(grads.data_ptr(), w.numel, w.grad_dtype,
+                      synth.key(w.seed, synth.KIND_GRAD, 1, rank), W.grad_sigma(w, scale), st)
+    step = ShardedStep(local)
+    t, good = 0, 0
+
+    def one():
+        nonlocal t, scale, good
+        _, skipped = step.step(grads, w.lr, w.beta1, w.beta2, w.eps, t + 1, loss_scale=scale)
+        if scale > 0:
+            scale, good = z.zero_scale_update(scale, skipped, good, w.growth_interval)
+        if not skipped:
+            t += 1
+        return skipped
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    clocks = Clocks(device_index, args.clocks_csv)
+    barrier(world_size)
+    torch.cuda.synchronize()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    skips = [one() for _ in range(args.steps)]
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world_size)
+    ms = allreduce_max(e0.elapsed_time(e1), world_size) / args.steps
+    # the local pass alone (the rank's fused kernel), for the roofline
+    pairs = []
+    for _ in range(args.steps):
+        torch.cuda.synchronize()
+        barrier(world_size)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        local.local_pass(step.slices(), w.lr, w.beta1, w.beta2, w.eps, t + 1, scale)
+        b.record()
+        local.finish(w.lr, w.beta1, w.beta2, w.eps, t + 1)
+        local.status()
+        pairs.append((a, b))
+        t += 1
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    assert not any(skips), "a timed step was skipped"
+    kms = allreduce_max(statistics.median(a.elapsed_time(b) for a, b in pairs), world_size)
+    bg = 4 if w.grad_dtype == 0 else 2
+    bp = 4 if w.param_dtype == 0 else 2
+    kbytes = w.world * bg * nv + (24 + bp) * S
+    peak, peak_kind = peaks()
+    achieved = kbytes / (kms * 1e-3) / 1e9
+    updated = S * w.world
+    step_bytes = kbytes + 2 * bp * S * (w.world - 1)     # + placing the other shards
+    res = {
+        "metric": METRIC, "value": updated / (ms * 1e-3), "unit": "params/s",
+        "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+        "storage": {"grads": "f32 bf16 f16".split()[w.grad_dtype],
+                    "params": "f32 bf16 f16".split()[w.param_dtype], "state": "f32"},
+        "data": "synthetic (seeded counter-based normal draws; no dataset)",
+        "config": {
+            "workload": describe(w), "params_updated_per_step": updated,
+            "l2": "inputs larger than L2 (129 MB); no flush between timed steps",
+            "parallelism": "%d processes, one data-parallel rank each (one-rank view; %s "
+                           "all-to-all of grad slices, MAX all-reduce of the flag word, "
+                           "all-gather of the cast shards)"
+                           % (world_size, args.dist_backend),
+            "path": path_of(w, scale > 0),
+        },
+        "measured": {"local_pass_ms": kms, "local_alg_bytes": kbytes,
+                     "local_bytes_per_rank_per_step": step_bytes,
+                     "timing": "K whole steps between one pair of CUDA events on each rank, "
+                               "max over ranks; then K local passes alone"},
+        "roofline": {"kernel": "fused_step_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "alg_bytes_per_launch": kbytes, "traffic": None},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clock_info,
+    }
+    local.close()
+    return res
 
 
 def bench_prefetch(args, rank, world_size, device_index):
@@ -1565,12 +1693,18 @@ def main():
     world_size = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = local
     if world_size > 1:
         import torch
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if backend == "nccl":
-            torch.cuda.set_device(local)
+        backend = args.dist_backend
+        if backend == "auto":
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+        args.dist_backend = backend
+        if torch.cuda.is_available():
+            # one GPU per process; a gloo group may put several on one GPU
+            device = local % torch.cuda.device_count()
+            torch.cuda.set_device(device)
         dist.init_process_group(backend)
     if args.impl == "reference":
         res = bench_reference(args, rank, world_size)
@@ -1579,11 +1713,13 @@ def main():
         __graft_entry__.build() if rank == 0 else None
         barrier(world_size)
         if args.workload in ("zero3_prefetch", "fsdp2_prefetch"):
-            res = bench_prefetch(args, rank, world_size, local)
+            res = bench_prefetch(args, rank, world_size, device)
         elif args.workload == "zero2_overlap":
-            res = bench_zero2_overlap(args, rank, world_size, local)
+            res = bench_zero2_overlap(args, rank, world_size, device)
+        elif world_size > 1 and not args.replicas:
+            res = bench_sharded(args, rank, world_size, device)
         else:
-            res = bench_ours(args, rank, world_size, local)
+            res = bench_ours(args, rank, world_size, device)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world_size > 1:

@@ -1,0 +1,109 @@
+"""The sharded step with libzero.so doing each rank's arithmetic: two
+processes, each one data-parallel rank in the one-rank view (LibraryRank)
+driven by ShardedStep, their data exchanged by gloo through host memory
+(this run has one GPU, so both processes use it; no kernel of one process
+waits for the other's).  The result must be bit-identical to the oracle's
+all-ranks step: the state of every shard, the full parameter buffer every
+rank ends with, and the skip of the step that holds a +inf -- with two
+state sets and with the fp32 scratch, loss-scaled and not."""
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+from tests.test_multiprocess_gloo import _all_ranks_reference, _free_port
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _rank(rank, world, port, numel, inject_at, shadow, out_dir):
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import oracle
+    import synth
+    import zero_sharded_optimizer_step_gb300 as z
+    from zero_sharded_optimizer_step_gb300.sharded import LibraryRank, ShardedStep
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(0)
+    local = LibraryRank(numel, world, rank, z.ZERO_F16, z.ZERO_F16, "cuda:0", shadow=shadow)
+    S = local.shard
+    lo = rank * S
+    nv = max(0, min(S, numel - lo))
+    x0 = np.zeros(S, np.float32)
+    x0[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER), 0.01, index0=lo)
+    local.set_master(torch.from_numpy(x0).cuda())
+    step = ShardedStep(local)
+    P = S * world
+    scale, good, t, skips = 2.0 ** 12, 0, 0, []
+    for it in (1, 2, 3):
+        g = np.zeros(P, np.uint16)
+        g[:numel] = synth.fill_host(numel, synth.F16, synth.key(0, synth.KIND_GRAD, it, rank),
+                                    1e-3 * scale)
+        if inject_at and it == inject_at[0] and rank == inject_at[1]:
+            g[inject_at[2]] = 0x7C00                          # +inf in fp16
+        dg = torch.from_numpy(g.view(np.int16)).cuda().view(torch.float16)
+        _, skipped = step.step(dg, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale)
+        skips.append(skipped)
+        if not skipped:
+            t += 1
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    torch.cuda.synchronize()
+    x, m, v = (a.cpu().numpy() for a in local.state())
+    full = local.params.cpu().view(torch.int16).numpy().view(np.uint16)
+    np.savez(os.path.join(out_dir, "rank%d.npz" % rank), x=x, m=m, v=v, full=full,
+             skips=np.array(skips))
+    local.close()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("numel,inject_at,shadow", [
+    (300_007, None, True),
+    (300_007, (2, 1, 299_999), True),     # rank 1's +inf in rank 1's shard
+    (300_007, (2, 0, 200_001), False),    # rank 0's +inf in rank 1's shard
+])
+def test_sharded_step_through_the_library(tmp_path, numel, inject_at, shadow):
+    world = 2
+    port = _free_port()
+    mp.start_processes(_rank, args=(world, port, numel, inject_at, shadow, str(tmp_path)),
+                       nprocs=world, join=True, start_method="spawn")
+    import oracle
+    x, m, v, full, skips = _all_ranks_reference(numel, world, inject_at)
+    assert skips == [bool(inject_at) and it == inject_at[0] for it in (1, 2, 3)]
+    S = oracle.shard_size(numel, world)
+    for r in range(world):
+        d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
+        assert list(d["skips"]) == skips, r
+        sl = slice(r * S, (r + 1) * S)
+        assert d["x"].tobytes() == x[sl].tobytes()
+        assert d["m"].tobytes() == m[sl].tobytes()
+        assert d["v"].tobytes() == v[sl].tobytes()
+        assert d["full"].tobytes() == full.tobytes()
+
+
+def test_bench_sharded_mode_runs():
+    """bench.py's default mode for --gpus 2 (one data-parallel rank per
+    process) under torchrun: two gloo ranks on this GPU, a small vector; the
+    line reports strong scaling and every step applied."""
+    import json
+    import subprocess
+    import sys
+    port = _free_port()
+    out = subprocess.run(
+        [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+         "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--gpus", "2",
+         "--dist-backend", "gloo", "--numel", "4000037", "--steps", "3", "--warmup", "3"],
+        cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["scaling"] == "strong" and d["value"] > 0
+    assert d["config"]["params_updated_per_step"] == 2 * (-(-4000037 // 2))
+    assert "gloo" in d["config"]["parallelism"]

@@ -1,9 +1,10 @@
 """The multi-rank protocol on CPU with real collectives (gloo, 2 and 4
-processes): each process is one data-parallel rank in the one-rank view --
-reduce-scatter in rank order, the overflow verdict combined across ranks with
-a MAX all-reduce between the reduce and the apply (as the one-rank ABI
-documents), Adam on the own shard, all-gather of the cast shards -- and the
-result must be bit-identical to the all-ranks step.  The same for ZeRO-3:
+processes): each process is one data-parallel rank in the one-rank view,
+driven by the library's sharded step (zero_sharded_optimizer_step_gb300.
+sharded: the all-to-all of the grad slices, the overflow verdict combined
+across ranks with a MAX all-reduce between the local pass and the rest of
+the step, the all-gather of the cast shards) with the rank's arithmetic done
+by the oracle -- and the result must be bit-identical to the all-ranks step.  The same for ZeRO-3:
 per unit an all-gather before forward and backward, the unit's
 reduce-scatter, and every unit's verdict combined before any unit's Adam
 counts.  Also covers the benchmark's cross-rank timing helpers (barrier,
@@ -26,57 +27,88 @@ def _free_port():
         return s.getsockname()[1]
 
 
+class OracleRank:
+    """Rank `rank`'s own arithmetic done by the CPU oracle, with the members
+    the library's ShardedStep drives (the same ones LibraryRank has): fp16
+    grads and params held as 16-bit patterns in CPU tensors, the step-tagged
+    flag word, the oracle's one-rank step once the verdict is combined."""
+
+    def __init__(self, numel, world, rank):
+        import oracle
+        import synth
+        self.oracle = oracle
+        self.numel, self.world, self.rank = numel, world, rank
+        self.shard = S = oracle.shard_size(numel, world)
+        lo = rank * S
+        self.nv = max(0, min(S, numel - lo))
+        self.x = np.zeros(S, np.float32)
+        self.x[:self.nv] = synth.fill_host(self.nv, synth.F32, synth.key(0, synth.KIND_MASTER),
+                                           0.01, index0=lo)
+        self.m, self.v = np.zeros(S, np.float32), np.zeros(S, np.float32)
+        self.params = torch.zeros(S * world, dtype=torch.int16)
+        self.own_params = self.params[lo:lo + S]
+        self.own_params.copy_(torch.from_numpy(oracle.cast(self.x, oracle.F16).view(np.int16)))
+        self.flag = torch.zeros(1, dtype=torch.int64)
+        self.step_id = 0
+
+    def grad_buffer(self, n):
+        return torch.zeros(n, dtype=torch.int16)
+
+    def local_pass(self, slices, lr, beta1, beta2, eps, t, loss_scale):
+        o = self.oracle
+        self.step_id += 1
+        self.scale = loss_scale
+        self.sl = [s.numpy().view(np.uint16).copy() for s in slices]
+        acc = o.rank_sum(self.sl, o.F16, self.shard, self.nv)
+        _, bad = o.average(acc, self.world, loss_scale)
+        if bad:
+            self.flag[0] = self.step_id
+
+    def finish(self, lr, beta1, beta2, eps, t):
+        o = self.oracle
+        others = int(self.flag.item() == self.step_id)     # any rank's finding
+        lp = self.own_params.numpy().view(np.uint16).copy()
+        o.zero_rank_step(self.sl, o.F16, self.numel, self.rank, self.x, self.m, self.v, lp,
+                         o.F16, lr, beta1, beta2, eps, t, loss_scale=self.scale,
+                         others_nonfinite=others)
+        self.own_params.copy_(torch.from_numpy(lp.view(np.int16)))
+
+    def status(self):
+        bad = self.flag.item() == self.step_id
+        return bad, bad and self.scale > 0
+
+
 def _rank_main(rank, world, port, numel, inject_at, out_dir):
+    """One data-parallel rank, driven by the library's sharded step (the
+    all-to-all of the grad slices, the MAX combine of the flag word, the
+    all-gather of the cast shards) with the oracle's arithmetic."""
     import sys
     sys.path.insert(0, ROOT)
     import oracle
     import synth
+    from zero_sharded_optimizer_step_gb300.sharded import ShardedStep
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
-    S = oracle.shard_size(numel, world)
-    P = S * world
-    lo = rank * S
-    nv = max(0, min(S, numel - lo))
-    x = np.zeros(S, np.float32)
-    x[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER), 0.01, index0=lo)
-    m, v = np.zeros(S, np.float32), np.zeros(S, np.float32)
+    local = OracleRank(numel, world, rank)
+    step = ShardedStep(local)
+    P = local.shard * world
     scale, good, t = 2.0 ** 12, 0, 0
-    full = np.zeros(P, np.uint16)
     skips = []
     for it in (1, 2, 3):
-        g = synth.fill_host(numel, synth.F16, synth.key(0, synth.KIND_GRAD, it, rank),
-                            1e-3 * scale)
+        g = np.zeros(P, np.uint16)
+        g[:numel] = synth.fill_host(numel, synth.F16, synth.key(0, synth.KIND_GRAD, it, rank),
+                                    1e-3 * scale)
         if inject_at and it == inject_at[0] and rank == inject_at[1]:
             g[inject_at[2]] = 0x7C00                          # +inf in fp16
-        padded = np.zeros(P, np.uint16)
-        padded[:numel] = g
-        # reduce-scatter in rank order: gather every rank's piece of my shard
-        # (16-bit patterns travel as int32: gloo has no 16-bit integer type)
-        pieces = [torch.zeros(S, dtype=torch.int32) for _ in range(world)]
-        for r in range(world):
-            send = torch.from_numpy(padded[r * S:(r + 1) * S].astype(np.int32))
-            dist.gather(send, pieces if r == rank else None, dst=r)
-        slices = [p.numpy().astype(np.uint16) for p in pieces]
-        # local verdict, then the MAX combine across ranks
-        acc = oracle.rank_sum(slices, oracle.F16, S, nv)
-        _, bad = oracle.average(acc, world, scale)
-        flag = torch.tensor([bad], dtype=torch.int64)
-        dist.all_reduce(flag, op=dist.ReduceOp.MAX)
-        others = int(flag.item())        # any rank's finding skips every rank
-        lp = full[lo:lo + S].copy()
-        skipped, _ = oracle.zero_rank_step(slices, oracle.F16, numel, rank, x, m, v, lp,
-                                           oracle.F16, 1e-3, 0.9, 0.999, 1e-8, t + 1,
-                                           loss_scale=scale, others_nonfinite=others)
+        _, skipped = step.step(torch.from_numpy(g.view(np.int16)), 1e-3, 0.9, 0.999, 1e-8,
+                               t + 1, loss_scale=scale)
         skips.append(skipped)
         if not skipped:
             t += 1
-        # all-gather of the cast shards
-        shards = [torch.zeros(S, dtype=torch.int32) for _ in range(world)]
-        dist.all_gather(shards, torch.from_numpy(lp.astype(np.int32)))
-        full = np.concatenate([s.numpy().astype(np.uint16) for s in shards])
         scale, good = oracle.scale_update(scale, skipped, good, 2000)
-    np.savez(os.path.join(out_dir, "rank%d.npz" % rank), x=x, m=m, v=v, full=full,
-             skips=np.array(skips))
+    full = local.params.numpy().view(np.uint16)
+    np.savez(os.path.join(out_dir, "rank%d.npz" % rank), x=local.x, m=local.m, v=local.v,
+             full=full, skips=np.array(skips))
     # the benchmark's helpers under gloo
     sys.argv = ["bench.py"]
     import bench
