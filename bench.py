@@ -57,32 +57,25 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from ncu
-# captures of the full workloads (dram__bytes_read.sum + dram__bytes_write.sum
-# per launch, and gpu__time_duration.sum in us per launch, cold and
-# serialized; one pass; summarised under profiles/).  Each entry is valid only
-# for the kernel source it was taken on (sha256 prefix); otherwise bench
-# reports null.
+# DRAM bytes (read + write) per launch of the dominant kernel and the ncu
+# duration of that launch in us (cold and serialized), from one-pass ncu
+# captures of dram__bytes_read.sum + dram__bytes_write.sum and
+# gpu__time_duration.sum on cases of a few GB (summarised under profiles/),
+# scaled to a full launch by the elements it processes where the case is
+# smaller (reads grow in proportion; the few tens of MB of writes still in
+# L2 when a launch ends do not, so a scaled write figure is slightly low).
+# Each entry is valid only for the kernel source it was taken on (sha256
+# prefix); otherwise bench reports null.
 TRAFFIC = {
-    ("gpt2_xl", "fused_step_kernel"): ("ef00f5525d2d15b7", 68.537e9 + 21.778e9, 12939.9),
-    ("one_rank_7p5b", "gather_kernel"): ("5ad5f8b67603e427", 14.788e9 + 14.724e9, 4254.7),
-    ("one_rank_7p5b", "fused_step_kernel"): ("ef00f5525d2d15b7", 16.408e9 + 1.621e9, 2568.0),
-    # means of two full-size launches; part of each launch's writes is still
-    # in L2 when it ends
-    ("zero3_llama7b", "gather_rows_kernel"): ("5ad5f8b67603e427", 404.79e6 + 349.72e6, 113.7),
+    # 60,000,000-element case (16 fp16 ranks, two state sets), x 25.96
+    ("gpt2_xl", "fused_step_kernel"): ("b1de68b92c2360fb", 68.538e9 + 20.968e9, 13141.8),
+    # 63 shards of 10,000,000 elements, x 11.72
+    ("one_rank_7p5b", "gather_kernel"): ("eae13d5b2b7affa8", 14.767e9 + 14.136e9, 4094.4),
+    # 2 Llama-7B layers: every gather has the full workload's shape
+    ("zero3_llama7b", "gather_rows_kernel"): ("eae13d5b2b7affa8", 404.82e6 + 349.29e6, 113.5),
     # the same gathers (2-byte params, the same shard sizes)
-    ("zero3_llama7b_fp16", "gather_rows_kernel"): ("5ad5f8b67603e427", 404.79e6 + 350.47e6, 113.3),
-    ("fsdp2_llama7b", "gather_rows_kernel"): ("5ad5f8b67603e427", 404.79e6 + 347.54e6, 112.4),
-    ("gpt2_small", "fused_step_kernel"): ("ef00f5525d2d15b7", 3.4844e9 + 1.6934e9, 750.0),
-    ("gpt2_xl_adamw", "fused_step_kernel"): ("ef00f5525d2d15b7", 68.536e9 + 21.778e9, 12920.9),
-    # mean over the 47 bucket launches of one step
-    ("gpt2_xl_bucketed", "fused_step_kernel"): ("ef00f5525d2d15b7", 1.45833e9 + 0.43173e9, 275.5),
-    ("gpt2_small_stage1", "fused_step_kernel"): ("ef00f5525d2d15b7", 3.4845e9 + 1.9535e9, 800.0),
-    # the two-pass loss-scaled step (--two-pass): its first, larger kernel
-    ("gpt2_xl", "reduce_kernel"): ("ef00f5525d2d15b7", 49.846e9 + 6.2133e9, 7941.7),
-    # mean over the 28 gathers of one step; the units' full buffers (14 to
-    # 79 MB) mostly stay in L2, so most of the writes never reach DRAM
-    ("zero3_gpt2_small", "gather_kernel"): ("5ad5f8b67603e427", 17.794e6 + 1.9392e6, 9.1),
+    ("zero3_llama7b_fp16", "gather_rows_kernel"): ("eae13d5b2b7affa8", 404.82e6 + 349.29e6,
+                                                   113.5),
 }
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
                           "zero_step_kernels.cu")
