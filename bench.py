@@ -714,52 +714,96 @@ def run_e2e(run, plan, args, world_size):
 
 def bench_sharded(args, rank, world_size, device_index):
     """One process per data-parallel rank (the default for --gpus N > 1):
-    process r is rank r of N in the one-rank view of the headline workload's
-    flat vector (N = the number of processes), stepped through the library's
-    sharded step: an all-to-all of the grad slices, the local fused pass into
-    the other state set, a MAX all-reduce of the flag word, the finalize, an
-    all-gather of the cast shards (zero_sharded_optimizer_step_gb300.sharded).
-    The total work is the whole vector whatever N is: strong scaling.
-    `value` is the elements of all shards updated per second."""
+    process r is rank r of N (N = the number of processes) in the one-rank
+    view of the workload, stepped through the library's sharded step
+    (zero_sharded_optimizer_step_gb300.sharded).  A flat vector: an
+    all-to-all of the grad slices, the local fused pass, a MAX all-reduce of
+    the flag word, the finalize, an all-gather of the cast shards.  Stage 3:
+    per unit an all-gather before forward and backward and, after the
+    unit's backward, the exchange of its grads and its local pass; the flag
+    combined after the last unit.  The total work is the whole workload
+    whatever N is: strong scaling.  `value` is the elements of all shards
+    updated per second."""
     import torch
 
     import synth
     import workloads as W
     import zero_sharded_optimizer_step_gb300 as z
-    from zero_sharded_optimizer_step_gb300.sharded import LibraryRank, ShardedStep
+    from zero_sharded_optimizer_step_gb300 import sharded as sh
 
     base = make_workload(args, args.workload)
-    if base.stage == 3 or base.rank >= 0 or base.bucket:
-        raise SystemExit("the sharded mode steps a stage-1/2 flat vector; --workload %s is not "
-                         "one (use --replicas)" % args.workload)
-    w = base.replace(world=world_size, name=base.name + "_sharded")
+    # a flat workload must be the all-ranks one (the mode picks each
+    # process's rank); stage-3 workloads are described as one rank's view
+    if (base.stage < 3 and base.rank >= 0) or base.bucket or base.groups or base.unit_rows:
+        raise SystemExit("the sharded mode steps a flat vector or flat stage-3 units; "
+                         "--workload %s is not one (use --replicas)" % args.workload)
+    w = base.replace(world=world_size, rank=rank, name=base.name + "_sharded")
     torch.cuda.set_device(device_index)
     dev = torch.device("cuda:%d" % device_index)
-    scale = w.loss_scale
-    local = LibraryRank(w.numel, w.world, rank, w.grad_dtype, w.param_dtype, dev,
-                        shadow=scale > 0, weight_decay=w.weight_decay)
-    S = local.shard
-    lo = rank * S
-    nv = max(0, min(S, w.numel - lo))
     st = torch.cuda.current_stream(dev).cuda_stream
-    if nv:
-        synth.fill_device(local.master.data_ptr(), nv, synth.F32,
-                          synth.key(w.seed, synth.KIND_MASTER), w.sigma_master, st, index0=lo)
-    local.set_master(local.master.clone())
-    grads = local.grad_buffer(S * w.world)
-    synth.fill_device(grads.data_ptr(), w.numel, w.grad_dtype,
-                      synth.key(w.seed, synth.KIND_GRAD, 1, rank), W.grad_sigma(w, scale), st)
-    step = ShardedStep(local)
+    scale = w.loss_scale
+    sigma = W.grad_sigma(w, scale)
+    bg = 4 if w.grad_dtype == 0 else 2
+    bp = 4 if w.param_dtype == 0 else 2
+    if w.stage < 3:
+        local = sh.LibraryRank(w.numel, w.world, rank, w.grad_dtype, w.param_dtype, dev,
+                               shadow=scale > 0, weight_decay=w.weight_decay)
+        units = [(w.numel, local.shard, local.master)]
+    else:
+        local = sh.LibraryRank3(w.units, w.world, rank, w.grad_dtype, w.param_dtype, dev,
+                                shadow=scale > 0, weight_decay=w.weight_decay)
+        units = [(nu, S, local.master[o:o + S])
+                 for nu, S, o in zip(w.units, local.shards, local.offsets)]
+    grads, kbytes, updated = [], 0, 0
+    for u, (nu, S, master) in enumerate(units):
+        nv = max(0, min(S, nu - rank * S))
+        if nv:
+            synth.fill_device(master.data_ptr(), nv, synth.F32,
+                              synth.key(w.seed, synth.KIND_MASTER, 0, 0, u), w.sigma_master, st,
+                              index0=rank * S)
+        g = local.grad_buffer(S * w.world)
+        synth.fill_device(g.data_ptr(), nu, w.grad_dtype,
+                          synth.key(w.seed, synth.KIND_GRAD, 1, rank, u), sigma, st)
+        grads.append(g)
+        kbytes += w.world * bg * nv + (24 + bp) * S
+        updated += S * w.world
+    if w.stage < 3:
+        local.set_master(local.master.clone())
+        step = sh.ShardedStep(local)
+    else:
+        for u, (nu, S, master) in enumerate(units):
+            local.set_master(u, master.clone())
+        step = sh.ShardedZero3Step(local)
     t, good = 0, 0
 
     def one():
         nonlocal t, scale, good
-        _, skipped = step.step(grads, w.lr, w.beta1, w.beta2, w.eps, t + 1, loss_scale=scale)
+        if w.stage < 3:
+            _, skipped = step.step(grads[0], w.lr, w.beta1, w.beta2, w.eps, t + 1,
+                                   loss_scale=scale)
+        else:
+            _, skipped = step.step(lambda u, params: grads[u], w.lr, w.beta1, w.beta2, w.eps,
+                                   t + 1, loss_scale=scale)
         if scale > 0:
             scale, good = z.zero_scale_update(scale, skipped, good, w.growth_interval)
         if not skipped:
             t += 1
         return skipped
+
+    def local_only():
+        # the rank's own kernels alone, on its local grads read as slices
+        # (the same bytes and arithmetic as the exchanged ones)
+        def slices(u):
+            S = units[u][1]
+            return [grads[u][k * S:(k + 1) * S] for k in range(w.world)]
+        hp = (w.lr, w.beta1, w.beta2, w.eps, t + 1)
+        if w.stage < 3:
+            local.local_pass(slices(0), *hp, scale)
+        else:
+            local.begin(scale)
+            for u in reversed(range(len(units))):
+                local.unit_pass(u, slices(u), *hp, scale)
+        local.finish(*hp)
 
     for _ in range(args.warmup):
         one()
@@ -775,16 +819,14 @@ def bench_sharded(args, rank, world_size, device_index):
     torch.cuda.synchronize()
     barrier(world_size)
     ms = allreduce_max(e0.elapsed_time(e1), world_size) / args.steps
-    # the local pass alone (the rank's fused kernel), for the roofline
     pairs = []
     for _ in range(args.steps):
         torch.cuda.synchronize()
         barrier(world_size)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        local.local_pass(step.slices(), w.lr, w.beta1, w.beta2, w.eps, t + 1, scale)
+        local_only()
         b.record()
-        local.finish(w.lr, w.beta1, w.beta2, w.eps, t + 1)
         local.status()
         pairs.append((a, b))
         t += 1
@@ -792,13 +834,9 @@ def bench_sharded(args, rank, world_size, device_index):
     clock_info = clocks.stop()
     assert not any(skips), "a timed step was skipped"
     kms = allreduce_max(statistics.median(a.elapsed_time(b) for a, b in pairs), world_size)
-    bg = 4 if w.grad_dtype == 0 else 2
-    bp = 4 if w.param_dtype == 0 else 2
-    kbytes = w.world * bg * nv + (24 + bp) * S
     peak, peak_kind = peaks()
     achieved = kbytes / (kms * 1e-3) / 1e9
-    updated = S * w.world
-    step_bytes = kbytes + 2 * bp * S * (w.world - 1)     # + placing the other shards
+    gathers = (2 * bp * sum(u[1] for u in units) * (w.world - 1) * (1 if w.stage < 3 else 2))
     res = {
         "metric": METRIC, "value": updated / (ms * 1e-3), "unit": "params/s",
         "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -807,22 +845,24 @@ def bench_sharded(args, rank, world_size, device_index):
                     "params": "f32 bf16 f16".split()[w.param_dtype], "state": "f32"},
         "data": "synthetic (seeded counter-based normal draws; no dataset)",
         "config": {
-            "workload": describe(w), "params_updated_per_step": updated,
+            "workload": describe(w.replace(rank=-1)), "params_updated_per_step": updated,
             "l2": "inputs larger than L2 (129 MB); no flush between timed steps",
             "parallelism": "%d processes, one data-parallel rank each (one-rank view; %s "
                            "all-to-all of grad slices, MAX all-reduce of the flag word, "
-                           "all-gather of the cast shards)"
-                           % (world_size, args.dist_backend),
+                           "all-gather of the cast shards%s)"
+                           % (world_size, args.dist_backend,
+                              ", per unit before forward and backward" if w.stage == 3 else ""),
             "path": path_of(w, scale > 0),
         },
-        "measured": {"local_pass_ms": kms, "local_alg_bytes": kbytes,
-                     "local_bytes_per_rank_per_step": step_bytes,
+        "measured": {"local_kernels_ms": kms, "local_alg_bytes": kbytes,
+                     "placed_bytes_per_rank_per_step": gathers,
                      "timing": "K whole steps between one pair of CUDA events on each rank, "
-                               "max over ranks; then K local passes alone"},
+                               "max over ranks; then the rank's own kernels alone, K times"},
         "roofline": {"kernel": "fused_step_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "alg_bytes_per_launch": kbytes, "traffic": None},
-        "gpu_launches": 2 * args.steps,
+                     "frac": achieved / peak, "alg_bytes_per_launch": kbytes / len(units),
+                     "traffic": None},
+        "gpu_launches": args.steps * (2 if w.stage < 3 else len(units) + 1),
         "clocks": clock_info,
     }
     local.close()

@@ -87,23 +87,121 @@ def test_sharded_step_through_the_library(tmp_path, numel, inject_at, shadow):
         assert d["full"].tobytes() == full.tobytes()
 
 
-def test_bench_sharded_mode_runs():
+@pytest.mark.parametrize("extra,updated", [
+    (["--numel", "4000037"], 2 * (-(-4000037 // 2))),
+    (["--workload", "zero3_gpt2_small"], None),
+])
+def test_bench_sharded_mode_runs(extra, updated):
     """bench.py's default mode for --gpus 2 (one data-parallel rank per
-    process) under torchrun: two gloo ranks on this GPU, a small vector; the
-    line reports strong scaling and every step applied."""
+    process) under torchrun: two gloo ranks on this GPU, a small flat vector
+    and the 14 ZeRO-3 units of GPT-2 small; the line reports strong scaling
+    and every step applied."""
     import json
     import subprocess
     import sys
+
+    import workloads as W
     port = _free_port()
     out = subprocess.run(
         [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
          "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--gpus", "2",
-         "--dist-backend", "gloo", "--numel", "4000037", "--steps", "3", "--warmup", "3"],
+         "--dist-backend", "gloo", "--steps", "2", "--warmup", "3", *extra],
         cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-3000:]
     lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["n_gpus"] == 2 and d["scaling"] == "strong" and d["value"] > 0
-    assert d["config"]["params_updated_per_step"] == 2 * (-(-4000037 // 2))
+    if updated is None:
+        w = W.zero3_gpt2_small().replace(world=2)
+        updated = 2 * sum(w.unit_shard(u) for u in range(len(w.units)))
+    assert d["config"]["params_updated_per_step"] == updated
     assert "gloo" in d["config"]["parallelism"]
+
+
+def _rank3(rank, world, port, units, inject_at, shadow, out_dir):
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import oracle
+    import synth
+    import zero_sharded_optimizer_step_gb300 as z
+    from zero_sharded_optimizer_step_gb300.sharded import LibraryRank3, ShardedZero3Step
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(0)
+    local = LibraryRank3(units, world, rank, z.ZERO_F16, z.ZERO_F16, "cuda:0", shadow=shadow)
+    for u, (nu, S) in enumerate(zip(units, local.shards)):
+        nv = max(0, min(S, nu - rank * S))
+        x = np.zeros(S, np.float32)
+        x[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER, 0, 0, u), 0.01,
+                                 index0=rank * S)
+        local.set_master(u, torch.from_numpy(x).cuda())
+    step = ShardedZero3Step(local)
+    scale, good, t, skips, gathered = 2.0 ** 12, 0, 0, [], {}
+    for it in (1, 2, 3):
+        def forward(u, params):
+            gathered[u] = params.cpu().view(torch.int16).numpy().view(np.uint16).copy()
+
+        def backward(u, params):
+            gathered[u] = params.cpu().view(torch.int16).numpy().view(np.uint16).copy()
+            nu, S = units[u], local.shards[u]
+            g = np.zeros(S * world, np.uint16)
+            g[:nu] = synth.fill_host(nu, synth.F16, synth.key(0, synth.KIND_GRAD, it, rank, u),
+                                     1e-3 * scale)
+            if inject_at and (it, rank, u) == inject_at[:3]:
+                g[inject_at[3]] = 0x7C00                  # +inf in fp16
+            return torch.from_numpy(g.view(np.int16)).cuda().view(torch.float16)
+        _, skipped = step.step(backward, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale,
+                               forward=forward)
+        skips.append(skipped)
+        if not skipped:
+            t += 1
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    torch.cuda.synchronize()
+    cx, cm, cv = (a.cpu().numpy() for a in local.state())
+    out = {"skips": np.array(skips)}
+    for u in range(len(units)):
+        o, S = local.offsets[u], local.shards[u]
+        out["x%d" % u], out["m%d" % u], out["v%d" % u] = cx[o:o + S], cm[o:o + S], cv[o:o + S]
+        out["lp%d" % u] = local.own_params(u).cpu().view(torch.int16).numpy().view(np.uint16)
+        out["full%d" % u] = gathered[u]
+    np.savez(os.path.join(out_dir, "rank%d.npz" % rank), **out)
+    local.close()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("inject_at,shadow", [
+    (None, True),
+    ((2, 1, 0, 1400), True),       # (iteration, rank, unit, element)
+    ((2, 0, 2, 4001), False),      # rank 0's element in rank 1's shard of unit 2
+])
+def test_sharded_zero3_through_the_library(tmp_path, inject_at, shadow):
+    """ZeRO-3 with one process per rank (ShardedZero3Step, LibraryRank3):
+    per unit an all-gather before forward and backward, the unit's grads
+    exchanged after its backward and stepped, every unit's verdict combined
+    -- bit-identical to the oracle's all-ranks step of every unit."""
+    from tests.test_multiprocess_gloo import _stage3_reference
+    world, units = 2, [3001, 17, 5000]
+    port = _free_port()
+    mp.start_processes(_rank3, args=(world, port, units, inject_at, shadow, str(tmp_path)),
+                       nprocs=world, join=True, start_method="spawn")
+    import oracle
+    st, fulls, skips = _stage3_reference(units, world, inject_at)
+    assert skips == [bool(inject_at) and it == 2 for it in (1, 2, 3)]
+    first = None
+    for r in range(world):
+        d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
+        assert list(d["skips"]) == skips, r
+        for u, nu in enumerate(units):
+            S = oracle.shard_size(nu, world)
+            sl = slice(r * S, (r + 1) * S)
+            for name, a in zip("xmv", st[u]):
+                assert d["%s%d" % (name, u)].tobytes() == a[sl].tobytes(), (r, u, name)
+            assert d["lp%d" % u].tobytes() == fulls[u][sl].tobytes()
+        if first is None:
+            first = {u: d["full%d" % u].copy() for u in range(len(units))}
+        else:
+            for u in range(len(units)):
+                assert d["full%d" % u].tobytes() == first[u].tobytes()

@@ -167,76 +167,113 @@ def test_one_rank_views_with_real_collectives(tmp_path, world, numel, inject_at)
 
 # ------------------------------------------------------------------ stage 3
 
+class OracleRank3:
+    """Rank `rank`'s own arithmetic of a stage-3 step done by the CPU oracle,
+    with the members the library's ShardedZero3Step drives (LibraryRank3's):
+    per unit fp16 param shards as 16-bit patterns in CPU tensors, the
+    step-tagged flag word; each unit's local verdict at its pass, every
+    unit's Adam once the combined verdict is in."""
+
+    def __init__(self, units, world, rank):
+        import oracle
+        import synth
+        self.o = oracle
+        self.units, self.world, self.rank = list(units), world, rank
+        self.shards = [oracle.shard_size(nu, world) for nu in units]
+        self.state, self.lp = [], []
+        for u, (nu, S) in enumerate(zip(units, self.shards)):
+            nv = max(0, min(S, nu - rank * S))
+            x = np.zeros(S, np.float32)
+            x[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER, 0, 0, u),
+                                     0.01, index0=rank * S)
+            self.state.append([x, np.zeros(S, np.float32), np.zeros(S, np.float32)])
+            self.lp.append(torch.from_numpy(oracle.cast(x, oracle.F16).view(np.int16)).clone())
+        self.flag = torch.zeros(1, dtype=torch.int64)
+        self.step_id = 0
+
+    def grad_buffer(self, n):
+        return torch.zeros(n, dtype=torch.int16)
+
+    def param_buffer(self, n):
+        return torch.zeros(n, dtype=torch.int16)
+
+    def own_params(self, u):
+        return self.lp[u]
+
+    def begin(self, loss_scale):
+        self.step_id += 1
+        self.scale = loss_scale
+        self.pending = {}
+
+    def unit_pass(self, u, slices, lr, beta1, beta2, eps, t, loss_scale):
+        o = self.o
+        S = self.shards[u]
+        nv = max(0, min(S, self.units[u] - self.rank * S))
+        sl = [s.numpy().view(np.uint16).copy() for s in slices]
+        _, bad = o.average(o.rank_sum(sl, o.F16, S, nv), self.world, loss_scale)
+        if bad:
+            self.flag[0] = self.step_id
+        self.pending[u] = sl
+
+    def finish(self, lr, beta1, beta2, eps, t):
+        o = self.o
+        others = int(self.flag.item() == self.step_id)    # any unit on any rank
+        for u, sl in self.pending.items():
+            x, m, v = self.state[u]
+            lp = self.lp[u].numpy().view(np.uint16).copy()
+            o.zero_rank_step(sl, o.F16, self.units[u], self.rank, x, m, v, lp, o.F16, lr,
+                             beta1, beta2, eps, t, loss_scale=self.scale,
+                             others_nonfinite=others)
+            self.lp[u].copy_(torch.from_numpy(lp.view(np.int16)))
+
+    def status(self):
+        bad = self.flag.item() == self.step_id
+        return bad, bad and self.scale > 0
+
+
 def _rank_main3(rank, world, port, units, inject_at, out_dir):
-    """One rank of a ZeRO-3 step over gloo: per unit an all-gather of the
-    cast shards before forward and again before backward, the unit's grads
-    reduce-scattered in rank order after its backward; with loss scaling
-    every unit's verdict is combined (MAX) before any unit's Adam counts."""
+    """One rank of a ZeRO-3 step over gloo through the library's
+    ShardedZero3Step: per unit an all-gather of the cast shards before
+    forward and again before backward, the unit's grads exchanged after its
+    backward (here: the seeded draws), every unit's verdict combined (MAX)
+    before any unit's Adam counts."""
     import sys
     sys.path.insert(0, ROOT)
     import oracle
     import synth
+    from zero_sharded_optimizer_step_gb300.sharded import ShardedZero3Step
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
-
-    def all_gather16(lp):
-        parts = [torch.zeros(lp.size, dtype=torch.int32) for _ in range(world)]
-        dist.all_gather(parts, torch.from_numpy(lp.astype(np.int32)))
-        return np.concatenate([p.numpy().astype(np.uint16) for p in parts])
-
-    state, lps, Ss = [], [], []
-    for u, nu in enumerate(units):
-        S = oracle.shard_size(nu, world)
-        nv = max(0, min(S, nu - rank * S))
-        x = np.zeros(S, np.float32)
-        x[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER, 0, 0, u), 0.01,
-                                 index0=rank * S)
-        state.append([x, np.zeros(S, np.float32), np.zeros(S, np.float32)])
-        lps.append(oracle.cast(x, oracle.F16))
-        Ss.append(S)
-    scale, good, t, skips, gathered = 2.0 ** 12, 0, 0, [], {}
+    local = OracleRank3(units, world, rank)
+    step = ShardedZero3Step(local)
+    scale, good, t, skips, gathered, seen = 2.0 ** 12, 0, 0, [], {}, []
     for it in (1, 2, 3):
-        for u in range(len(units)):                       # forward
-            gathered[u] = all_gather16(lps[u])
-        slices_of, bad_total = {}, 0
-        for u in reversed(range(len(units))):             # backward
-            gathered[u] = all_gather16(lps[u])
-            nu, S = units[u], Ss[u]
-            g = synth.fill_host(nu, synth.F16, synth.key(0, synth.KIND_GRAD, it, rank, u),
-                                1e-3 * scale)
+        def forward(u, params):
+            seen.append(("fwd", u))
+            gathered[u] = params.numpy().view(np.uint16).copy()
+
+        def backward(u, params):
+            seen.append(("bwd", u))
+            gathered[u] = params.numpy().view(np.uint16).copy()
+            nu, S = units[u], local.shards[u]
+            g = np.zeros(S * world, np.uint16)
+            g[:nu] = synth.fill_host(nu, synth.F16, synth.key(0, synth.KIND_GRAD, it, rank, u),
+                                     1e-3 * scale)
             if inject_at and (it, rank, u) == inject_at[:3]:
                 g[inject_at[3]] = 0x7C00                  # +inf in fp16
-            padded = np.zeros(S * world, np.uint16)
-            padded[:nu] = g
-            pieces = [torch.zeros(S, dtype=torch.int32) for _ in range(world)]
-            for r in range(world):
-                send = torch.from_numpy(padded[r * S:(r + 1) * S].astype(np.int32))
-                dist.gather(send, pieces if r == rank else None, dst=r)
-            slices = [p.numpy().astype(np.uint16) for p in pieces]
-            nv = max(0, min(S, nu - rank * S))
-            _, bad = oracle.average(oracle.rank_sum(slices, oracle.F16, S, nv), world, scale)
-            bad_total += bad
-            slices_of[u] = slices
-        flag = torch.tensor([bad_total], dtype=torch.int64)
-        dist.all_reduce(flag, op=dist.ReduceOp.MAX)
-        others = int(flag.item())
-        skipped = False
-        for u in range(len(units)):                       # Adam, now that the verdict is in
-            x, m, v = state[u]
-            lp = lps[u].copy()
-            sk, _ = oracle.zero_rank_step(slices_of[u], oracle.F16, units[u], rank, x, m, v, lp,
-                                          oracle.F16, 1e-3, 0.9, 0.999, 1e-8, t + 1,
-                                          loss_scale=scale, others_nonfinite=others)
-            skipped = skipped or sk
-            lps[u] = lp
+            return torch.from_numpy(g.view(np.int16))
+        _, skipped = step.step(backward, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale,
+                               forward=forward)
         skips.append(skipped)
         if not skipped:
             t += 1
         scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    U = len(units)
+    assert seen == 3 * ([("fwd", u) for u in range(U)] + [("bwd", u) for u in reversed(range(U))])
     out = {"skips": np.array(skips)}
-    for u in range(len(units)):
-        out["x%d" % u], out["m%d" % u], out["v%d" % u] = state[u]
-        out["lp%d" % u] = lps[u]
+    for u in range(U):
+        out["x%d" % u], out["m%d" % u], out["v%d" % u] = local.state[u]
+        out["lp%d" % u] = local.lp[u].numpy().view(np.uint16)
         out["full%d" % u] = gathered[u]
     np.savez(os.path.join(out_dir, "rank%d.npz" % rank), **out)
     dist.destroy_process_group()

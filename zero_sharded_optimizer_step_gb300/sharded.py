@@ -185,3 +185,143 @@ class ShardedStep:
         verdict = self.local.status()
         gather_params(self.local.params, self.local.own_params, self.group)
         return verdict
+
+
+class LibraryRank3:
+    """Rank `rank`'s own part of a stage-3 step in libzero.so's one-rank view:
+    per unit u a shard of S_u = ceil(numel_u / N) elements of fp32 state and
+    of low-precision params (the persistent shards, unit after unit), owned
+    here with the flag word.  Loss-scaled steps update every unit in one pass
+    into a second state set (`shadow`, the default; the finalize after the
+    last unit keeps or discards all of them) or reduce every unit into the
+    fp32 scratch and apply once."""
+
+    def __init__(self, unit_numels, world: int, rank: int, grad_dtype: int, param_dtype: int,
+                 device, shadow: bool = True, weight_decay: float = 0.0):
+        self.device = torch.device(device)
+        self.grad_dtype, self.param_dtype = grad_dtype, param_dtype
+        self.units = list(unit_numels)
+        self.ctx = z.zero_init(sum(self.units), world, 3, grad_dtype, param_dtype, rank,
+                               self.units)
+        self.shards = [z.zero_ctx_shard_size(self.ctx, u) for u in range(len(self.units))]
+        self.offsets = [z.zero_ctx_unit_state_offset(self.ctx, u) for u in range(len(self.units))]
+        n = z.zero_ctx_state_elems(self.ctx)
+        f32 = dict(dtype=torch.float32, device=self.device)
+        self.master = torch.zeros(n, **f32)
+        self.m = torch.zeros(n, **f32)
+        self.v = torch.zeros(n, **f32)
+        self.params = torch.zeros(z.zero_ctx_param_elems(self.ctx), dtype=_TORCH[param_dtype],
+                                  device=self.device)
+        self.flag = torch.zeros(1, dtype=torch.int64, device=self.device)
+        self.shadow = None
+        self.scratch = None
+        if shadow:
+            self.shadow = tuple(torch.zeros(n, **f32) for _ in range(3))
+            self.cur = torch.zeros(1, dtype=torch.int64, device=self.device)
+        else:
+            self.scratch = torch.zeros(n, **f32)
+        z.zero_bind(self.ctx, self.master, self.m, self.v, self.params, self.scratch, self.flag)
+        if shadow:
+            z.zero_bind_shadow(self.ctx, *self.shadow, self.cur)
+        if weight_decay:
+            z.zero_set_weight_decay(self.ctx, weight_decay)
+        self._scaled = False
+
+    def grad_buffer(self, n: int) -> torch.Tensor:
+        return torch.zeros(n, dtype=_TORCH[self.grad_dtype], device=self.device)
+
+    def param_buffer(self, n: int) -> torch.Tensor:
+        return torch.zeros(n, dtype=_TORCH[self.param_dtype], device=self.device)
+
+    def own_params(self, u: int) -> torch.Tensor:
+        return self.params[self.offsets[u]:self.offsets[u] + self.shards[u]]
+
+    def set_master(self, u: int, x: torch.Tensor) -> None:
+        """Unit u's initial fp32 shard; its params become their cast."""
+        view = self.master[self.offsets[u]:self.offsets[u] + self.shards[u]]
+        view.copy_(x)
+        self.own_params(u).copy_(view.to(self.params.dtype))
+
+    def begin(self, loss_scale) -> None:
+        self._scaled = loss_scale > 0
+        z.zero3_begin_step_scaled(self.ctx, loss_scale)
+
+    def unit_pass(self, u, slices, lr, beta1, beta2, eps, t, loss_scale, stream=None):
+        if self._scaled and self.shadow is None:
+            z.zero3_reduce_unit(self.ctx, u, slices, loss_scale, stream)
+        else:
+            z.zero3_step_unit(self.ctx, u, slices, lr, beta1, beta2, eps, t, stream)
+
+    def finish(self, lr, beta1, beta2, eps, t, stream=None):
+        if self.shadow is not None:
+            z.zero3_end_step(self.ctx, stream)
+        elif self._scaled:
+            z.zero_step_apply(self.ctx, lr, beta1, beta2, eps, t, stream)
+
+    def status(self):
+        return z.zero_step_status(self.ctx)
+
+    def state(self):
+        if self.shadow is None or z.zero_current_state(self.ctx) == 0:
+            return self.master, self.m, self.v
+        return self.shadow
+
+    def close(self):
+        self.ctx.close()
+
+
+class ShardedZero3Step:
+    """One ZeRO-3 step of this process's rank ("ZeRO 与 FSDP…", section ZeRO-3
+    与 FSDP): in the forward every unit's shards are all-gathered into a unit
+    buffer before the unit's forward runs; in the backward, last unit first,
+    the unit is gathered again, its backward runs, its grads are exchanged
+    (the all-to-all of slices) and its local pass follows; after the last
+    unit the flag word is combined over the ranks (MAX) -- every unit's
+    verdict is in -- and the rest of the step runs (the finalize over two
+    state sets, or the apply from the scratch).
+
+    `local` does the rank's arithmetic: a LibraryRank3, or any object with
+    the same members (shards, grad_buffer, param_buffer, own_params, begin,
+    unit_pass, finish, status, flag).  The caller's model enters through
+    `forward(u, params)`, called after unit u's forward gather, and
+    `backward(u, params)`, called after its backward gather, which returns
+    this rank's local grads of unit u (N * S_u elements, zeros past the
+    unit's end).  The unit buffer is reused for every unit: a hook must be
+    done with it when it returns."""
+
+    def __init__(self, local, group=None):
+        self.local = local
+        self.group = group
+        self.world = dist.get_world_size(group)
+        longest = max(local.shards) * self.world
+        self.full = local.param_buffer(longest)
+        self.recv = local.grad_buffer(longest)
+
+    def unit_params(self, u: int) -> torch.Tensor:
+        """All-gather unit u's shards into the unit buffer; returns its view."""
+        n = self.local.shards[u] * self.world
+        if n:
+            gather_params(self.full[:n], self.local.own_params(u), self.group)
+        return self.full[:n]
+
+    def step(self, backward, lr, beta1, beta2, eps, t, loss_scale=0.0, forward=None):
+        """Returns (nonfinite, skipped); every rank returns the same."""
+        local = self.local
+        U = len(local.shards)
+        local.begin(loss_scale)
+        for u in range(U):
+            params = self.unit_params(u)
+            if forward is not None:
+                forward(u, params)
+        for u in reversed(range(U)):
+            params = self.unit_params(u)
+            grads = backward(u, params)
+            S = local.shards[u]
+            n = S * self.world
+            if n:
+                exchange_slices(self.recv[:n], grads, self.group)
+            slices = [self.recv[k * S:(k + 1) * S] for k in range(self.world)]
+            local.unit_pass(u, slices, lr, beta1, beta2, eps, t, loss_scale)
+        combine_flag(local.flag, self.group)
+        local.finish(lr, beta1, beta2, eps, t)
+        return local.status()
