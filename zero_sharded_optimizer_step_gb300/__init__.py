@@ -22,4 +22,7 @@ def __getattr__(name):
     if name == "ZeroAdam":
         from .optim import ZeroAdam
         return ZeroAdam
+    if name == "ShardedZeroAdam":
+        from .optim import ShardedZeroAdam
+        return ShardedZeroAdam
     raise AttributeError(name)

@@ -1,7 +1,8 @@
 """ZeroAdam: the optimizer interface of "ZeRO 与 FSDP：切分优化器状态、梯度与参数"
 (section 从零实现 ZeRO 的 Adam: ZeroAdam(params, lr, betas, eps) with step(),
-zero_grad() and state_bytes()) over the C ABI, for N data-parallel ranks
-simulated on one GPU.
+zero_grad() and state_bytes()) over the C ABI -- `ZeroAdam` for N
+data-parallel ranks simulated on one GPU, `ShardedZeroAdam` with one process
+per rank as the page's listing runs it.
 
 Buffer management only.  The model's parameters become views of one flat,
 zero-padded parameter buffer (the page's flat vector in parameters() order);
@@ -128,3 +129,103 @@ class ZeroAdam:
 
     def close(self) -> None:
         self.ctx.close()
+
+
+class ShardedZeroAdam:
+    """The pages' ZeroAdam as its listing runs ("ZeRO 与 FSDP…", section 从零
+    实现 ZeRO 的 Adam): one process per data-parallel rank, torch.distributed
+    initialized, every process holding the whole model and computing its own
+    grads.  The parameters become views of one flat, zero-padded buffer of P
+    = N*S elements; this rank keeps fp32 master, m and v of its shard only
+    (S = ceil(numel / N)).  step() copies the parameters' .grad into one flat
+    gradient and runs the sharded step (sharded.ShardedStep over the
+    library's one-rank view): the all-to-all of gradient slices, the local
+    pass (sum in rank order, average, unscale, Adam, cast), the verdict
+    combined over the ranks and the all-gather that leaves every rank's
+    parameters updated in place.
+
+    params        tensors of one dtype (fp32, bf16 or fp16) on this process's
+                  CUDA device, the same model on every rank; their .grad is
+                  this rank's local gradient (None counts as zero).
+    loss_scale    > 0 turns on loss scaling (grads divided by it; a step with
+                  inf/nan on any rank is skipped on every rank, the scale
+                  halved; doubled after growth_interval clean steps), in one
+                  pass over two fp32 state sets.
+    weight_decay  decoupled (AdamW) decay; 0 = Adam.
+    group         the process group (None: the default group).
+    """
+
+    def __init__(self, params: Iterable[torch.Tensor], lr: float = 1e-3, betas=(0.9, 0.999),
+                 eps: float = 1e-8, weight_decay: float = 0.0, loss_scale: float = 0.0,
+                 growth_interval: int = 2000, group=None):
+        import torch.distributed as dist
+
+        from .sharded import LibraryRank, ShardedStep
+        self.params: List[torch.Tensor] = list(params)
+        if not self.params:
+            raise ValueError("ShardedZeroAdam needs at least one parameter")
+        dev, pdt = self.params[0].device, self.params[0].dtype
+        if dev.type != "cuda" or pdt not in _DT:
+            raise ValueError("parameters must be fp32, bf16 or fp16 CUDA tensors")
+        for p in self.params:
+            if p.device != dev or p.dtype != pdt:
+                raise ValueError("all parameters must share one device and dtype")
+        self.lr, (self.beta1, self.beta2), self.eps = lr, betas, eps
+        self.world, self.rank = dist.get_world_size(group), dist.get_rank(group)
+        self.t, self.scale = 0, float(loss_scale)
+        self.growth_interval, self.good_steps = growth_interval, 0
+        self.numel = sum(p.numel() for p in self.params)
+        self.local = LibraryRank(self.numel, self.world, self.rank, _DT[pdt], _DT[pdt], dev,
+                                 shadow=self.scale > 0, weight_decay=weight_decay)
+        flat = self.local.params
+        self._offsets = []
+        off = 0
+        with torch.no_grad():
+            for p in self.params:
+                n = p.numel()
+                flat[off:off + n].copy_(p.reshape(-1))
+                p.data = flat[off:off + n].view_as(p)
+                self._offsets.append((off, n))
+                off += n
+        # the own shard's master weights: its params widened (exact)
+        self.local.set_master(self.local.own_params.float())
+        self.flat_grad = self.local.grad_buffer(flat.numel())
+        self._step = ShardedStep(self.local, group)
+
+    def zero_grad(self) -> None:
+        for p in self.params:
+            p.grad = None
+
+    def step(self) -> bool:
+        """One optimizer step over this rank's grads (a collective: every
+        rank calls it).  Returns True when the step was skipped on every rank
+        (loss scaling on and a non-finite grad on any rank); then t does not
+        advance."""
+        with torch.no_grad():
+            for p, (off, n) in zip(self.params, self._offsets):
+                dst = self.flat_grad[off:off + n]
+                if p.grad is None:
+                    dst.zero_()
+                else:
+                    dst.copy_(p.grad.reshape(-1))
+        _, skipped = self._step.step(self.flat_grad, self.lr, self.beta1, self.beta2, self.eps,
+                                     self.t + 1, loss_scale=self.scale)
+        if not skipped:
+            self.t += 1
+        if self.scale > 0:
+            self.scale, self.good_steps = z.zero_scale_update(self.scale, skipped,
+                                                              self.good_steps,
+                                                              self.growth_interval)
+        return skipped
+
+    def state(self):
+        """(master, m, v) of this rank's shard, current state set."""
+        return self.local.state()
+
+    def state_bytes(self) -> int:
+        """Bytes of fp32 optimizer state this rank holds: 12 * S, what the
+        page's ZeroAdam.state_bytes() reports."""
+        return 12 * self.local.shard
+
+    def close(self) -> None:
+        self.local.close()
