@@ -834,6 +834,48 @@ def bench_sharded(args, rank, world_size, device_index):
     clock_info = clocks.stop()
     assert not any(skips), "a timed step was skipped"
     kms = allreduce_max(statistics.median(a.elapsed_time(b) for a, b in pairs), world_size)
+    e2e = None
+    in_bytes = sum(g.numel() * g.element_size() for g in grads)
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", str(world_size)))
+    if not args.no_e2e and 2 * in_bytes < 0.3 * host_ram_available() / max(1, local_ranks):
+        # the same steps with this rank's grads copied in from pinned host
+        # memory (unit by unit, inside the backward, for stage 3) and its
+        # parameter buffer copied back to pinned host memory after the step
+        host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True).copy_(g) for g in grads]
+        out = torch.empty(local.params.numel(), dtype=local.params.dtype, pin_memory=True)
+        dgrads = grads
+
+        def one_e2e():
+            nonlocal t, scale, good
+            if w.stage < 3:
+                dgrads[0].copy_(host[0], non_blocking=True)
+                _, skipped = step.step(dgrads[0], w.lr, w.beta1, w.beta2, w.eps, t + 1,
+                                       loss_scale=scale)
+            else:
+                def backward(u, params):
+                    return dgrads[u].copy_(host[u], non_blocking=True)
+                _, skipped = step.step(backward, w.lr, w.beta1, w.beta2, w.eps, t + 1,
+                                       loss_scale=scale)
+            out.copy_(local.params, non_blocking=True)
+            if scale > 0:
+                scale, good = z.zero_scale_update(scale, skipped, good, w.growth_interval)
+            if not skipped:
+                t += 1
+
+        one_e2e()
+        torch.cuda.synchronize()
+        barrier(world_size)
+        steps = max(2, args.e2e_steps)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one_e2e()
+        torch.cuda.synchronize()
+        dt = allreduce_max(time.perf_counter() - t0, world_size)
+        e2e = {"value": updated * steps / dt, "unit": "params/s", "ms_per_step": dt / steps * 1e3,
+               "h2d_bytes_per_step": in_bytes * world_size,
+               "d2h_bytes_per_step": (out.numel() * out.element_size() + 8) * world_size,
+               "per_rank": "its local grads in, its parameter buffer and the verdict out",
+               "path": "copies on each rank's compute stream around the sharded step"}
     peak, peak_kind = peaks()
     achieved = kbytes / (kms * 1e-3) / 1e9
     gathers = (2 * bp * sum(u[1] for u in units) * (w.world - 1) * (1 if w.stage < 3 else 2))
@@ -865,6 +907,8 @@ def bench_sharded(args, rank, world_size, device_index):
         "gpu_launches": args.steps * (2 if w.stage < 3 else len(units) + 1),
         "clocks": clock_info,
     }
+    if e2e is not None:
+        res["e2e"] = e2e
     local.close()
     return res
 

@@ -41,18 +41,21 @@ def _as_bytes(t: torch.Tensor) -> torch.Tensor:
     return t.reshape(-1).view(torch.uint8)
 
 
-def _staged(group, *tensors):
-    """Host copies of device tensors for a gloo group (which moves host
-    memory), or the tensors themselves."""
+def _staged(group, *tensors, outputs=()):
+    """For a gloo group (which moves host memory) and device tensors: host
+    copies of the inputs and host buffers for the outputs (positions in
+    `outputs`, whose contents are not read); otherwise the tensors
+    themselves."""
     if dist.get_backend(group) == "gloo" and any(t.is_cuda for t in tensors):
-        return [t.cpu() if t.is_cuda else t for t in tensors], True
+        return [(torch.empty(t.shape, dtype=t.dtype) if i in outputs else t.cpu())
+                if t.is_cuda else t for i, t in enumerate(tensors)], True
     return list(tensors), False
 
 
 def exchange_slices(recv: torch.Tensor, send: torch.Tensor, group=None) -> None:
     """All-to-all of equal pieces: piece k of `send` (this rank's grads of
     shard k) goes to rank k, and piece j of `recv` arrives from rank j."""
-    (r, s), staged = _staged(group, _as_bytes(recv), _as_bytes(send))
+    (r, s), staged = _staged(group, _as_bytes(recv), _as_bytes(send), outputs=(0,))
     dist.all_to_all_single(r, s, group=group)
     if staged:
         _as_bytes(recv).copy_(r)
@@ -69,7 +72,7 @@ def combine_flag(flag: torch.Tensor, group=None) -> None:
 def gather_params(full: torch.Tensor, own: torch.Tensor, group=None) -> None:
     """All-gather of every rank's cast shard into the full buffer (`own` is
     this rank's shard, a view into `full` or a buffer of its own)."""
-    (f, o), staged = _staged(group, _as_bytes(full), _as_bytes(own))
+    (f, o), staged = _staged(group, _as_bytes(full), _as_bytes(own), outputs=(0,))
     at, lo = o.data_ptr(), f.data_ptr()
     if lo <= at < lo + f.numel() and at != lo + dist.get_rank(group) * o.numel():
         o = o.clone()          # inside `full` but not at its own place: no aliasing
