@@ -57,6 +57,30 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("world,rank,scaled", [(1, 0, True), (1, -1, False), (13, 12, True),
+                                               (13, -1, False), (64, 63, False)])
+def test_visits_at_edge_worlds(world, rank, scaled):
+    """One rank (the sum is the identity), an odd world with the last rank
+    (whose shards are mostly padding), and 64 ranks (small shards, many
+    rows): gathers, state and params bit for bit the oracle's."""
+    from workloads.runner import Runner
+    units = [50_001, 1_000, 77_777, 64]
+    w = W.Workload("visit_e", sum(units), world, 3, W.BF16, W.BF16, rank=rank, units=units,
+                   steps=2, loss_scale=2.0 ** 8 if scaled else 0.0)
+    run = Runner(w, shadow=scaled)
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        seen = []
+        _visit_step(run, it, seen)
+        ref.step(it)
+        want = [g[2] for g in ref.gathers[-2 * len(units):]]
+        for a, b in zip(seen, want):
+            assert a.tobytes() == b.tobytes()
+    assert run.skips == ref.skips
+    compare_runner(run, ref, what="visits world %d rank %d" % (world, rank))
+    run.close()
+
+
 @pytest.mark.parametrize("rank,gdt,pdt,scaled", CASES)
 def test_visits_equal_the_oracle(rank, gdt, pdt, scaled):
     """Units of uneven sizes (an empty one and a 7-element one among them),
