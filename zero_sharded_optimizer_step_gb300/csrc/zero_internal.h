@@ -110,6 +110,7 @@ struct StepGatherArgs {
     GatherArgs gather;
     int32_t step_blocks;
     int32_t row_blocks;
+    int32_t step_short;            // the step part takes the 4-wide body
 };
 
 // A placement of independent rows in one launch: row y copies bytes[y]

@@ -411,6 +411,142 @@ fused_step_kernel(const __grid_constant__ StepArgs a)
     fused_step_body<GT, PT, AVG, HYPER>(a, blockIdx.x, gridDim.x);
 }
 
+// ------------------------------------------------ the 4-wide fused pass
+
+__device__ __forceinline__ uint2 ld_stream8(const void *p)
+{
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+// Store 8 bytes at an address aligned to `align` (8, 4 or 2) bytes.
+__device__ __forceinline__ void st8(void *p, uint2 v, int align)
+{
+    if (align >= 8) {
+        __stcs(reinterpret_cast<uint2 *>(p), v);
+    } else if (align == 4) {
+        unsigned *q = reinterpret_cast<unsigned *>(p);
+        q[0] = v.x;
+        q[1] = v.y;
+    } else {
+        unsigned short *q = reinterpret_cast<unsigned short *>(p);
+        q[0] = (unsigned short)(v.x & 0xffffu);
+        q[1] = (unsigned short)(v.x >> 16);
+        q[2] = (unsigned short)(v.y & 0xffffu);
+        q[3] = (unsigned short)(v.y >> 16);
+    }
+}
+
+// Four 16-bit values (8 bytes) widened to fp32, exactly.
+template <int GT>
+__device__ __forceinline__ void widen4(uint2 r, float (&o)[4])
+{
+    if constexpr (GT == BF16) {
+        o[0] = __uint_as_float(r.x << 16);
+        o[1] = __uint_as_float(r.x & 0xffff0000u);
+        o[2] = __uint_as_float(r.y << 16);
+        o[3] = __uint_as_float(r.y & 0xffff0000u);
+    } else {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&r.y));
+        o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+    }
+}
+
+// Four params cast (RNE) and stored at element i of `base`, whose byte
+// alignment is `align`.
+template <int PT>
+__device__ __forceinline__ void store_params4(void *base, int64_t i, const float (&x)[4],
+                                              int align)
+{
+    if constexpr (PT == F32) {
+        st16(static_cast<char *>(base) + i * 4,
+             make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                        __float_as_uint(x[3])), align);
+    } else {
+        unsigned w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if constexpr (PT == BF16) {
+                __nv_bfloat162 v = __floats2bfloat162_rn(x[2 * h], x[2 * h + 1]);
+                w[h] = *reinterpret_cast<unsigned *>(&v);
+            } else {
+                __half2 v = __floats2half2_rn(x[2 * h], x[2 * h + 1]);
+                w[h] = *reinterpret_cast<unsigned *>(&v);
+            }
+        }
+        st8(static_cast<char *>(base) + i * 2, make_uint2(w[0], w[1]), align < 8 ? align : 8);
+    }
+}
+
+// The fused pass with 4 elements per thread and every load of an iteration
+// issued before its arithmetic: the state first, then the ranks 8 at a time
+// -- one memory round trip for up to 8 ranks, where fused_step_body makes
+// three (two rank chunks, then the state, which it loads last to stay at 64
+// registers).  For ranges that give a thread one iteration of the 8-wide
+// layout at most (a small unit's step inside a visit), where those round
+// trips are the launch's latency.  16-bit grads; the same operations in the
+// same order as fused_step_body, element by element.
+template <int GT, int PT>
+__device__ __forceinline__ void fused_step_body4(const StepArgs &a, int64_t block, int64_t nblocks)
+{
+    static_assert(GT != F32, "16-bit grads only");
+    constexpr int kChunk = 8;
+    const int64_t stride = nblocks * blockDim.x;
+    const int64_t tid = block * blockDim.x + threadIdx.x;
+    const int64_t nvec = a.vec_ok ? a.n_valid / 4 : 0;
+    const StatePtrs st = select_state(a, true);
+    const AverageScalars &av = a.av;
+    const AdamScalars &ad = a.ad;
+    bool bad = false;
+    for (int64_t k = tid; k < nvec; k += stride) {
+        const int64_t i = k * 4;
+        const float4 xs = ld_state(st.sx + i), ms = ld_state(st.sm + i), vs = ld_state(st.sv + i);
+        float acc[4];
+        for (int c = 0; c < a.world; c += kChunk) {
+            uint2 raw[kChunk];
+#pragma unroll
+            for (int u = 0; u < kChunk; ++u)
+                if (c + u < a.world)
+                    raw[u] = ld_stream8(static_cast<const char *>(a.grads[c + u]) + i * 2);
+#pragma unroll
+            for (int u = 0; u < kChunk; ++u) {
+                if (c + u < a.world) {
+                    float f[4];
+                    widen4<GT>(raw[u], f);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[e] = c + u == 0 ? f[e] : __fadd_rn(acc[e], f[e]);
+                }
+            }
+        }
+        float x[4] = {xs.x, xs.y, xs.z, xs.w}, m[4] = {ms.x, ms.y, ms.z, ms.w};
+        float v[4] = {vs.x, vs.y, vs.z, vs.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float g = average(acc[e], av);
+            bad |= nonfinite(g);
+            adam1(g, x[e], m[e], v[e], ad);
+        }
+        st_state(st.dx + i, make_float4(x[0], x[1], x[2], x[3]));
+        st_state(st.dm + i, make_float4(m[0], m[1], m[2], m[3]));
+        st_state(st.dv + i, make_float4(v[0], v[1], v[2], v[3]));
+        store_params4<PT>(a.params, i, x, a.param_align);
+    }
+    // per-element path: ragged tail, padding, unaligned buffers
+    for (int64_t i = nvec * 4 + tid; i < a.n; i += stride) {
+        const float g = average(rank_sum1<GT>(a, i), av);
+        bad |= nonfinite(g);
+        float x = st.sx[i], m = st.sm[i], v = st.sv[i];
+        adam1(g, x, m, v, ad);
+        st.dx[i] = x;
+        st.dm[i] = m;
+        st.dv[i] = v;
+        Ty<PT>::store1(a.params, i, x);
+    }
+    publish_flag(a, bad, a.step_id);
+}
+
 // A ZeRO-3 backward visit in one launch: blocks [0, step_blocks) run the
 // fused pass over one unit (as fused_step_kernel), the rest place the next
 // unit's shards (as gather_kernel, row_blocks blocks per shard).  The two
@@ -424,6 +560,12 @@ step_gather_kernel(const __grid_constant__ StepGatherArgs a)
     pdl_launch_dependents();
     const int b = (int)blockIdx.x;
     if (b < a.step_blocks) {
+        if constexpr (GT != F32) {
+            if (a.step_short) {
+                fused_step_body4<GT, PT>(a.step, b, a.step_blocks);
+                return;
+            }
+        }
         fused_step_body<GT, PT, false, false>(a.step, b, a.step_blocks);
         return;
     }
@@ -675,9 +817,17 @@ cudaError_t step_gather_pt(const StepArgs &st, const GatherArgs &g, int sms, int
     int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(kernel), kThreads);
     const int resident = sms * per_sm;
     if (cap_per_sm > 0 && per_sm > cap_per_sm) per_sm = cap_per_sm;
-    // the step part: the grid fused_step_kernel would get
-    const int64_t want = (items(st, st.n_valid) + kThreads - 1) / kThreads;
     const int64_t cap = (int64_t)sms * per_sm;
+    // a short step range (one 8-wide iteration per thread at most) of 16-bit
+    // grads takes the 4-wide body, which issues an iteration's loads at once
+    const bool step_short = GT != F32 && st.vec_ok && st.n_valid <= cap * kThreads * kVec;
+    int64_t work = items(st, st.n_valid);
+    if (step_short) {
+        const int64_t nvec4 = st.n_valid / 4, tail = st.n - nvec4 * 4;
+        work = nvec4 > tail ? nvec4 : tail;
+    }
+    // the step part: the grid fused_step_kernel would get for that work
+    const int64_t want = (work + kThreads - 1) / kThreads;
     int64_t step_blocks = st.n > 0 ? (want < cap ? want : cap) : 0;
     if (st.n > 0 && step_blocks < 1) step_blocks = 1;
     // the gather part: the rows gather_kernel would get
@@ -688,6 +838,7 @@ cudaError_t step_gather_pt(const StepArgs &st, const GatherArgs &g, int sms, int
         g.shard_bytes > 0 ? rowcopy::row_blocks(g.shard_bytes, kThreads, resident) : 0;
     a.step_blocks = (int32_t)step_blocks;
     a.row_blocks = (int32_t)row_blocks;
+    a.step_short = step_short ? 1 : 0;
     const int64_t blocks = step_blocks + row_blocks * (g.shard_bytes > 0 ? g.n : 0);
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
