@@ -207,3 +207,90 @@ def test_sharded_zero3_through_the_library(tmp_path, inject_at, shadow):
         else:
             for u in range(len(units)):
                 assert d["full%d" % u].tobytes() == first[u].tobytes()
+
+
+def _nccl_one_rank(index, port, out_dir):
+    """A process group of one over NCCL: every collective the sharded steps
+    make (the byte all-to-all, the int64 MAX all-reduce, the in-place
+    all-gather) runs through the NCCL backend on this GPU."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import synth
+    import zero_sharded_optimizer_step_gb300 as z
+    from zero_sharded_optimizer_step_gb300.sharded import (LibraryRank, LibraryRank3,
+                                                           ShardedStep, ShardedZero3Step)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    assert dist.get_backend() == "nccl"
+    numel = 100_003
+    local = LibraryRank(numel, 1, 0, z.ZERO_BF16, z.ZERO_BF16, "cuda:0", shadow=True)
+    x0 = synth.fill_host(numel, synth.F32, synth.key(5, synth.KIND_MASTER), 0.01)
+    local.set_master(torch.from_numpy(x0).cuda())
+    step = ShardedStep(local)
+    g = synth.fill_host(numel, synth.BF16, synth.key(5, synth.KIND_GRAD, 1, 0), 1e-3)
+    dg = torch.from_numpy(g.view(np.int16)).cuda().view(torch.bfloat16)
+    verdict = step.step(dg, 1e-3, 0.9, 0.999, 1e-8, 1, loss_scale=256.0)
+    torch.cuda.synchronize()
+    x, m, v = (a.cpu().numpy() for a in local.state())
+    p = local.params.cpu().view(torch.int16).numpy().view(np.uint16)
+    units = [30_001, 7, 50_000]
+    l3 = LibraryRank3(units, 1, 0, z.ZERO_BF16, z.ZERO_BF16, "cuda:0", shadow=False)
+    g3 = []
+    for u, nu in enumerate(units):
+        xu = synth.fill_host(nu, synth.F32, synth.key(5, synth.KIND_MASTER, 0, 0, u), 0.01)
+        l3.set_master(u, torch.from_numpy(xu).cuda())
+        gu = synth.fill_host(nu, synth.BF16, synth.key(5, synth.KIND_GRAD, 1, 0, u), 1e-3)
+        g3.append(torch.from_numpy(gu.view(np.int16)).cuda().view(torch.bfloat16))
+    seen = {}
+
+    def backward(u, params):
+        seen[u] = params.cpu().view(torch.int16).numpy().view(np.uint16).copy()
+        return g3[u]
+    verdict3 = ShardedZero3Step(l3).step(backward, 1e-3, 0.9, 0.999, 1e-8, 1)
+    torch.cuda.synchronize()
+    x3, m3, v3 = (a.cpu().numpy() for a in l3.state())
+    np.savez(os.path.join(out_dir, "nccl.npz"), x=x, m=m, v=v, p=p, verdict=np.array(verdict),
+             x3=x3, p3=l3.params.cpu().view(torch.int16).numpy().view(np.uint16),
+             verdict3=np.array(verdict3), **{"seen%d" % u: s for u, s in seen.items()})
+    local.close()
+    l3.close()
+    dist.destroy_process_group()
+
+
+def test_sharded_steps_over_a_one_rank_nccl_group(tmp_path):
+    """ShardedStep and ShardedZero3Step over a real NCCL group of one rank:
+    the result is the oracle's (one rank: the step on the whole vector)."""
+    mp.start_processes(_nccl_one_rank, args=(_free_port(), str(tmp_path)), nprocs=1, join=True,
+                       start_method="spawn")
+    import oracle
+    import synth
+    d = np.load(os.path.join(tmp_path, "nccl.npz"))
+    numel = 100_003
+    x = synth.fill_host(numel, synth.F32, synth.key(5, synth.KIND_MASTER), 0.01)
+    m, v = np.zeros(numel, np.float32), np.zeros(numel, np.float32)
+    full = np.zeros(numel, np.uint16)
+    g = synth.fill_host(numel, synth.BF16, synth.key(5, synth.KIND_GRAD, 1, 0), 1e-3)
+    oracle.zero_step([g], oracle.BF16, numel, x, m, v, full, oracle.BF16, 1e-3, 0.9, 0.999, 1e-8,
+                     1, loss_scale=256.0)
+    assert tuple(d["verdict"]) == (False, False)
+    assert d["x"].tobytes() == x.tobytes() and d["m"].tobytes() == m.tobytes()
+    assert d["v"].tobytes() == v.tobytes() and d["p"].tobytes() == full.tobytes()
+    units = [30_001, 7, 50_000]
+    xs, ps = [], []
+    for u, nu in enumerate(units):
+        xu = synth.fill_host(nu, synth.F32, synth.key(5, synth.KIND_MASTER, 0, 0, u), 0.01)
+        # the gathers before the update placed the cast initial weights
+        assert d["seen%d" % u].tobytes() == oracle.cast(xu, oracle.BF16).tobytes()
+        gu = synth.fill_host(nu, synth.BF16, synth.key(5, synth.KIND_GRAD, 1, 0, u), 1e-3)
+        mu, vu = np.zeros(nu, np.float32), np.zeros(nu, np.float32)
+        fu = np.zeros(nu, np.uint16)
+        oracle.zero_step([gu], oracle.BF16, nu, xu, mu, vu, fu, oracle.BF16, 1e-3, 0.9, 0.999,
+                         1e-8, 1)
+        xs.append(xu)
+        ps.append(fu)
+    assert tuple(d["verdict3"]) == (False, False)
+    assert d["x3"].tobytes() == np.concatenate(xs).tobytes()
+    assert d["p3"].tobytes() == np.concatenate(ps).tobytes()
