@@ -402,6 +402,9 @@ int zero_step_apply(zero_ctx *ctx, double lr, double beta1, double beta2, double
  *     scratch; zero_bucket_end applies Adam to every element, or to none.
  * Bucket offsets that are multiples of 8 elements keep every access on the
  * 16-byte vector path. */
+/* With one process per rank (the one-rank view), zero_bucket_end of a
+ * loss-scaled step decides from the flag word: combine it with the other
+ * ranks' words first (a MAX all-reduce), as before zero_step_apply. */
 int zero_bucket_begin(zero_ctx *ctx, float loss_scale);
 int zero_bucket_step(zero_ctx *ctx, int64_t offset, int64_t count, const void *const *grads,
                      int32_t n_grads, double lr, double beta1, double beta2, double eps,
@@ -484,7 +487,10 @@ int zero3_begin_step(zero_ctx *ctx);
 int zero3_begin_step_scaled(zero_ctx *ctx, float loss_scale);
 
 /* End a stage-3 step begun with a second state set bound (the finalize
- * described above, one small launch); without one it does nothing. */
+ * described above, one small launch); without one it does nothing.  In the
+ * one-rank view with one process per rank, combine the flag word with the
+ * other ranks' words first (a MAX all-reduce of the 8 bytes: every rank runs
+ * the same step ids), so that every rank keeps or discards the step alike. */
 int zero3_end_step(zero_ctx *ctx, void *stream);
 
 /* Gather unit `unit`'s N parameter shards (S_u elements of param_dtype
