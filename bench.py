@@ -898,6 +898,11 @@ def bench_sharded(args, rank, world_size, device_index):
         },
         "measured": {"local_kernels_ms": kms, "local_alg_bytes": kbytes,
                      "placed_bytes_per_rank_per_step": gathers,
+                     # what the step spends outside the rank's own kernels
+                     # (the collectives and their waits); the Paddle page's
+                     # profiling advice flags a collective share above 30%
+                     "collective_share_of_step": max(0.0, 1.0 - kms / ms),
+                     "collective_share_above_30pct": (1.0 - kms / ms) > 0.30,
                      "timing": "K whole steps between one pair of CUDA events on each rank, "
                                "max over ranks; then the rank's own kernels alone, K times"},
         "roofline": {"kernel": "fused_step_kernel", "bound": "hbm", "achieved": achieved,

@@ -117,6 +117,7 @@ def test_bench_sharded_mode_runs(extra, updated):
         updated = 2 * sum(w.unit_shard(u) for u in range(len(w.units)))
     assert d["config"]["params_updated_per_step"] == updated
     assert "gloo" in d["config"]["parallelism"]
+    assert 0.0 <= d["measured"]["collective_share_of_step"] <= 1.0
     assert d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] > 0
     assert d["e2e"]["d2h_bytes_per_step"] > 0
 

@@ -37,6 +37,26 @@ from . import binding as z
 _TORCH = {z.ZERO_F32: torch.float32, z.ZERO_BF16: torch.bfloat16, z.ZERO_F16: torch.float16}
 
 
+class _Range:
+    """An NVTX range around a phase of the step (exchange, local pass,
+    verdict, rest, all-gather), for a profiler's timeline; a no-op where
+    NVTX is not available."""
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        try:
+            torch.cuda.nvtx.range_push(self.name)
+            self.pushed = True
+        except Exception:
+            self.pushed = False
+
+    def __exit__(self, *exc):
+        if self.pushed:
+            torch.cuda.nvtx.range_pop()
+
+
 def _as_bytes(t: torch.Tensor) -> torch.Tensor:
     return t.reshape(-1).view(torch.uint8)
 
@@ -181,12 +201,16 @@ class ShardedStep:
         """local_grads: this rank's gradient of the whole padded vector (P =
         N*S elements, zeros past numel).  Returns (nonfinite, skipped); every
         rank returns the same."""
-        exchange_slices(self.recv, local_grads, self.group)
-        self.local.local_pass(self.slices(), lr, beta1, beta2, eps, t, loss_scale)
-        combine_flag(self.local.flag, self.group)
-        self.local.finish(lr, beta1, beta2, eps, t)
-        verdict = self.local.status()
-        gather_params(self.local.params, self.local.own_params, self.group)
+        with _Range("zero: exchange"):
+            exchange_slices(self.recv, local_grads, self.group)
+        with _Range("zero: local pass"):
+            self.local.local_pass(self.slices(), lr, beta1, beta2, eps, t, loss_scale)
+        with _Range("zero: verdict"):
+            combine_flag(self.local.flag, self.group)
+            self.local.finish(lr, beta1, beta2, eps, t)
+            verdict = self.local.status()
+        with _Range("zero: all-gather"):
+            gather_params(self.local.params, self.local.own_params, self.group)
         return verdict
 
 
@@ -313,18 +337,23 @@ class ShardedZero3Step:
         U = len(local.shards)
         local.begin(loss_scale)
         for u in range(U):
-            params = self.unit_params(u)
+            with _Range("zero3: gather %d" % u):
+                params = self.unit_params(u)
             if forward is not None:
                 forward(u, params)
         for u in reversed(range(U)):
-            params = self.unit_params(u)
+            with _Range("zero3: gather %d" % u):
+                params = self.unit_params(u)
             grads = backward(u, params)
             S = local.shards[u]
             n = S * self.world
-            if n:
-                exchange_slices(self.recv[:n], grads, self.group)
+            with _Range("zero3: exchange %d" % u):
+                if n:
+                    exchange_slices(self.recv[:n], grads, self.group)
             slices = [self.recv[k * S:(k + 1) * S] for k in range(self.world)]
-            local.unit_pass(u, slices, lr, beta1, beta2, eps, t, loss_scale)
-        combine_flag(local.flag, self.group)
-        local.finish(lr, beta1, beta2, eps, t)
-        return local.status()
+            with _Range("zero3: local pass %d" % u):
+                local.unit_pass(u, slices, lr, beta1, beta2, eps, t, loss_scale)
+        with _Range("zero3: verdict"):
+            combine_flag(local.flag, self.group)
+            local.finish(lr, beta1, beta2, eps, t)
+            return local.status()
