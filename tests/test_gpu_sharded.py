@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _rank(rank, world, port, numel, inject_at, shadow, out_dir):
+def _rank(rank, world, port, numel, inject_at, shadow, out_dir, weight_decay=0.0):
     import sys
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
@@ -32,7 +32,8 @@ def _rank(rank, world, port, numel, inject_at, shadow, out_dir):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     torch.cuda.set_device(0)
-    local = LibraryRank(numel, world, rank, z.ZERO_F16, z.ZERO_F16, "cuda:0", shadow=shadow)
+    local = LibraryRank(numel, world, rank, z.ZERO_F16, z.ZERO_F16, "cuda:0", shadow=shadow,
+                        weight_decay=weight_decay)
     S = local.shard
     lo = rank * S
     nv = max(0, min(S, numel - lo))
@@ -295,3 +296,41 @@ def test_sharded_steps_over_a_one_rank_nccl_group(tmp_path):
     assert tuple(d["verdict3"]) == (False, False)
     assert d["x3"].tobytes() == np.concatenate(xs).tobytes()
     assert d["p3"].tobytes() == np.concatenate(ps).tobytes()
+
+
+def test_sharded_step_with_decoupled_weight_decay(tmp_path):
+    """AdamW (weight decay 0.1) through ShardedStep and LibraryRank, two
+    processes, a skipped step: bit-identical to the oracle's all-ranks
+    AdamW step."""
+    import oracle
+    import synth
+    world, numel, inject_at, wd = 2, 200_003, (2, 0, 150_001), 0.1
+    mp.start_processes(_rank, args=(world, _free_port(), numel, inject_at, True, str(tmp_path),
+                                    wd), nprocs=world, join=True, start_method="spawn")
+    S = oracle.shard_size(numel, world)
+    P = S * world
+    x = np.zeros(P, np.float32)
+    x[:numel] = synth.fill_host(numel, synth.F32, synth.key(0, synth.KIND_MASTER), 0.01)
+    m, v = np.zeros(P, np.float32), np.zeros(P, np.float32)
+    full = np.zeros(P, np.uint16)
+    scale, good, t, skips = 2.0 ** 12, 0, 0, []
+    for it in (1, 2, 3):
+        grads = [synth.fill_host(numel, synth.F16, synth.key(0, synth.KIND_GRAD, it, k),
+                                 1e-3 * scale) for k in range(world)]
+        if it == inject_at[0]:
+            grads[inject_at[1]][inject_at[2]] = 0x7C00
+        skipped, _ = oracle.zero_step(grads, oracle.F16, numel, x, m, v, full, oracle.F16, 1e-3,
+                                      0.9, 0.999, 1e-8, t + 1, loss_scale=scale,
+                                      weight_decay=wd)
+        skips.append(skipped)
+        if not skipped:
+            t += 1
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    assert skips == [False, True, False]
+    for r in range(world):
+        d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
+        assert list(d["skips"]) == skips
+        sl = slice(r * S, (r + 1) * S)
+        assert d["x"].tobytes() == x[sl].tobytes() and d["m"].tobytes() == m[sl].tobytes()
+        assert d["v"].tobytes() == v[sl].tobytes() and d["full"].tobytes() == full.tobytes()
+

@@ -204,3 +204,26 @@ def test_visits_that_would_overlap_are_refused():
     for x, y in zip(before, (run.master, run.m, run.v, run.params, run.unit_full)):
         assert torch.equal(x, y)
     run.close()
+
+
+@pytest.mark.parametrize("rank", [1, -1])
+def test_visits_with_decoupled_weight_decay(rank):
+    """AdamW (weight decay 0.05) through both step bodies of the visit kernel
+    (a small unit takes the 4-wide body, a 1.5M-element one the 8-wide
+    body): bit for bit the oracle's."""
+    from workloads.runner import Runner
+    units = [6_000_004, 10_007, 250_000]
+    w = W.Workload("visit_wd", sum(units), 4, 3, W.BF16, W.BF16, rank=rank, units=units,
+                   steps=3, weight_decay=0.05)
+    run = Runner(w)
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        seen = []
+        _visit_step(run, it, seen)
+        ref.step(it)
+        want = [g[2] for g in ref.gathers[-2 * len(units):]]
+        for a, b in zip(seen, want):
+            assert a.tobytes() == b.tobytes()
+    compare_runner(run, ref, what="visits AdamW rank %d" % rank)
+    run.close()
+
