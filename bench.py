@@ -773,7 +773,8 @@ def bench_sharded(args, rank, world_size, device_index):
     else:
         for u, (nu, S, master) in enumerate(units):
             local.set_master(u, master.clone())
-        step = sh.ShardedZero3Step(local)
+        # the next unit's all-gather in flight while a unit is worked on
+        step = sh.ShardedZero3Step(local, prefetch=True)
     t, good = 0, 0
 
     def one():

@@ -123,7 +123,7 @@ def test_bench_sharded_mode_runs(extra, updated):
     assert d["e2e"]["d2h_bytes_per_step"] > 0
 
 
-def _rank3(rank, world, port, units, inject_at, shadow, out_dir):
+def _rank3(rank, world, port, units, inject_at, shadow, out_dir, prefetch=False):
     import sys
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
@@ -142,7 +142,7 @@ def _rank3(rank, world, port, units, inject_at, shadow, out_dir):
         x[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER, 0, 0, u), 0.01,
                                  index0=rank * S)
         local.set_master(u, torch.from_numpy(x).cuda())
-    step = ShardedZero3Step(local)
+    step = ShardedZero3Step(local, prefetch=prefetch)
     scale, good, t, skips, gathered = 2.0 ** 12, 0, 0, [], {}
     for it in (1, 2, 3):
         def forward(u, params):
@@ -176,12 +176,14 @@ def _rank3(rank, world, port, units, inject_at, shadow, out_dir):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("inject_at,shadow", [
-    (None, True),
-    ((2, 1, 0, 1400), True),       # (iteration, rank, unit, element)
-    ((2, 0, 2, 4001), False),      # rank 0's element in rank 1's shard of unit 2
+@pytest.mark.parametrize("inject_at,shadow,prefetch", [
+    (None, True, False),
+    ((2, 1, 0, 1400), True, False),    # (iteration, rank, unit, element)
+    ((2, 0, 2, 4001), False, False),   # rank 0's element in rank 1's shard of unit 2
+    ((2, 1, 0, 1400), True, True),     # the next unit's gather in flight
+    (None, False, True),
 ])
-def test_sharded_zero3_through_the_library(tmp_path, inject_at, shadow):
+def test_sharded_zero3_through_the_library(tmp_path, inject_at, shadow, prefetch):
     """ZeRO-3 with one process per rank (ShardedZero3Step, LibraryRank3):
     per unit an all-gather before forward and backward, the unit's grads
     exchanged after its backward and stepped, every unit's verdict combined
@@ -189,8 +191,8 @@ def test_sharded_zero3_through_the_library(tmp_path, inject_at, shadow):
     from tests.test_multiprocess_gloo import _stage3_reference
     world, units = 2, [3001, 17, 5000]
     port = _free_port()
-    mp.start_processes(_rank3, args=(world, port, units, inject_at, shadow, str(tmp_path)),
-                       nprocs=world, join=True, start_method="spawn")
+    mp.start_processes(_rank3, args=(world, port, units, inject_at, shadow, str(tmp_path),
+                                     prefetch), nprocs=world, join=True, start_method="spawn")
     import oracle
     st, fulls, skips = _stage3_reference(units, world, inject_at)
     assert skips == [bool(inject_at) and it == 2 for it in (1, 2, 3)]

@@ -231,7 +231,7 @@ class OracleRank3:
         return bad, bad and self.scale > 0
 
 
-def _rank_main3(rank, world, port, units, inject_at, out_dir):
+def _rank_main3(rank, world, port, units, inject_at, out_dir, prefetch=False):
     """One rank of a ZeRO-3 step over gloo through the library's
     ShardedZero3Step: per unit an all-gather of the cast shards before
     forward and again before backward, the unit's grads exchanged after its
@@ -245,7 +245,7 @@ def _rank_main3(rank, world, port, units, inject_at, out_dir):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     local = OracleRank3(units, world, rank)
-    step = ShardedZero3Step(local)
+    step = ShardedZero3Step(local, prefetch=prefetch)
     scale, good, t, skips, gathered, seen = 2.0 ** 12, 0, 0, [], {}, []
     for it in (1, 2, 3):
         def forward(u, params):
@@ -314,14 +314,16 @@ def _stage3_reference(units, world, inject_at):
     return st, fulls, skips
 
 
-@pytest.mark.parametrize("world,units,inject_at", [
-    (2, [3001, 17, 5000], None),
-    (2, [3001, 17, 5000], (2, 1, 0, 1400)),      # (iteration, rank, unit, element)
-    (4, [3001, 17, 5000], (2, 3, 2, 11)),       # rank 3's element in rank 0's shard of unit 2
+@pytest.mark.parametrize("world,units,inject_at,prefetch", [
+    (2, [3001, 17, 5000], None, False),
+    (2, [3001, 17, 5000], (2, 1, 0, 1400), False),    # (iteration, rank, unit, element)
+    (4, [3001, 17, 5000], (2, 3, 2, 11), False),     # rank 3's element in rank 0's shard of unit 2
+    (2, [3001, 17, 5000, 64], (2, 1, 0, 1400), True),  # the next unit's gather in flight
+    (4, [3001, 17, 5000], (2, 3, 2, 11), True),
 ])
-def test_stage3_ranks_with_real_collectives(tmp_path, world, units, inject_at):
+def test_stage3_ranks_with_real_collectives(tmp_path, world, units, inject_at, prefetch):
     port = _free_port()
-    mp.start_processes(_rank_main3, args=(world, port, units, inject_at, str(tmp_path)),
+    mp.start_processes(_rank_main3, args=(world, port, units, inject_at, str(tmp_path), prefetch),
                        nprocs=world, join=True, start_method="spawn")
     import oracle
     st, fulls, skips = _stage3_reference(units, world, inject_at)

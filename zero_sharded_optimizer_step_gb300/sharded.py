@@ -89,16 +89,37 @@ def combine_flag(flag: torch.Tensor, group=None) -> None:
         flag.copy_(f)
 
 
-def gather_params(full: torch.Tensor, own: torch.Tensor, group=None) -> None:
+class Pending:
+    """An all-gather in flight (gather_params with async_op=True): wait()
+    makes the caller's stream wait for it (and, over gloo, copies the
+    gathered bytes from host memory into the destination)."""
+
+    def __init__(self, work, dst=None, src=None):
+        self.work, self.dst, self.src = work, dst, src
+
+    def wait(self) -> None:
+        if self.work is not None:
+            self.work.wait()
+            self.work = None
+            if self.dst is not None:
+                self.dst.copy_(self.src)
+
+
+def gather_params(full: torch.Tensor, own: torch.Tensor, group=None, async_op: bool = False):
     """All-gather of every rank's cast shard into the full buffer (`own` is
-    this rank's shard, a view into `full` or a buffer of its own)."""
+    this rank's shard, a view into `full` or a buffer of its own).  With
+    async_op the collective is left in flight and a Pending is returned."""
     (f, o), staged = _staged(group, _as_bytes(full), _as_bytes(own), outputs=(0,))
     at, lo = o.data_ptr(), f.data_ptr()
     if lo <= at < lo + f.numel() and at != lo + dist.get_rank(group) * o.numel():
         o = o.clone()          # inside `full` but not at its own place: no aliasing
-    dist.all_gather_into_tensor(f, o, group=group)
-    if staged:
-        _as_bytes(full).copy_(f)
+    work = dist.all_gather_into_tensor(f, o, group=group, async_op=async_op)
+    pending = Pending(work, _as_bytes(full) if staged else None, f if staged else None)
+    if not async_op:
+        if staged:
+            _as_bytes(full).copy_(f)
+        return None
+    return pending
 
 
 class LibraryRank:
@@ -313,37 +334,66 @@ class ShardedZero3Step:
     `forward(u, params)`, called after unit u's forward gather, and
     `backward(u, params)`, called after its backward gather, which returns
     this rank's local grads of unit u (N * S_u elements, zeros past the
-    unit's end).  The unit buffer is reused for every unit: a hook must be
-    done with it when it returns."""
+    unit's end).  A hook must be done with its unit buffer when it returns.
 
-    def __init__(self, local, group=None):
+    prefetch=True gathers ahead ("ZeRO 与 FSDP…", ZeRO-3 与 FSDP: the next
+    unit's all-gather is issued before this unit computes, so the two
+    overlap): two unit buffers alternate, and the all-gather of the unit
+    visited next is in flight while a hook runs on the current one.  The
+    results are the same either way."""
+
+    def __init__(self, local, group=None, prefetch: bool = False):
         self.local = local
         self.group = group
         self.world = dist.get_world_size(group)
+        self.prefetch = prefetch
         longest = max(local.shards) * self.world
-        self.full = local.param_buffer(longest)
+        self.fulls = [local.param_buffer(longest) for _ in range(2 if prefetch else 1)]
+        self.full = self.fulls[0]
         self.recv = local.grad_buffer(longest)
+
+    def _issue(self, u: int, buf: int, async_op: bool):
+        """Start (or, without async_op, do) unit u's all-gather into unit
+        buffer `buf`; returns (view, pending or None)."""
+        n = self.local.shards[u] * self.world
+        view = self.fulls[buf][:n]
+        pending = None
+        if n:
+            with _Range("zero3: gather %d" % u):
+                pending = gather_params(view, self.local.own_params(u), self.group,
+                                        async_op=async_op)
+        return view, pending
 
     def unit_params(self, u: int) -> torch.Tensor:
         """All-gather unit u's shards into the unit buffer; returns its view."""
-        n = self.local.shards[u] * self.world
-        if n:
-            gather_params(self.full[:n], self.local.own_params(u), self.group)
-        return self.full[:n]
+        return self._issue(u, 0, False)[0]
+
+    def _visits(self, order):
+        """(unit, gathered params) for the units in `order`, each gathered
+        before it is yielded; with prefetch the next unit's gather is in
+        flight while the caller works on the yielded one."""
+        if not self.prefetch:
+            for u in order:
+                yield u, self.unit_params(u)
+            return
+        ahead = self._issue(order[0], 0, True) if order else None
+        for j, u in enumerate(order):
+            view, pending = ahead
+            if pending is not None:
+                pending.wait()
+            if j + 1 < len(order):
+                ahead = self._issue(order[j + 1], (j + 1) % 2, True)
+            yield u, view
 
     def step(self, backward, lr, beta1, beta2, eps, t, loss_scale=0.0, forward=None):
         """Returns (nonfinite, skipped); every rank returns the same."""
         local = self.local
         U = len(local.shards)
         local.begin(loss_scale)
-        for u in range(U):
-            with _Range("zero3: gather %d" % u):
-                params = self.unit_params(u)
+        for u, params in self._visits(list(range(U))):
             if forward is not None:
                 forward(u, params)
-        for u in reversed(range(U)):
-            with _Range("zero3: gather %d" % u):
-                params = self.unit_params(u)
+        for u, params in self._visits(list(reversed(range(U)))):
             grads = backward(u, params)
             S = local.shards[u]
             n = S * self.world
