@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _rank(rank, world, port, numel, inject_at, shadow, out_dir, weight_decay=0.0):
+def _rank(rank, world, port, numel, inject_at, shadow, out_dir, weight_decay=0.0, bucket=0):
     import sys
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
@@ -50,7 +50,17 @@ def _rank(rank, world, port, numel, inject_at, shadow, out_dir, weight_decay=0.0
         if inject_at and it == inject_at[0] and rank == inject_at[1]:
             g[inject_at[2]] = 0x7C00                          # +inf in fp16
         dg = torch.from_numpy(g.view(np.int16)).cuda().view(torch.float16)
-        _, skipped = step.step(dg, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale)
+        if bucket:
+            # bucket by bucket from one reused device buffer
+            buf = torch.zeros(bucket, dtype=torch.float16, device="cuda:0")
+            step.begin(scale)
+            for off in range(0, P, bucket):
+                n = min(bucket, P - off)
+                buf[:n].copy_(dg[off:off + n])
+                step.bucket(off, buf[:n], 1e-3, 0.9, 0.999, 1e-8, t + 1)
+            _, skipped = step.end(1e-3, 0.9, 0.999, 1e-8, t + 1)
+        else:
+            _, skipped = step.step(dg, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale)
         skips.append(skipped)
         if not skipped:
             t += 1
@@ -64,16 +74,18 @@ def _rank(rank, world, port, numel, inject_at, shadow, out_dir, weight_decay=0.0
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("numel,inject_at,shadow", [
-    (300_007, None, True),
-    (300_007, (2, 1, 299_999), True),     # rank 1's +inf in rank 1's shard
-    (300_007, (2, 0, 200_001), False),    # rank 0's +inf in rank 1's shard
+@pytest.mark.parametrize("numel,inject_at,shadow,bucket", [
+    (300_007, None, True, 0),
+    (300_007, (2, 1, 299_999), True, 0),      # rank 1's +inf in rank 1's shard
+    (300_007, (2, 0, 200_001), False, 0),     # rank 0's +inf in rank 1's shard
+    (300_007, (2, 0, 200_001), True, 70_001),  # buckets, one across the shard boundary
+    (300_007, (2, 1, 299_999), False, 70_001),
 ])
-def test_sharded_step_through_the_library(tmp_path, numel, inject_at, shadow):
+def test_sharded_step_through_the_library(tmp_path, numel, inject_at, shadow, bucket):
     world = 2
     port = _free_port()
-    mp.start_processes(_rank, args=(world, port, numel, inject_at, shadow, str(tmp_path)),
-                       nprocs=world, join=True, start_method="spawn")
+    mp.start_processes(_rank, args=(world, port, numel, inject_at, shadow, str(tmp_path), 0.0,
+                                    bucket), nprocs=world, join=True, start_method="spawn")
     import oracle
     x, m, v, full, skips = _all_ranks_reference(numel, world, inject_at)
     assert skips == [bool(inject_at) and it == inject_at[0] for it in (1, 2, 3)]

@@ -77,8 +77,30 @@ class OracleRank:
         bad = self.flag.item() == self.step_id
         return bad, bad and self.scale > 0
 
+    # the bucketed form: pieces of the shard arrive bucket by bucket; each
+    # piece's local verdict at once, the oracle's step on the whole shard once
+    # the combined verdict is in (the update is elementwise)
+    def bucket_begin(self, loss_scale):
+        self.step_id += 1
+        self.scale = loss_scale
+        self.sl = [np.zeros(self.shard, np.uint16) for _ in range(self.world)]
 
-def _rank_main(rank, world, port, numel, inject_at, out_dir):
+    def bucket_pass(self, offset, count, slices, lr, beta1, beta2, eps, t):
+        o = self.oracle
+        piece = []
+        for k, s in enumerate(slices):
+            self.sl[k][offset:offset + count] = s.numpy().view(np.uint16)
+            piece.append(self.sl[k][offset:offset + count].copy())
+        nv = max(0, min(count, self.nv - offset))
+        _, bad = o.average(o.rank_sum(piece, o.F16, count, nv), self.world, self.scale)
+        if bad:
+            self.flag[0] = self.step_id
+
+    def bucket_end(self, lr, beta1, beta2, eps, t):
+        self.finish(lr, beta1, beta2, eps, t)
+
+
+def _rank_main(rank, world, port, numel, inject_at, out_dir, bucket=0):
     """One data-parallel rank, driven by the library's sharded step (the
     all-to-all of the grad slices, the MAX combine of the flag word, the
     all-gather of the cast shards) with the oracle's arithmetic."""
@@ -100,8 +122,18 @@ def _rank_main(rank, world, port, numel, inject_at, out_dir):
                                     1e-3 * scale)
         if inject_at and it == inject_at[0] and rank == inject_at[1]:
             g[inject_at[2]] = 0x7C00                          # +inf in fp16
-        _, skipped = step.step(torch.from_numpy(g.view(np.int16)), 1e-3, 0.9, 0.999, 1e-8,
-                               t + 1, loss_scale=scale)
+        gt = torch.from_numpy(g.view(np.int16))
+        if bucket:
+            # the same step bucket by bucket, each bucket from one reused buffer
+            buf = torch.zeros(bucket, dtype=torch.int16)
+            step.begin(scale)
+            for off in range(0, P, bucket):
+                n = min(bucket, P - off)
+                buf[:n].copy_(gt[off:off + n])
+                step.bucket(off, buf[:n], 1e-3, 0.9, 0.999, 1e-8, t + 1)
+            _, skipped = step.end(1e-3, 0.9, 0.999, 1e-8, t + 1)
+        else:
+            _, skipped = step.step(gt, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale)
         skips.append(skipped)
         if not skipped:
             t += 1
@@ -141,14 +173,17 @@ def _all_ranks_reference(numel, world, inject_at):
     return x, m, v, full, skips
 
 
-@pytest.mark.parametrize("world,numel,inject_at", [
-    (2, 10_001, None),
-    (2, 10_001, (2, 1, 9_999)),      # rank 1's element in rank 1's shard
-    (4, 20_003, (2, 3, 17)),         # rank 3's element in rank 0's shard
+@pytest.mark.parametrize("world,numel,inject_at,bucket", [
+    (2, 10_001, None, 0),
+    (2, 10_001, (2, 1, 9_999), 0),      # rank 1's element in rank 1's shard
+    (4, 20_003, (2, 3, 17), 0),         # rank 3's element in rank 0's shard
+    (2, 10_001, (2, 1, 9_999), 3_001),  # buckets, one across the shard boundary
+    (4, 20_003, (2, 3, 17), 7_000),
+    (4, 20_003, None, 20_004),          # one bucket: the whole vector
 ])
-def test_one_rank_views_with_real_collectives(tmp_path, world, numel, inject_at):
+def test_one_rank_views_with_real_collectives(tmp_path, world, numel, inject_at, bucket):
     port = _free_port()
-    mp.start_processes(_rank_main, args=(world, port, numel, inject_at, str(tmp_path)),
+    mp.start_processes(_rank_main, args=(world, port, numel, inject_at, str(tmp_path), bucket),
                        nprocs=world, join=True, start_method="spawn")
     import oracle
     x, m, v, full, skips = _all_ranks_reference(numel, world, inject_at)
