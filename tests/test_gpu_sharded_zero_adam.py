@@ -26,7 +26,7 @@ def _flat(params):
     return torch.cat([p.detach().reshape(-1).float().cpu() for p in params]).numpy()
 
 
-def _rank(rank, port, out_dir):
+def _rank(rank, port, out_dir, bucket_elems=0):
     import copy
     import sys
     sys.path.insert(0, ROOT)
@@ -42,7 +42,8 @@ def _rank(rank, port, out_dir):
                                 torch.nn.Linear(256, 10)).to(dev)
     ref = copy.deepcopy(model)
     init = _flat(model.parameters())
-    opt = z.ShardedZeroAdam(model.parameters(), lr=LR, betas=(0.9, 0.999), eps=1e-8)
+    opt = z.ShardedZeroAdam(model.parameters(), lr=LR, betas=(0.9, 0.999), eps=1e-8,
+                            bucket_elems=bucket_elems)
     ref_opt = torch.optim.Adam(ref.parameters(), lr=LR, betas=(0.9, 0.999), eps=1e-8)
     loss_fn = torch.nn.CrossEntropyLoss()
     grads = []
@@ -52,8 +53,19 @@ def _rank(rank, port, out_dir):
         y = torch.randint(0, 10, (WORLD * PER_RANK,), generator=gen).to(dev)
         sl = slice(rank * PER_RANK, (rank + 1) * PER_RANK)
         opt.zero_grad()
-        loss_fn(model(x[sl]), y[sl]).backward()
-        grads.append(torch.cat([p.grad.reshape(-1) for p in model.parameters()]).cpu().numpy())
+        if bucket_elems:
+            # this rank's grads, for the oracle, from an identical backward of
+            # a copy (the bucketed optimizer consumes and frees .grad)
+            twin = copy.deepcopy(model)
+            loss_fn(twin(x[sl]), y[sl]).backward()
+            grads.append(torch.cat([p.grad.reshape(-1) for p in twin.parameters()]).cpu().numpy())
+            loss_fn(model(x[sl]), y[sl]).backward()
+            # the buckets were exchanged during the backward; no grad is kept
+            assert all(p.grad is None for p in model.parameters())
+        else:
+            loss_fn(model(x[sl]), y[sl]).backward()
+            grads.append(torch.cat([p.grad.reshape(-1)
+                                    for p in model.parameters()]).cpu().numpy())
         assert opt.step() is False
         ref_opt.zero_grad(set_to_none=True)
         loss_fn(ref(x), y).backward()
@@ -67,13 +79,17 @@ def _rank(rank, port, out_dir):
     dist.destroy_process_group()
 
 
-def test_sharded_zero_adam_trains_the_pages_mlp():
+@pytest.mark.parametrize("bucket_elems", [0, 4_000])
+def test_sharded_zero_adam_trains_the_pages_mlp(bucket_elems):
+    """bucket_elems > 0: the grads exchanged bucket by bucket during the
+    backward (5 buckets of the 19,212-element vector, across parameter and
+    shard boundaries) -- the same result bit for bit."""
     import tempfile
 
     import oracle
     with tempfile.TemporaryDirectory() as out:
-        mp.start_processes(_rank, args=(_free_port(), out), nprocs=WORLD, join=True,
-                           start_method="spawn")
+        mp.start_processes(_rank, args=(_free_port(), out, bucket_elems), nprocs=WORLD,
+                           join=True, start_method="spawn")
         ranks = [np.load(os.path.join(out, "rank%d.npz" % r)) for r in range(WORLD)]
     for d in ranks:
         assert int(d["numel"]) == 19_210

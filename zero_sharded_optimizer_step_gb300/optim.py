@@ -153,11 +153,22 @@ class ShardedZeroAdam:
                   pass over two fp32 state sets.
     weight_decay  decoupled (AdamW) decay; 0 = Adam.
     group         the process group (None: the default group).
+    bucket_elems  > 0: exchange the gradients bucket by bucket during the
+                  backward, as ZeRO-2 does ("ZeRO 与 FSDP…", 从零实现 ZeRO 的
+                  Adam, closing note).  The flat vector is cut into buckets of
+                  this many elements, last bucket first (backward produces
+                  the last parameters' grads first); each parameter's grad is
+                  copied into its buckets as soon as it is accumulated and
+                  then freed, and a bucket, once complete, is exchanged and
+                  stepped at once (in bucket order on every rank).  step()
+                  flushes what is left and finishes.  One backward per step
+                  (no accumulation over several).  0 (default): step()
+                  takes the whole gradient at once.
     """
 
     def __init__(self, params: Iterable[torch.Tensor], lr: float = 1e-3, betas=(0.9, 0.999),
                  eps: float = 1e-8, weight_decay: float = 0.0, loss_scale: float = 0.0,
-                 growth_interval: int = 2000, group=None):
+                 growth_interval: int = 2000, group=None, bucket_elems: int = 0):
         import torch.distributed as dist
 
         from .sharded import LibraryRank, ShardedStep
@@ -189,8 +200,69 @@ class ShardedZeroAdam:
                 off += n
         # the own shard's master weights: its params widened (exact)
         self.local.set_master(self.local.own_params.float())
-        self.flat_grad = self.local.grad_buffer(flat.numel())
         self._step = ShardedStep(self.local, group)
+        self.bucket_elems = int(bucket_elems)
+        if self.bucket_elems > 0:
+            self._init_buckets(flat.numel())
+        else:
+            self.flat_grad = self.local.grad_buffer(flat.numel())
+
+    # ---- buckets exchanged during backward
+
+    def _init_buckets(self, P: int) -> None:
+        B = self.bucket_elems
+        # bucket b covers [lo_b, hi_b), b = 0 the last range of the vector
+        self._buckets = []
+        hi = P
+        while hi > 0:
+            lo = max(0, hi - B)
+            self._buckets.append((lo, hi))
+            hi = lo
+        self._hooks = [p.register_post_accumulate_grad_hook(self._grad_ready)
+                       for p in self.params]
+        self._by_param = {}
+        for p, (off, n) in zip(self.params, self._offsets):
+            self._by_param[id(p)] = (off, n)
+        self._reset_buckets()
+
+    def _reset_buckets(self) -> None:
+        self._bufs = {}
+        self._next = 0                  # the next bucket to exchange
+        self._begun = False
+        # elements still awaited per bucket (the padding needs none)
+        self._left = [max(0, min(hi, self.numel) - lo) for lo, hi in self._buckets]
+
+    def _buf(self, b: int) -> torch.Tensor:
+        if b not in self._bufs:
+            lo, hi = self._buckets[b]
+            self._bufs[b] = self.local.grad_buffer(hi - lo)
+        return self._bufs[b]
+
+    def _grad_ready(self, p: torch.Tensor) -> None:
+        off, n = self._by_param[id(p)]
+        g = p.grad.reshape(-1)
+        with torch.no_grad():
+            for b, (lo, hi) in enumerate(self._buckets):
+                a, e = max(lo, off), min(hi, off + n)
+                if a < e:
+                    self._buf(b)[a - lo:e - lo].copy_(g[a - off:e - off])
+                    self._left[b] -= e - a
+        p.grad = None               # this rank keeps only the buckets in flight
+        self._flush(False)
+
+    def _flush(self, all_of_them: bool) -> None:
+        """Exchange and step the complete buckets, in bucket order; with
+        all_of_them every remaining one (missing grads count as zero)."""
+        while self._next < len(self._buckets) and (all_of_them or self._left[self._next] == 0):
+            b = self._next
+            if not self._begun:
+                self._step.begin(self.scale)
+                self._begun = True
+            lo, hi = self._buckets[b]
+            self._step.bucket(lo, self._buf(b), self.lr, self.beta1, self.beta2, self.eps,
+                              self.t + 1)
+            del self._bufs[b]
+            self._next += 1
 
     def zero_grad(self) -> None:
         for p in self.params:
@@ -201,15 +273,20 @@ class ShardedZeroAdam:
         rank calls it).  Returns True when the step was skipped on every rank
         (loss scaling on and a non-finite grad on any rank); then t does not
         advance."""
-        with torch.no_grad():
-            for p, (off, n) in zip(self.params, self._offsets):
-                dst = self.flat_grad[off:off + n]
-                if p.grad is None:
-                    dst.zero_()
-                else:
-                    dst.copy_(p.grad.reshape(-1))
-        _, skipped = self._step.step(self.flat_grad, self.lr, self.beta1, self.beta2, self.eps,
-                                     self.t + 1, loss_scale=self.scale)
+        if self.bucket_elems > 0:
+            self._flush(True)
+            _, skipped = self._step.end(self.lr, self.beta1, self.beta2, self.eps, self.t + 1)
+            self._reset_buckets()
+        else:
+            with torch.no_grad():
+                for p, (off, n) in zip(self.params, self._offsets):
+                    dst = self.flat_grad[off:off + n]
+                    if p.grad is None:
+                        dst.zero_()
+                    else:
+                        dst.copy_(p.grad.reshape(-1))
+            _, skipped = self._step.step(self.flat_grad, self.lr, self.beta1, self.beta2,
+                                         self.eps, self.t + 1, loss_scale=self.scale)
         if not skipped:
             self.t += 1
         if self.scale > 0:
@@ -228,4 +305,6 @@ class ShardedZeroAdam:
         return 12 * self.local.shard
 
     def close(self) -> None:
+        for h in getattr(self, "_hooks", []):
+            h.remove()
         self.local.close()
