@@ -712,6 +712,37 @@ def run_e2e(run, plan, args, world_size):
     return e2e or bench_e2e(run, plan, args, world_size)
 
 
+def sharded_workload(args, world_size, rank=0):
+    """The workload of the sharded mode: the command line's, with N = the
+    number of processes (and this process's rank)."""
+    base = make_workload(args, args.workload)
+    # a flat workload must be the all-ranks one (the mode picks each
+    # process's rank); stage-3 workloads are described as one rank's view
+    if (base.stage < 3 and base.rank >= 0) or base.bucket or base.groups or base.unit_rows:
+        raise SystemExit("the sharded mode steps a flat vector or flat stage-3 units; "
+                         "--workload %s is not one (use --replicas)" % args.workload)
+    return base.replace(world=world_size, rank=rank, name=base.name + "_sharded")
+
+
+def sharded_config(args, world_size):
+    """The sharded mode's `config` (no measurement in it; the reference arm
+    prints the same dictionary under the same launch)."""
+    w = sharded_workload(args, world_size)
+    shards = ([w.shard] if w.stage < 3 else
+              [w.unit_shard(u) for u in range(len(w.units))])
+    return {
+        "workload": describe(w.replace(rank=-1)),
+        "params_updated_per_step": sum(shards) * w.world,
+        "l2": "inputs larger than L2 (129 MB); no flush between timed steps",
+        "parallelism": "%d processes, one data-parallel rank each (one-rank view; %s "
+                       "all-to-all of grad slices, MAX all-reduce of the flag word, "
+                       "all-gather of the cast shards%s)"
+                       % (world_size, args.dist_backend,
+                          ", per unit before forward and backward" if w.stage == 3 else ""),
+        "path": path_of(w, w.loss_scale > 0),
+    }
+
+
 def bench_sharded(args, rank, world_size, device_index):
     """One process per data-parallel rank (the default for --gpus N > 1):
     process r is rank r of N (N = the number of processes) in the one-rank
@@ -731,13 +762,7 @@ def bench_sharded(args, rank, world_size, device_index):
     import zero_sharded_optimizer_step_gb300 as z
     from zero_sharded_optimizer_step_gb300 import sharded as sh
 
-    base = make_workload(args, args.workload)
-    # a flat workload must be the all-ranks one (the mode picks each
-    # process's rank); stage-3 workloads are described as one rank's view
-    if (base.stage < 3 and base.rank >= 0) or base.bucket or base.groups or base.unit_rows:
-        raise SystemExit("the sharded mode steps a flat vector or flat stage-3 units; "
-                         "--workload %s is not one (use --replicas)" % args.workload)
-    w = base.replace(world=world_size, rank=rank, name=base.name + "_sharded")
+    w = sharded_workload(args, world_size, rank)
     torch.cuda.set_device(device_index)
     dev = torch.device("cuda:%d" % device_index)
     st = torch.cuda.current_stream(dev).cuda_stream
@@ -887,16 +912,7 @@ def bench_sharded(args, rank, world_size, device_index):
         "storage": {"grads": "f32 bf16 f16".split()[w.grad_dtype],
                     "params": "f32 bf16 f16".split()[w.param_dtype], "state": "f32"},
         "data": "synthetic (seeded counter-based normal draws; no dataset)",
-        "config": {
-            "workload": describe(w.replace(rank=-1)), "params_updated_per_step": updated,
-            "l2": "inputs larger than L2 (129 MB); no flush between timed steps",
-            "parallelism": "%d processes, one data-parallel rank each (one-rank view; %s "
-                           "all-to-all of grad slices, MAX all-reduce of the flag word, "
-                           "all-gather of the cast shards%s)"
-                           % (world_size, args.dist_backend,
-                              ", per unit before forward and backward" if w.stage == 3 else ""),
-            "path": path_of(w, scale > 0),
-        },
+        "config": sharded_config(args, world_size),
         "measured": {"local_kernels_ms": kms, "local_alg_bytes": kbytes,
                      "placed_bytes_per_rank_per_step": gathers,
                      # what the step spends outside the rank's own kernels
@@ -1741,13 +1757,15 @@ def bench_reference(args, rank, world_size):
                     "one thread each; %d timed steps; C oracle" % (n_s, w.name, T, len(times))}
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
             "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms / len(times), "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": ms / len(times), "higher_is_better": True,
+            "scaling": "strong" if world_size > 1 and not args.replicas else "weak",
             "vs_baseline": None, "dtype": "f32",
             "storage": {"grads": "f32 bf16 f16".split()[w.grad_dtype],
                         "params": "f32 bf16 f16".split()[w.param_dtype], "state": "f32"},
             "data": "synthetic (seeded counter-based normal draws; no dataset)",
             # the very dictionary the GPU arm prints for the same command line
-            "config": static_config(args, world_size),
+            "config": (sharded_config(args, world_size) if world_size > 1 and not args.replicas
+                       else static_config(args, world_size)),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

@@ -78,7 +78,19 @@ def test_reference_arm_under_torchrun_two_ranks():
                   "bench.py", "--impl", "reference", "--workload", "gpt2_small", "--gpus", "2",
                   "--steps", "1", "--warmup", "1"])
     assert len(lines) == 1
-    assert _check(lines[0])["n_gpus"] == 2
+    d = _check(lines[0])
+    assert d["n_gpus"] == 2 and d["scaling"] == "strong"
+    # the config the GPU arm's sharded mode prints for the same launch
+    sys.path.insert(0, ROOT)
+    import bench
+    old = sys.argv
+    sys.argv = ["bench.py", "--workload", "gpt2_small", "--gpus", "2"]
+    try:
+        args = bench.parse()
+    finally:
+        sys.argv = old
+    args.dist_backend = "gloo"
+    assert d["config"] == bench.sharded_config(args, 2)
 
 
 def _plan_bytes(w, shadow=False):
