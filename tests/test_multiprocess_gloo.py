@@ -180,6 +180,7 @@ def _all_ranks_reference(numel, world, inject_at):
     (2, 10_001, (2, 1, 9_999), 3_001),  # buckets, one across the shard boundary
     (4, 20_003, (2, 3, 17), 7_000),
     (4, 20_003, None, 20_004),          # one bucket: the whole vector
+    (3, 10_001, (2, 2, 5), 2_500),      # three ranks, one pad element, odd buckets
 ])
 def test_one_rank_views_with_real_collectives(tmp_path, world, numel, inject_at, bucket):
     port = _free_port()
@@ -355,6 +356,7 @@ def _stage3_reference(units, world, inject_at):
     (4, [3001, 17, 5000], (2, 3, 2, 11), False),     # rank 3's element in rank 0's shard of unit 2
     (2, [3001, 17, 5000, 64], (2, 1, 0, 1400), True),  # the next unit's gather in flight
     (4, [3001, 17, 5000], (2, 3, 2, 11), True),
+    (3, [3001, 17, 5000], (2, 2, 1, 16), True),     # three ranks: padding in every unit
 ])
 def test_stage3_ranks_with_real_collectives(tmp_path, world, units, inject_at, prefetch):
     port = _free_port()
