@@ -109,3 +109,93 @@ def test_sharded_zero_adam_trains_the_pages_mlp(bucket_elems):
                          it + 1)
     for r, d in enumerate(ranks):
         assert d["final"].tobytes() == full[:numel].tobytes(), r
+
+
+def _rank_fp16(rank, port, out_dir, bucket_elems):
+    """The MLP in fp16 with loss scaling: the loss is multiplied by the
+    optimizer's current scale; rank 1 plants a +inf in one grad element at
+    step 2 (a tensor hook, before accumulation), which must skip the step on
+    every rank and halve the scale."""
+    import copy
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import zero_sharded_optimizer_step_gb300 as z
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    world = 2
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    torch.manual_seed(0)
+    model = torch.nn.Sequential(torch.nn.Linear(64, 256), torch.nn.GELU(),
+                                torch.nn.Linear(256, 10)).to(dev).half()
+    init = _flat(model.parameters())
+    opt = z.ShardedZeroAdam(model.parameters(), lr=LR, betas=(0.9, 0.999), eps=1e-8,
+                            loss_scale=1024.0, bucket_elems=bucket_elems)
+    first = next(iter(model.parameters()))
+    plant = {"on": False}
+
+    def inf_hook(g):
+        if plant["on"]:
+            g = g.clone()
+            g.view(-1)[5] = float("inf")
+        return g
+    first.register_hook(inf_hook)
+    loss_fn = torch.nn.CrossEntropyLoss()
+    grads, skips, scales = [], [], []
+    for it in range(4):
+        gen = torch.Generator().manual_seed(200 + it)
+        x = torch.randn(world * PER_RANK, 64, generator=gen).to(dev).half()
+        y = torch.randint(0, 10, (world * PER_RANK,), generator=gen).to(dev)
+        sl = slice(rank * PER_RANK, (rank + 1) * PER_RANK)
+        plant["on"] = rank == 1 and it == 1
+        scales.append(opt.scale)
+        opt.zero_grad()
+        twin = copy.deepcopy(model)              # the same backward, for the record
+        twin_first = next(iter(twin.parameters()))
+        twin_first.register_hook(inf_hook)
+        (loss_fn(twin(x[sl]).float(), y[sl]) * opt.scale).backward()
+        grads.append(torch.cat([p.grad.reshape(-1) for p in twin.parameters()])
+                     .cpu().view(torch.int16).numpy().view(np.uint16))
+        (loss_fn(model(x[sl]).float(), y[sl]) * opt.scale).backward()
+        skips.append(opt.step())
+    torch.cuda.synchronize()
+    final = torch.cat([p.detach().reshape(-1) for p in model.parameters()]).cpu()
+    np.savez(os.path.join(out_dir, "rank%d.npz" % rank), init=init, grads=np.stack(grads),
+             skips=np.array(skips), scales=np.array(scales),
+             final=final.view(torch.int16).numpy().view(np.uint16), scale=opt.scale, t=opt.t)
+    opt.close()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("bucket_elems", [0, 5_000])
+def test_sharded_zero_adam_fp16_loss_scaled_skip(bucket_elems):
+    import tempfile
+
+    import oracle
+    with tempfile.TemporaryDirectory() as out:
+        mp.start_processes(_rank_fp16, args=(_free_port(), out, bucket_elems), nprocs=2,
+                           join=True, start_method="spawn")
+        ranks = [np.load(os.path.join(out, "rank%d.npz" % r)) for r in range(2)]
+    numel, world = 19_210, 2
+    P = oracle.shard_size(numel, world) * world
+    x = np.zeros(P, np.float32)
+    x[:numel] = ranks[0]["init"]
+    m, v = np.zeros(P, np.float32), np.zeros(P, np.float32)
+    full = np.zeros(P, np.uint16)
+    scale, good, t, skips = 1024.0, 0, 0, []
+    for it in range(4):
+        assert float(ranks[0]["scales"][it]) == scale
+        g = [np.ascontiguousarray(d["grads"][it]) for d in ranks]
+        sk, _ = oracle.zero_step(g, oracle.F16, numel, x, m, v, full, oracle.F16, LR, 0.9,
+                                 0.999, 1e-8, t + 1, loss_scale=scale)
+        skips.append(sk)
+        if not sk:
+            t += 1
+        scale, good = oracle.scale_update(scale, sk, good, 2000)
+    assert skips == [False, True, False, False]
+    for r, d in enumerate(ranks):
+        assert list(d["skips"]) == skips, r
+        assert float(d["scale"]) == scale == 512.0 and int(d["t"]) == t == 3
+        assert d["final"].tobytes() == full[:numel].tobytes(), r
