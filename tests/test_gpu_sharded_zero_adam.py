@@ -199,3 +199,71 @@ def test_sharded_zero_adam_fp16_loss_scaled_skip(bucket_elems):
         assert list(d["skips"]) == skips, r
         assert float(d["scale"]) == scale == 512.0 and int(d["t"]) == t == 3
         assert d["final"].tobytes() == full[:numel].tobytes(), r
+
+
+def _rank_resume(rank, port, out_dir, bucket_elems):
+    """Two steps, a checkpoint of every rank's shard, two more steps (A);
+    then a fresh model and optimizer loaded from the checkpoint run the same
+    two steps (B).  A and B must agree bit for bit."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import zero_sharded_optimizer_step_gb300 as z
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    world = 2
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    loss_fn = torch.nn.CrossEntropyLoss()
+
+    def build(seed):
+        torch.manual_seed(seed)
+        m = torch.nn.Sequential(torch.nn.Linear(64, 256), torch.nn.GELU(),
+                                torch.nn.Linear(256, 10)).to(dev).half()
+        o = z.ShardedZeroAdam(m.parameters(), lr=LR, betas=(0.9, 0.999), eps=1e-8,
+                              loss_scale=2048.0, bucket_elems=bucket_elems)
+        return m, o
+
+    def train(model, opt, its):
+        for it in its:
+            gen = torch.Generator().manual_seed(300 + it)
+            x = torch.randn(world * PER_RANK, 64, generator=gen).to(dev).half()
+            y = torch.randint(0, 10, (world * PER_RANK,), generator=gen).to(dev)
+            sl = slice(rank * PER_RANK, (rank + 1) * PER_RANK)
+            opt.zero_grad()
+            (loss_fn(model(x[sl]).float(), y[sl]) * opt.scale).backward()
+            opt.step()
+
+    model, opt = build(0)
+    train(model, opt, [0, 1])
+    sd = opt.state_dict()
+    sd = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in sd.items()}   # as if saved
+    train(model, opt, [2, 3])
+    a = torch.cat([p.detach().reshape(-1) for p in model.parameters()]).cpu()
+    ax = opt.state()[0].cpu()
+    model2, opt2 = build(1)                     # other initial weights: all must come back
+    opt2.load_state_dict(sd)
+    train(model2, opt2, [2, 3])
+    b = torch.cat([p.detach().reshape(-1) for p in model2.parameters()]).cpu()
+    bx = opt2.state()[0].cpu()
+    np.savez(os.path.join(out_dir, "rank%d.npz" % rank),
+             a=a.view(torch.int16).numpy(), b=b.view(torch.int16).numpy(),
+             ax=ax.numpy(), bx=bx.numpy(), ta=opt.t, tb=opt2.t, sa=opt.scale, sb=opt2.scale)
+    opt.close()
+    opt2.close()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("bucket_elems", [0, 6_000])
+def test_sharded_zero_adam_resumes_from_its_state(bucket_elems):
+    import tempfile
+    with tempfile.TemporaryDirectory() as out:
+        mp.start_processes(_rank_resume, args=(_free_port(), out, bucket_elems), nprocs=2,
+                           join=True, start_method="spawn")
+        ranks = [np.load(os.path.join(out, "rank%d.npz" % r)) for r in range(2)]
+    for d in ranks:
+        assert d["a"].tobytes() == d["b"].tobytes()
+        assert d["ax"].tobytes() == d["bx"].tobytes()
+        assert int(d["ta"]) == int(d["tb"]) == 4 and float(d["sa"]) == float(d["sb"])
+    assert ranks[0]["a"].tobytes() == ranks[1]["a"].tobytes()

@@ -299,6 +299,39 @@ class ShardedZeroAdam:
         """(master, m, v) of this rank's shard, current state set."""
         return self.local.state()
 
+    def state_dict(self) -> dict:
+        """This rank's part of a sharded checkpoint ("PaddlePaddle ZeRO优化":
+        each rank saves and restores its own shard of the optimizer state):
+        copies of its shard's fp32 master, m and v (the current set), the step
+        count and the loss-scale state.  The parameters are not included:
+        they are the master weights cast, restored from them."""
+        x, m, v = self.local.state()
+        return {"master": x.clone(), "m": m.clone(), "v": v.clone(), "t": self.t,
+                "scale": self.scale, "good_steps": self.good_steps,
+                "world": self.world, "rank": self.rank, "numel": self.numel}
+
+    def load_state_dict(self, sd: dict) -> None:
+        """Resume from this rank's state_dict() (the same model, world and
+        rank), between steps: the saved set becomes the bound set, the
+        current-set word and the flag word are cleared, and every rank's
+        parameters are cast from the masters and all-gathered -- a
+        collective, every rank calls it."""
+        from .sharded import gather_params
+        if (sd["world"], sd["rank"], sd["numel"]) != (self.world, self.rank, self.numel):
+            raise ValueError("the state was saved by rank %d of %d over %d parameters"
+                             % (sd["rank"], sd["world"], sd["numel"]))
+        loc = self.local
+        torch.cuda.synchronize(loc.device)
+        loc.master.copy_(sd["master"])
+        loc.m.copy_(sd["m"])
+        loc.v.copy_(sd["v"])
+        if loc.shadow is not None:
+            loc.cur.zero_()
+        loc.flag.zero_()
+        self.t, self.scale, self.good_steps = sd["t"], sd["scale"], sd["good_steps"]
+        loc.own_params.copy_(loc.master.to(loc.params.dtype))
+        gather_params(loc.params, loc.own_params, self._step.group)
+
     def state_bytes(self) -> int:
         """Bytes of fp32 optimizer state this rank holds: 12 * S, what the
         page's ZeroAdam.state_bytes() reports."""
