@@ -20,7 +20,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _rank(rank, world, port, numel, inject_at, shadow, out_dir, weight_decay=0.0, bucket=0):
+def _rank(rank, world, port, numel, inject_at, shadow, out_dir, weight_decay=0.0, bucket=0,
+          stage=2):
     import sys
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
@@ -33,7 +34,7 @@ def _rank(rank, world, port, numel, inject_at, shadow, out_dir, weight_decay=0.0
     dist.init_process_group("gloo", rank=rank, world_size=world)
     torch.cuda.set_device(0)
     local = LibraryRank(numel, world, rank, z.ZERO_F16, z.ZERO_F16, "cuda:0", shadow=shadow,
-                        weight_decay=weight_decay)
+                        weight_decay=weight_decay, stage=stage)
     S = local.shard
     lo = rank * S
     nv = max(0, min(S, numel - lo))
@@ -68,8 +69,11 @@ def _rank(rank, world, port, numel, inject_at, shadow, out_dir, weight_decay=0.0
     torch.cuda.synchronize()
     x, m, v = (a.cpu().numpy() for a in local.state())
     full = local.params.cpu().view(torch.int16).numpy().view(np.uint16)
+    extra = {}
+    if stage == 1:
+        extra["avg"] = local.grad_avg.cpu().view(torch.int16).numpy().view(np.uint16)
     np.savez(os.path.join(out_dir, "rank%d.npz" % rank), x=x, m=m, v=v, full=full,
-             skips=np.array(skips))
+             skips=np.array(skips), **extra)
     local.close()
     dist.destroy_process_group()
 
@@ -347,4 +351,31 @@ def test_sharded_step_with_decoupled_weight_decay(tmp_path):
         sl = slice(r * S, (r + 1) * S)
         assert d["x"].tobytes() == x[sl].tobytes() and d["m"].tobytes() == m[sl].tobytes()
         assert d["v"].tobytes() == v[sl].tobytes() and d["full"].tobytes() == full.tobytes()
+
+
+@pytest.mark.parametrize("bucket", [0, 50_001])
+def test_sharded_stage1_keeps_the_averaged_gradient(tmp_path, bucket):
+    """Stage 1 across two processes: besides the step (bit-identical to the
+    oracle), every rank ends with the whole averaged gradient of the last
+    step -- its own range written by the step, the rest all-gathered --
+    equal to the oracle's all-reduce mean (reading: before unscaling, in the
+    gradient type)."""
+    import oracle
+    import synth
+    world, numel = 2, 200_003
+    mp.start_processes(_rank, args=(world, _free_port(), numel, None, True, str(tmp_path), 0.0,
+                                    bucket, 1), nprocs=world, join=True, start_method="spawn")
+    x, m, v, full, skips = _all_ranks_reference(numel, world, None)
+    S = oracle.shard_size(numel, world)
+    P = S * world
+    scale = 2.0 ** 12                       # no skip: the scale in force at step 3
+    grads = [synth.fill_host(numel, synth.F16, synth.key(0, synth.KIND_GRAD, 3, k), 1e-3 * scale)
+             for k in range(world)]
+    want = oracle.cast(oracle.all_reduce_mean(grads, oracle.F16, numel), oracle.F16)
+    assert want.size == P and not want[numel:].any()     # the padding's mean is +0
+    for r in range(world):
+        d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
+        sl = slice(r * S, (r + 1) * S)
+        assert d["x"].tobytes() == x[sl].tobytes() and d["full"].tobytes() == full.tobytes()
+        assert d["avg"].tobytes() == want.tobytes(), r
 

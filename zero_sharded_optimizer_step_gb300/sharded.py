@@ -143,10 +143,10 @@ class LibraryRank:
     with an fp32 scratch."""
 
     def __init__(self, numel: int, world: int, rank: int, grad_dtype: int, param_dtype: int,
-                 device, shadow: bool = True, weight_decay: float = 0.0):
+                 device, shadow: bool = True, weight_decay: float = 0.0, stage: int = 2):
         self.device = torch.device(device)
         self.grad_dtype, self.param_dtype = grad_dtype, param_dtype
-        self.ctx = z.zero_init(numel, world, 2, grad_dtype, param_dtype, rank)
+        self.ctx = z.zero_init(numel, world, stage, grad_dtype, param_dtype, rank)
         self.shard = z.zero_ctx_shard_size(self.ctx, -1)
         S, P = self.shard, z.zero_ctx_param_elems(self.ctx)
         f32 = dict(dtype=torch.float32, device=self.device)
@@ -168,6 +168,14 @@ class LibraryRank:
             z.zero_bind_shadow(self.ctx, *self.shadow, self.cur)
         if weight_decay:
             z.zero_set_weight_decay(self.ctx, weight_decay)
+        # stage 1 keeps the whole averaged gradient on every rank (guanweilu.cn
+        # article 1460, Stage 1): the step writes the mean of this rank's
+        # range, ShardedStep all-gathers the rest
+        self.grad_avg = self.own_grad_avg = None
+        if stage == 1:
+            self.grad_avg = torch.zeros(P, dtype=_TORCH[grad_dtype], device=self.device)
+            self.own_grad_avg = self.grad_avg[rank * S:(rank + 1) * S]
+            z.zero_bind_allreduce_out(self.ctx, self.grad_avg)
         self._scaled = False
 
     def grad_buffer(self, n: int) -> torch.Tensor:
@@ -258,7 +266,14 @@ class ShardedStep:
             verdict = self.local.status()
         with _Range("zero: all-gather"):
             gather_params(self.local.params, self.local.own_params, self.group)
+            self._gather_mean_grads()
         return verdict
+
+    def _gather_mean_grads(self) -> None:
+        """Stage 1: every rank's part of the averaged gradient, all-gathered
+        into its whole (the all-reduce's result)."""
+        if getattr(self.local, "grad_avg", None) is not None:
+            gather_params(self.local.grad_avg, self.local.own_grad_avg, self.group)
 
     # ---- the same step bucket by bucket, as ZeRO-2 reduce-scatters during
     # backward ("ZeRO 与 FSDP…", 从零实现 ZeRO 的 Adam, closing note: real
@@ -305,6 +320,7 @@ class ShardedStep:
             verdict = self.local.status()
         with _Range("zero: all-gather"):
             gather_params(self.local.params, self.local.own_params, self.group)
+            self._gather_mean_grads()
         return verdict
 
 
