@@ -269,20 +269,35 @@ def _nccl_one_rank(index, port, out_dir):
     def backward(u, params):
         seen[u] = params.cpu().view(torch.int16).numpy().view(np.uint16).copy()
         return g3[u]
-    verdict3 = ShardedZero3Step(l3).step(backward, 1e-3, 0.9, 0.999, 1e-8, 1)
+    verdict3 = ShardedZero3Step(l3, prefetch=True).step(backward, 1e-3, 0.9, 0.999, 1e-8, 1)
     torch.cuda.synchronize()
     x3, m3, v3 = (a.cpu().numpy() for a in l3.state())
+    # the bucketed form (the split-size all-to-all) over NCCL: the same step
+    # as above from a fresh rank, in buckets of 30,001
+    lb = LibraryRank(numel, 1, 0, z.ZERO_BF16, z.ZERO_BF16, "cuda:0", shadow=True)
+    lb.set_master(torch.from_numpy(x0).cuda())
+    sb = ShardedStep(lb)
+    sb.begin(256.0)
+    for off in range(0, numel, 30_001):
+        sb.bucket(off, dg[off:off + 30_001], 1e-3, 0.9, 0.999, 1e-8, 1)
+    verdict_b = sb.end(1e-3, 0.9, 0.999, 1e-8, 1)
+    torch.cuda.synchronize()
+    xb = lb.state()[0].cpu().numpy()
+    pb = lb.params.cpu().view(torch.int16).numpy().view(np.uint16)
     np.savez(os.path.join(out_dir, "nccl.npz"), x=x, m=m, v=v, p=p, verdict=np.array(verdict),
+             xb=xb, pb=pb, verdict_b=np.array(verdict_b),
              x3=x3, p3=l3.params.cpu().view(torch.int16).numpy().view(np.uint16),
              verdict3=np.array(verdict3), **{"seen%d" % u: s for u, s in seen.items()})
     local.close()
     l3.close()
+    lb.close()
     dist.destroy_process_group()
 
 
 def test_sharded_steps_over_a_one_rank_nccl_group(tmp_path):
-    """ShardedStep and ShardedZero3Step over a real NCCL group of one rank:
-    the result is the oracle's (one rank: the step on the whole vector)."""
+    """ShardedStep (whole and bucketed) and ShardedZero3Step (prefetching)
+    over a real NCCL group of one rank: the result is the oracle's (one rank:
+    the step on the whole vector)."""
     mp.start_processes(_nccl_one_rank, args=(_free_port(), str(tmp_path)), nprocs=1, join=True,
                        start_method="spawn")
     import oracle
@@ -298,6 +313,9 @@ def test_sharded_steps_over_a_one_rank_nccl_group(tmp_path):
     assert tuple(d["verdict"]) == (False, False)
     assert d["x"].tobytes() == x.tobytes() and d["m"].tobytes() == m.tobytes()
     assert d["v"].tobytes() == v.tobytes() and d["p"].tobytes() == full.tobytes()
+    # the bucketed step: the same result
+    assert tuple(d["verdict_b"]) == (False, False)
+    assert d["xb"].tobytes() == x.tobytes() and d["pb"].tobytes() == full.tobytes()
     units = [30_001, 7, 50_000]
     xs, ps = [], []
     for u, nu in enumerate(units):
