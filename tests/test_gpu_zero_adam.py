@@ -122,3 +122,45 @@ def test_zero_adam_trains_the_pages_mlp_like_torch_adam():
     worst = max((a - b).abs().max().item() for a, b in zip(model.parameters(), ref.parameters()))
     assert worst < 1e-5, worst
     opt.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dt,scale", [(torch.bfloat16, 0.0), (torch.float16, 2.0 ** 10)])
+def test_zero_adam_resumes_from_its_state(dt, scale):
+    """Two steps, a checkpoint, two more steps; a fresh model and optimizer
+    (other initial weights) loaded from the checkpoint run the same two steps
+    to the same bits -- the flat parameters, the state, t and the scale."""
+    import zero_sharded_optimizer_step_gb300 as z
+    world = 4
+    code = z.dtype_code(dt)
+
+    def grads_of(opt, it):
+        for k in range(world):
+            g = synth.fill_host(opt.numel, code, synth.key(13, synth.KIND_GRAD, it, k),
+                                1e-3 * (scale or 1.0))
+            flat = torch.from_numpy(g.view(np.int16)).to("cuda:0").view(dt)
+            off = 0
+            for view in opt.rank_grads(k):
+                view.copy_(flat[off:off + view.numel()].view_as(view))
+                off += view.numel()
+
+    def run(opt, its):
+        for it in its:
+            opt.zero_grad()
+            grads_of(opt, it)
+            opt.step()
+
+    a = z.ZeroAdam(_mlp(dt), world, lr=1e-2, loss_scale=scale)
+    run(a, [1, 2])
+    sd = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in a.state_dict().items()}
+    run(a, [3, 4])
+    b = z.ZeroAdam([p * 0 + 0.5 for p in _mlp(dt)], world, lr=1e-2, loss_scale=scale)
+    b.load_state_dict(sd)
+    run(b, [3, 4])
+    torch.cuda.synchronize()
+    assert torch.equal(a.flat, b.flat)
+    for x, y in zip(a.state(), b.state()):
+        assert torch.equal(x, y)
+    assert a.t == b.t == 4 and a.scale == b.scale
+    a.close()
+    b.close()

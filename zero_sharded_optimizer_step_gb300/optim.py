@@ -122,6 +122,33 @@ class ZeroAdam:
             return self._shadow[:3]
         return self.master, self.m, self.v
 
+    def state_dict(self) -> dict:
+        """Copies of the current fp32 state set (master, m, v; every rank's
+        shard, padded length), the step count and the loss-scale state.  The
+        parameters are the masters cast, restored from them."""
+        x, m, v = self.state()
+        return {"master": x.clone(), "m": m.clone(), "v": v.clone(), "t": self.t,
+                "scale": self.scale, "good_steps": self.good_steps,
+                "world": self.world, "numel": self.numel}
+
+    def load_state_dict(self, sd: dict) -> None:
+        """Resume from state_dict() of the same model and world, between
+        steps (the resume protocol of zero.h at zero_bind: the saved set
+        bound, the current-set and flag words cleared)."""
+        if (sd["world"], sd["numel"]) != (self.world, self.numel):
+            raise ValueError("the state was saved for %d ranks over %d parameters"
+                             % (sd["world"], sd["numel"]))
+        torch.cuda.synchronize(self.flat.device)
+        self.master.copy_(sd["master"])
+        self.m.copy_(sd["m"])
+        self.v.copy_(sd["v"])
+        if self._shadow is not None:
+            self._shadow[3].zero_()
+        self.flag.zero_()
+        self.t, self.scale, self.good_steps = sd["t"], sd["scale"], sd["good_steps"]
+        with torch.no_grad():
+            self.flat.copy_(self.master.to(self.flat.dtype))
+
     def state_bytes(self) -> int:
         """Bytes of fp32 optimizer state (master, m, v) per rank: 12 * S, as
         the page's ZeroAdam.state_bytes() reports for its shard."""
