@@ -31,13 +31,17 @@ and, for the default run, `workloads`: the 7.5B one-rank view with its
 placement, GPT-2 small and the two ZeRO-3 unit paths, each timed after the
 headline in a runner of its own (with its own clocks and e2e).
 
-With --gpus N > 1 (torchrun), process r is data-parallel rank r of N in the
-one-rank view of the headline workload's flat vector, stepped through the
-library's sharded step (an all-to-all of the grad slices, the local fused
-pass, a MAX all-reduce of the flag word, the finalize and an all-gather of
-the cast shards; NCCL, or gloo through host memory with --dist-backend
-gloo): strong scaling.  --replicas instead runs one full replica of the
-workload per GPU with no data-path collective (weak scaling).
+With --gpus N > 1 (torchrun), the workload's W data-parallel ranks (16 for
+the headline; --dp-ranks W to choose) are spread over the N processes, W/N
+consecutive ranks each, every rank in the library's one-rank view, stepped
+through the library's sharded step (per rank an all-to-all of its grad
+slices, each rank's local fused pass, a MAX all-reduce of the flag word, the
+finalizes and an all-gather of the cast shards; NCCL, or gloo through host
+memory with --dist-backend gloo).  The workload is the same at every N:
+strong scaling, and with N = 1 (--sharded: a group of one, no collective) it
+is the headline's step done rank by rank.  --replicas instead runs one full
+replica of the workload per GPU with no data-path collective (weak
+scaling).
 `--impl reference` times the CPU oracle instead (rank 0 only).
 """
 from __future__ import annotations
@@ -125,6 +129,13 @@ def parse():
     ap.add_argument("--replicas", action="store_true",
                     help="with --gpus N > 1: N independent replicas of the workload (the "
                          "simulated ranks on every GPU) instead of one rank per process")
+    ap.add_argument("--dp-ranks", type=int, default=0,
+                    help="sharded mode: the data-parallel ranks W spread over the N processes, "
+                         "W/N each (default: the workload's own rank count for a flat vector, "
+                         "N for stage 3)")
+    ap.add_argument("--sharded", action="store_true",
+                    help="the sharded mode with one process too (a group of one: the W ranks' "
+                         "steps in one process, no collective)")
     ap.add_argument("--dist-backend", default="auto", choices=["auto", "nccl", "gloo"],
                     help="process group backend with --gpus N > 1 (auto: nccl on GPUs); a "
                          "gloo group moves the exchanged data through host memory")
@@ -713,15 +724,23 @@ def run_e2e(run, plan, args, world_size):
 
 
 def sharded_workload(args, world_size, rank=0):
-    """The workload of the sharded mode: the command line's, with N = the
-    number of processes (and this process's rank)."""
+    """The workload of the sharded mode: the command line's over W
+    data-parallel ranks (--dp-ranks; a flat vector keeps the workload's own
+    rank count, stage 3 takes one rank per process), each of the N processes
+    holding W / N consecutive ranks; `rank` is the process's index."""
     base = make_workload(args, args.workload)
     # a flat workload must be the all-ranks one (the mode picks each
-    # process's rank); stage-3 workloads are described as one rank's view
+    # process's ranks); stage-3 workloads are described as one rank's view
     if (base.stage < 3 and base.rank >= 0) or base.bucket or base.groups or base.unit_rows:
         raise SystemExit("the sharded mode steps a flat vector or flat stage-3 units; "
                          "--workload %s is not one (use --replicas)" % args.workload)
-    return base.replace(world=world_size, rank=rank, name=base.name + "_sharded")
+    W = args.dp_ranks or (base.world if base.stage < 3 else world_size)
+    if base.stage == 3 and W != world_size:
+        raise SystemExit("the sharded ZeRO-3 step holds one rank per process: --dp-ranks %d"
+                         % world_size)
+    if W % world_size:
+        raise SystemExit("--dp-ranks %d is not a multiple of the %d processes" % (W, world_size))
+    return base.replace(world=W, rank=rank, name=base.name + "_sharded")
 
 
 def sharded_config(args, world_size):
@@ -734,25 +753,30 @@ def sharded_config(args, world_size):
         "workload": describe(w.replace(rank=-1)),
         "params_updated_per_step": sum(shards) * w.world,
         "l2": "inputs larger than L2 (129 MB); no flush between timed steps",
-        "parallelism": "%d processes, one data-parallel rank each (one-rank view; %s "
-                       "all-to-all of grad slices, MAX all-reduce of the flag word, "
-                       "all-gather of the cast shards%s)"
-                       % (world_size, args.dist_backend,
-                          ", per unit before forward and backward" if w.stage == 3 else ""),
+        "parallelism": "%d data-parallel ranks over %d process(es), %d each (one-rank "
+                       "views; %s)"
+                       % (w.world, world_size, w.world // world_size,
+                          "no collective: a group of one" if world_size == 1 else
+                          "%s all-to-all of grad slices, MAX all-reduce of the flag word, "
+                          "all-gather of the cast shards%s"
+                          % (args.dist_backend,
+                             ", per unit before forward and backward" if w.stage == 3 else "")),
         "path": path_of(w, w.loss_scale > 0),
     }
 
 
 def bench_sharded(args, rank, world_size, device_index):
-    """One process per data-parallel rank (the default for --gpus N > 1):
-    process r is rank r of N (N = the number of processes) in the one-rank
-    view of the workload, stepped through the library's sharded step
-    (zero_sharded_optimizer_step_gb300.sharded).  A flat vector: an
-    all-to-all of the grad slices, the local fused pass, a MAX all-reduce of
-    the flag word, the finalize, an all-gather of the cast shards.  Stage 3:
-    per unit an all-gather before forward and backward and, after the
-    unit's backward, the exchange of its grads and its local pass; the flag
-    combined after the last unit.  The total work is the whole workload
+    """The sharded mode (the default for --gpus N > 1; --sharded with one
+    process): the workload's W data-parallel ranks over the N processes,
+    process p holding ranks p*k .. p*k + k - 1 (k = W/N) in the library's
+    one-rank view, stepped through the library's sharded step
+    (zero_sharded_optimizer_step_gb300.sharded).  A flat vector (RanksStep):
+    per rank an all-to-all of its grad slices, each rank's local fused pass,
+    a MAX all-reduce of the shared flag word, the finalizes, an all-gather of
+    the cast shards -- with N = 1 no collective.  Stage 3 (one rank per
+    process): per unit an all-gather before forward and backward and, after
+    the unit's backward, the exchange of its grads and its local pass; the
+    flag combined after the last unit.  The total work is the whole workload
     whatever N is: strong scaling.  `value` is the elements of all shards
     updated per second."""
     import torch
@@ -770,31 +794,44 @@ def bench_sharded(args, rank, world_size, device_index):
     sigma = W.grad_sigma(w, scale)
     bg = 4 if w.grad_dtype == 0 else 2
     bp = 4 if w.param_dtype == 0 else 2
+    k = w.world // world_size                  # ranks held by this process
     if w.stage < 3:
-        local = sh.LibraryRank(w.numel, w.world, rank, w.grad_dtype, w.param_dtype, dev,
+        # process `rank` holds ranks rank*k .. rank*k + k - 1, sharing one
+        # parameter buffer and one flag word
+        first = sh.LibraryRank(w.numel, w.world, rank * k, w.grad_dtype, w.param_dtype, dev,
                                shadow=scale > 0, weight_decay=w.weight_decay)
-        units = [(w.numel, local.shard, local.master)]
+        ranks = [first] + [sh.LibraryRank(w.numel, w.world, rank * k + c, w.grad_dtype,
+                                          w.param_dtype, dev, shadow=scale > 0,
+                                          weight_decay=w.weight_decay, params=first.params,
+                                          flag=first.flag) for c in range(1, k)]
+        local = first
+        units = [(w.numel, first.shard, None)]
     else:
         local = sh.LibraryRank3(w.units, w.world, rank, w.grad_dtype, w.param_dtype, dev,
                                 shadow=scale > 0, weight_decay=w.weight_decay)
+        ranks = [local]
         units = [(nu, S, local.master[o:o + S])
                  for nu, S, o in zip(w.units, local.shards, local.offsets)]
     grads, kbytes, updated = [], 0, 0
     for u, (nu, S, master) in enumerate(units):
-        nv = max(0, min(S, nu - rank * S))
-        if nv:
-            synth.fill_device(master.data_ptr(), nv, synth.F32,
-                              synth.key(w.seed, synth.KIND_MASTER, 0, 0, u), w.sigma_master, st,
-                              index0=rank * S)
-        g = local.grad_buffer(S * w.world)
-        synth.fill_device(g.data_ptr(), nu, w.grad_dtype,
-                          synth.key(w.seed, synth.KIND_GRAD, 1, rank, u), sigma, st)
-        grads.append(g)
-        kbytes += w.world * bg * nv + (24 + bp) * S
+        for c in range(k):
+            r = rank * k + c                   # the global rank
+            nv = max(0, min(S, nu - r * S))
+            m = master if master is not None else ranks[c].master
+            if nv:
+                synth.fill_device(m.data_ptr(), nv, synth.F32,
+                                  synth.key(w.seed, synth.KIND_MASTER, 0, 0, u), w.sigma_master,
+                                  st, index0=r * S)
+            g = local.grad_buffer(S * w.world)
+            synth.fill_device(g.data_ptr(), nu, w.grad_dtype,
+                              synth.key(w.seed, synth.KIND_GRAD, 1, r, u), sigma, st)
+            grads.append(g)
+            kbytes += w.world * bg * nv + (24 + bp) * S
         updated += S * w.world
     if w.stage < 3:
-        local.set_master(local.master.clone())
-        step = sh.ShardedStep(local)
+        for r in ranks:
+            r.set_master(r.master.clone())
+        step = sh.RanksStep(ranks)
     else:
         for u, (nu, S, master) in enumerate(units):
             local.set_master(u, master.clone())
@@ -805,7 +842,7 @@ def bench_sharded(args, rank, world_size, device_index):
     def one():
         nonlocal t, scale, good
         if w.stage < 3:
-            _, skipped = step.step(grads[0], w.lr, w.beta1, w.beta2, w.eps, t + 1,
+            _, skipped = step.step(grads, w.lr, w.beta1, w.beta2, w.eps, t + 1,
                                    loss_scale=scale)
         else:
             _, skipped = step.step(lambda u, params: grads[u], w.lr, w.beta1, w.beta2, w.eps,
@@ -817,18 +854,22 @@ def bench_sharded(args, rank, world_size, device_index):
         return skipped
 
     def local_only():
-        # the rank's own kernels alone, on its local grads read as slices
-        # (the same bytes and arithmetic as the exchanged ones)
-        def slices(u):
-            S = units[u][1]
-            return [grads[u][k * S:(k + 1) * S] for k in range(w.world)]
+        # the process's own kernels alone: each of its ranks' passes over
+        # its W slices (the exchanged ones, or the local grads in a group of
+        # one; stage 3: the local grads read as slices, the same bytes and
+        # arithmetic as the exchanged ones)
         hp = (w.lr, w.beta1, w.beta2, w.eps, t + 1)
         if w.stage < 3:
-            local.local_pass(slices(0), *hp, scale)
-        else:
-            local.begin(scale)
-            for u in reversed(range(len(units))):
-                local.unit_pass(u, slices(u), *hp, scale)
+            for jj, r in enumerate(ranks):
+                r.local_pass(step.slices(jj, grads), *hp, scale)
+            for r in ranks:
+                r.finish(*hp)
+            return
+        local.begin(scale)
+        for u in reversed(range(len(units))):
+            S = units[u][1]
+            local.unit_pass(u, [grads[u][q * S:(q + 1) * S] for q in range(w.world)], *hp,
+                            scale)
         local.finish(*hp)
 
     for _ in range(args.warmup):
@@ -874,8 +915,9 @@ def bench_sharded(args, rank, world_size, device_index):
         def one_e2e():
             nonlocal t, scale, good
             if w.stage < 3:
-                dgrads[0].copy_(host[0], non_blocking=True)
-                _, skipped = step.step(dgrads[0], w.lr, w.beta1, w.beta2, w.eps, t + 1,
+                for d, h in zip(dgrads, host):
+                    d.copy_(h, non_blocking=True)
+                _, skipped = step.step(dgrads, w.lr, w.beta1, w.beta2, w.eps, t + 1,
                                        loss_scale=scale)
             else:
                 def backward(u, params):
@@ -904,7 +946,8 @@ def bench_sharded(args, rank, world_size, device_index):
                "path": "copies on each rank's compute stream around the sharded step"}
     peak, peak_kind = peaks()
     achieved = kbytes / (kms * 1e-3) / 1e9
-    gathers = (2 * bp * sum(u[1] for u in units) * (w.world - 1) * (1 if w.stage < 3 else 2))
+    gathers = (2 * bp * sum(u[1] for u in units) * k * (world_size - 1)
+               * (1 if w.stage < 3 else 2))
     res = {
         "metric": METRIC, "value": updated / (ms * 1e-3), "unit": "params/s",
         "n_gpus": world_size, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -924,14 +967,16 @@ def bench_sharded(args, rank, world_size, device_index):
                                "max over ranks; then the rank's own kernels alone, K times"},
         "roofline": {"kernel": "fused_step_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "alg_bytes_per_launch": kbytes / len(units),
+                     "frac": achieved / peak,
+                     "alg_bytes_per_launch": kbytes / (len(units) * k),
                      "traffic": None},
-        "gpu_launches": args.steps * (2 if w.stage < 3 else len(units) + 1),
+        "gpu_launches": args.steps * (2 * k if w.stage < 3 else len(units) + 1),
         "clocks": clock_info,
     }
     if e2e is not None:
         res["e2e"] = e2e
-    local.close()
+    for r in ranks:
+        r.close()
     return res
 
 
@@ -1764,7 +1809,7 @@ def bench_reference(args, rank, world_size):
                         "params": "f32 bf16 f16".split()[w.param_dtype], "state": "f32"},
             "data": "synthetic (seeded counter-based normal draws; no dataset)",
             # the very dictionary the GPU arm prints for the same command line
-            "config": (sharded_config(args, world_size) if world_size > 1 and not args.replicas
+            "config": (sharded_config(args, world_size) if sharded_mode(args, world_size)
                        else static_config(args, world_size)),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
@@ -1772,6 +1817,12 @@ def bench_reference(args, rank, world_size):
 
 
 # -------------------------------------------------------------- distributed
+
+def sharded_mode(args, world_size):
+    """Whether this command line runs the sharded mode (the default with
+    several processes, --sharded with one)."""
+    return (world_size > 1 or args.sharded) and not args.replicas
+
 
 def barrier(world_size):
     if world_size > 1:
@@ -1807,6 +1858,13 @@ def main():
             device = local % torch.cuda.device_count()
             torch.cuda.set_device(device)
         dist.init_process_group(backend)
+    elif args.sharded and args.impl == "ours":
+        # the sharded mode in a group of one
+        import torch
+        import torch.distributed as dist
+        if args.dist_backend == "auto":
+            args.dist_backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(args.dist_backend, store=dist.HashStore(), rank=0, world_size=1)
     if args.impl == "reference":
         res = bench_reference(args, rank, world_size)
     else:
@@ -1817,15 +1875,16 @@ def main():
             res = bench_prefetch(args, rank, world_size, device)
         elif args.workload == "zero2_overlap":
             res = bench_zero2_overlap(args, rank, world_size, device)
-        elif world_size > 1 and not args.replicas:
+        elif sharded_mode(args, world_size):
             res = bench_sharded(args, rank, world_size, device)
         else:
             res = bench_ours(args, rank, world_size, device)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
-    if world_size > 1:
+    if "torch.distributed" in sys.modules:
         import torch.distributed as dist
-        dist.destroy_process_group()
+        if dist.is_initialized():
+            dist.destroy_process_group()
 
 
 if __name__ == "__main__":

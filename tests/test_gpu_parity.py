@@ -209,6 +209,86 @@ def test_misaligned_buffers_take_the_exact_path():
     assert to_np(params).tobytes() == ref.full.tobytes()
 
 
+@pytest.mark.parametrize("gdt,offs,poff,mode", [
+    # every grad 8 bytes past a 16-byte boundary (a rank's slices of flat
+    # vectors at a shard length of 4 mod 8): the grads read in 8-byte halves
+    (W.F16, [4, 4, 4, 4, 4], 0, "plain"),
+    (W.F16, [4, 4, 4, 4, 4], 4, "shadow"),      # params there too; two state sets, a skip
+    (W.BF16, [4, 4, 4, 4, 4], 1, "scratch"),    # the two passes, a skip
+    (W.BF16, [4, 4, 4, 4, 4], 0, "avg"),        # stage 1: the mean written too
+    (W.BF16, [0, 4, 0, 4, 8], 0, "plain"),      # mixed offsets
+    (W.F16, [0, 4, 0, 12, 8], 4, "shadow"),
+    (W.F32, [2, 2, 2, 2, 2], 0, "plain"),       # fp32 grads 8 bytes off
+    (W.F16, [2, 2, 2, 2, 2], 0, "plain"),       # 4 bytes off: the per-element path
+    (W.F16, [0, 0, 0, 0, 0], 4, "shadow"),      # aligned grads, params 8 bytes off
+])
+def test_grad_offsets_pick_a_load_width(gdt, offs, poff, mode):
+    """Rank grads that start off a 16-byte boundary -- a rank's slices of
+    flat vectors whose shard length is not a multiple of 8 elements -- read
+    the way their offsets allow (8-byte halves, or element by element);
+    every result bit-identical to the oracle's, skipped step included."""
+    import zero_sharded_optimizer_step_gb300 as z
+    numel, world = 100_003, len(offs)
+    pdt = W.F16 if gdt == W.F16 else W.BF16
+    scaled = mode in ("shadow", "scratch")
+    w = W.Workload("offs", numel, world, 1 if mode == "avg" else 2, gdt, pdt, steps=3,
+                   loss_scale=2.0 ** 12 if scaled else 0.0, inject=(2, 1) if scaled else None)
+    ref = refs.OracleRun(w)
+    P = w.shard * world
+    dev = torch.device("cuda:0")
+    tdt = {W.F32: torch.float32, W.BF16: torch.bfloat16, W.F16: torch.float16}
+
+    def buf(n, dt, off):
+        return torch.zeros(n + 16, dtype=dt, device=dev)[off:off + n]
+
+    def dev_copy(a, dt):
+        h = torch.from_numpy(a if a.dtype == np.float32 else a.view(np.int16))
+        return h.view(tdt[dt]).to(dev)
+
+    f32 = lambda: torch.zeros(P, dtype=torch.float32, device=dev)  # noqa: E731
+    master, m, v = f32(), f32(), f32()
+    master.copy_(torch.from_numpy(refs.host_master(w)).to(dev))
+    params = buf(P, tdt[pdt], poff)
+    params.copy_(dev_copy(ref.full, pdt))
+    flag = torch.zeros(1, dtype=torch.int64, device=dev)
+    scratch = f32() if mode == "scratch" else None
+    ctx = z.zero_init(numel, world, w.stage, gdt, pdt, -1)
+    z.zero_bind(ctx, master, m, v, params, scratch, flag)
+    shadow = None
+    if mode == "shadow":
+        shadow = (f32(), f32(), f32())
+        cur_word = torch.zeros(1, dtype=torch.int64, device=dev)   # held while ctx lives
+        z.zero_bind_shadow(ctx, *shadow, cur_word)
+    avg = None
+    if mode == "avg":
+        avg = buf(P, tdt[gdt], 4)
+        z.zero_bind_allreduce_out(ctx, avg)
+    scale, good, t = w.loss_scale, 0, 0
+    for it in (1, 2, 3):
+        hg = refs.host_grads(w, it, scale)
+        gd = [buf(numel, tdt[gdt], offs[k]) for k in range(world)]
+        for k in range(world):
+            gd[k].copy_(dev_copy(hg[k], gdt))
+        z.zero_step(ctx, gd, w.lr, w.beta1, w.beta2, w.eps, t + 1, scale)
+        _, skipped = z.zero_step_status(ctx)
+        assert skipped == ref.step(it), it
+        if not skipped:
+            t += 1
+        if scale > 0:
+            scale, good = z.zero_scale_update(scale, skipped, good, w.growth_interval)
+    torch.cuda.synchronize()
+    assert ref.skips == [False, scaled, False]
+    cur = (master, m, v) if shadow is None or z.zero_current_state(ctx) == 0 else shadow
+    x, mm, vv = ref.state[0]
+    for got, want, what in ((cur[0], x, "master"), (cur[1], mm, "m"), (cur[2], vv, "v")):
+        assert_bit_identical(to_np(got), want, oracle.F32, what)
+    assert_bit_identical(to_np(params), ref.full, pdt, "params")
+    if avg is not None:
+        want = oracle.cast(oracle.all_reduce_mean(hg, gdt, numel), gdt)
+        assert to_np(avg).tobytes() == want.tobytes()
+    ctx.close()
+
+
 @pytest.mark.parametrize("rank", [-1, 2])
 def test_stage1_allreduce_output(rank):
     """Stage 1 keeps the full averaged grads: RS + AG == AR, bit-exact."""
@@ -591,7 +671,8 @@ def test_lean_gather_placement(S, world, dtype, src_off, dst_off):
     full = torch.zeros(S * world + 16, dtype=tdt, device=dev)[dst_off:dst_off + S * world]
     st = torch.zeros(S, device=dev)
     flag = torch.zeros(1, dtype=torch.int64, device=dev)
-    z.zero_bind(ctx, st, st, st, torch.zeros(S, dtype=tdt, device=dev), None, flag)
+    params = torch.zeros(S, dtype=tdt, device=dev)      # bound buffers live as long as ctx
+    z.zero_bind(ctx, st, st, st, params, None, flag)
     z.zero3_begin_step(ctx)
     for _ in range(2):
         z.zero3_gather_unit(ctx, 0, shards, full)
@@ -614,8 +695,9 @@ def test_lean_gather_wait_that_runs_out_is_reported():
     ctx = z.zero_init(S * world, world, 3, dtype, dtype, 0, [S * world])
     z.zero_set_gather_mode(ctx, z.ZERO_GATHER_LEAN)
     st = torch.zeros(S, device=dev)
-    z.zero_bind(ctx, st, st, st, torch.zeros(S, dtype=torch.bfloat16, device=dev), None,
-                torch.zeros(1, dtype=torch.int64, device=dev))
+    params = torch.zeros(S, dtype=torch.bfloat16, device=dev)   # bound buffers live as
+    flag = torch.zeros(1, dtype=torch.int64, device=dev)        # long as ctx
+    z.zero_bind(ctx, st, st, st, params, None, flag)
     z.zero3_begin_step(ctx)
     full = torch.full((S * world,), 7.0, dtype=torch.bfloat16, device=dev)
     sentinel = to_np(full).tobytes()

@@ -104,15 +104,107 @@ def test_sharded_step_through_the_library(tmp_path, numel, inject_at, shadow, bu
         assert d["full"].tobytes() == full.tobytes()
 
 
+def _ranks(proc, nprocs, port, numel, world, inject_at, shadow, out_dir):
+    """Process `proc` of `nprocs` holding world // nprocs consecutive ranks
+    in the library's one-rank view (RanksStep), sharing one parameter
+    buffer and one flag word."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import oracle
+    import synth
+    import zero_sharded_optimizer_step_gb300 as z
+    from zero_sharded_optimizer_step_gb300.sharded import LibraryRank, RanksStep
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=proc, world_size=nprocs)
+    torch.cuda.set_device(0)
+    k = world // nprocs
+    ranks = []
+    for c in range(k):
+        share = dict(params=ranks[0].params, flag=ranks[0].flag) if ranks else {}
+        ranks.append(LibraryRank(numel, world, proc * k + c, z.ZERO_F16, z.ZERO_F16, "cuda:0",
+                                 shadow=shadow, **share))
+    S = ranks[0].shard
+    P = S * world
+    for c, r in enumerate(ranks):
+        lo = (proc * k + c) * S
+        nv = max(0, min(S, numel - lo))
+        x0 = np.zeros(S, np.float32)
+        x0[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER), 0.01,
+                                  index0=lo)
+        r.set_master(torch.from_numpy(x0).cuda())
+    step = RanksStep(ranks)
+    scale, good, t, skips = 2.0 ** 12, 0, 0, []
+    for it in (1, 2, 3):
+        dgs = []
+        for c in range(k):
+            g = np.zeros(P, np.uint16)
+            g[:numel] = synth.fill_host(numel, synth.F16,
+                                        synth.key(0, synth.KIND_GRAD, it, proc * k + c),
+                                        1e-3 * scale)
+            if inject_at and it == inject_at[0] and proc * k + c == inject_at[1]:
+                g[inject_at[2]] = 0x7C00
+            dgs.append(torch.from_numpy(g.view(np.int16)).cuda().view(torch.float16))
+        _, skipped = step.step(dgs, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale)
+        skips.append(skipped)
+        if not skipped:
+            t += 1
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    torch.cuda.synchronize()
+    full = ranks[0].params.cpu().view(torch.int16).numpy().view(np.uint16)
+    for c, r in enumerate(ranks):
+        x, m, v = (a.cpu().numpy() for a in r.state())
+        np.savez(os.path.join(out_dir, "rank%d.npz" % (proc * k + c)), x=x, m=m, v=v, full=full,
+                 skips=np.array(skips))
+        r.close()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("nprocs,world,numel,inject_at,shadow", [
+    (1, 4, 300_007, (2, 3, 17), True),        # four ranks in one process, no collective
+    (1, 4, 300_013, (2, 2, 75_011), True),    # S = 4 mod 8: odd ranks' slices take the head
+    (2, 4, 300_013, None, False),
+    (1, 4, 300_007, (2, 1, 299_999), False),  # the fp32 scratch
+    (2, 4, 300_007, (2, 3, 17), True),        # two ranks in each of two processes
+    (2, 4, 300_001, None, True),
+    (2, 6, 300_001, (2, 5, 1), False),
+])
+def test_ranks_per_process_through_the_library(tmp_path, nprocs, world, numel, inject_at,
+                                               shadow):
+    """W ranks over N processes (RanksStep): with N = 1 the all-ranks step of
+    one GPU done rank by rank, with N = 2 the exchange of each rank's slices
+    between processes; the state of every rank, the full parameter buffer
+    and the skips bit-identical to the oracle's all-ranks step."""
+    port = _free_port()
+    mp.start_processes(_ranks, args=(nprocs, port, numel, world, inject_at, shadow,
+                                     str(tmp_path)), nprocs=nprocs, join=True,
+                       start_method="spawn")
+    import oracle
+    x, m, v, full, skips = _all_ranks_reference(numel, world, inject_at)
+    assert skips == [bool(inject_at) and it == inject_at[0] for it in (1, 2, 3)]
+    S = oracle.shard_size(numel, world)
+    for r in range(world):
+        d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
+        assert list(d["skips"]) == skips, r
+        sl = slice(r * S, (r + 1) * S)
+        assert d["x"].tobytes() == x[sl].tobytes(), r
+        assert d["m"].tobytes() == m[sl].tobytes(), r
+        assert d["v"].tobytes() == v[sl].tobytes(), r
+        assert d["full"].tobytes() == full.tobytes(), r
+
+
 @pytest.mark.parametrize("extra,updated", [
-    (["--numel", "4000037"], 2 * (-(-4000037 // 2))),
+    (["--numel", "4000037"], 16 * (-(-4000037 // 16))),
+    (["--numel", "4000037", "--dp-ranks", "2"], 2 * (-(-4000037 // 2))),
     (["--workload", "zero3_gpt2_small"], None),
 ])
 def test_bench_sharded_mode_runs(extra, updated):
-    """bench.py's default mode for --gpus 2 (one data-parallel rank per
-    process) under torchrun: two gloo ranks on this GPU, a small flat vector
-    and the 14 ZeRO-3 units of GPT-2 small; the line reports strong scaling
-    and every step applied."""
+    """bench.py's default mode for --gpus 2 under torchrun: two gloo
+    processes on this GPU, a small flat vector over the workload's 16 ranks
+    (8 per process) or over 2 (one each), and the 14 ZeRO-3 units of GPT-2
+    small (one rank per process); the line reports strong scaling and every
+    step applied."""
     import json
     import subprocess
     import sys

@@ -33,7 +33,7 @@ class OracleRank:
     grads and params held as 16-bit patterns in CPU tensors, the step-tagged
     flag word, the oracle's one-rank step once the verdict is combined."""
 
-    def __init__(self, numel, world, rank):
+    def __init__(self, numel, world, rank, params=None, flag=None):
         import oracle
         import synth
         self.oracle = oracle
@@ -45,10 +45,11 @@ class OracleRank:
         self.x[:self.nv] = synth.fill_host(self.nv, synth.F32, synth.key(0, synth.KIND_MASTER),
                                            0.01, index0=lo)
         self.m, self.v = np.zeros(S, np.float32), np.zeros(S, np.float32)
-        self.params = torch.zeros(S * world, dtype=torch.int16)
+        # the ranks of one process may share the parameter buffer and the flag
+        self.params = torch.zeros(S * world, dtype=torch.int16) if params is None else params
         self.own_params = self.params[lo:lo + S]
         self.own_params.copy_(torch.from_numpy(oracle.cast(self.x, oracle.F16).view(np.int16)))
-        self.flag = torch.zeros(1, dtype=torch.int64)
+        self.flag = torch.zeros(1, dtype=torch.int64) if flag is None else flag
         self.step_id = 0
 
     def grad_buffer(self, n):
@@ -199,6 +200,70 @@ def test_one_rank_views_with_real_collectives(tmp_path, world, numel, inject_at,
         assert d["m"].tobytes() == m[sl].tobytes()
         assert d["v"].tobytes() == v[sl].tobytes()
         assert d["full"].tobytes() == full.tobytes()
+
+
+def _ranks_main(proc, nprocs, port, numel, world, inject_at, out_dir):
+    """Process `proc` of `nprocs` holding world // nprocs consecutive ranks
+    (RanksStep), each with the oracle's arithmetic, sharing one parameter
+    buffer and one flag word."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import oracle
+    import synth
+    from zero_sharded_optimizer_step_gb300.sharded import RanksStep
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=proc, world_size=nprocs)
+    k = world // nprocs
+    S = oracle.shard_size(numel, world)
+    P = S * world
+    params, flag = torch.zeros(P, dtype=torch.int16), torch.zeros(1, dtype=torch.int64)
+    ranks = [OracleRank(numel, world, proc * k + c, params, flag) for c in range(k)]
+    step = RanksStep(ranks)
+    scale, good, t, skips = 2.0 ** 12, 0, 0, []
+    for it in (1, 2, 3):
+        gts = []
+        for c in range(k):
+            r = proc * k + c
+            g = np.zeros(P, np.uint16)
+            g[:numel] = synth.fill_host(numel, synth.F16, synth.key(0, synth.KIND_GRAD, it, r),
+                                        1e-3 * scale)
+            if inject_at and it == inject_at[0] and r == inject_at[1]:
+                g[inject_at[2]] = 0x7C00
+            gts.append(torch.from_numpy(g.view(np.int16)))
+        _, skipped = step.step(gts, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale)
+        skips.append(skipped)
+        if not skipped:
+            t += 1
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    for c, r in enumerate(ranks):
+        np.savez(os.path.join(out_dir, "rank%d.npz" % r.rank), x=r.x, m=r.m, v=r.v,
+                 full=params.numpy().view(np.uint16), skips=np.array(skips))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("nprocs,world,numel,inject_at", [
+    (1, 4, 20_003, (2, 3, 17)),          # all four ranks in one process: no collective
+    (2, 4, 20_003, (2, 3, 17)),          # two ranks per process
+    (2, 4, 10_001, (2, 1, 9_999)),       # one pad element, the planted value in rank 3's shard
+    (2, 6, 10_001, None),
+    (3, 6, 10_001, (2, 4, 5)),           # three processes of two ranks
+])
+def test_ranks_per_process_with_real_collectives(tmp_path, nprocs, world, numel, inject_at):
+    port = _free_port()
+    mp.start_processes(_ranks_main, args=(nprocs, port, numel, world, inject_at, str(tmp_path)),
+                       nprocs=nprocs, join=True, start_method="spawn")
+    import oracle
+    x, m, v, full, skips = _all_ranks_reference(numel, world, inject_at)
+    S = oracle.shard_size(numel, world)
+    assert skips == [bool(inject_at) and it == inject_at[0] for it in (1, 2, 3)]
+    for r in range(world):
+        d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
+        assert list(d["skips"]) == skips, r
+        sl = slice(r * S, (r + 1) * S)
+        assert d["x"].tobytes() == x[sl].tobytes(), r
+        assert d["m"].tobytes() == m[sl].tobytes(), r
+        assert d["v"].tobytes() == v[sl].tobytes(), r
+        assert d["full"].tobytes() == full.tobytes(), r
 
 
 # ------------------------------------------------------------------ stage 3

@@ -1,12 +1,14 @@
-"""The step kernels' choice between the 16-byte vector path and the
-per-element path, checked on the CPU: zgb::step_vector_path_ok, the one
-predicate every launch (zero_step_noalloc included) takes its vec_ok from,
+"""The step kernels' choice between the vector path and the per-element
+path, checked on the CPU: zgb::step_vector_path_ok, the one predicate every
+launch (zero_step_noalloc included) takes its vec_ok from, and
+zgb::step_grad_align, the width the vector path reads the rank grads with,
 compiled from the library's internal header into a small host program.
 
-A buffer the vector path would touch at an address off a 16-byte boundary
-must send the launch down the per-element path; that is what keeps a
-misaligned second state set, scratch or grad buffer from a misaligned
-16-byte access on the GPU."""
+An fp32 buffer the vector path would touch at an address off a 16-byte
+boundary, or a grad buffer off an 8-byte one, must send the launch down the
+per-element path; that is what keeps a misaligned second state set,
+scratch or grad buffer from a misaligned vector access on the GPU.  Grads
+on an 8-byte boundary are read 8 bytes per load."""
 import os
 import subprocess
 
@@ -48,6 +50,18 @@ int main()
     a = base(4); a.g = f(900);              EXPECT(zgb::step_vector_path_ok(a), false);
     a = base(4); a.g = f(896);              EXPECT(zgb::step_vector_path_ok(a), true);
     a = base(4); a.grads[3] = f(292);       EXPECT(zgb::step_vector_path_ok(a), false);
+    // grads on an 8-byte boundary (a rank's slice of a flat vector whose
+    // shard length is 4 mod 8 elements) keep the vector path, read in halves
+    a = base(4);                            EXPECT(zgb::step_grad_align(a) == 16, true);
+    a = base(4); a.grads[1] = f(232);       EXPECT(zgb::step_vector_path_ok(a), true);
+                                            EXPECT(zgb::step_grad_align(a) == 8, true);
+    a = base(4); a.grads[1] = f(228);       EXPECT(zgb::step_grad_align(a) == 0, true);
+    a = base(4); a.grads[0] = f(194);       EXPECT(zgb::step_vector_path_ok(a), false);
+    // mixed 16- and 8-byte offsets: the common alignment, 8
+    a = base(4); a.grads[2] = f(200);       EXPECT(zgb::step_grad_align(a) == 8, true);
+                                            EXPECT(zgb::step_vector_path_ok(a), true);
+    // the state stays on 16 bytes: 8 is not enough there
+    a = base(4); a.master = f(8);           EXPECT(zgb::step_vector_path_ok(a), false);
     a = base(4); a.grads[2] = nullptr;      EXPECT(zgb::step_vector_path_ok(a), true);
     // a pointer past `world` is never read by the kernels
     a = base(4); a.grads[4] = f(2);         EXPECT(zgb::step_vector_path_ok(a), true);
@@ -69,7 +83,9 @@ int main()
     a = base(256);
     for (int k = 0; k < 256; ++k) a.grads[k] = f(0);
     EXPECT(zgb::step_vector_path_ok(a), true);
-    a.grads[255] = f(8);                    EXPECT(zgb::step_vector_path_ok(a), false);
+    a.grads[255] = f(8);                    EXPECT(zgb::step_vector_path_ok(a), true);
+                                            EXPECT(zgb::step_grad_align(a) == 8, true);
+    a.grads[255] = f(12);                   EXPECT(zgb::step_vector_path_ok(a), false);
     if (fails) return 1;
     printf("ok\n");
     return 0;

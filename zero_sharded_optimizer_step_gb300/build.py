@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzero.so")
 SOURCES = ["zero_abi.cu", "zero_step_kernels.cu", "zero_gather.cu", "zero_advance.cu"]
-HEADERS = ["zero_internal.h", os.path.join("..", "..", "include", "zero.h")]
+HEADERS = ["zero_internal.h", "zero_row_copy.cuh", os.path.join("..", "..", "include", "zero.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -299,6 +299,7 @@ StepArgs make_args(const zero_ctx *c, const Range &r, const void *const *grads)
     a.slot = c->hyper_slot;
     if (grads)
         for (int32_t k = 0; k < c->world; ++k) a.grads[k] = grads[k];
+    a.grad_align = zgb::step_grad_align(a);
     a.vec_ok = zgb::step_vector_path_ok(a) ? 1 : 0;
     return a;
 }

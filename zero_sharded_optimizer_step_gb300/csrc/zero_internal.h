@@ -57,7 +57,8 @@ static_assert(sizeof(AdvanceState) == 32, "AdvanceState is 32 bytes");
 struct StepArgs {
     const void *grads[kMaxRanks];  // rank k's grads for this range
     int32_t world;
-    int32_t vec_ok;                // grads, state, scratch 16-byte aligned
+    int32_t vec_ok;                // the vector path may run (step_vector_path_ok)
+    int32_t grad_align;            // 16 or 8: how the vector path loads the rank grads
     int32_t param_align;           // byte alignment of `params` (2..16)
     int32_t avg_align;             // byte alignment of `grad_avg`
     int64_t n;                     // elements in the range
@@ -78,20 +79,31 @@ struct StepArgs {
     AdamScalars ad;
 };
 
-// Whether the step kernels may take their 16-byte vector path over a range:
-// every buffer they read or write with 16-byte accesses -- the rank grads,
-// master/m/v, the fp32 scratch and, with a second state set bound, that set
-// too -- starts on a 16-byte boundary (null pointers are not accessed).  The
-// params and the stage-1 output are stored at their own alignment
-// (param_align, avg_align) and take no part.  Computed from the finished
-// arguments, so that no launch can leave one of the buffers out.
+// The common byte alignment of the rank grads, as the vector path reads
+// them: 16 (one 16-byte load per 16 bytes), 8 (two 8-byte loads: a rank's
+// slices of flat vectors whose shard length is 4 mod 8 elements start on an
+// 8-byte boundary) or 0 (the per-element path).
+inline int32_t step_grad_align(const StepArgs &a)
+{
+    uintptr_t bits = 0;
+    for (int32_t k = 0; k < a.world && k < kMaxRanks; ++k) bits |= (uintptr_t)a.grads[k];
+    return (bits & 15) == 0 ? 16 : (bits & 7) == 0 ? 8 : 0;
+}
+
+// Whether the step kernels may take their vector path over a range: every
+// fp32 buffer they read or write with 16-byte accesses -- master/m/v, the
+// fp32 scratch and, with a second state set bound, that set too -- starts
+// on a 16-byte boundary (null pointers are not accessed), and the rank
+// grads on an 8-byte one (step_grad_align).  The params and the stage-1
+// output are stored at their own alignment (param_align, avg_align) and
+// take no part.  Computed from the finished arguments, so that no launch
+// can leave one of the buffers out.
 inline bool step_vector_path_ok(const StepArgs &a)
 {
     auto al16 = [](const void *p) { return ((uintptr_t)p & 15) == 0; };
     bool ok = al16(a.master) && al16(a.m) && al16(a.v) && al16(a.g);
     if (a.cur) ok = ok && al16(a.xb) && al16(a.mb) && al16(a.vb);
-    for (int32_t k = 0; k < a.world && k < kMaxRanks; ++k) ok = ok && al16(a.grads[k]);
-    return ok;
+    return ok && step_grad_align(a) >= 8;
 }
 
 struct GatherArgs {

@@ -206,17 +206,29 @@ __device__ __forceinline__ void adam1(float g, float &x, float &m, float &v, con
     x = __fsub_rn(xd, upd);
 }
 
+// 16 bytes from an address on an 8-byte boundary, as two 8-byte loads.
+__device__ __forceinline__ uint4 ld_stream_halves(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2+8];" : "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
 // Rank-order sum of 8 consecutive elements at vector index k of every rank
-// buffer, chunk by chunk: a chunk's 16-byte loads (4 ranks) are all issued
-// before any of them is added, and within the chunk the adds go in rank
-// order.  Four ranks per chunk keeps the registers low enough for four
-// resident blocks per SM; the bytes in flight come from occupancy.
+// buffer, chunk by chunk: a chunk's loads (4 ranks) are all issued before
+// any of them is added, and within the chunk the adds go in rank order.
+// Four ranks per chunk keeps the registers low enough for four resident
+// blocks per SM; the bytes in flight come from occupancy.  Rank grads on a
+// 16-byte boundary are read 16 bytes per load, those on an 8-byte boundary
+// (grad_align, the same for the whole launch) 8 bytes per load.
 template <int GT>
 __device__ __forceinline__ void rank_sum8(const StepArgs &a, int64_t i, float (&acc)[kVec])
 {
     constexpr int L = Ty<GT>::kLoads;
     constexpr int kChunk = 4;
     const int64_t byte_off = i * (GT == F32 ? 4 : 2);
+    const bool halves = a.grad_align < 16;
     for (int c = 0; c < a.world; c += kChunk) {
         uint4 raw[kChunk][L];
 #pragma unroll
@@ -224,7 +236,8 @@ __device__ __forceinline__ void rank_sum8(const StepArgs &a, int64_t i, float (&
             if (c + u < a.world) {
                 const char *p = static_cast<const char *>(a.grads[c + u]) + byte_off;
 #pragma unroll
-                for (int l = 0; l < L; ++l) raw[u][l] = ld_stream(p + 16 * l);
+                for (int l = 0; l < L; ++l)
+                    raw[u][l] = halves ? ld_stream_halves(p + 16 * l) : ld_stream(p + 16 * l);
             }
         }
 #pragma unroll

@@ -143,7 +143,8 @@ class LibraryRank:
     with an fp32 scratch."""
 
     def __init__(self, numel: int, world: int, rank: int, grad_dtype: int, param_dtype: int,
-                 device, shadow: bool = True, weight_decay: float = 0.0, stage: int = 2):
+                 device, shadow: bool = True, weight_decay: float = 0.0, stage: int = 2,
+                 params: torch.Tensor | None = None, flag: torch.Tensor | None = None):
         self.device = torch.device(device)
         self.grad_dtype, self.param_dtype = grad_dtype, param_dtype
         self.ctx = z.zero_init(numel, world, stage, grad_dtype, param_dtype, rank)
@@ -153,9 +154,23 @@ class LibraryRank:
         self.master = torch.zeros(S, **f32)
         self.m = torch.zeros(S, **f32)
         self.v = torch.zeros(S, **f32)
-        self.params = torch.zeros(P, dtype=_TORCH[param_dtype], device=self.device)
+        # the full parameter buffer; ranks held by one process may share one
+        # (each writes only its own shard's place)
+        if params is not None:
+            if params.numel() != P or params.dtype != _TORCH[param_dtype]:
+                raise ValueError("params must hold %d elements of the param type" % P)
+            self.params = params
+        else:
+            self.params = torch.zeros(P, dtype=_TORCH[param_dtype], device=self.device)
         self.own_params = self.params[rank * S:(rank + 1) * S]
-        self.flag = torch.zeros(1, dtype=torch.int64, device=self.device)
+        # the flag word; ranks held by one process may share one, as the
+        # all-ranks view has one: every pass raises it to the same step id
+        if flag is not None:
+            if flag.numel() != 1 or flag.dtype != torch.int64:
+                raise ValueError("flag must be one int64 word")
+            self.flag = flag
+        else:
+            self.flag = torch.zeros(1, dtype=torch.int64, device=self.device)
         self.shadow = None
         self.scratch = None
         if shadow:
@@ -496,3 +511,86 @@ class ShardedZero3Step:
             combine_flag(local.flag, self.group)
             local.finish(lr, beta1, beta2, eps, t)
             return local.status()
+
+
+class RanksStep:
+    """Several consecutive data-parallel ranks in each process: W ranks over
+    N processes, process p holding ranks p*k .. p*k + k - 1 (k = W / N), each
+    in the library's one-rank view.  `ranks` are the process's k LibraryRank
+    objects (or objects with the same members), in rank order, sharing one
+    full parameter buffer and one flag word.  With k = 1 this is ShardedStep;
+    with N = 1 it is the all-ranks step done rank by rank, on one GPU, with
+    no collective at all.  The workload -- W ranks over the flat vector -- is
+    the same whatever N is, so its time compares across process counts.
+
+    The exchange is k all-to-alls of equal pieces: in call c every process
+    sends its rank p*k + c's local gradient, piece q (the shards of process
+    q's k ranks) to process q, so the W incoming slices of each local rank
+    are views into the k receive buffers (with N = 1, into the local
+    gradients themselves).  The shared flag word already holds the MAX over
+    the process's ranks once their passes have run; one MAX all-reduce
+    combines it over the processes."""
+
+    def __init__(self, ranks, group=None):
+        self.ranks = list(ranks)
+        if not self.ranks:
+            raise ValueError("no ranks")
+        self.group = group
+        self.k = len(self.ranks)
+        self.N = dist.get_world_size(group)
+        self.p = dist.get_rank(group)
+        self.W = self.k * self.N
+        r0 = self.ranks[0]
+        S = r0.shard
+        self.params, self.flag = r0.params, r0.flag
+        for r in self.ranks:
+            if r.shard != S:
+                raise ValueError("the ranks must have one shard size")
+            if (r.params.data_ptr() != self.params.data_ptr()
+                    or r.flag.data_ptr() != self.flag.data_ptr()):
+                raise ValueError("the ranks of one process must share one parameter "
+                                 "buffer and one flag word")
+        if self.params.numel() != S * self.W:
+            raise ValueError("the parameter buffer must hold the W shards")
+        lo = self.p * self.k * S
+        self.own_params = self.params[lo:lo + self.k * S]
+        self.recv = ([r0.grad_buffer(S * self.W) for _ in range(self.k)]
+                     if self.N > 1 else None)
+
+    def slices(self, jj: int, local_grads):
+        """The W incoming slices of this process's rank jj (its shard of
+        every rank's gradient), in rank order."""
+        S, k = self.ranks[0].shard, self.k
+        src = self.recv if self.N > 1 else local_grads
+        lo = (self.p * k + jj) * S
+        out = []
+        for i in range(self.W):
+            q, c = divmod(i, k)
+            # process q's rank c sent its piece for process p in call c
+            base = q * k * S + jj * S if self.N > 1 else lo
+            out.append(src[c][base:base + S])
+        return out
+
+    def step(self, local_grads, lr, beta1, beta2, eps, t, loss_scale=0.0):
+        """local_grads: the k ranks' gradients of the whole padded vector
+        (W*S elements each, zeros past numel).  Returns (nonfinite, skipped),
+        the same for every rank of every process."""
+        if len(local_grads) != self.k:
+            raise ValueError("one gradient per rank of this process")
+        if self.N > 1:
+            with _Range("zero: exchange"):
+                for c in range(self.k):
+                    exchange_slices(self.recv[c], local_grads[c], self.group)
+        with _Range("zero: local pass"):
+            for jj, r in enumerate(self.ranks):
+                r.local_pass(self.slices(jj, local_grads), lr, beta1, beta2, eps, t, loss_scale)
+        with _Range("zero: verdict"):
+            if self.N > 1:
+                combine_flag(self.flag, self.group)
+            for r in self.ranks:
+                r.finish(lr, beta1, beta2, eps, t)
+            verdict = self.ranks[0].status()
+        if self.N > 1:
+            with _Range("zero: all-gather"):
+                gather_params(self.params, self.own_params, self.group)
+        return verdict
