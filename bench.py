@@ -33,13 +33,13 @@ headline in a runner of its own (with its own clocks and e2e).
 
 With --gpus N > 1 (torchrun), the workload's W data-parallel ranks (16 for
 the headline; --dp-ranks W to choose) are spread over the N processes, W/N
-consecutive ranks each, every rank in the library's one-rank view, stepped
-through the library's sharded step (per rank an all-to-all of its grad
-slices, each rank's local fused pass, a MAX all-reduce of the flag word, the
-finalizes and an all-gather of the cast shards; NCCL, or gloo through host
-memory with --dist-backend gloo).  The workload is the same at every N:
-strong scaling, and with N = 1 (--sharded: a group of one, no collective) it
-is the headline's step done rank by rank.  --replicas instead runs one full
+consecutive ranks each, every process one library view of its ranks,
+stepped through the library's sharded step (per held rank an all-to-all of
+its grad pieces, the process's one fused pass over its shards, a MAX
+all-reduce of the flag word, the finalize and an all-gather of the cast
+shards; NCCL, or gloo through host memory with --dist-backend gloo).  The
+workload is the same at every N: strong scaling, and with N = 1 (--sharded:
+a group of one, no collective) it is the headline's step.  --replicas instead runs one full
 replica of the workload per GPU with no data-path collective (weak
 scaling).
 `--impl reference` times the CPU oracle instead (rank 0 only).
@@ -412,6 +412,16 @@ def step_plan(run):
     return plan
 
 
+def settle_device_memory():
+    """Hand the allocator's cached but unused device blocks back before a
+    timed region.  Measured on GB300 (GPT-2 XL step, the same kernel and
+    buffers): with about 12 GB of set-up temporaries left cached after the
+    grads were allocated the step took 13.45 ms, with them released 13.03."""
+    import torch
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
 def run_step(run, plan, events=None):
     if events is None:
         for L in plan:
@@ -551,7 +561,7 @@ def measure(args, w, shadow, world_size, device_index, steps, kernel_steps, cloc
         run.stream = torch.cuda.Stream(run.dev)
     plan = step_plan(run)
     assert sum(L.alg_bytes for L in plan) == static_plan_bytes(w, shadow)
-    torch.cuda.synchronize()
+    settle_device_memory()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(run.stream)
     for _ in range(args.warmup):
@@ -768,12 +778,13 @@ def sharded_config(args, world_size):
 def bench_sharded(args, rank, world_size, device_index):
     """The sharded mode (the default for --gpus N > 1; --sharded with one
     process): the workload's W data-parallel ranks over the N processes,
-    process p holding ranks p*k .. p*k + k - 1 (k = W/N) in the library's
-    one-rank view, stepped through the library's sharded step
+    process p holding ranks p*k .. p*k + k - 1 (k = W/N) in one library
+    view of those ranks, stepped through the library's sharded step
     (zero_sharded_optimizer_step_gb300.sharded).  A flat vector (RanksStep):
-    per rank an all-to-all of its grad slices, each rank's local fused pass,
-    a MAX all-reduce of the shared flag word, the finalizes, an all-gather of
-    the cast shards -- with N = 1 no collective.  Stage 3 (one rank per
+    per held rank an all-to-all of its grad pieces, the process's one fused
+    pass over its k shards, a MAX all-reduce of the flag word, the finalize,
+    an all-gather of the cast shards -- with N = 1 no collective, and the
+    pass is the headline's single all-ranks launch.  Stage 3 (one rank per
     process): per unit an all-gather before forward and backward and, after
     the unit's backward, the exchange of its grads and its local pass; the
     flag combined after the last unit.  The total work is the whole workload
@@ -796,45 +807,37 @@ def bench_sharded(args, rank, world_size, device_index):
     bp = 4 if w.param_dtype == 0 else 2
     k = w.world // world_size                  # ranks held by this process
     if w.stage < 3:
-        # process `rank` holds ranks rank*k .. rank*k + k - 1, sharing one
-        # parameter buffer and one flag word
-        first = sh.LibraryRank(w.numel, w.world, rank * k, w.grad_dtype, w.param_dtype, dev,
-                               shadow=scale > 0, weight_decay=w.weight_decay)
-        ranks = [first] + [sh.LibraryRank(w.numel, w.world, rank * k + c, w.grad_dtype,
-                                          w.param_dtype, dev, shadow=scale > 0,
-                                          weight_decay=w.weight_decay, params=first.params,
-                                          flag=first.flag) for c in range(1, k)]
-        local = first
-        units = [(w.numel, first.shard, None)]
+        # process `rank` holds ranks rank*k .. rank*k + k - 1 in one view:
+        # its k shards end to end, one pass over them
+        local = sh.LibraryRank(w.numel, w.world, rank * k, w.grad_dtype, w.param_dtype, dev,
+                               shadow=scale > 0, weight_decay=w.weight_decay, n_ranks=k)
+        units = [(w.numel, local.shard * k, local.master)]
     else:
         local = sh.LibraryRank3(w.units, w.world, rank, w.grad_dtype, w.param_dtype, dev,
                                 shadow=scale > 0, weight_decay=w.weight_decay)
-        ranks = [local]
         units = [(nu, S, local.master[o:o + S])
                  for nu, S, o in zip(w.units, local.shards, local.offsets)]
     grads, kbytes, updated = [], 0, 0
-    for u, (nu, S, master) in enumerate(units):
+    for u, (nu, n, master) in enumerate(units):
+        # n: the view's range ([rank*n, rank*n + n): k shards, or the unit's shard)
+        nv = max(0, min(n, nu - rank * n))
+        if nv:
+            synth.fill_device(master.data_ptr(), nv, synth.F32,
+                              synth.key(w.seed, synth.KIND_MASTER, 0, 0, u), w.sigma_master, st,
+                              index0=rank * n)
         for c in range(k):
-            r = rank * k + c                   # the global rank
-            nv = max(0, min(S, nu - r * S))
-            m = master if master is not None else ranks[c].master
-            if nv:
-                synth.fill_device(m.data_ptr(), nv, synth.F32,
-                                  synth.key(w.seed, synth.KIND_MASTER, 0, 0, u), w.sigma_master,
-                                  st, index0=r * S)
-            g = local.grad_buffer(S * w.world)
+            g = local.grad_buffer(n * world_size)
             synth.fill_device(g.data_ptr(), nu, w.grad_dtype,
-                              synth.key(w.seed, synth.KIND_GRAD, 1, r, u), sigma, st)
+                              synth.key(w.seed, synth.KIND_GRAD, 1, rank * k + c, u), sigma, st)
             grads.append(g)
-            kbytes += w.world * bg * nv + (24 + bp) * S
-        updated += S * w.world
+        kbytes += w.world * bg * nv + (24 + bp) * n
+        updated += n * world_size
     if w.stage < 3:
-        for r in ranks:
-            r.set_master(r.master.clone())
-        step = sh.RanksStep(ranks)
+        local.set_master()                     # the params: the filled master's cast
+        step = sh.RanksStep(local)
     else:
-        for u, (nu, S, master) in enumerate(units):
-            local.set_master(u, master.clone())
+        for u in range(len(units)):
+            local.set_master(u)
         # the next unit's all-gather in flight while a unit is worked on
         step = sh.ShardedZero3Step(local, prefetch=True)
     t, good = 0, 0
@@ -853,17 +856,17 @@ def bench_sharded(args, rank, world_size, device_index):
             t += 1
         return skipped
 
+    settle_device_memory()
+
     def local_only():
-        # the process's own kernels alone: each of its ranks' passes over
-        # its W slices (the exchanged ones, or the local grads in a group of
-        # one; stage 3: the local grads read as slices, the same bytes and
-        # arithmetic as the exchanged ones)
+        # the process's own kernels alone: the pass over its range from the
+        # W ranks' pieces (the exchanged ones, or the local grads in a group
+        # of one; stage 3: the local grads read as slices, the same bytes
+        # and arithmetic as the exchanged ones)
         hp = (w.lr, w.beta1, w.beta2, w.eps, t + 1)
         if w.stage < 3:
-            for jj, r in enumerate(ranks):
-                r.local_pass(step.slices(jj, grads), *hp, scale)
-            for r in ranks:
-                r.finish(*hp)
+            local.local_pass(step.pieces(grads), *hp, scale)
+            local.finish(*hp)
             return
         local.begin(scale)
         for u in reversed(range(len(units))):
@@ -904,7 +907,11 @@ def bench_sharded(args, rank, world_size, device_index):
     e2e = None
     in_bytes = sum(g.numel() * g.element_size() for g in grads)
     local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", str(world_size)))
-    if not args.no_e2e and 2 * in_bytes < 0.3 * host_ram_available() / max(1, local_ranks):
+    out_bytes = local.params.numel() * local.params.element_size()
+    # pinned host copies of the grads in and of the parameter buffer out, the
+    # same budget as the single-process e2e
+    if (not args.no_e2e
+            and in_bytes + out_bytes < 0.3 * host_ram_available() / max(1, local_ranks)):
         # the same steps with this rank's grads copied in from pinned host
         # memory (unit by unit, inside the backward, for stage 3) and its
         # parameter buffer copied back to pinned host memory after the step
@@ -946,7 +953,7 @@ def bench_sharded(args, rank, world_size, device_index):
                "path": "copies on each rank's compute stream around the sharded step"}
     peak, peak_kind = peaks()
     achieved = kbytes / (kms * 1e-3) / 1e9
-    gathers = (2 * bp * sum(u[1] for u in units) * k * (world_size - 1)
+    gathers = (2 * bp * sum(u[1] for u in units) * (world_size - 1)
                * (1 if w.stage < 3 else 2))
     res = {
         "metric": METRIC, "value": updated / (ms * 1e-3), "unit": "params/s",
@@ -968,15 +975,14 @@ def bench_sharded(args, rank, world_size, device_index):
         "roofline": {"kernel": "fused_step_kernel", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "alg_bytes_per_launch": kbytes / (len(units) * k),
+                     "alg_bytes_per_launch": kbytes / len(units),
                      "traffic": None},
-        "gpu_launches": args.steps * (2 * k if w.stage < 3 else len(units) + 1),
+        "gpu_launches": args.steps * (2 if w.stage < 3 else len(units) + 1),
         "clocks": clock_info,
     }
     if e2e is not None:
         res["e2e"] = e2e
-    for r in ranks:
-        r.close()
+    local.close()
     return res
 
 

@@ -123,6 +123,26 @@ def test_init_validation(z):
         assert z.zero_last_error()
 
 
+def test_view_of_several_ranks(z):
+    """zero_init_ranks: ranks [r, r + k) of N, stages 1 and 2 only; the state
+    is their k shards end to end, the parameter buffer the whole vector."""
+    c = z.zero_init_ranks(19210, 4, 2, z.ZERO_F32, z.ZERO_F32, 1, 3)
+    assert z.zero_ctx_shard_size(c, -1) == 4803
+    assert z.zero_ctx_state_elems(c) == 3 * 4803
+    assert z.zero_ctx_param_elems(c) == 19212
+    assert z.zero_state_bytes(c) == 3 * 57636
+    # k = 1 is one rank's view; ranks 0..N-1 the all-ranks view's state
+    assert z.zero_ctx_state_elems(z.zero_init_ranks(19210, 4, 1, z.ZERO_F32, z.ZERO_F32, 3,
+                                                    1)) == 4803
+    assert z.zero_ctx_state_elems(z.zero_init_ranks(19210, 4, 2, z.ZERO_F32, z.ZERO_F32, 0,
+                                                    4)) == 19212
+    for first, k, stage in ((0, 0, 2), (-1, 2, 2), (2, 3, 2), (4, 1, 2), (0, 2, 3), (0, 2, 0)):
+        with pytest.raises(z.ZeroError) as ei:
+            z.zero_init_ranks(19210, 4, stage, z.ZERO_F32, z.ZERO_F32, first, k)
+        assert ei.value.code == z.ZERO_EINVAL, (first, k, stage)
+        assert z.zero_last_error()
+
+
 def test_context_geometry(z):
     c = z.zero_init(19210, 4, 2, z.ZERO_F32, z.ZERO_F32, -1)
     assert z.zero_ctx_shard_size(c, -1) == 4803

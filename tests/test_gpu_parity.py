@@ -289,6 +289,80 @@ def test_grad_offsets_pick_a_load_width(gdt, offs, poff, mode):
     ctx.close()
 
 
+@pytest.mark.parametrize("numel,bucket,shadow", [
+    (100_000, 0, True),          # S = 20,000: aligned pieces, one pass
+    (100_003, 7_777, True),      # S = 20,001: 2-byte-aligned pieces, buckets across shards
+    (100_012, 9_000, False),     # S = 20,003 (pieces 8 bytes off for odd ranks), the scratch
+])
+def test_view_of_several_ranks_equals_the_oracle(numel, bucket, shadow):
+    """A view of ranks 1..3 of 5 (zero_init_ranks): the pieces [S, 4S) of
+    every rank's gradient stepped in one pass (or bucket by bucket), the
+    three shards' state and their places in the full parameter buffer
+    bit-identical to the oracle's all-ranks step over the same range, the
+    rest of the buffer untouched; a +inf inside the range skips step 2."""
+    import zero_sharded_optimizer_step_gb300 as z
+    world, first, k = 5, 1, 3
+    dt = W.BF16
+    w = W.Workload("view", numel, world, 2, dt, dt, steps=3, loss_scale=2.0 ** 10)
+    S = w.shard
+    P = S * world
+    lo, hi = first * S, (first + k) * S
+    dev = torch.device("cuda:0")
+    x = refs.host_master(w)
+    m_ref, v_ref = np.zeros(P, np.float32), np.zeros(P, np.float32)
+    full_ref = oracle.cast(x, dt)
+    full0 = full_ref.copy()
+    ctx = z.zero_init_ranks(numel, world, 2, dt, dt, first, k)
+    assert z.zero_ctx_state_elems(ctx) == k * S
+    f32 = lambda: torch.zeros(k * S, dtype=torch.float32, device=dev)  # noqa: E731
+    master, m, v = f32(), f32(), f32()
+    master.copy_(torch.from_numpy(x[lo:hi]).to(dev))
+    params = torch.from_numpy(full_ref.view(np.int16)).to(dev).view(torch.bfloat16)
+    flag = torch.zeros(1, dtype=torch.int64, device=dev)
+    scratch = None if shadow else f32()
+    z.zero_bind(ctx, master, m, v, params, scratch, flag)
+    if shadow:
+        sets = (f32(), f32(), f32())
+        cur_word = torch.zeros(1, dtype=torch.int64, device=dev)
+        z.zero_bind_shadow(ctx, *sets, cur_word)
+    scale, good, t = w.loss_scale, 0, 0
+    for it in (1, 2, 3):
+        hg = refs.host_grads(w, it, scale)
+        if it == 2:
+            hg[3][lo + 12_345] = oracle.cast(np.array([np.inf], np.float32), dt)[0]
+        skipped_ref, _ = oracle.zero_step(hg, dt, numel, x, m_ref, v_ref, full_ref, dt, w.lr,
+                                          w.beta1, w.beta2, w.eps, t + 1, loss_scale=scale)
+        full_g = []
+        for g in hg:
+            d = torch.zeros(P, dtype=torch.bfloat16, device=dev)
+            d[:numel].copy_(torch.from_numpy(g.view(np.int16)).view(torch.bfloat16))
+            full_g.append(d)
+        pieces = [d[lo:hi] for d in full_g]
+        if bucket:
+            z.zero_bucket_begin(ctx, scale)
+            for off in range(0, k * S, bucket):
+                cnt = min(bucket, k * S - off)
+                z.zero_bucket_step(ctx, off, cnt, [pc[off:off + cnt] for pc in pieces], w.lr,
+                                   w.beta1, w.beta2, w.eps, t + 1)
+            z.zero_bucket_end(ctx, w.lr, w.beta1, w.beta2, w.eps, t + 1)
+        else:
+            z.zero_step(ctx, pieces, w.lr, w.beta1, w.beta2, w.eps, t + 1, scale)
+        _, skipped = z.zero_step_status(ctx)
+        assert skipped == bool(skipped_ref) == (it == 2), it
+        if not skipped:
+            t += 1
+        scale, good = z.zero_scale_update(scale, skipped, good, w.growth_interval)
+    torch.cuda.synchronize()
+    cur = (master, m, v) if not shadow or z.zero_current_state(ctx) == 0 else sets
+    for got, want, what in ((cur[0], x, "master"), (cur[1], m_ref, "m"), (cur[2], v_ref, "v")):
+        assert_bit_identical(to_np(got), want[lo:hi], oracle.F32, what)
+    got = to_np(params)
+    assert_bit_identical(got[lo:hi], full_ref[lo:hi], dt, "params in the view's range")
+    assert got[:lo].tobytes() == full0[:lo].tobytes()
+    assert got[hi:].tobytes() == full0[hi:].tobytes()
+    ctx.close()
+
+
 @pytest.mark.parametrize("rank", [-1, 2])
 def test_stage1_allreduce_output(rank):
     """Stage 1 keeps the full averaged grads: RS + AG == AR, bit-exact."""

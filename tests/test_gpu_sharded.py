@@ -104,10 +104,10 @@ def test_sharded_step_through_the_library(tmp_path, numel, inject_at, shadow, bu
         assert d["full"].tobytes() == full.tobytes()
 
 
-def _ranks(proc, nprocs, port, numel, world, inject_at, shadow, out_dir):
+def _ranks(proc, nprocs, port, numel, world, inject_at, shadow, out_dir, stage=2):
     """Process `proc` of `nprocs` holding world // nprocs consecutive ranks
-    in the library's one-rank view (RanksStep), sharing one parameter
-    buffer and one flag word."""
+    in the library's view of several ranks (LibraryRank(n_ranks=k)), driven
+    by RanksStep."""
     import sys
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
@@ -120,21 +120,16 @@ def _ranks(proc, nprocs, port, numel, world, inject_at, shadow, out_dir):
     dist.init_process_group("gloo", rank=proc, world_size=nprocs)
     torch.cuda.set_device(0)
     k = world // nprocs
-    ranks = []
-    for c in range(k):
-        share = dict(params=ranks[0].params, flag=ranks[0].flag) if ranks else {}
-        ranks.append(LibraryRank(numel, world, proc * k + c, z.ZERO_F16, z.ZERO_F16, "cuda:0",
-                                 shadow=shadow, **share))
-    S = ranks[0].shard
+    local = LibraryRank(numel, world, proc * k, z.ZERO_F16, z.ZERO_F16, "cuda:0",
+                        shadow=shadow, stage=stage, n_ranks=k)
+    S = local.shard
     P = S * world
-    for c, r in enumerate(ranks):
-        lo = (proc * k + c) * S
-        nv = max(0, min(S, numel - lo))
-        x0 = np.zeros(S, np.float32)
-        x0[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER), 0.01,
-                                  index0=lo)
-        r.set_master(torch.from_numpy(x0).cuda())
-    step = RanksStep(ranks)
+    lo = proc * k * S
+    nv = max(0, min(k * S, numel - lo))
+    x0 = np.zeros(k * S, np.float32)
+    x0[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER), 0.01, index0=lo)
+    local.set_master(torch.from_numpy(x0).cuda())
+    step = RanksStep(local)
     scale, good, t, skips = 2.0 ** 12, 0, 0, []
     for it in (1, 2, 3):
         dgs = []
@@ -152,38 +147,51 @@ def _ranks(proc, nprocs, port, numel, world, inject_at, shadow, out_dir):
             t += 1
         scale, good = oracle.scale_update(scale, skipped, good, 2000)
     torch.cuda.synchronize()
-    full = ranks[0].params.cpu().view(torch.int16).numpy().view(np.uint16)
-    for c, r in enumerate(ranks):
-        x, m, v = (a.cpu().numpy() for a in r.state())
-        np.savez(os.path.join(out_dir, "rank%d.npz" % (proc * k + c)), x=x, m=m, v=v, full=full,
-                 skips=np.array(skips))
-        r.close()
+    full = local.params.cpu().view(torch.int16).numpy().view(np.uint16)
+    x, m, v = (a.cpu().numpy() for a in local.state())
+    extra = {}
+    if stage == 1:
+        extra["avg"] = local.grad_avg.cpu().view(torch.int16).numpy().view(np.uint16)
+    for c in range(k):
+        sl = slice(c * S, (c + 1) * S)
+        np.savez(os.path.join(out_dir, "rank%d.npz" % (proc * k + c)), x=x[sl], m=m[sl],
+                 v=v[sl], full=full, skips=np.array(skips), **extra)
+    local.close()
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("nprocs,world,numel,inject_at,shadow", [
-    (1, 4, 300_007, (2, 3, 17), True),        # four ranks in one process, no collective
-    (1, 4, 300_013, (2, 2, 75_011), True),    # S = 4 mod 8: odd ranks' slices take the head
-    (2, 4, 300_013, None, False),
-    (1, 4, 300_007, (2, 1, 299_999), False),  # the fp32 scratch
-    (2, 4, 300_007, (2, 3, 17), True),        # two ranks in each of two processes
-    (2, 4, 300_001, None, True),
-    (2, 6, 300_001, (2, 5, 1), False),
+@pytest.mark.parametrize("nprocs,world,numel,inject_at,shadow,stage", [
+    (1, 4, 300_007, (2, 3, 17), True, 2),        # every rank in one view, no collective
+    (1, 4, 300_007, (2, 1, 299_999), False, 2),  # the fp32 scratch
+    (1, 4, 300_013, (2, 2, 75_011), True, 2),    # S = 4 mod 8
+    (2, 4, 300_007, (2, 3, 17), True, 2),        # two ranks in each of two processes
+    (2, 4, 300_013, None, False, 2),
+    (2, 6, 300_001, (2, 5, 1), False, 2),
+    (2, 4, 300_013, None, True, 1),              # stage 1: the averaged grads gathered too
 ])
 def test_ranks_per_process_through_the_library(tmp_path, nprocs, world, numel, inject_at,
-                                               shadow):
-    """W ranks over N processes (RanksStep): with N = 1 the all-ranks step of
-    one GPU done rank by rank, with N = 2 the exchange of each rank's slices
-    between processes; the state of every rank, the full parameter buffer
-    and the skips bit-identical to the oracle's all-ranks step."""
+                                               shadow, stage):
+    """W ranks over N processes, each process one library view of its W/N
+    ranks (RanksStep): with N = 1 the view holds every rank and the step is
+    one pass with no collective; with N = 2 each rank's pieces are exchanged
+    between the processes.  The state of every rank, the full parameter
+    buffer (and, stage 1, the averaged grads) and the skips bit-identical to
+    the oracle's all-ranks step."""
     port = _free_port()
     mp.start_processes(_ranks, args=(nprocs, port, numel, world, inject_at, shadow,
-                                     str(tmp_path)), nprocs=nprocs, join=True,
+                                     str(tmp_path), stage), nprocs=nprocs, join=True,
                        start_method="spawn")
     import oracle
+    import synth
     x, m, v, full, skips = _all_ranks_reference(numel, world, inject_at)
     assert skips == [bool(inject_at) and it == inject_at[0] for it in (1, 2, 3)]
     S = oracle.shard_size(numel, world)
+    avg = None
+    if stage == 1:
+        # no overflow: the scale stays 2^12 and step 3's grads are these
+        grads = [synth.fill_host(numel, synth.F16, synth.key(0, synth.KIND_GRAD, 3, k),
+                                 1e-3 * 2.0 ** 12) for k in range(world)]
+        avg = oracle.cast(oracle.all_reduce_mean(grads, oracle.F16, numel), oracle.F16)
     for r in range(world):
         d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
         assert list(d["skips"]) == skips, r
@@ -192,6 +200,8 @@ def test_ranks_per_process_through_the_library(tmp_path, nprocs, world, numel, i
         assert d["m"].tobytes() == m[sl].tobytes(), r
         assert d["v"].tobytes() == v[sl].tobytes(), r
         assert d["full"].tobytes() == full.tobytes(), r
+        if avg is not None:
+            assert d["avg"].tobytes() == avg.tobytes(), r
 
 
 @pytest.mark.parametrize("extra,updated", [

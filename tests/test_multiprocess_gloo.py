@@ -202,10 +202,42 @@ def test_one_rank_views_with_real_collectives(tmp_path, world, numel, inject_at,
         assert d["full"].tobytes() == full.tobytes()
 
 
+class OracleRanks:
+    """The view of k consecutive ranks (the members RanksStep drives, as the
+    library's LibraryRank(n_ranks=k) has them), each rank's arithmetic done
+    by the oracle: its pieces of k*S elements are cut into the k ranks'
+    slices; one parameter buffer and one flag word for all."""
+
+    def __init__(self, numel, world, first, k):
+        import oracle
+        self.n_ranks, self.rank = k, first
+        self.shard = S = oracle.shard_size(numel, world)
+        self.params = torch.zeros(S * world, dtype=torch.int16)
+        self.flag = torch.zeros(1, dtype=torch.int64)
+        self.ranks = [OracleRank(numel, world, first + j, self.params, self.flag)
+                      for j in range(k)]
+        self.own_params = self.params[first * S:(first + k) * S]
+
+    def grad_buffer(self, n):
+        return torch.zeros(n, dtype=torch.int16)
+
+    def local_pass(self, pieces, lr, beta1, beta2, eps, t, loss_scale):
+        S = self.shard
+        for j, r in enumerate(self.ranks):
+            r.local_pass([pc[j * S:(j + 1) * S] for pc in pieces], lr, beta1, beta2, eps, t,
+                         loss_scale)
+
+    def finish(self, lr, beta1, beta2, eps, t):
+        for r in self.ranks:
+            r.finish(lr, beta1, beta2, eps, t)
+
+    def status(self):
+        return self.ranks[0].status()
+
+
 def _ranks_main(proc, nprocs, port, numel, world, inject_at, out_dir):
     """Process `proc` of `nprocs` holding world // nprocs consecutive ranks
-    (RanksStep), each with the oracle's arithmetic, sharing one parameter
-    buffer and one flag word."""
+    in one view (RanksStep), each rank's arithmetic the oracle's."""
     import sys
     sys.path.insert(0, ROOT)
     import oracle
@@ -216,9 +248,9 @@ def _ranks_main(proc, nprocs, port, numel, world, inject_at, out_dir):
     k = world // nprocs
     S = oracle.shard_size(numel, world)
     P = S * world
-    params, flag = torch.zeros(P, dtype=torch.int16), torch.zeros(1, dtype=torch.int64)
-    ranks = [OracleRank(numel, world, proc * k + c, params, flag) for c in range(k)]
-    step = RanksStep(ranks)
+    view = OracleRanks(numel, world, proc * k, k)
+    params, ranks = view.params, view.ranks
+    step = RanksStep(view)
     scale, good, t, skips = 2.0 ** 12, 0, 0, []
     for it in (1, 2, 3):
         gts = []

@@ -46,6 +46,8 @@ _SIGS = {
     "zero_last_error": (ctypes.c_char_p, []),
     "zero_init": (ctypes.c_int, [ctypes.POINTER(_ctxp), _i64, _i32, _i32, _i32, _i32, _i32,
                                  ctypes.POINTER(_i64), _i32]),
+    "zero_init_ranks": (ctypes.c_int, [ctypes.POINTER(_ctxp), _i64, _i32, _i32, _i32, _i32,
+                                       _i32, _i32]),
     "zero_init_dim0": (ctypes.c_int, [ctypes.POINTER(_ctxp), _i32, _i32, _i32, _i32,
                                       ctypes.POINTER(_i64), ctypes.POINTER(_i64), _i32]),
     "zero_destroy": (ctypes.c_int, [_ctxp]),
@@ -206,6 +208,15 @@ def zero_init(numel: int, world: int, stage: int, grad_dtype: int, param_dtype: 
         units = (_i64 * n_units)(*unit_numels)
     _check(_L.zero_init(ctypes.byref(h), numel, world, stage, grad_dtype, param_dtype, rank,
                         units, n_units))
+    return Ctx(h.value)
+
+
+def zero_init_ranks(numel: int, world: int, stage: int, grad_dtype: int, param_dtype: int,
+                    first_rank: int, n_ranks: int) -> Ctx:
+    """Stages 1, 2: a view of ranks [first_rank, first_rank + n_ranks)."""
+    h = _ctxp()
+    _check(_L.zero_init_ranks(ctypes.byref(h), numel, world, stage, grad_dtype, param_dtype,
+                              first_rank, n_ranks))
     return Ctx(h.value)
 
 

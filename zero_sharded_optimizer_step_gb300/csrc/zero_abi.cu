@@ -60,6 +60,7 @@ bool pow2_with_normal_inverse(float x)
 struct zero_ctx {
     int64_t numel = 0;
     int32_t world = 1, stage = 2, gdt = 0, pdt = 0, rank = -1;
+    int32_t nranks = 1;          // rank >= 0: the view holds ranks [rank, rank + nranks)
     int64_t S = 0, P = 0;
     std::vector<int64_t> unit_numel, unit_S, unit_state_off;
     int64_t state_elems = 0, param_elems = 0;
@@ -201,9 +202,10 @@ Range vector_range(const zero_ctx *c)
         r.params = static_cast<char *>(c->params);
         r.grad_avg = static_cast<char *>(c->grad_avg);
     } else {
+        // the view's consecutive shards, [rank*S, (rank + nranks)*S)
         const int64_t lo = (int64_t)c->rank * c->S;
-        r.n = c->S;
-        r.n_valid = std::max<int64_t>(0, std::min<int64_t>(c->S, c->numel - lo));
+        r.n = c->S * c->nranks;
+        r.n_valid = std::max<int64_t>(0, std::min<int64_t>(r.n, c->numel - lo));
         r.params = static_cast<char *>(c->params) + lo * es_p;
         r.grad_avg = c->grad_avg ? static_cast<char *>(c->grad_avg) + lo * es_g : nullptr;
     }
@@ -549,6 +551,28 @@ int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage, int32
             return rc;
         }
     }
+    *out = c;
+    return ZERO_OK;
+}
+
+int zero_init_ranks(zero_ctx **out, int64_t numel, int32_t world, int32_t stage,
+                    int32_t grad_dtype, int32_t param_dtype, int32_t first_rank,
+                    int32_t n_ranks)
+{
+    if (!out) return fail(ZERO_EINVAL, "out is null");
+    *out = nullptr;
+    if (stage != 1 && stage != 2)
+        return fail(ZERO_EINVAL, "a view of several ranks is for stages 1 and 2 (got %d)", stage);
+    if (world < 1 || world > ZERO_MAX_RANKS)
+        return fail(ZERO_EINVAL, "world must be in [1, %d] (got %d)", ZERO_MAX_RANKS, world);
+    if (first_rank < 0 || n_ranks < 1 || n_ranks > world - first_rank)
+        return fail(ZERO_EINVAL, "ranks [%d, %d + %d) are not within [0, %d)", first_rank,
+                    first_rank, n_ranks, world);
+    zero_ctx *c = nullptr;
+    int rc = zero_init(&c, numel, world, stage, grad_dtype, param_dtype, first_rank, nullptr, 0);
+    if (rc) return rc;
+    c->nranks = n_ranks;
+    c->state_elems = c->S * n_ranks;
     *out = c;
     return ZERO_OK;
 }

@@ -137,47 +137,41 @@ def gather_params(full: torch.Tensor, own: torch.Tensor, group=None, async_op: b
 
 class LibraryRank:
     """Rank `rank`'s own part of the step, in libzero.so's one-rank view
-    (stages 1 and 2): the fp32 shard state, the full parameter buffer and
-    the flag word on `device`, all owned here.  Loss-scaled steps run as one
-    pass over two state sets (`shadow`, the default) or as the two passes
-    with an fp32 scratch."""
+    (stages 1 and 2) -- or, with n_ranks = k > 1, the part of the k
+    consecutive ranks rank .. rank + k - 1 that one process holds, in the
+    library's view of several ranks (one pass over their k shards): the fp32
+    state of the shards, the full parameter buffer and the flag word on
+    `device`, all owned here.  Loss-scaled steps run as one pass over two
+    state sets (`shadow`, the default) or as the two passes with an fp32
+    scratch."""
 
     def __init__(self, numel: int, world: int, rank: int, grad_dtype: int, param_dtype: int,
                  device, shadow: bool = True, weight_decay: float = 0.0, stage: int = 2,
-                 params: torch.Tensor | None = None, flag: torch.Tensor | None = None):
+                 n_ranks: int = 1):
         self.device = torch.device(device)
         self.grad_dtype, self.param_dtype = grad_dtype, param_dtype
-        self.ctx = z.zero_init(numel, world, stage, grad_dtype, param_dtype, rank)
+        self.rank, self.n_ranks = rank, n_ranks
+        self.ctx = (z.zero_init(numel, world, stage, grad_dtype, param_dtype, rank)
+                    if n_ranks == 1 else
+                    z.zero_init_ranks(numel, world, stage, grad_dtype, param_dtype, rank,
+                                      n_ranks))
         self.shard = z.zero_ctx_shard_size(self.ctx, -1)
         S, P = self.shard, z.zero_ctx_param_elems(self.ctx)
+        self.n = n = z.zero_ctx_state_elems(self.ctx)  # the view's range: n_ranks * S
         f32 = dict(dtype=torch.float32, device=self.device)
-        self.master = torch.zeros(S, **f32)
-        self.m = torch.zeros(S, **f32)
-        self.v = torch.zeros(S, **f32)
-        # the full parameter buffer; ranks held by one process may share one
-        # (each writes only its own shard's place)
-        if params is not None:
-            if params.numel() != P or params.dtype != _TORCH[param_dtype]:
-                raise ValueError("params must hold %d elements of the param type" % P)
-            self.params = params
-        else:
-            self.params = torch.zeros(P, dtype=_TORCH[param_dtype], device=self.device)
-        self.own_params = self.params[rank * S:(rank + 1) * S]
-        # the flag word; ranks held by one process may share one, as the
-        # all-ranks view has one: every pass raises it to the same step id
-        if flag is not None:
-            if flag.numel() != 1 or flag.dtype != torch.int64:
-                raise ValueError("flag must be one int64 word")
-            self.flag = flag
-        else:
-            self.flag = torch.zeros(1, dtype=torch.int64, device=self.device)
+        self.master = torch.zeros(n, **f32)
+        self.m = torch.zeros(n, **f32)
+        self.v = torch.zeros(n, **f32)
+        self.params = torch.zeros(P, dtype=_TORCH[param_dtype], device=self.device)
+        self.own_params = self.params[rank * S:rank * S + n]
+        self.flag = torch.zeros(1, dtype=torch.int64, device=self.device)
         self.shadow = None
         self.scratch = None
         if shadow:
-            self.shadow = tuple(torch.zeros(S, **f32) for _ in range(3))
+            self.shadow = tuple(torch.zeros(n, **f32) for _ in range(3))
             self.cur = torch.zeros(1, dtype=torch.int64, device=self.device)
         else:
-            self.scratch = torch.zeros(S, **f32)
+            self.scratch = torch.zeros(n, **f32)
         z.zero_bind(self.ctx, self.master, self.m, self.v, self.params, self.scratch, self.flag)
         if shadow:
             z.zero_bind_shadow(self.ctx, *self.shadow, self.cur)
@@ -189,17 +183,19 @@ class LibraryRank:
         self.grad_avg = self.own_grad_avg = None
         if stage == 1:
             self.grad_avg = torch.zeros(P, dtype=_TORCH[grad_dtype], device=self.device)
-            self.own_grad_avg = self.grad_avg[rank * S:(rank + 1) * S]
+            self.own_grad_avg = self.grad_avg[rank * S:rank * S + n]
             z.zero_bind_allreduce_out(self.ctx, self.grad_avg)
         self._scaled = False
 
     def grad_buffer(self, n: int) -> torch.Tensor:
         return torch.zeros(n, dtype=_TORCH[self.grad_dtype], device=self.device)
 
-    def set_master(self, x: torch.Tensor) -> None:
-        """The shard's initial fp32 weights; its params become their cast."""
-        self.master.copy_(x)
-        self.own_params.copy_(self.master.to(self.params.dtype))
+    def set_master(self, x: torch.Tensor | None = None) -> None:
+        """The shards' initial fp32 weights (x, or the master as it stands);
+        their params become their cast (a casting copy: no temporary)."""
+        if x is not None:
+            self.master.copy_(x)
+        self.own_params.copy_(self.master)
 
     def local_pass(self, slices, lr, beta1, beta2, eps, t, loss_scale, stream=None):
         self._scaled = loss_scale > 0
@@ -209,8 +205,7 @@ class LibraryRank:
         elif self.shadow is not None:
             # one pass into the other state set; the finalize waits for the verdict
             z.zero_bucket_begin(self.ctx, loss_scale)
-            z.zero_bucket_step(self.ctx, 0, self.shard, slices, lr, beta1, beta2, eps, t,
-                               stream)
+            z.zero_bucket_step(self.ctx, 0, self.n, slices, lr, beta1, beta2, eps, t, stream)
         else:
             z.zero_step_reduce(self.ctx, slices, loss_scale, stream)
 
@@ -227,8 +222,8 @@ class LibraryRank:
         z.zero_bucket_begin(self.ctx, loss_scale)
 
     def bucket_pass(self, offset, count, slices, lr, beta1, beta2, eps, t, stream=None):
-        """Elements [offset, offset + count) of the shard, from the N slices
-        of that range (the library's bucketed step in the one-rank view)."""
+        """Elements [offset, offset + count) of the view's range, from the N
+        slices of that range (the library's bucketed step)."""
         z.zero_bucket_step(self.ctx, offset, count, slices, lr, beta1, beta2, eps, t, stream)
 
     def bucket_end(self, lr, beta1, beta2, eps, t, stream=None):
@@ -388,11 +383,13 @@ class LibraryRank3:
     def own_params(self, u: int) -> torch.Tensor:
         return self.params[self.offsets[u]:self.offsets[u] + self.shards[u]]
 
-    def set_master(self, u: int, x: torch.Tensor) -> None:
-        """Unit u's initial fp32 shard; its params become their cast."""
+    def set_master(self, u: int, x: torch.Tensor | None = None) -> None:
+        """Unit u's initial fp32 shard (x, or the master as it stands); its
+        params become their cast (a casting copy: no temporary)."""
         view = self.master[self.offsets[u]:self.offsets[u] + self.shards[u]]
-        view.copy_(x)
-        self.own_params(u).copy_(view.to(self.params.dtype))
+        if x is not None:
+            view.copy_(x)
+        self.own_params(u).copy_(view)
 
     def begin(self, loss_scale) -> None:
         self._scaled = loss_scale > 0
@@ -515,66 +512,55 @@ class ShardedZero3Step:
 
 class RanksStep:
     """Several consecutive data-parallel ranks in each process: W ranks over
-    N processes, process p holding ranks p*k .. p*k + k - 1 (k = W / N), each
-    in the library's one-rank view.  `ranks` are the process's k LibraryRank
-    objects (or objects with the same members), in rank order, sharing one
-    full parameter buffer and one flag word.  With k = 1 this is ShardedStep;
-    with N = 1 it is the all-ranks step done rank by rank, on one GPU, with
-    no collective at all.  The workload -- W ranks over the flat vector -- is
-    the same whatever N is, so its time compares across process counts.
+    N processes, process p holding ranks p*k .. p*k + k - 1 (k = W / N) in
+    one view (`local`: a LibraryRank with n_ranks = k, or an object with the
+    same members), whose range is the k shards [p*k*S, (p+1)*k*S).  With
+    k = 1 this is ShardedStep; with N = 1 the view holds every rank and the
+    step is the all-ranks step of one GPU, with no collective at all.  The
+    workload -- W ranks over the flat vector -- is the same whatever N is,
+    so its time compares across process counts.
 
     The exchange is k all-to-alls of equal pieces: in call c every process
-    sends its rank p*k + c's local gradient, piece q (the shards of process
-    q's k ranks) to process q, so the W incoming slices of each local rank
-    are views into the k receive buffers (with N = 1, into the local
-    gradients themselves).  The shared flag word already holds the MAX over
-    the process's ranks once their passes have run; one MAX all-reduce
-    combines it over the processes."""
+    sends its rank p*k + c's local gradient, piece q (the range of process
+    q's view) to process q, so each of the W ranks' pieces of this
+    process's range is one contiguous view into the k receive buffers (with
+    N = 1, the local gradients themselves); then the one local pass, one MAX
+    all-reduce of the flag word, the finalize (or apply) and one all-gather
+    of the process's k cast shards."""
 
-    def __init__(self, ranks, group=None):
-        self.ranks = list(ranks)
-        if not self.ranks:
-            raise ValueError("no ranks")
+    def __init__(self, local, group=None):
+        self.local = local
         self.group = group
-        self.k = len(self.ranks)
+        self.k = local.n_ranks
         self.N = dist.get_world_size(group)
         self.p = dist.get_rank(group)
         self.W = self.k * self.N
-        r0 = self.ranks[0]
-        S = r0.shard
-        self.params, self.flag = r0.params, r0.flag
-        for r in self.ranks:
-            if r.shard != S:
-                raise ValueError("the ranks must have one shard size")
-            if (r.params.data_ptr() != self.params.data_ptr()
-                    or r.flag.data_ptr() != self.flag.data_ptr()):
-                raise ValueError("the ranks of one process must share one parameter "
-                                 "buffer and one flag word")
-        if self.params.numel() != S * self.W:
+        if local.rank != self.p * self.k:
+            raise ValueError("process %d must hold ranks from %d (the view starts at %d)"
+                             % (self.p, self.p * self.k, local.rank))
+        S = local.shard
+        if local.params.numel() != S * self.W:
             raise ValueError("the parameter buffer must hold the W shards")
-        lo = self.p * self.k * S
-        self.own_params = self.params[lo:lo + self.k * S]
-        self.recv = ([r0.grad_buffer(S * self.W) for _ in range(self.k)]
+        self.recv = ([local.grad_buffer(S * self.W) for _ in range(self.k)]
                      if self.N > 1 else None)
 
-    def slices(self, jj: int, local_grads):
-        """The W incoming slices of this process's rank jj (its shard of
-        every rank's gradient), in rank order."""
-        S, k = self.ranks[0].shard, self.k
-        src = self.recv if self.N > 1 else local_grads
-        lo = (self.p * k + jj) * S
+    def pieces(self, local_grads):
+        """The W ranks' gradients over this process's range (k*S elements
+        each), in rank order."""
+        K = self.k * self.local.shard
+        if self.N == 1:
+            return [g[:K] for g in local_grads]
         out = []
         for i in range(self.W):
-            q, c = divmod(i, k)
-            # process q's rank c sent its piece for process p in call c
-            base = q * k * S + jj * S if self.N > 1 else lo
-            out.append(src[c][base:base + S])
+            q, c = divmod(i, self.k)
+            # process q's rank c sent its piece for this process in call c
+            out.append(self.recv[c][q * K:(q + 1) * K])
         return out
 
     def step(self, local_grads, lr, beta1, beta2, eps, t, loss_scale=0.0):
         """local_grads: the k ranks' gradients of the whole padded vector
         (W*S elements each, zeros past numel).  Returns (nonfinite, skipped),
-        the same for every rank of every process."""
+        the same on every process."""
         if len(local_grads) != self.k:
             raise ValueError("one gradient per rank of this process")
         if self.N > 1:
@@ -582,15 +568,17 @@ class RanksStep:
                 for c in range(self.k):
                     exchange_slices(self.recv[c], local_grads[c], self.group)
         with _Range("zero: local pass"):
-            for jj, r in enumerate(self.ranks):
-                r.local_pass(self.slices(jj, local_grads), lr, beta1, beta2, eps, t, loss_scale)
+            self.local.local_pass(self.pieces(local_grads), lr, beta1, beta2, eps, t,
+                                  loss_scale)
         with _Range("zero: verdict"):
             if self.N > 1:
-                combine_flag(self.flag, self.group)
-            for r in self.ranks:
-                r.finish(lr, beta1, beta2, eps, t)
-            verdict = self.ranks[0].status()
+                combine_flag(self.local.flag, self.group)
+            self.local.finish(lr, beta1, beta2, eps, t)
+            verdict = self.local.status()
         if self.N > 1:
             with _Range("zero: all-gather"):
-                gather_params(self.params, self.own_params, self.group)
+                gather_params(self.local.params, self.local.own_params, self.group)
+                # stage 1: the averaged gradient's other ranges too
+                if getattr(self.local, "grad_avg", None) is not None:
+                    gather_params(self.local.grad_avg, self.local.own_grad_avg, self.group)
         return verdict
