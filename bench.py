@@ -977,7 +977,12 @@ def bench_sharded(args, rank, world_size, device_index):
                      "frac": achieved / peak,
                      "alg_bytes_per_launch": kbytes / len(units),
                      "traffic": None},
-        "gpu_launches": args.steps * (2 if w.stage < 3 else len(units) + 1),
+        # per step: the pass and the finalize (or the reduce and the apply)
+        # when loss-scaled, the fused pass alone otherwise; stage 3: one
+        # pass per unit, and the finalize (or the apply) when loss-scaled
+        # (the unit gathers are the collective's own)
+        "gpu_launches": args.steps * ((1 if w.stage < 3 else len(units))
+                                      + (1 if scale > 0 else 0)),
         "clocks": clock_info,
     }
     if e2e is not None:
