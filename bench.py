@@ -735,19 +735,16 @@ def run_e2e(run, plan, args, world_size):
 
 def sharded_workload(args, world_size, rank=0):
     """The workload of the sharded mode: the command line's over W
-    data-parallel ranks (--dp-ranks; a flat vector keeps the workload's own
-    rank count, stage 3 takes one rank per process), each of the N processes
-    holding W / N consecutive ranks; `rank` is the process's index."""
+    data-parallel ranks (--dp-ranks; by default the workload's own rank
+    count), each of the N processes holding W / N consecutive ranks; `rank`
+    is the process's index."""
     base = make_workload(args, args.workload)
     # a flat workload must be the all-ranks one (the mode picks each
     # process's ranks); stage-3 workloads are described as one rank's view
     if (base.stage < 3 and base.rank >= 0) or base.bucket or base.groups or base.unit_rows:
         raise SystemExit("the sharded mode steps a flat vector or flat stage-3 units; "
                          "--workload %s is not one (use --replicas)" % args.workload)
-    W = args.dp_ranks or (base.world if base.stage < 3 else world_size)
-    if base.stage == 3 and W != world_size:
-        raise SystemExit("the sharded ZeRO-3 step holds one rank per process: --dp-ranks %d"
-                         % world_size)
+    W = args.dp_ranks or base.world
     if W % world_size:
         raise SystemExit("--dp-ranks %d is not a multiple of the %d processes" % (W, world_size))
     return base.replace(world=W, rank=rank, name=base.name + "_sharded")
@@ -763,10 +760,12 @@ def sharded_config(args, world_size):
         "workload": describe(w.replace(rank=-1)),
         "params_updated_per_step": sum(shards) * w.world,
         "l2": "inputs larger than L2 (129 MB); no flush between timed steps",
-        "parallelism": "%d data-parallel ranks over %d process(es), %d each (one-rank "
-                       "views; %s)"
+        "parallelism": "%d data-parallel ranks over %d process(es), %d each (one library "
+                       "view per process; %s)"
                        % (w.world, world_size, w.world // world_size,
-                          "no collective: a group of one" if world_size == 1 else
+                          ("no collective: a group of one%s"
+                           % ("; the unit gathers by the library" if w.stage == 3 else ""))
+                          if world_size == 1 else
                           "%s all-to-all of grad slices, MAX all-reduce of the flag word, "
                           "all-gather of the cast shards%s"
                           % (args.dist_backend,
@@ -813,9 +812,10 @@ def bench_sharded(args, rank, world_size, device_index):
                                shadow=scale > 0, weight_decay=w.weight_decay, n_ranks=k)
         units = [(w.numel, local.shard * k, local.master)]
     else:
-        local = sh.LibraryRank3(w.units, w.world, rank, w.grad_dtype, w.param_dtype, dev,
-                                shadow=scale > 0, weight_decay=w.weight_decay)
-        units = [(nu, S, local.master[o:o + S])
+        # per unit the process's k shards end to end
+        local = sh.LibraryRank3(w.units, w.world, rank * k, w.grad_dtype, w.param_dtype, dev,
+                                shadow=scale > 0, weight_decay=w.weight_decay, n_ranks=k)
+        units = [(nu, S * k, local.master[o:o + S * k])
                  for nu, S, o in zip(w.units, local.shards, local.offsets)]
     grads, kbytes, updated = [], 0, 0
     for u, (nu, n, master) in enumerate(units):
@@ -848,8 +848,8 @@ def bench_sharded(args, rank, world_size, device_index):
             _, skipped = step.step(grads, w.lr, w.beta1, w.beta2, w.eps, t + 1,
                                    loss_scale=scale)
         else:
-            _, skipped = step.step(lambda u, params: grads[u], w.lr, w.beta1, w.beta2, w.eps,
-                                   t + 1, loss_scale=scale)
+            _, skipped = step.step(lambda u, params: grads[u * k:(u + 1) * k], w.lr, w.beta1,
+                                   w.beta2, w.eps, t + 1, loss_scale=scale)
         if scale > 0:
             scale, good = z.zero_scale_update(scale, skipped, good, w.growth_interval)
         if not skipped:
@@ -859,10 +859,9 @@ def bench_sharded(args, rank, world_size, device_index):
     settle_device_memory()
 
     def local_only():
-        # the process's own kernels alone: the pass over its range from the
-        # W ranks' pieces (the exchanged ones, or the local grads in a group
-        # of one; stage 3: the local grads read as slices, the same bytes
-        # and arithmetic as the exchanged ones)
+        # the process's own kernels alone: the pass over its range (per
+        # unit, for stage 3) from the W ranks' pieces -- the exchanged ones,
+        # or the local grads in a group of one
         hp = (w.lr, w.beta1, w.beta2, w.eps, t + 1)
         if w.stage < 3:
             local.local_pass(step.pieces(grads), *hp, scale)
@@ -870,9 +869,7 @@ def bench_sharded(args, rank, world_size, device_index):
             return
         local.begin(scale)
         for u in reversed(range(len(units))):
-            S = units[u][1]
-            local.unit_pass(u, [grads[u][q * S:(q + 1) * S] for q in range(w.world)], *hp,
-                            scale)
+            local.unit_pass(u, step.pieces(u, grads[u * k:(u + 1) * k]), *hp, scale)
         local.finish(*hp)
 
     for _ in range(args.warmup):
@@ -928,7 +925,8 @@ def bench_sharded(args, rank, world_size, device_index):
                                        loss_scale=scale)
             else:
                 def backward(u, params):
-                    return dgrads[u].copy_(host[u], non_blocking=True)
+                    mine = range(u * k, (u + 1) * k)
+                    return [dgrads[i].copy_(host[i], non_blocking=True) for i in mine]
                 _, skipped = step.step(backward, w.lr, w.beta1, w.beta2, w.eps, t + 1,
                                        loss_scale=scale)
             out.copy_(local.params, non_blocking=True)

@@ -33,13 +33,15 @@
  *              gradient that belongs to shard r (what reduce-scatter brings to
  *              rank r).  The updated shard is cast into rank r's place of the
  *              full parameter buffer; zero_allgather() places the others.
- *   ranks r..r+k-1 (zero_init_ranks, stages 1 and 2): the k shards of
- *              ranks r to r+k-1 laid end to end (k*S floats, rank r+j's at
- *              j*S); grads[i] is the k*S-element piece [r*S, (r+k)*S) of
- *              rank i's flat gradient.  One pass steps all k shards and casts
- *              them into their places of the full buffer: what k one-rank
- *              views would do, in one launch.  k = 1 is rank r's view; r = 0,
- *              k = N holds the same state as the all-ranks view.
+ *   ranks r..r+k-1 (zero_init_ranks): the k shards of ranks r to r+k-1
+ *              laid end to end (k*S floats, rank r+j's at j*S); grads[i] is
+ *              the k*S-element piece [r*S, (r+k)*S) of rank i's flat
+ *              gradient.  One pass steps all k shards and casts them into
+ *              their places of the full buffer: what k one-rank views would
+ *              do, in one launch.  k = 1 is rank r's view; r = 0, k = N holds
+ *              the same state as the all-ranks view.  Stage 3 likewise per
+ *              unit: k*S_u floats and persistent param elements, grads of
+ *              k*S_u elements.
  *
  * Numerics (every backend path follows this exactly, element by element):
  *   acc = g_0 + g_1 + ... + g_{N-1}      (fp32, rank order, starting at g_0)
@@ -160,16 +162,20 @@ int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage,
               const int64_t *unit_numels, int32_t n_units);
 
 /* A context holding the consecutive ranks [first_rank, first_rank + n_ranks)
- * of `world` (stages 1 and 2 only): the third view above, for a process
- * that is several data-parallel ranks ("ZeRO 与 FSDP…", 从零实现 ZeRO 的
- * Adam: each rank owns shard r of S = ceil(numel/world); here one process
- * owns k of them).  zero_ctx_state_elems() is n_ranks * S; every stage 1
- * and 2 call works as in one rank's view, over that longer range (bucket
- * offsets run over [0, n_ranks*S)).  ZERO_EINVAL for stage 3, or ranks not
- * within [0, world). */
+ * of `world`: the third view above, for a process that is several
+ * data-parallel ranks ("ZeRO 与 FSDP…", 从零实现 ZeRO 的 Adam: each rank owns
+ * shard r of S = ceil(numel/world); here one process owns k of them).  The
+ * other arguments are zero_init's.  Stages 1 and 2: zero_ctx_state_elems()
+ * is n_ranks * S, and every call works as in one rank's view over that
+ * longer range (bucket offsets run over [0, n_ranks*S)).  Stage 3: unit u's
+ * state, scratch and persistent params are its n_ranks * S_u elements
+ * (zero_ctx_unit_state_offset gives where they start), and every unit call
+ * works as in one rank's view over them; the gathers still place `world`
+ * shards of S_u.  ZERO_EINVAL for ranks not within [0, world) or as
+ * zero_init. */
 int zero_init_ranks(zero_ctx **out, int64_t numel, int32_t world, int32_t stage,
                     int32_t grad_dtype, int32_t param_dtype, int32_t first_rank,
-                    int32_t n_ranks);
+                    int32_t n_ranks, const int64_t *unit_numels, int32_t n_units);
 
 /* A stage-3 context in FSDP2's per-parameter layout ("ZeRO 与 FSDP…", section
  * ZeRO-3 与 FSDP: each parameter is a DTensor sharded along dim 0, a

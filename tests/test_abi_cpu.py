@@ -124,8 +124,9 @@ def test_init_validation(z):
 
 
 def test_view_of_several_ranks(z):
-    """zero_init_ranks: ranks [r, r + k) of N, stages 1 and 2 only; the state
-    is their k shards end to end, the parameter buffer the whole vector."""
+    """zero_init_ranks: ranks [r, r + k) of N; the state is their k shards
+    end to end (per unit for stage 3), the parameter buffer the whole vector
+    (stages 1 and 2) or the view's persistent shards (stage 3)."""
     c = z.zero_init_ranks(19210, 4, 2, z.ZERO_F32, z.ZERO_F32, 1, 3)
     assert z.zero_ctx_shard_size(c, -1) == 4803
     assert z.zero_ctx_state_elems(c) == 3 * 4803
@@ -136,11 +137,19 @@ def test_view_of_several_ranks(z):
                                                     1)) == 4803
     assert z.zero_ctx_state_elems(z.zero_init_ranks(19210, 4, 2, z.ZERO_F32, z.ZERO_F32, 0,
                                                     4)) == 19212
-    for first, k, stage in ((0, 0, 2), (-1, 2, 2), (2, 3, 2), (4, 1, 2), (0, 2, 3), (0, 2, 0)):
+    for first, k, stage in ((0, 0, 2), (-1, 2, 2), (2, 3, 2), (4, 1, 2), (0, 2, 0)):
         with pytest.raises(z.ZeroError) as ei:
             z.zero_init_ranks(19210, 4, stage, z.ZERO_F32, z.ZERO_F32, first, k)
         assert ei.value.code == z.ZERO_EINVAL, (first, k, stage)
         assert z.zero_last_error()
+    # stage 3: per unit the view's k shards end to end; units are required
+    with pytest.raises(z.ZeroError):
+        z.zero_init_ranks(19210, 4, 3, z.ZERO_F32, z.ZERO_F32, 0, 2)
+    units = [10, 7, 33]                       # S_u = 3, 2, 9 over 4 ranks
+    c3 = z.zero_init_ranks(sum(units), 4, 3, z.ZERO_BF16, z.ZERO_BF16, 1, 2, units)
+    assert [z.zero_ctx_shard_size(c3, u) for u in range(3)] == [3, 2, 9]
+    assert [z.zero_ctx_unit_state_offset(c3, u) for u in range(3)] == [0, 6, 10]
+    assert z.zero_ctx_state_elems(c3) == 28 and z.zero_ctx_param_elems(c3) == 28
 
 
 def test_context_geometry(z):

@@ -213,8 +213,8 @@ def test_bench_sharded_mode_runs(extra, updated):
     """bench.py's default mode for --gpus 2 under torchrun: two gloo
     processes on this GPU, a small flat vector over the workload's 16 ranks
     (8 per process) or over 2 (one each), and the 14 ZeRO-3 units of GPT-2
-    small (one rank per process); the line reports strong scaling and every
-    step applied."""
+    small over its 8 ranks (4 per process); the line reports strong scaling
+    and every step applied."""
     import json
     import subprocess
     import sys
@@ -232,8 +232,8 @@ def test_bench_sharded_mode_runs(extra, updated):
     d = json.loads(lines[0])
     assert d["n_gpus"] == 2 and d["scaling"] == "strong" and d["value"] > 0
     if updated is None:
-        w = W.zero3_gpt2_small().replace(world=2)
-        updated = 2 * sum(w.unit_shard(u) for u in range(len(w.units)))
+        w = W.zero3_gpt2_small()               # its own 8 ranks, 4 per process
+        updated = w.world * sum(w.unit_shard(u) for u in range(len(w.units)))
     assert d["config"]["params_updated_per_step"] == updated
     assert "gloo" in d["config"]["parallelism"]
     assert 0.0 <= d["measured"]["collective_share_of_step"] <= 1.0
@@ -241,7 +241,9 @@ def test_bench_sharded_mode_runs(extra, updated):
     assert d["e2e"]["d2h_bytes_per_step"] > 0
 
 
-def _rank3(rank, world, port, units, inject_at, shadow, out_dir, prefetch=False):
+def _rank3(proc, nprocs, world, port, units, inject_at, shadow, out_dir, prefetch=False):
+    """Process `proc` of `nprocs`, holding world // nprocs consecutive ranks
+    of a ZeRO-3 step (LibraryRank3, one rank's view or a view of several)."""
     import sys
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
@@ -251,14 +253,17 @@ def _rank3(rank, world, port, units, inject_at, shadow, out_dir, prefetch=False)
     import zero_sharded_optimizer_step_gb300 as z
     from zero_sharded_optimizer_step_gb300.sharded import LibraryRank3, ShardedZero3Step
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    dist.init_process_group("gloo", rank=proc, world_size=nprocs)
     torch.cuda.set_device(0)
-    local = LibraryRank3(units, world, rank, z.ZERO_F16, z.ZERO_F16, "cuda:0", shadow=shadow)
+    k = world // nprocs
+    first = proc * k
+    local = LibraryRank3(units, world, first, z.ZERO_F16, z.ZERO_F16, "cuda:0", shadow=shadow,
+                         n_ranks=k)
     for u, (nu, S) in enumerate(zip(units, local.shards)):
-        nv = max(0, min(S, nu - rank * S))
-        x = np.zeros(S, np.float32)
+        nv = max(0, min(k * S, nu - first * S))
+        x = np.zeros(k * S, np.float32)
         x[:nv] = synth.fill_host(nv, synth.F32, synth.key(0, synth.KIND_MASTER, 0, 0, u), 0.01,
-                                 index0=rank * S)
+                                 index0=first * S)
         local.set_master(u, torch.from_numpy(x).cuda())
     step = ShardedZero3Step(local, prefetch=prefetch)
     scale, good, t, skips, gathered = 2.0 ** 12, 0, 0, [], {}
@@ -269,12 +274,16 @@ def _rank3(rank, world, port, units, inject_at, shadow, out_dir, prefetch=False)
         def backward(u, params):
             gathered[u] = params.cpu().view(torch.int16).numpy().view(np.uint16).copy()
             nu, S = units[u], local.shards[u]
-            g = np.zeros(S * world, np.uint16)
-            g[:nu] = synth.fill_host(nu, synth.F16, synth.key(0, synth.KIND_GRAD, it, rank, u),
-                                     1e-3 * scale)
-            if inject_at and (it, rank, u) == inject_at[:3]:
-                g[inject_at[3]] = 0x7C00                  # +inf in fp16
-            return torch.from_numpy(g.view(np.int16)).cuda().view(torch.float16)
+            out = []
+            for c in range(k):
+                r = first + c
+                g = np.zeros(S * world, np.uint16)
+                g[:nu] = synth.fill_host(nu, synth.F16, synth.key(0, synth.KIND_GRAD, it, r, u),
+                                         1e-3 * scale)
+                if inject_at and (it, r, u) == inject_at[:3]:
+                    g[inject_at[3]] = 0x7C00              # +inf in fp16
+                out.append(torch.from_numpy(g.view(np.int16)).cuda().view(torch.float16))
+            return out if k > 1 else out[0]
         _, skipped = step.step(backward, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale,
                                forward=forward)
         skips.append(skipped)
@@ -283,34 +292,42 @@ def _rank3(rank, world, port, units, inject_at, shadow, out_dir, prefetch=False)
         scale, good = oracle.scale_update(scale, skipped, good, 2000)
     torch.cuda.synchronize()
     cx, cm, cv = (a.cpu().numpy() for a in local.state())
-    out = {"skips": np.array(skips)}
-    for u in range(len(units)):
-        o, S = local.offsets[u], local.shards[u]
-        out["x%d" % u], out["m%d" % u], out["v%d" % u] = cx[o:o + S], cm[o:o + S], cv[o:o + S]
-        out["lp%d" % u] = local.own_params(u).cpu().view(torch.int16).numpy().view(np.uint16)
-        out["full%d" % u] = gathered[u]
-    np.savez(os.path.join(out_dir, "rank%d.npz" % rank), **out)
+    for j in range(k):
+        out = {"skips": np.array(skips)}
+        for u in range(len(units)):
+            S = local.shards[u]
+            o = local.offsets[u] + j * S
+            out["x%d" % u], out["m%d" % u], out["v%d" % u] = cx[o:o + S], cm[o:o + S], cv[o:o + S]
+            lp = local.own_params(u).cpu().view(torch.int16).numpy().view(np.uint16)
+            out["lp%d" % u] = lp[j * S:(j + 1) * S]
+            out["full%d" % u] = gathered[u]
+        np.savez(os.path.join(out_dir, "rank%d.npz" % (first + j)), **out)
     local.close()
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("inject_at,shadow,prefetch", [
-    (None, True, False),
-    ((2, 1, 0, 1400), True, False),    # (iteration, rank, unit, element)
-    ((2, 0, 2, 4001), False, False),   # rank 0's element in rank 1's shard of unit 2
-    ((2, 1, 0, 1400), True, True),     # the next unit's gather in flight
-    (None, False, True),
+@pytest.mark.parametrize("nprocs,world,inject_at,shadow,prefetch", [
+    (2, 2, None, True, False),
+    (2, 2, (2, 1, 0, 1400), True, False),    # (iteration, rank, unit, element)
+    (2, 2, (2, 0, 2, 4001), False, False),   # rank 0's element in rank 1's shard of unit 2
+    (2, 2, (2, 1, 0, 1400), True, True),     # the next unit's gather in flight
+    (2, 2, None, False, True),
+    (1, 4, (2, 3, 2, 11), True, False),      # every rank in one process: the library gathers
+    (1, 4, (2, 1, 0, 1400), False, True),
+    (2, 4, (2, 3, 2, 11), True, True),       # two ranks in each of two processes
+    (1, 3, (2, 2, 1, 16), True, False),      # padding in every unit
 ])
-def test_sharded_zero3_through_the_library(tmp_path, inject_at, shadow, prefetch):
-    """ZeRO-3 with one process per rank (ShardedZero3Step, LibraryRank3):
-    per unit an all-gather before forward and backward, the unit's grads
+def test_sharded_zero3_through_the_library(tmp_path, nprocs, world, inject_at, shadow, prefetch):
+    """ZeRO-3 across processes (ShardedZero3Step over LibraryRank3), one rank
+    or several per process: per unit an all-gather before forward and
+    backward (with one process, the library's placement), the unit's grads
     exchanged after its backward and stepped, every unit's verdict combined
     -- bit-identical to the oracle's all-ranks step of every unit."""
     from tests.test_multiprocess_gloo import _stage3_reference
-    world, units = 2, [3001, 17, 5000]
+    units = [3001, 17, 5000]
     port = _free_port()
-    mp.start_processes(_rank3, args=(world, port, units, inject_at, shadow, str(tmp_path),
-                                     prefetch), nprocs=world, join=True, start_method="spawn")
+    mp.start_processes(_rank3, args=(nprocs, world, port, units, inject_at, shadow, str(tmp_path),
+                                     prefetch), nprocs=nprocs, join=True, start_method="spawn")
     import oracle
     st, fulls, skips = _stage3_reference(units, world, inject_at)
     assert skips == [bool(inject_at) and it == 2 for it in (1, 2, 3)]
@@ -371,9 +388,18 @@ def _nccl_one_rank(index, port, out_dir):
     def backward(u, params):
         seen[u] = params.cpu().view(torch.int16).numpy().view(np.uint16).copy()
         return g3[u]
+    # in a group of one the stage-3 step places with the library's gather
     verdict3 = ShardedZero3Step(l3, prefetch=True).step(backward, 1e-3, 0.9, 0.999, 1e-8, 1)
     torch.cuda.synchronize()
     x3, m3, v3 = (a.cpu().numpy() for a in l3.state())
+    # the asynchronous all-gather (the prefetch's collective across
+    # processes) through NCCL: unit 2's shard into a buffer of its own
+    from zero_sharded_optimizer_step_gb300.sharded import gather_params
+    agb = torch.zeros_like(l3.own_params(2))
+    pending = gather_params(agb, l3.own_params(2), async_op=True)
+    pending.wait()
+    torch.cuda.synchronize()
+    async_ok = torch.equal(agb, l3.own_params(2))
     # the bucketed form (the split-size all-to-all) over NCCL: the same step
     # as above from a fresh rank, in buckets of 30,001
     lb = LibraryRank(numel, 1, 0, z.ZERO_BF16, z.ZERO_BF16, "cuda:0", shadow=True)
@@ -389,7 +415,8 @@ def _nccl_one_rank(index, port, out_dir):
     np.savez(os.path.join(out_dir, "nccl.npz"), x=x, m=m, v=v, p=p, verdict=np.array(verdict),
              xb=xb, pb=pb, verdict_b=np.array(verdict_b),
              x3=x3, p3=l3.params.cpu().view(torch.int16).numpy().view(np.uint16),
-             verdict3=np.array(verdict3), **{"seen%d" % u: s for u, s in seen.items()})
+             verdict3=np.array(verdict3), async_ok=np.array(async_ok),
+             **{"seen%d" % u: s for u, s in seen.items()})
     local.close()
     l3.close()
     lb.close()
@@ -398,8 +425,10 @@ def _nccl_one_rank(index, port, out_dir):
 
 def test_sharded_steps_over_a_one_rank_nccl_group(tmp_path):
     """ShardedStep (whole and bucketed) and ShardedZero3Step (prefetching)
-    over a real NCCL group of one rank: the result is the oracle's (one rank:
-    the step on the whole vector)."""
+    in a real NCCL group of one rank: the result is the oracle's (one rank:
+    the step on the whole vector).  ShardedStep's collectives and the
+    asynchronous all-gather run through NCCL; the stage-3 step of a group of
+    one places with the library."""
     mp.start_processes(_nccl_one_rank, args=(_free_port(), str(tmp_path)), nprocs=1, join=True,
                        start_method="spawn")
     import oracle
@@ -434,6 +463,7 @@ def test_sharded_steps_over_a_one_rank_nccl_group(tmp_path):
     assert tuple(d["verdict3"]) == (False, False)
     assert d["x3"].tobytes() == np.concatenate(xs).tobytes()
     assert d["p3"].tobytes() == np.concatenate(ps).tobytes()
+    assert bool(d["async_ok"])
 
 
 def test_sharded_step_with_decoupled_weight_decay(tmp_path):

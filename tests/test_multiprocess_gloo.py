@@ -412,6 +412,101 @@ def _rank_main3(rank, world, port, units, inject_at, out_dir, prefetch=False):
     dist.destroy_process_group()
 
 
+class OracleRanks3:
+    """The view of k consecutive ranks of a stage-3 step (the members
+    ShardedZero3Step drives, as LibraryRank3(n_ranks=k) has them), each
+    rank's arithmetic the oracle's (OracleRank3): per unit the k ranks'
+    param shards end to end in one tensor, one flag word for all; with every
+    rank held, `place` is the gather."""
+
+    def __init__(self, units, world, first, k):
+        self.n_ranks, self.rank, self.world = k, first, world
+        self.subs = [OracleRank3(units, world, first + j) for j in range(k)]
+        self.shards = self.subs[0].shards
+        self.flag = torch.zeros(1, dtype=torch.int64)
+        self.lp = []
+        for u, S in enumerate(self.shards):
+            joined = torch.cat([s.lp[u] for s in self.subs])
+            self.lp.append(joined)
+            for j, s in enumerate(self.subs):
+                s.lp[u] = joined[j * S:(j + 1) * S]      # each rank writes its part in place
+        for s in self.subs:
+            s.flag = self.flag
+
+    def grad_buffer(self, n):
+        return torch.zeros(n, dtype=torch.int16)
+
+    def param_buffer(self, n):
+        return torch.zeros(n, dtype=torch.int16)
+
+    def own_params(self, u):
+        return self.lp[u]
+
+    def place(self, u, full):
+        assert self.n_ranks == self.world
+        full.copy_(self.lp[u])
+
+    def begin(self, loss_scale):
+        for s in self.subs:
+            s.begin(loss_scale)
+
+    def unit_pass(self, u, pieces, lr, beta1, beta2, eps, t, loss_scale):
+        S = self.shards[u]
+        for j, s in enumerate(self.subs):
+            s.unit_pass(u, [pc[j * S:(j + 1) * S] for pc in pieces], lr, beta1, beta2, eps, t,
+                        loss_scale)
+
+    def finish(self, lr, beta1, beta2, eps, t):
+        for s in self.subs:
+            s.finish(lr, beta1, beta2, eps, t)
+
+    def status(self):
+        return self.subs[0].status()
+
+
+def _ranks_main3(proc, nprocs, port, world, units, inject_at, out_dir, prefetch):
+    """Process `proc` of `nprocs` holding world // nprocs consecutive ranks of
+    a ZeRO-3 step (ShardedZero3Step over a view of several ranks)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import oracle
+    import synth
+    from zero_sharded_optimizer_step_gb300.sharded import ShardedZero3Step
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=proc, world_size=nprocs)
+    k = world // nprocs
+    view = OracleRanks3(units, world, proc * k, k)
+    step = ShardedZero3Step(view, prefetch=prefetch)
+    scale, good, t, skips, gathered = 2.0 ** 12, 0, 0, [], {}
+    for it in (1, 2, 3):
+        def backward(u, params):
+            gathered[u] = params.numpy().view(np.uint16).copy()
+            nu, S = units[u], view.shards[u]
+            out = []
+            for c in range(k):
+                r = proc * k + c
+                g = np.zeros(S * world, np.uint16)
+                g[:nu] = synth.fill_host(nu, synth.F16, synth.key(0, synth.KIND_GRAD, it, r, u),
+                                         1e-3 * scale)
+                if inject_at and (it, r, u) == inject_at[:3]:
+                    g[inject_at[3]] = 0x7C00
+                out.append(torch.from_numpy(g.view(np.int16)))
+            return out
+        _, skipped = step.step(backward, 1e-3, 0.9, 0.999, 1e-8, t + 1, loss_scale=scale)
+        skips.append(skipped)
+        if not skipped:
+            t += 1
+        scale, good = oracle.scale_update(scale, skipped, good, 2000)
+    for j, s in enumerate(view.subs):
+        out = {"skips": np.array(skips)}
+        for u in range(len(units)):
+            out["x%d" % u], out["m%d" % u], out["v%d" % u] = s.state[u]
+            out["lp%d" % u] = s.lp[u].numpy().view(np.uint16)
+            out["full%d" % u] = gathered[u]
+        np.savez(os.path.join(out_dir, "rank%d.npz" % (proc * k + j)), **out)
+    dist.destroy_process_group()
+
+
 def _stage3_reference(units, world, inject_at):
     """All ranks in one process: per unit the oracle's all-ranks step on the
     unit's own flat vector; a step counts only if no unit overflowed."""
@@ -474,6 +569,36 @@ def test_stage3_ranks_with_real_collectives(tmp_path, world, units, inject_at, p
             # the last gather (before unit u's backward) placed the shards
             # every rank held then, which the third step has since updated
         # every rank saw the same gathered units
+        if r == 0:
+            first = {u: d["full%d" % u].copy() for u in range(len(units))}
+        else:
+            for u in range(len(units)):
+                assert d["full%d" % u].tobytes() == first[u].tobytes()
+
+
+@pytest.mark.parametrize("nprocs,world,units,inject_at,prefetch", [
+    (1, 4, [3001, 17, 5000], (2, 3, 2, 11), False),    # every rank in one process
+    (2, 4, [3001, 17, 5000], (2, 3, 2, 11), False),    # two ranks per process
+    (2, 4, [3001, 17, 5000, 64], (2, 1, 0, 1400), True),
+    (1, 3, [3001, 17, 5000], (2, 2, 1, 16), True),     # padding in every unit
+])
+def test_stage3_ranks_per_process(tmp_path, nprocs, world, units, inject_at, prefetch):
+    port = _free_port()
+    mp.start_processes(_ranks_main3, args=(nprocs, port, world, units, inject_at, str(tmp_path),
+                                           prefetch), nprocs=nprocs, join=True,
+                       start_method="spawn")
+    import oracle
+    st, fulls, skips = _stage3_reference(units, world, inject_at)
+    assert skips == [bool(inject_at) and it == 2 for it in (1, 2, 3)]
+    for r in range(world):
+        d = np.load(os.path.join(tmp_path, "rank%d.npz" % r))
+        assert list(d["skips"]) == skips, r
+        for u, nu in enumerate(units):
+            S = oracle.shard_size(nu, world)
+            sl = slice(r * S, (r + 1) * S)
+            for name, a in zip("xmv", st[u]):
+                assert d["%s%d" % (name, u)].tobytes() == a[sl].tobytes(), (r, u, name)
+            assert d["lp%d" % u].tobytes() == fulls[u][sl].tobytes()
         if r == 0:
             first = {u: d["full%d" % u].copy() for u in range(len(units))}
         else:

@@ -47,7 +47,7 @@ _SIGS = {
     "zero_init": (ctypes.c_int, [ctypes.POINTER(_ctxp), _i64, _i32, _i32, _i32, _i32, _i32,
                                  ctypes.POINTER(_i64), _i32]),
     "zero_init_ranks": (ctypes.c_int, [ctypes.POINTER(_ctxp), _i64, _i32, _i32, _i32, _i32,
-                                       _i32, _i32]),
+                                       _i32, _i32, ctypes.POINTER(_i64), _i32]),
     "zero_init_dim0": (ctypes.c_int, [ctypes.POINTER(_ctxp), _i32, _i32, _i32, _i32,
                                       ctypes.POINTER(_i64), ctypes.POINTER(_i64), _i32]),
     "zero_destroy": (ctypes.c_int, [_ctxp]),
@@ -212,11 +212,17 @@ def zero_init(numel: int, world: int, stage: int, grad_dtype: int, param_dtype: 
 
 
 def zero_init_ranks(numel: int, world: int, stage: int, grad_dtype: int, param_dtype: int,
-                    first_rank: int, n_ranks: int) -> Ctx:
-    """Stages 1, 2: a view of ranks [first_rank, first_rank + n_ranks)."""
+                    first_rank: int, n_ranks: int, unit_numels=None) -> Ctx:
+    """A view of ranks [first_rank, first_rank + n_ranks) (stage 3: of each
+    unit)."""
     h = _ctxp()
+    units = None
+    n_units = 0
+    if unit_numels is not None:
+        n_units = len(unit_numels)
+        units = (_i64 * n_units)(*unit_numels)
     _check(_L.zero_init_ranks(ctypes.byref(h), numel, world, stage, grad_dtype, param_dtype,
-                              first_rank, n_ranks))
+                              first_rank, n_ranks, units, n_units))
     return Ctx(h.value)
 
 

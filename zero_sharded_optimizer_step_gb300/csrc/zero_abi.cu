@@ -223,8 +223,9 @@ Range unit_range(const zero_ctx *c, int32_t u)
         r.n = Su * c->world;
         r.n_valid = c->unit_numel[u];
     } else {
-        r.n = Su;
-        r.n_valid = std::max<int64_t>(0, std::min<int64_t>(Su, c->unit_numel[u] - (int64_t)c->rank * Su));
+        // the view's consecutive shards of the unit
+        r.n = Su * c->nranks;
+        r.n_valid = std::max<int64_t>(0, std::min<int64_t>(r.n, c->unit_numel[u] - (int64_t)c->rank * Su));
     }
     r.params = static_cast<char *>(c->params) + r.state_off * es_p;
     return r;
@@ -435,7 +436,7 @@ int init_units(zero_ctx *c, const int64_t *numel, const int64_t *shard, int32_t 
         c->unit_numel.push_back(nu);
         c->unit_S.push_back(su);
         c->unit_state_off.push_back(off);
-        off += c->rank < 0 ? su * c->world : su;
+        off += c->rank < 0 ? su * c->world : su * c->nranks;
         sum += nu;
         if (sum > kLimit || off > kLimit) return fail(ZERO_EINVAL, "units too large");
     }
@@ -504,8 +505,10 @@ const char *zero_strerror(int code)
 
 const char *zero_last_error(void) { return g_last_error.c_str(); }
 
-int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage, int32_t grad_dtype,
-              int32_t param_dtype, int32_t rank, const int64_t *unit_numels, int32_t n_units)
+// A context of `nranks` consecutive ranks from `rank` (rank -1: all of them).
+static int init_ctx(zero_ctx **out, int64_t numel, int32_t world, int32_t stage,
+                    int32_t grad_dtype, int32_t param_dtype, int32_t rank, int32_t nranks,
+                    const int64_t *unit_numels, int32_t n_units)
 {
     if (!out) return fail(ZERO_EINVAL, "out is null");
     *out = nullptr;
@@ -523,6 +526,7 @@ int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage, int32
     c->gdt = grad_dtype;
     c->pdt = param_dtype;
     c->rank = rank;
+    c->nranks = rank < 0 ? world : nranks;
     if (stage < 3) {
         if (unit_numels || n_units) {
             delete c;
@@ -535,7 +539,7 @@ int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage, int32
         c->numel = numel;
         c->S = ceil_div(numel, world);
         c->P = c->S * world;
-        c->state_elems = rank < 0 ? c->P : c->S;
+        c->state_elems = rank < 0 ? c->P : c->S * nranks;
         c->param_elems = c->P;
     } else {
         if (!unit_numels || n_units < 1) {
@@ -555,26 +559,26 @@ int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage, int32
     return ZERO_OK;
 }
 
+int zero_init(zero_ctx **out, int64_t numel, int32_t world, int32_t stage, int32_t grad_dtype,
+              int32_t param_dtype, int32_t rank, const int64_t *unit_numels, int32_t n_units)
+{
+    return init_ctx(out, numel, world, stage, grad_dtype, param_dtype, rank, 1, unit_numels,
+                    n_units);
+}
+
 int zero_init_ranks(zero_ctx **out, int64_t numel, int32_t world, int32_t stage,
                     int32_t grad_dtype, int32_t param_dtype, int32_t first_rank,
-                    int32_t n_ranks)
+                    int32_t n_ranks, const int64_t *unit_numels, int32_t n_units)
 {
     if (!out) return fail(ZERO_EINVAL, "out is null");
     *out = nullptr;
-    if (stage != 1 && stage != 2)
-        return fail(ZERO_EINVAL, "a view of several ranks is for stages 1 and 2 (got %d)", stage);
     if (world < 1 || world > ZERO_MAX_RANKS)
         return fail(ZERO_EINVAL, "world must be in [1, %d] (got %d)", ZERO_MAX_RANKS, world);
     if (first_rank < 0 || n_ranks < 1 || n_ranks > world - first_rank)
         return fail(ZERO_EINVAL, "ranks [%d, %d + %d) are not within [0, %d)", first_rank,
                     first_rank, n_ranks, world);
-    zero_ctx *c = nullptr;
-    int rc = zero_init(&c, numel, world, stage, grad_dtype, param_dtype, first_rank, nullptr, 0);
-    if (rc) return rc;
-    c->nranks = n_ranks;
-    c->state_elems = c->S * n_ranks;
-    *out = c;
-    return ZERO_OK;
+    return init_ctx(out, numel, world, stage, grad_dtype, param_dtype, first_rank, n_ranks,
+                    unit_numels, n_units);
 }
 
 int zero_init_dim0(zero_ctx **out, int32_t world, int32_t grad_dtype, int32_t param_dtype,

@@ -335,21 +335,26 @@ class ShardedStep:
 
 
 class LibraryRank3:
-    """Rank `rank`'s own part of a stage-3 step in libzero.so's one-rank view:
-    per unit u a shard of S_u = ceil(numel_u / N) elements of fp32 state and
-    of low-precision params (the persistent shards, unit after unit), owned
-    here with the flag word.  Loss-scaled steps update every unit in one pass
-    into a second state set (`shadow`, the default; the finalize after the
-    last unit keeps or discards all of them) or reduce every unit into the
-    fp32 scratch and apply once."""
+    """Rank `rank`'s own part of a stage-3 step in libzero.so's one-rank view
+    -- or, with n_ranks = k > 1, that of the k consecutive ranks rank ..
+    rank + k - 1 one process holds, in the library's view of several ranks:
+    per unit u the view's k shards of S_u = ceil(numel_u / N) elements of
+    fp32 state and of low-precision params (the persistent shards, unit
+    after unit), owned here with the flag word.  Loss-scaled steps update
+    every unit in one pass into a second state set (`shadow`, the default;
+    the finalize after the last unit keeps or discards all of them) or
+    reduce every unit into the fp32 scratch and apply once."""
 
     def __init__(self, unit_numels, world: int, rank: int, grad_dtype: int, param_dtype: int,
-                 device, shadow: bool = True, weight_decay: float = 0.0):
+                 device, shadow: bool = True, weight_decay: float = 0.0, n_ranks: int = 1):
         self.device = torch.device(device)
         self.grad_dtype, self.param_dtype = grad_dtype, param_dtype
         self.units = list(unit_numels)
-        self.ctx = z.zero_init(sum(self.units), world, 3, grad_dtype, param_dtype, rank,
-                               self.units)
+        self.world, self.rank, self.n_ranks = world, rank, n_ranks
+        self.ctx = (z.zero_init(sum(self.units), world, 3, grad_dtype, param_dtype, rank,
+                                self.units) if n_ranks == 1 else
+                    z.zero_init_ranks(sum(self.units), world, 3, grad_dtype, param_dtype, rank,
+                                      n_ranks, self.units))
         self.shards = [z.zero_ctx_shard_size(self.ctx, u) for u in range(len(self.units))]
         self.offsets = [z.zero_ctx_unit_state_offset(self.ctx, u) for u in range(len(self.units))]
         n = z.zero_ctx_state_elems(self.ctx)
@@ -381,15 +386,26 @@ class LibraryRank3:
         return torch.zeros(n, dtype=_TORCH[self.param_dtype], device=self.device)
 
     def own_params(self, u: int) -> torch.Tensor:
-        return self.params[self.offsets[u]:self.offsets[u] + self.shards[u]]
+        """Unit u's persistent params of this view (its k shards)."""
+        return self.params[self.offsets[u]:self.offsets[u] + self.shards[u] * self.n_ranks]
 
     def set_master(self, u: int, x: torch.Tensor | None = None) -> None:
-        """Unit u's initial fp32 shard (x, or the master as it stands); its
+        """Unit u's initial fp32 shards (x, or the master as it stands); their
         params become their cast (a casting copy: no temporary)."""
-        view = self.master[self.offsets[u]:self.offsets[u] + self.shards[u]]
+        view = self.master[self.offsets[u]:self.offsets[u] + self.shards[u] * self.n_ranks]
         if x is not None:
             view.copy_(x)
         self.own_params(u).copy_(view)
+
+    def place(self, u: int, full: torch.Tensor, stream=None) -> None:
+        """Unit u's gather when this view holds every rank (one process): the
+        library places the N persistent shards into `full`."""
+        if self.n_ranks != self.world:
+            raise ValueError("the view holds %d of %d ranks: the gather needs the others'"
+                             % (self.n_ranks, self.world))
+        S, own = self.shards[u], self.own_params(u)
+        z.zero3_gather_unit(self.ctx, u, [own[k * S:(k + 1) * S] for k in range(self.world)],
+                            full, stream)
 
     def begin(self, loss_scale) -> None:
         self._scaled = loss_scale > 0
@@ -420,22 +436,27 @@ class LibraryRank3:
 
 
 class ShardedZero3Step:
-    """One ZeRO-3 step of this process's rank ("ZeRO 与 FSDP…", section ZeRO-3
-    与 FSDP): in the forward every unit's shards are all-gathered into a unit
-    buffer before the unit's forward runs; in the backward, last unit first,
-    the unit is gathered again, its backward runs, its grads are exchanged
-    (the all-to-all of slices) and its local pass follows; after the last
-    unit the flag word is combined over the ranks (MAX) -- every unit's
-    verdict is in -- and the rest of the step runs (the finalize over two
-    state sets, or the apply from the scratch).
+    """One ZeRO-3 step of this process's ranks ("ZeRO 与 FSDP…", section
+    ZeRO-3 与 FSDP): in the forward every unit's shards are all-gathered into
+    a unit buffer before the unit's forward runs; in the backward, last unit
+    first, the unit is gathered again, its backward runs, its grads are
+    exchanged (the all-to-all of slices) and its local pass follows; after
+    the last unit the flag word is combined over the processes (MAX) --
+    every unit's verdict is in -- and the rest of the step runs (the
+    finalize over two state sets, or the apply from the scratch).
 
-    `local` does the rank's arithmetic: a LibraryRank3, or any object with
-    the same members (shards, grad_buffer, param_buffer, own_params, begin,
-    unit_pass, finish, status, flag).  The caller's model enters through
-    `forward(u, params)`, called after unit u's forward gather, and
-    `backward(u, params)`, called after its backward gather, which returns
-    this rank's local grads of unit u (N * S_u elements, zeros past the
-    unit's end).  A hook must be done with its unit buffer when it returns.
+    `local` does the process's arithmetic: a LibraryRank3 of one rank, or of
+    k = local.n_ranks consecutive ranks p*k .. p*k + k - 1 (W = k*N ranks in
+    all), or any object with the same members (shards, n_ranks, rank,
+    grad_buffer, param_buffer, own_params, place, begin, unit_pass, finish,
+    status, flag).  The caller's model enters through `forward(u, params)`,
+    called after unit u's forward gather, and `backward(u, params)`, called
+    after its backward gather, which returns the process's local grads of
+    unit u: one tensor of W * S_u elements per held rank (a list of k, or
+    the tensor itself when k = 1; zeros past the unit's end).  A hook must
+    be done with its unit buffer when it returns.  With one process (N = 1)
+    the view holds every rank: the gathers are the library's placement of
+    the persistent shards and nothing is exchanged.
 
     prefetch=True gathers ahead ("ZeRO 与 FSDP…", ZeRO-3 与 FSDP: the next
     unit's all-gather is issued before this unit computes, so the two
@@ -446,23 +467,32 @@ class ShardedZero3Step:
     def __init__(self, local, group=None, prefetch: bool = False):
         self.local = local
         self.group = group
-        self.world = dist.get_world_size(group)
+        self.N = dist.get_world_size(group)
+        self.p = dist.get_rank(group)
+        self.k = getattr(local, "n_ranks", 1)
+        self.world = self.W = self.k * self.N
+        if getattr(local, "rank", self.p * self.k) != self.p * self.k:
+            raise ValueError("process %d must hold ranks from %d" % (self.p, self.p * self.k))
         self.prefetch = prefetch
-        longest = max(local.shards) * self.world
+        longest = max(local.shards) * self.W
         self.fulls = [local.param_buffer(longest) for _ in range(2 if prefetch else 1)]
         self.full = self.fulls[0]
-        self.recv = local.grad_buffer(longest)
+        self.recv = ([local.grad_buffer(longest) for _ in range(self.k)] if self.N > 1
+                     else None)
 
     def _issue(self, u: int, buf: int, async_op: bool):
         """Start (or, without async_op, do) unit u's all-gather into unit
         buffer `buf`; returns (view, pending or None)."""
-        n = self.local.shards[u] * self.world
+        n = self.local.shards[u] * self.W
         view = self.fulls[buf][:n]
         pending = None
         if n:
             with _Range("zero3: gather %d" % u):
-                pending = gather_params(view, self.local.own_params(u), self.group,
-                                        async_op=async_op)
+                if self.N == 1:
+                    self.local.place(u, view)         # in stream order: nothing pending
+                else:
+                    pending = gather_params(view, self.local.own_params(u), self.group,
+                                            async_op=async_op)
         return view, pending
 
     def unit_params(self, u: int) -> torch.Tensor:
@@ -486,8 +516,21 @@ class ShardedZero3Step:
                 ahead = self._issue(order[j + 1], (j + 1) % 2, True)
             yield u, view
 
+    def pieces(self, u: int, grads):
+        """The W ranks' grads of unit u over this process's range (k * S_u
+        elements each), in rank order: views into the receive buffers, or
+        into the local grads with one process."""
+        K = self.local.shards[u] * self.k
+        if self.N == 1:
+            return [g[:K] for g in grads]
+        out = []
+        for i in range(self.W):
+            q, c = divmod(i, self.k)
+            out.append(self.recv[c][q * K:(q + 1) * K])
+        return out
+
     def step(self, backward, lr, beta1, beta2, eps, t, loss_scale=0.0, forward=None):
-        """Returns (nonfinite, skipped); every rank returns the same."""
+        """Returns (nonfinite, skipped); every process returns the same."""
         local = self.local
         U = len(local.shards)
         local.begin(loss_scale)
@@ -496,16 +539,20 @@ class ShardedZero3Step:
                 forward(u, params)
         for u, params in self._visits(list(reversed(range(U)))):
             grads = backward(u, params)
-            S = local.shards[u]
-            n = S * self.world
-            with _Range("zero3: exchange %d" % u):
-                if n:
-                    exchange_slices(self.recv[:n], grads, self.group)
-            slices = [self.recv[k * S:(k + 1) * S] for k in range(self.world)]
+            if isinstance(grads, torch.Tensor):
+                grads = [grads]
+            if len(grads) != self.k:
+                raise ValueError("unit %d: %d grads for %d held ranks" % (u, len(grads), self.k))
+            n = local.shards[u] * self.W
+            if self.N > 1 and n:
+                with _Range("zero3: exchange %d" % u):
+                    for c in range(self.k):
+                        exchange_slices(self.recv[c][:n], grads[c], self.group)
             with _Range("zero3: local pass %d" % u):
-                local.unit_pass(u, slices, lr, beta1, beta2, eps, t, loss_scale)
+                local.unit_pass(u, self.pieces(u, grads), lr, beta1, beta2, eps, t, loss_scale)
         with _Range("zero3: verdict"):
-            combine_flag(local.flag, self.group)
+            if self.N > 1:
+                combine_flag(local.flag, self.group)
             local.finish(lr, beta1, beta2, eps, t)
             return local.status()
 
