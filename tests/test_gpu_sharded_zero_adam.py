@@ -267,3 +267,99 @@ def test_sharded_zero_adam_resumes_from_its_state(bucket_elems):
         assert d["ax"].tobytes() == d["bx"].tobytes()
         assert int(d["ta"]) == int(d["tb"]) == 4 and float(d["sa"]) == float(d["sb"])
     assert ranks[0]["a"].tobytes() == ranks[1]["a"].tobytes()
+
+
+def _mlp(dev, seed):
+    torch.manual_seed(seed)
+    return torch.nn.Sequential(torch.nn.Linear(64, 256), torch.nn.GELU(),
+                               torch.nn.Linear(256, 10)).to(dev)
+
+
+def _train_steps(model, opt, rank, world, its, dev):
+    """The pages' data-parallel step: every rank the same global batch,
+    its own slice of it; returns this rank's local grads of each step."""
+    loss_fn = torch.nn.CrossEntropyLoss()
+    grads = []
+    for it in its:
+        gen = torch.Generator().manual_seed(500 + it)
+        x = torch.randn(4 * PER_RANK, 64, generator=gen).to(dev)
+        y = torch.randint(0, 10, (4 * PER_RANK,), generator=gen).to(dev)
+        per = 4 * PER_RANK // world
+        sl = slice(rank * per, (rank + 1) * per)
+        opt.zero_grad()
+        loss_fn(model(x[sl]), y[sl]).backward()
+        grads.append(torch.cat([p.grad.reshape(-1) for p in model.parameters()]).cpu().numpy())
+        assert opt.step() is False
+    return grads
+
+
+def _rank_reshard(rank, world, port, out_dir, phase):
+    """Phase "save": two ranks train two steps and save their shards.  Phase
+    "resume": four ranks start from other weights, load the two-rank
+    checkpoint resharded for four, and train two more steps."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import zero_sharded_optimizer_step_gb300 as z
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    if phase == "save":
+        model = _mlp(dev, 0)
+        opt = z.ShardedZeroAdam(model.parameters(), lr=LR, betas=(0.9, 0.999), eps=1e-8)
+        _train_steps(model, opt, rank, world, [0, 1], dev)
+        sd = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in opt.state_dict().items()}
+        torch.save(sd, os.path.join(out_dir, "ckpt%d.pt" % rank))
+        np.save(os.path.join(out_dir, "saved_params%d.npy" % rank), _flat(model.parameters()))
+    else:
+        model = _mlp(dev, 1)                    # other weights: all must come from the checkpoint
+        opt = z.ShardedZeroAdam(model.parameters(), lr=LR, betas=(0.9, 0.999), eps=1e-8)
+        full = z.consolidate_state([torch.load(os.path.join(out_dir, "ckpt%d.pt" % r))
+                                    for r in range(2)])
+        opt.load_state_dict(z.shard_state(full, world, rank))
+        loaded = _flat(model.parameters())
+        grads = _train_steps(model, opt, rank, world, [2, 3], dev)
+        np.savez(os.path.join(out_dir, "resume%d.npz" % rank), loaded=loaded,
+                 grads=np.stack(grads), final=_flat(model.parameters()),
+                 master=opt.state()[0].cpu().numpy(), t=opt.t)
+    opt.close()
+    dist.destroy_process_group()
+
+
+def test_checkpoint_resumes_on_another_rank_count(tmp_path):
+    """A two-rank checkpoint, consolidated and resharded, resumes on four
+    ranks: every rank's parameters come back as saved, and the next two
+    steps equal, bit for bit, the oracle's all-ranks steps from the
+    consolidated state on the four ranks' gradients."""
+    import oracle
+
+    import zero_sharded_optimizer_step_gb300 as z
+    for world, phase in ((2, "save"), (4, "resume")):
+        mp.start_processes(_rank_reshard, args=(world, _free_port(), str(tmp_path), phase),
+                           nprocs=world, join=True, start_method="spawn")
+    saved = np.load(os.path.join(tmp_path, "saved_params0.npy"))
+    assert saved.tobytes() == np.load(os.path.join(tmp_path, "saved_params1.npy")).tobytes()
+    ranks = [np.load(os.path.join(tmp_path, "resume%d.npz" % r)) for r in range(4)]
+    for d in ranks:
+        assert d["loaded"].tobytes() == saved.tobytes()
+    full = z.consolidate_state([torch.load(os.path.join(tmp_path, "ckpt%d.pt" % r))
+                                for r in range(2)])
+    numel = full["numel"]
+    S = oracle.shard_size(numel, 4)
+    P = 4 * S
+    x, m, v = (np.zeros(P, np.float32) for _ in range(3))
+    x[:numel], m[:numel], v[:numel] = (full[k].numpy() for k in ("master", "m", "v"))
+    params = np.zeros(P, np.float32)
+    t = full["t"]
+    assert t == 2
+    for j in range(2):
+        g = [np.ascontiguousarray(d["grads"][j], np.float32) for d in ranks]
+        oracle.zero_step(g, oracle.F32, numel, x, m, v, params, oracle.F32, LR, 0.9, 0.999,
+                         1e-8, t + 1)
+        t += 1
+    for r, d in enumerate(ranks):
+        assert int(d["t"]) == 4
+        assert d["final"].tobytes() == params[:numel].tobytes(), r
+        assert d["master"].tobytes() == x[r * S:(r + 1) * S].tobytes(), r

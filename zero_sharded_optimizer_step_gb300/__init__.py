@@ -25,4 +25,7 @@ def __getattr__(name):
     if name == "ShardedZeroAdam":
         from .optim import ShardedZeroAdam
         return ShardedZeroAdam
+    if name in ("consolidate_state", "shard_state"):
+        from . import optim
+        return getattr(optim, name)
     raise AttributeError(name)

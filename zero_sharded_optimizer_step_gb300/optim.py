@@ -147,7 +147,7 @@ class ZeroAdam:
         self.flag.zero_()
         self.t, self.scale, self.good_steps = sd["t"], sd["scale"], sd["good_steps"]
         with torch.no_grad():
-            self.flat.copy_(self.master.to(self.flat.dtype))
+            self.flat.copy_(self.master)              # a casting copy
 
     def state_bytes(self) -> int:
         """Bytes of fp32 optimizer state (master, m, v) per rank: 12 * S, as
@@ -356,7 +356,7 @@ class ShardedZeroAdam:
             loc.cur.zero_()
         loc.flag.zero_()
         self.t, self.scale, self.good_steps = sd["t"], sd["scale"], sd["good_steps"]
-        loc.own_params.copy_(loc.master.to(loc.params.dtype))
+        loc.own_params.copy_(loc.master)              # a casting copy
         gather_params(loc.params, loc.own_params, self._step.group)
 
     def state_bytes(self) -> int:
@@ -368,3 +368,86 @@ class ShardedZeroAdam:
         for h in getattr(self, "_hooks", []):
             h.remove()
         self.local.close()
+
+
+# ---- sharded checkpoints across rank counts ("PaddlePaddle ZeRO优化": each
+# rank saves and restores its own shard of the optimizer state).  The state
+# lives on one flat vector cut into equal shards, so a checkpoint taken over
+# N ranks is the vector's first numel elements, whatever N was; these two
+# functions move between that whole and the shards of any rank count.  They
+# only slice and concatenate (no arithmetic), on whatever device the saved
+# tensors are.
+
+_STATE_KEYS = ("master", "m", "v")
+
+
+def consolidate_state(shards) -> dict:
+    """The optimizer state of the whole flat vector from a checkpoint:
+    `shards` is either every rank's ShardedZeroAdam.state_dict() (any order,
+    ranks 0..N-1 each once) or a single ZeroAdam.state_dict() (which holds
+    every rank's shard already).  Returns {"master", "m", "v"} over the
+    numel parameters (the padding dropped) with "t", "scale", "good_steps"
+    and "numel"; the step count and loss-scale state must agree across
+    ranks.  ValueError on an incomplete or inconsistent checkpoint."""
+    if isinstance(shards, dict):
+        shards = [shards]
+    shards = list(shards)
+    if not shards:
+        raise ValueError("no state to consolidate")
+    first = shards[0]
+    numel, world = first["numel"], first["world"]
+    for sd in shards:
+        if (sd["numel"], sd["world"]) != (numel, world):
+            raise ValueError("the shards come from different checkpoints")
+        if (sd["t"], sd["scale"], sd["good_steps"]) != (first["t"], first["scale"],
+                                                        first["good_steps"]):
+            raise ValueError("the ranks disagree on the step count or the loss scale")
+    if "rank" not in first:                     # ZeroAdam: every shard in one state
+        if len(shards) != 1:
+            raise ValueError("a ZeroAdam state holds every rank: pass it alone")
+        parts = {k: first[k] for k in _STATE_KEYS}
+    else:
+        by_rank = {sd["rank"]: sd for sd in shards}
+        if sorted(by_rank) != list(range(world)) or len(shards) != world:
+            raise ValueError("a checkpoint of %d ranks needs each rank's state once (got %s)"
+                             % (world, sorted(sd["rank"] for sd in shards)))
+        parts = {k: torch.cat([by_rank[r][k].reshape(-1) for r in range(world)])
+                 for k in _STATE_KEYS}
+    S = z.zero_shard_size(numel, world)
+    out = {}
+    for k, t in parts.items():
+        if t.numel() != S * world:
+            raise ValueError("%s holds %d elements, the layout %d" % (k, t.numel(), S * world))
+        out[k] = t.reshape(-1)[:numel].clone()
+    out.update(t=first["t"], scale=first["scale"], good_steps=first["good_steps"], numel=numel)
+    return out
+
+
+def shard_state(full: dict, world: int, rank: int | None = None) -> dict:
+    """The inverse of consolidate_state for `world` ranks: rank `rank`'s
+    ShardedZeroAdam.state_dict() (its shard of S = ceil(numel / world)
+    elements, zeros past numel), or with rank None a ZeroAdam.state_dict()
+    of `world` ranks (every shard, N * S elements).  The result loads with
+    load_state_dict into an optimizer of that rank count over the same
+    parameters."""
+    numel = full["numel"]
+    S = z.zero_shard_size(numel, world)
+    if S < 0:
+        raise ValueError("bad rank count %d" % world)
+    lo, n = (0, S * world) if rank is None else (rank * S, S)
+    if rank is not None and not 0 <= rank < world:
+        raise ValueError("rank %d is not in [0, %d)" % (rank, world))
+    out = {}
+    for k in _STATE_KEYS:
+        src = full[k].reshape(-1)
+        part = torch.zeros(n, dtype=src.dtype, device=src.device)
+        hi = min(numel, lo + n)
+        if hi > lo:
+            part[:hi - lo] = src[lo:hi]
+        out[k] = part
+    out.update(t=full["t"], scale=full["scale"], good_steps=full["good_steps"],
+               world=world, numel=numel)
+    if rank is not None:
+        out["rank"] = rank
+    return out
+
