@@ -1,8 +1,12 @@
-"""The ZeRO step with one process per data-parallel rank.
+"""The ZeRO step across processes: one process per data-parallel rank, or
+several consecutive ranks per process.
 
-Each process is rank r of N in the library's one-rank view: it owns shard r
-(S = ceil(numel / N) elements of fp32 master, m and v) and holds the full
-low-precision parameter buffer of P = N*S elements.  One step ("ZeRO 与
+With one rank per process, process r is rank r of N in the library's
+one-rank view: it owns shard r (S = ceil(numel / N) elements of fp32
+master, m and v) and holds the full low-precision parameter buffer of P =
+N*S elements.  (A process holding k ranks is one library view of their k
+shards, and everything below happens per held rank; RanksStep and
+ShardedZero3Step.)  One step ("ZeRO 与
 FSDP…", section 从零实现 ZeRO 的 Adam: reduce-scatter of the grads, g /= world,
 Adam on the own shard, all-gather of the updated shards) becomes:
 
@@ -23,9 +27,10 @@ Adam on the own shard, all-gather of the updated shards) becomes:
 
 The collectives move raw bytes (uint8 views), so any element type travels
 bit for bit over NCCL or gloo; with a gloo group, device tensors are staged
-through host memory.  The rank's own arithmetic is done by a `local` object
-(LibraryRank here; the tests also drive this module with a rank whose
-arithmetic is the CPU oracle's), so the data plane is the same code for both.
+through host memory.  The process's own arithmetic is done by a `local`
+object (LibraryRank / LibraryRank3 here; the tests also drive this module
+with ranks whose arithmetic is the CPU oracle's), so the data plane is the
+same code for both.
 """
 from __future__ import annotations
 
