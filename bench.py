@@ -373,9 +373,18 @@ def step_plan(run):
         # one call, which the library makes one launch when the gathered
         # shards are under 32 MiB (and two, the separate calls', otherwise)
         fused_visits = one_pass and not w.groups and getattr(run, "visits", "fused") == "fused"
-        for i in range(len(pieces)):
-            S, _ = sizes(i)
-            plan.append(Launch(gname(i), 2 * bp * S * w.world, gather(i)))
+        if w.groups:                                             # forward
+            for i in range(len(pieces)):
+                S, _ = sizes(i)
+                plan.append(Launch(gname(i), 2 * bp * S * w.world, gather(i)))
+        else:
+            # the Runner's forward runs: a unit alone, or a pair in one call
+            # (the group gather's row kernel)
+            for f, n in run.fwd_runs():
+                S = sum(w.unit_shard(u) for u in range(f, f + n))
+                plan.append(Launch(gname(f) if n == 1 else "gather_rows_kernel",
+                                   2 * bp * S * w.world,
+                                   (lambda f=f, n=n: run.gather_run(f, n, st))))
         total_S = 0
         U = len(pieces)
         for i in reversed(range(U)):
@@ -487,12 +496,14 @@ def static_plan_bytes(w, shadow):
         shards = [[None] * w.world for _ in w.units]
     elif w.rank >= 0 and w.gather_after:
         shards = [None if k == w.rank else object() for k in range(w.world)]
+    from workloads.runner import forward_runs
     run = SimpleNamespace(w=w, stream=None, shadow=(None,) if shadow else None,
                           scale=w.loss_scale, grads=[[None]], shards=shards,
                           grad_avg=object() if w.allreduce_out else None, bucket_buffers=None,
                           bucket_ranges=bucket_ranges, group_ranges=group_ranges,
                           group_fulls=[None] * len(w.groups or []), group_grads=None,
-                          params=None, unit_full=None, ctx=None, t=0)
+                          params=None, unit_full=None, ctx=None, t=0,
+                          fwd_runs=lambda: forward_runs(w), gather_run=None)
     return sum(L.alg_bytes for L in step_plan(run))
 
 
@@ -1613,8 +1624,12 @@ def bench_e2e_units(run, args, world_size):
 
     def one(record=False):
         z.zero3_begin_step_scaled(run.ctx, run.scale)
-        for i in range(len(pieces)):                         # forward gathers
-            gather(i)
+        if w.groups:                                         # forward gathers
+            for i in range(len(pieces)):
+                gather(i)
+        else:
+            for f, n in run.fwd_runs():
+                run.gather_run(f, n, st)
         for j, i in enumerate(reversed(range(len(pieces)))):  # backward
             k2 = j % 2
             views = [d[:h.numel()] for d, h in zip(dev[k2], host[i])]

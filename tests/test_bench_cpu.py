@@ -153,3 +153,24 @@ def test_algorithmic_bytes_match_the_closed_forms():
     fs = W.fsdp2_llama7b()
     assert sum(fs.unit_shard(u) for u in range(len(fs.units))) == 32 * Su
     assert _plan_bytes(fs) == _plan_bytes(W.fsdp2_llama7b_per_param()) == 85_810_544_640
+
+
+def test_forward_runs_pair_only_small_units():
+    """The ZeRO-3 forward's gather calls: consecutive units whose shards are
+    both under 32 MiB go in pairs, larger ones alone, an odd one out last;
+    every unit exactly once, in order."""
+    sys.path.insert(0, ROOT)
+    import workloads as W
+    from workloads.runner import forward_runs
+    assert forward_runs(W.zero3_gpt2_small()) == [(u, 2) for u in range(0, 14, 2)]
+    assert forward_runs(W.zero3_llama7b(4)) == [(u, 1) for u in range(4)]
+    assert forward_runs(W.zero3_gpt2_small(), pairs=False) == [(u, 1) for u in range(14)]
+    # 8 ranks of bf16: 134,217,728 elements make a 32 MiB shard
+    big = 8 * (16 << 20)
+    w = W.Workload("mix", 0, 8, 3, W.BF16, W.BF16, rank=0,
+                   units=[1000, 2000, big, 3000, 4000, 5000, big - 8, 7])
+    w = w.replace(numel=sum(w.units))
+    runs = forward_runs(w)
+    assert runs == [(0, 2), (2, 1), (3, 2), (5, 2), (7, 1)]
+    covered = [u for f, n in runs for u in range(f, f + n)]
+    assert covered == list(range(len(w.units)))

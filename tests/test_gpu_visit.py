@@ -227,3 +227,61 @@ def test_visits_with_decoupled_weight_decay(rank):
     compare_runner(run, ref, what="visits AdamW rank %d" % rank)
     run.close()
 
+
+
+def _paired_step(run, it, seen):
+    """One ZeRO-3 step with the Runner's forward (pairs of units placed into
+    the two unit buffers by one call) and fused backward visits, recording
+    what each gather left in its buffer."""
+    w = run.w
+    run.fill_grads(it)
+    hp = run._hp(run.t + 1)
+    U = len(w.units)
+    z.zero3_begin_step_scaled(run.ctx, run.scale)
+
+    def look(buf, u):
+        torch.cuda.synchronize()
+        seen.append(to_np(buf[:w.unit_shard(u) * w.world]).copy())
+    for f, n in run.fwd_runs():
+        run.gather_run(f, n, run.stream)
+        look(run.unit_full, f)
+        if n == 2:
+            look(run.unit_full2, f + 1)
+    z.zero3_gather_unit(run.ctx, U - 1, run.shards[U - 1], run.unit_full, run.stream)
+    look(run.unit_full, U - 1)
+    for u in reversed(range(1, U)):
+        z.zero3_step_unit_gather(run.ctx, u, run.grads[u], *hp, u - 1, run.shards[u - 1],
+                                 run.unit_full, run.stream)
+        look(run.unit_full, u - 1)
+    z.zero3_step_unit(run.ctx, 0, run.grads[0], *hp, run.stream)
+    if run.shadow is not None:
+        z.zero3_end_step(run.ctx, run.stream)
+    return run.finish_step()
+
+
+@pytest.mark.parametrize("units,rank,scaled", [
+    ([100_003, 7, 0, 250_000, 33_333, 4096], 1, False),     # six units: three pairs
+    ([50_001, 1_000, 77_777, 64, 3], -1, True),             # five: two pairs and a single
+])
+def test_forward_pairs_equal_the_oracle(units, rank, scaled):
+    """The forward's gathers in pairs (zero3_gather_group into two unit
+    buffers): every gathered buffer, the state and the params bit for bit
+    the oracle's, over steps whose updates change what the next forward
+    gathers."""
+    from workloads.runner import Runner
+    w = W.Workload("pairs", sum(units), 4, 3, W.BF16, W.BF16, rank=rank, units=units, steps=3,
+                   loss_scale=2.0 ** 10 if scaled else 0.0, inject=(2, 1) if scaled else None)
+    run = Runner(w, shadow=scaled)
+    assert run.fwd_runs()[0] == (0, 2)
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        seen = []
+        _paired_step(run, it, seen)
+        ref.step(it)
+        want = [g[2] for g in ref.gathers[-2 * len(units):]]
+        assert len(seen) == len(want)
+        for a, b in zip(seen, want):
+            assert a.tobytes() == b.tobytes()
+    assert run.skips == ref.skips
+    compare_runner(run, ref, what="forward pairs")
+    run.close()

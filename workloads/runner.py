@@ -15,7 +15,7 @@ import torch
 import synth
 import zero_sharded_optimizer_step_gb300 as z
 
-from . import KIND_SHARD, Workload, grad_sigma
+from . import F32, KIND_SHARD, Workload, grad_sigma
 
 TORCH_DTYPE = {0: torch.float32, 1: torch.bfloat16, 2: torch.float16}
 
@@ -30,15 +30,44 @@ def inject_index(w: Workload, it: int, rank: int, unit: int = 0) -> int:
     return synth.pick_index(w.seed, n, step=it, rank=rank, unit=unit)
 
 
+# Shards from this size on are placed by the row kernel, at the copy rate
+# whatever the launch count; a pair's launch saves only on smaller ones.
+PAIR_MAX_SHARD_BYTES = 32 << 20
+
+
+def forward_runs(w: Workload, pairs: bool = True):
+    """The stage-3 forward's gather calls over units without groups, each a
+    run (first unit, count).  With pairs, two consecutive units whose shards
+    are both under PAIR_MAX_SHARD_BYTES are placed by one call into two unit
+    buffers ("ZeRO 与 FSDP…", ZeRO-3 与 FSDP: the next unit's all-gather is
+    issued before the current unit computes); every other unit alone."""
+    U = len(w.units or [])
+    es = 4 if w.param_dtype == F32 else 2
+    small = [w.unit_shard(u) * es < PAIR_MAX_SHARD_BYTES for u in range(U)]
+    runs, u = [], 0
+    while u < U:
+        if pairs and u + 1 < U and small[u] and small[u + 1]:
+            runs.append((u, 2))
+            u += 2
+        else:
+            runs.append((u, 1))
+            u += 1
+    return runs
+
+
 class Runner:
     def __init__(self, w: Workload, device: str = "cuda:0", scratch: bool | None = None,
                  shadow: bool = False, alloc_grads: bool = True, hyper: bool = False,
-                 visits: str = "fused"):
+                 visits: str = "fused", fwd_pairs: bool = True):
         self.w = w
         # stage 3 backward: "fused" issues unit u's update and the gather of
         # unit u-1 as one call (zero3_step_unit_gather), "separate" as two
         assert visits in ("fused", "separate")
         self.visits = visits
+        # stage 3 forward (units without groups): the next unit's gather
+        # issued with the current one's, two unit buffers alternating, the
+        # pair placed by one call (zero3_gather_group); else unit by unit
+        self.fwd_pairs = fwd_pairs
         self.dev = torch.device(device)
         torch.cuda.set_device(self.dev)
         if w.unit_rows:
@@ -154,6 +183,20 @@ class Runner:
         for n in lens:
             self.grads.append([torch.zeros(n, dtype=dt, device=self.dev) for _ in range(w.world)])
 
+    def fwd_runs(self):
+        """The stage-3 forward's gather calls (units without groups): see
+        forward_runs."""
+        return forward_runs(self.w, self.fwd_pairs)
+
+    def gather_run(self, first: int, n: int, stream):
+        """Place a forward run: one unit into the unit buffer, or a pair into
+        the two unit buffers in one call."""
+        if n == 1:
+            z.zero3_gather_unit(self.ctx, first, self.shards[first], self.unit_full, stream)
+        else:
+            z.zero3_gather_group(self.ctx, first, self.shards[first:first + 2],
+                                 [self.unit_full, self.unit_full2], stream)
+
     def _alloc_shards(self):
         """The other ranks' parameter shards (one-rank view with placement,
         and stage 3) and the stage-3 unit buffer."""
@@ -180,6 +223,8 @@ class Runner:
                 self.shards.append(row)
                 Pmax = max(Pmax, Su * w.world)
             self.unit_full = torch.zeros(Pmax, dtype=dt, device=self.dev)
+            self.unit_full2 = (torch.zeros(Pmax, dtype=dt, device=self.dev)
+                               if self.fwd_pairs and not w.groups else None)
             self.group_fulls = None
             if w.groups:
                 # one destination per unit of a group, side by side in one buffer
@@ -290,8 +335,12 @@ class Runner:
                         z.zero3_step_unit(self.ctx, i, self.grads[i], *hp, st)
                     else:
                         z.zero3_reduce_unit(self.ctx, i, self.grads[i], self.scale, st)
-            for i in range(len(pieces)):                 # forward
-                gather(i)
+            if w.groups:                                 # forward
+                for i in range(len(pieces)):
+                    gather(i)
+            else:
+                for f, n in self.fwd_runs():
+                    self.gather_run(f, n, st)
             if one_pass and not w.groups and self.visits == "fused" and pieces:
                 # backward: after unit i's backward, its update and the
                 # gather of unit i-1 in one call
