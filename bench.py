@@ -364,6 +364,12 @@ def step_plan(run):
             nv = sum(min(w.unit_shard(u), max(0, w.units[u] - w.rank * w.unit_shard(u)))
                      for u in range(f, f + n))
             return S, nv
+        def chunk_visit(f, n, gf, gn):
+            return lambda: z.zero3_step_units_gather(
+                run.ctx, f, [run.grads[u] for u in range(f, f + n)], w.lr, w.beta1, w.beta2,
+                w.eps, run.t + 1, gf, [run.shards[u] for u in range(gf, gf + gn)],
+                [run.unit_full, run.unit_full2][:gn], st)
+
         def visit(i):
             # unit i's update and unit i-1's gather in one call
             return lambda: z.zero3_step_unit_gather(run.ctx, i, run.grads[i], w.lr, w.beta1,
@@ -387,7 +393,26 @@ def step_plan(run):
                                    (lambda f=f, n=n: run.gather_run(f, n, st))))
         total_S = 0
         U = len(pieces)
-        for i in reversed(range(U)):
+        chunks = run.bwd_chunks() if fused_visits else None
+        if chunks:
+            # the Runner's backward in chunks of two (one call each: the
+            # chunk's steps and the next chunk's gathers)
+            def unit_bytes(u):
+                # as sizes() counts a unit's step
+                S = w.unit_shard(u)
+                nv = min(S, max(0, w.units[u] - w.rank * S))
+                return w.world * bg * nv + (24 + bp) * S
+            f0, n0 = chunks[0]
+            S0 = sum(w.unit_shard(u) for u in range(f0, f0 + n0))
+            plan.append(Launch(gname(f0) if n0 == 1 else "gather_rows_kernel",
+                               2 * bp * S0 * w.world, (lambda f=f0, n=n0: run.gather_run(f, n, st))))
+            for c, (f, n) in enumerate(chunks):
+                gf, gn = chunks[c + 1] if c + 1 < len(chunks) else (0, 0)
+                step_b = sum(unit_bytes(u) for u in range(f, f + n))
+                gath_b = 2 * bp * w.world * sum(w.unit_shard(u) for u in range(gf, gf + gn))
+                plan.append(Launch("visit_kernel", step_b + gath_b, chunk_visit(f, n, gf, gn)))
+                total_S += sum(w.unit_shard(u) for u in range(f, f + n))
+        for i in (reversed(range(U)) if not chunks else ()):
             S, nv = sizes(i)
             total_S += S
             step_bytes = w.world * bg * nv + (24 + bp) * S
@@ -496,14 +521,15 @@ def static_plan_bytes(w, shadow):
         shards = [[None] * w.world for _ in w.units]
     elif w.rank >= 0 and w.gather_after:
         shards = [None if k == w.rank else object() for k in range(w.world)]
-    from workloads.runner import forward_runs
+    from workloads.runner import backward_chunks, forward_runs
     run = SimpleNamespace(w=w, stream=None, shadow=(None,) if shadow else None,
                           scale=w.loss_scale, grads=[[None]], shards=shards,
                           grad_avg=object() if w.allreduce_out else None, bucket_buffers=None,
                           bucket_ranges=bucket_ranges, group_ranges=group_ranges,
                           group_fulls=[None] * len(w.groups or []), group_grads=None,
                           params=None, unit_full=None, ctx=None, t=0,
-                          fwd_runs=lambda: forward_runs(w), gather_run=None)
+                          fwd_runs=lambda: forward_runs(w), gather_run=None,
+                          bwd_chunks=lambda: backward_chunks(w))
     return sum(L.alg_bytes for L in step_plan(run))
 
 

@@ -559,6 +559,29 @@ int zero3_step_unit_gather(zero_ctx *ctx, int32_t unit, const void *const *grads
                            int64_t t, int32_t gather_unit, const void *const *shards,
                            int32_t n_shards, void *unit_full, void *stream);
 
+/* A visit of two units in one call: the steps of units [first_unit,
+ * first_unit + n_units) (1 or 2 units, each as zero3_step_unit; grads holds
+ * n_units * world pointers, unit-major) and the gathers of units
+ * [gather_first, gather_first + gather_n) (0 to 2 units, as
+ * zero3_gather_unit into unit_fulls[j]; shards holds gather_n * world
+ * pointers, unit-major).  With two unit buffers the backward can step two
+ * units and gather the two visited next at once ("ZeRO 与 FSDP…", ZeRO-3 与
+ * FSDP: the next units' all-gathers issued before the current ones are
+ * done), halving the launches of zero3_step_unit_gather.  The result equals
+ * the separate calls, bit for bit.
+ *   - The gathered units must not be stepped ones, the two unit buffers must
+ *     not overlap, and every gather must touch memory disjoint from every
+ *     step as for zero3_step_unit_gather (ZERO_EINVAL, nothing launched).
+ *   - One launch for the default gather mode when the placed shards number
+ *     64 at most and are under 32 MiB each; otherwise (and in the lean mode,
+ *     with a bound scalar block or a capped step occupancy) the launches of
+ *     the separate calls. */
+int zero3_step_units_gather(zero_ctx *ctx, int32_t first_unit, int32_t n_units,
+                            const void *const *grads, int32_t n_grads, double lr, double beta1,
+                            double beta2, double eps, int64_t t, int32_t gather_first,
+                            int32_t gather_n, const void *const *shards, int32_t n_shards,
+                            void *const *unit_fulls, void *stream);
+
 /* Loss-scaled stage 3: first pass for one unit (as zero_step_reduce on the
  * unit's range).  After every unit, one zero_step_apply() applies Adam to all
  * units, or to none if any unit overflowed. */

@@ -149,24 +149,33 @@ def test_two_launch_forms_equal_the_oracle(mode):
 
 
 def test_fused_visits_equal_separate_calls():
-    """The Runner's two backward forms on one workload: identical bits."""
+    """The Runner's backward forms on one workload: unit-by-unit visits,
+    separate calls and (the default for small units) chunks of two --
+    identical bits."""
     from workloads.runner import Runner
     units = [300_001, 150_000, 77_777, 500_000]
     w = W.Workload("visit3", sum(units), 8, 3, W.F16, W.F16, rank=5, units=units, steps=3,
                    loss_scale=2.0 ** 12, inject=(2, 3))
-    a = Runner(w, shadow=True, visits="fused")
-    b = Runner(w, shadow=True, visits="separate")
+    a = Runner(w, shadow=True, visits="fused", fwd_pairs=False)
+    b = Runner(w, shadow=True, visits="separate", fwd_pairs=False)
+    c = Runner(w, shadow=True)
+    assert a.bwd_chunks() is None and c.bwd_chunks() is not None
     for it in range(1, w.steps + 1):
-        a.step(it)
-        b.step(it)
+        for r in (a, b, c):
+            r.step(it)
     torch.cuda.synchronize()
-    assert a.skips == b.skips
-    for x, y in zip(a.state(), b.state()):
-        assert torch.equal(x, y)
-    assert torch.equal(a.params, b.params)
+    assert a.skips == b.skips == c.skips
+    for r in (a, c):
+        for x, y in zip(r.state(), b.state()):
+            assert torch.equal(x, y)
+        assert torch.equal(r.params, b.params)
     assert torch.equal(a.unit_full, b.unit_full)
-    a.close()
-    b.close()
+    # unit 0 is gathered last in every form; the chunks leave it in the
+    # first unit buffer too (what lies past it differs: another unit's rest)
+    n0 = w.unit_shard(0) * w.world
+    assert torch.equal(c.unit_full[:n0], b.unit_full[:n0])
+    for r in (a, b, c):
+        r.close()
 
 
 def test_visits_that_would_overlap_are_refused():
@@ -284,4 +293,85 @@ def test_forward_pairs_equal_the_oracle(units, rank, scaled):
             assert a.tobytes() == b.tobytes()
     assert run.skips == ref.skips
     compare_runner(run, ref, what="forward pairs")
+    run.close()
+
+
+def _chunked_step(run, it, fwd, bwd):
+    """One ZeRO-3 step as the Runner makes it with small units: the forward
+    in pairs, the backward in chunks of two (zero3_step_units_gather),
+    recording what every gather left in its buffer, per unit."""
+    w = run.w
+    run.fill_grads(it)
+    hp = run._hp(run.t + 1)
+    z.zero3_begin_step_scaled(run.ctx, run.scale)
+    bufs = [run.unit_full, run.unit_full2]
+
+    def look(into, first, n):
+        torch.cuda.synchronize()
+        for j in range(n):
+            u = first + j
+            into[u] = to_np(bufs[j][:w.unit_shard(u) * w.world]).copy()
+    for f, n in run.fwd_runs():
+        run.gather_run(f, n, run.stream)
+        look(fwd, f, n)
+    chunks = run.bwd_chunks()
+    run.gather_run(chunks[0][0], chunks[0][1], run.stream)
+    look(bwd, *chunks[0])
+    for c, (f, n) in enumerate(chunks):
+        gf, gn = chunks[c + 1] if c + 1 < len(chunks) else (0, 0)
+        z.zero3_step_units_gather(run.ctx, f, [run.grads[u] for u in range(f, f + n)], *hp, gf,
+                                  [run.shards[u] for u in range(gf, gf + gn)], bufs[:gn],
+                                  run.stream)
+        look(bwd, gf, gn)
+    if run.shadow is not None:
+        z.zero3_end_step(run.ctx, run.stream)
+    return run.finish_step()
+
+
+@pytest.mark.parametrize("units,world,rank,gdt,scaled", [
+    ([100_003, 7, 0, 250_000, 33_333, 4096], 4, 1, W.BF16, False),   # three chunks
+    ([50_001, 1_000, 77_777, 64, 3], 4, -1, W.F16, True),          # an odd unit out
+    ([30_000, 30_000, 30_001, 29_999], 8, 7, W.BF16, True),         # the last rank's padding
+    ([5_000, 7_000, 6_000], 32, 0, W.F16, False),                   # 64 rows of placement
+])
+def test_backward_in_chunks_equals_the_oracle(units, world, rank, gdt, scaled):
+    """The backward in chunks of two units, each call stepping a chunk and
+    gathering the next into the two unit buffers: every gathered buffer of
+    every step, the state and the params bit for bit the oracle's."""
+    from workloads.runner import Runner
+    w = W.Workload("chunks", sum(units), world, 3, gdt, gdt, rank=rank, units=units, steps=3,
+                   loss_scale=2.0 ** 10 if scaled else 0.0, inject=(2, 0) if scaled else None)
+    run = Runner(w, shadow=scaled)
+    assert run.bwd_chunks() is not None
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        fwd, bwd = {}, {}
+        _chunked_step(run, it, fwd, bwd)
+        ref.step(it)
+        mine = ref.gathers[-2 * len(units):]
+        for kind, u, want in mine:
+            got = (fwd if kind == "fwd" else bwd)[u]
+            assert got.tobytes() == want.tobytes(), (it, kind, u)
+    assert run.skips == ref.skips
+    compare_runner(run, ref, what="backward in chunks")
+    run.close()
+
+
+def test_units_visit_refuses_overlaps():
+    """zero3_step_units_gather refuses, launching nothing: a gathered unit
+    that is also stepped, three units, overlapping unit buffers."""
+    from workloads.runner import Runner
+    units = [10_000, 10_000, 10_000, 10_000]
+    w = W.Workload("refuse", sum(units), 4, 3, W.BF16, W.BF16, rank=0, units=units, steps=1)
+    run = Runner(w)
+    hp = run._hp(1)
+    z.zero3_begin_step_scaled(run.ctx, 0.0)
+    bufs = [run.unit_full, run.unit_full2]
+    g = [run.grads[2], run.grads[3]]
+    for args in ((2, g, 3, [run.shards[3]], bufs[:1]),                   # 3 stepped and gathered
+                 (1, [run.grads[1]] * 3, 0, [run.shards[0]], bufs[:1]),  # three stepped units
+                 (2, g, 0, run.shards[0:2], [run.unit_full, run.unit_full[8:]])):   # overlap
+        with pytest.raises(z.ZeroError) as ei:
+            z.zero3_step_units_gather(run.ctx, args[0], args[1], *hp, args[2], args[3], args[4])
+        assert ei.value.code == z.ZERO_EINVAL
     run.close()

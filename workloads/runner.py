@@ -55,6 +55,26 @@ def forward_runs(w: Workload, pairs: bool = True):
     return runs
 
 
+def backward_chunks(w: Workload, pairs: bool = True):
+    """The stage-3 backward in chunks of two units when every unit is small
+    (shards under PAIR_MAX_SHARD_BYTES), from the last unit down: the first
+    chunk is gathered, then each call steps a chunk and gathers the next
+    (zero3_step_units_gather, two unit buffers) -- the next two units'
+    gathers issued while the current two are worked on ("ZeRO 与 FSDP…",
+    ZeRO-3 与 FSDP).  None: the unit-by-unit visits instead."""
+    U = len(w.units or [])
+    es = 4 if w.param_dtype == F32 else 2
+    if not pairs or U < 2 or w.groups or any(w.unit_shard(u) * es >= PAIR_MAX_SHARD_BYTES
+                                             for u in range(U)):
+        return None
+    chunks, hi = [], U
+    while hi > 0:
+        lo = max(0, hi - 2)
+        chunks.append((lo, hi - lo))
+        hi = lo
+    return chunks
+
+
 class Runner:
     def __init__(self, w: Workload, device: str = "cuda:0", scratch: bool | None = None,
                  shadow: bool = False, alloc_grads: bool = True, hyper: bool = False,
@@ -187,6 +207,11 @@ class Runner:
         """The stage-3 forward's gather calls (units without groups): see
         forward_runs."""
         return forward_runs(self.w, self.fwd_pairs)
+
+    def bwd_chunks(self):
+        """The stage-3 backward's chunks of two units, or None: see
+        backward_chunks."""
+        return backward_chunks(self.w, self.fwd_pairs)
 
     def gather_run(self, first: int, n: int, stream):
         """Place a forward run: one unit into the unit buffer, or a pair into
@@ -341,7 +366,18 @@ class Runner:
             else:
                 for f, n in self.fwd_runs():
                     self.gather_run(f, n, st)
-            if one_pass and not w.groups and self.visits == "fused" and pieces:
+            chunks = self.bwd_chunks() if one_pass and self.visits == "fused" else None
+            if chunks:
+                # backward in chunks of two: gather the first, then step
+                # each and gather the next in one call
+                self.gather_run(chunks[0][0], chunks[0][1], st)
+                for c, (f, n) in enumerate(chunks):
+                    gf, gn = chunks[c + 1] if c + 1 < len(chunks) else (0, 0)
+                    z.zero3_step_units_gather(
+                        self.ctx, f, [self.grads[u] for u in range(f, f + n)], *hp, gf,
+                        [self.shards[u] for u in range(gf, gf + gn)],
+                        [self.unit_full, self.unit_full2][:gn], st)
+            elif one_pass and not w.groups and self.visits == "fused" and pieces:
                 # backward: after unit i's backward, its update and the
                 # gather of unit i-1 in one call
                 U = len(pieces)

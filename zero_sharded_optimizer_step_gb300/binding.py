@@ -94,6 +94,8 @@ _SIGS = {
     "zero3_reduce_unit": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f32, _vp]),
     "zero3_step_unit_gather": (ctypes.c_int, [_ctxp, _i32, _vpp, _i32, _f64, _f64, _f64, _f64,
                                               _i64, _i32, _vpp, _i32, _vp, _vp]),
+    "zero3_step_units_gather": (ctypes.c_int, [_ctxp, _i32, _i32, _vpp, _i32, _f64, _f64, _f64,
+                                               _f64, _i64, _i32, _i32, _vpp, _i32, _vpp, _vp]),
     "zero3_gather_group": (ctypes.c_int, [_ctxp, _i32, _i32, _vpp, _i32, _vpp, _vp]),
     "zero3_step_group": (ctypes.c_int, [_ctxp, _i32, _i32, _vpp, _i32, _f64, _f64, _f64, _f64,
                                         _i64, _vp]),
@@ -442,6 +444,20 @@ def zero3_step_unit_gather(ctx, unit: int, grads, lr: float, beta1: float, beta2
     _check(_L.zero3_step_unit_gather(_h(ctx), unit, _ptrs(grads), len(grads), lr, beta1, beta2,
                                      eps, t, gather_unit, _ptrs(shards), len(shards),
                                      _ptr(unit_full), _stream(stream)))
+
+
+def zero3_step_units_gather(ctx, first_unit: int, grads, lr: float, beta1: float, beta2: float,
+                            eps: float, t: int, gather_first: int, shards, unit_fulls,
+                            stream=None) -> None:
+    """grads: one list of N grads per stepped unit (1 or 2 units from
+    first_unit); shards: one list of N shards per gathered unit (0 to 2 units
+    from gather_first), unit_fulls: one destination per gathered unit."""
+    flat_g = [p for row in grads for p in row]
+    flat_s = [p for row in shards for p in row]
+    _check(_L.zero3_step_units_gather(_h(ctx), first_unit, len(grads), _ptrs(flat_g),
+                                      len(flat_g), lr, beta1, beta2, eps, t, gather_first,
+                                      len(unit_fulls), _ptrs(flat_s), len(flat_s),
+                                      _ptrs(unit_fulls), _stream(stream)))
 
 
 def zero3_reduce_unit(ctx, unit: int, grads, loss_scale: float = 0.0, stream=None) -> None:

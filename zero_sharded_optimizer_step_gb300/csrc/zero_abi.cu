@@ -1303,6 +1303,102 @@ int zero3_step_unit_gather(zero_ctx *c, int32_t unit, const void *const *grads, 
     return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "visit kernel");
 }
 
+int zero3_step_units_gather(zero_ctx *c, int32_t first_unit, int32_t n_units,
+                            const void *const *grads, int32_t n_grads, double lr, double b1,
+                            double b2, double eps, int64_t t, int32_t gather_first,
+                            int32_t gather_n, const void *const *shards, int32_t n_shards,
+                            void *const *unit_fulls, void *stream)
+{
+    int rc = check_ready(c);
+    if (rc) return rc;
+    if (c->stage != 3) return fail(ZERO_EINVAL, "unit calls are for stage 3");
+    const int32_t U = (int32_t)c->unit_S.size();
+    const int32_t N = c->world;
+    if (n_units < 1 || n_units > zgb::kVisitSteps || first_unit < 0 || first_unit > U - n_units)
+        return fail(ZERO_EINVAL, "stepped units [%d, %d + %d) must be 1 or 2 units of [0, %d)",
+                    first_unit, first_unit, n_units, U);
+    if (gather_n < 0 || gather_n > zgb::kVisitSteps ||
+        (gather_n > 0 && (gather_first < 0 || gather_first > U - gather_n)))
+        return fail(ZERO_EINVAL, "gathered units [%d, %d + %d) must be 0 to 2 units of [0, %d)",
+                    gather_first, gather_first, gather_n, U);
+    if (gather_n > 0 && gather_first < first_unit + n_units && first_unit < gather_first + gather_n)
+        return fail(ZERO_EINVAL, "a visit gathers units other than those it steps");
+    if ((rc = check_hyper(lr, b1, b2, eps, t))) return rc;
+    if ((rc = check_stage3_pass(c))) return rc;
+    if (!grads || n_grads != n_units * N)
+        return fail(ZERO_EINVAL, "grads: %d pointers given, %d units need %d", n_grads, n_units,
+                    n_units * N);
+    const int es_g = zgb::elem_size(c->gdt), es = zgb::elem_size(c->pdt);
+    Range r[zgb::kVisitSteps];
+    for (int32_t i = 0; i < n_units; ++i) {
+        r[i] = unit_range(c, first_unit + i);
+        rc = check_ptr_array(grads + (int64_t)i * N, N, N, es_g, r[i].n_valid > 0, "grads");
+        if (rc) return rc;
+    }
+    if (n_shards != gather_n * N)
+        return fail(ZERO_EINVAL, "shards: %d pointers given, %d units need %d", n_shards,
+                    gather_n, gather_n * N);
+    if (gather_n > 0 && (!shards || !unit_fulls)) return fail(ZERO_EINVAL, "null pointer array");
+    int64_t Sg[zgb::kVisitSteps] = {0, 0};
+    for (int32_t j = 0; j < gather_n; ++j) {
+        Sg[j] = c->unit_S[gather_first + j];
+        const void *const *sh = shards + (int64_t)j * N;
+        if ((rc = check_ptr_array(sh, N, N, es, false, "shards"))) return rc;
+        if (!unit_fulls[j] && Sg[j] > 0) return fail(ZERO_EINVAL, "unit_fulls[%d] is null", j);
+        if (!aligned(unit_fulls[j], es))
+            return fail(ZERO_EALIGN, "unit_fulls[%d] not aligned to %d bytes", j, es);
+        for (int32_t i = 0; i < n_units; ++i) {
+            rc = check_visit_disjoint(c, r[i], grads + (int64_t)i * N, sh, Sg[j] * es,
+                                      unit_fulls[j], Sg[j] * es * N);
+            if (rc) return rc;
+        }
+    }
+    if (gather_n == 2 &&
+        overlap(unit_fulls[0], Sg[0] * es * N, unit_fulls[1], Sg[1] * es * N))
+        return fail(ZERO_EINVAL, "the two unit buffers overlap");
+    cudaStream_t s = (cudaStream_t)stream;
+    // The separate calls where one launch would not pay, as for
+    // zero3_step_unit_gather, or where the rows would not fit one launch.
+    bool separate = c->gather_mode == ZERO_GATHER_LEAN || c->hyper || c->step_per_sm > 0 ||
+                    gather_n * N > zgb::kVisitRows;
+    for (int32_t j = 0; j < gather_n; ++j) separate |= Sg[j] * es >= kRowsGatherMinShardBytes;
+    if (separate) {
+        for (int32_t i = 0; i < n_units; ++i)
+            if ((rc = stage3_fused(c, r[i], grads + (int64_t)i * N, lr, b1, b2, eps, t, s)))
+                return rc;
+        for (int32_t j = 0; j < gather_n; ++j)
+            if ((rc = gather(c, shards + (int64_t)j * N, N, unit_fulls[j], c->pdt, Sg[j], s, true)))
+                return rc;
+        return ZERO_OK;
+    }
+    zgb::VisitArgs v;
+    memset(&v, 0, sizeof v);
+    v.n_steps = n_units;
+    bool steps = false;
+    for (int32_t i = 0; i < n_units; ++i) {
+        StepArgs a = make_args(c, r[i], grads + (int64_t)i * N);
+        // with two state sets the pass writes the other set under the
+        // step's loss scale (zero3_end_step decides); with one, unscaled
+        a.av = average_scalars(N, c->cur ? c->step_scale : 0.0f);
+        a.ad = adam_scalars(lr, b1, b2, eps, t, c->weight_decay);
+        a.step_id = c->step_id;
+        v.step[i] = a;
+        steps |= r[i].n > 0;
+    }
+    v.n_rows = gather_n * N;
+    v.es = es;
+    for (int32_t j = 0; j < gather_n; ++j)
+        for (int32_t k = 0; k < N; ++k) {
+            const int32_t y = j * N + k;
+            v.src[y] = Sg[j] > 0 ? shards[(int64_t)j * N + k] : nullptr;
+            v.dst[y] = static_cast<char *>(unit_fulls[j]) + (int64_t)k * Sg[j] * es;
+            v.bytes[y] = Sg[j] * es;
+        }
+    const cudaError_t e = zgb::launch_visit(c->gdt, c->pdt, v, c->sms, 0, s);
+    if (steps) return finish_launch(c, e, "visit kernel", s);
+    return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "visit kernel");
+}
+
 int zero3_reduce_unit(zero_ctx *c, int32_t unit, const void *const *grads, int32_t n_grads,
                       float loss_scale, void *stream)
 {

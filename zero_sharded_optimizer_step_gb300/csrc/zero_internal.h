@@ -125,6 +125,26 @@ struct StepGatherArgs {
     int32_t step_short;            // the step part takes the 4-wide body
 };
 
+// A ZeRO-3 backward visit of up to two units in one launch: the fused pass
+// over each of up to kVisitSteps unit ranges (step s owns blocks
+// [step_first_block[s], step_first_block[s + 1])), then the placement of up
+// to kVisitRows shards (row y owns the blocks [row_first_block[y],
+// row_first_block[y + 1]) after the steps' blocks).
+constexpr int kVisitSteps = 2;
+constexpr int kVisitRows = 64;
+struct VisitArgs {
+    StepArgs step[kVisitSteps];
+    int32_t step_first_block[kVisitSteps + 1];
+    int32_t step_short[kVisitSteps];   // the step takes the 4-wide body
+    int32_t n_steps;
+    const void *src[kVisitRows];       // null = skip the row
+    char *dst[kVisitRows];
+    int64_t bytes[kVisitRows];
+    int32_t row_first_block[kVisitRows + 1];
+    int32_t n_rows;
+    int32_t es;
+};
+
 // A placement of independent rows in one launch: row y copies bytes[y]
 // bytes from src[y] to dst[y] (a group of units, one row per unit and shard).
 // The launcher fills first_block: row y owns blocks [first_block[y],
@@ -209,6 +229,11 @@ cudaError_t launch_gather(const GatherArgs &a, int sms, cudaStream_t s);
 cudaError_t launch_step_gather(int32_t gdt, int32_t pdt, const StepArgs &step,
                                const GatherArgs &gather, int sms, int cap_per_sm,
                                cudaStream_t s);
+// A visit of up to two units (VisitArgs): the launcher fills a copy's block
+// tables (each step range the grid launch_fused_step would give it, each
+// row the blocks launch_gather would) and launches once.
+cudaError_t launch_visit(int32_t gdt, int32_t pdt, const VisitArgs &a, int sms, int cap_per_sm,
+                         cudaStream_t s);
 // Fills a copy's first_block table and launches; `a` itself is not changed.
 cudaError_t launch_gather_rows(const GatherRowsArgs &a, int sms, cudaStream_t s);
 // The bulk-copy (TMA) placement for 16-byte aligned shards: one warp per SM,

@@ -590,6 +590,55 @@ step_gather_kernel(const __grid_constant__ StepGatherArgs a)
                         a.gather.shard_bytes, a.gather.es, gb % a.row_blocks, a.row_blocks);
 }
 
+// A backward visit of up to two units in one launch (launch_visit): the
+// blocks of step range s run the fused pass over it (the 4-wide body when
+// its range gives a thread one 8-wide iteration at most), the blocks after
+// all steps place the rows.  The parts touch disjoint memory (the host
+// checks it), so none waits for another.  The two step ranges are selected
+// with constant indices, so each reads its arguments at fixed offsets.
+template <int GT, int PT>
+__device__ __forceinline__ void visit_step(const StepArgs &st, int short_body, int32_t block,
+                                           int32_t nblocks)
+{
+    if constexpr (GT != F32) {
+        if (short_body) {
+            fused_step_body4<GT, PT>(st, block, nblocks);
+            return;
+        }
+    }
+    fused_step_body<GT, PT, false, false>(st, block, nblocks);
+}
+
+template <int GT, int PT>
+__global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
+visit_kernel(const __grid_constant__ VisitArgs a)
+{
+    pdl_wait();                 // the previous kernel in the stream is done
+    pdl_launch_dependents();
+    const int32_t b = (int32_t)blockIdx.x;
+    if (a.n_steps > 0 && b < a.step_first_block[1]) {
+        visit_step<GT, PT>(a.step[0], a.step_short[0], b, a.step_first_block[1]);
+        return;
+    }
+    if (a.n_steps > 1 && b < a.step_first_block[2]) {
+        visit_step<GT, PT>(a.step[1], a.step_short[1], b - a.step_first_block[1],
+                           a.step_first_block[2] - a.step_first_block[1]);
+        return;
+    }
+    if (a.n_rows <= 0) return;
+    // the row this block belongs to: the last y with row_first_block[y] <= gb
+    const int32_t gb = b - a.step_first_block[a.n_steps];
+    int lo = 0, hi = a.n_rows - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.row_first_block[mid] <= gb) lo = mid; else hi = mid - 1;
+    }
+    const char *src = static_cast<const char *>(a.src[lo]);
+    if (src == nullptr || a.bytes[lo] <= 0) return;
+    rowcopy::gather_row(src, a.dst[lo], a.bytes[lo], a.es, gb - a.row_first_block[lo],
+                        a.row_first_block[lo + 1] - a.row_first_block[lo]);
+}
+
 template <int GT, bool AVG, bool HYPER>
 __global__ void __launch_bounds__(kThreads, MinBlocks<GT>::value)
 reduce_kernel(const __grid_constant__ StepArgs a)
@@ -878,7 +927,73 @@ cudaError_t step_gather_gt(int32_t pdt, const StepArgs &st, const GatherArgs &g,
     return cudaErrorInvalidValue;
 }
 
+template <int GT, int PT>
+cudaError_t visit_pt(const VisitArgs &in, int sms, int cap_per_sm, cudaStream_t s)
+{
+    auto kernel = visit_kernel<GT, PT>;
+    int per_sm = resident_blocks_per_sm(reinterpret_cast<const void *>(kernel), kThreads);
+    const int resident = sms * per_sm;
+    if (cap_per_sm > 0 && per_sm > cap_per_sm) per_sm = cap_per_sm;
+    const int64_t cap = (int64_t)sms * per_sm;
+    if (in.n_steps < 0 || in.n_steps > kVisitSteps || in.n_rows < 0 || in.n_rows > kVisitRows)
+        return cudaErrorInvalidValue;
+    VisitArgs a = in;
+    int64_t total = 0;
+    for (int i = 0; i < a.n_steps; ++i) {
+        // each step range gets the grid step_gather_pt gives one
+        const StepArgs &st = a.step[i];
+        const bool step_short = GT != F32 && st.vec_ok && st.n_valid <= cap * kThreads * kVec;
+        int64_t work = items(st, st.n_valid);
+        if (step_short) {
+            const int64_t nvec4 = st.n_valid / 4, tail = st.n - nvec4 * 4;
+            work = nvec4 > tail ? nvec4 : tail;
+        }
+        const int64_t want = (work + kThreads - 1) / kThreads;
+        int64_t blocks = st.n > 0 ? (want < cap ? want : cap) : 0;
+        if (st.n > 0 && blocks < 1) blocks = 1;
+        a.step_first_block[i] = (int32_t)total;
+        a.step_short[i] = step_short ? 1 : 0;
+        total += blocks;
+    }
+    a.step_first_block[a.n_steps] = (int32_t)total;
+    int64_t rows = 0;
+    for (int32_t y = 0; y < a.n_rows; ++y) {
+        a.row_first_block[y] = (int32_t)rows;
+        if (a.src[y] && a.bytes[y] > 0)
+            rows += rowcopy::row_blocks(a.bytes[y], kThreads, resident);
+        if (total + rows > 0x7fffffff) return cudaErrorInvalidValue;
+    }
+    a.row_first_block[a.n_rows] = (int32_t)rows;
+    const int64_t blocks = total + rows;
+    if (blocks == 0) return cudaSuccess;
+    return launch_dependent(kernel, dim3((unsigned)blocks), dim3(kThreads), 0, s, a);
+}
+
+template <int GT>
+cudaError_t visit_gt(int32_t pdt, const VisitArgs &a, int sms, int cap_per_sm, cudaStream_t s)
+{
+    switch (pdt) {
+    case F32: return visit_pt<GT, F32>(a, sms, cap_per_sm, s);
+    case BF16: return visit_pt<GT, BF16>(a, sms, cap_per_sm, s);
+    case F16: return visit_pt<GT, F16>(a, sms, cap_per_sm, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
+
+cudaError_t launch_visit(int32_t gdt, int32_t pdt, const VisitArgs &a, int sms, int cap_per_sm,
+                         cudaStream_t s)
+{
+    for (int i = 0; i < a.n_steps && i < kVisitSteps; ++i)
+        if (a.step[i].hyper || a.step[i].grad_avg) return cudaErrorInvalidValue;   // eager only
+    switch (gdt) {
+    case F32: return visit_gt<F32>(pdt, a, sms, cap_per_sm, s);
+    case BF16: return visit_gt<BF16>(pdt, a, sms, cap_per_sm, s);
+    case F16: return visit_gt<F16>(pdt, a, sms, cap_per_sm, s);
+    }
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_step_gather(int32_t gdt, int32_t pdt, const StepArgs &st,
                                const GatherArgs &g, int sms, int cap_per_sm, cudaStream_t s)
