@@ -174,3 +174,21 @@ def test_forward_runs_pair_only_small_units():
     assert runs == [(0, 2), (2, 1), (3, 2), (5, 2), (7, 1)]
     covered = [u for f, n in runs for u in range(f, f + n)]
     assert covered == list(range(len(w.units)))
+
+
+def test_backward_chunks_of_small_units():
+    """The ZeRO-3 backward in chunks of two from the last unit down (an odd
+    one out at unit 0) when every unit is small; none when any shard is 32
+    MiB or more, or with pairs off."""
+    sys.path.insert(0, ROOT)
+    import workloads as W
+    from workloads.runner import backward_chunks
+    assert backward_chunks(W.zero3_gpt2_small()) == [(u, 2) for u in range(12, -1, -2)]
+    assert backward_chunks(W.zero3_llama7b(4)) is None
+    assert backward_chunks(W.zero3_gpt2_small(), pairs=False) is None
+    w = W.Workload("odd", 0, 4, 3, W.BF16, W.BF16, rank=0, units=[10, 20, 30, 40, 50])
+    w = w.replace(numel=sum(w.units))
+    chunks = backward_chunks(w)
+    assert chunks == [(3, 2), (1, 2), (0, 1)]
+    covered = [u for f, n in chunks for u in reversed(range(f, f + n))]
+    assert covered == [4, 3, 2, 1, 0]
