@@ -72,7 +72,7 @@ import numpy as np  # noqa: E402
 # prefix); otherwise bench reports null.
 TRAFFIC = {
     # 60,000,000-element case (16 fp16 ranks, two state sets), x 25.96
-    ("gpt2_xl", "fused_step_kernel"): ("bbfe4acf8d36d2ca", 68.539e9 + 20.971e9, 13170.1),
+    ("gpt2_xl", "fused_step_kernel"): ("dd04a6e84427b70e", 68.538e9 + 20.968e9, 13178.4),
     # 63 shards of 10,000,000 elements, x 11.72
     ("one_rank_7p5b", "gather_kernel"): ("eae13d5b2b7affa8", 14.767e9 + 14.136e9, 4094.4),
     # 2 Llama-7B layers: every gather has the full workload's shape
