@@ -84,9 +84,10 @@ class Runner:
         # unit u-1 as one call (zero3_step_unit_gather), "separate" as two
         assert visits in ("fused", "separate")
         self.visits = visits
-        # stage 3 forward (units without groups): the next unit's gather
-        # issued with the current one's, two unit buffers alternating, the
-        # pair placed by one call (zero3_gather_group); else unit by unit
+        # stage 3 over two unit buffers (units without groups): the forward
+        # in pairs of small units (forward_runs) and, when every unit is
+        # small, the backward in chunks of two (backward_chunks); False:
+        # unit by unit, over one unit buffer's worth of schedule
         self.fwd_pairs = fwd_pairs
         self.dev = torch.device(device)
         torch.cuda.set_device(self.dev)
