@@ -375,3 +375,34 @@ def test_units_visit_refuses_overlaps():
             z.zero3_step_units_gather(run.ctx, args[0], args[1], *hp, args[2], args[3], args[4])
         assert ei.value.code == z.ZERO_EINVAL
     run.close()
+
+
+@pytest.mark.parametrize("mode", ["lean", "hyper", "capped", "rows"])
+def test_units_visit_separate_forms_equal_the_oracle(mode):
+    """The forms in which zero3_step_units_gather makes the separate calls'
+    launches (the lean gather mode, a bound scalar block, a capped step
+    occupancy, more than 64 shards to place): every gathered buffer, the
+    state and the params still the oracle's."""
+    from workloads.runner import Runner
+    units = [200_000, 33_333, 120_000, 7_001]
+    world, rank = (64, 3) if mode == "rows" else (4, 0)
+    w = W.Workload("chunks2", sum(units), world, 3, W.BF16, W.BF16, rank=rank, units=units,
+                   steps=2)
+    run = Runner(w, hyper=mode == "hyper")
+    if mode == "lean":
+        z.zero_set_gather_mode(run.ctx, z.ZERO_GATHER_LEAN)
+    if mode == "capped":
+        z.zero_set_step_occupancy(run.ctx, 2)
+    ref = refs.OracleRun(w)
+    for it in range(1, w.steps + 1):
+        fwd, bwd = {}, {}
+        _chunked_step(run, it, fwd, bwd)
+        ref.step(it)
+        for kind, u, want in ref.gathers[-2 * len(units):]:
+            got = (fwd if kind == "fwd" else bwd)[u]
+            assert got.tobytes() == want.tobytes(), (it, kind, u)
+    torch.cuda.synchronize()
+    compare_runner(run, ref, what="units visit, separate launches: %s" % mode)
+    if mode == "hyper":
+        z.zero_bind_hyper(run.ctx, None)
+    run.close()
