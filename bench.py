@@ -773,15 +773,18 @@ def run_e2e(run, plan, args, world_size):
 def sharded_workload(args, world_size, rank=0):
     """The workload of the sharded mode: the command line's over W
     data-parallel ranks (--dp-ranks; by default the workload's own rank
-    count), each of the N processes holding W / N consecutive ranks; `rank`
-    is the process's index."""
+    count, or one rank per process when N does not divide it), each of the
+    N processes holding W / N consecutive ranks; `rank` is the process's
+    index."""
     base = make_workload(args, args.workload)
     # a flat workload must be the all-ranks one (the mode picks each
     # process's ranks); stage-3 workloads are described as one rank's view
     if (base.stage < 3 and base.rank >= 0) or base.bucket or base.groups or base.unit_rows:
         raise SystemExit("the sharded mode steps a flat vector or flat stage-3 units; "
                          "--workload %s is not one (use --replicas)" % args.workload)
-    W = args.dp_ranks or base.world
+    # the workload's own rank count when the processes divide it, else one
+    # rank per process (--dp-ranks chooses explicitly)
+    W = args.dp_ranks or (base.world if base.world % world_size == 0 else world_size)
     if W % world_size:
         raise SystemExit("--dp-ranks %d is not a multiple of the %d processes" % (W, world_size))
     return base.replace(world=W, rank=rank, name=base.name + "_sharded")
