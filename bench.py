@@ -80,6 +80,9 @@ TRAFFIC = {
     # the same gathers (2-byte params, the same shard sizes)
     ("zero3_llama7b_fp16", "gather_rows_kernel"): ("eae13d5b2b7affa8", 404.82e6 + 349.29e6,
                                                    113.5),
+    # the 7 two-unit visits of one step, averaged (the launches differ in
+    # size as the bytes per launch do); the full workload itself
+    ("zero3_gpt2_small", "visit_kernel"): ("dd04a6e84427b70e", 95.855e6 + 18.091e6, 29.73),
 }
 KERNEL_SRC = os.path.join(ROOT, "zero_sharded_optimizer_step_gb300", "csrc",
                           "zero_step_kernels.cu")
